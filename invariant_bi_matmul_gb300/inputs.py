@@ -1,0 +1,152 @@
+"""Seeded synthetic inputs shaped like the workloads the pages describe.
+
+This module holds none of the method's arithmetic: it only draws random numbers
+(``torch.Generator`` seeded per call), casts them to bf16 and lays them out.  Both the
+CUDA path and the CPU oracle are fed from here, so neither depends on the other.
+
+Workload shapes (the pages' configurations):
+  * tiny check: x ``[M,256]`` N(0,1), M in {1,2,4,8}; W ``[256,256]`` N(0,0.02);
+    gamma N(1,0.1), eps 1e-6; attention with 4 heads, head_dim 64, 128 cached tokens.
+  * GEMM: K=N=4096, X N(0,1), W N(0,0.02), M in {1,2,4,8,16,64,256,2048}.
+  * RMSNorm: hidden 8192, x N(0, std 3) with 1% of elements (independent Bernoulli
+    draws) multiplied by 50 before the bf16 cast, gamma N(1,0.1), eps 1e-5.
+  * attention: 32 query heads, 8 KV heads, head_dim 128, K/V/Q N(0,1), paged cache with
+    64-token pages whose physical order is a random permutation.
+"""
+from __future__ import annotations
+
+from dataclasses import dataclass
+
+import torch
+
+PAGE_SIZE = 64
+
+
+def generator(seed: int) -> torch.Generator:
+    g = torch.Generator(device="cpu")
+    g.manual_seed(int(seed))
+    return g
+
+
+def normal_bf16(shape, mean: float = 0.0, std: float = 1.0, seed: int = 0) -> torch.Tensor:
+    """N(mean, std) drawn in fp32 on the CPU, cast to bf16 (round to nearest even)."""
+    t = torch.randn(*shape, generator=generator(seed), dtype=torch.float32)
+    return (t * std + mean).to(torch.bfloat16)
+
+
+def small_int_bf16(shape, lo: int, hi: int, exp2: int = 0, seed: int = 0) -> torch.Tensor:
+    """Integers in [lo, hi] times 2**exp2, exactly representable in bf16 (|v| <= 256)."""
+    t = torch.randint(lo, hi + 1, tuple(shape), generator=generator(seed), dtype=torch.int32)
+    return (t.to(torch.float32) * (2.0 ** exp2)).to(torch.bfloat16)
+
+
+def bf16_bits(t: torch.Tensor):
+    """bf16 tensor -> numpy uint16 array of its bit patterns (for the C oracle)."""
+    return t.detach().cpu().contiguous().view(torch.int16).numpy().view("uint16")
+
+
+# ----------------------------------------------------------------------------- GEMM
+
+@dataclass
+class GemmInputs:
+    x: torch.Tensor      # [M, K] bf16
+    w_nk: torch.Tensor   # [N, K] bf16 (nn.Linear weight, "transposed B")
+    w_kn: torch.Tensor   # [K, N] bf16, the same matrix stored naturally
+
+
+def gemm_inputs(M: int, N: int, K: int, seed: int, x_std: float = 1.0,
+                w_std: float = 0.02) -> GemmInputs:
+    x = normal_bf16((M, K), 0.0, x_std, seed=seed * 1000003 + 1)
+    w_nk = normal_bf16((N, K), 0.0, w_std, seed=seed * 1000003 + 2)
+    return GemmInputs(x=x, w_nk=w_nk, w_kn=w_nk.t().contiguous())
+
+
+# -------------------------------------------------------------------------- RMSNorm
+
+def rmsnorm_inputs(B: int, H: int, seed: int, std: float = 3.0, outlier_p: float = 0.01,
+                   outlier_scale: float = 50.0):
+    """x [B,H] bf16 with independent outliers, gamma [H] bf16 N(1, 0.1)."""
+    g = generator(seed)
+    x = torch.randn(B, H, generator=g, dtype=torch.float32) * std
+    if outlier_p > 0:
+        mask = torch.rand(B, H, generator=g) < outlier_p
+        x = torch.where(mask, x * outlier_scale, x)
+    gamma = torch.randn(H, generator=g, dtype=torch.float32) * 0.1 + 1.0
+    return x.to(torch.bfloat16), gamma.to(torch.bfloat16)
+
+
+# ------------------------------------------------------------- paged KV + attention
+
+@dataclass
+class PagedInputs:
+    q: torch.Tensor            # [T, Hq, D] bf16, T = sum of q_lens
+    k_new: torch.Tensor        # [T, Hkv, D] bf16 (the block's own keys)
+    v_new: torch.Tensor        # [T, Hkv, D] bf16
+    k_cache: torch.Tensor      # [num_pages, Hkv, PAGE, D] bf16
+    v_cache: torch.Tensor      # [num_pages, Hkv, PAGE, D] bf16
+    block_table: torch.Tensor  # [B, max_pages] int32
+    seq_lens: torch.Tensor     # [B] int32, includes the new tokens
+    cu_q: torch.Tensor         # [B+1] int32
+    page_size: int
+
+    @property
+    def B(self) -> int:
+        return int(self.seq_lens.numel())
+
+    @property
+    def T(self) -> int:
+        return int(self.q.shape[0])
+
+
+def paged_inputs(seq_lens, q_lens, Hq: int, Hkv: int, D: int, seed: int,
+                 page_size: int = PAGE_SIZE, spare_pages: int = 3, kv_std: float = 1.0,
+                 q_std: float = 1.0, device: str = "cpu") -> PagedInputs:
+    """A batch of sequences whose caches hold seq_lens[b] tokens (the last q_lens[b] of
+    them being the verify block's own tokens, delivered separately in k_new/v_new).
+    Every page of the pool is filled with N(0, kv_std) so slots nobody owns are finite;
+    physical pages are handed out in a seeded random order.  ``device='cuda'`` draws the
+    large cache tensors with the CUDA generator (same recipe, different stream)."""
+    seq_lens = [int(s) for s in seq_lens]
+    q_lens = [int(q) for q in q_lens]
+    if len(seq_lens) != len(q_lens):
+        raise ValueError("seq_lens and q_lens differ in length")
+    for s, ql in zip(seq_lens, q_lens):
+        if ql < 0 or s < ql:
+            raise ValueError("each sequence must hold at least its block")
+    B = len(seq_lens)
+    g = generator(seed)
+    pages_per_seq = [max(1, -(-s // page_size)) for s in seq_lens]
+    max_pages = max(pages_per_seq) if B else 1
+    num_pages = sum(pages_per_seq) + spare_pages
+    perm = torch.randperm(num_pages, generator=g).to(torch.int32)
+    block_table = torch.full((max(B, 1), max_pages), -1, dtype=torch.int32)[:B]
+    cursor = 0
+    for b, n in enumerate(pages_per_seq):
+        block_table[b, :n] = perm[cursor:cursor + n]
+        cursor += n
+    T = sum(q_lens)
+    cu = [0]
+    for ql in q_lens:
+        cu.append(cu[-1] + ql)
+    shape = (num_pages, Hkv, page_size, D)
+    if device == "cpu":
+        k_cache = (torch.randn(*shape, generator=g) * kv_std).to(torch.bfloat16)
+        v_cache = (torch.randn(*shape, generator=g) * kv_std).to(torch.bfloat16)
+    else:
+        gc = torch.Generator(device=device)
+        gc.manual_seed(int(seed) + 17)
+        k_cache = (torch.randn(*shape, generator=gc, device=device) * kv_std).to(torch.bfloat16)
+        v_cache = (torch.randn(*shape, generator=gc, device=device) * kv_std).to(torch.bfloat16)
+    q = (torch.randn(T, Hq, D, generator=g) * q_std).to(torch.bfloat16)
+    k_new = (torch.randn(T, Hkv, D, generator=g) * kv_std).to(torch.bfloat16)
+    v_new = (torch.randn(T, Hkv, D, generator=g) * kv_std).to(torch.bfloat16)
+    return PagedInputs(q=q, k_new=k_new, v_new=v_new, k_cache=k_cache, v_cache=v_cache,
+                       block_table=block_table.contiguous(),
+                       seq_lens=torch.tensor(seq_lens, dtype=torch.int32),
+                       cu_q=torch.tensor(cu, dtype=torch.int32), page_size=page_size)
+
+
+def mixed_lengths(B: int, seed: int, choices=(1028, 8196, 16388, 65540)):
+    """Sequence lengths drawn uniformly (seeded) from the pages' Lk values."""
+    idx = torch.randint(0, len(choices), (B,), generator=generator(seed))
+    return [int(choices[i]) for i in idx]

@@ -1,0 +1,228 @@
+"""ctypes front end of the plain C oracle (``bi_oracle.c``).
+
+TEST INFRASTRUCTURE ONLY: the product library never imports this package.  Only the
+test-suite, ``__graft_entry__.smoke()`` and the CPU-baseline leg of ``bench.py`` use it.
+It shares no code with the CUDA path; inputs arrive as numpy arrays of bf16 bit
+patterns (``uint16``) and results leave as unrounded fp32 plus, on request, the
+oracle's own bf16 rounding.
+"""
+from __future__ import annotations
+
+import ctypes
+import os
+import subprocess
+
+import numpy as np
+
+_HERE = os.path.dirname(os.path.abspath(__file__))
+_SRC = os.path.join(_HERE, "bi_oracle.c")
+_LIB = os.path.join(_HERE, "libbi_oracle.so")
+
+# Strict IEEE fp32: no fused multiply-add contraction, no fast-math reassociation.
+CFLAGS = ["-O2", "-std=c11", "-fPIC", "-shared", "-ffp-contract=off", "-fno-fast-math",
+          "-fvisibility=hidden"]
+
+
+def build(force: bool = False) -> str:
+    """Compile the oracle shared library with gcc (seconds); returns its path."""
+    if force or not os.path.exists(_LIB) or os.path.getmtime(_LIB) < os.path.getmtime(_SRC):
+        tmp = _LIB + f".tmp{os.getpid()}"
+        subprocess.run(["gcc", *CFLAGS, _SRC, "-o", tmp, "-lm"], check=True)
+        os.replace(tmp, _LIB)
+    return _LIB
+
+
+_lib = None
+
+
+def lib() -> ctypes.CDLL:
+    global _lib
+    if _lib is None:
+        _lib = ctypes.CDLL(build())
+        _declare(_lib)
+    return _lib
+
+
+_p = ctypes.c_void_p
+_i64 = ctypes.c_int64
+
+
+def _declare(L: ctypes.CDLL) -> None:
+    L.oracle_bf16_round.argtypes = [_p, _p, _i64]
+    L.oracle_bf16_widen.argtypes = [_p, _p, _i64]
+    L.oracle_left_fold_f64.argtypes = [_p, _i64]
+    L.oracle_left_fold_f64.restype = ctypes.c_double
+    for name in ("oracle_sum_sequential_f32", "oracle_sum_pairwise_f32", "oracle_sum_squares_f32"):
+        getattr(L, name).argtypes = [_p, _i64]
+        getattr(L, name).restype = ctypes.c_float
+    L.oracle_sum_split_f32.argtypes = [_p, _i64, _i64]
+    L.oracle_sum_split_f32.restype = ctypes.c_float
+    L.oracle_argmax_f32.argtypes = [_p, _i64]
+    L.oracle_argmax_f32.restype = _i64
+    L.oracle_matmul.argtypes = [_p, _i64, _p, _i64, ctypes.c_int, _p, _i64, _i64, _i64, _i64]
+    L.oracle_rmsnorm.argtypes = [_p, _i64, _p, _p, _i64, _i64, _i64, ctypes.c_float]
+    L.oracle_kv_append.argtypes = [_p, _p, _p, _p, _p, _i64, _p, _p, _i64, _i64, _i64, _i64]
+    L.oracle_attention_row.argtypes = [_p, _p, _p, _p, _i64, _p, _p, _i64, _i64, _i64, _i64,
+                                       _i64, _i64, _i64, ctypes.c_float, _p, _p]
+    L.oracle_attention_row.restype = ctypes.c_int
+    L.oracle_attention.argtypes = [_p, _p, _p, _p, _i64, _p, _p, _i64, _i64, _i64, _i64, _i64,
+                                   ctypes.c_float, _p, _p]
+    L.oracle_attention.restype = ctypes.c_int
+
+
+def _ptr(a: np.ndarray):
+    return a.ctypes.data_as(ctypes.c_void_p)
+
+
+def _as(a, dtype) -> np.ndarray:
+    a = np.ascontiguousarray(a)
+    if a.dtype != dtype:
+        raise TypeError(f"oracle expects {np.dtype(dtype)}, got {a.dtype}")
+    return a
+
+
+# ----------------------------------------------------------------------------- bf16
+
+def bf16_round(x: np.ndarray) -> np.ndarray:
+    """fp32 -> bf16 bit patterns (uint16), round to nearest even."""
+    x = _as(x, np.float32)
+    out = np.empty(x.shape, dtype=np.uint16)
+    lib().oracle_bf16_round(_ptr(x), _ptr(out), x.size)
+    return out
+
+
+def bf16_widen(h: np.ndarray) -> np.ndarray:
+    h = _as(h, np.uint16)
+    out = np.empty(h.shape, dtype=np.float32)
+    lib().oracle_bf16_widen(_ptr(h), _ptr(out), h.size)
+    return out
+
+
+# ------------------------------------------------------------------ reduction trees
+
+def left_fold_f64(xs) -> float:
+    a = _as(np.asarray(xs, dtype=np.float64), np.float64)
+    return float(lib().oracle_left_fold_f64(_ptr(a), a.size))
+
+
+def sum_sequential_f32(a) -> np.float32:
+    a = _as(a, np.float32)
+    return np.float32(lib().oracle_sum_sequential_f32(_ptr(a), a.size))
+
+
+def sum_pairwise_f32(a) -> np.float32:
+    a = _as(a, np.float32)
+    return np.float32(lib().oracle_sum_pairwise_f32(_ptr(a), a.size))
+
+
+def sum_split_f32(a, splits: int) -> np.float32:
+    a = _as(a, np.float32)
+    return np.float32(lib().oracle_sum_split_f32(_ptr(a), a.size, splits))
+
+
+def sum_squares_f32(a) -> np.float32:
+    a = _as(a, np.float32)
+    return np.float32(lib().oracle_sum_squares_f32(_ptr(a), a.size))
+
+
+def argmax_f32(v) -> int:
+    v = _as(v, np.float32)
+    return int(lib().oracle_argmax_f32(_ptr(v), v.size))
+
+
+# --------------------------------------------------------------------------- matmul
+
+W_NK, W_KN = 0, 1
+
+
+def matmul(x: np.ndarray, w: np.ndarray, w_layout: int) -> np.ndarray:
+    """x uint16 [M,K] (bf16 bits); w uint16 [N,K] (W_NK) or [K,N] (W_KN) -> fp32 [M,N]."""
+    x = _as(x, np.uint16)
+    w = _as(w, np.uint16)
+    M, K = x.shape
+    N = w.shape[0] if w_layout == W_NK else w.shape[1]
+    Kw = w.shape[1] if w_layout == W_NK else w.shape[0]
+    if Kw != K:
+        raise ValueError("inner dimensions differ")
+    y = np.empty((M, N), dtype=np.float32)
+    lib().oracle_matmul(_ptr(x), K, _ptr(w), w.shape[1], w_layout, _ptr(y), N, M, N, K)
+    return y
+
+
+def matmul_strided(x, ldx, w, ldw, w_layout, M, N, K, ldy) -> np.ndarray:
+    """Raw strided call: x, w flat uint16 buffers; returns flat fp32 [M*ldy]."""
+    x = _as(x, np.uint16)
+    w = _as(w, np.uint16)
+    y = np.full(M * ldy, np.nan, dtype=np.float32)
+    lib().oracle_matmul(_ptr(x), ldx, _ptr(w), ldw, w_layout, _ptr(y), ldy, M, N, K)
+    return y
+
+
+# -------------------------------------------------------------------------- rmsnorm
+
+def rmsnorm(x: np.ndarray, gamma: np.ndarray, eps: float) -> np.ndarray:
+    """x uint16 [rows,H], gamma uint16 [H] -> fp32 [rows,H] (unrounded)."""
+    x = _as(x, np.uint16)
+    gamma = _as(gamma, np.uint16)
+    rows, H = x.shape
+    y = np.empty((rows, H), dtype=np.float32)
+    lib().oracle_rmsnorm(_ptr(x), H, _ptr(gamma), _ptr(y), H, rows, H, ctypes.c_float(eps))
+    return y
+
+
+# ----------------------------------------------------------------- paged attention
+
+def kv_append(k_new, v_new, k_cache, v_cache, block_table, seq_lens, cu_q, page_size):
+    """Returns updated copies of (k_cache, v_cache) (uint16 [pages,Hkv,page,D])."""
+    k_new = _as(k_new, np.uint16)
+    v_new = _as(v_new, np.uint16)
+    kc = _as(k_cache, np.uint16).copy()
+    vc = _as(v_cache, np.uint16).copy()
+    bt = _as(block_table, np.int32)
+    sl = _as(seq_lens, np.int32)
+    cq = _as(cu_q, np.int32)
+    B = sl.size
+    Hkv, D = kc.shape[1], kc.shape[3]
+    lib().oracle_kv_append(_ptr(k_new), _ptr(v_new), _ptr(kc), _ptr(vc), _ptr(bt), bt.shape[1],
+                           _ptr(sl), _ptr(cq), B, Hkv, D, page_size)
+    return kc, vc
+
+
+def attention(q, k_cache, v_cache, block_table, seq_lens, cu_q, Hq, scale):
+    """q uint16 [T,Hq,D]; caches uint16 [pages,Hkv,page,D] -> (out fp32 [T,Hq,D], lse fp32 [T,Hq])."""
+    q = _as(q, np.uint16)
+    kc = _as(k_cache, np.uint16)
+    vc = _as(v_cache, np.uint16)
+    bt = _as(block_table, np.int32)
+    sl = _as(seq_lens, np.int32)
+    cq = _as(cu_q, np.int32)
+    T, _, D = q.shape
+    Hkv, page = kc.shape[1], kc.shape[2]
+    out = np.empty((T, Hq, D), dtype=np.float32)
+    lse = np.empty((T, Hq), dtype=np.float32)
+    rc = lib().oracle_attention(_ptr(q), _ptr(kc), _ptr(vc), _ptr(bt), bt.shape[1], _ptr(sl),
+                                _ptr(cq), sl.size, Hq, Hkv, D, page, ctypes.c_float(scale),
+                                _ptr(out), _ptr(lse))
+    if rc:
+        raise RuntimeError(f"oracle_attention failed ({rc})")
+    return out, lse
+
+
+def attention_row(q, k_cache, v_cache, block_table, seq_lens, cu_q, b, j, h, Hq, scale):
+    """One (sequence b, query j, head h) row: (out fp32 [D], lse)."""
+    q = _as(q, np.uint16)
+    kc = _as(k_cache, np.uint16)
+    vc = _as(v_cache, np.uint16)
+    bt = _as(block_table, np.int32)
+    sl = _as(seq_lens, np.int32)
+    cq = _as(cu_q, np.int32)
+    D = q.shape[-1]
+    Hkv, page = kc.shape[1], kc.shape[2]
+    out = np.empty(D, dtype=np.float32)
+    lse = np.empty(1, dtype=np.float32)
+    rc = lib().oracle_attention_row(_ptr(q), _ptr(kc), _ptr(vc), _ptr(bt), bt.shape[1], _ptr(sl),
+                                    _ptr(cq), b, j, Hq, Hkv, D, page, h, ctypes.c_float(scale),
+                                    _ptr(out), _ptr(lse))
+    if rc:
+        raise RuntimeError(f"oracle_attention_row failed ({rc})")
+    return out, float(lse[0])
