@@ -1,0 +1,233 @@
+/*
+ * bi.h -- C ABI of libbi: batch-invariant transformer reductions on one NVIDIA GB300
+ * (sm_103a).  Matmul, RMSNorm, paged KV-cache append and decode / speculative-verify
+ * attention whose output bits for a given row or query do not depend on how many other
+ * rows share the batch, nor on whether a token is evaluated alone or inside a short
+ * causal verification block.
+ *
+ * Sources (web pages this library restates):
+ *   [MLX-4279] "Fix/speculative shape invariance", ml-explore/mlx pull request 4279:
+ *              sections Problem, Changes and the review thread (limit semantics, both
+ *              B orientations, query-length-independent attention split).
+ *   [BOOK]     "Batch-invariant kernels: why temperature-0 decoding is still
+ *              nondeterministic" (kanthi.in book chapter): Cases 2-5 (reduction trees),
+ *              Case 6 strategy table (data-parallel RMSNorm, one matmul config with no
+ *              Split-K, fixed split *size* for attention with the cache updated first),
+ *              and "The boring rule".
+ *
+ * Conventions shared by every entry point
+ *   - All tensor pointers are DEVICE pointers owned by the caller; the library never
+ *     allocates, frees or retains them.  Host-side state owned by the library: the
+ *     batch-invariant limit, a small cache of TMA descriptors (host memory), and one
+ *     32-bit device error word per device.
+ *   - Every launch is asynchronous and ordered on `stream` (a cudaStream_t; NULL means
+ *     the legacy default stream).  Nothing synchronises except bi_device_status().
+ *   - bf16 means IEEE bfloat16 stored as 16-bit patterns; outputs are rounded to
+ *     nearest-even from an fp32 accumulator.
+ *   - Argument errors return BI_ERR_INVALID_ARG (or BI_ERR_UNSUPPORTED for legal but
+ *     unimplemented shapes/alignments) BEFORE anything is launched.  A failed launch
+ *     returns BI_ERR_CUDA.  Every device-side wait is bounded: a wait that runs out sets
+ *     the device error word and the kernel returns; bi_device_status() then reports
+ *     BI_ERR_TIMEOUT.  Nothing traps or aborts.  bi_last_error_message() gives a
+ *     one-line, thread-local explanation of the last non-OK status.
+ *   - Determinism contract: for a fixed library build, the bits of output row m of
+ *     bi_matmul / bi_rmsnorm depend only on that row's inputs (and W / gamma), never on
+ *     M, on the other rows, or on the row's position in the batch.  The bits of a
+ *     query's attention output depend only on that query, its position and the keys
+ *     and values at positions 0..pos of its own sequence -- not on the batch, on the
+ *     verify-block width, or on the sequence's total length.
+ */
+#ifndef BI_H_
+#define BI_H_
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+#define BI_ABI_VERSION 1
+
+/* cudaStream_t without pulling in the CUDA headers. */
+typedef struct CUstream_st* bi_stream_t;
+
+typedef enum {
+    BI_OK = 0,
+    BI_ERR_INVALID_ARG = 1,  /* null pointer, negative size, inconsistent shape      */
+    BI_ERR_UNSUPPORTED = 2,  /* legal but not implemented (alignment, head_dim, ...) */
+    BI_ERR_CUDA = 3,         /* a CUDA runtime/driver call or launch failed          */
+    BI_ERR_TIMEOUT = 4,      /* a bounded device-side wait ran out                   */
+    BI_ERR_DEVICE_ARG = 5    /* a kernel found a bad device-resident argument
+                                (block-table entry out of range, q_len over max_q,
+                                seq_len shorter than its block); the work item was
+                                skipped, never read or written out of bounds          */
+} bi_status;
+
+typedef enum { BI_BF16 = 0, BI_F32 = 1 } bi_dtype;
+
+typedef enum {
+    BI_W_NK = 0,  /* W stored [N, K] row-major ("b_transposed", nn.Linear weight)  */
+    BI_W_KN = 1   /* W stored [K, N] row-major (natural orientation)               */
+} bi_wlayout;
+
+/* Fixed compile-time constants of this build (they decide the output bits). */
+#define BI_PAGE_SIZE 64        /* tokens per KV-cache page                           */
+#define BI_ATTN_CHUNK 512      /* keys per split-KV chunk (fixed split size)         */
+#define BI_ATTN_MAX_Q 8        /* widest verify block per sequence                   */
+#define BI_ATTN_MAX_ROWS 32    /* max q_len * (num_q_heads / num_kv_heads)            */
+
+int bi_abi_version(void);
+const char* bi_status_string(bi_status s);
+/* Thread-local one-line explanation of the last non-OK status returned on this thread. */
+const char* bi_last_error_message(void);
+
+/* ---------------------------------------------------------------------------------
+ * Batch-invariant limit  [MLX-4279, Changes: set_batch_invariant_limit /
+ * get_batch_invariant_limit and the MLX_METAL_BATCH_INVARIANT_LIMIT variable]
+ *
+ * Process-wide, stored atomically, default 0 (= disabled).  The environment variable
+ * BI_BATCH_INVARIANT_LIMIT, if set to a non-negative integer, gives the initial value
+ * (read once, at the first call of any entry point).  When the leading dimension
+ * (matmul M, RMSNorm rows) or the verify-block width (attention max_q) is <= limit,
+ * the entry point MUST use its invariant configuration.  Above the limit, or with the
+ * limit at 0, a library may pick a faster non-invariant path; this build has only the
+ * invariant kernels, so every call is invariant whatever the limit says.
+ * A negative limit returns BI_ERR_INVALID_ARG and leaves the setting unchanged.
+ * ------------------------------------------------------------------------------- */
+bi_status bi_set_batch_invariant_limit(int64_t limit);
+int64_t bi_get_batch_invariant_limit(void);
+/* 1 if a call with leading dimension / verify width `dim` falls inside the limit. */
+int bi_within_batch_invariant_limit(int64_t dim);
+
+/* ---------------------------------------------------------------------------------
+ * bi_matmul  [BOOK Case 3 and Case 6 "Matmul": one compiled config for all shapes, no
+ * Split-K; MLX-4279 Problem (GEMV vs gemv_wide vs GEMM by row count is the defect) and
+ * review thread (both B orientations)]
+ *
+ *   Y[m, n] = sum_{k < K} X[m, k] * W(k, n),  fp32 accumulation, then bf16 RNE
+ *   (y_dtype BI_BF16) or the fp32 accumulator itself (BI_F32).
+ *
+ *   x       bf16 [M, K] row-major, row stride ldx elements (ldx >= K).
+ *   w       bf16, layout BI_W_NK: [N, K] with row stride ldw (ldw >= K);
+ *                 layout BI_W_KN: [K, N] with row stride ldw (ldw >= N).
+ *   y       [M, N] row-major, row stride ldy (ldy >= N), dtype y_dtype.
+ *   M, N, K >= 0; M = 0 or N = 0 is a no-op; K = 0 writes zeros.
+ *   Invariant construction: one tcgen05 tile shape (128 x BN x 16 instructions, BK = 64
+ *   K-blocks taken in ascending order, fp32 accumulation in tensor memory) for every M.
+ *   Row m is always computed in M-tile m/128 at lane m%128; rows beyond M are zero-filled
+ *   by TMA and never stored.
+ *   Alignment (TMA rule): x, w 16-byte aligned; ldx, ldw multiples of 8 elements;
+ *   otherwise BI_ERR_UNSUPPORTED.  y needs only element alignment.
+ *   Limits: M, N, K < 2^31.
+ * ------------------------------------------------------------------------------- */
+bi_status bi_matmul(const void* x, int64_t ldx, const void* w, int64_t ldw, int w_layout,
+                    void* y, int64_t ldy, int y_dtype, int64_t M, int64_t N, int64_t K,
+                    bi_stream_t stream);
+
+/* ---------------------------------------------------------------------------------
+ * bi_rmsnorm  [BOOK Case 4 (definition and the load-dependent-tree defect) and Case 6
+ * "RMSNorm": data-parallel, one row per core, never split]
+ *
+ *   ss = sum_i x_i^2 (fp32);  y_i = x_i * rsqrt(ss / H + eps) * gamma_i
+ *
+ *   x      bf16 [rows, H], row stride ldx >= H.   gamma bf16 [H].
+ *   y      [rows, H], row stride ldy >= H, dtype y_dtype (bf16 RNE or fp32).
+ *   Each row is reduced by exactly one CTA with a reduction tree that is a function of
+ *   H only (per-thread ascending sums over 8-element groups, then a fixed warp-shuffle
+ *   tree, then a fixed cross-warp tree).  rows = 0 is a no-op.  H in [1, 2^20].
+ *   eps must be finite and >= 0.  Any alignment is accepted (16-byte aligned rows use
+ *   128-bit loads; the arithmetic is the same either way).
+ * ------------------------------------------------------------------------------- */
+bi_status bi_rmsnorm(const void* x, int64_t ldx, const void* gamma, void* y, int64_t ldy,
+                     int y_dtype, int64_t rows, int64_t hidden, float eps,
+                     bi_stream_t stream);
+
+/* ---------------------------------------------------------------------------------
+ * Paged KV cache (shared by the three attention entry points)
+ *
+ *   k_cache, v_cache  bf16 [num_pages, num_kv_heads, BI_PAGE_SIZE, head_dim]; 16-byte
+ *                     aligned.
+ *   block_table       int32 [batch, max_pages]: block_table[b*max_pages + i] is the
+ *                     physical page holding positions [i*PAGE, (i+1)*PAGE) of sequence b.
+ *   seq_lens          int32 [batch]: tokens in sequence b INCLUDING its new block.
+ *   cu_q              int32 [batch + 1]: new tokens of sequence b are rows
+ *                     cu_q[b] .. cu_q[b+1]-1 of the token-major tensors; token j of the
+ *                     block sits at position seq_lens[b] - (cu_q[b+1]-cu_q[b]) + j.
+ *   All of these are device pointers.  page_size must equal BI_PAGE_SIZE.
+ * ------------------------------------------------------------------------------- */
+
+/* bi_kv_append  [BOOK Case 6 "Attention": update the KV cache before the kernel]
+ *   Copies k_new / v_new (bf16 [total_q, num_kv_heads, head_dim]) into their slots.
+ *   Must run (stream-ordered) before bi_verify_block for the same block. */
+bi_status bi_kv_append(const void* k_new, const void* v_new, void* k_cache, void* v_cache,
+                       int64_t num_pages, const int32_t* block_table, int64_t max_pages,
+                       const int32_t* seq_lens, const int32_t* cu_q, int64_t batch,
+                       int64_t total_q, int64_t num_kv_heads, int64_t head_dim,
+                       int64_t page_size, bi_stream_t stream);
+
+/* Bytes of caller-provided workspace bi_verify_block / bi_decode_attn need: one fp32
+ * partial (m, l, o[head_dim]) per (token, query head, chunk), for chunks of
+ * BI_ATTN_CHUNK keys up to max_seq_len.  Returns 0 for invalid arguments. */
+size_t bi_attn_workspace_size(int64_t total_q, int64_t num_q_heads, int64_t head_dim,
+                              int64_t max_seq_len);
+
+/* bi_verify_block  [MLX-4279 Problem/Changes (two-pass SDPA split count must not follow
+ * the query length); BOOK Case 6 "Attention" (fixed split size, varying #splits) and
+ * the requirement that token 1000 reduces identically with 0 or 999 cached tokens]
+ *
+ *   For every sequence b and block token j (position pos = seq_lens[b]-q_b+j) and query
+ *   head h (KV head h / (num_q_heads/num_kv_heads)):
+ *     out[t, h, :] = softmax_i(scale * q[t,h,:] . k_i) @ v_i over keys i = 0..pos
+ *     lse[t, h]    = log sum_i exp(scale * q . k_i)            (natural log; nullable)
+ *   Split-KV with a FIXED chunk length BI_ATTN_CHUNK counted from key 0: chunk c covers
+ *   keys [c*CHUNK, (c+1)*CHUNK); a query uses chunks 0..pos/CHUNK, each reduced with the
+ *   same instruction sequence whatever the batch or block width, and the partials are
+ *   merged by log-sum-exp in ascending chunk order.
+ *
+ *   q        bf16 [total_q, num_q_heads, head_dim]; out bf16 same shape; lse fp32
+ *            [total_q, num_q_heads] or NULL.  workspace: device memory of at least
+ *            bi_attn_workspace_size(total_q, num_q_heads, head_dim, max_seq_len) bytes,
+ *            16-byte aligned, contents scratch.
+ *   max_q    upper bound of every q_b (1..BI_ATTN_MAX_Q), max_q * (num_q_heads /
+ *            num_kv_heads) <= BI_ATTN_MAX_ROWS.  max_seq_len: upper bound of every
+ *            seq_lens[b] (>= 1).  head_dim in {64, 128}.  num_q_heads % num_kv_heads == 0.
+ *   Device-resident arguments are checked in the kernel (page index < num_pages,
+ *   1 <= q_b <= max_q, q_b <= seq_len <= max_seq_len); an offending work item is skipped
+ *   and BI_ERR_DEVICE_ARG is latched for bi_device_status(). */
+bi_status bi_verify_block(const void* q, const void* k_cache, const void* v_cache,
+                          int64_t num_pages, const int32_t* block_table, int64_t max_pages,
+                          const int32_t* seq_lens, const int32_t* cu_q, int64_t batch,
+                          int64_t total_q, int64_t max_q, int64_t max_seq_len,
+                          int64_t num_q_heads, int64_t num_kv_heads, int64_t head_dim,
+                          int64_t page_size, float scale, void* out, float* lse,
+                          void* workspace, size_t workspace_bytes, bi_stream_t stream);
+
+/* bi_decode_attn: bi_verify_block with exactly one new token per sequence (token b is
+ * the last position of sequence b; q, out: [batch, num_q_heads, head_dim]).  Runs the
+ * same kernels, so its bits equal bi_verify_block's with q_b = 1. */
+bi_status bi_decode_attn(const void* q, const void* k_cache, const void* v_cache,
+                         int64_t num_pages, const int32_t* block_table, int64_t max_pages,
+                         const int32_t* seq_lens, int64_t batch, int64_t max_seq_len,
+                         int64_t num_q_heads, int64_t num_kv_heads, int64_t head_dim,
+                         int64_t page_size, float scale, void* out, float* lse,
+                         void* workspace, size_t workspace_bytes, bi_stream_t stream);
+
+/* ---------------------------------------------------------------------------------
+ * Device error word
+ * bi_device_status synchronises `stream`, reads and clears the current device's error
+ * word and returns BI_OK, BI_ERR_TIMEOUT (a bounded wait ran out), BI_ERR_DEVICE_ARG,
+ * or BI_ERR_CUDA if the synchronisation itself failed.
+ * ------------------------------------------------------------------------------- */
+bi_status bi_device_status(bi_stream_t stream);
+
+/* Failure-detection self-test: launches one CTA that waits on an mbarrier nobody
+ * arrives at, bounded by timeout_ns nanoseconds (1e3 .. 1e10).  The wait runs out, the
+ * kernel latches BI_ERR_TIMEOUT in the error word and returns, leaving the context
+ * usable.  Used by the tests to exercise the timeout path without faulting a GPU. */
+bi_status bi_selftest_wait_timeout(uint64_t timeout_ns, bi_stream_t stream);
+
+#ifdef __cplusplus
+}
+#endif
+#endif /* BI_H_ */

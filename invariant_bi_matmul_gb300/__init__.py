@@ -1,5 +1,286 @@
-"""Batch-invariant transformer reductions for one GB300 (sm_103a).
+"""Batch-invariant transformer reductions for one NVIDIA GB300 (sm_103a).
 
-The compute lives in ``libbi.so`` (CUDA kernels behind a C ABI, see ``include/bi.h``);
-this package is its thin ctypes binding.  The shared library is loaded on first use.
+The compute lives in ``libbi.so`` -- hand-written CUDA kernels behind the C ABI declared
+in ``include/bi.h``.  This module is its thin ctypes binding: it checks that tensors are
+CUDA tensors of the right dtype, reads their pointers, strides and the current stream,
+and calls the C entry point of the same name.  Outputs it is asked to create are
+allocated with torch (device memory is torch's job); every arithmetic step runs in the
+kernels.  There is no CPU fallback: if the library is missing or fails to load, every
+call raises.
 """
+from __future__ import annotations
+
+import ctypes
+import os
+from typing import Optional
+
+HERE = os.path.dirname(os.path.abspath(__file__))
+LIB_PATH = os.environ.get("BI_LIBRARY_PATH") or os.path.join(HERE, "libbi.so")
+
+BI_OK, BI_ERR_INVALID_ARG, BI_ERR_UNSUPPORTED, BI_ERR_CUDA, BI_ERR_TIMEOUT, BI_ERR_DEVICE_ARG = range(6)
+BI_BF16, BI_F32 = 0, 1
+BI_W_NK, BI_W_KN = 0, 1
+PAGE_SIZE = 64
+ATTN_CHUNK = 512
+ATTN_MAX_Q = 8
+ATTN_MAX_ROWS = 32
+
+# every function include/bi.h declares, with its ctypes signature
+_p, _i64, _f32, _sz, _int = ctypes.c_void_p, ctypes.c_int64, ctypes.c_float, ctypes.c_size_t, ctypes.c_int
+SIGNATURES = {
+    "bi_abi_version": ([], _int),
+    "bi_status_string": ([_int], ctypes.c_char_p),
+    "bi_last_error_message": ([], ctypes.c_char_p),
+    "bi_set_batch_invariant_limit": ([_i64], _int),
+    "bi_get_batch_invariant_limit": ([], _i64),
+    "bi_within_batch_invariant_limit": ([_i64], _int),
+    "bi_matmul": ([_p, _i64, _p, _i64, _int, _p, _i64, _int, _i64, _i64, _i64, _p], _int),
+    "bi_rmsnorm": ([_p, _i64, _p, _p, _i64, _int, _i64, _i64, _f32, _p], _int),
+    "bi_kv_append": ([_p, _p, _p, _p, _i64, _p, _i64, _p, _p, _i64, _i64, _i64, _i64, _i64, _p],
+                     _int),
+    "bi_attn_workspace_size": ([_i64, _i64, _i64, _i64], _sz),
+    "bi_verify_block": ([_p, _p, _p, _i64, _p, _i64, _p, _p, _i64, _i64, _i64, _i64, _i64, _i64,
+                         _i64, _i64, _f32, _p, _p, _p, _sz, _p], _int),
+    "bi_decode_attn": ([_p, _p, _p, _i64, _p, _i64, _p, _i64, _i64, _i64, _i64, _i64, _i64, _f32,
+                        _p, _p, _p, _sz, _p], _int),
+    "bi_device_status": ([_p], _int),
+    "bi_selftest_wait_timeout": ([ctypes.c_uint64, _p], _int),
+}
+
+_lib: Optional[ctypes.CDLL] = None
+
+
+class BIError(RuntimeError):
+    def __init__(self, status: int, message: str):
+        super().__init__(f"{_status_name(status)}: {message}")
+        self.status = status
+
+
+def _status_name(s: int) -> str:
+    names = ["BI_OK", "BI_ERR_INVALID_ARG", "BI_ERR_UNSUPPORTED", "BI_ERR_CUDA", "BI_ERR_TIMEOUT",
+             "BI_ERR_DEVICE_ARG"]
+    return names[s] if 0 <= s < len(names) else f"status {s}"
+
+
+def lib() -> ctypes.CDLL:
+    """The loaded libbi.so (raises if it was never built)."""
+    global _lib
+    if _lib is None:
+        if not os.path.exists(LIB_PATH):
+            raise RuntimeError(f"libbi.so not found at {LIB_PATH}; build it with "
+                               "`python -c 'import __graft_entry__ as g; g.build()'`")
+        L = ctypes.CDLL(LIB_PATH)
+        for name, (args, res) in SIGNATURES.items():
+            fn = getattr(L, name)
+            fn.argtypes = args
+            fn.restype = res
+        _lib = L
+    return _lib
+
+
+def _check(status: int) -> None:
+    if status != BI_OK:
+        msg = lib().bi_last_error_message().decode(errors="replace")
+        raise BIError(status, msg)
+
+
+def _torch():
+    import torch
+    return torch
+
+
+def _stream(stream) -> int:
+    torch = _torch()
+    if stream is None:
+        return torch.cuda.current_stream().cuda_stream
+    if isinstance(stream, int):
+        return stream
+    return stream.cuda_stream
+
+
+def _ptr(t) -> Optional[int]:
+    return None if t is None else t.data_ptr()
+
+
+def _need(t, dtype, name, ndim=None):
+    torch = _torch()
+    if not isinstance(t, torch.Tensor):
+        raise TypeError(f"{name} must be a torch.Tensor")
+    if not t.is_cuda:
+        raise ValueError(f"{name} must be a CUDA tensor (there is no CPU path)")
+    if t.dtype != dtype:
+        raise TypeError(f"{name} must be {dtype}, got {t.dtype}")
+    if ndim is not None and t.dim() != ndim:
+        raise ValueError(f"{name} must have {ndim} dimensions, got {t.dim()}")
+
+
+def _row_major_2d(t, name):
+    if t.stride(1) != 1:
+        raise ValueError(f"{name} must have unit stride in its last dimension")
+    return t.stride(0) if t.shape[0] > 1 else max(t.stride(0), t.shape[1])
+
+
+# ------------------------------------------------------------------------------ limit
+
+def set_batch_invariant_limit(limit: int) -> None:
+    _check(lib().bi_set_batch_invariant_limit(int(limit)))
+
+
+def get_batch_invariant_limit() -> int:
+    return int(lib().bi_get_batch_invariant_limit())
+
+
+def within_batch_invariant_limit(dim: int) -> bool:
+    return bool(lib().bi_within_batch_invariant_limit(int(dim)))
+
+
+# ----------------------------------------------------------------------------- matmul
+
+def matmul(x, w, w_layout: str = "nk", out=None, out_dtype=None, stream=None):
+    """Y = X @ W for X bf16 [M,K] and W bf16 [N,K] ("nk", nn.Linear) or [K,N] ("kn")."""
+    torch = _torch()
+    _need(x, torch.bfloat16, "x", 2)
+    _need(w, torch.bfloat16, "w", 2)
+    layout = {"nk": BI_W_NK, "kn": BI_W_KN}[w_layout]
+    M, K = x.shape
+    N = w.shape[0] if layout == BI_W_NK else w.shape[1]
+    if (w.shape[1] if layout == BI_W_NK else w.shape[0]) != K:
+        raise ValueError("inner dimensions of x and w differ")
+    if out is None:
+        out = torch.empty(M, N, dtype=out_dtype or torch.bfloat16, device=x.device)
+    if out.dtype not in (torch.bfloat16, torch.float32) or tuple(out.shape) != (M, N):
+        raise ValueError("out must be [M,N] bf16 or fp32")
+    _check(lib().bi_matmul(_ptr(x), _row_major_2d(x, "x"), _ptr(w), _row_major_2d(w, "w"), layout,
+                           _ptr(out), _row_major_2d(out, "out"),
+                           BI_F32 if out.dtype == torch.float32 else BI_BF16, M, N, K,
+                           _stream(stream)))
+    return out
+
+
+# ---------------------------------------------------------------------------- rmsnorm
+
+def rmsnorm(x, gamma, eps: float, out=None, out_dtype=None, stream=None):
+    """y = x * rsqrt(mean(x^2) + eps) * gamma over the last dim of a bf16 [rows, H] x."""
+    torch = _torch()
+    _need(x, torch.bfloat16, "x", 2)
+    _need(gamma, torch.bfloat16, "gamma", 1)
+    rows, H = x.shape
+    if gamma.shape[0] != H or gamma.stride(0) != 1:
+        raise ValueError("gamma must be a contiguous [H] tensor")
+    if out is None:
+        out = torch.empty(rows, H, dtype=out_dtype or torch.bfloat16, device=x.device)
+    _check(lib().bi_rmsnorm(_ptr(x), _row_major_2d(x, "x"), _ptr(gamma), _ptr(out),
+                            _row_major_2d(out, "out"),
+                            BI_F32 if out.dtype == torch.float32 else BI_BF16, rows, H,
+                            float(eps), _stream(stream)))
+    return out
+
+
+# ------------------------------------------------------------------ paged attention
+
+def _paged_common(k_cache, v_cache, block_table, seq_lens):
+    torch = _torch()
+    _need(k_cache, torch.bfloat16, "k_cache", 4)
+    _need(v_cache, torch.bfloat16, "v_cache", 4)
+    _need(block_table, torch.int32, "block_table", 2)
+    _need(seq_lens, torch.int32, "seq_lens", 1)
+    if not (k_cache.is_contiguous() and v_cache.is_contiguous() and block_table.is_contiguous()
+            and seq_lens.is_contiguous()):
+        raise ValueError("caches, block_table and seq_lens must be contiguous")
+    if k_cache.shape != v_cache.shape:
+        raise ValueError("k_cache and v_cache shapes differ")
+    num_pages, hkv, page, d = k_cache.shape
+    return num_pages, hkv, page, d
+
+
+def kv_append(k_new, v_new, k_cache, v_cache, block_table, seq_lens, cu_q, stream=None):
+    """Writes the block's new keys/values into their cache slots (before attention)."""
+    torch = _torch()
+    num_pages, hkv, page, d = _paged_common(k_cache, v_cache, block_table, seq_lens)
+    _need(k_new, torch.bfloat16, "k_new", 3)
+    _need(v_new, torch.bfloat16, "v_new", 3)
+    _need(cu_q, torch.int32, "cu_q", 1)
+    if not (k_new.is_contiguous() and v_new.is_contiguous() and cu_q.is_contiguous()):
+        raise ValueError("k_new, v_new and cu_q must be contiguous")
+    B = seq_lens.shape[0]
+    _check(lib().bi_kv_append(_ptr(k_new), _ptr(v_new), _ptr(k_cache), _ptr(v_cache), num_pages,
+                              _ptr(block_table), block_table.shape[1], _ptr(seq_lens), _ptr(cu_q),
+                              B, k_new.shape[0], hkv, d, page, _stream(stream)))
+
+
+def attn_workspace_size(total_q: int, num_q_heads: int, head_dim: int, max_seq_len: int) -> int:
+    return int(lib().bi_attn_workspace_size(total_q, num_q_heads, head_dim, max_seq_len))
+
+
+def _attn_out(q, out, lse, want_lse):
+    torch = _torch()
+    T, hq, d = q.shape
+    if out is None:
+        out = torch.empty(T, hq, d, dtype=torch.bfloat16, device=q.device)
+    _need(out, torch.bfloat16, "out", 3)
+    if not out.is_contiguous() or tuple(out.shape) != (T, hq, d):
+        raise ValueError("out must be a contiguous [T, Hq, D] bf16 tensor")
+    if lse is None and want_lse:
+        lse = torch.empty(T, hq, dtype=torch.float32, device=q.device)
+    if lse is not None:
+        _need(lse, torch.float32, "lse", 2)
+        if not lse.is_contiguous() or tuple(lse.shape) != (T, hq):
+            raise ValueError("lse must be a contiguous [T, Hq] fp32 tensor")
+    return out, lse
+
+
+def _workspace(workspace, need, device):
+    torch = _torch()
+    if workspace is None:
+        workspace = torch.empty(max(need, 16), dtype=torch.uint8, device=device)
+    return workspace, workspace.numel() * workspace.element_size()
+
+
+def verify_block(q, k_cache, v_cache, block_table, seq_lens, cu_q, max_q: int, max_seq_len: int,
+                 scale: float, out=None, lse=None, want_lse=True, workspace=None, stream=None):
+    """Causal attention of each sequence's new block (q bf16 [T,Hq,D]) over its paged cache."""
+    torch = _torch()
+    num_pages, hkv, page, d = _paged_common(k_cache, v_cache, block_table, seq_lens)
+    _need(q, torch.bfloat16, "q", 3)
+    _need(cu_q, torch.int32, "cu_q", 1)
+    if not q.is_contiguous() or not cu_q.is_contiguous():
+        raise ValueError("q and cu_q must be contiguous")
+    T, hq, _ = q.shape
+    out, lse = _attn_out(q, out, lse, want_lse)
+    ws, ws_bytes = _workspace(workspace, attn_workspace_size(T, hq, d, max_seq_len), q.device)
+    _check(lib().bi_verify_block(_ptr(q), _ptr(k_cache), _ptr(v_cache), num_pages,
+                                 _ptr(block_table), block_table.shape[1], _ptr(seq_lens),
+                                 _ptr(cu_q), seq_lens.shape[0], T, int(max_q), int(max_seq_len),
+                                 hq, hkv, d, page, float(scale), _ptr(out), _ptr(lse), _ptr(ws),
+                                 ws_bytes, _stream(stream)))
+    return out, lse
+
+
+def decode_attn(q, k_cache, v_cache, block_table, seq_lens, max_seq_len: int, scale: float,
+                out=None, lse=None, want_lse=True, workspace=None, stream=None):
+    """One new token per sequence: q bf16 [B,Hq,D]; token b is the last position of b."""
+    torch = _torch()
+    num_pages, hkv, page, d = _paged_common(k_cache, v_cache, block_table, seq_lens)
+    _need(q, torch.bfloat16, "q", 3)
+    if not q.is_contiguous():
+        raise ValueError("q must be contiguous")
+    B, hq, _ = q.shape
+    out, lse = _attn_out(q, out, lse, want_lse)
+    ws, ws_bytes = _workspace(workspace, attn_workspace_size(B, hq, d, max_seq_len), q.device)
+    _check(lib().bi_decode_attn(_ptr(q), _ptr(k_cache), _ptr(v_cache), num_pages,
+                                _ptr(block_table), block_table.shape[1], _ptr(seq_lens), B,
+                                int(max_seq_len), hq, hkv, d, page, float(scale), _ptr(out),
+                                _ptr(lse), _ptr(ws), ws_bytes, _stream(stream)))
+    return out, lse
+
+
+# ---------------------------------------------------------------------- device status
+
+def device_status(stream=None) -> int:
+    """Synchronises the stream; returns the bi_status of the device error word (and
+    clears it)."""
+    return int(lib().bi_device_status(_stream(stream)))
+
+
+def selftest_wait_timeout(timeout_ns: int, stream=None) -> None:
+    _check(lib().bi_selftest_wait_timeout(int(timeout_ns), _stream(stream)))

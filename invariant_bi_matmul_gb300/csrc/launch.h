@@ -1,0 +1,69 @@
+// launch.h -- host-side launchers of the libbi kernels (internal; the public surface is
+// include/bi.h).  Arguments are already validated by api.cu when these are called.
+#pragma once
+
+#include <cuda_runtime.h>
+#include <stddef.h>
+#include <stdint.h>
+
+namespace bi {
+
+// Bits of the per-device error word (the host maps them to bi_status codes).
+enum : unsigned int {
+    kErrTimeout = 1u,    // a bounded wait ran out
+    kErrDeviceArg = 2u,  // a device-resident argument was out of range; work skipped
+};
+
+struct DeviceInfo {
+    int device = -1;
+    int num_sms = 0;
+    unsigned int* err_word = nullptr;  // device address of this device's error word
+};
+
+// Current device's cached properties and error-word address (nullptr on failure).
+const DeviceInfo* current_device_info(cudaError_t* why);
+
+// ---------------------------------------------------------------- RMSNorm (rmsnorm.cu)
+cudaError_t launch_rmsnorm(const void* x, int64_t ldx, const void* gamma, void* y, int64_t ldy,
+                           bool y_f32, int64_t rows, int64_t hidden, float eps,
+                           cudaStream_t stream);
+
+// ------------------------------------------------------------------- GEMM (gemm.cu)
+// Returns cudaErrorNotSupported when a TMA descriptor cannot be encoded.
+cudaError_t launch_gemm(const DeviceInfo& dev, const void* x, int64_t ldx, const void* w,
+                        int64_t ldw, bool w_kn, void* y, int64_t ldy, bool y_f32, int64_t M,
+                        int64_t N, int64_t K, cudaStream_t stream);
+int gemm_tile_n();
+
+// ------------------------------------------------------------ attention (attention.cu)
+struct PagedArgs {
+    const void* k_cache;
+    const void* v_cache;
+    int64_t num_pages;
+    const int32_t* block_table;
+    int64_t max_pages;
+    const int32_t* seq_lens;
+    const int32_t* cu_q;  // nullptr: one token per sequence (decode)
+    int64_t batch;
+    int64_t total_q;
+    int64_t max_q;
+    int64_t max_seq_len;
+    int64_t hq;
+    int64_t hkv;
+    int64_t head_dim;
+};
+
+cudaError_t launch_kv_append(const DeviceInfo& dev, const void* k_new, const void* v_new,
+                             void* k_cache, void* v_cache, const PagedArgs& a,
+                             cudaStream_t stream);
+
+size_t attn_workspace_bytes(int64_t total_q, int64_t hq, int64_t head_dim, int64_t max_seq_len);
+
+cudaError_t launch_attention(const DeviceInfo& dev, const void* q, const PagedArgs& a,
+                             float scale, void* out, float* lse, void* workspace,
+                             cudaStream_t stream);
+
+cudaError_t launch_selftest_wait(const DeviceInfo& dev, unsigned long long timeout_ns,
+                                 cudaStream_t stream);
+
+}  // namespace bi

@@ -1,0 +1,58 @@
+"""Parity tolerances between the CUDA path and the CPU oracle.
+
+The pages state the accuracy bar as max abs error <= 2e-2 and relative error <= 1e-2 for
+bf16 outputs and <= 1e-4 relative for fp32 outputs.  Read elementwise, against the
+oracle's UNROUNDED fp32 value o:
+  bf16 output g:   |g - o| <= 2e-2 + 1e-2 * |o|
+  fp32 output g:   |g - o| <= 1e-4 * S
+where S is the natural error scale of the reduction: sum_k |x_k w_k| for a dot product,
+|o| for RMSNorm, max_i |v_i| for attention.  (Comparing against the bf16-rounded oracle
+instead would let one rounding-boundary flip exceed 2e-2 once |o| >= 4.)
+"""
+import numpy as np
+
+BF16_ATOL = 2e-2
+BF16_RTOL = 1e-2
+F32_REL = 1e-4
+
+
+def to_f64(t) -> np.ndarray:
+    return t.detach().float().cpu().numpy().astype(np.float64)
+
+
+def check_bf16(gpu, oracle_f32, what=""):
+    g = to_f64(gpu)
+    o = np.asarray(oracle_f32, dtype=np.float64)
+    assert g.shape == o.shape, (g.shape, o.shape)
+    assert np.all(np.isfinite(g)), f"{what}: non-finite GPU output"
+    err = np.abs(g - o)
+    bound = BF16_ATOL + BF16_RTOL * np.abs(o)
+    bad = err > bound
+    if bad.any():
+        i = np.unravel_index(np.argmax(err - bound), err.shape)
+        raise AssertionError(f"{what}: {int(bad.sum())} elements outside tolerance; worst at {i}: "
+                             f"gpu={g[i]!r} oracle={o[i]!r}")
+    return float(err.max()) if err.size else 0.0
+
+
+def check_f32(gpu, oracle_f32, scale, what=""):
+    g = to_f64(gpu)
+    o = np.asarray(oracle_f32, dtype=np.float64)
+    s = np.broadcast_to(np.asarray(scale, dtype=np.float64), o.shape)
+    err = np.abs(g - o)
+    bound = F32_REL * s + 1e-30
+    bad = err > bound
+    if bad.any():
+        i = np.unravel_index(np.argmax(err / bound), err.shape)
+        raise AssertionError(f"{what}: {int(bad.sum())} elements outside fp32 tolerance; worst at "
+                             f"{i}: gpu={g[i]!r} oracle={o[i]!r} scale={s[i]!r}")
+    return float(err.max()) if err.size else 0.0
+
+
+def bits_equal(a, b) -> bool:
+    """Bitwise equality of two CUDA/CPU tensors of the same dtype."""
+    import torch
+    if a.dtype != b.dtype or a.shape != b.shape:
+        return False
+    view = {torch.bfloat16: torch.int16, torch.float32: torch.int32}[a.dtype]
+    return bool(torch.equal(a.contiguous().view(view).cpu(), b.contiguous().view(view).cpu()))
