@@ -1,0 +1,614 @@
+"""Throughput of the batch-invariant hot path on GB300.
+
+One step = one speculative-verify step of M = 8 tokens through every reduction of the
+path, on the pages' shapes:
+  1. bi_rmsnorm       x [8, 4096] bf16 (eps 1e-5)
+  2. bi_matmul (NK)   [8, 4096] x W[4096, 4096] stored [N, K]  -> q  [8, 32, 128]
+  3. bi_kv_append     the block's 8 new K/V tokens (8 KV heads, head_dim 128)
+  4. bi_verify_block  1 sequence, causal block of q = 8, Lk = 65540, 32 query heads /
+                      8 KV heads, bf16 paged cache (64-token pages, permuted)
+  5. bi_matmul (KN)   [8, 4096] x W[4096, 4096] stored [K, N]  -> y  [8, 4096]
+All of it is HBM-bound at M = 8, so `value` is the step's algorithmic bytes (every
+operand read once, every result written once) divided by the device time of the step:
+whole-job GB/s over all ranks.  Inputs are resident in HBM before the timed region; the
+step streams ~336 MB (KV cache 268 MB + two 32 MiB weights), more than 2x the 126 MB L2,
+so no input survives in L2 from one step to the next.
+
+`python bench.py [--gpus N --steps K --warmup W]` prints one JSON line.
+`--impl reference` times the plain CPU oracle on a bounded sample of the same step.
+`--sweep` prints extra lines (GEMM M sweep vs cuBLAS, RMSNorm and attention configs).
+"""
+from __future__ import annotations
+
+import argparse
+import hashlib
+import json
+import math
+import os
+import re
+import statistics
+import subprocess
+import sys
+import threading
+import time
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+if ROOT not in sys.path:
+    sys.path.insert(0, ROOT)
+
+METRIC = "invariant GEMM TFLOP/s & decode-attn HBM GB/s at M=1..8, % roofline, 1 GB300"
+
+# step shape
+M_TOK = 8
+HIDDEN = 4096
+HQ, HKV, HEAD_DIM = 32, 8, 128
+LK = 65540
+EPS = 1e-5
+PAGE = 64
+
+FALLBACK_PEAKS = {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustained": 1700.0}
+
+
+def step_bytes() -> dict:
+    """Algorithmic bytes of each call of one step."""
+    tok = M_TOK * HIDDEN * 2
+    kv_tok = M_TOK * HKV * HEAD_DIM * 2
+    return {
+        "rmsnorm": 2 * tok + HIDDEN * 2,
+        "matmul_nk": HIDDEN * HIDDEN * 2 + 2 * tok,
+        "kv_append": 2 * 2 * kv_tok,
+        "verify_block": LK * HKV * HEAD_DIM * 2 * 2 + 2 * tok + M_TOK * HQ * 4,
+        "matmul_kn": HIDDEN * HIDDEN * 2 + 2 * tok,
+    }
+
+
+def step_flops() -> dict:
+    return {
+        "matmul_nk": 2 * M_TOK * HIDDEN * HIDDEN,
+        "matmul_kn": 2 * M_TOK * HIDDEN * HIDDEN,
+        # q.k and p.v for every (query, head, visible key)
+        "verify_block": sum(4 * HQ * HEAD_DIM * (LK - M_TOK + j + 1) for j in range(M_TOK)),
+    }
+
+
+def load_peaks():
+    path = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    if os.path.exists(path):
+        with open(path) as f:
+            d = json.load(f)
+        return d, "measured"
+    return dict(FALLBACK_PEAKS), "fallback"
+
+
+def source_digest(*names) -> str:
+    h = hashlib.sha256()
+    for n in names:
+        with open(os.path.join(ROOT, "invariant_bi_matmul_gb300", "csrc", n), "rb") as f:
+            h.update(f.read())
+    return h.hexdigest()[:16]
+
+
+def recorded_traffic():
+    """dram bytes per launch of the verify kernels, from the committed ncu summary, or
+    None once the attention sources differ from the ones profiled."""
+    path = os.path.join(ROOT, "profiles", "attn_verify_q8_L65540.md")
+    if not os.path.exists(path):
+        return None
+    text = open(path).read()
+    m = re.search(r"traffic_bytes_per_call:\s*([0-9.eE+]+)", text)
+    s = re.search(r"source_digest:\s*([0-9a-f]+)", text)
+    if not m or not s:
+        return None
+    if s.group(1) != source_digest("attention.cu", "common.cuh"):
+        return None
+    return float(m.group(1))
+
+
+# ---------------------------------------------------------------------------- clocks
+
+class ClockSampler:
+    """nvidia-smi samples (200 ms) taken while the timed region runs."""
+
+    FIELDS = ("clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+              "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+              "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, index: int):
+        self.index = index
+        self.proc = None
+        self.lines = []
+
+    def __enter__(self):
+        try:
+            self.proc = subprocess.Popen(
+                ["nvidia-smi", "-i", str(self.index), f"--query-gpu={self.FIELDS}",
+                 "--format=csv,noheader,nounits", "-lms", "200"],
+                stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
+            self.thread = threading.Thread(target=self._read, daemon=True)
+            self.thread.start()
+        except OSError:
+            self.proc = None
+        return self
+
+    def _read(self):
+        for line in self.proc.stdout:
+            self.lines.append(line.strip())
+
+    def __exit__(self, *exc):
+        if self.proc is not None:
+            self.proc.terminate()
+            try:
+                self.proc.wait(timeout=5)
+            except subprocess.TimeoutExpired:
+                self.proc.kill()
+            self.thread.join(timeout=2)
+
+    def summary(self):
+        sm, mx, reasons = [], None, set()
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        for line in self.lines:
+            parts = [p.strip() for p in line.split(",")]
+            if len(parts) < 8:
+                continue
+            try:
+                sm.append(float(parts[0]))
+                mx = float(parts[1])
+            except ValueError:
+                continue
+            for n, v in zip(names, parts[4:8]):
+                if v.lower().startswith("active"):
+                    reasons.add(n)
+        if not sm:
+            return {"sm_mhz": None, "sm_max_mhz": mx, "reasons": [], "samples": 0}
+        return {"sm_mhz": statistics.median(sm), "sm_max_mhz": mx, "reasons": sorted(reasons),
+                "samples": len(sm)}
+
+
+# ------------------------------------------------------------------------ GPU arm
+
+class Step:
+    """Device-resident buffers of one verify step and its five C-ABI calls."""
+
+    def __init__(self, dev, seed: int = 5):
+        import torch
+        import invariant_bi_matmul_gb300 as bi
+        from invariant_bi_matmul_gb300 import inputs
+        self.torch, self.bi, self.dev = torch, bi, dev
+        L = bi.lib()
+        self.L = L
+        g = inputs.gemm_inputs(M_TOK, HIDDEN, HIDDEN, seed=seed)
+        self.x = g.x.to(dev)
+        self.gamma = inputs.normal_bf16((HIDDEN,), 1.0, 0.1, seed=seed + 1).to(dev)
+        self.w_q = g.w_nk.to(dev)                                       # [N, K]
+        self.w_o = inputs.gemm_inputs(1, HIDDEN, HIDDEN, seed=seed + 2).w_kn.to(dev)  # [K, N]
+        p = inputs.paged_inputs([LK], [M_TOK], Hq=HQ, Hkv=HKV, D=HEAD_DIM, seed=seed + 3,
+                                device=dev)
+        self.k_cache, self.v_cache = p.k_cache, p.v_cache
+        self.block_table = p.block_table.to(dev)
+        self.seq_lens = p.seq_lens.to(dev)
+        self.cu_q = p.cu_q.to(dev)
+        self.k_new, self.v_new = p.k_new.to(dev), p.v_new.to(dev)
+        self.h = torch.empty(M_TOK, HIDDEN, dtype=torch.bfloat16, device=dev)
+        self.q = torch.empty(M_TOK, HQ, HEAD_DIM, dtype=torch.bfloat16, device=dev)
+        self.o = torch.empty(M_TOK, HQ, HEAD_DIM, dtype=torch.bfloat16, device=dev)
+        self.lse = torch.empty(M_TOK, HQ, dtype=torch.float32, device=dev)
+        self.y = torch.empty(M_TOK, HIDDEN, dtype=torch.bfloat16, device=dev)
+        ws_bytes = bi.attn_workspace_size(M_TOK, HQ, HEAD_DIM, LK)
+        self.ws = torch.empty(ws_bytes, dtype=torch.uint8, device=dev)
+        self.num_pages = self.k_cache.shape[0]
+        self.stream = torch.cuda.current_stream(dev).cuda_stream
+        self.scale = 1.0 / math.sqrt(HEAD_DIM)
+
+    def calls(self):
+        """The five calls as (name, thunk) through the raw C ABI."""
+        L, s = self.L, self.stream
+        import ctypes
+        f = ctypes.c_float
+        x, h, q, o, y = (t.data_ptr() for t in (self.x, self.h, self.q, self.o, self.y))
+        return [
+            ("rmsnorm", lambda: L.bi_rmsnorm(x, HIDDEN, self.gamma.data_ptr(), h, HIDDEN, 0,
+                                             M_TOK, HIDDEN, f(EPS), s)),
+            ("matmul_nk", lambda: L.bi_matmul(h, HIDDEN, self.w_q.data_ptr(), HIDDEN, 0, q,
+                                              HIDDEN, 0, M_TOK, HIDDEN, HIDDEN, s)),
+            ("kv_append", lambda: L.bi_kv_append(
+                self.k_new.data_ptr(), self.v_new.data_ptr(), self.k_cache.data_ptr(),
+                self.v_cache.data_ptr(), self.num_pages, self.block_table.data_ptr(),
+                self.block_table.shape[1], self.seq_lens.data_ptr(), self.cu_q.data_ptr(), 1,
+                M_TOK, HKV, HEAD_DIM, PAGE, s)),
+            ("verify_block", lambda: L.bi_verify_block(
+                q, self.k_cache.data_ptr(), self.v_cache.data_ptr(), self.num_pages,
+                self.block_table.data_ptr(), self.block_table.shape[1], self.seq_lens.data_ptr(),
+                self.cu_q.data_ptr(), 1, M_TOK, M_TOK, LK, HQ, HKV, HEAD_DIM, PAGE, f(self.scale),
+                o, self.lse.data_ptr(), self.ws.data_ptr(), self.ws.numel(), s)),
+            ("matmul_kn", lambda: L.bi_matmul(o, HIDDEN, self.w_o.data_ptr(), HIDDEN, 1, y,
+                                              HIDDEN, 0, M_TOK, HIDDEN, HIDDEN, s)),
+        ]
+
+    LAUNCHES_PER_STEP = 6  # rmsnorm, gemm, kv_append, attention partial + merge, gemm
+
+
+def run_gpu(args, rank, world, local_rank):
+    import torch
+    import invariant_bi_matmul_gb300 as bi
+
+    dev = torch.device(f"cuda:{local_rank}")
+    torch.cuda.set_device(dev)
+    bi.set_batch_invariant_limit(M_TOK)
+    st = Step(dev)
+    calls = st.calls()
+    names = [n for n, _ in calls]
+
+    def one_step(events=None):
+        for i, (_, fn) in enumerate(calls):
+            if events is not None:
+                events[i].record()
+            rc = fn()
+            if rc != 0:
+                raise RuntimeError(f"{names[i]} returned {bi.lib().bi_status_string(rc).decode()}: "
+                                   f"{bi.lib().bi_last_error_message().decode()}")
+        if events is not None:
+            events[len(calls)].record()
+
+    for _ in range(args.warmup):
+        one_step()
+    torch.cuda.synchronize()
+    if bi.device_status() != bi.BI_OK:
+        raise RuntimeError("device error word set during warm-up")
+
+    # per-call CUDA events over the whole timed region (same stream as the launches)
+    ev = [[torch.cuda.Event(enable_timing=True) for _ in range(len(calls) + 1)]
+          for _ in range(args.steps)]
+    dist = world > 1
+    if dist:
+        torch.distributed.barrier()
+    torch.cuda.synchronize()
+    start = torch.cuda.Event(enable_timing=True)
+    end = torch.cuda.Event(enable_timing=True)
+    with ClockSampler(local_rank) as clocks:
+        start.record()
+        for k in range(args.steps):
+            one_step(ev[k])
+        end.record()
+        torch.cuda.synchronize()
+    if dist:
+        torch.distributed.barrier()
+    elapsed_ms = start.elapsed_time(end)
+    per_call_ms = {n: 0.0 for n in names}
+    for k in range(args.steps):
+        for i, n in enumerate(names):
+            per_call_ms[n] += ev[k][i].elapsed_time(ev[k][i + 1])
+    per_call_ms = {n: v / args.steps for n, v in per_call_ms.items()}
+    status = bi.device_status()
+    if status != bi.BI_OK:
+        raise RuntimeError(f"device error word after the timed region: {status}")
+
+    t_max = elapsed_ms
+    if dist:
+        t = torch.tensor([elapsed_ms], device=dev)
+        torch.distributed.all_reduce(t, op=torch.distributed.ReduceOp.MAX)
+        t_max = float(t.item())
+
+    e2e = run_e2e(st, args, dist)
+    extra = gemm_vs_cublas(st) if rank == 0 else {}
+    return {"elapsed_ms": t_max, "per_call_ms": per_call_ms, "clocks": clocks.summary(),
+            "e2e": e2e, "cublas": extra}
+
+
+def run_e2e(st: Step, args, dist):
+    """Same step through the public Python API with host buffers: pinned H2D of the
+    step's inputs (hidden states, new K/V), the five calls, D2H of the result, every
+    step; timed on the host clock around the synchronised loop."""
+    import torch
+    import invariant_bi_matmul_gb300 as bi
+    dev = st.dev
+    hx = st.x.cpu().pin_memory()
+    hk = st.k_new.cpu().pin_memory()
+    hv = st.v_new.cpu().pin_memory()
+    hy = torch.empty(M_TOK, HIDDEN, dtype=torch.bfloat16).pin_memory()
+    x = torch.empty_like(st.x)
+    kn = torch.empty_like(st.k_new)
+    vn = torch.empty_like(st.v_new)
+
+    def step():
+        x.copy_(hx, non_blocking=True)
+        kn.copy_(hk, non_blocking=True)
+        vn.copy_(hv, non_blocking=True)
+        bi.rmsnorm(x, st.gamma, EPS, out=st.h)
+        bi.matmul(st.h, st.w_q, "nk", out=st.q.view(M_TOK, HIDDEN))
+        bi.kv_append(kn, vn, st.k_cache, st.v_cache, st.block_table, st.seq_lens, st.cu_q)
+        bi.verify_block(st.q, st.k_cache, st.v_cache, st.block_table, st.seq_lens, st.cu_q,
+                        max_q=M_TOK, max_seq_len=LK, scale=st.scale, out=st.o, lse=st.lse,
+                        workspace=st.ws)
+        bi.matmul(st.o.view(M_TOK, HIDDEN), st.w_o, "kn", out=st.y)
+        hy.copy_(st.y, non_blocking=True)
+        torch.cuda.current_stream(dev).synchronize()
+
+    n = max(10, min(args.steps, 2000))
+    for _ in range(3):
+        step()
+    if dist:
+        torch.distributed.barrier()
+    t0 = time.perf_counter()
+    for _ in range(n):
+        step()
+    dt = (time.perf_counter() - t0) / n
+    if dist:
+        t = torch.tensor([dt], device=dev)
+        torch.distributed.all_reduce(t, op=torch.distributed.ReduceOp.MAX)
+        dt = float(t.item())
+    h2d = hx.numel() * 2 + hk.numel() * 2 + hv.numel() * 2
+    d2h = hy.numel() * 2
+    return {"sec_per_step": dt, "h2d": h2d, "d2h": d2h, "steps": n}
+
+
+def gemm_vs_cublas(st: Step):
+    """Invariance cost at the step's shape: bi_matmul vs torch.matmul (cuBLAS, free to
+    pick split-K) at M = 8, K = N = 4096, L2 evicted before every rep, A/B alternated."""
+    import torch
+    import invariant_bi_matmul_gb300 as bi
+    flush = torch.ones(128 * 1024 * 1024, dtype=torch.float32, device=st.dev)
+    out = torch.empty(M_TOK, HIDDEN, dtype=torch.bfloat16, device=st.dev)
+    a_t, b_t = [], []
+    for rep in range(31):
+        for which in (0, 1) if rep % 2 == 0 else (1, 0):
+            flush.sum()  # read-based L2 eviction (leaves no dirty lines)
+            s = torch.cuda.Event(enable_timing=True)
+            e = torch.cuda.Event(enable_timing=True)
+            s.record()
+            if which == 0:
+                bi.matmul(st.h, st.w_q, "nk", out=out)
+            else:
+                torch.matmul(st.h, st.w_q.t(), out=out)
+            e.record()
+            torch.cuda.synchronize()
+            (a_t if which == 0 else b_t).append(s.elapsed_time(e) * 1e3)
+    a, b = statistics.median(a_t[1:]), statistics.median(b_t[1:])
+    return {"bi_matmul_us": round(a, 2), "cublas_us": round(b, 2), "ratio": round(a / b, 3)}
+
+
+# --------------------------------------------------------------------- oracle arm
+
+def oracle_step_sample(frac_cols: int = 8, frac_rows: int = 8):
+    """One bounded sample of the step on the CPU oracle: every RMSNorm row and KV-append
+    token, 1/frac_cols of each matmul's output columns, 1/frac_rows of the attention
+    (token, head) rows.  Returns (estimated full-step seconds, description)."""
+    import numpy as np
+    import torch
+    import oracle
+    from invariant_bi_matmul_gb300 import inputs
+    if not hasattr(oracle_step_sample, "data"):
+        g = inputs.gemm_inputs(M_TOK, HIDDEN, HIDDEN, seed=5)
+        p = inputs.paged_inputs([LK], [M_TOK], Hq=HQ, Hkv=HKV, D=HEAD_DIM, seed=8)
+        b = inputs.bf16_bits
+        oracle_step_sample.data = dict(
+            x=b(g.x), gamma=b(inputs.normal_bf16((HIDDEN,), 1.0, 0.1, seed=6)),
+            w_q=b(g.w_nk), w_o=b(inputs.gemm_inputs(1, HIDDEN, HIDDEN, seed=7).w_kn),
+            q=b(p.q), kn=b(p.k_new), vn=b(p.v_new), kc=b(p.k_cache), vc=b(p.v_cache),
+            bt=p.block_table.numpy(), sl=p.seq_lens.numpy(), cu=p.cu_q.numpy())
+    d = oracle_step_sample.data
+    ncols = HIDDEN // frac_cols
+    t = {}
+    t0 = time.perf_counter()
+    h = oracle.rmsnorm(d["x"], d["gamma"], EPS)
+    t["rmsnorm"] = time.perf_counter() - t0
+    hb = oracle.bf16_round(h)
+    t0 = time.perf_counter()
+    oracle.matmul(hb, np.ascontiguousarray(d["w_q"][:ncols]), oracle.W_NK)
+    t["matmul_nk"] = (time.perf_counter() - t0) * frac_cols
+    t0 = time.perf_counter()
+    kc, vc = oracle.kv_append(d["kn"], d["vn"], d["kc"], d["vc"], d["bt"], d["sl"], d["cu"], PAGE)
+    t["kv_append"] = time.perf_counter() - t0
+    t0 = time.perf_counter()
+    rows = [(j, hh) for j in range(M_TOK) for hh in range(HQ)][::frac_rows]
+    for j, hh in rows:
+        oracle.attention_row(d["q"], kc, vc, d["bt"], d["sl"], d["cu"], 0, j, hh, HQ,
+                             1.0 / math.sqrt(HEAD_DIM))
+    t["verify_block"] = (time.perf_counter() - t0) * frac_rows
+    t0 = time.perf_counter()
+    oracle.matmul(hb, np.ascontiguousarray(d["w_o"][:, :ncols]), oracle.W_KN)
+    t["matmul_kn"] = (time.perf_counter() - t0) * frac_cols
+    desc = (f"all {M_TOK} RMSNorm rows and KV-append tokens, 1/{frac_cols} of each matmul's "
+            f"output columns, 1/{frac_rows} of the {M_TOK * HQ} attention (token, head) rows; "
+            f"times scaled to the full step")
+    return sum(t.values()), desc, t
+
+
+def run_reference(args, rank, world):
+    if rank != 0:
+        return
+    total_bytes = sum(step_bytes().values())
+    for _ in range(args.warmup):
+        oracle_step_sample()
+    secs = []
+    for _ in range(args.steps):
+        s, desc, _ = oracle_step_sample()
+        secs.append(s)
+    sec = statistics.mean(secs)
+    value = total_bytes / sec / 1e9
+    line = {
+        "impl": "reference", "metric": METRIC, "value": value, "unit": "GB/s", "n_gpus": 1,
+        "steps": args.steps, "warmup": args.warmup, "ms_per_step": sec * 1e3,
+        "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f32",
+        "data": "synthetic", "config": workload_config(),
+        "cpu_baseline": {"value": value, "unit": "GB/s", "cores": 1, "kind": "oracle",
+                         "sample": desc},
+        "e2e": {"value": value, "unit": "GB/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
+    }
+    print(json.dumps(line), flush=True)
+
+
+def workload_config():
+    return {
+        "workload": ("verify step, M=8 tokens: rmsnorm [8,4096] -> matmul NK K=N=4096 -> "
+                     "kv_append -> verify attention (1 seq, q=8, Lk=65540, 32 q / 8 kv heads, "
+                     "head_dim 128, 64-token pages) -> matmul KN K=N=4096"),
+        "M": M_TOK, "K": HIDDEN, "N": HIDDEN, "seq_len": LK, "verify_width": M_TOK,
+        "q_heads": HQ, "kv_heads": HKV, "head_dim": HEAD_DIM, "batch_invariant_limit": M_TOK,
+        "l2": "inputs larger than L2: ~336 MB streamed per step vs 126 MB L2, no flush",
+    }
+
+
+# ---------------------------------------------------------------------------- main
+
+def main():
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=20000)
+    ap.add_argument("--warmup", type=int, default=50)
+    ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
+    ap.add_argument("--cpu-sample", action="store_true", default=True)
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--sweep", action="store_true")
+    args = ap.parse_args()
+    if args.warmup < 3:
+        args.warmup = 3
+
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    local_rank = int(os.environ.get("LOCAL_RANK", "0"))
+
+    if args.impl == "reference":
+        if args.steps == 20000:
+            args.steps = 10
+        if args.warmup == 50:
+            args.warmup = 3
+        run_reference(args, rank, world)
+        return
+
+    # The oracle baseline runs before any CUDA work (no fork after CUDA init).
+    cpu = None
+    if rank == 0 and world == 1 and not args.no_cpu_baseline:
+        s, desc, _ = oracle_step_sample()
+        cpu = {"value": sum(step_bytes().values()) / s / 1e9, "unit": "GB/s", "cores": 1,
+               "kind": "oracle", "sample": desc}
+
+    import torch
+    if world > 1:
+        torch.distributed.init_process_group("nccl", device_id=torch.device(f"cuda:{local_rank}"))
+    res = run_gpu(args, rank, world, local_rank)
+    if args.sweep and rank == 0:
+        run_sweep()
+    if world > 1:
+        torch.distributed.destroy_process_group()
+    if rank != 0:
+        return
+
+    peaks, peak_kind = load_peaks()
+    nbytes = step_bytes()
+    flops = step_flops()
+    total = sum(nbytes.values())
+    ms = res["elapsed_ms"] / args.steps
+    value = total * world / (ms * 1e-3) / 1e9
+    calls_ms = res["per_call_ms"]
+    share = {n: round(v / sum(calls_ms.values()), 4) for n, v in calls_ms.items()}
+    parts = {}
+    for n, v in calls_ms.items():
+        parts[n] = {"us": round(v * 1e3, 2), "GB/s": round(nbytes[n] / (v * 1e-3) / 1e9, 1),
+                    "share": share[n]}
+        if n in flops:
+            parts[n]["TFLOP/s"] = round(flops[n] / (v * 1e-3) / 1e12, 2)
+    dom = max(calls_ms, key=calls_ms.get)
+    achieved = nbytes[dom] / (calls_ms[dom] * 1e-3) / 1e9
+    hbm = float(peaks["hbm_gbs"])
+    roof = {"kernel": f"{dom} (split-KV partial + LSE merge)" if dom == "verify_block" else dom,
+            "bound": "hbm", "achieved": round(achieved, 1), "peak": hbm, "unit": "GB/s",
+            "frac": round(achieved / hbm, 4), "peak_source": f"{peak_kind} hbm_gbs",
+            "traffic": recorded_traffic() if dom == "verify_block" else None,
+            "algorithmic_bytes": nbytes[dom]}
+    e2e = res["e2e"]
+    line = {
+        "metric": METRIC, "value": round(value, 1), "unit": "GB/s", "n_gpus": world,
+        "steps": args.steps, "warmup": args.warmup, "ms_per_step": round(ms, 5),
+        "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "bf16",
+        "data": "synthetic (seeded N(0,1) activations/KV, N(0,0.02) weights)",
+        "config": workload_config(),
+        "roofline": roof,
+        "cpu_baseline": cpu,
+        "e2e": {"value": round(total * world / e2e["sec_per_step"] / 1e9, 1), "unit": "GB/s",
+                "h2d_bytes_per_step": e2e["h2d"], "d2h_bytes_per_step": e2e["d2h"],
+                "ms_per_step": round(e2e["sec_per_step"] * 1e3, 4)},
+        "gpu_launches": Step.LAUNCHES_PER_STEP * args.steps,
+        "clocks": res["clocks"],
+        "parts": parts,
+        "gemm_vs_cublas_m8": res["cublas"],
+    }
+    print(json.dumps(line), flush=True)
+
+
+def run_sweep():
+    """Extra JSON lines: GEMM over M (both layouts, vs cuBLAS), RMSNorm at hidden 8192,
+    attention over the pages' Lk and q.  Cold L2 (flushed) before every rep."""
+    import torch
+    import invariant_bi_matmul_gb300 as bi
+    from invariant_bi_matmul_gb300 import inputs
+    peaks, peak_kind = load_peaks()
+    dev = torch.device("cuda:0")
+    # evict L2 by READING a buffer 4x its size (a write-based flush would leave dirty lines
+    # whose write-back then competes with the timed kernel's reads)
+    flush = torch.ones(128 * 1024 * 1024, dtype=torch.float32, device=dev)
+
+    def t_us(fn, reps=21):
+        for _ in range(3):
+            fn()
+        ts = []
+        for _ in range(reps):
+            flush.sum()
+            s = torch.cuda.Event(enable_timing=True)
+            e = torch.cuda.Event(enable_timing=True)
+            s.record()
+            fn()
+            e.record()
+            torch.cuda.synchronize()
+            ts.append(s.elapsed_time(e) * 1e3)
+        return statistics.median(ts)
+
+    K = N = 4096
+    gi = inputs.gemm_inputs(2048, N, K, seed=2)
+    x, wnk, wkn = gi.x.to(dev), gi.w_nk.to(dev), gi.w_kn.to(dev)
+    for M in (1, 2, 4, 8, 16, 64, 256, 2048):
+        xm = x[:M].contiguous()
+        y = torch.empty(M, N, dtype=torch.bfloat16, device=dev)
+        tn = t_us(lambda: bi.matmul(xm, wnk, "nk", out=y))
+        tk = t_us(lambda: bi.matmul(xm, wkn, "kn", out=y))
+        tc = t_us(lambda: torch.matmul(xm, wnk.t(), out=y))
+        fl = 2 * M * N * K
+        by = 2 * N * K + 4 * M * K
+        tf_peak = float(peaks.get("bf16_tflops", 1900.0))
+        print(json.dumps({"sweep": "gemm", "M": M, "K": K, "N": N, "nk_us": round(tn, 2),
+                          "kn_us": round(tk, 2), "cublas_us": round(tc, 2),
+                          "nk_vs_cublas": round(tn / tc, 3), "kn_vs_cublas": round(tk / tc, 3),
+                          "nk_TFLOP/s": round(fl / tn / 1e6, 1), "nk_GB/s": round(by / tn / 1e3, 1),
+                          "nk_frac_hbm": round(by / tn / 1e3 / peaks["hbm_gbs"], 3),
+                          "nk_frac_tensor": round(fl / tn / 1e6 / tf_peak, 3)}), flush=True)
+    for B in (1, 3, 16, 128, 2048):
+        xr, g = inputs.rmsnorm_inputs(B, 8192, seed=3)
+        xr, g = xr.to(dev), g.to(dev)
+        yr = torch.empty_like(xr)
+        t = t_us(lambda: bi.rmsnorm(xr, g, 1e-5, out=yr))
+        by = 4 * B * 8192 + 2 * 8192
+        print(json.dumps({"sweep": "rmsnorm", "B": B, "H": 8192, "us": round(t, 2),
+                          "GB/s": round(by / t / 1e3, 1),
+                          "frac_hbm": round(by / t / 1e3 / peaks["hbm_gbs"], 3)}), flush=True)
+    for B, q, L in ((1, 1, 65540), (1, 8, 65540), (1, 8, 16388), (1, 8, 8196), (1, 8, 1028),
+                    (8, 1, 65540), (64, 1, 16388), (64, 4, 8196)):
+        p = inputs.paged_inputs([L] * B, [q] * B, Hq=HQ, Hkv=HKV, D=HEAD_DIM, seed=4, device=dev)
+        d = {k: getattr(p, k).to(dev) for k in ("q", "k_cache", "v_cache", "block_table",
+                                                 "seq_lens", "cu_q")}
+        ws = torch.empty(bi.attn_workspace_size(B * q, HQ, HEAD_DIM, L), dtype=torch.uint8,
+                         device=dev)
+        out = torch.empty(B * q, HQ, HEAD_DIM, dtype=torch.bfloat16, device=dev)
+        lse = torch.empty(B * q, HQ, dtype=torch.float32, device=dev)
+        t = t_us(lambda: bi.verify_block(d["q"], d["k_cache"], d["v_cache"], d["block_table"],
+                                         d["seq_lens"], d["cu_q"], max_q=q, max_seq_len=L,
+                                         scale=1 / math.sqrt(HEAD_DIM), out=out, lse=lse,
+                                         workspace=ws))
+        by = B * L * HKV * HEAD_DIM * 2 * 2
+        print(json.dumps({"sweep": "attention", "B": B, "q": q, "Lk": L, "us": round(t, 2),
+                          "GB/s": round(by / t / 1e3, 1),
+                          "frac_hbm": round(by / t / 1e3 / peaks["hbm_gbs"], 3)}), flush=True)
+        del p, d, ws
+        torch.cuda.empty_cache()
+
+
+if __name__ == "__main__":
+    main()

@@ -76,6 +76,7 @@ typedef enum {
 #define BI_ATTN_CHUNK 512      /* keys per split-KV chunk (fixed split size)         */
 #define BI_ATTN_MAX_Q 8        /* widest verify block per sequence                   */
 #define BI_ATTN_MAX_ROWS 32    /* max q_len * (num_q_heads / num_kv_heads)            */
+#define BI_ATTN_MAX_BATCH 1024 /* sequences per attention call                        */
 
 int bi_abi_version(void);
 const char* bi_status_string(bi_status s);
@@ -183,12 +184,13 @@ size_t bi_attn_workspace_size(int64_t total_q, int64_t num_q_heads, int64_t head
  *   Split-KV with a FIXED chunk length BI_ATTN_CHUNK counted from key 0: chunk c covers
  *   keys [c*CHUNK, (c+1)*CHUNK); a query uses chunks 0..pos/CHUNK, each reduced with the
  *   same instruction sequence whatever the batch or block width, and the partials are
- *   merged by log-sum-exp in ascending chunk order.
+ *   merged by log-sum-exp over a fixed tree (eight contiguous chunk ranges folded in
+ *   ascending order, then combined in ascending order) that depends on pos alone.
  *
  *   q        bf16 [total_q, num_q_heads, head_dim]; out bf16 same shape; lse fp32
  *            [total_q, num_q_heads] or NULL.  workspace: device memory of at least
  *            bi_attn_workspace_size(total_q, num_q_heads, head_dim, max_seq_len) bytes,
- *            16-byte aligned, contents scratch.
+ *            16-byte aligned, contents scratch.  batch <= BI_ATTN_MAX_BATCH.
  *   max_q    upper bound of every q_b (1..BI_ATTN_MAX_Q), max_q * (num_q_heads /
  *            num_kv_heads) <= BI_ATTN_MAX_ROWS.  max_seq_len: upper bound of every
  *            seq_lens[b] (>= 1).  head_dim in {64, 128}.  num_q_heads % num_kv_heads == 0.

@@ -38,8 +38,7 @@ bi_status fail(bi_status s, const char* fmt, ...) {
 
 bi_status cuda_fail(cudaError_t e, const char* what) {
     if (e == cudaErrorNotSupported)
-        return fail(BI_ERR_UNSUPPORTED, "%s: TMA descriptor could not be encoded for these "
-                                        "pointers/strides", what);
+        return fail(BI_ERR_UNSUPPORTED, "%s: shape or pointer layout not supported", what);
     return fail(BI_ERR_CUDA, "%s: %s (%s)", what, cudaGetErrorName(e), cudaGetErrorString(e));
 }
 
@@ -225,6 +224,8 @@ bi_status check_paged(const char* fn, const PagedArgs& a, int64_t page_size, boo
     if (a.max_q * (a.hq / a.hkv) > BI_ATTN_MAX_ROWS)
         return fail(BI_ERR_UNSUPPORTED, "%s: max_q * (num_q_heads/num_kv_heads) must be <= %d",
                     fn, BI_ATTN_MAX_ROWS);
+    if (a.batch > BI_ATTN_MAX_BATCH)
+        return fail(BI_ERR_UNSUPPORTED, "%s: batch must be <= %d", fn, BI_ATTN_MAX_BATCH);
     if (a.max_seq_len < 1 || a.max_seq_len > a.max_pages * BI_PAGE_SIZE)
         return fail(BI_ERR_INVALID_ARG, "%s: max_seq_len must be in [1, max_pages*page_size]",
                     fn);

@@ -24,10 +24,17 @@ __device__ __forceinline__ uint32_t smem_addr(const void* p) {
     return static_cast<uint32_t>(__cvta_generic_to_shared(p));
 }
 
-__device__ __forceinline__ unsigned long long global_timer_ns() {
-    unsigned long long t;
-    asm volatile("mov.u64 %0, %%globaltimer;" : "=l"(t));
-    return t;
+// One lane of a converged warp: the issuing lane for TMA / tcgen05 instructions.  The
+// rest of the warp runs the same loop (waits, descriptor arithmetic) so it stays
+// converged and its loop state stays warp-uniform.
+__device__ __forceinline__ bool elect_one() {
+    uint32_t pred = 0;
+    asm volatile(
+        "{\n\t.reg .pred P;\n\t"
+        "elect.sync _|P, 0xffffffff;\n\t"
+        "selp.b32 %0, 1, 0, P;\n\t}"
+        : "=r"(pred));
+    return pred != 0;
 }
 
 __device__ __forceinline__ void latch_error(unsigned int* err, unsigned int bits) {
@@ -74,19 +81,36 @@ __device__ __forceinline__ bool mbar_try_wait(uint64_t* bar, uint32_t parity) {
 }
 
 // Waits for the phase with the given parity to complete.  Returns false (and never
-// hangs) when `*abort_flag` becomes non-zero or when `timeout_ns` elapses.
+// hangs) when `*abort_flag` becomes non-zero or when about `timeout_ns` have passed.
+// The fast path is a bare try_wait; the abort flag and the SM cycle counter (a cheap
+// register read, unlike %globaltimer) are consulted only every 64 polls, and the
+// budget is counted in cycles at <= 2.5 GHz, so a slower clock only lengthens it.
 __device__ __forceinline__ bool mbar_wait(uint64_t* bar, uint32_t parity,
                                           const volatile int* abort_flag,
                                           unsigned long long timeout_ns = kWaitTimeoutNs) {
     if (mbar_try_wait(bar, parity)) return true;
-    const unsigned long long t0 = global_timer_ns();
+    const long long budget = static_cast<long long>(timeout_ns) * 5 / 2;  // cycles
+    long long t0 = 0;
     for (uint32_t it = 1;; ++it) {
         if (mbar_try_wait(bar, parity)) return true;
-        if ((it & 15u) == 0u) {
+        if ((it & 63u) == 0u) {
             if (abort_flag && *abort_flag) return false;
-            if (global_timer_ns() - t0 > timeout_ns) return false;
+            const long long now = clock64();
+            if (t0 == 0) {
+                t0 = now;
+            } else if (now - t0 > budget) {
+                return false;
+            }
         }
     }
+}
+
+// The same wait by every lane of a warp, with one warp-wide verdict (so a timeout never
+// splits a warp that then meets elect.sync or a collective).
+__device__ __forceinline__ bool mbar_wait_warp(uint64_t* bar, uint32_t parity,
+                                               const volatile int* abort_flag,
+                                               unsigned long long timeout_ns = kWaitTimeoutNs) {
+    return __all_sync(0xffffffffu, mbar_wait(bar, parity, abort_flag, timeout_ns)) != 0;
 }
 
 // ------------------------------------------------------------------------------ TMA

@@ -35,6 +35,16 @@ cudaError_t launch_gemm(const DeviceInfo& dev, const void* x, int64_t ldx, const
                         int64_t N, int64_t K, cudaStream_t stream);
 int gemm_tile_n();
 
+// How a GEMM launch is scheduled (never what it computes): X rows staged per K-block,
+// 32-wide instruction tiles per CTA tile, shared-memory ring depth, CTA tiles.
+struct GemmSchedule {
+    int a_rows = 128;
+    int nsub = 1;
+    int stages = 0;
+    int64_t tiles = 0;
+};
+GemmSchedule gemm_schedule(int64_t M, int64_t N, int num_sms);
+
 // ------------------------------------------------------------ attention (attention.cu)
 struct PagedArgs {
     const void* k_cache;

@@ -1,0 +1,95 @@
+// tmap.cu -- host-side TMA tensor-map encoding (cuTensorMapEncodeTiled, reached through
+// the runtime's driver entry-point query so no -lcuda is needed) with a small cache keyed
+// by pointer, shape, stride, box and swizzle.
+#include <cuda_runtime.h>
+
+#include <mutex>
+#include <unordered_map>
+
+#include "tmap.h"
+
+namespace bi {
+namespace {
+
+using EncodeTiledFn = CUresult (*)(CUtensorMap*, CUtensorMapDataType, cuuint32_t, void*,
+                                   const cuuint64_t*, const cuuint64_t*, const cuuint32_t*,
+                                   const cuuint32_t*, CUtensorMapInterleave, CUtensorMapSwizzle,
+                                   CUtensorMapL2promotion, CUtensorMapFloatOOBfill);
+
+EncodeTiledFn encode_fn() {
+    static EncodeTiledFn fn = []() -> EncodeTiledFn {
+        void* p = nullptr;
+        cudaDriverEntryPointQueryResult q;
+        if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &p, 12000,
+                                             cudaEnableDefault, &q) != cudaSuccess ||
+            q != cudaDriverEntryPointSuccess)
+            return nullptr;
+        return reinterpret_cast<EncodeTiledFn>(p);
+    }();
+    return fn;
+}
+
+struct MapKey {
+    uintptr_t ptr;
+    uint64_t inner, outer, stride;
+    uint32_t box_inner, box_outer, swizzle;
+    bool operator==(const MapKey& o) const {
+        return ptr == o.ptr && inner == o.inner && outer == o.outer && stride == o.stride &&
+               box_inner == o.box_inner && box_outer == o.box_outer && swizzle == o.swizzle;
+    }
+};
+struct MapKeyHash {
+    size_t operator()(const MapKey& k) const {
+        uint64_t h = k.ptr * 0x9E3779B97F4A7C15ull;
+        h ^= k.inner + 0x9E3779B97F4A7C15ull + (h << 6) + (h >> 2);
+        h ^= k.outer + 0x9E3779B97F4A7C15ull + (h << 6) + (h >> 2);
+        h ^= k.stride + 0x9E3779B97F4A7C15ull + (h << 6) + (h >> 2);
+        h ^= (uint64_t(k.box_inner) << 32 | k.box_outer) + (h << 6) + (h >> 2);
+        return size_t(h ^ k.swizzle);
+    }
+};
+
+std::mutex g_map_mu;
+std::unordered_map<MapKey, CUtensorMap, MapKeyHash> g_maps;
+
+bool tmap_2d_bf16_impl(CUtensorMap* out, const void* ptr, uint64_t inner, uint64_t outer, uint64_t stride,
+                uint32_t box_inner, uint32_t box_outer, int swizzle_bytes) {
+    const MapKey key{reinterpret_cast<uintptr_t>(ptr), inner, outer, stride, box_inner, box_outer,
+                     uint32_t(swizzle_bytes)};
+    {
+        std::lock_guard<std::mutex> lk(g_map_mu);
+        auto it = g_maps.find(key);
+        if (it != g_maps.end()) {
+            *out = it->second;
+            return true;
+        }
+    }
+    EncodeTiledFn fn = encode_fn();
+    if (!fn) return false;
+    CUtensorMap m;
+    const cuuint64_t dims[2] = {inner, outer};
+    const cuuint64_t strides[1] = {stride * 2};
+    const cuuint32_t box[2] = {box_inner, box_outer};
+    const cuuint32_t estr[2] = {1, 1};
+    const CUtensorMapSwizzle sw = swizzle_bytes == 128  ? CU_TENSOR_MAP_SWIZZLE_128B
+                                  : swizzle_bytes == 64 ? CU_TENSOR_MAP_SWIZZLE_64B
+                                                        : CU_TENSOR_MAP_SWIZZLE_32B;
+    if (fn(&m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, const_cast<void*>(ptr), dims, strides, box,
+           estr, CU_TENSOR_MAP_INTERLEAVE_NONE, sw, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+           CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) != CUDA_SUCCESS)
+        return false;
+    std::lock_guard<std::mutex> lk(g_map_mu);
+    if (g_maps.size() > 4096) g_maps.clear();
+    g_maps.emplace(key, m);
+    *out = m;
+    return true;
+}
+
+}  // namespace
+
+bool tmap_2d_bf16(CUtensorMap* out, const void* ptr, uint64_t inner, uint64_t outer,
+                  uint64_t stride, uint32_t box_inner, uint32_t box_outer, int swizzle_bytes) {
+    return tmap_2d_bf16_impl(out, ptr, inner, outer, stride, box_inner, box_outer, swizzle_bytes);
+}
+
+}  // namespace bi

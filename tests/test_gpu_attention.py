@@ -1,0 +1,239 @@
+"""KV append + decode/verify attention on the GPU: parity with the CPU oracle and the
+invariance the pages ask for ("Fix/speculative shape invariance", ml-explore/mlx PR 4279,
+Changes: a query evaluated alone or inside a short causal block gives the same result;
+book chapter "Batch-invariant kernels...", Case 6: token 1000 reduces identically with
+0 or 999 tokens already cached; fixed split size)."""
+import dataclasses
+
+import numpy as np
+import pytest
+import torch
+
+import oracle
+from invariant_bi_matmul_gb300 import inputs
+from tolerance import bits_equal, check_bf16
+
+pytestmark = pytest.mark.gpu
+
+bi = pytest.importorskip("invariant_bi_matmul_gb300")
+
+
+@pytest.fixture(scope="module")
+def dev():
+    if not torch.cuda.is_available():
+        pytest.skip("no CUDA device")
+    return torch.device("cuda:0")
+
+
+def to_dev(p: inputs.PagedInputs, dev):
+    return dataclasses.replace(p, **{f.name: getattr(p, f.name).to(dev)
+                                     for f in dataclasses.fields(p)
+                                     if isinstance(getattr(p, f.name), torch.Tensor)})
+
+
+def run_block(p, dev, max_q=None, max_seq_len=None, append=True, lse=True):
+    """kv_append then verify_block on the GPU; returns (out, lse, device inputs)."""
+    d = to_dev(p, dev)
+    if append:
+        bi.kv_append(d.k_new, d.v_new, d.k_cache, d.v_cache, d.block_table, d.seq_lens, d.cu_q)
+    Hq = p.q.shape[1]
+    D = p.q.shape[2]
+    mq = max_q or int((p.cu_q[1:] - p.cu_q[:-1]).max())
+    msl = max_seq_len or int(p.seq_lens.max())
+    out, l = bi.verify_block(d.q, d.k_cache, d.v_cache, d.block_table, d.seq_lens, d.cu_q,
+                             max_q=mq, max_seq_len=msl, scale=1.0 / np.sqrt(D), want_lse=lse)
+    return out, l, d
+
+
+def oracle_block(p):
+    b = inputs.bf16_bits
+    kc, vc = oracle.kv_append(b(p.k_new), b(p.v_new), b(p.k_cache), b(p.v_cache),
+                              p.block_table.numpy(), p.seq_lens.numpy(), p.cu_q.numpy(),
+                              p.page_size)
+    D = p.q.shape[2]
+    out, lse = oracle.attention(b(p.q), kc, vc, p.block_table.numpy(), p.seq_lens.numpy(),
+                                p.cu_q.numpy(), p.q.shape[1], 1.0 / np.sqrt(D))
+    return out, lse
+
+
+CASES = [
+    # (seq_lens, q_lens, Hq, Hkv, D)
+    ([128], [4], 4, 4, 64),                      # the pages' tiny check
+    ([128, 128, 128, 128], [1, 2, 3, 4], 4, 4, 64),
+    ([1], [1], 32, 8, 128),                      # one key
+    ([64, 65, 511, 512, 513], [1, 1, 2, 4, 8], 32, 8, 128),   # page / chunk boundaries
+    ([1028, 700, 3], [8, 3, 2], 32, 8, 128),     # ragged last chunk
+    ([2000, 1025], [4, 3], 16, 2, 128),          # group size 8: 32 and 24 rows
+]
+
+
+@pytest.mark.parametrize("case", range(len(CASES)))
+def test_attention_parity(dev, case):
+    seq_lens, q_lens, Hq, Hkv, D = CASES[case]
+    if max(q_lens) * (Hq // Hkv) > bi.ATTN_MAX_ROWS:
+        pytest.skip("rows per (sequence, KV head) above the kernel's 32")
+    p = inputs.paged_inputs(seq_lens, q_lens, Hq=Hq, Hkv=Hkv, D=D, seed=100 + case)
+    out, lse, _ = run_block(p, dev)
+    ref, ref_lse = oracle_block(p)
+    check_bf16(out, ref, f"attention case {case}")
+    assert np.allclose(lse.cpu().numpy(), ref_lse, rtol=1e-5, atol=1e-4)
+
+
+def test_kv_append_bit_exact(dev):
+    p = inputs.paged_inputs([70, 513, 9], [3, 8, 1], Hq=32, Hkv=8, D=128, seed=7)
+    d = to_dev(p, dev)
+    bi.kv_append(d.k_new, d.v_new, d.k_cache, d.v_cache, d.block_table, d.seq_lens, d.cu_q)
+    b = inputs.bf16_bits
+    kc, vc = oracle.kv_append(b(p.k_new), b(p.v_new), b(p.k_cache), b(p.v_cache),
+                              p.block_table.numpy(), p.seq_lens.numpy(), p.cu_q.numpy(), 64)
+    assert np.array_equal(b(d.k_cache.cpu()), kc)
+    assert np.array_equal(b(d.v_cache.cpu()), vc)
+
+
+def _alone(p, d, b, j, dev):
+    """Query j of sequence b evaluated by itself: its cache truncated at its position."""
+    q_b = int(p.cu_q[b + 1] - p.cu_q[b])
+    pos = int(p.seq_lens[b]) - q_b + j
+    t = int(p.cu_q[b]) + j
+    q1 = d.q[t:t + 1].contiguous()
+    sl = torch.tensor([pos + 1], dtype=torch.int32, device=dev)
+    cu = torch.tensor([0, 1], dtype=torch.int32, device=dev)
+    bt = d.block_table[b:b + 1].contiguous()
+    out, lse = bi.verify_block(q1, d.k_cache, d.v_cache, bt, sl, cu, max_q=1,
+                               max_seq_len=pos + 1, scale=1.0 / np.sqrt(p.q.shape[2]))
+    dec, dlse = bi.decode_attn(q1, d.k_cache, d.v_cache, bt, sl, max_seq_len=pos + 1,
+                               scale=1.0 / np.sqrt(p.q.shape[2]))
+    assert bits_equal(out, dec) and bits_equal(lse, dlse), "decode != verify with q=1"
+    return out, lse
+
+
+@pytest.mark.parametrize("L", [1028, 8196])
+def test_query_alone_equals_query_in_verify_block(dev, L):
+    """Each query of a causal block of 2..8 gives the bits it gives alone."""
+    for q in (2, 4, 8):
+        p = inputs.paged_inputs([L], [q], Hq=32, Hkv=8, D=128, seed=L + q)
+        out, lse, d = run_block(p, dev)
+        for j in range(q):
+            o1, l1 = _alone(p, d, 0, j, dev)
+            assert bits_equal(o1, out[j:j + 1]), f"L={L} q={q} query {j} differs alone"
+            assert bits_equal(l1, lse[j:j + 1])
+
+
+def test_sequence_alone_equals_sequence_in_mixed_batch(dev):
+    """B = 1 vs mixed batches of up to 64 sequences (lengths drawn from the pages' Lk)."""
+    lens = inputs.mixed_lengths(64, seed=5, choices=(1028, 8196, 16388))
+    qls = [int(x) for x in torch.randint(1, 9, (64,), generator=inputs.generator(6))]
+    p = inputs.paged_inputs(lens, qls, Hq=32, Hkv=8, D=128, seed=8, device=dev)
+    out, lse, d = run_block(p, dev)
+    for b in (0, 17, 63):
+        c0, c1 = int(p.cu_q[b]), int(p.cu_q[b + 1])
+        sl = d.seq_lens[b:b + 1].contiguous()
+        cu = torch.tensor([0, c1 - c0], dtype=torch.int32, device=dev)
+        o1, l1 = bi.verify_block(d.q[c0:c1].contiguous(), d.k_cache, d.v_cache,
+                                 d.block_table[b:b + 1].contiguous(), sl, cu, max_q=8,
+                                 max_seq_len=int(sl[0]), scale=1.0 / np.sqrt(128))
+        assert bits_equal(o1, out[c0:c1]) and bits_equal(l1, lse[c0:c1])
+    # batch permutation permutes the rows exactly
+    perm = torch.randperm(64, generator=inputs.generator(9)).tolist()
+    cu = [0]
+    for b in perm:
+        cu.append(cu[-1] + qls[b])
+    rows = torch.cat([torch.arange(int(p.cu_q[b]), int(p.cu_q[b + 1])) for b in perm]).to(dev)
+    o2, l2 = bi.verify_block(d.q[rows].contiguous(), d.k_cache, d.v_cache,
+                             d.block_table[perm].contiguous(), d.seq_lens[perm].contiguous(),
+                             torch.tensor(cu, dtype=torch.int32, device=dev), max_q=8,
+                             max_seq_len=int(p.seq_lens.max()), scale=1.0 / np.sqrt(128))
+    assert bits_equal(o2, out[rows]) and bits_equal(l2, lse[rows])
+    # sampled parity against the oracle for a few rows of the batch
+    b16 = inputs.bf16_bits
+    kc, vc = b16(d.k_cache.cpu()), b16(d.v_cache.cpu())
+    for b, j, h in ((0, 0, 0), (17, qls[17] - 1, 31), (63, 0, 13)):
+        ref, ref_lse = oracle.attention_row(b16(p.q), kc, vc, p.block_table.numpy(),
+                                            p.seq_lens.numpy(), p.cu_q.numpy(), b, j, h, 32,
+                                            1.0 / np.sqrt(128))
+        t = int(p.cu_q[b]) + j
+        check_bf16(out[t, h], ref, f"mixed batch row b={b} j={j} h={h}")
+        assert abs(float(lse[t, h]) - ref_lse) < 1e-4
+
+
+@pytest.mark.parametrize("L", [1028, 8196, 16388, 65540])
+def test_full_size_sampled_parity(dev, L):
+    p = inputs.paged_inputs([L], [8], Hq=32, Hkv=8, D=128, seed=L)
+    out, lse, d = run_block(p, dev)
+    b16 = inputs.bf16_bits
+    kc, vc = b16(d.k_cache.cpu()), b16(d.v_cache.cpu())
+    for j, h in ((0, 0), (3, 17), (7, 31)):
+        ref, ref_lse = oracle.attention_row(b16(p.q), kc, vc, p.block_table.numpy(),
+                                            p.seq_lens.numpy(), p.cu_q.numpy(), 0, j, h, 32,
+                                            1.0 / np.sqrt(128))
+        check_bf16(out[j, h], ref, f"L={L} j={j} h={h}")
+        assert abs(float(lse[j, h]) - ref_lse) < 1e-4
+
+
+def test_garbage_past_sequence_end_is_ignored(dev):
+    """Unwritten cache slots (NaN/Inf bit patterns) past seq_len never reach the output."""
+    p = inputs.paged_inputs([100], [4], Hq=32, Hkv=8, D=128, seed=21)
+    out, lse, d = run_block(p, dev)
+    last = int(p.block_table[0, 1])
+    d.k_cache[last, :, 100 - 64:] = float("nan")
+    d.v_cache[last, :, 100 - 64:] = float("inf")
+    out2, lse2 = bi.verify_block(d.q, d.k_cache, d.v_cache, d.block_table, d.seq_lens, d.cu_q,
+                                 max_q=4, max_seq_len=100, scale=1.0 / np.sqrt(128))
+    assert torch.isfinite(out2.float()).all()
+    assert bits_equal(out2, out) and bits_equal(lse2, lse)
+
+
+def test_repeat_runs_one_result_and_decode_batch(dev):
+    lens = [1028, 8196, 300, 65540]
+    p = inputs.paged_inputs(lens, [1, 1, 1, 1], Hq=32, Hkv=8, D=128, seed=31)
+    out, lse, d = run_block(p, dev)
+    dec, dlse = bi.decode_attn(d.q, d.k_cache, d.v_cache, d.block_table, d.seq_lens,
+                               max_seq_len=65540, scale=1.0 / np.sqrt(128))
+    assert bits_equal(dec, out) and bits_equal(dlse, lse)
+    seen = set()
+    for _ in range(50):
+        o, _ = bi.verify_block(d.q, d.k_cache, d.v_cache, d.block_table, d.seq_lens, d.cu_q,
+                               max_q=1, max_seq_len=65540, scale=1.0 / np.sqrt(128))
+        seen.add(bytes(o.view(torch.int16).cpu().numpy()))
+    assert len(seen) == 1
+    # and with full verify blocks (both M-tiles, both page parities busy)
+    p8 = inputs.paged_inputs([8196, 700, 16388], [8, 3, 8], Hq=32, Hkv=8, D=128, seed=32)
+    o8, _, d8 = run_block(p8, dev)
+    seen = set()
+    for _ in range(50):
+        o, _ = bi.verify_block(d8.q, d8.k_cache, d8.v_cache, d8.block_table, d8.seq_lens,
+                               d8.cu_q, max_q=8, max_seq_len=16388, scale=1.0 / np.sqrt(128))
+        seen.add(bytes(o.view(torch.int16).cpu().numpy()))
+    assert len(seen) == 1 and bits_equal(o, o8)
+
+
+def test_out_of_range_page_is_reported_not_read(dev):
+    p = inputs.paged_inputs([200], [2], Hq=32, Hkv=8, D=128, seed=41)
+    d = to_dev(p, dev)
+    bt = d.block_table.clone()
+    bt[0, 1] = p.k_cache.shape[0] + 5          # past the pool
+    assert bi.device_status() == bi.BI_OK
+    bi.verify_block(d.q, d.k_cache, d.v_cache, bt, d.seq_lens, d.cu_q, max_q=2,
+                    max_seq_len=200, scale=0.1)
+    assert bi.device_status() == bi.BI_ERR_DEVICE_ARG
+    assert bi.device_status() == bi.BI_OK
+
+
+def test_workspace_and_guard_bands(dev):
+    """The kernels write nothing outside out / lse / the workspace size they ask for."""
+    p = inputs.paged_inputs([1500, 40], [8, 2], Hq=32, Hkv=8, D=128, seed=51)
+    d = to_dev(p, dev)
+    bi.kv_append(d.k_new, d.v_new, d.k_cache, d.v_cache, d.block_table, d.seq_lens, d.cu_q)
+    T = p.T
+    need = bi.attn_workspace_size(T, 32, 128, 1500)
+    ws = torch.full((need + 4096,), 0x5A, dtype=torch.uint8, device=dev)
+    obuf = torch.full((T + 2, 32, 128), 3.0, dtype=torch.bfloat16, device=dev)
+    lbuf = torch.full((T + 2, 32), 3.0, dtype=torch.float32, device=dev)
+    bi.verify_block(d.q, d.k_cache, d.v_cache, d.block_table, d.seq_lens, d.cu_q, max_q=8,
+                    max_seq_len=1500, scale=1.0 / np.sqrt(128), out=obuf[1:T + 1],
+                    lse=lbuf[1:T + 1], workspace=ws[:need])
+    assert torch.all(ws[need:] == 0x5A)
+    assert torch.all(obuf[0] == 3.0) and torch.all(obuf[T + 1] == 3.0)
+    assert torch.all(lbuf[0] == 3.0) and torch.all(lbuf[T + 1] == 3.0)
+    ref, _ = oracle_block(p)
+    check_bf16(obuf[1:T + 1], ref, "guarded out")

@@ -83,7 +83,9 @@ def test_matmul_rows_invariant_across_M(dev, layout):
     w = (gi.w_nk if layout == "nk" else gi.w_kn).to(dev)
     x = gi.x.to(dev)
     full = bi.matmul(x, w, layout)
-    for M in (1, 2, 4, 8, 16, 64, 256):
+    # every M crosses a different staging / CTA-tiling choice of the scheduler:
+    # staged X rows 8..128, one to eight 32-wide instruction tiles per CTA
+    for M in (1, 2, 3, 4, 8, 9, 16, 17, 64, 100, 127, 128, 129, 256, 600, 1000, 1500):
         part = bi.matmul(x[:M].contiguous(), w, layout)
         assert bits_equal(part, full[:M]), f"rows differ at M={M}"
     # a row evaluated alone from the middle of the batch (not only the first rows)
@@ -102,6 +104,24 @@ def test_matmul_full_size_sampled_parity(dev, layout):
     for i in (0, 127, 128, 1024, 2047):
         ref = oracle.matmul(inputs.bf16_bits(gi.x[i:i + 1]), wb, oracle.W_NK)
         check_bf16(y[i:i + 1], ref, f"row {i}")
+
+
+@pytest.mark.parametrize("layout", ["nk", "kn"])
+def test_matmul_parity_wide_cta_tiles_ragged_n(dev, layout):
+    """Large M (several instruction tiles per CTA) with N not a multiple of the CTA tile."""
+    M, N, K = 1500, 1000, 256
+    gi = inputs.gemm_inputs(M, N, K, seed=81)
+    w = gi.w_nk if layout == "nk" else gi.w_kn
+    y = bi.matmul(gi.x.to(dev), w.to(dev), layout).cpu()
+    rows = [0, 1, 127, 128, 700, 1499]
+    ref = oracle.matmul(inputs.bf16_bits(gi.x[rows]), inputs.bf16_bits(gi.w_nk), oracle.W_NK)
+    check_bf16(y[rows], ref, f"wide tiles {layout}")
+    yf = bi.matmul(gi.x.to(dev), w.to(dev), layout, out_dtype=torch.float32).cpu()
+    check_f32(yf[rows], ref, _abs_scale(gi.x[rows], gi.w_nk), f"wide tiles f32 {layout}")
+    # and every row of this launch equals the row computed alone
+    for i in (3, 1499):
+        alone = bi.matmul(gi.x[i:i + 1].to(dev), w.to(dev), layout).cpu()
+        assert bits_equal(alone, y[i:i + 1])
 
 
 def test_matmul_permutation_and_repeat(dev):
