@@ -114,10 +114,11 @@ int bi_within_batch_invariant_limit(int64_t dim);
  *                 layout BI_W_KN: [K, N] with row stride ldw (ldw >= N).
  *   y       [M, N] row-major, row stride ldy (ldy >= N), dtype y_dtype.
  *   M, N, K >= 0; M = 0 or N = 0 is a no-op; K = 0 writes zeros.
- *   Invariant construction: one tcgen05 tile shape (128 x BN x 16 instructions, BK = 64
- *   K-blocks taken in ascending order, fp32 accumulation in tensor memory) for every M.
- *   Row m is always computed in M-tile m/128 at lane m%128; rows beyond M are zero-filled
- *   by TMA and never stored.
+ *   Invariant construction: one tcgen05 instruction shape (128 x 64 x 16, kind::f16, fp32
+ *   accumulation in tensor memory) and one K order (64-wide K-blocks ascending, four
+ *   16-wide steps ascending inside each) for every M.  Row m is always lane m%128 of
+ *   M-tile m/128; rows beyond M are never stored.  Only scheduling follows M (how many X
+ *   rows are staged, how many instruction tiles one CTA covers).
  *   Alignment (TMA rule): x, w 16-byte aligned; ldx, ldw multiples of 8 elements;
  *   otherwise BI_ERR_UNSUPPORTED.  y needs only element alignment.
  *   Limits: M, N, K < 2^31.

@@ -9,9 +9,9 @@
 // reduction) and the review thread (both B orientations must be covered).
 //
 // What decides the bits of Y[m, n] -- identical for every M:
-//   * the instruction tcgen05.mma.cta_group::1.kind::f16 of shape 128 x 32 x 16 (bf16 in,
+//   * the instruction tcgen05.mma.cta_group::1.kind::f16 of shape 128 x 64 x 16 (bf16 in,
 //     fp32 accumulator in tensor memory), always with token row m at lane m % 128 of
-//     M-tile m / 128 and column n in the 32-wide instruction tile n / 32;
+//     M-tile m / 128 and column n in the 64-wide instruction tile n / 64;
 //   * the K order: 64-wide K-blocks in ascending order, and inside a block the four
 //     16-wide steps in ascending order, the first one overwriting the accumulator;
 //   * the epilogue: fp32 -> bf16 round-to-nearest-even (or fp32 as is).
@@ -20,21 +20,27 @@
 //     The MMA always reads 128 rows; rows past a_rows read whatever lies in shared
 //     memory after the staged rows and land in tensor-memory lanes that are never
 //     stored, so no real row depends on them;
-//   * nsub: how many adjacent 32-wide instruction tiles one CTA covers with the X block
-//     it staged (1 for small M to spread W over every SM, up to 8 for large M to stop
-//     re-reading X from L2);
-//   * stages: the depth of the shared-memory ring, from what one stage occupies.
+//   * nsub: how many adjacent instruction tiles one CTA covers with the X block it staged
+//     (1 for small M to spread W over every SM, up to 4 for large M to stop re-reading X
+//     from L2);
+//   * kbs and stages: how many K-blocks one ring stage carries and how deep the ring is.
+// (A 128 x N x 16 instruction costs about the same ~60 cycles for N up to 128, so N
+// trades small-M parallelism (N/64 CTAs at M <= 128) against large-M tensor throughput;
+// 64 is the fixed compromise.)
 //
 // Warp roles (192 threads, persistent, one CTA per SM): warp 0 = TMA producer, warp 1 =
 // TMEM allocator + MMA issuer, warps 2..5 = epilogue (tcgen05.ld -> convert -> global).
 // Producer and MMA warps run their loops with all 32 lanes converged and let one
 // elected lane issue each TMA / tcgen05 instruction.  Full/empty mbarriers guard the
 // ring; two TMEM accumulators let the epilogue of tile i overlap the main loop of tile
-// i+1.  W layout NK ([N,K]) feeds the MMA
-// as a K-major operand with 128-byte swizzle, layout KN ([K,N]) as an N-major operand
-// with 64-byte swizzle.  Every mbarrier wait is bounded: a wait that runs out latches
-// the device error word, raises a CTA-wide abort flag, drains outstanding copies and
-// MMAs (bounded), frees tensor memory and returns.
+// i+1.  Descriptors and shared addresses are computed once and advanced by adds in the
+// issue loops (per-instruction descriptor arithmetic was measured to double the cost of
+// each MMA).  W layout NK ([N,K]) feeds the MMA as a K-major operand with 128-byte
+// swizzle, layout KN ([K,N]) as an N-major operand with 128-byte swizzle.  When K is a
+// multiple of 64 one rank-3 TMA copy per operand brings all the K-blocks of a stage.
+// Every mbarrier wait is bounded: a wait that runs out latches the device error word,
+// raises a CTA-wide abort flag, drains outstanding copies and MMAs (bounded), frees
+// tensor memory and returns.
 #include "common.cuh"
 #include "launch.h"
 #include "tmap.h"
@@ -42,20 +48,32 @@
 namespace bi {
 namespace {
 
+#ifndef BI_GEMM_BN
+#define BI_GEMM_BN 64
+#endif
+
 constexpr int BM = 128;                     // instruction M: token rows
-constexpr int BN = 32;                      // instruction N: output columns
+constexpr int BN = BI_GEMM_BN;              // instruction N: output columns
 constexpr int BK = 64;                      // K-block: one 128-byte swizzle row of bf16
 constexpr int UK = 16;                      // K of one kind::f16 instruction
-constexpr int MAX_NSUB = 8;
+constexpr int MAX_NSUB = 256 / BN;          // two accumulators of nsub*BN columns in 512
+constexpr int MAX_KBS = 8;                  // K-blocks per ring stage (K-major operands)
+constexpr int MAX_KBS_KN = 4;               // N-major W: one box spans 64*kbs <= 256 k-rows
 constexpr int MAX_STAGES = 48;
 constexpr int THREADS = 192;
 constexpr int EPI_THREADS = 128;
-constexpr int B_SUB_BYTES = BN * BK * 2;    // 4 KiB: one instruction tile's W block
-constexpr int A_MMA_BYTES = BM * BK * 2;    // 16 KiB: what one MMA reads from the X block
+constexpr int B_KB_BYTES = BN * BK * 2;     // one instruction tile's W block per K-block
+constexpr int A_MMA_BYTES = BM * BK * 2;    // 16 KiB: what one MMA reads from an X block
 constexpr int SMEM_BYTES = 220 * 1024;      // dynamic shared memory per CTA
 constexpr int CTRL_BYTES = 1024;            // barriers and flags at the end
 constexpr int RING_BYTES = SMEM_BYTES - 1024 /* alignment slack */ - CTRL_BYTES;
+// N-major W (layout KN): one swizzle atom spans min(BN, 64) columns
+constexpr int KN_ATOM_N = BN < 64 ? BN : 64;
+constexpr int KN_ATOM_BYTES = KN_ATOM_N * 2 * BK;  // one atom column of a K-block
+constexpr int KN_SWIZZLE = KN_ATOM_N * 2;          // 64 or 128 bytes
+constexpr uint32_t KN_LAYOUT = KN_SWIZZLE == 128 ? 2u : 4u;
 
+static_assert(BN == 32 || BN == 64 || BN == 128, "instruction N must be 32, 64 or 128");
 static_assert((2 * MAX_STAGES + 5) * 8 + 16 <= CTRL_BYTES, "control block too small");
 
 struct GemmArgs {
@@ -64,11 +82,13 @@ struct GemmArgs {
     int M, N, K;
     int a_rows;          // X rows staged per K-block (multiple of 8, <= 128)
     int nsub;            // instruction tiles per CTA tile along N
+    int kbs;             // K-blocks per ring stage
+    int blocked;         // K % 64 == 0: one rank-3 copy per operand per stage
     int stages;          // ring depth
     int w_stream_once;   // one M-tile: W is read exactly once (L2 evict-first hint)
 };
 
-template <bool KN, bool F32OUT>
+template <bool KN, bool F32OUT, int NSUB>
 __global__ void __launch_bounds__(THREADS, 1)
 gemm_kernel(const __grid_constant__ CUtensorMap tmap_x, const __grid_constant__ CUtensorMap tmap_w,
             const GemmArgs args, unsigned int* err) {
@@ -76,12 +96,12 @@ gemm_kernel(const __grid_constant__ CUtensorMap tmap_x, const __grid_constant__ 
     uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) &
                                                ~uintptr_t(1023));
     const int S = args.stages;
-    const int nsub = args.nsub;
-    const int a_bytes = args.a_rows * (BK * 2);
-    const int b_bytes = nsub * B_SUB_BYTES;
-    const uint32_t stage_tx = uint32_t(a_bytes + b_bytes);
-    uint8_t* sA = smem;                         // S x a_bytes
-    uint8_t* sB = smem + S * a_bytes;           // S x b_bytes
+    constexpr int nsub = NSUB;
+    const int kbs = args.kbs;
+    const int a_bytes = args.a_rows * (BK * 2);   // one X block (one K-block)
+    const int b_bytes = nsub * B_KB_BYTES;        // one W block (one K-block, every sub-tile)
+    uint8_t* sA = smem;                           // S*kbs X blocks
+    uint8_t* sB = smem + S * kbs * a_bytes;       // S*kbs W blocks
     uint64_t* full = reinterpret_cast<uint64_t*>(smem + RING_BYTES);
     uint64_t* empty = full + MAX_STAGES;
     uint64_t* tfull = empty + MAX_STAGES;
@@ -137,34 +157,57 @@ gemm_kernel(const __grid_constant__ CUtensorMap tmap_x, const __grid_constant__ 
         uint32_t stage = 0, phase = 0, issued = 0;
         const uint64_t w_policy = l2_policy_evict_first();
         bool ok = true;
+        const uint32_t sA_s = smem_addr(sA), sB_s = smem_addr(sB), full_s = smem_addr(full);
+        const uint32_t stage_a = uint32_t(kbs * a_bytes), stage_b = uint32_t(kbs * b_bytes);
+        const uint32_t blk_tx = uint32_t(a_bytes + b_bytes);
+        const bool w_once = args.w_stream_once != 0;
+        const bool blocked = args.blocked != 0;
         for (int t = blockIdx.x; ok && t < num_tiles; t += gridDim.x) {
             const int mt = t / n_tiles, nt = t % n_tiles;
-            for (int kb = 0; kb < nkb; ++kb) {
+            const int m0 = mt * BM, n0 = nt * tile_n;
+            for (int kb = 0; kb < nkb; kb += kbs) {
                 if (!mbar_wait_warp(&empty[stage], phase ^ 1u, abort_flag)) {
                     ok = false;
                     break;
                 }
                 if (elect_one()) {
-                    uint64_t* bar = &full[stage];
-                    mbar_arrive_expect_tx(bar, stage_tx);
-                    tma_load_2d(sA + stage * a_bytes, &tmap_x, bar, kb * BK, mt * BM);
-                    uint8_t* bdst = sB + stage * b_bytes;
-                    if (KN) {
-                        // one N-major box of 32 columns x 64 k-rows per instruction tile
-                        for (int j = 0; j < nsub; ++j) {
-                            const int c0 = nt * tile_n + j * BN;
-                            if (args.w_stream_once)
-                                tma_load_2d_hint(bdst + j * B_SUB_BYTES, &tmap_w, bar, c0, kb * BK,
-                                                 w_policy);
-                            else
-                                tma_load_2d(bdst + j * B_SUB_BYTES, &tmap_w, bar, c0, kb * BK);
-                        }
+                    const uint32_t bar = full_s + stage * 8u;
+                    const int nk = nkb - kb < kbs ? nkb - kb : kbs;  // K-blocks in this stage
+                    // a rank-3 copy always delivers all kbs blocks (zeros past K), a rank-2
+                    // copy one block; N-major W boxes always span kbs blocks
+                    const int x_blocks = blocked ? kbs : nk;
+                    const int w_blocks = (blocked || KN) ? kbs : nk;
+                    mbar_arrive_expect_tx_s(bar, uint32_t(x_blocks * a_bytes + w_blocks * b_bytes));
+                    const uint32_t a_dst = sA_s + stage * stage_a;
+                    const uint32_t b_dst = sB_s + stage * stage_b;
+                    if (blocked) {
+                        tma_load_3d_s(a_dst, &tmap_x, bar, 0, m0, kb);
                     } else {
-                        // one K-major box of 64 k x (nsub*32) rows covers every instruction tile
-                        if (args.w_stream_once)
-                            tma_load_2d_hint(bdst, &tmap_w, bar, kb * BK, nt * tile_n, w_policy);
+                        for (int i = 0; i < nk; ++i)
+                            tma_load_2d_s(a_dst + uint32_t(i * a_bytes), &tmap_x, bar, (kb + i) * BK, m0);
+                    }
+                    if (KN) {
+                        // per swizzle atom (KN_ATOM_N columns) one box of 64*kbs k-rows
+                        for (int c = 0; c < tile_n; c += KN_ATOM_N) {
+                            const uint32_t dst = b_dst + uint32_t(c / KN_ATOM_N) * uint32_t(kbs * KN_ATOM_BYTES);
+                            if (w_once)
+                                tma_load_2d_s_hint(dst, &tmap_w, bar, n0 + c, kb * BK, w_policy);
+                            else
+                                tma_load_2d_s(dst, &tmap_w, bar, n0 + c, kb * BK);
+                        }
+                    } else if (blocked) {
+                        if (w_once)
+                            tma_load_3d_s_hint(b_dst, &tmap_w, bar, 0, n0, kb, w_policy);
                         else
-                            tma_load_2d(bdst, &tmap_w, bar, kb * BK, nt * tile_n);
+                            tma_load_3d_s(b_dst, &tmap_w, bar, 0, n0, kb);
+                    } else {
+                        for (int i = 0; i < nk; ++i) {
+                            const uint32_t dst = b_dst + uint32_t(i * b_bytes);
+                            if (w_once)
+                                tma_load_2d_s_hint(dst, &tmap_w, bar, (kb + i) * BK, n0, w_policy);
+                            else
+                                tma_load_2d_s(dst, &tmap_w, bar, (kb + i) * BK, n0);
+                        }
                     }
                 }
                 __syncwarp();
@@ -188,6 +231,24 @@ gemm_kernel(const __grid_constant__ CUtensorMap tmap_x, const __grid_constant__ 
         // ---------------------------------------------------------------- MMA issuer
         // The whole warp runs the loop; one elected lane issues the MMAs and commits.
         constexpr uint32_t idesc = umma_idesc_bf16(BM, BN, 0, KN ? 1 : 0);
+        // X: K-major, 128-byte swizzle, 8-row groups 1024 B apart; +32 B per k16 step
+        const uint64_t a_desc0 = umma_smem_desc(smem_addr(sA), 16, 1024, 2);
+        // W, layout NK: K-major like X.  Layout KN: N-major; k-rows of KN_SWIZZLE bytes,
+        // 8 k-rows per swizzle-atom group, atoms of KN_ATOM_N columns KN_ATOM_BYTES apart;
+        // a k16 step skips 16 k-rows
+        // (KN: a stage holds, per atom of KN_ATOM_N columns, kbs K-blocks of 64 k-rows, so
+        // atoms sit kbs*KN_ATOM_BYTES apart and K-blocks KN_ATOM_BYTES apart)
+        const uint64_t b_desc0 = KN ? umma_smem_desc(smem_addr(sB), uint32_t(kbs * KN_ATOM_BYTES),
+                                                     8 * KN_SWIZZLE, KN_LAYOUT)
+                                    : umma_smem_desc(smem_addr(sB), 16, 1024, 2);
+        constexpr int A_K16 = (UK * 2) >> 4;
+        constexpr int B_K16 = KN ? (UK * KN_SWIZZLE) >> 4 : (UK * 2) >> 4;
+        const uint64_t a_step = uint64_t(a_bytes >> 4);
+        const uint64_t b_step = uint64_t((KN ? KN_ATOM_BYTES : b_bytes) >> 4);
+        const uint64_t b_sub = uint64_t(KN ? ((BN / KN_ATOM_N) * kbs * KN_ATOM_BYTES) >> 4
+                                           : B_KB_BYTES >> 4);
+        const uint32_t stage_a = uint32_t(kbs * a_bytes), stage_b = uint32_t(kbs * b_bytes);
+        const uint32_t empty_s = smem_addr(empty);
         uint32_t stage = 0, phase = 0;
         bool ok = true;
         int local = 0;
@@ -200,35 +261,31 @@ gemm_kernel(const __grid_constant__ CUtensorMap tmap_x, const __grid_constant__ 
             }
             tc_fence_after_sync();
             const uint32_t d_tmem = tmem_base + uint32_t(acc * tile_n);
-            for (int kb = 0; kb < nkb; ++kb) {
+            for (int kb = 0; kb < nkb; kb += kbs) {
                 if (!mbar_wait_warp(&full[stage], phase, abort_flag)) {
                     ok = false;
                     break;
                 }
                 tc_fence_after_sync();
-                const uint32_t a_addr = smem_addr(sA + stage * a_bytes);
-                const uint32_t b_addr = smem_addr(sB + stage * b_bytes);
+                const int nk = nkb - kb < kbs ? nkb - kb : kbs;
                 if (elect_one()) {
+                    // descriptors are advanced by adding (byte offset >> 4) to the start-
+                    // address field; shared addresses stay below 2^18 so it never carries
+                    uint64_t a_blk = a_desc0 + (uint64_t(stage * stage_a) >> 4);
+                    uint64_t b_blk = b_desc0 + (uint64_t(stage * stage_b) >> 4);
+                    for (int i = 0; i < nk; ++i, a_blk += a_step, b_blk += b_step) {
+                        const uint32_t first = (kb + i) == 0 ? 1u : 0u;
 #pragma unroll
-                    for (int k = 0; k < BK / UK; ++k) {
-                        // X: K-major, 128-byte swizzle, 8-row groups 1024 B apart, +32 B per k16
-                        const uint64_t a_desc = umma_smem_desc(a_addr + k * UK * 2, 16, 1024, 2);
-                        for (int j = 0; j < nsub; ++j) {
-                            uint64_t b_desc;
-                            if (KN) {
-                                // W: N-major, 64-byte swizzle; k-rows of 64 B, 8 k-rows per
-                                // 512-byte atom; a k16 step skips 16 k-rows (1024 B)
-                                b_desc = umma_smem_desc(b_addr + j * B_SUB_BYTES + k * UK * 64,
-                                                        BK * 64, 512, 4);
-                            } else {
-                                b_desc = umma_smem_desc(b_addr + j * B_SUB_BYTES + k * UK * 2, 16,
-                                                        1024, 2);
-                            }
-                            tc_mma_bf16(d_tmem + uint32_t(j * BN), a_desc, b_desc, idesc,
-                                        (kb | k) != 0 ? 1u : 0u);
+                        for (int k = 0; k < BK / UK; ++k) {
+                            const uint64_t a_desc = a_blk + uint64_t(k * A_K16);
+                            uint64_t b_desc = b_blk + uint64_t(k * B_K16);
+                            uint32_t d = d_tmem;
+#pragma unroll
+                            for (int j = 0; j < NSUB; ++j, b_desc += b_sub, d += uint32_t(BN))
+                                tc_mma_bf16(d, a_desc, b_desc, idesc, (first && k == 0) ? 0u : 1u);
                         }
                     }
-                    tc_commit(&empty[stage]);  // frees the stage once these MMAs finish
+                    tc_commit_s(empty_s + stage * 8u);  // frees the stage once these MMAs finish
                 }
                 __syncwarp();
                 if (++stage == uint32_t(S)) {
@@ -316,10 +373,10 @@ gemm_kernel(const __grid_constant__ CUtensorMap tmap_x, const __grid_constant__ 
     }
 }
 
-template <bool KN, bool F32OUT>
+template <bool KN, bool F32OUT, int NSUB>
 cudaError_t launch_t(const DeviceInfo& dev, const CUtensorMap& mx, const CUtensorMap& mw,
                      const GemmArgs& a, int grid, cudaStream_t s) {
-    auto kern = gemm_kernel<KN, F32OUT>;
+    auto kern = gemm_kernel<KN, F32OUT, NSUB>;
     static bool attr_done[64] = {};
     if (dev.device >= 0 && dev.device < 64 && !attr_done[dev.device]) {
         cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize,
@@ -331,11 +388,22 @@ cudaError_t launch_t(const DeviceInfo& dev, const CUtensorMap& mx, const CUtenso
     return cudaGetLastError();
 }
 
+template <bool KN, bool F32OUT>
+cudaError_t launch_nsub(const DeviceInfo& dev, const CUtensorMap& mx, const CUtensorMap& mw,
+                        const GemmArgs& a, int grid, cudaStream_t s) {
+    switch (a.nsub) {
+        case 1: return launch_t<KN, F32OUT, 1>(dev, mx, mw, a, grid, s);
+        case 2: return launch_t<KN, F32OUT, (MAX_NSUB >= 2 ? 2 : 1)>(dev, mx, mw, a, grid, s);
+        case 4: return launch_t<KN, F32OUT, (MAX_NSUB >= 4 ? 4 : 1)>(dev, mx, mw, a, grid, s);
+        default: return launch_t<KN, F32OUT, MAX_NSUB>(dev, mx, mw, a, grid, s);
+    }
+}
+
 }  // namespace
 
 int gemm_tile_n() { return BN; }
 
-GemmSchedule gemm_schedule(int64_t M, int64_t N, int num_sms) {
+GemmSchedule gemm_schedule(int64_t M, int64_t N, int64_t K, bool w_kn, int num_sms) {
     GemmSchedule g;
     const int64_t m_tiles = (M + BM - 1) / BM;
     g.a_rows = m_tiles == 1 ? int((M + 7) / 8 * 8) : BM;
@@ -348,10 +416,20 @@ GemmSchedule gemm_schedule(int64_t M, int64_t N, int num_sms) {
             break;
         }
     }
-    const int stage_bytes = g.a_rows * BK * 2 + g.nsub * B_SUB_BYTES;
-    g.stages = RING_BYTES / stage_bytes;
+    // as many K-blocks per stage as keep at least four stages in the ring (fewer
+    // barrier round trips per MMA)
+    const int blk_bytes = g.a_rows * BK * 2 + g.nsub * B_KB_BYTES;
+    g.kbs = 1;
+    for (int kbs = w_kn ? MAX_KBS_KN : MAX_KBS; kbs >= 2; kbs >>= 1) {
+        if (RING_BYTES / (kbs * blk_bytes) >= 4) {
+            g.kbs = kbs;
+            break;
+        }
+    }
+    g.stages = RING_BYTES / (g.kbs * blk_bytes);
     if (g.stages > MAX_STAGES) g.stages = MAX_STAGES;
     g.tiles = m_tiles * ((N + int64_t(g.nsub) * BN - 1) / (int64_t(g.nsub) * BN));
+    g.blocked = (K % BK) == 0 ? 1 : 0;
     return g;
 }
 
@@ -364,18 +442,28 @@ cudaError_t launch_gemm(const DeviceInfo& dev, const void* x, int64_t ldx, const
         const size_t es = y_f32 ? 4 : 2;
         return cudaMemset2DAsync(y, size_t(ldy) * es, 0, size_t(N) * es, size_t(M), stream);
     }
-    const GemmSchedule g = gemm_schedule(M, N, dev.num_sms);
-    // the MMA of the last stage reads A_MMA_BYTES from its X block: keep that in the ring
-    const int a_bytes = g.a_rows * BK * 2;
-    if ((g.stages - 1) * a_bytes + A_MMA_BYTES > g.stages * (a_bytes + g.nsub * B_SUB_BYTES) ||
-        g.stages < 2)
+    const GemmSchedule g = gemm_schedule(M, N, K, w_kn, dev.num_sms);
+    // an MMA reads A_MMA_BYTES from the start of its X block: the last X block's read must
+    // stay inside the ring (it runs into the W blocks that follow the X blocks)
+    const int64_t a_bytes = int64_t(g.a_rows) * BK * 2;
+    const int64_t blocks = int64_t(g.stages) * g.kbs;
+    if ((blocks - 1) * a_bytes + A_MMA_BYTES > blocks * (a_bytes + int64_t(g.nsub) * B_KB_BYTES) ||
+        blocks * (a_bytes + int64_t(g.nsub) * B_KB_BYTES) > RING_BYTES || g.stages < 2)
         return cudaErrorNotSupported;
     CUtensorMap mx, mw;
-    if (!tmap_2d_bf16(&mx, x, uint64_t(K), uint64_t(M), uint64_t(ldx), BK, uint32_t(g.a_rows), 128))
-        return cudaErrorNotSupported;
     bool ok;
+    if (g.blocked)
+        ok = tmap_kblocked_bf16(&mx, x, uint64_t(K), uint64_t(M), uint64_t(ldx), BK,
+                                uint32_t(g.a_rows), uint32_t(g.kbs), 128);
+    else
+        ok = tmap_2d_bf16(&mx, x, uint64_t(K), uint64_t(M), uint64_t(ldx), BK, uint32_t(g.a_rows), 128);
+    if (!ok) return cudaErrorNotSupported;
     if (w_kn)
-        ok = tmap_2d_bf16(&mw, w, uint64_t(N), uint64_t(K), uint64_t(ldw), BN, BK, 64);
+        ok = tmap_2d_bf16(&mw, w, uint64_t(N), uint64_t(K), uint64_t(ldw), KN_ATOM_N,
+                          uint32_t(BK * g.kbs), KN_SWIZZLE);
+    else if (g.blocked)
+        ok = tmap_kblocked_bf16(&mw, w, uint64_t(K), uint64_t(N), uint64_t(ldw), BK,
+                                uint32_t(g.nsub * BN), uint32_t(g.kbs), 128);
     else
         ok = tmap_2d_bf16(&mw, w, uint64_t(K), uint64_t(N), uint64_t(ldw), BK,
                           uint32_t(g.nsub * BN), 128);
@@ -388,14 +476,16 @@ cudaError_t launch_gemm(const DeviceInfo& dev, const void* x, int64_t ldx, const
     a.K = int(K);
     a.a_rows = g.a_rows;
     a.nsub = g.nsub;
+    a.kbs = g.kbs;
+    a.blocked = g.blocked;
     a.stages = g.stages;
     a.w_stream_once = (M + BM - 1) / BM == 1 ? 1 : 0;
     const int grid = int(g.tiles < dev.num_sms ? g.tiles : dev.num_sms);
     if (w_kn)
-        return y_f32 ? launch_t<true, true>(dev, mx, mw, a, grid, stream)
-                     : launch_t<true, false>(dev, mx, mw, a, grid, stream);
-    return y_f32 ? launch_t<false, true>(dev, mx, mw, a, grid, stream)
-                 : launch_t<false, false>(dev, mx, mw, a, grid, stream);
+        return y_f32 ? launch_nsub<true, true>(dev, mx, mw, a, grid, stream)
+                     : launch_nsub<true, false>(dev, mx, mw, a, grid, stream);
+    return y_f32 ? launch_nsub<false, true>(dev, mx, mw, a, grid, stream)
+                 : launch_nsub<false, false>(dev, mx, mw, a, grid, stream);
 }
 
 }  // namespace bi

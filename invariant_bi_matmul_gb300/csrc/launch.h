@@ -40,10 +40,12 @@ int gemm_tile_n();
 struct GemmSchedule {
     int a_rows = 128;
     int nsub = 1;
+    int kbs = 1;
+    int blocked = 0;
     int stages = 0;
     int64_t tiles = 0;
 };
-GemmSchedule gemm_schedule(int64_t M, int64_t N, int num_sms);
+GemmSchedule gemm_schedule(int64_t M, int64_t N, int64_t K, bool w_kn, int num_sms);
 
 // ------------------------------------------------------------ attention (attention.cu)
 struct PagedArgs {

@@ -33,9 +33,11 @@ struct MapKey {
     uintptr_t ptr;
     uint64_t inner, outer, stride;
     uint32_t box_inner, box_outer, swizzle;
+    uint32_t box_blocks;  // 0: rank-2 map; >0: rank-3 K-blocked map with this many blocks
     bool operator==(const MapKey& o) const {
         return ptr == o.ptr && inner == o.inner && outer == o.outer && stride == o.stride &&
-               box_inner == o.box_inner && box_outer == o.box_outer && swizzle == o.swizzle;
+               box_inner == o.box_inner && box_outer == o.box_outer && swizzle == o.swizzle &&
+               box_blocks == o.box_blocks;
     }
 };
 struct MapKeyHash {
@@ -45,17 +47,17 @@ struct MapKeyHash {
         h ^= k.outer + 0x9E3779B97F4A7C15ull + (h << 6) + (h >> 2);
         h ^= k.stride + 0x9E3779B97F4A7C15ull + (h << 6) + (h >> 2);
         h ^= (uint64_t(k.box_inner) << 32 | k.box_outer) + (h << 6) + (h >> 2);
-        return size_t(h ^ k.swizzle);
+        return size_t(h ^ k.swizzle ^ (uint64_t(k.box_blocks) << 40));
     }
 };
 
 std::mutex g_map_mu;
 std::unordered_map<MapKey, CUtensorMap, MapKeyHash> g_maps;
 
-bool tmap_2d_bf16_impl(CUtensorMap* out, const void* ptr, uint64_t inner, uint64_t outer, uint64_t stride,
-                uint32_t box_inner, uint32_t box_outer, int swizzle_bytes) {
+bool tmap_bf16_impl(CUtensorMap* out, const void* ptr, uint64_t inner, uint64_t outer, uint64_t stride,
+                uint32_t box_inner, uint32_t box_outer, int swizzle_bytes, uint32_t box_blocks) {
     const MapKey key{reinterpret_cast<uintptr_t>(ptr), inner, outer, stride, box_inner, box_outer,
-                     uint32_t(swizzle_bytes)};
+                     uint32_t(swizzle_bytes), box_blocks};
     {
         std::lock_guard<std::mutex> lk(g_map_mu);
         auto it = g_maps.find(key);
@@ -67,17 +69,30 @@ bool tmap_2d_bf16_impl(CUtensorMap* out, const void* ptr, uint64_t inner, uint64
     EncodeTiledFn fn = encode_fn();
     if (!fn) return false;
     CUtensorMap m;
-    const cuuint64_t dims[2] = {inner, outer};
-    const cuuint64_t strides[1] = {stride * 2};
-    const cuuint32_t box[2] = {box_inner, box_outer};
-    const cuuint32_t estr[2] = {1, 1};
     const CUtensorMapSwizzle sw = swizzle_bytes == 128  ? CU_TENSOR_MAP_SWIZZLE_128B
                                   : swizzle_bytes == 64 ? CU_TENSOR_MAP_SWIZZLE_64B
                                                         : CU_TENSOR_MAP_SWIZZLE_32B;
-    if (fn(&m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, const_cast<void*>(ptr), dims, strides, box,
-           estr, CU_TENSOR_MAP_INTERLEAVE_NONE, sw, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
-           CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) != CUDA_SUCCESS)
-        return false;
+    CUresult r;
+    if (box_blocks == 0) {
+        const cuuint64_t dims[2] = {inner, outer};
+        const cuuint64_t strides[1] = {stride * 2};
+        const cuuint32_t box[2] = {box_inner, box_outer};
+        const cuuint32_t estr[2] = {1, 1};
+        r = fn(&m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, const_cast<void*>(ptr), dims, strides, box,
+               estr, CU_TENSOR_MAP_INTERLEAVE_NONE, sw, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+               CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+    } else {
+        // [outer][inner] viewed as (box_inner-wide column, row, column block): element
+        // (c, r, b) = base[r*stride + b*box_inner + c]; inner must be a multiple of box_inner
+        const cuuint64_t dims[3] = {box_inner, outer, inner / box_inner};
+        const cuuint64_t strides[2] = {stride * 2, uint64_t(box_inner) * 2};
+        const cuuint32_t box[3] = {box_inner, box_outer, box_blocks};
+        const cuuint32_t estr[3] = {1, 1, 1};
+        r = fn(&m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 3, const_cast<void*>(ptr), dims, strides, box,
+               estr, CU_TENSOR_MAP_INTERLEAVE_NONE, sw, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+               CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+    }
+    if (r != CUDA_SUCCESS) return false;
     std::lock_guard<std::mutex> lk(g_map_mu);
     if (g_maps.size() > 4096) g_maps.clear();
     g_maps.emplace(key, m);
@@ -89,7 +104,15 @@ bool tmap_2d_bf16_impl(CUtensorMap* out, const void* ptr, uint64_t inner, uint64
 
 bool tmap_2d_bf16(CUtensorMap* out, const void* ptr, uint64_t inner, uint64_t outer,
                   uint64_t stride, uint32_t box_inner, uint32_t box_outer, int swizzle_bytes) {
-    return tmap_2d_bf16_impl(out, ptr, inner, outer, stride, box_inner, box_outer, swizzle_bytes);
+    return tmap_bf16_impl(out, ptr, inner, outer, stride, box_inner, box_outer, swizzle_bytes, 0);
+}
+
+bool tmap_kblocked_bf16(CUtensorMap* out, const void* ptr, uint64_t inner, uint64_t outer,
+                        uint64_t stride, uint32_t box_inner, uint32_t box_outer,
+                        uint32_t box_blocks, int swizzle_bytes) {
+    if (box_blocks == 0 || inner % box_inner != 0) return false;
+    return tmap_bf16_impl(out, ptr, inner, outer, stride, box_inner, box_outer, swizzle_bytes,
+                          box_blocks);
 }
 
 }  // namespace bi

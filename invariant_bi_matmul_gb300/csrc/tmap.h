@@ -12,4 +12,12 @@ namespace bi {
 bool tmap_2d_bf16(CUtensorMap* out, const void* ptr, uint64_t inner, uint64_t outer,
                   uint64_t stride, uint32_t box_inner, uint32_t box_outer, int swizzle_bytes);
 
+// The same tensor viewed in rank 3 as (box_inner-wide column, row, column block), so one
+// copy of box (box_inner, box_outer, box_blocks) lands as box_blocks consecutive
+// [box_outer x box_inner] tiles in shared memory (K-blocks of a K-major operand).
+// Requires inner % box_inner == 0 (the view never reaches past a row).
+bool tmap_kblocked_bf16(CUtensorMap* out, const void* ptr, uint64_t inner, uint64_t outer,
+                        uint64_t stride, uint32_t box_inner, uint32_t box_outer,
+                        uint32_t box_blocks, int swizzle_bytes);
+
 }  // namespace bi
