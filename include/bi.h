@@ -217,6 +217,34 @@ bi_status bi_decode_attn(const void* q, const void* k_cache, const void* v_cache
                          void* workspace, size_t workspace_bytes, bi_stream_t stream);
 
 /* ---------------------------------------------------------------------------------
+ * bi_verify_block_static_ws -- bi_verify_block without a caller-provided workspace.
+ * (No counterpart on the pages; it exists for callers that cannot allocate.)
+ *
+ * For callers that cannot call cudaMalloc where they run attention (code recorded into
+ * or replayed from someone else's CUDA graph, allocator-free runtimes that only hand
+ * over the tensors they own, real-time paths where an allocation and its implicit
+ * synchronisation are not allowed).  Same arguments and results as bi_verify_block
+ * minus workspace / workspace_bytes: the workspace is a fixed device array of
+ * BI_STATIC_WS_BYTES inside the library, present on every GPU that loads it until the
+ * process exits.  Nothing is allocated.
+ *   - A block whose bi_attn_workspace_size(...) exceeds BI_STATIC_WS_BYTES is refused
+ *     with BI_ERR_UNSUPPORTED (message names both sizes); use bi_verify_block then.
+ *   - The first call on a device looks the array's device address up
+ *     (cudaGetSymbolAddress); make that first call before any stream capture.
+ *   - Every call shares the one array and it keeps the last call's contents (nothing in
+ *     it needs to start at zero).  Calls whose kernels overlap on the GPU -- different
+ *     streams, different host threads -- race on it: serialise them.
+ * ------------------------------------------------------------------------------- */
+#define BI_STATIC_WS_BYTES (32u * 1024u * 1024u)
+bi_status bi_verify_block_static_ws(const void* q, const void* k_cache, const void* v_cache,
+                                    int64_t num_pages, const int32_t* block_table,
+                                    int64_t max_pages, const int32_t* seq_lens,
+                                    const int32_t* cu_q, int64_t batch, int64_t total_q,
+                                    int64_t max_q, int64_t max_seq_len, int64_t num_q_heads,
+                                    int64_t num_kv_heads, int64_t head_dim, int64_t page_size,
+                                    float scale, void* out, float* lse, bi_stream_t stream);
+
+/* ---------------------------------------------------------------------------------
  * Device error word
  * bi_device_status synchronises `stream`, reads and clears the current device's error
  * word and returns BI_OK, BI_ERR_TIMEOUT (a bounded wait ran out), BI_ERR_DEVICE_ARG,

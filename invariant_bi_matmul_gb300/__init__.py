@@ -24,6 +24,7 @@ PAGE_SIZE = 64
 ATTN_CHUNK = 512
 ATTN_MAX_Q = 8
 ATTN_MAX_ROWS = 32
+STATIC_WS_BYTES = 32 * 1024 * 1024
 
 # every function include/bi.h declares, with its ctypes signature
 _p, _i64, _f32, _sz, _int = ctypes.c_void_p, ctypes.c_int64, ctypes.c_float, ctypes.c_size_t, ctypes.c_int
@@ -43,6 +44,8 @@ SIGNATURES = {
                          _i64, _i64, _f32, _p, _p, _p, _sz, _p], _int),
     "bi_decode_attn": ([_p, _p, _p, _i64, _p, _i64, _p, _i64, _i64, _i64, _i64, _i64, _i64, _f32,
                         _p, _p, _p, _sz, _p], _int),
+    "bi_verify_block_static_ws": ([_p, _p, _p, _i64, _p, _i64, _p, _p, _i64, _i64, _i64, _i64, _i64,
+                                   _i64, _i64, _i64, _f32, _p, _p, _p], _int),
     "bi_device_status": ([_p], _int),
     "bi_selftest_wait_timeout": ([ctypes.c_uint64, _p], _int),
 }
@@ -253,6 +256,28 @@ def verify_block(q, k_cache, v_cache, block_table, seq_lens, cu_q, max_q: int, m
                                  _ptr(cu_q), seq_lens.shape[0], T, int(max_q), int(max_seq_len),
                                  hq, hkv, d, page, float(scale), _ptr(out), _ptr(lse), _ptr(ws),
                                  ws_bytes, _stream(stream)))
+    return out, lse
+
+
+def verify_block_static_ws(q, k_cache, v_cache, block_table, seq_lens, cu_q, max_q: int,
+                           max_seq_len: int, scale: float, out=None, lse=None, want_lse=True,
+                           stream=None):
+    """verify_block with the library's fixed device workspace instead of one from the
+    caller: for callers that cannot allocate device memory (see include/bi.h).  Calls
+    whose kernels overlap on the GPU share that workspace and must not overlap."""
+    torch = _torch()
+    num_pages, hkv, page, d = _paged_common(k_cache, v_cache, block_table, seq_lens)
+    _need(q, torch.bfloat16, "q", 3)
+    _need(cu_q, torch.int32, "cu_q", 1)
+    if not q.is_contiguous() or not cu_q.is_contiguous():
+        raise ValueError("q and cu_q must be contiguous")
+    T, hq, _ = q.shape
+    out, lse = _attn_out(q, out, lse, want_lse)
+    _check(lib().bi_verify_block_static_ws(_ptr(q), _ptr(k_cache), _ptr(v_cache), num_pages,
+                                           _ptr(block_table), block_table.shape[1], _ptr(seq_lens),
+                                           _ptr(cu_q), seq_lens.shape[0], T, int(max_q),
+                                           int(max_seq_len), hq, hkv, d, page, float(scale),
+                                           _ptr(out), _ptr(lse), _stream(stream)))
     return out, lse
 
 

@@ -68,6 +68,8 @@ bool aligned(const void* p, size_t a) { return reinterpret_cast<uintptr_t>(p) % 
 
 }  // namespace
 
+void set_last_error_message(const char* msg) { t_last_message = msg ? msg : ""; }
+
 const DeviceInfo* current_device_info(cudaError_t* why) {
     int d = -1;
     cudaError_t e = cudaGetDevice(&d);
