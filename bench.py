@@ -164,6 +164,24 @@ class ClockSampler:
                 "samples": len(sm)}
 
 
+# ------------------------------------------------------------------ multi-rank glue
+
+def max_over_ranks(value: float, device) -> float:
+    """Largest `value` over all ranks (the slowest replica sets the job's time)."""
+    import torch
+    import torch.distributed as dist
+    if not (dist.is_available() and dist.is_initialized()) or dist.get_world_size() == 1:
+        return float(value)
+    t = torch.tensor([float(value)], dtype=torch.float64, device=device)
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return float(t.item())
+
+
+def job_throughput(bytes_per_step: float, world: int, seconds_per_step: float) -> float:
+    """Whole-job GB/s: every replica streams bytes_per_step per step (weak scaling)."""
+    return bytes_per_step * world / seconds_per_step / 1e9
+
+
 # ------------------------------------------------------------------------ GPU arm
 
 class Step:
@@ -282,11 +300,7 @@ def run_gpu(args, rank, world, local_rank):
     if status != bi.BI_OK:
         raise RuntimeError(f"device error word after the timed region: {status}")
 
-    t_max = elapsed_ms
-    if dist:
-        t = torch.tensor([elapsed_ms], device=dev)
-        torch.distributed.all_reduce(t, op=torch.distributed.ReduceOp.MAX)
-        t_max = float(t.item())
+    t_max = max_over_ranks(elapsed_ms, dev)
 
     e2e = run_e2e(st, args, dist)
     extra = gemm_vs_cublas(st) if rank == 0 else {}
@@ -331,11 +345,7 @@ def run_e2e(st: Step, args, dist):
     t0 = time.perf_counter()
     for _ in range(n):
         step()
-    dt = (time.perf_counter() - t0) / n
-    if dist:
-        t = torch.tensor([dt], device=dev)
-        torch.distributed.all_reduce(t, op=torch.distributed.ReduceOp.MAX)
-        dt = float(t.item())
+    dt = max_over_ranks((time.perf_counter() - t0) / n, dev)
     h2d = hx.numel() * 2 + hk.numel() * 2 + hv.numel() * 2
     d2h = hy.numel() * 2
     return {"sec_per_step": dt, "h2d": h2d, "d2h": d2h, "steps": n}
@@ -498,7 +508,7 @@ def main():
     flops = step_flops()
     total = sum(nbytes.values())
     ms = res["elapsed_ms"] / args.steps
-    value = total * world / (ms * 1e-3) / 1e9
+    value = job_throughput(total, world, ms * 1e-3)
     calls_ms = res["per_call_ms"]
     share = {n: round(v / sum(calls_ms.values()), 4) for n, v in calls_ms.items()}
     parts = {}
@@ -524,7 +534,7 @@ def main():
         "config": workload_config(),
         "roofline": roof,
         "cpu_baseline": cpu,
-        "e2e": {"value": round(total * world / e2e["sec_per_step"] / 1e9, 1), "unit": "GB/s",
+        "e2e": {"value": round(job_throughput(total, world, e2e["sec_per_step"]), 1), "unit": "GB/s",
                 "h2d_bytes_per_step": e2e["h2d"], "d2h_bytes_per_step": e2e["d2h"],
                 "ms_per_step": round(e2e["sec_per_step"] * 1e3, 4)},
         "gpu_launches": Step.LAUNCHES_PER_STEP * args.steps,
