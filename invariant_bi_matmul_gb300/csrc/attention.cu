@@ -128,6 +128,8 @@ attn_partial_kernel(const __grid_constant__ CUtensorMap tmap_k,
     const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
     const int G = Hq / Hkv;
 
+    pdl_wait();
+    pdl_trigger();
     if (tid == 0) {
         for (int s = 0; s < NST; ++s) {
             mbar_init(&full[s], 1);
@@ -471,6 +473,8 @@ attn_merge_kernel(const int32_t* __restrict__ seq_lens, const int32_t* __restric
     constexpr int UNROLL = 4;
     __shared__ float sM[MERGE_WARPS], sL[MERGE_WARPS];
     __shared__ float sO[MERGE_WARPS][D];
+    pdl_wait();
+    pdl_trigger();
     const int t = int(blockIdx.x / unsigned(Hq));
     const int hq = int(blockIdx.x - unsigned(t) * unsigned(Hq));
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
@@ -566,6 +570,8 @@ kv_append_kernel(const uint4* __restrict__ k_new, const uint4* __restrict__ v_ne
                  const int32_t* __restrict__ seq_lens, const int32_t* __restrict__ cu_q, int B,
                  int total_q, int Hkv, int D, unsigned int* err) {
     // one thread per 16-byte piece of one token's K (and V) row of one KV head
+    pdl_wait();
+    pdl_trigger();
     const int per_tok = Hkv * (D / 8);
     const int64_t idx = int64_t(blockIdx.x) * blockDim.x + threadIdx.x;
     if (idx >= int64_t(total_q) * per_tok) return;
@@ -623,16 +629,17 @@ cudaError_t launch_attention_t(const DeviceInfo& dev, const void* q, const Paged
     float* ws_o = static_cast<float*>(workspace);
     float* ws_ml = ws_o + a.total_q * a.hq * int64_t(maxC) * D;
     const float scale_log2 = scale * kLog2e;
-    kern<<<grid, THREADS, Cf::SMEM, stream>>>(
-        tk, tv, static_cast<const __nv_bfloat16*>(q), a.block_table, int(a.max_pages),
-        int(a.num_pages), a.seq_lens, a.cu_q, int(a.batch), int(a.total_q), int(a.max_q),
-        int(a.max_seq_len), int(a.hq), int(a.hkv), scale_log2, ws_o, ws_ml, maxC, dev.err_word);
-    cudaError_t e = cudaGetLastError();
-    if (e != cudaSuccess) return e;
-    attn_merge_kernel<D><<<unsigned(a.total_q * a.hq), MERGE_WARPS * 32, 0, stream>>>(
+    cudaError_t e = launch_pdl(
+        kern, dim3(grid), dim3(THREADS), Cf::SMEM, stream, tk, tv,
+        static_cast<const __nv_bfloat16*>(q), a.block_table, int(a.max_pages), int(a.num_pages),
         a.seq_lens, a.cu_q, int(a.batch), int(a.total_q), int(a.max_q), int(a.max_seq_len),
-        int(a.hq), ws_o, ws_ml, maxC, static_cast<__nv_bfloat16*>(out), lse);
-    return cudaGetLastError();
+        int(a.hq), int(a.hkv), scale_log2, ws_o, ws_ml, maxC, dev.err_word);
+    if (e != cudaSuccess) return e;
+    return launch_pdl(attn_merge_kernel<D>, dim3(unsigned(a.total_q * a.hq)),
+                      dim3(MERGE_WARPS * 32), 0, stream, a.seq_lens, a.cu_q, int(a.batch),
+                      int(a.total_q), int(a.max_q), int(a.max_seq_len), int(a.hq),
+                      static_cast<const float*>(ws_o), static_cast<const float*>(ws_ml), maxC,
+                      static_cast<__nv_bfloat16*>(out), lse);
 }
 
 }  // namespace
@@ -646,12 +653,11 @@ cudaError_t launch_kv_append(const DeviceInfo& dev, const void* k_new, const voi
                              void* k_cache, void* v_cache, const PagedArgs& a,
                              cudaStream_t stream) {
     const int64_t n = a.total_q * a.hkv * (a.head_dim / 8);
-    kv_append_kernel<<<unsigned((n + 255) / 256), 256, 0, stream>>>(
-        static_cast<const uint4*>(k_new), static_cast<const uint4*>(v_new),
-        static_cast<uint4*>(k_cache), static_cast<uint4*>(v_cache), int(a.num_pages),
-        a.block_table, int(a.max_pages), a.seq_lens, a.cu_q, int(a.batch), int(a.total_q),
-        int(a.hkv), int(a.head_dim), dev.err_word);
-    return cudaGetLastError();
+    return launch_pdl(kv_append_kernel, dim3(unsigned((n + 255) / 256)), dim3(256), 0, stream,
+                      static_cast<const uint4*>(k_new), static_cast<const uint4*>(v_new),
+                      static_cast<uint4*>(k_cache), static_cast<uint4*>(v_cache),
+                      int(a.num_pages), a.block_table, int(a.max_pages), a.seq_lens, a.cu_q,
+                      int(a.batch), int(a.total_q), int(a.hkv), int(a.head_dim), dev.err_word);
 }
 
 cudaError_t launch_attention(const DeviceInfo& dev, const void* q, const PagedArgs& a,

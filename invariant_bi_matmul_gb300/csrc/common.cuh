@@ -41,6 +41,14 @@ __device__ __forceinline__ void latch_error(unsigned int* err, unsigned int bits
     if (err) atomicOr(err, bits);
 }
 
+// Programmatic dependent launch: wait until the previous grid in the stream has completed
+// and its memory is visible (call before the first global access), and let the next
+// grid be scheduled early (its own wait still orders it after this grid).
+__device__ __forceinline__ void pdl_wait() { asm volatile("griddepcontrol.wait;" ::: "memory"); }
+__device__ __forceinline__ void pdl_trigger() {
+    asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
+}
+
 // ------------------------------------------------------------------------- mbarrier
 
 __device__ __forceinline__ void mbar_init(uint64_t* bar, uint32_t count) {

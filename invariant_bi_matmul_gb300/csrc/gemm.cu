@@ -145,6 +145,9 @@ gemm_kernel(const __grid_constant__ CUtensorMap tmap_x, const __grid_constant__ 
     __syncthreads();
     tc_fence_after_sync();
     const uint32_t tmem_base = *tmem_slot;
+    // set-up above touches no global memory; from here on the previous grid must be done
+    pdl_wait();
+    pdl_trigger();
 
     auto fail = [&]() {
         *abort_flag = 1;
@@ -384,8 +387,7 @@ cudaError_t launch_t(const DeviceInfo& dev, const CUtensorMap& mx, const CUtenso
         if (e != cudaSuccess) return e;
         attr_done[dev.device] = true;
     }
-    kern<<<grid, THREADS, SMEM_BYTES, s>>>(mx, mw, a, dev.err_word);
-    return cudaGetLastError();
+    return launch_pdl(kern, dim3(grid), dim3(THREADS), SMEM_BYTES, s, mx, mw, a, dev.err_word);
 }
 
 template <bool KN, bool F32OUT>

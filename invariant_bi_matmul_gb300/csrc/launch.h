@@ -6,6 +6,8 @@
 #include <stddef.h>
 #include <stdint.h>
 
+#include <utility>
+
 namespace bi {
 
 // Bits of the per-device error word (the host maps them to bi_status codes).
@@ -13,6 +15,27 @@ enum : unsigned int {
     kErrTimeout = 1u,    // a bounded wait ran out
     kErrDeviceArg = 2u,  // a device-resident argument was out of range; work skipped
 };
+
+// Launches `kernel` with programmatic dependent launch allowed: the next kernel in the
+// stream may be scheduled as soon as every CTA of this one has started (each kernel
+// triggers its dependents early), and each kernel waits (griddepcontrol.wait) for the
+// previous grid to complete and flush before it touches global memory.  Only launch
+// latency and prologues overlap; completion order and memory visibility are unchanged.
+template <typename... KArgs, typename... Args>
+cudaError_t launch_pdl(void (*kernel)(KArgs...), dim3 grid, dim3 block, size_t smem,
+                       cudaStream_t stream, Args&&... args) {
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = grid;
+    cfg.blockDim = block;
+    cfg.dynamicSmemBytes = smem;
+    cfg.stream = stream;
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr[0].val.programmaticStreamSerializationAllowed = 1;
+    cfg.attrs = attr;
+    cfg.numAttrs = 1;
+    return cudaLaunchKernelEx(&cfg, kernel, std::forward<Args>(args)...);
+}
 
 struct DeviceInfo {
     int device = -1;

@@ -90,6 +90,8 @@ rmsnorm_kernel(const __nv_bfloat16* __restrict__ x, int64_t ldx,
                const __nv_bfloat16* __restrict__ gamma, void* __restrict__ y, int64_t ldy,
                int H, float eps, int vec) {
     __shared__ float warp_sums[kWarps];
+    pdl_wait();
+    pdl_trigger();
     const int64_t row = blockIdx.x;
     const __nv_bfloat16* __restrict__ xr = x + row * ldx;
     const int64_t ngroups = (H + 7) / 8;
@@ -171,10 +173,10 @@ cudaError_t launch_impl(const void* x, int64_t ldx, const void* gamma, void* y, 
     auto xb = static_cast<const __nv_bfloat16*>(x);
     auto gb = static_cast<const __nv_bfloat16*>(gamma);
     if (y_f32)
-        rmsnorm_kernel<MAXJ, true><<<grid, block, 0, s>>>(xb, ldx, gb, y, ldy, H, eps, vec);
-    else
-        rmsnorm_kernel<MAXJ, false><<<grid, block, 0, s>>>(xb, ldx, gb, y, ldy, H, eps, vec);
-    return cudaGetLastError();
+        return launch_pdl(rmsnorm_kernel<MAXJ, true>, grid, block, 0, s, xb, ldx, gb, y, ldy, H,
+                          eps, vec);
+    return launch_pdl(rmsnorm_kernel<MAXJ, false>, grid, block, 0, s, xb, ldx, gb, y, ldy, H, eps,
+                      vec);
 }
 
 }  // namespace
