@@ -150,3 +150,93 @@ def mixed_lengths(B: int, seed: int, choices=(1028, 8196, 16388, 65540)):
     """Sequence lengths drawn uniformly (seeded) from the pages' Lk values."""
     idx = torch.randint(0, len(choices), (B,), generator=generator(seed))
     return [int(choices[i]) for i in idx]
+
+
+# --------------------------------------------------------- greedy-trace decoder stack
+
+@dataclass(frozen=True)
+class DecoderConfig:
+    """Shape of a Llama-style decoder stack (sizes only)."""
+    hidden: int
+    heads: int
+    kv_heads: int
+    head_dim: int
+    inter: int
+    layers: int
+    vocab: int
+    context: int          # tokens already in every sequence's KV cache
+    eps: float = 1e-5
+    theta: float = 500000.0
+
+
+# The full-decoder workload: Llama-3-8B shapes, 8 layers, 8192-token contexts.  The pages
+# name no vocabulary size; 128256 is Llama-3's.
+LLAMA3_8B_8L = DecoderConfig(hidden=4096, heads=32, kv_heads=8, head_dim=128, inter=14336,
+                             layers=8, vocab=128256, context=8192)
+
+# A stack the oracle runs in seconds: two layers, GQA with 2 query heads per KV head.
+TINY_DECODER = DecoderConfig(hidden=256, heads=4, kv_heads=2, head_dim=64, inter=512,
+                             layers=2, vocab=1000, context=100)
+
+
+def _name_seed(seed: int, name: str) -> int:
+    import zlib
+    return (int(seed) * 1000003 + zlib.crc32(name.encode())) & 0x7fffffffffff
+
+
+def _normal_on(shape, std: float, mean: float, seed: int, device) -> torch.Tensor:
+    device = torch.device(device)
+    g = torch.Generator(device=device)
+    g.manual_seed(int(seed))
+    t = torch.randn(*shape, generator=g, dtype=torch.float32, device=device)
+    return (t * std + mean).to(torch.bfloat16)
+
+
+def decoder_weight_shapes(cfg: DecoderConfig) -> dict:
+    """Every weight of the stack with its shape (nn.Linear matrices are [out, in])."""
+    q, kv = cfg.heads * cfg.head_dim, cfg.kv_heads * cfg.head_dim
+    shapes = {"embed": (cfg.vocab, cfg.hidden), "lm_head": (cfg.vocab, cfg.hidden),
+              "final_norm": (cfg.hidden,)}
+    for i in range(cfg.layers):
+        p = f"l{i}."
+        shapes.update({p + "attn_norm": (cfg.hidden,), p + "wq": (q, cfg.hidden),
+                       p + "wk": (kv, cfg.hidden), p + "wv": (kv, cfg.hidden),
+                       p + "wo": (cfg.hidden, q), p + "mlp_norm": (cfg.hidden,),
+                       p + "w_gate": (cfg.inter, cfg.hidden), p + "w_up": (cfg.inter, cfg.hidden),
+                       p + "w_down": (cfg.hidden, cfg.inter)})
+    return shapes
+
+
+def decoder_weights(cfg: DecoderConfig, seed: int, device="cpu", std: float = 0.02,
+                    norm_std: float = 0.0) -> dict:
+    """Random-init bf16 weights: matrices N(0, std); norm gains N(1, norm_std) (ones at
+    the default 0, the usual initialisation).  Each tensor has its own seed, derived from
+    its name, so a tensor does not depend on which others are drawn."""
+    out = {}
+    for name, shape in decoder_weight_shapes(cfg).items():
+        if len(shape) == 1:
+            out[name] = _normal_on(shape, norm_std, 1.0, _name_seed(seed, name), device)
+        else:
+            out[name] = _normal_on(shape, std, 0.0, _name_seed(seed, name), device)
+    return out
+
+
+def decoder_context(cfg: DecoderConfig, seq_id: int, layer: int, seed: int, device="cpu"):
+    """K and V rows (bf16 [context, Hkv, D], N(0,1)) that stand for sequence seq_id's
+    already-processed context in one layer.  They depend only on (seed, seq_id, layer),
+    never on the batch the sequence is decoded in."""
+    shape = (cfg.context, cfg.kv_heads, cfg.head_dim)
+    base = _name_seed(seed, f"ctx.{seq_id}.{layer}")
+    return (_normal_on(shape, 1.0, 0.0, base * 2 + 1, device),
+            _normal_on(shape, 1.0, 0.0, base * 2 + 2, device))
+
+
+def decoder_first_token(cfg: DecoderConfig, seq_id: int, seed: int) -> int:
+    """The token sequence seq_id is decoded from (uniform over the vocabulary)."""
+    g = generator(_name_seed(seed, f"tok.{seq_id}"))
+    return int(torch.randint(0, cfg.vocab, (1,), generator=g).item())
+
+
+def page_permutation(num_pages: int, seed: int) -> torch.Tensor:
+    """A seeded permutation of physical page ids (int32)."""
+    return torch.randperm(num_pages, generator=generator(seed)).to(torch.int32)

@@ -68,6 +68,10 @@ def _declare(L: ctypes.CDLL) -> None:
     L.oracle_attention.argtypes = [_p, _p, _p, _p, _i64, _p, _p, _i64, _i64, _i64, _i64, _i64,
                                    ctypes.c_float, _p, _p]
     L.oracle_attention.restype = ctypes.c_int
+    L.oracle_positions.argtypes = [_p, _p, _i64, _p]
+    L.oracle_rope.argtypes = [_p, _i64, _p, _i64, _i64, _i64, _i64, _p, ctypes.c_double]
+    L.oracle_swiglu.argtypes = [_p, _p, _p, _i64]
+    L.oracle_add.argtypes = [_p, _p, _p, _i64]
 
 
 def _ptr(a: np.ndarray):
@@ -226,3 +230,58 @@ def attention_row(q, k_cache, v_cache, block_table, seq_lens, cu_q, b, j, h, Hq,
     if rc:
         raise RuntimeError(f"oracle_attention_row failed ({rc})")
     return out, float(lse[0])
+
+
+# ------------------------------------------------------------------- decoder glue
+
+def positions(seq_lens, cu_q=None) -> np.ndarray:
+    """Position of every token of a ragged block (int32 [T]); cu_q None = one per sequence."""
+    sl = np.ascontiguousarray(seq_lens, dtype=np.int32)
+    if cu_q is None:
+        pos = np.empty(sl.size, dtype=np.int32)
+        lib().oracle_positions(_ptr(sl), None, sl.size, _ptr(pos))
+        return pos
+    cq = np.ascontiguousarray(cu_q, dtype=np.int32)
+    pos = np.empty(int(cq[-1]), dtype=np.int32)
+    lib().oracle_positions(_ptr(sl), _ptr(cq), sl.size, _ptr(pos))
+    return pos
+
+
+def rope(x: np.ndarray, pos: np.ndarray, theta: float) -> np.ndarray:
+    """x uint16 [T,H,D] (bf16 bits), pos int32 [T] -> rotated fp64 [T,H,D] (unrounded)."""
+    x = _as(x, np.uint16)
+    pos = np.ascontiguousarray(pos, dtype=np.int32)
+    T, H, D = x.shape
+    if pos.size != T or D % 2:
+        raise ValueError("pos must have one entry per token and D must be even")
+    y = np.empty((T, H, D), dtype=np.float64)
+    lib().oracle_rope(_ptr(x), H * D, _ptr(y), H * D, T, H, D, _ptr(pos), float(theta))
+    return y
+
+
+def swiglu(g: np.ndarray, u: np.ndarray) -> np.ndarray:
+    """silu(g) * u elementwise for bf16 bits g, u (same shape) -> fp64 (unrounded)."""
+    g = _as(g, np.uint16)
+    u = _as(u, np.uint16)
+    if g.shape != u.shape:
+        raise ValueError("g and u shapes differ")
+    y = np.empty(g.shape, dtype=np.float64)
+    lib().oracle_swiglu(_ptr(g), _ptr(u), _ptr(y), g.size)
+    return y
+
+
+def add(a: np.ndarray, b: np.ndarray) -> np.ndarray:
+    """a + b elementwise for bf16 bits a, b (same shape) -> fp64 (exact)."""
+    a = _as(a, np.uint16)
+    b = _as(b, np.uint16)
+    if a.shape != b.shape:
+        raise ValueError("a and b shapes differ")
+    y = np.empty(a.shape, dtype=np.float64)
+    lib().oracle_add(_ptr(a), _ptr(b), _ptr(y), a.size)
+    return y
+
+
+def to_bf16(y: np.ndarray) -> np.ndarray:
+    """Unrounded oracle values (fp32 or fp64) -> bf16 bits: fp64 narrows to fp32 (round
+    to nearest even), then fp32 rounds to bf16 (nearest even)."""
+    return bf16_round(np.asarray(y, dtype=np.float32))

@@ -126,10 +126,16 @@ ORACLE_API float oracle_sum_squares_f32(const float* a, int64_t n) {
 
 /* Greedy decoding picks the largest logit; among equal maxima the lowest index. */
 ORACLE_API int64_t oracle_argmax_f32(const float* v, int64_t n) {
+    /* Greedy decoding picks the largest logit; among equal maxima the lowest index
+     * wins.  NaN ranks below every number (below -inf too), so a NaN is picked only
+     * when the whole vector is NaN, and then the lowest index.  The pages define no
+     * NaN rule; this one makes the choice a total order, independent of scan order. */
     if (n <= 0) return -1;
     int64_t best = 0;
     for (int64_t i = 1; i < n; ++i) {
-        if (v[i] > v[best]) best = i;
+        int best_nan = isnan(v[best]), cur_nan = isnan(v[i]);
+        if (best_nan && !cur_nan) best = i;
+        else if (!best_nan && !cur_nan && v[i] > v[best]) best = i;
     }
     return best;
 }
@@ -301,4 +307,70 @@ ORACLE_API int oracle_attention(const uint16_t* q, const uint16_t* k_cache, cons
         }
     }
     return 0;
+}
+
+/* ============================================================================== */
+/* Decoder glue for the greedy-trace workload: a Llama-3-8B-shaped decoder stack   */
+/* (hidden 4096, 32 query / 8 KV heads, SwiGLU MLP 14336, 8 layers) whose greedy   */
+/* token trace must not depend on batch size or verify width ("Fix/speculative    */
+/* shape invariance", section Problem; book chapter Case 5, the greedy token under */
+/* three loads).  The pages name the stack's shape but define neither the rotary   */
+/* embedding nor the MLP activation; the standard published definitions are used   */
+/* (rotary position embedding: Su et al., RoFormer, 2021, in the rotate-half       */
+/* pairing of the Llama checkpoints; SwiGLU: Shazeer, "GLU Variants Improve         */
+/* Transformer", 2020).  Everything below is evaluated in fp64 and returned        */
+/* unrounded; callers narrow to fp32 and then round to bf16 (oracle_bf16_round)   */
+/* where the GPU path stores bf16.                                                 */
+/* ============================================================================== */
+
+/* Position of token t (0..total-1): tokens of sequence b are cu_q[b]..cu_q[b+1]-1  */
+/* and sit at the last q_b positions of its seq_lens[b] tokens.  cu_q == NULL means */
+/* one token per sequence (decode).                                                 */
+ORACLE_API void oracle_positions(const int32_t* seq_lens, const int32_t* cu_q, int64_t B,
+                                 int32_t* pos) {
+    for (int64_t b = 0; b < B; ++b) {
+        int64_t t0 = cu_q ? cu_q[b] : b;
+        int64_t q_b = cu_q ? cu_q[b + 1] - cu_q[b] : 1;
+        for (int64_t j = 0; j < q_b; ++j) pos[t0 + j] = (int32_t)(seq_lens[b] - q_b + j);
+    }
+}
+
+/* Rotary position embedding of x [T][H][D] (row t at x + t*ldx, heads contiguous)  */
+/* at positions pos[t].  Pair i (0 <= i < D/2) joins elements i and i + D/2 and is  */
+/* turned by the angle pos * theta^(-2i/D):                                          */
+/*   y[i]       = x[i] cos(a) - x[i+D/2] sin(a)                                     */
+/*   y[i+D/2]   = x[i+D/2] cos(a) + x[i] sin(a)                                     */
+ORACLE_API void oracle_rope(const uint16_t* x, int64_t ldx, double* y, int64_t ldy, int64_t T,
+                            int64_t H, int64_t D, const int32_t* pos, double theta) {
+    int64_t half = D / 2;
+    for (int64_t t = 0; t < T; ++t) {
+        for (int64_t h = 0; h < H; ++h) {
+            const uint16_t* xr = x + t * ldx + h * D;
+            double* yr = y + t * ldy + h * D;
+            for (int64_t i = 0; i < half; ++i) {
+                double freq = pow(theta, -2.0 * (double)i / (double)D);
+                double a = (double)pos[t] * freq;
+                double c = cos(a), s = sin(a);
+                double lo = (double)bf16_bits_to_f32(xr[i]);
+                double hi = (double)bf16_bits_to_f32(xr[i + half]);
+                yr[i] = lo * c - hi * s;
+                yr[i + half] = hi * c + lo * s;
+            }
+        }
+    }
+}
+
+/* SwiGLU gating: y = silu(g) * u with silu(g) = g / (1 + exp(-g)). */
+ORACLE_API void oracle_swiglu(const uint16_t* g, const uint16_t* u, double* y, int64_t n) {
+    for (int64_t i = 0; i < n; ++i) {
+        double gv = (double)bf16_bits_to_f32(g[i]);
+        double uv = (double)bf16_bits_to_f32(u[i]);
+        y[i] = gv / (1.0 + exp(-gv)) * uv;
+    }
+}
+
+/* Residual add: y = a + b. */
+ORACLE_API void oracle_add(const uint16_t* a, const uint16_t* b, double* y, int64_t n) {
+    for (int64_t i = 0; i < n; ++i)
+        y[i] = (double)bf16_bits_to_f32(a[i]) + (double)bf16_bits_to_f32(b[i]);
 }
