@@ -26,7 +26,7 @@ ATTN_MAX_Q = 8
 ATTN_MAX_ROWS = 32
 STATIC_WS_BYTES = 32 * 1024 * 1024
 
-# every function include/bi.h declares, with its ctypes signature
+# every function include/bi.h and include/bi_glue.h declare, with its ctypes signature
 _p, _i64, _f32, _sz, _int = ctypes.c_void_p, ctypes.c_int64, ctypes.c_float, ctypes.c_size_t, ctypes.c_int
 SIGNATURES = {
     "bi_abi_version": ([], _int),
@@ -48,6 +48,12 @@ SIGNATURES = {
                                    _i64, _i64, _i64, _f32, _p, _p, _p], _int),
     "bi_device_status": ([_p], _int),
     "bi_selftest_wait_timeout": ([ctypes.c_uint64, _p], _int),
+    # decoder glue (include/bi_glue.h)
+    "bi_embedding": ([_p, _i64, _i64, _p, _i64, _p, _i64, _p], _int),
+    "bi_rope": ([_p, _i64, _i64, _i64, _i64, _p, _p, _i64, _f32, _p], _int),
+    "bi_swiglu": ([_p, _i64, _p, _i64, _p, _i64, _i64, _i64, _p], _int),
+    "bi_add": ([_p, _p, _p, _i64, _p], _int),
+    "bi_argmax": ([_p, _i64, _i64, _i64, _p, _p], _int),
 }
 
 _lib: Optional[ctypes.CDLL] = None
@@ -309,3 +315,89 @@ def device_status(stream=None) -> int:
 
 def selftest_wait_timeout(timeout_ns: int, stream=None) -> None:
     _check(lib().bi_selftest_wait_timeout(int(timeout_ns), _stream(stream)))
+
+
+# ----------------------------------------------------------------------- decoder glue
+
+def embedding(table, ids, out=None, stream=None):
+    """out[t] = table[ids[t]] for a bf16 [vocab, hidden] table and int32 ids [n]."""
+    torch = _torch()
+    _need(table, torch.bfloat16, "table", 2)
+    _need(ids, torch.int32, "ids", 1)
+    if not table.is_contiguous() or not ids.is_contiguous():
+        raise ValueError("table and ids must be contiguous")
+    vocab, hidden = table.shape
+    n = ids.shape[0]
+    if out is None:
+        out = torch.empty(n, hidden, dtype=torch.bfloat16, device=table.device)
+    _need(out, torch.bfloat16, "out", 2)
+    if tuple(out.shape) != (n, hidden):
+        raise ValueError("out must be [n, hidden]")
+    _check(lib().bi_embedding(_ptr(table), vocab, hidden, _ptr(ids), n, _ptr(out),
+                              _row_major_2d(out, "out"), _stream(stream)))
+    return out
+
+
+def rope(x, seq_lens, cu_q=None, theta: float = 500000.0, stream=None):
+    """Rotary embedding in place on x bf16 [T, H, D] (rows may be strided: x[t] at
+    x.stride(0)); positions from seq_lens / cu_q as in verify_block."""
+    torch = _torch()
+    _need(x, torch.bfloat16, "x", 3)
+    _need(seq_lens, torch.int32, "seq_lens", 1)
+    T, H, D = x.shape
+    if x.stride(2) != 1 or x.stride(1) != D:
+        raise ValueError("x must have contiguous heads within a token")
+    if cu_q is not None:
+        _need(cu_q, torch.int32, "cu_q", 1)
+    _check(lib().bi_rope(_ptr(x), x.stride(0) if T > 1 else H * D, T, H, D, _ptr(seq_lens),
+                         _ptr(cu_q), seq_lens.shape[0], float(theta), _stream(stream)))
+    return x
+
+
+def swiglu(gate, up, out=None, stream=None):
+    """silu(gate) * up elementwise for bf16 [rows, inter] gate and up."""
+    torch = _torch()
+    _need(gate, torch.bfloat16, "gate", 2)
+    _need(up, torch.bfloat16, "up", 2)
+    if gate.shape != up.shape:
+        raise ValueError("gate and up shapes differ")
+    rows, inter = gate.shape
+    if out is None:
+        out = torch.empty(rows, inter, dtype=torch.bfloat16, device=gate.device)
+    _need(out, torch.bfloat16, "out", 2)
+    _check(lib().bi_swiglu(_ptr(gate), _row_major_2d(gate, "gate"), _ptr(up),
+                           _row_major_2d(up, "up"), _ptr(out), _row_major_2d(out, "out"), rows,
+                           inter, _stream(stream)))
+    return out
+
+
+def add(a, b, out=None, stream=None):
+    """a + b elementwise for contiguous bf16 tensors of one shape (out may be a or b)."""
+    torch = _torch()
+    _need(a, torch.bfloat16, "a")
+    _need(b, torch.bfloat16, "b")
+    if a.shape != b.shape or not a.is_contiguous() or not b.is_contiguous():
+        raise ValueError("a and b must be contiguous tensors of one shape")
+    if out is None:
+        out = torch.empty_like(a)
+    _need(out, torch.bfloat16, "out")
+    if out.shape != a.shape or not out.is_contiguous():
+        raise ValueError("out must be contiguous with a's shape")
+    _check(lib().bi_add(_ptr(a), _ptr(b), _ptr(out), a.numel(), _stream(stream)))
+    return out
+
+
+def argmax(logits, out=None, stream=None):
+    """Greedy token of each row of fp32 [rows, n] logits (int32 [rows]); lowest index among
+    equal maxima, NaN ranked below every number."""
+    torch = _torch()
+    _need(logits, torch.float32, "logits", 2)
+    rows, n = logits.shape
+    if out is None:
+        out = torch.empty(rows, dtype=torch.int32, device=logits.device)
+    _need(out, torch.int32, "out", 1)
+    if out.shape[0] != rows or not out.is_contiguous():
+        raise ValueError("out must be a contiguous int32 [rows] tensor")
+    _check(lib().bi_argmax(_ptr(logits), _row_major_2d(logits, "logits"), rows, n, _ptr(out),
+                           _stream(stream)))
+    return out

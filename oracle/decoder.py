@@ -44,11 +44,13 @@ class OracleDecoder:
         self.k_cache = [np.zeros(shape, dtype=np.uint16) for _ in range(cfg.layers)]
         self.v_cache = [np.zeros(shape, dtype=np.uint16) for _ in range(cfg.layers)]
 
-    def append_context(self, layer: int, k: np.ndarray, v: np.ndarray, seq_lens, cu_q):
-        """Writes given K/V rows (uint16 [T,Hkv,D]) into a layer's cache slots."""
+    def append_context(self, layer: int, slot: int, k: np.ndarray, v: np.ndarray):
+        """Writes a sequence's context K/V rows (uint16 [n,Hkv,D], positions 0..n-1) into
+        the cache pages of block-table row `slot` of one layer."""
+        n = k.shape[0]
         self.k_cache[layer], self.v_cache[layer] = kv_append(
-            k, v, self.k_cache[layer], self.v_cache[layer], self.block_table, seq_lens, cu_q,
-            self.page)
+            k, v, self.k_cache[layer], self.v_cache[layer], self.block_table[slot:slot + 1],
+            np.array([n], dtype=np.int32), np.array([0, n], dtype=np.int32), self.page)
 
     def forward(self, tokens, seq_lens, cu_q) -> np.ndarray:
         """Logits fp32 [T,V] for a ragged block: tokens int [T]; sequence b's tokens are

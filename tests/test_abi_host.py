@@ -13,13 +13,20 @@ import pytest
 import invariant_bi_matmul_gb300 as bi
 
 ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
-HEADER = os.path.join(ROOT, "include", "bi.h")
+HEADERS = [os.path.join(ROOT, "include", h) for h in ("bi.h", "bi_glue.h")]
 
 
 def declared_functions():
-    src = open(HEADER).read()
-    src = re.sub(r"/\*.*?\*/", "", src, flags=re.S)
-    return sorted(set(re.findall(r"\b(bi_[a-z0-9_]+)\s*\(", src)))
+    names = set()
+    for h in HEADERS:
+        src = re.sub(r"/\*.*?\*/", "", open(h).read(), flags=re.S)
+        names.update(re.findall(r"\b(bi_[a-z0-9_]+)\s*\(", src))
+    return sorted(names)
+
+
+def test_every_header_is_checked():
+    assert sorted(os.listdir(os.path.join(ROOT, "include"))) == sorted(
+        os.path.basename(h) for h in HEADERS)
 
 
 @pytest.fixture(scope="module")
@@ -30,6 +37,7 @@ def L():
 def test_header_declares_the_boundary():
     names = declared_functions()
     for must in ("bi_matmul", "bi_rmsnorm", "bi_decode_attn", "bi_verify_block", "bi_kv_append",
+                 "bi_embedding", "bi_rope", "bi_swiglu", "bi_add", "bi_argmax",
                  "bi_set_batch_invariant_limit", "bi_get_batch_invariant_limit",
                  "bi_attn_workspace_size", "bi_device_status"):
         assert must in names
@@ -180,3 +188,33 @@ def test_binding_refuses_cpu_tensors():
         bi.matmul(x, torch.zeros(8, 8, dtype=torch.bfloat16))
     with pytest.raises(ValueError, match="CUDA"):
         bi.rmsnorm(x, torch.ones(8, dtype=torch.bfloat16), 1e-5)
+
+
+def test_glue_argument_errors_before_launch(L):
+    d = 1 << 20  # a fake, 16-byte aligned address: nothing may touch it
+    f = ctypes.c_float
+    # embedding: vocab < 1, hidden not a multiple of 8, ldo < hidden, null ids
+    assert L.bi_embedding(d, 0, 64, d, 1, d, 64, None) == bi.BI_ERR_INVALID_ARG
+    assert L.bi_embedding(d, 10, 60, d, 1, d, 64, None) == bi.BI_ERR_UNSUPPORTED
+    assert L.bi_embedding(d, 10, 64, d, 1, d, 32, None) == bi.BI_ERR_INVALID_ARG
+    assert L.bi_embedding(d, 10, 64, None, 1, d, 64, None) == bi.BI_ERR_INVALID_ARG
+    assert L.bi_embedding(d + 8, 10, 64, d, 1, d, 64, None) == bi.BI_ERR_UNSUPPORTED
+    assert L.bi_embedding(None, 10, 64, None, 0, None, 64, None) == bi.BI_OK  # n = 0
+    # rope: head_dim not a multiple of 16, theta <= 0, no cu_q with total_q != batch
+    assert L.bi_rope(d, 96, 1, 4, 24, d, None, 1, f(1e4), None) == bi.BI_ERR_UNSUPPORTED
+    assert L.bi_rope(d, 128, 1, 2, 64, d, None, 1, f(0.0), None) == bi.BI_ERR_INVALID_ARG
+    assert L.bi_rope(d, 128, 2, 2, 64, d, None, 1, f(1e4), None) == bi.BI_ERR_INVALID_ARG
+    assert L.bi_rope(d, 64, 1, 2, 64, d, None, 1, f(1e4), None) == bi.BI_ERR_INVALID_ARG
+    assert L.bi_rope(d, 128, 1, 2, 64, d, None, 0, f(1e4), None) == bi.BI_ERR_INVALID_ARG
+    # swiglu: stride < inter, inter not a multiple of 8
+    assert L.bi_swiglu(d, 8, d, 16, d, 16, 1, 16, None) == bi.BI_ERR_INVALID_ARG
+    assert L.bi_swiglu(d, 12, d, 12, d, 12, 1, 12, None) == bi.BI_ERR_UNSUPPORTED
+    # add: n < 0, misaligned
+    assert L.bi_add(d, d, d, -1, None) == bi.BI_ERR_INVALID_ARG
+    assert L.bi_add(d + 2, d, d, 8, None) == bi.BI_ERR_UNSUPPORTED
+    # argmax: n < 1, ld < n, ld not a multiple of 4
+    assert L.bi_argmax(d, 8, 1, 0, d, None) == bi.BI_ERR_INVALID_ARG
+    assert L.bi_argmax(d, 4, 1, 8, d, None) == bi.BI_ERR_INVALID_ARG
+    assert L.bi_argmax(d + 2, 10, 1, 10, d, None) == bi.BI_ERR_INVALID_ARG
+    assert "bi_argmax" in L.bi_last_error_message().decode()
+    assert L.bi_argmax(d, 8, 0, 8, d, None) == bi.BI_OK  # rows = 0

@@ -1,0 +1,223 @@
+"""The greedy-trace workload on the GPU: a Llama-style decoder stack run through libbi.
+
+  * parity: a two-layer stack's logits at every step (token by token, then verify
+    blocks of 4 with drafted tokens) against the oracle's forward pass fed the same
+    tokens;
+  * invariance at full size: 8 Llama-3-8B-shaped layers, 8192-token contexts, 256
+    greedy steps -- the token traces are identical whether decoded token by token or
+    with verify blocks of 4, at batch 1, 8 and 32 ("Fix/speculative shape invariance",
+    section Problem; book chapter Case 5, the greedy token under several loads).
+"""
+import math
+import time
+
+import numpy as np
+import pytest
+import torch
+
+from invariant_bi_matmul_gb300 import inputs
+from tolerance import check_bf16, check_f32
+
+pytestmark = pytest.mark.gpu
+
+bi = pytest.importorskip("invariant_bi_matmul_gb300")
+from invariant_bi_matmul_gb300.decoder import (GreedyDecoder, lookup_drafter,  # noqa: E402
+                                               reference_drafter)
+
+
+@pytest.fixture(scope="module")
+def dev():
+    if not torch.cuda.is_available():
+        pytest.skip("no CUDA device")
+    return torch.device("cuda:0")
+
+
+# ---------------------------------------------------------------- parity (tiny)
+
+def _stack_rel_bound(cfg):
+    """Relative L2 bound for a stack's logits against the oracle's forward pass.  Both
+    sides store every activation in bf16; wherever their fp32 values differ by summation
+    order, a stored element may round to a neighbouring bf16 value (relative step
+    2^-8).  Each layer stores 15 activations (RMSNorm, q, k, v, rotated q and k,
+    attention, o, residual, RMSNorm, gate, up, SwiGLU, down, residual) and the final
+    RMSNorm one more; independent discrepancies add like a random walk."""
+    return 2.0 ** -8 * math.sqrt(15 * cfg.layers + 1)
+
+
+def _check_logits(gpu, ora, cfg, what):
+    g = gpu.double().cpu().numpy()
+    for r in range(ora.shape[0]):
+        rel = np.linalg.norm(g[r] - ora[r]) / np.linalg.norm(ora[r])
+        assert rel < _stack_rel_bound(cfg), f"{what}: row {r} relative L2 error {rel}"
+        # the greedy token agrees wherever the oracle's top two logits are further apart
+        # than twice the largest logit difference of the row
+        top2 = np.sort(ora[r])[-2:]
+        if top2[1] - top2[0] > 2 * np.abs(g[r] - ora[r]).max():
+            assert int(np.argmax(g[r])) == int(np.argmax(ora[r])), f"{what}: row {r}"
+
+
+def test_tiny_stack_matches_oracle_step_by_step(dev):
+    import oracle
+    from oracle.decoder import OracleDecoder
+
+    cfg, seed = inputs.TINY_DECODER, 501
+    w_cpu = inputs.decoder_weights(cfg, seed, std=0.05, norm_std=0.1)
+    w_dev = {k: v.to(dev) for k, v in w_cpu.items()}
+    B, width, max_len = 3, 4, cfg.context + 64
+    dec = GreedyDecoder(cfg, w_dev, max_batch=B, max_len=max_len, max_width=width,
+                        device=dev, page_seed=7)
+    ctx = {(s, l): inputs.decoder_context(cfg, s, l, seed) for s in range(B)
+           for l in range(cfg.layers)}
+    dec.start(list(range(B)), seed, context_fn=lambda s, l: ctx[(s, l)])
+
+    pps = math.ceil(max_len / 64)
+    od = OracleDecoder(cfg, {k: inputs.bf16_bits(v) for k, v in w_cpu.items()},
+                       num_pages=B * pps, block_table=np.arange(B * pps).reshape(B, pps))
+    for (s, l), (k, v) in ctx.items():
+        od.append_context(l, s, inputs.bf16_bits(k), inputs.bf16_bits(v))
+
+    def step(q_lens, drafts):
+        ids = []
+        for b in range(B):
+            ids += [dec.last[b]] + drafts[b]
+        lens = [dec.cached[b] + q_lens[b] for b in range(B)]
+        cu = np.concatenate([[0], np.cumsum(q_lens)])
+        greedy = dec.forward(ids, q_lens).tolist()
+        want = od.forward(ids, lens, cu)
+        _check_logits(dec.logits[:len(ids)], want.astype(np.float64), cfg, f"block {q_lens}")
+        assert greedy == [oracle.argmax_f32(r) for r in dec.logits[:len(ids)].cpu().numpy()]
+        for b in range(B):  # greedy acceptance, as GreedyDecoder.speculate applies it
+            gb = greedy[cu[b]:cu[b + 1]]
+            n = 0
+            while n < q_lens[b] - 1 and drafts[b][n] == gb[n]:
+                n += 1
+            dec.cached[b] += n + 1
+            dec.last[b] = gb[n]
+
+    for _ in range(4):
+        step([1] * B, [[] for _ in range(B)])
+    for s in range(3):
+        step([width] * B, [[(7 * b + s) % cfg.vocab, 5, 5] for b in range(B)])
+    step([1, width, 2], [[], [1, 2, 3], [9]])            # ragged block widths
+    assert bi.device_status() == bi.BI_OK
+
+
+def test_tiny_stack_each_operation_matches_oracle(dev):
+    """Every operation of one verify block, fed the GPU's own inputs, against the same
+    oracle operation: the per-kernel tolerance holds at each step of the stack."""
+    import oracle
+
+    cfg, seed = inputs.TINY_DECODER, 504
+    w = inputs.decoder_weights(cfg, seed, std=0.05, norm_std=0.1)
+    wd = {k: v.to(dev) for k, v in w.items()}
+    wb = {k: inputs.bf16_bits(v) for k, v in w.items()}
+    bits = inputs.bf16_bits
+    dec = GreedyDecoder(cfg, wd, max_batch=2, max_len=cfg.context + 8, max_width=4, device=dev)
+    dec.start([0, 1], seed)
+    ids, lens, cu = [dec.last[0], dec.last[1], 3, 4, 5], [cfg.context + 1, cfg.context + 4], [0, 1, 5]
+    T = len(ids)
+    sl = torch.tensor(lens, dtype=torch.int32, device=dev)
+    cq = torch.tensor(cu, dtype=torch.int32, device=dev)
+    pos = oracle.positions(np.array(lens), np.array(cu))
+    h = bi.embedding(wd["embed"], torch.tensor(ids, dtype=torch.int32, device=dev))
+    assert np.array_equal(bits(h), wb["embed"][ids])
+    for i in range(cfg.layers):
+        p = f"l{i}."
+        x = bi.rmsnorm(h, wd[p + "attn_norm"], cfg.eps)
+        check_bf16(x, oracle.rmsnorm(bits(h), wb[p + "attn_norm"], cfg.eps), "rmsnorm")
+        q, k, v = (bi.matmul(x, wd[p + n]) for n in ("wq", "wk", "wv"))
+        for n, y in (("wq", q), ("wk", k), ("wv", v)):
+            check_bf16(y, oracle.matmul(bits(x), wb[p + n], oracle.W_NK), n)
+        q3, k3 = q.view(T, cfg.heads, -1), k.view(T, cfg.kv_heads, -1)
+        v3 = v.view(T, cfg.kv_heads, -1)
+        want_q, want_k = oracle.rope(bits(q3), pos, cfg.theta), oracle.rope(bits(k3), pos, cfg.theta)
+        bi.rope(q3, sl, cq, cfg.theta)
+        bi.rope(k3, sl, cq, cfg.theta)
+        check_bf16(q3, want_q, "rope q")
+        check_bf16(k3, want_k, "rope k")
+        bt = dec.block_table[:2]
+        kc_before = dec.k_cache[i].clone()
+        bi.kv_append(k3, v3, dec.k_cache[i], dec.v_cache[i], bt, sl, cq)
+        btn, sln, cun = bt.cpu().numpy(), np.array(lens, np.int32), np.array(cu, np.int32)
+        kco, _ = oracle.kv_append(bits(k3), bits(v3), bits(kc_before), bits(kc_before), btn, sln,
+                                  cun, 64)
+        assert np.array_equal(bits(dec.k_cache[i]), kco)
+        a, _ = bi.verify_block(q3, dec.k_cache[i], dec.v_cache[i], bt, sl, cq, max_q=4,
+                               max_seq_len=max(lens), scale=1 / math.sqrt(cfg.head_dim))
+        ao, _ = oracle.attention(bits(q3), bits(dec.k_cache[i]), bits(dec.v_cache[i]), btn, sln,
+                                 cun, cfg.heads, 1 / math.sqrt(cfg.head_dim))
+        check_bf16(a, ao, "attention")
+        o = bi.matmul(a.view(T, -1), wd[p + "wo"])
+        check_bf16(o, oracle.matmul(bits(a.view(T, -1)), wb[p + "wo"], oracle.W_NK), "wo")
+        h2 = bi.add(h, o)
+        assert np.array_equal(bits(h2), oracle.to_bf16(oracle.add(bits(h), bits(o)))), "add"
+        h = h2
+        x = bi.rmsnorm(h, wd[p + "mlp_norm"], cfg.eps)
+        g, u = bi.matmul(x, wd[p + "w_gate"]), bi.matmul(x, wd[p + "w_up"])
+        act = bi.swiglu(g, u)
+        check_bf16(act, oracle.swiglu(bits(g), bits(u)), "swiglu")
+        d = bi.matmul(act, wd[p + "w_down"])
+        check_bf16(d, oracle.matmul(bits(act), wb[p + "w_down"], oracle.W_NK), "w_down")
+        h = bi.add(h, d)
+    x = bi.rmsnorm(h, wd["final_norm"], cfg.eps)
+    logits = bi.matmul(x, wd["lm_head"], out_dtype=torch.float32)
+    xw = oracle.bf16_widen(bits(x)).astype(np.float64)
+    scale = np.abs(xw) @ np.abs(oracle.bf16_widen(wb["lm_head"]).astype(np.float64)).T
+    check_f32(logits, oracle.matmul(bits(x), wb["lm_head"], oracle.W_NK), scale, "lm head")
+    assert bi.argmax(logits).tolist() == [oracle.argmax_f32(r) for r in logits.cpu().numpy()]
+    assert bi.device_status() == bi.BI_OK
+
+
+# ----------------------------------------------------------- invariance (tiny)
+
+def test_tiny_traces_identical_across_batch_and_width(dev):
+    cfg, seed, steps = inputs.TINY_DECODER, 502, 48
+    w = inputs.decoder_weights(cfg, seed, device=dev, std=0.05, norm_std=0.1)
+    dec = GreedyDecoder(cfg, w, max_batch=5, max_len=cfg.context + 2 * steps + 8, max_width=4,
+                        device=dev)
+    dec.start(range(5), seed)
+    ref = dec.decode(steps)
+    for B in (1, 2, 5):
+        dec.start(range(B), seed)
+        assert dec.decode(steps) == ref[:B]
+        for width, drafter in ((4, reference_drafter(ref, 3, cfg.vocab)), (2, lookup_drafter),
+                               (4, lookup_drafter)):
+            dec.start(range(B), seed)
+            traces, _, _ = dec.speculate(steps, width, drafter)
+            assert traces == ref[:B], (B, width)
+    assert bi.device_status() == bi.BI_OK
+
+
+# ------------------------------------------------- invariance (Llama-3-8B, 8 layers)
+
+def test_llama3_8b_8_layer_greedy_traces_identical(dev):
+    cfg, seed, steps, width = inputs.LLAMA3_8B_8L, 503, 256, 4
+    w = inputs.decoder_weights(cfg, seed, device=dev)
+    dec = GreedyDecoder(cfg, w, max_batch=32, max_len=cfg.context + 2 * steps + 2 * width,
+                        max_width=width, device=dev, page_seed=11)
+    report = {}
+
+    def run(B, mode, drafter=None):
+        dec.start(range(B), seed)
+        torch.cuda.synchronize()
+        t0 = time.perf_counter()
+        if mode == "token":
+            traces, blocks, acc = dec.decode(steps), steps, 0
+        else:
+            traces, blocks, acc = dec.speculate(steps, width, drafter)
+        report[(B, mode)] = (round(time.perf_counter() - t0, 2), blocks, acc)
+        return traces
+
+    ref = run(32, "token")
+    assert len({tuple(t) for t in ref}) > 1          # sequences decode different traces
+    assert run(8, "token") == ref[:8]
+    assert run(1, "token") == ref[:1]
+    drafter = reference_drafter(ref, 5, cfg.vocab)
+    for B in (32, 8, 1):
+        assert run(B, "verify4", drafter) == ref[:B], B
+    assert run(8, "verify4-lookup", lookup_drafter) == ref[:8]
+    assert bi.device_status() == bi.BI_OK
+    # blocks ended both by accepted and by rejected drafts
+    blocks32, acc32 = report[(32, "verify4")][1:]
+    assert 0 < acc32 < blocks32 * (width - 1) * 32
+    print("greedy-trace runs (seconds, blocks, accepted drafts):", report)
