@@ -14,21 +14,28 @@
 // Reduction tree of one (query, head) -- a function of the query's position only:
 //   * keys are cut into chunks of CHUNK = 512 counted from key 0; the query uses chunks
 //     0 .. pos/CHUNK (keys after pos are masked to -inf, so p = +0 exactly);
-//   * inside a chunk, 64-key pages 0,2,4,6 are folded by one warp and pages 1,3,5,7 by
-//     another, each with an online softmax (running max, exp2 rescale), scores and P.V
-//     on the tensor cores (mma.m16n8k16, bf16 in, fp32 accumulate) in a fixed order;
-//     the two warp states are then combined, even-page warp first;
+//   * per 64-key page, the scores S = Q K^T come from tcgen05 MMAs (bf16 in, fp32
+//     accumulate in tensor memory; head-dim steps of 16 in ascending order);
+//   * the chunk's pages are folded in ascending order with an online softmax against a
+//     reference max m that is raised only when a page's row max exceeds it by more than
+//     2^8 (then O and the row sums are rescaled by exp2(m_old - m_new)); P = exp2(S - m)
+//     is rounded to bf16 and O += P V accumulates in tensor memory (tcgen05, the page's
+//     keys in 16-key steps, ascending); each of four warps sums its 16-key slice of the
+//     row key by key, and the four slice sums are added in ascending slice order;
 //   * chunk partials (m, l, o) are merged by the merge kernel: eight contiguous chunk
 //     ranges, each folded in ascending order, then combined in ascending range order --
 //     a tree fixed by the number of chunks, i.e. by the query's position.
-// A query's row position inside the MMA tile, the number of other queries, sequences,
-// or keys beyond pos change none of these steps.
+// A query's row inside the MMA tile, the number of other queries, sequences, or keys
+// beyond pos change none of these steps.
 //
-// Data movement: one persistent CTA per SM; a producer warp streams K and V pages with
-// TMA (2D tensor maps over the cache viewed as [pages*Hkv*PAGE, D], 128-byte swizzle)
-// into a 5-deep shared-memory ring; four consumer warps (2 M-tiles x 2 page parities)
-// walk every stage in order and compute on the pages of their parity.  Work items (sequence, KV head, chunk) are enumerated on the device
-// from seq_lens, so mixed-length batches launch no idle CTAs.
+// Data movement: one persistent CTA of seven warps per SM.  Warp 5 streams K and V pages
+// with TMA (2D tensor maps over the cache viewed as [pages*Hkv*PAGE, D], 128-byte
+// swizzle) into a shared-memory ring; warp 6 issues the MMAs (S into a double-buffered
+// tensor-memory tile, then P V into a per-item fp32 O accumulator, double-buffered);
+// warps 0..3 run the softmax, each on a 16-key slice of every page (the <= 32 query rows
+// are repeated in each of the four tensor-memory lane quarters); warp 4 reads each
+// finished O out and writes the chunk partial while the next item runs.  Work items (sequence, KV head, chunk) are
+// enumerated on the device from seq_lens, so mixed-length batches launch no idle CTAs.
 #include "common.cuh"
 #include "launch.h"
 #include "tmap.h"
@@ -41,39 +48,55 @@ constexpr int PAGE = 64;
 constexpr int CHUNK = 512;
 constexpr int PAGES_PER_CHUNK = CHUNK / PAGE;
 constexpr int MAXR = 32;       // query rows per (sequence, KV head): q_len * group size
-constexpr int NCONS = 4;       // consumer warps
-constexpr int THREADS = (NCONS + 1) * 32;
-constexpr int NST = 5;         // page stages in the ring
+constexpr int NSM = 4;         // softmax warps 0..3, one per tensor-memory lane quarter
+constexpr int KSL = PAGE / NSM;  // keys of a page per softmax warp
+constexpr int EPILOGUE = NSM;  // reads O (lanes 0..31: a warp whose index is 0 mod 4)
+constexpr int PRODUCER = NSM + 1, MMA_WARP = NSM + 2;
+constexpr int THREADS = (NSM + 3) * 32;
+constexpr int MMA_M = 128;     // instruction rows: Q rows repeated once per lane quarter
+constexpr int TMEM_COLS = 512;
+constexpr float kRescaleLog2 = 8.0f;  // rescale O only when the row max grows by > 2^8
 constexpr int MAX_BATCH = BI_ATTN_MAX_BATCH;
 constexpr float kLog2e = 1.4426950408889634f;
 constexpr float kLn2 = 0.6931471805599453f;
 
 static_assert(CHUNK % PAGE == 0, "chunk must hold whole pages");
+static_assert(PAGE == 64 && KSL == 16, "a page is one 64-column S tile, 16 keys per warp");
+static_assert(NSM * MAXR == MMA_M, "one copy of the query rows per lane quarter");
+static_assert(EPILOGUE % 4 == 0, "the epilogue warp must own tensor-memory lanes 0..31");
 
 template <int D>
 struct Cfg {
+    static constexpr int NST = D == 64 ? 8 : 5;         // page stages in the ring
     static constexpr int BOXES = D / 64;                // 64-element (128 B) column boxes
     static constexpr int BOX_BYTES = PAGE * 128;        // one box of a page: 64 rows x 128 B
     static constexpr int PAGE_BYTES = BOXES * BOX_BYTES;
     static constexpr int STAGE_BYTES = 2 * PAGE_BYTES;  // K page + V page
-    static constexpr int QBOX_BYTES = MAXR * 128;
+    static constexpr int QBOX_BYTES = MMA_M * 128;      // 128 rows: the MAXR rows, 4 times
     static constexpr int Q_BYTES = BOXES * QBOX_BYTES;
-    static constexpr int NDN = D / 8;                   // 8-wide column tiles of O
-    static constexpr int COMB_O_BYTES = 2 * NDN * 32 * 16;
-    static constexpr int COMB_ML_BYTES = 2 * 32 * 16;
-    static constexpr size_t SMEM = 1024 + size_t(NST) * STAGE_BYTES + Q_BYTES + COMB_O_BYTES +
-                                   COMB_ML_BYTES + 2 * NST * 8 + NST * 4 + (MAX_BATCH + 1) * 4 +
-                                   64;
+    // P holds MAXR real rows.  An M = 128 MMA reads 128 rows (16 KB) from its base; rows
+    // >= MAXR only feed accumulator rows that are never read, so that read may run on
+    // into the ring, which follows and is larger than 16 KB.
+    static constexpr int P_BYTES = MAXR * 128;
+    static constexpr int RING_OFF = Q_BYTES + 2 * P_BYTES;
+    static constexpr int BAR_OFF = RING_OFF + NST * STAGE_BYTES;
+    static constexpr int NBARS = 2 * NST + 14 + 2;      // ring, 7 pairs, q_full, drain
+    static constexpr int XCH_OFF = BAR_OFF + NBARS * 8 + 16;
+    static constexpr int XCH_BYTES = 2 * (NSM + 1) * MAXR * 4;  // per item: sums, max
+    static constexpr size_t SMEM = 1024 + size_t(XCH_OFF) + XCH_BYTES + NST * 4 +
+                                   (MAX_BATCH + 1) * 4 + 3 * MAX_BATCH * 4 + 64;
+    static constexpr int S_COL = 0;                     // S buffers: columns [0,64), [64,128)
+    static constexpr int O_COL = 2 * PAGE;              // O buffers (by item): D columns each
+    static_assert(NST * STAGE_BYTES >= MMA_M * 128, "MMA over-reads must stay in the ring");
+    static_assert(O_COL + 2 * D <= TMEM_COLS, "tensor memory columns");
+    static_assert(RING_OFF % 1024 == 0 && BAR_OFF % 1024 == 0, "1024-byte aligned buffers");
+    static_assert(SMEM <= 232448, "shared memory per CTA");
 };
 
 // byte offset of (row, 16-byte chunk) in a 128-byte-swizzled box (the TMA SWIZZLE_128B
 // pattern: chunk index XOR row mod 8)
 __device__ __forceinline__ uint32_t swz(int row, int chunk) {
     return uint32_t(row) * 128u + (uint32_t((chunk ^ (row & 7)) & 7) << 4);
-}
-
-__device__ __forceinline__ void named_barrier_consumers() {
-    asm volatile("bar.sync 1, %0;" ::"n"(NCONS * 32) : "memory");
 }
 
 struct SeqInfo {
@@ -111,43 +134,75 @@ attn_partial_kernel(const __grid_constant__ CUtensorMap tmap_k,
                     float* __restrict__ ws_o, float* __restrict__ ws_ml, int maxC,
                     unsigned int* err) {
     using C = Cfg<D>;
+    constexpr int NST = C::NST;
     extern __shared__ uint8_t smem_raw[];
     uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) &
                                                ~uintptr_t(1023));
-    uint8_t* sStage = smem;
-    uint8_t* sQ = sStage + NST * C::STAGE_BYTES;
-    float4* comb_o = reinterpret_cast<float4*>(sQ + C::Q_BYTES);
-    float4* comb_ml = reinterpret_cast<float4*>(sQ + C::Q_BYTES + C::COMB_O_BYTES);
-    uint64_t* full = reinterpret_cast<uint64_t*>(sQ + C::Q_BYTES + C::COMB_O_BYTES +
-                                                 C::COMB_ML_BYTES);
+    uint8_t* sQ = smem;
+    uint8_t* sP = smem + C::Q_BYTES;                    // two P buffers
+    uint8_t* sStage = smem + C::RING_OFF;
+    uint64_t* full = reinterpret_cast<uint64_t*>(smem + C::BAR_OFF);
     uint64_t* empty = full + NST;
-    int* stage_valid = reinterpret_cast<int*>(empty + NST);
+    uint64_t* s_full = empty + NST;    // scores of page g in S buffer g&1
+    uint64_t* s_empty = s_full + 2;    // ... read by all softmax warps
+    uint64_t* p_full = s_empty + 2;    // P of page g in P buffer g&1 (all softmax warps)
+    uint64_t* p_empty = p_full + 2;    // P V of page g has completed (MMA commit)
+    uint64_t* o_full = p_empty + 2;    // item k's O (buffer k&1) is complete (MMA commit)
+    uint64_t* o_empty = o_full + 2;    // ... and read out by the epilogue warp
+    uint64_t* xs_bar = o_empty + 2;    // item k's row sums and max are in x_sum[k&1]
+    uint64_t* q_full = xs_bar + 2;
+    uint64_t* drain = q_full + 1;
+    uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(drain + 1);
+    float* x_sum = reinterpret_cast<float*>(smem + C::XCH_OFF);  // [2][NSM+1][MAXR]
+    int* stage_valid = reinterpret_cast<int*>(x_sum + 2 * (NSM + 1) * MAXR);
     int* prefix = stage_valid + NST;  // [B+1]
-    volatile int* abort_flag = prefix + MAX_BATCH + 1;
+    int* seq_len = prefix + MAX_BATCH + 1;   // per sequence: length, first token, block width
+    int* seq_t0 = seq_len + MAX_BATCH;
+    int* seq_qb = seq_t0 + MAX_BATCH;
+    volatile int* abort_flag = seq_qb + MAX_BATCH;
 
     const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
     const int G = Hq / Hkv;
 
+    if (warp == MMA_WARP) {  // the MMA warp owns the tensor memory
+        tmem_alloc(tmem_slot, TMEM_COLS);
+        tmem_relinquish();
+    }
     pdl_wait();
     pdl_trigger();
     if (tid == 0) {
-        for (int s = 0; s < NST; ++s) {
-            mbar_init(&full[s], 1);
-            // every consumer warp releases every stage (also pages of the other parity),
-            // so no warp can run a full ring cycle ahead and alias an mbarrier phase
-            mbar_init(&empty[s], NCONS);
+        for (int i = 0; i < NST; ++i) {
+            mbar_init(&full[i], 1);
+            mbar_init(&empty[i], 1);   // released by the MMA warp's commit after P V
         }
+        for (int i = 0; i < 2; ++i) {
+            mbar_init(&s_full[i], 1);
+            mbar_init(&s_empty[i], NSM);
+            mbar_init(&p_full[i], NSM);
+            mbar_init(&p_empty[i], 1);
+            mbar_init(&o_full[i], 1);
+            mbar_init(&o_empty[i], 1);
+            mbar_init(&xs_bar[i], NSM);
+        }
+        mbar_init(q_full, NSM);
+        mbar_init(drain, 1);
         *abort_flag = 0;
         fence_barrier_init();
     }
     // work items per sequence: chunks x KV heads (0 for a malformed sequence)
+    // (kept in shared memory: every warp decodes every item from them)
     for (int b = tid; b < B; b += THREADS) {
-        const SeqInfo s = seq_info(seq_lens, cu_q, b);
-        const bool ok = seq_ok(s, max_q, max_seq_len, total_q);
+        const SeqInfo si = seq_info(seq_lens, cu_q, b);
+        const bool ok = seq_ok(si, max_q, max_seq_len, total_q);
         if (!ok) latch_error(err, kErrDeviceArg);
-        prefix[b + 1] = ok ? ((s.L + CHUNK - 1) / CHUNK) * Hkv : 0;
+        prefix[b + 1] = ok ? ((si.L + CHUNK - 1) / CHUNK) * Hkv : 0;
+        seq_len[b] = si.L;
+        seq_t0[b] = si.t0;
+        seq_qb[b] = si.qb;
     }
+    tc_fence_before_sync();
     __syncthreads();
+    tc_fence_after_sync();
     if (warp == 0) {  // inclusive scan of prefix[1..B], 32 at a time
         int carry = 0;
         for (int base = 0; base < B; base += 32) {
@@ -165,6 +220,7 @@ attn_partial_kernel(const __grid_constant__ CUtensorMap tmap_k,
     }
     __syncthreads();
     const int total = prefix[B];
+    const uint32_t tmem_base = *tmem_slot;
 
     auto decode = [&](int w, int& b, int& c, int& h) {
         int lo = 0, hi = B;
@@ -177,8 +233,29 @@ attn_partial_kernel(const __grid_constant__ CUtensorMap tmap_k,
         c = r / Hkv;
         h = r - c * Hkv;
     };
+    auto seq_of = [&](int b) {
+        SeqInfo si;
+        si.L = seq_len[b];
+        si.t0 = seq_t0[b];
+        si.qb = seq_qb[b];
+        return si;
+    };
+    auto pages_of = [&](const SeqInfo& si, int c) {
+        return min(PAGES_PER_CHUNK, (si.L - c * CHUNK + PAGE - 1) / PAGE);
+    };
+    auto give_up = [&]() {
+        if (!*abort_flag) {
+            *abort_flag = 1;
+            latch_error(err, kErrTimeout);
+        }
+    };
+    bool ok = true;
+    auto wait = [&](uint64_t* bar, uint32_t parity) {
+        if (ok && !mbar_wait_warp(bar, parity, abort_flag)) ok = false;
+        return ok;
+    };
 
-    if (warp == NCONS) {
+    if (warp == PRODUCER) {
         // ------------------------------------------------------------------ producer
         // The whole warp runs the loop (converged, warp-uniform state); one elected lane
         // reads the page index and issues the copies.
@@ -187,19 +264,13 @@ attn_partial_kernel(const __grid_constant__ CUtensorMap tmap_k,
             tma_prefetch_desc(&tmap_v);
         }
         uint32_t g = 0;
-        bool ok = true;
         for (int w = blockIdx.x; ok && w < total; w += gridDim.x) {
             int b, c, h;
             decode(w, b, c, h);
-            const SeqInfo si = seq_info(seq_lens, cu_q, b);
-            const int npages = min(PAGES_PER_CHUNK, (si.L - c * CHUNK + PAGE - 1) / PAGE);
+            const int npages = pages_of(seq_of(b), c);
             for (int i = 0; i < npages; ++i, ++g) {
                 const int s = int(g % NST);
-                const uint32_t ph = (g / NST) & 1u;
-                if (!mbar_wait_warp(&empty[s], ph ^ 1u, abort_flag)) {
-                    ok = false;
-                    break;
-                }
+                if (!wait(&empty[s], ((g / NST) & 1u) ^ 1u)) break;
                 if (elect_one()) {
                     const int pidx = c * PAGES_PER_CHUNK + i;
                     const int phys =
@@ -225,233 +296,317 @@ attn_partial_kernel(const __grid_constant__ CUtensorMap tmap_k,
             }
         }
         if (!ok) {
-            if (lane == 0 && !*abort_flag) {
-                *abort_flag = 1;
-                latch_error(err, kErrTimeout);
-            }
+            if (lane == 0) give_up();
             // copies already issued land before the CTA exits (bounded)
             for (int k = 1; k <= NST && k <= int(g); ++k) {
                 const uint32_t gg = g - k;
                 mbar_wait(&full[gg % NST], (gg / NST) & 1u, nullptr, 100000000ull);
             }
         }
-        return;  // the producer takes no part in the consumers' named barriers
-    }
-
-    // ---------------------------------------------------------------------- consumers
-    const int mt = warp & 1;   // M-tile: query rows 16*mt .. 16*mt+15
-    const int par = warp >> 1; // page parity folded by this warp
-    const int quad_row = lane >> 2;
-    const int quad_col = (lane & 3) * 2;
-    const uint32_t sQa = smem_addr(sQ);
-    uint32_t g = 0;
-    bool alive = true;
-
-    for (int w = blockIdx.x; w < total; w += gridDim.x) {
-        int b, c, h;
-        decode(w, b, c, h);
-        const SeqInfo si = seq_info(seq_lens, cu_q, b);
-        const int L = si.L, qb = si.qb;
-        const int npages = min(PAGES_PER_CHUNK, (L - c * CHUNK + PAGE - 1) / PAGE);
-        const int R = qb * G;
-        const bool active = alive && (mt * 16 < R);
-
-        // Q tile of (sequence b, KV head h): row r = j*G + gg, zero past R
-        named_barrier_consumers();
-        for (int idx = tid; idx < MAXR * (D / 8); idx += NCONS * 32) {
-            const int r = idx / (D / 8), ch = idx - r * (D / 8);
-            uint4 v = make_uint4(0, 0, 0, 0);
-            if (r < R) {
-                const int j = r / G, gg = r - j * G;
-                const int64_t off = (int64_t(si.t0 + j) * Hq + int64_t(h) * G + gg) * D + ch * 8;
-                v = *reinterpret_cast<const uint4*>(q + off);
+    } else if (warp == MMA_WARP) {
+        // ---------------------------------------------------------------- MMA issuer
+        // S(page) = Q K^T into S buffer (page & 1); O(item) += P V, issued one page behind
+        // S so the softmax of page i overlaps the scores of page i+1.
+        constexpr uint32_t idesc_s = umma_idesc_bf16(MMA_M, PAGE, 0, 0);  // K K-major
+        constexpr uint32_t idesc_pv = umma_idesc_bf16(MMA_M, 64, 0, 1);   // V N-major
+        const uint64_t q_desc0 = umma_smem_desc(smem_addr(sQ), 16, 1024, 2);
+        const uint64_t p_desc0 = umma_smem_desc(smem_addr(sP), 16, 1024, 2);
+        const uint64_t k_desc0 = umma_smem_desc(smem_addr(sStage), 16, 1024, 2);
+        const uint64_t v_desc0 =
+            umma_smem_desc(smem_addr(sStage + C::PAGE_BYTES), C::BOX_BYTES, 1024, 2);
+        auto issue_pv = [&](uint32_t gj, int item, bool first, bool last) {
+            const int s = int(gj % NST), pb = int(gj & 1u), ob = item & 1;
+            if (!wait(&p_full[pb], (gj >> 1) & 1u)) return;
+            // the O buffer of this item was read out for item-2
+            if (first && !wait(&o_empty[ob], (uint32_t(item >> 1) & 1u) ^ 1u)) return;
+            tc_fence_after_sync();
+            if (elect_one()) {
+                const uint64_t p_desc = p_desc0 + uint64_t((pb * C::P_BYTES) >> 4);
+                const uint64_t v_desc = v_desc0 + uint64_t((s * C::STAGE_BYTES) >> 4);
+                const uint32_t o_tmem = tmem_base + uint32_t(C::O_COL + ob * D);
+#pragma unroll
+                for (int k = 0; k < PAGE / 16; ++k)      // keys 16k .. 16k+15: +32 B in P,
+#pragma unroll                                           // +16 rows (2 KB) in V
+                    for (int nh = 0; nh < C::BOXES; ++nh)
+                        tc_mma_bf16(o_tmem + uint32_t(nh * 64), p_desc + uint64_t(k * 2),
+                                    v_desc + uint64_t(nh * (C::BOX_BYTES >> 4) + k * 128),
+                                    idesc_pv, (first && k == 0) ? 0u : 1u);
+                tc_commit(&p_empty[pb]);
+                tc_commit(&empty[s]);   // K and V of the page are no longer read
+                if (last) tc_commit(&o_full[ob]);
             }
-            *reinterpret_cast<uint4*>(sQ + (ch >> 3) * C::QBOX_BYTES + swz(r, ch & 7)) = v;
+            __syncwarp();
+        };
+        // One stream over every page of every item of this CTA: S of page g, then P V of
+        // page g-1, so the next item's first scores are computed while the softmax
+        // finishes the previous item (its Q is published early, see the softmax warps).
+        uint32_t g = 0;
+        int item = 0;
+        bool have_prev = false;               // a P V is pending for page g-1
+        int prev_item = 0;
+        bool prev_first = false, prev_last = false;
+        for (int w = blockIdx.x; ok && w < total; w += gridDim.x, ++item) {
+            int b, c, h;
+            decode(w, b, c, h);
+            const int npages = pages_of(seq_of(b), c);
+            if (!wait(q_full, uint32_t(item) & 1u)) break;
+            for (int i = 0; i < npages; ++i) {
+                const uint32_t gi = g + uint32_t(i);
+                const int s = int(gi % NST), sb = int(gi & 1u);
+                if (!wait(&full[s], (gi / NST) & 1u) || !wait(&s_empty[sb], ((gi >> 1) & 1u) ^ 1u))
+                    break;
+                tc_fence_after_sync();
+                if (elect_one()) {
+                    const uint64_t k_desc = k_desc0 + uint64_t((s * C::STAGE_BYTES) >> 4);
+                    const uint32_t d = tmem_base + uint32_t(C::S_COL + sb * PAGE);
+#pragma unroll
+                    for (int bx = 0; bx < C::BOXES; ++bx)      // head dims 64bx .. 64bx+63
+#pragma unroll
+                        for (int k = 0; k < 4; ++k)            // in 16-wide steps: +32 B
+                            tc_mma_bf16(d, q_desc0 + uint64_t(bx * (C::QBOX_BYTES >> 4) + k * 2),
+                                        k_desc + uint64_t(bx * (C::BOX_BYTES >> 4) + k * 2),
+                                        idesc_s, (bx | k) != 0 ? 1u : 0u);
+                    tc_commit(&s_full[sb]);
+                }
+                __syncwarp();
+                if (have_prev) issue_pv(gi - 1u, prev_item, prev_first, prev_last);
+                if (!ok) break;
+                have_prev = true;
+                prev_item = item;
+                prev_first = i == 0;
+                prev_last = i == npages - 1;
+            }
+            g += uint32_t(npages);
         }
-        named_barrier_consumers();
-
-        const int rA = mt * 16 + quad_row, rB = rA + 8;
-        const int posA = rA < R ? L - qb + rA / G : -1;
-        const int posB = rB < R ? L - qb + rB / G : -1;
-        float m_run[2] = {-INFINITY, -INFINITY}, l_run[2] = {0.f, 0.f};
-        float o[C::NDN][4];
+        if (ok && have_prev) issue_pv(g - 1u, prev_item, prev_first, prev_last);
+        if (!ok && lane == 0) give_up();
+        // every MMA this warp issued completes before tensor memory is released
+        if (elect_one()) tc_commit(drain);
+        __syncwarp();
+        mbar_wait(drain, 0, nullptr, 100000000ull);
+    } else if (warp == EPILOGUE) {
+        // ------------------------------------------------------------------ epilogue
+        // Item k's O (tensor-memory lanes 0..31, buffer k&1) and its row sums and max,
+        // written as the chunk partial (m, l, o) of every row that sees the chunk.  The
+        // softmax warps move on to the next item meanwhile.
+        const int r = lane;
+        int item = 0;
+        for (int w = blockIdx.x; ok && w < total; w += gridDim.x, ++item) {
+            int b, c, h;
+            decode(w, b, c, h);
+            const SeqInfo si = seq_of(b);
+            const int R = si.qb * G;
+            const int j = r / G, gg = r - (r / G) * G;
+            const int pos = r < R ? si.L - si.qb + j : -1;
+            const int ob = item & 1;
+            const uint32_t par = uint32_t(item >> 1) & 1u;
+            if (!wait(&xs_bar[ob], par) || !wait(&o_full[ob], par)) break;
+            tc_fence_after_sync();
+            const float* xs = x_sum + ob * ((NSM + 1) * MAXR);
+            const float l_tot = ((xs[r] + xs[MAXR + r]) + xs[2 * MAXR + r]) + xs[3 * MAXR + r];
+            const float m_ref = xs[NSM * MAXR + r];
+            const bool store = r < R && pos >= c * CHUNK;
+            const int64_t idx = (int64_t(si.t0 + j) * Hq + int64_t(h) * G + gg) * maxC + c;
+            float4* dst = reinterpret_cast<float4*>(ws_o + idx * D);
 #pragma unroll
-        for (int dn = 0; dn < C::NDN; ++dn) o[dn][0] = o[dn][1] = o[dn][2] = o[dn][3] = 0.f;
-
-        for (int i = 0; i < npages; ++i) {
-            const uint32_t gi = g + i;
-            const int s = int(gi % NST);
-            if (alive && !mbar_wait_warp(&full[s], (gi / NST) & 1u, abort_flag)) {
-                alive = false;
-                if (!*abort_flag) {
-                    *abort_flag = 1;
-                    latch_error(err, kErrTimeout);
+            for (int cc = 0; cc < D / 32; ++cc) {
+                uint32_t v[32];
+                tmem_load_32x32b_x32_sync(tmem_base + uint32_t(C::O_COL + ob * D + cc * 32), v);
+                if (store) {
+#pragma unroll
+                    for (int k = 0; k < 32; k += 4)
+                        dst[(cc * 32 + k) / 4] =
+                            make_float4(__uint_as_float(v[k]), __uint_as_float(v[k + 1]),
+                                        __uint_as_float(v[k + 2]), __uint_as_float(v[k + 3]));
                 }
             }
-            if ((i & 1) == par && active && alive && stage_valid[s]) {
-                const int page_base = c * CHUNK + i * PAGE;
-                const uint32_t kb = smem_addr(sStage + s * C::STAGE_BYTES);
-                const uint32_t vb = kb + C::PAGE_BYTES;
-                // ---- S = Q K^T (16 rows x 64 keys), fp32
-                float sc[8][4];
+            tc_fence_before_sync();
+            __syncwarp();
+            if (lane == 0) mbar_arrive(&o_empty[ob]);
+            if (store) *reinterpret_cast<float2*>(ws_ml + idx * 2) = make_float2(m_ref, l_tot);
+        }
+        if (!ok && lane == 0) give_up();
+    } else if (warp < NSM) {
+        // ------------------------------------------------------------------- softmax
+        // Warp sw (0..3) reads tensor-memory lanes 32sw .. 32sw+31, which hold a copy of
+        // the query rows (row r = lane, so each warp sees every score of the row), and
+        // owns keys 16sw .. 16sw+15 of every page: its slice of each P row, its slice of
+        // the row sum.  The four warps compute the same reference max m, so their P
+        // slices form one P row and one MMA accumulates the whole O in lanes 0..31.
+        const int sw = warp;
+        const int r = lane;
+        uint32_t g = 0;
+        int item = 0;
+        int q_b = -1, q_h = -1;  // (sequence, KV head) whose Q tile sQ holds
+        const uint32_t lane_base = uint32_t(32 * sw) << 16;
+        // Q tile of item w, (b, h): rows 32sw + r hold query row r = j*G + gg (zero past
+        // R); rewritten only when (b, h) changes.  Item w+grid's tile is published as
+        // soon as this warp has read the scores of item w's last page: every MMA that
+        // read the old tile has completed by then.
+        auto publish_q = [&](int wq) {
+            if (wq < total) {
+                int b, c, h;
+                decode(wq, b, c, h);
+                if (b != q_b || h != q_h) {
+                    const SeqInfo si = seq_of(b);
+                    const int R = si.qb * G;
+                    const int j = r / G, gg = r - (r / G) * G;
+                    const __nv_bfloat16* src =
+                        q + (int64_t(si.t0 + j) * Hq + int64_t(h) * G + gg) * D;
 #pragma unroll
-                for (int nt = 0; nt < 8; ++nt) sc[nt][0] = sc[nt][1] = sc[nt][2] = sc[nt][3] = 0.f;
-#pragma unroll
-                for (int kk = 0; kk < D / 16; ++kk) {
-                    uint32_t a[4];
-                    {
-                        const int r = mt * 16 + (lane & 7) + ((lane >> 3) & 1) * 8;
-                        const int dch = kk * 2 + (lane >> 4);
-                        ldmatrix_x4(sQa + (dch >> 3) * C::QBOX_BYTES + swz(r, dch & 7), a[0], a[1],
-                                    a[2], a[3]);
+                    for (int ch = 0; ch < D / 8; ++ch) {
+                        uint4 v = make_uint4(0, 0, 0, 0);
+                        if (r < R) v = *reinterpret_cast<const uint4*>(src + ch * 8);
+                        *reinterpret_cast<uint4*>(sQ + (ch >> 3) * C::QBOX_BYTES +
+                                                  swz(32 * sw + r, ch & 7)) = v;
                     }
-#pragma unroll
-                    for (int np = 0; np < 4; ++np) {
-                        const int mi = lane >> 3;
-                        const int key = np * 16 + (lane & 7) + (mi >> 1) * 8;
-                        const int dch = kk * 2 + (mi & 1);
-                        uint32_t b0, b1, b2, b3;
-                        ldmatrix_x4(kb + (dch >> 3) * C::BOX_BYTES + swz(key, dch & 7), b0, b1, b2,
-                                    b3);
-                        mma_bf16_16816(sc[2 * np], a, b0, b1);
-                        mma_bf16_16816(sc[2 * np + 1], a, b2, b3);
-                    }
-                }
-                // ---- scale (log2 domain), causal mask, row max
-                float mx[2] = {-INFINITY, -INFINITY};
-#pragma unroll
-                for (int nt = 0; nt < 8; ++nt) {
-#pragma unroll
-                    for (int e = 0; e < 4; ++e) {
-                        const int key = page_base + nt * 8 + quad_col + (e & 1);
-                        const int pos = e < 2 ? posA : posB;
-                        const float v = key <= pos ? sc[nt][e] * scale_log2 : -INFINITY;
-                        sc[nt][e] = v;
-                        mx[e >> 1] = fmaxf(mx[e >> 1], v);
-                    }
-                }
-                float alpha[2], m_use[2];
-#pragma unroll
-                for (int hh = 0; hh < 2; ++hh) {
-                    mx[hh] = fmaxf(mx[hh], __shfl_xor_sync(0xffffffffu, mx[hh], 1));
-                    mx[hh] = fmaxf(mx[hh], __shfl_xor_sync(0xffffffffu, mx[hh], 2));
-                    const float m_new = fmaxf(m_run[hh], mx[hh]);
-                    m_use[hh] = m_new == -INFINITY ? 0.f : m_new;
-                    alpha[hh] = exp2f(m_run[hh] - m_use[hh]);
-                    m_run[hh] = m_new;
-                }
-                // ---- p = exp2(s - m), row sums in a fixed order, P packed to bf16
-                float ps[2] = {0.f, 0.f};
-                uint32_t pa[8][2];
-#pragma unroll
-                for (int nt = 0; nt < 8; ++nt) {
-                    const float p0 = exp2f(sc[nt][0] - m_use[0]);
-                    const float p1 = exp2f(sc[nt][1] - m_use[0]);
-                    const float p2 = exp2f(sc[nt][2] - m_use[1]);
-                    const float p3 = exp2f(sc[nt][3] - m_use[1]);
-                    ps[0] = ps[0] + p0;
-                    ps[0] = ps[0] + p1;
-                    ps[1] = ps[1] + p2;
-                    ps[1] = ps[1] + p3;
-                    pa[nt][0] = pack_bf16x2(p0, p1);
-                    pa[nt][1] = pack_bf16x2(p2, p3);
-                }
-#pragma unroll
-                for (int hh = 0; hh < 2; ++hh) {
-                    ps[hh] += __shfl_xor_sync(0xffffffffu, ps[hh], 1);
-                    ps[hh] += __shfl_xor_sync(0xffffffffu, ps[hh], 2);
-                    l_run[hh] = l_run[hh] * alpha[hh] + ps[hh];
-                }
-#pragma unroll
-                for (int dn = 0; dn < C::NDN; ++dn) {
-                    o[dn][0] *= alpha[0];
-                    o[dn][1] *= alpha[0];
-                    o[dn][2] *= alpha[1];
-                    o[dn][3] *= alpha[1];
-                }
-                // ---- O += P V (keys as K dimension); V rows past the sequence end are
-                // zeroed so unwritten cache slots cannot inject NaN/Inf through 0 * v
-                const bool tail = page_base + PAGE > L;
-#pragma unroll
-                for (int k2 = 0; k2 < 4; ++k2) {
-                    const uint32_t a[4] = {pa[2 * k2][0], pa[2 * k2][1], pa[2 * k2 + 1][0],
-                                           pa[2 * k2 + 1][1]};
-                    const int klo = page_base + k2 * 16 + quad_col;  // keys of b0 (b1: +8)
-#pragma unroll
-                    for (int dp = 0; dp < C::NDN / 2; ++dp) {
-                        const int mi = lane >> 3;
-                        const int key = k2 * 16 + (lane & 7) + (mi & 1) * 8;
-                        const int dch = dp * 2 + (mi >> 1);
-                        uint32_t b0, b1, b2, b3;
-                        ldmatrix_x4_trans(vb + (dch >> 3) * C::BOX_BYTES + swz(key, dch & 7), b0,
-                                          b1, b2, b3);
-                        if (tail) {
-                            const uint32_t m0 = (klo < L ? 0x0000ffffu : 0u) |
-                                                (klo + 1 < L ? 0xffff0000u : 0u);
-                            const uint32_t m1 = (klo + 8 < L ? 0x0000ffffu : 0u) |
-                                                (klo + 9 < L ? 0xffff0000u : 0u);
-                            b0 &= m0;
-                            b2 &= m0;
-                            b1 &= m1;
-                            b3 &= m1;
-                        }
-                        mma_bf16_16816(o[2 * dp], a, b0, b1);
-                        mma_bf16_16816(o[2 * dp + 1], a, b2, b3);
-                    }
+                    q_b = b;
+                    q_h = h;
+                    fence_proxy_async_smem();
                 }
             }
             __syncwarp();
-            if (lane == 0) mbar_arrive(&empty[s]);
-        }
-        g += npages;
+            if (lane == 0) mbar_arrive(q_full);  // one arrival per item (also the last)
+        };
+        publish_q(blockIdx.x);
+        for (int w = blockIdx.x; ok && w < total; w += gridDim.x, ++item) {
+            int b, c, h;
+            decode(w, b, c, h);
+            const SeqInfo si = seq_of(b);
+            const int L = si.L, qb = si.qb;
+            const int npages = pages_of(si, c);
+            const int R = qb * G;
+            const int pos = r < R ? L - qb + r / G : -1;
+            const int ob = item & 1;
 
-        // ---- combine the two page parities (even pages first) and write the partial
-        if (par == 1 && active) {
+            float m_ref = -INFINITY, l_run = 0.f;
+            for (int i = 0; i < npages && ok; ++i) {
+                const uint32_t gi = g + uint32_t(i);
+                const int s = int(gi % NST), sb = int(gi & 1u);
+                const uint32_t par = (gi >> 1) & 1u;
+                const int page0 = c * CHUNK + i * PAGE;  // first key of the page
+                // all 64 scores of the page, then release the S buffer
+                if (!wait(&s_full[sb], par)) break;
+                tc_fence_after_sync();
+                uint32_t sv[PAGE];
+                tmem_load_32x32b_x64_sync(tmem_base + lane_base + uint32_t(C::S_COL + sb * PAGE), sv);
+                tc_fence_before_sync();
+                __syncwarp();
+                if (lane == 0) mbar_arrive(&s_empty[sb]);
+                if (i == npages - 1) publish_q(w + gridDim.x);
+                // the stage's K/V landed before its scores were computed; this wait only
+                // orders the valid flag and the V rows zeroed below after the copy
+                if (!wait(&full[s], (gi / NST) & 1u)) break;
+                const bool valid = stage_valid[s] != 0;
+
+                // causal mask (masked keys -> -inf) and the row max over the page, taken on
+                // the raw scores with a fixed tree (exact: max does not round); scaling by
+                // the positive scale_log2 afterwards gives the max of the scaled scores
+                float sm[PAGE];
 #pragma unroll
-            for (int dn = 0; dn < C::NDN; ++dn)
-                comb_o[(mt * C::NDN + dn) * 32 + lane] = make_float4(o[dn][0], o[dn][1], o[dn][2],
-                                                                     o[dn][3]);
-            comb_ml[mt * 32 + lane] = make_float4(m_run[0], m_run[1], l_run[0], l_run[1]);
-        }
-        named_barrier_consumers();
-        if (par == 0 && active) {
-            const float4 mlB = comb_ml[mt * 32 + lane];
-            const float mB[2] = {mlB.x, mlB.y}, lB[2] = {mlB.z, mlB.w};
-            float wa[2], wb[2], mm[2], ll[2];
+                for (int k = 0; k < PAGE; ++k)
+                    sm[k] = (valid && page0 + k <= pos) ? __uint_as_float(sv[k]) : -INFINITY;
+                float mt[PAGE / 2];
 #pragma unroll
-            for (int hh = 0; hh < 2; ++hh) {
-                mm[hh] = fmaxf(m_run[hh], mB[hh]);
-                if (mm[hh] == -INFINITY) {
-                    wa[hh] = 0.f;
-                    wb[hh] = 0.f;
-                } else {
-                    wa[hh] = exp2f(m_run[hh] - mm[hh]);
-                    wb[hh] = exp2f(mB[hh] - mm[hh]);
+                for (int k = 0; k < PAGE / 2; ++k) mt[k] = fmaxf(sm[k], sm[k + PAGE / 2]);
+#pragma unroll
+                for (int width = PAGE / 4; width >= 1; width /= 2)
+#pragma unroll
+                    for (int k = 0; k < width; ++k) mt[k] = fmaxf(mt[k], mt[k + width]);
+                const float m_page = mt[0] * scale_log2;
+
+                // reference max: raised (and O, l rescaled) only when the page max exceeds
+                // it by more than 2^8, so p = exp2(s - m_ref) <= 2^8
+                const bool raise = m_page > m_ref + kRescaleLog2 ||
+                                   (m_ref == -INFINITY && m_page != -INFINITY);
+                const float factor = raise ? exp2f(m_ref - m_page) : 1.f;  // 0 on the first
+                if (raise) m_ref = m_page;
+                l_run *= factor;
+                // P buffer sb is free once P V of page gi-2 has completed
+                if (!wait(&p_empty[sb], par ^ 1u)) break;
+                if (sw == 0 && i > 0 && __any_sync(0xffffffffu, raise)) {
+                    // O (lanes 0..31) *= factor after P V of page gi-1 has completed
+                    const uint32_t gp = gi - 1u;
+                    if (!wait(&p_empty[gp & 1u], (gp >> 1) & 1u)) break;
+                    tc_fence_after_sync();
+#pragma unroll
+                    for (int cc = 0; cc < D / 32; ++cc) {
+                        uint32_t v[32];
+                        const uint32_t ta = tmem_base + uint32_t(C::O_COL + ob * D + cc * 32);
+                        tmem_load_32x32b_x32_sync(ta, v);
+#pragma unroll
+                        for (int k = 0; k < 32; ++k)
+                            v[k] = __float_as_uint(__uint_as_float(v[k]) * factor);
+                        tmem_store_32x32b_x32_sync(ta, v);
+                    }
+                    tc_fence_before_sync();
                 }
-                ll[hh] = l_run[hh] * wa[hh] + lB[hh] * wb[hh];
-            }
-            const int rows[2] = {rA, rB};
-            const int poss[2] = {posA, posB};
+                const float m_use = m_ref == -INFINITY ? 0.f : m_ref;
+                // this warp's 16 keys (selected with constant register indices); a masked
+                // key (-inf) gives p = +0
+                float sl[KSL];
 #pragma unroll
-            for (int hh = 0; hh < 2; ++hh) {
-                const int r = rows[hh];
-                if (r >= R || poss[hh] < c * CHUNK) continue;
-                const int j = r / G, gg = r - j * G;
-                const int64_t idx = (int64_t(si.t0 + j) * Hq + int64_t(h) * G + gg) * maxC + c;
-                float* dst = ws_o + idx * D + quad_col;
+                for (int k = 0; k < KSL; ++k) {
+                    float v = sm[k];
 #pragma unroll
-                for (int dn = 0; dn < C::NDN; ++dn) {
-                    const float4 ob = comb_o[(mt * C::NDN + dn) * 32 + lane];
-                    const float obv0 = hh == 0 ? ob.x : ob.z;
-                    const float obv1 = hh == 0 ? ob.y : ob.w;
-                    const float v0 = o[dn][2 * hh] * wa[hh] + obv0 * wb[hh];
-                    const float v1 = o[dn][2 * hh + 1] * wa[hh] + obv1 * wb[hh];
-                    *reinterpret_cast<float2*>(dst + dn * 8) = make_float2(v0, v1);
+                    for (int t = 1; t < NSM; ++t) v = sw == t ? sm[t * KSL + k] : v;
+                    sl[k] = v;
                 }
-                if ((lane & 3) == 0)
-                    *reinterpret_cast<float2*>(ws_ml + idx * 2) = make_float2(mm[hh], ll[hh]);
+                // p = exp2(s * scale_log2 - m), the row-slice sum by a fixed pairwise tree
+                float pv[KSL];
+#pragma unroll
+                for (int k = 0; k < KSL; ++k) pv[k] = exp2f(fmaf(sl[k], scale_log2, -m_use));
+                uint32_t pk[KSL / 2];
+#pragma unroll
+                for (int k = 0; k < KSL; k += 2) pk[k / 2] = pack_bf16x2(pv[k], pv[k + 1]);
+#pragma unroll
+                for (int width = KSL / 2; width >= 1; width /= 2)
+#pragma unroll
+                    for (int k = 0; k < width; ++k) pv[k] = pv[k] + pv[k + width];
+                const float ps = pv[0];
+                l_run = l_run + ps;
+                // this warp's 16 keys of P row r (two 16-byte pieces of the 128-byte row)
+                uint8_t* pbuf = sP + sb * C::P_BYTES;
+                *reinterpret_cast<uint4*>(pbuf + swz(r, 2 * sw)) =
+                    make_uint4(pk[0], pk[1], pk[2], pk[3]);
+                *reinterpret_cast<uint4*>(pbuf + swz(r, 2 * sw + 1)) =
+                    make_uint4(pk[4], pk[5], pk[6], pk[7]);
+                // V rows of this slice past the sequence end (or of an invalid page) are
+                // zeroed so unwritten cache slots cannot inject NaN/Inf through 0 * v
+                const int vend = valid ? L - page0 : 0;  // first row to zero
+                if (vend < (sw + 1) * KSL) {
+                    const int r0 = max(vend, sw * KSL);
+                    uint8_t* vst = sStage + s * C::STAGE_BYTES + C::PAGE_BYTES;
+                    const int n16 = ((sw + 1) * KSL - r0) * 8;  // 16-byte pieces per box
+                    for (int idx = lane; idx < C::BOXES * n16; idx += 32) {
+                        const int bx = idx / n16, rem = idx - bx * n16;
+                        *reinterpret_cast<uint4*>(vst + bx * C::BOX_BYTES + r0 * 128 + rem * 16) =
+                            make_uint4(0, 0, 0, 0);
+                    }
+                }
+                fence_proxy_async_smem();
+                __syncwarp();
+                if (lane == 0) mbar_arrive(&p_full[sb]);
             }
+            if (!ok) break;
+            g += uint32_t(npages);
+            // the slice sums (and the shared max) for the epilogue warp, once it has read
+            // this buffer's previous contents (item-2)
+            if (!wait(&o_empty[ob], (uint32_t(item >> 1) & 1u) ^ 1u)) break;
+            float* xs = x_sum + ob * ((NSM + 1) * MAXR);
+            xs[sw * MAXR + r] = l_run;
+            if (sw == 0) xs[NSM * MAXR + r] = m_ref;
+            __syncwarp();
+            if (lane == 0) mbar_arrive(&xs_bar[ob]);
         }
+        if (!ok && lane == 0) give_up();
+    }
+    // every warp is done with tensor memory and shared memory past this barrier
+    tc_fence_before_sync();
+    __syncthreads();
+    if (warp == MMA_WARP) {
+        tc_fence_after_sync();
+        tmem_dealloc(tmem_base, TMEM_COLS);
     }
 }
 
@@ -470,7 +625,7 @@ attn_merge_kernel(const int32_t* __restrict__ seq_lens, const int32_t* __restric
                   const float* __restrict__ ws_o, const float* __restrict__ ws_ml, int maxC,
                   __nv_bfloat16* __restrict__ out, float* __restrict__ lse) {
     constexpr int PER = D / 32;
-    constexpr int UNROLL = 4;
+    constexpr int UNROLL = 8;
     __shared__ float sM[MERGE_WARPS], sL[MERGE_WARPS];
     __shared__ float sO[MERGE_WARPS][D];
     pdl_wait();
@@ -496,6 +651,25 @@ attn_merge_kernel(const int32_t* __restrict__ seq_lens, const int32_t* __restric
     const int64_t base = (int64_t(t) * Hq + hq) * maxC;
     const int c0 = warp * nC / MERGE_WARPS, c1 = (warp + 1) * nC / MERGE_WARPS;
 
+    // The first UNROLL partials of the range are requested before the range max is
+    // reduced (they do not depend on it), so the two global round trips overlap.
+    auto load = [&](int c, float (&v)[PER], float2& ml) {
+        ml = *reinterpret_cast<const float2*>(ws_ml + (base + c) * 2);
+        const float* src = ws_o + (base + c) * D + lane * PER;
+        if (PER == 4) {
+            const float4 f = *reinterpret_cast<const float4*>(src);
+            v[0] = f.x; v[1 % PER] = f.y; v[2 % PER] = f.z; v[3 % PER] = f.w;
+        } else {
+            const float2 f = *reinterpret_cast<const float2*>(src);
+            v[0] = f.x; v[1 % PER] = f.y;
+        }
+    };
+    float v[UNROLL][PER];
+    float2 ml[UNROLL];
+#pragma unroll
+    for (int u = 0; u < UNROLL; ++u)
+        if (c0 + u < c1) load(c0 + u, v[u], ml[u]);
+
     // range max: lanes stride over chunks, then a butterfly (max is exact)
     float Mw = -INFINITY;
     for (int c = c0 + lane; c < c1; c += 32) Mw = fmaxf(Mw, ws_ml[(base + c) * 2]);
@@ -507,21 +681,10 @@ attn_merge_kernel(const int32_t* __restrict__ seq_lens, const int32_t* __restric
 #pragma unroll
     for (int i = 0; i < PER; ++i) acc[i] = 0.f;
     for (int c = c0; c < c1; c += UNROLL) {
-        float v[UNROLL][PER];
-        float2 ml[UNROLL];
+        if (c > c0) {
 #pragma unroll
-        for (int u = 0; u < UNROLL; ++u) {  // issue the loads of UNROLL chunks first
-            if (c + u < c1) {
-                ml[u] = *reinterpret_cast<const float2*>(ws_ml + (base + c + u) * 2);
-                const float* src = ws_o + (base + c + u) * D + lane * PER;
-                if (PER == 4) {
-                    const float4 f = *reinterpret_cast<const float4*>(src);
-                    v[u][0] = f.x; v[u][1 % PER] = f.y; v[u][2 % PER] = f.z; v[u][3 % PER] = f.w;
-                } else {
-                    const float2 f = *reinterpret_cast<const float2*>(src);
-                    v[u][0] = f.x; v[u][1 % PER] = f.y;
-                }
-            }
+            for (int u = 0; u < UNROLL; ++u)  // issue the loads of UNROLL chunks first
+                if (c + u < c1) load(c + u, v[u], ml[u]);
         }
 #pragma unroll
         for (int u = 0; u < UNROLL; ++u) {  // then fold them in ascending chunk order
