@@ -83,8 +83,10 @@ struct Cfg {
     static constexpr int NBARS = 2 * NST + 14 + 2;      // ring, 7 pairs, q_full, drain
     static constexpr int XCH_OFF = BAR_OFF + NBARS * 8 + 16;
     static constexpr int XCH_BYTES = 2 * (NSM + 1) * MAXR * 4;  // per item: sums, max
-    static constexpr size_t SMEM = 1024 + size_t(XCH_OFF) + XCH_BYTES + NST * 4 +
-                                   (MAX_BATCH + 1) * 4 + 3 * MAX_BATCH * 4 + 64;
+    static constexpr int EPI_STRIDE = 32 * 4 + 16;      // staged O row: 32 floats + pad
+    static constexpr size_t SMEM = 1024 + size_t(XCH_OFF) + XCH_BYTES + MAXR * EPI_STRIDE +
+                                   NST * 4 + (MAX_BATCH + 1) * 4 + 2 * MAX_BATCH * 4 +
+                                   MAX_BATCH + 64;
     static constexpr int S_COL = 0;                     // S buffers: columns [0,64), [64,128)
     static constexpr int O_COL = 2 * PAGE;              // O buffers (by item): D columns each
     static_assert(NST * STAGE_BYTES >= MMA_M * 128, "MMA over-reads must stay in the ring");
@@ -154,12 +156,13 @@ attn_partial_kernel(const __grid_constant__ CUtensorMap tmap_k,
     uint64_t* drain = q_full + 1;
     uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(drain + 1);
     float* x_sum = reinterpret_cast<float*>(smem + C::XCH_OFF);  // [2][NSM+1][MAXR]
-    int* stage_valid = reinterpret_cast<int*>(x_sum + 2 * (NSM + 1) * MAXR);
+    uint8_t* epi_stage = reinterpret_cast<uint8_t*>(x_sum + 2 * (NSM + 1) * MAXR);
+    int* stage_valid = reinterpret_cast<int*>(epi_stage + MAXR * C::EPI_STRIDE);
     int* prefix = stage_valid + NST;  // [B+1]
     int* seq_len = prefix + MAX_BATCH + 1;   // per sequence: length, first token, block width
     int* seq_t0 = seq_len + MAX_BATCH;
-    int* seq_qb = seq_t0 + MAX_BATCH;
-    volatile int* abort_flag = seq_qb + MAX_BATCH;
+    uint8_t* seq_qb = reinterpret_cast<uint8_t*>(seq_t0 + MAX_BATCH);
+    volatile int* abort_flag = reinterpret_cast<volatile int*>(seq_qb + MAX_BATCH);
 
     const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
     const int G = Hq / Hkv;
@@ -198,7 +201,7 @@ attn_partial_kernel(const __grid_constant__ CUtensorMap tmap_k,
         prefix[b + 1] = ok ? ((si.L + CHUNK - 1) / CHUNK) * Hkv : 0;
         seq_len[b] = si.L;
         seq_t0[b] = si.t0;
-        seq_qb[b] = si.qb;
+        seq_qb[b] = uint8_t(ok ? si.qb : 0);  // <= BI_ATTN_MAX_Q
     }
     tc_fence_before_sync();
     __syncthreads();
@@ -407,18 +410,30 @@ attn_partial_kernel(const __grid_constant__ CUtensorMap tmap_k,
             const float m_ref = xs[NSM * MAXR + r];
             const bool store = r < R && pos >= c * CHUNK;
             const int64_t idx = (int64_t(si.t0 + j) * Hq + int64_t(h) * G + gg) * maxC + c;
-            float4* dst = reinterpret_cast<float4*>(ws_o + idx * D);
-#pragma unroll
+            // O row r of 32 columns at a time: staged through shared memory (rows padded
+            // to 144 B, conflict-free) so that each store instruction writes four rows'
+            // 128-byte segments instead of 32 scattered 16-byte pieces
+            const int rr = lane >> 3, part = lane & 7;  // reader: row within 4, 16-B piece
+#pragma unroll 1
             for (int cc = 0; cc < D / 32; ++cc) {
                 uint32_t v[32];
                 tmem_load_32x32b_x32_sync(tmem_base + uint32_t(C::O_COL + ob * D + cc * 32), v);
-                if (store) {
 #pragma unroll
-                    for (int k = 0; k < 32; k += 4)
-                        dst[(cc * 32 + k) / 4] =
-                            make_float4(__uint_as_float(v[k]), __uint_as_float(v[k + 1]),
-                                        __uint_as_float(v[k + 2]), __uint_as_float(v[k + 3]));
+                for (int k = 0; k < 8; ++k)
+                    *reinterpret_cast<uint4*>(epi_stage + r * C::EPI_STRIDE + k * 16) =
+                        make_uint4(v[4 * k], v[4 * k + 1], v[4 * k + 2], v[4 * k + 3]);
+                __syncwarp();
+#pragma unroll
+                for (int k = 0; k < MAXR / 4; ++k) {
+                    const int row = 4 * k + rr;
+                    const bool st = __shfl_sync(0xffffffffu, store ? 1 : 0, row) != 0;
+                    const int64_t ridx = __shfl_sync(0xffffffffu, idx, row);
+                    if (st)
+                        *reinterpret_cast<uint4*>(ws_o + ridx * D + cc * 32 + part * 4) =
+                            *reinterpret_cast<const uint4*>(epi_stage + row * C::EPI_STRIDE +
+                                                           part * 16);
                 }
+                __syncwarp();
             }
             tc_fence_before_sync();
             __syncwarp();
