@@ -145,8 +145,10 @@ gemm_kernel(const __grid_constant__ CUtensorMap tmap_x, const __grid_constant__ 
     __syncthreads();
     tc_fence_after_sync();
     const uint32_t tmem_base = *tmem_slot;
-    // set-up above touches no global memory; from here on the previous grid must be done
-    pdl_wait();
+    // The set-up above touches no global memory.  The previous grid in the stream may
+    // still be running: the producer starts fetching W (which no kernel of this library
+    // writes) before it waits for that grid, and X only after; the epilogue waits before
+    // its first store; the MMA warp touches only shared and tensor memory.
     pdl_trigger();
 
     auto fail = [&]() {
@@ -162,9 +164,72 @@ gemm_kernel(const __grid_constant__ CUtensorMap tmap_x, const __grid_constant__ 
         bool ok = true;
         const uint32_t sA_s = smem_addr(sA), sB_s = smem_addr(sB), full_s = smem_addr(full);
         const uint32_t stage_a = uint32_t(kbs * a_bytes), stage_b = uint32_t(kbs * b_bytes);
-        const uint32_t blk_tx = uint32_t(a_bytes + b_bytes);
         const bool w_once = args.w_stream_once != 0;
         const bool blocked = args.blocked != 0;
+        // W blocks of K-blocks kb .. kb+kbs-1 of tile column n0 into stage `st`
+        auto issue_w = [&](uint32_t st, int n0, int kb, int nk) {
+            const uint32_t bar = full_s + st * 8u;
+            const uint32_t b_dst = sB_s + st * stage_b;
+            if (KN) {
+                // per swizzle atom (KN_ATOM_N columns) one box of 64*kbs k-rows
+                for (int c = 0; c < tile_n; c += KN_ATOM_N) {
+                    const uint32_t dst = b_dst + uint32_t(c / KN_ATOM_N) * uint32_t(kbs * KN_ATOM_BYTES);
+                    if (w_once)
+                        tma_load_2d_s_hint(dst, &tmap_w, bar, n0 + c, kb * BK, w_policy);
+                    else
+                        tma_load_2d_s(dst, &tmap_w, bar, n0 + c, kb * BK);
+                }
+            } else if (blocked) {
+                if (w_once)
+                    tma_load_3d_s_hint(b_dst, &tmap_w, bar, 0, n0, kb, w_policy);
+                else
+                    tma_load_3d_s(b_dst, &tmap_w, bar, 0, n0, kb);
+            } else {
+                for (int i = 0; i < nk; ++i) {
+                    const uint32_t dst = b_dst + uint32_t(i * b_bytes);
+                    if (w_once)
+                        tma_load_2d_s_hint(dst, &tmap_w, bar, (kb + i) * BK, n0, w_policy);
+                    else
+                        tma_load_2d_s(dst, &tmap_w, bar, (kb + i) * BK, n0);
+                }
+            }
+        };
+        // X blocks of K-blocks kb .. kb+kbs-1 of tile row m0 into stage `st`
+        auto issue_x = [&](uint32_t st, int m0, int kb, int nk) {
+            const uint32_t bar = full_s + st * 8u;
+            const uint32_t a_dst = sA_s + st * stage_a;
+            if (blocked) {
+                tma_load_3d_s(a_dst, &tmap_x, bar, 0, m0, kb);
+            } else {
+                for (int i = 0; i < nk; ++i)
+                    tma_load_2d_s(a_dst + uint32_t(i * a_bytes), &tmap_x, bar, (kb + i) * BK, m0);
+            }
+        };
+        // a rank-3 copy always delivers all kbs blocks (zeros past K), a rank-2 copy one
+        // block; N-major W boxes always span kbs blocks
+        auto stage_tx = [&](int nk) {
+            const int x_blocks = blocked ? kbs : nk;
+            const int w_blocks = (blocked || KN) ? kbs : nk;
+            return uint32_t(x_blocks * a_bytes + w_blocks * b_bytes);
+        };
+
+        // Before the previous grid is done: W of the first tile's first stages goes
+        // straight into the (empty) ring, so the weight stream overlaps the previous
+        // kernel's tail.
+        int early = 0;  // stages of the first tile whose W is already issued
+        if (int(blockIdx.x) < num_tiles) {
+            const int n0 = (int(blockIdx.x) % n_tiles) * tile_n;
+            for (int kb = 0; kb < nkb && early < S; kb += kbs, ++early) {
+                const int nk = nkb - kb < kbs ? nkb - kb : kbs;
+                if (elect_one()) {
+                    mbar_arrive_expect_tx_s(full_s + uint32_t(early) * 8u, stage_tx(nk));
+                    issue_w(uint32_t(early), n0, kb, nk);
+                }
+                __syncwarp();
+            }
+        }
+        pdl_wait();
+
         for (int t = blockIdx.x; ok && t < num_tiles; t += gridDim.x) {
             const int mt = t / n_tiles, nt = t % n_tiles;
             const int m0 = mt * BM, n0 = nt * tile_n;
@@ -174,44 +239,12 @@ gemm_kernel(const __grid_constant__ CUtensorMap tmap_x, const __grid_constant__ 
                     break;
                 }
                 if (elect_one()) {
-                    const uint32_t bar = full_s + stage * 8u;
                     const int nk = nkb - kb < kbs ? nkb - kb : kbs;  // K-blocks in this stage
-                    // a rank-3 copy always delivers all kbs blocks (zeros past K), a rank-2
-                    // copy one block; N-major W boxes always span kbs blocks
-                    const int x_blocks = blocked ? kbs : nk;
-                    const int w_blocks = (blocked || KN) ? kbs : nk;
-                    mbar_arrive_expect_tx_s(bar, uint32_t(x_blocks * a_bytes + w_blocks * b_bytes));
-                    const uint32_t a_dst = sA_s + stage * stage_a;
-                    const uint32_t b_dst = sB_s + stage * stage_b;
-                    if (blocked) {
-                        tma_load_3d_s(a_dst, &tmap_x, bar, 0, m0, kb);
-                    } else {
-                        for (int i = 0; i < nk; ++i)
-                            tma_load_2d_s(a_dst + uint32_t(i * a_bytes), &tmap_x, bar, (kb + i) * BK, m0);
+                    if (int(issued) >= early) {
+                        mbar_arrive_expect_tx_s(full_s + stage * 8u, stage_tx(nk));
+                        issue_w(stage, n0, kb, nk);
                     }
-                    if (KN) {
-                        // per swizzle atom (KN_ATOM_N columns) one box of 64*kbs k-rows
-                        for (int c = 0; c < tile_n; c += KN_ATOM_N) {
-                            const uint32_t dst = b_dst + uint32_t(c / KN_ATOM_N) * uint32_t(kbs * KN_ATOM_BYTES);
-                            if (w_once)
-                                tma_load_2d_s_hint(dst, &tmap_w, bar, n0 + c, kb * BK, w_policy);
-                            else
-                                tma_load_2d_s(dst, &tmap_w, bar, n0 + c, kb * BK);
-                        }
-                    } else if (blocked) {
-                        if (w_once)
-                            tma_load_3d_s_hint(b_dst, &tmap_w, bar, 0, n0, kb, w_policy);
-                        else
-                            tma_load_3d_s(b_dst, &tmap_w, bar, 0, n0, kb);
-                    } else {
-                        for (int i = 0; i < nk; ++i) {
-                            const uint32_t dst = b_dst + uint32_t(i * b_bytes);
-                            if (w_once)
-                                tma_load_2d_s_hint(dst, &tmap_w, bar, (kb + i) * BK, n0, w_policy);
-                            else
-                                tma_load_2d_s(dst, &tmap_w, bar, (kb + i) * BK, n0);
-                        }
-                    }
+                    issue_x(stage, m0, kb, nk);
                 }
                 __syncwarp();
                 ++issued;
@@ -307,6 +340,7 @@ gemm_kernel(const __grid_constant__ CUtensorMap tmap_x, const __grid_constant__ 
         mbar_wait(drain, 0, nullptr, 100000000ull);
     } else {
         // ------------------------------------------------------------------ epilogue
+        pdl_wait();  // Y may still be read by the previous grid
         const int quad = warp & 3;  // TMEM lanes 32*quad .. 32*quad+31
         const int row_in_tile = quad * 32 + lane;
         int local = 0;
