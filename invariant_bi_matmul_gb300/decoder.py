@@ -17,10 +17,11 @@ token the verify block computed at its position; the first mismatch is replaced 
 greedy token, which ends the step.
 
 Contexts: each sequence starts with ``cfg.context`` tokens already in its KV caches.
-There is no prefill path in the library, so those cache rows are synthetic -- seeded
-N(0,1) keys and values per (sequence, layer), written with bi_kv_append -- and the first
-decoded token is drawn per sequence.  Both depend only on the sequence id, never on the
-batch it runs in.
+``prefill`` computes them from a prompt through the same kernels, in causal blocks of up
+to 8 tokens (the widest verify block); ``start`` instead loads synthetic cache rows
+(seeded N(0,1) keys and values per sequence and layer, written with bi_kv_append), for
+small checks against the oracle.  Either way a sequence's context depends only on the
+sequence, never on the batch it runs in.
 """
 from __future__ import annotations
 
@@ -112,11 +113,13 @@ class GreedyDecoder:
                      [decoder_first_token(c, sid, seed) for sid in seq_ids])
 
     # ------------------------------------------------------------------- forward
-    def forward(self, ids: Sequence[int], q_lens: Sequence[int]) -> torch.Tensor:
+    def forward(self, ids: Sequence[int], q_lens: Sequence[int],
+                logits: bool = True) -> Optional[torch.Tensor]:
         """Runs one ragged block: sequence b contributes q_lens[b] tokens (its next input
         token first) at positions cached[b] .. cached[b]+q_lens[b]-1; their K/V are
         appended to the caches.  Returns the greedy tokens (device int32 [T]); the fp32
-        logits stay in ``self.logits[:T]``."""
+        logits stay in ``self.logits[:T]``.  With logits=False (prefill) the final norm,
+        LM head and argmax are skipped and None is returned."""
         c, w = self.cfg, self.w
         B = self.batch
         T = len(ids)
@@ -158,9 +161,50 @@ class GreedyDecoder:
             swiglu(g, u, out=a)
             matmul(a, w[p + "w_down"], out=o)
             add(h, o, out=h)
+        if not logits:
+            return None
         rmsnorm(h, w["final_norm"], c.eps, out=x)
         matmul(x, w["lm_head"], out=self.logits[:T])
         return argmax(self.logits[:T], out=self.tokens[:T])
+
+    # ------------------------------------------------------------------ prefill
+    def prefill(self, prompts: Sequence[Sequence[int]], width: Optional[int] = None) -> None:
+        """Puts prompts (one per cache slot 0..len-1, all of one length P) through the
+        stack: tokens 0..P-2 in causal blocks of `width` (default max_width), their K/V
+        into the caches; token P-1 becomes the first input of decoding."""
+        B = len(prompts)
+        P = len(prompts[0])
+        width = width or self.max_width
+        if not 1 <= B <= self.max_batch or any(len(p) != P for p in prompts) or P < 1:
+            raise ValueError("1..max_batch prompts of one length >= 1")
+        if not 1 <= width <= self.max_width or P - 1 + self.max_width > self.max_len:
+            raise ValueError("width or prompt length out of range")
+        self.batch = B
+        self.cached = [0] * B
+        for s0 in range(0, P - 1, width):
+            n = min(width, P - 1 - s0)
+            ids = [t for p in prompts for t in p[s0:s0 + n]]
+            self.forward(ids, [n] * B, logits=False)
+            self.cached = [x + n for x in self.cached]
+        self.last = [p[P - 1] for p in prompts]
+
+    def snapshot(self):
+        """The caches and per-sequence state, to run several decodings from one context."""
+        return ([k.clone() for k in self.k_cache], [v.clone() for v in self.v_cache],
+                self.batch, list(self.cached), list(self.last))
+
+    def restore(self, snap, batch: Optional[int] = None) -> None:
+        """Back to a snapshot, keeping its first `batch` sequences (cache slots)."""
+        ks, vs, B, cached, last = snap
+        for dst, src in zip(self.k_cache, ks):
+            dst.copy_(src)
+        for dst, src in zip(self.v_cache, vs):
+            dst.copy_(src)
+        self.batch = B if batch is None else batch
+        if not 1 <= self.batch <= B:
+            raise ValueError("batch must be in [1, snapshot batch]")
+        self.cached = cached[:self.batch]
+        self.last = last[:self.batch]
 
     # ------------------------------------------------------------------- drivers
     def decode(self, steps: int) -> List[List[int]]:
@@ -225,10 +269,25 @@ def lookup_drafter(b: int, history: List[int], n: int) -> List[int]:
     return [last] * n
 
 
-def reference_drafter(reference: List[List[int]], corrupt_every: int, vocab: int) -> Drafter:
-    """Drafts the continuation a reference run produced, with every corrupt_every-th
-    drafted position (counted along the trace) replaced by another token, so blocks end
-    at varying depths."""
+def random_drafter(vocab: int, seed: int) -> Drafter:
+    """Seeded random drafts (almost always rejected: every block ends at its first
+    token)."""
+    g = torch.Generator().manual_seed(int(seed))
+
+    def draft(b: int, history: List[int], n: int) -> List[int]:
+        return torch.randint(0, vocab, (n,), generator=g).tolist()
+    return draft
+
+
+def reference_drafter(reference: List[List[int]], corrupt_fraction: float, vocab: int,
+                      seed: int = 0) -> Drafter:
+    """Drafts the continuation a reference run produced, with a seeded pseudo-random
+    `corrupt_fraction` of the trace positions replaced by another token, so blocks end
+    at varying depths (0 replays the reference: every draft is accepted)."""
+    def corrupted(t: int) -> bool:
+        hsh = ((t + 1) * 2654435761 + seed * 40503) & 0xffffffff
+        return (hsh >> 8) % 1000 < corrupt_fraction * 1000
+
     def draft(b: int, history: List[int], n: int) -> List[int]:
         done = len(history) - 1  # tokens emitted so far
         ref = reference[b]
@@ -236,7 +295,7 @@ def reference_drafter(reference: List[List[int]], corrupt_every: int, vocab: int
         for i in range(n):
             t = done + i
             tok = ref[t] if t < len(ref) else history[-1]
-            if corrupt_every and (t + 1) % corrupt_every == 0:
+            if corrupted(t):
                 tok = (tok + 1) % vocab
             out.append(tok)
         return out

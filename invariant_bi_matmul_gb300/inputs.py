@@ -237,6 +237,12 @@ def decoder_first_token(cfg: DecoderConfig, seq_id: int, seed: int) -> int:
     return int(torch.randint(0, cfg.vocab, (1,), generator=g).item())
 
 
+def decoder_prompt(cfg: DecoderConfig, seq_id: int, seed: int, length: int) -> list:
+    """Sequence seq_id's prompt: `length` token ids, uniform over the vocabulary."""
+    g = generator(_name_seed(seed, f"prompt.{seq_id}"))
+    return torch.randint(0, cfg.vocab, (length,), generator=g).tolist()
+
+
 def page_permutation(num_pages: int, seed: int) -> torch.Tensor:
     """A seeded permutation of physical page ids (int32)."""
     return torch.randperm(num_pages, generator=generator(seed)).to(torch.int32)

@@ -3,10 +3,13 @@
   * parity: a two-layer stack's logits at every step (token by token, then verify
     blocks of 4 with drafted tokens) against the oracle's forward pass fed the same
     tokens;
-  * invariance at full size: 8 Llama-3-8B-shaped layers, 8192-token contexts, 256
-    greedy steps -- the token traces are identical whether decoded token by token or
-    with verify blocks of 4, at batch 1, 8 and 32 ("Fix/speculative shape invariance",
-    section Problem; book chapter Case 5, the greedy token under several loads).
+  * prefill: a prompt put through the stack in blocks of 8 leaves the same cache bits
+    as in blocks of 4 or alone in the batch, and matches the oracle's logits after it;
+  * invariance at full size: 8 Llama-3-8B-shaped layers, 8192-token prompts prefilled
+    through the kernels, 256 greedy steps -- the token traces are identical whether
+    decoded token by token or with verify blocks of 4 (drafts replayed, random, or 25%
+    corrupted), at batch 1, 8 and 32 ("Fix/speculative shape invariance", section
+    Problem; book chapter Case 5, the greedy token under several loads).
 """
 import math
 import time
@@ -16,13 +19,13 @@ import pytest
 import torch
 
 from invariant_bi_matmul_gb300 import inputs
-from tolerance import check_bf16, check_f32
+from tolerance import bits_equal, check_bf16, check_f32
 
 pytestmark = pytest.mark.gpu
 
 bi = pytest.importorskip("invariant_bi_matmul_gb300")
 from invariant_bi_matmul_gb300.decoder import (GreedyDecoder, lookup_drafter,  # noqa: E402
-                                               reference_drafter)
+                                               random_drafter, reference_drafter)
 
 
 @pytest.fixture(scope="module")
@@ -168,6 +171,61 @@ def test_tiny_stack_each_operation_matches_oracle(dev):
     assert bi.device_status() == bi.BI_OK
 
 
+def _slot_rows(dec, layer, slot, n):
+    """K and V rows of cache slot `slot`, positions 0..n-1 (bf16 [n, Hkv, D])."""
+    pages = dec.block_table[slot].long()
+    pos = torch.arange(n, device=dec.block_table.device)
+    phys = pages[pos // 64]
+    k = dec.k_cache[layer][phys, :, pos % 64, :]
+    v = dec.v_cache[layer][phys, :, pos % 64, :]
+    return k, v
+
+
+def test_tiny_prefill_is_invariant_to_block_width_and_batch(dev):
+    cfg, seed, P = inputs.TINY_DECODER, 505, 45
+    w = inputs.decoder_weights(cfg, seed, device=dev, std=0.05, norm_std=0.1)
+    dec = GreedyDecoder(cfg, w, max_batch=3, max_len=P + 16, max_width=8, device=dev)
+    prompts = [inputs.decoder_prompt(cfg, s, seed, P) for s in range(3)]
+    dec.prefill(prompts, width=8)
+    batch3 = [[t.clone() for t in _slot_rows(dec, l, 0, P - 1)] for l in range(cfg.layers)]
+    for width in (4, 1, 7):
+        dec.prefill(prompts[:1], width=width)
+        for l in range(cfg.layers):
+            k, v = _slot_rows(dec, l, 0, P - 1)
+            assert bits_equal(k, batch3[l][0]) and bits_equal(v, batch3[l][1]), (width, l)
+    assert bi.device_status() == bi.BI_OK
+
+
+def test_tiny_prefill_then_decode_matches_oracle(dev):
+    import oracle
+    from oracle.decoder import OracleDecoder
+
+    cfg, seed, P = inputs.TINY_DECODER, 506, 21
+    w_cpu = inputs.decoder_weights(cfg, seed, std=0.05, norm_std=0.1)
+    B, max_len = 2, P + 16
+    dec = GreedyDecoder(cfg, {k: v.to(dev) for k, v in w_cpu.items()}, max_batch=B,
+                        max_len=max_len, max_width=8, device=dev)
+    prompts = [inputs.decoder_prompt(cfg, s, seed, P) for s in range(B)]
+    dec.prefill(prompts, width=8)
+    pps = math.ceil(max_len / 64)
+    od = OracleDecoder(cfg, {k: inputs.bf16_bits(v) for k, v in w_cpu.items()},
+                       num_pages=B * pps, block_table=np.arange(B * pps).reshape(B, pps))
+    for s0 in range(0, P - 1, 8):  # the oracle takes the same blocks
+        n = min(8, P - 1 - s0)
+        od.forward([t for p in prompts for t in p[s0:s0 + n]], [s0 + n] * B,
+                   np.arange(B + 1) * n)
+    for _ in range(3):
+        ids = list(dec.last)
+        lens = [dec.cached[b] + 1 for b in range(B)]
+        greedy = dec.forward(ids, [1] * B).tolist()
+        want = od.forward(ids, lens, np.arange(B + 1))
+        _check_logits(dec.logits[:B], want.astype(np.float64), cfg, "after prefill")
+        for b in range(B):
+            dec.cached[b] += 1
+            dec.last[b] = greedy[b]
+    assert bi.device_status() == bi.BI_OK
+
+
 # ----------------------------------------------------------- invariance (tiny)
 
 def test_tiny_traces_identical_across_batch_and_width(dev):
@@ -180,7 +238,7 @@ def test_tiny_traces_identical_across_batch_and_width(dev):
     for B in (1, 2, 5):
         dec.start(range(B), seed)
         assert dec.decode(steps) == ref[:B]
-        for width, drafter in ((4, reference_drafter(ref, 3, cfg.vocab)), (2, lookup_drafter),
+        for width, drafter in ((4, reference_drafter(ref, 0.3, cfg.vocab)), (2, lookup_drafter),
                                (4, lookup_drafter)):
             dec.start(range(B), seed)
             traces, _, _ = dec.speculate(steps, width, drafter)
@@ -193,31 +251,40 @@ def test_tiny_traces_identical_across_batch_and_width(dev):
 def test_llama3_8b_8_layer_greedy_traces_identical(dev):
     cfg, seed, steps, width = inputs.LLAMA3_8B_8L, 503, 256, 4
     w = inputs.decoder_weights(cfg, seed, device=dev)
-    dec = GreedyDecoder(cfg, w, max_batch=32, max_len=cfg.context + 2 * steps + 2 * width,
-                        max_width=width, device=dev, page_seed=11)
-    report = {}
+    dec = GreedyDecoder(cfg, w, max_batch=32, max_len=cfg.context + 2 * steps + 16,
+                        max_width=8, device=dev, page_seed=11)
+    # 8193-token prompts: 8192 context tokens prefilled in blocks of 8 through the
+    # kernels, the last one the first input of decoding; one snapshot for every run
+    t0 = time.perf_counter()
+    dec.prefill([inputs.decoder_prompt(cfg, s, seed, cfg.context + 1) for s in range(32)])
+    torch.cuda.synchronize()
+    report = {"prefill 32 x 8192 (s)": round(time.perf_counter() - t0, 2)}
+    snap = dec.snapshot()
 
     def run(B, mode, drafter=None):
-        dec.start(range(B), seed)
+        dec.restore(snap, B)
         torch.cuda.synchronize()
-        t0 = time.perf_counter()
+        t1 = time.perf_counter()
         if mode == "token":
             traces, blocks, acc = dec.decode(steps), steps, 0
         else:
             traces, blocks, acc = dec.speculate(steps, width, drafter)
-        report[(B, mode)] = (round(time.perf_counter() - t0, 2), blocks, acc)
+        report[(B, mode)] = (round(time.perf_counter() - t1, 2), blocks, acc)
         return traces
 
     ref = run(32, "token")
     assert len({tuple(t) for t in ref}) > 1          # sequences decode different traces
     assert run(8, "token") == ref[:8]
     assert run(1, "token") == ref[:1]
-    drafter = reference_drafter(ref, 5, cfg.vocab)
-    for B in (32, 8, 1):
-        assert run(B, "verify4", drafter) == ref[:B], B
-    assert run(8, "verify4-lookup", lookup_drafter) == ref[:8]
+    assert run(32, "replay", reference_drafter(ref, 0, cfg.vocab)) == ref
+    assert run(8, "random", random_drafter(cfg.vocab, seed)) == ref[:8]
+    corrupt = reference_drafter(ref, 0.25, cfg.vocab, seed)  # a quarter of drafts wrong
+    for B in (32, 1):
+        assert run(B, "25% corrupted", corrupt) == ref[:B], B
+    assert run(8, "lookup", lookup_drafter) == ref[:8]
     assert bi.device_status() == bi.BI_OK
-    # blocks ended both by accepted and by rejected drafts
-    blocks32, acc32 = report[(32, "verify4")][1:]
+    # replayed drafts are all accepted; corrupted ones end blocks at every depth
+    assert report[(32, "replay")][2] == report[(32, "replay")][1] * (width - 1) * 32
+    blocks32, acc32 = report[(32, "25% corrupted")][1:]
     assert 0 < acc32 < blocks32 * (width - 1) * 32
     print("greedy-trace runs (seconds, blocks, accepted drafts):", report)
