@@ -80,103 +80,133 @@ __device__ __forceinline__ void store_group(void* __restrict__ yrow, int64_t g, 
     }
 }
 
-// MAXJ > 0: the row stays in registers (packed bf16) between the two passes
-// (H <= 8*256*MAXJ).  MAXJ == 0: the second pass reads the row again (very wide rows).
-// MAXJ only bounds a loop; the per-thread order (ascending group, ascending element)
-// and therefore the bits are the same for every MAXJ that fits H.
-template <int MAXJ, bool F32OUT>
+// MAXJ > 0: the rows stay in registers (packed bf16) between the two passes
+// (H <= 8*256*MAXJ); a CTA takes ROWS consecutive rows, each reduced exactly as if it
+// were alone.  MAXJ == 0: one row per CTA, and the second pass reads it again (very wide
+// rows).  MAXJ and ROWS only bound loops; the per-thread order (ascending group,
+// ascending element), the butterfly and the warp tree of a row -- and therefore its
+// bits -- are the same for every MAXJ that fits H and every ROWS.
+template <int MAXJ, bool F32OUT, int ROWS>
 __global__ void __launch_bounds__(kThreads)
 rmsnorm_kernel(const __nv_bfloat16* __restrict__ x, int64_t ldx,
                const __nv_bfloat16* __restrict__ gamma, void* __restrict__ y, int64_t ldy,
-               int H, float eps, int vec) {
-    __shared__ float warp_sums[kWarps];
+               int64_t rows, int H, float eps, int vec) {
+    __shared__ float warp_sums[ROWS][kWarps];
     pdl_wait();
     pdl_trigger();
-    const int64_t row = blockIdx.x;
-    const __nv_bfloat16* __restrict__ xr = x + row * ldx;
+    const int64_t row0 = int64_t(blockIdx.x) * ROWS;
     const int64_t ngroups = (H + 7) / 8;
     const int t = threadIdx.x;
     const bool v16 = vec != 0;
     constexpr int J = MAXJ > 0 ? MAXJ : 1;
 
-    float acc = 0.0f;
-    uint4 xs[J];
-    if (MAXJ > 0) {
+    float acc[ROWS];
+    uint4 xs[ROWS][J], gs[J];
 #pragma unroll
-        for (int j = 0; j < J; ++j) {
-            const int64_t g = t + static_cast<int64_t>(j) * kThreads;
-            xs[j] = (g < ngroups) ? load_group_raw(xr, g, H, v16) : make_uint4(0, 0, 0, 0);
+    for (int rr = 0; rr < ROWS; ++rr) acc[rr] = 0.0f;
+    if (MAXJ > 0) {
+        // the rows and gamma are all requested before any arithmetic: gamma's (L2) round
+        // trip overlaps the rows' instead of following the reduction
+#pragma unroll
+        for (int rr = 0; rr < ROWS; ++rr) {
+            const __nv_bfloat16* __restrict__ xr = x + (row0 + rr) * ldx;
+            const bool live = row0 + rr < rows;
+#pragma unroll
+            for (int j = 0; j < J; ++j) {
+                const int64_t g = t + static_cast<int64_t>(j) * kThreads;
+                xs[rr][j] = (live && g < ngroups) ? load_group_raw(xr, g, H, v16)
+                                                  : make_uint4(0, 0, 0, 0);
+            }
         }
 #pragma unroll
         for (int j = 0; j < J; ++j) {
             const int64_t g = t + static_cast<int64_t>(j) * kThreads;
-            if (g < ngroups) {
-                float v[8];
-                unpack_group(xs[j], v);
+            gs[j] = (g < ngroups) ? load_group_raw(gamma, g, H, v16) : make_uint4(0, 0, 0, 0);
+        }
 #pragma unroll
-                for (int i = 0; i < 8; ++i) acc = fmaf(v[i], v[i], acc);
+        for (int rr = 0; rr < ROWS; ++rr) {
+#pragma unroll
+            for (int j = 0; j < J; ++j) {
+                const int64_t g = t + static_cast<int64_t>(j) * kThreads;
+                if (g < ngroups) {
+                    float v[8];
+                    unpack_group(xs[rr][j], v);
+#pragma unroll
+                    for (int i = 0; i < 8; ++i) acc[rr] = fmaf(v[i], v[i], acc[rr]);
+                }
             }
         }
     } else {
+        const __nv_bfloat16* __restrict__ xr = x + row0 * ldx;
         for (int64_t g = t; g < ngroups; g += kThreads) {
             float v[8];
             load_group(xr, g, H, v16, v);
 #pragma unroll
-            for (int i = 0; i < 8; ++i) acc = fmaf(v[i], v[i], acc);
+            for (int i = 0; i < 8; ++i) acc[0] = fmaf(v[i], v[i], acc[0]);
         }
     }
 
     // warp butterfly: every lane ends with identical bits (each step is a+b on a pair)
 #pragma unroll
-    for (int off = 16; off >= 1; off >>= 1) acc += __shfl_xor_sync(0xffffffffu, acc, off);
-    if ((t & 31) == 0) warp_sums[t >> 5] = acc;
-    __syncthreads();
-    // fixed pairwise tree over the 8 warp partials, evaluated by every thread
-    const float s01 = warp_sums[0] + warp_sums[1];
-    const float s23 = warp_sums[2] + warp_sums[3];
-    const float s45 = warp_sums[4] + warp_sums[5];
-    const float s67 = warp_sums[6] + warp_sums[7];
-    const float ss = (s01 + s23) + (s45 + s67);
-    const float inv = rsqrtf(ss / static_cast<float>(H) + eps);
-
-    void* yrow = F32OUT ? static_cast<void*>(static_cast<float*>(y) + row * ldy)
-                        : static_cast<void*>(static_cast<__nv_bfloat16*>(y) + row * ldy);
-    if (MAXJ > 0) {
+    for (int rr = 0; rr < ROWS; ++rr) {
 #pragma unroll
-        for (int j = 0; j < J; ++j) {
-            const int64_t g = t + static_cast<int64_t>(j) * kThreads;
-            if (g < ngroups) {
+        for (int off = 16; off >= 1; off >>= 1)
+            acc[rr] += __shfl_xor_sync(0xffffffffu, acc[rr], off);
+        if ((t & 31) == 0) warp_sums[rr][t >> 5] = acc[rr];
+    }
+    __syncthreads();
+#pragma unroll
+    for (int rr = 0; rr < ROWS; ++rr) {
+        const int64_t row = row0 + rr;
+        if (row >= rows) break;
+        // fixed pairwise tree over the 8 warp partials, evaluated by every thread
+        const float s01 = warp_sums[rr][0] + warp_sums[rr][1];
+        const float s23 = warp_sums[rr][2] + warp_sums[rr][3];
+        const float s45 = warp_sums[rr][4] + warp_sums[rr][5];
+        const float s67 = warp_sums[rr][6] + warp_sums[rr][7];
+        const float ss = (s01 + s23) + (s45 + s67);
+        const float inv = rsqrtf(ss / static_cast<float>(H) + eps);
+
+        void* yrow = F32OUT ? static_cast<void*>(static_cast<float*>(y) + row * ldy)
+                            : static_cast<void*>(static_cast<__nv_bfloat16*>(y) + row * ldy);
+        if (MAXJ > 0) {
+#pragma unroll
+            for (int j = 0; j < J; ++j) {
+                const int64_t g = t + static_cast<int64_t>(j) * kThreads;
+                if (g < ngroups) {
+                    float v[8], gm[8], o[8];
+                    unpack_group(xs[rr][j], v);
+                    unpack_group(gs[j], gm);
+#pragma unroll
+                    for (int i = 0; i < 8; ++i) o[i] = (v[i] * inv) * gm[i];
+                    store_group<F32OUT>(yrow, g, H, v16, o);
+                }
+            }
+        } else {
+            const __nv_bfloat16* __restrict__ xr = x + row * ldx;
+            for (int64_t g = t; g < ngroups; g += kThreads) {
                 float v[8], gm[8], o[8];
-                unpack_group(xs[j], v);
+                load_group(xr, g, H, v16, v);
                 load_group(gamma, g, H, v16, gm);
 #pragma unroll
                 for (int i = 0; i < 8; ++i) o[i] = (v[i] * inv) * gm[i];
                 store_group<F32OUT>(yrow, g, H, v16, o);
             }
         }
-    } else {
-        for (int64_t g = t; g < ngroups; g += kThreads) {
-            float v[8], gm[8], o[8];
-            load_group(xr, g, H, v16, v);
-            load_group(gamma, g, H, v16, gm);
-#pragma unroll
-            for (int i = 0; i < 8; ++i) o[i] = (v[i] * inv) * gm[i];
-            store_group<F32OUT>(yrow, g, H, v16, o);
-        }
     }
 }
 
-template <int MAXJ>
+template <int MAXJ, int ROWS>
 cudaError_t launch_impl(const void* x, int64_t ldx, const void* gamma, void* y, int64_t ldy,
                         bool y_f32, int64_t rows, int H, float eps, int vec, cudaStream_t s) {
-    dim3 grid(static_cast<unsigned>(rows)), block(kThreads);
+    dim3 grid(static_cast<unsigned>((rows + ROWS - 1) / ROWS)), block(kThreads);
     auto xb = static_cast<const __nv_bfloat16*>(x);
     auto gb = static_cast<const __nv_bfloat16*>(gamma);
     if (y_f32)
-        return launch_pdl(rmsnorm_kernel<MAXJ, true>, grid, block, 0, s, xb, ldx, gb, y, ldy, H,
-                          eps, vec);
-    return launch_pdl(rmsnorm_kernel<MAXJ, false>, grid, block, 0, s, xb, ldx, gb, y, ldy, H, eps,
-                      vec);
+        return launch_pdl(rmsnorm_kernel<MAXJ, true, ROWS>, grid, block, 0, s, xb, ldx, gb, y,
+                          ldy, rows, H, eps, vec);
+    return launch_pdl(rmsnorm_kernel<MAXJ, false, ROWS>, grid, block, 0, s, xb, ldx, gb, y, ldy,
+                      rows, H, eps, vec);
 }
 
 }  // namespace
@@ -199,17 +229,23 @@ cudaError_t launch_rmsnorm(const void* x, int64_t ldx, const void* gamma, void* 
                          : static_cast<void*>(static_cast<__nv_bfloat16*>(y) + r0 * ldy);
         const int64_t groups_per_thread = ((H + 7) / 8 + kThreads - 1) / kThreads;
         cudaError_t e;
+        // two rows per CTA once there are enough rows to keep every SM busy: more bytes
+        // in flight per thread (scheduling only; each row's arithmetic is unchanged)
+        const bool two = n >= 1024;
         if (groups_per_thread <= 1)
-            e = launch_impl<1>(xs, ldx, gamma, ys, ldy, y_f32, n, H, eps, vec, stream);
+            e = two ? launch_impl<1, 2>(xs, ldx, gamma, ys, ldy, y_f32, n, H, eps, vec, stream)
+                    : launch_impl<1, 1>(xs, ldx, gamma, ys, ldy, y_f32, n, H, eps, vec, stream);
         else if (groups_per_thread <= 2)
-            e = launch_impl<2>(xs, ldx, gamma, ys, ldy, y_f32, n, H, eps, vec, stream);
+            e = two ? launch_impl<2, 2>(xs, ldx, gamma, ys, ldy, y_f32, n, H, eps, vec, stream)
+                    : launch_impl<2, 1>(xs, ldx, gamma, ys, ldy, y_f32, n, H, eps, vec, stream);
         else if (groups_per_thread <= 4)
-            e = launch_impl<4>(xs, ldx, gamma, ys, ldy, y_f32, n, H, eps, vec, stream);
+            e = two ? launch_impl<4, 2>(xs, ldx, gamma, ys, ldy, y_f32, n, H, eps, vec, stream)
+                    : launch_impl<4, 1>(xs, ldx, gamma, ys, ldy, y_f32, n, H, eps, vec, stream);
         else if (groups_per_thread <= kMaxGroupsInRegs)
-            e = launch_impl<kMaxGroupsInRegs>(xs, ldx, gamma, ys, ldy, y_f32, n, H, eps, vec,
-                                              stream);
+            e = launch_impl<kMaxGroupsInRegs, 1>(xs, ldx, gamma, ys, ldy, y_f32, n, H, eps, vec,
+                                                 stream);
         else
-            e = launch_impl<0>(xs, ldx, gamma, ys, ldy, y_f32, n, H, eps, vec, stream);
+            e = launch_impl<0, 1>(xs, ldx, gamma, ys, ldy, y_f32, n, H, eps, vec, stream);
         if (e != cudaSuccess) return e;
     }
     return cudaSuccess;
