@@ -640,7 +640,7 @@ attn_merge_kernel(const int32_t* __restrict__ seq_lens, const int32_t* __restric
                   const float* __restrict__ ws_o, const float* __restrict__ ws_ml, int maxC,
                   __nv_bfloat16* __restrict__ out, float* __restrict__ lse) {
     constexpr int PER = D / 32;
-    constexpr int UNROLL = 8;
+    constexpr int UNROLL = 17;  // a warp's whole range up to 136 chunks (69,632 keys)
     __shared__ float sM[MERGE_WARPS], sL[MERGE_WARPS];
     __shared__ float sO[MERGE_WARPS][D];
     pdl_wait();
@@ -666,8 +666,8 @@ attn_merge_kernel(const int32_t* __restrict__ seq_lens, const int32_t* __restric
     const int64_t base = (int64_t(t) * Hq + hq) * maxC;
     const int c0 = warp * nC / MERGE_WARPS, c1 = (warp + 1) * nC / MERGE_WARPS;
 
-    // The first UNROLL partials of the range are requested before the range max is
-    // reduced (they do not depend on it), so the two global round trips overlap.
+    // The first UNROLL partials of the range are requested before anything else (for
+    // ranges up to UNROLL chunks: all of them, in one global round trip).
     auto load = [&](int c, float (&v)[PER], float2& ml) {
         ml = *reinterpret_cast<const float2*>(ws_ml + (base + c) * 2);
         const float* src = ws_o + (base + c) * D + lane * PER;
@@ -685,11 +685,19 @@ attn_merge_kernel(const int32_t* __restrict__ seq_lens, const int32_t* __restric
     for (int u = 0; u < UNROLL; ++u)
         if (c0 + u < c1) load(c0 + u, v[u], ml[u]);
 
-    // range max: lanes stride over chunks, then a butterfly (max is exact)
+    // range max (exact in any order): from the registers when the whole range was loaded
+    // above, else lanes stride over the chunks and a butterfly combines them
     float Mw = -INFINITY;
-    for (int c = c0 + lane; c < c1; c += 32) Mw = fmaxf(Mw, ws_ml[(base + c) * 2]);
+    if (c1 - c0 <= UNROLL) {
 #pragma unroll
-    for (int off = 16; off >= 1; off >>= 1) Mw = fmaxf(Mw, __shfl_xor_sync(0xffffffffu, Mw, off));
+        for (int u = 0; u < UNROLL; ++u)
+            if (c0 + u < c1) Mw = fmaxf(Mw, ml[u].x);
+    } else {
+        for (int c = c0 + lane; c < c1; c += 32) Mw = fmaxf(Mw, ws_ml[(base + c) * 2]);
+#pragma unroll
+        for (int off = 16; off >= 1; off >>= 1)
+            Mw = fmaxf(Mw, __shfl_xor_sync(0xffffffffu, Mw, off));
+    }
 
     float Lw = 0.f;
     float acc[PER];
