@@ -559,7 +559,10 @@ def run_sweep():
     attention over the pages' Lk and q.  Two timings per shape: one call with L2 evicted
     before it (`*_us`, includes the launch), and `steady_*_us`, the per-call time of a
     back-to-back stream over rotating input sets larger than 2x L2 (for attention, one
-    set when its K/V already exceed that; otherwise marked warm)."""
+    set when its K/V already exceed that; otherwise marked warm).  Each GEMM and attention
+    shape is timed inside the batch-invariant limit and again with the limit at 0 (the
+    non-invariant configuration the library picks: split-K, the chosen chunk length), and
+    `invariance_tax` is the invariant time over the fast one, minus 1."""
     import torch
     import invariant_bi_matmul_gb300 as bi
     from invariant_bi_matmul_gb300 import inputs
@@ -597,7 +600,38 @@ def run_sweep():
         torch.cuda.synchronize()
         return s.elapsed_time(e) * 1e3 / n
 
+    def graph_us(fns, n=64, reps=7):
+        """Per-call device time of n calls (cycling through fns) captured in one CUDA
+        graph: no host launch cost between the calls, so kernels shorter than the Python
+        binding's per-call cost are timed as the GPU runs them back to back."""
+        side = torch.cuda.Stream()
+        side.wait_stream(torch.cuda.current_stream())
+        with torch.cuda.stream(side):
+            for f in fns:  # first calls (function attributes, occupancy queries) uncaptured
+                f()
+        torch.cuda.current_stream().wait_stream(side)
+        torch.cuda.synchronize()
+        g = torch.cuda.CUDAGraph()
+        with torch.cuda.graph(g):
+            for i in range(n):
+                fns[i % len(fns)]()
+        g.replay()
+        torch.cuda.synchronize()
+        ts = []
+        for _ in range(reps):
+            s = torch.cuda.Event(enable_timing=True)
+            e = torch.cuda.Event(enable_timing=True)
+            s.record()
+            g.replay()
+            e.record()
+            torch.cuda.synchronize()
+            ts.append(s.elapsed_time(e) * 1e3 / n)
+        del g
+        return statistics.median(ts)
+
     SET_BYTES = 256 * 1024 * 1024  # rotating inputs: more than 2x the 126 MB L2
+    INVARIANT, FAST = 1 << 40, 0   # limits: every call inside it / the limit disabled
+    sms = torch.cuda.get_device_properties(dev).multi_processor_count
 
     K = N = 4096
     gi = inputs.gemm_inputs(2048, N, K, seed=2)
@@ -606,11 +640,20 @@ def run_sweep():
     for M in (1, 2, 4, 8, 16, 64, 256, 2048):
         xm = x[:M].contiguous()
         y = torch.empty(M, N, dtype=torch.bfloat16, device=dev)
+        bi.set_batch_invariant_limit(INVARIANT)
         tn = t_us(lambda: bi.matmul(xm, wnk, "nk", out=y))
         tk = t_us(lambda: bi.matmul(xm, wkn, "kn", out=y))
         tc = t_us(lambda: torch.matmul(xm, wnk.t(), out=y))
         tns = steady_us([lambda w=w: bi.matmul(xm, w, "nk", out=y) for w in wsets])
         tcs = steady_us([lambda w=w: torch.matmul(xm, w.t(), out=y) for w in wsets])
+        tng = graph_us([lambda w=w: bi.matmul(xm, w, "nk", out=y) for w in wsets])
+        tcg = graph_us([lambda w=w: torch.matmul(xm, w.t(), out=y) for w in wsets])
+        # the same call outside the limit (split-K where it pays)
+        bi.set_batch_invariant_limit(FAST)
+        splits = bi.matmul_splits(M, N, K, "nk", sms)
+        tf = t_us(lambda: bi.matmul(xm, wnk, "nk", out=y))
+        tfs = steady_us([lambda w=w: bi.matmul(xm, w, "nk", out=y) for w in wsets])
+        tfg = graph_us([lambda w=w: bi.matmul(xm, w, "nk", out=y) for w in wsets])
         fl = 2 * M * N * K
         by = 2 * N * K + 4 * M * K
         tf_peak = float(peaks.get("bf16_tflops", 1900.0))
@@ -623,7 +666,18 @@ def run_sweep():
                           "steady_nk_us": round(tns, 2), "steady_cublas_us": round(tcs, 2),
                           "steady_nk_vs_cublas": round(tns / tcs, 3),
                           "steady_nk_frac_hbm": round(by / tns / 1e3 / peaks["hbm_gbs"], 3),
-                          "steady_nk_frac_tensor": round(fl / tns / 1e6 / tf_peak, 3)}),
+                          "steady_nk_frac_tensor": round(fl / tns / 1e6 / tf_peak, 3),
+                          "fast_splits": splits, "fast_nk_us": round(tf, 2),
+                          "steady_fast_nk_us": round(tfs, 2),
+                          "invariance_tax": round(tn / tf - 1.0, 3),
+                          "steady_invariance_tax": round(tns / tfs - 1.0, 3),
+                          "graph_nk_us": round(tng, 2), "graph_fast_nk_us": round(tfg, 2),
+                          "graph_cublas_us": round(tcg, 2),
+                          "graph_nk_vs_cublas": round(tng / tcg, 3),
+                          "graph_fast_vs_cublas": round(tfg / tcg, 3),
+                          "graph_invariance_tax": round(tng / tfg - 1.0, 3),
+                          "graph_nk_frac_hbm": round(by / tng / 1e3 / peaks["hbm_gbs"], 3),
+                          "graph_nk_frac_tensor": round(fl / tng / 1e6 / tf_peak, 3)}),
               flush=True)
     del wsets
     for B in (1, 3, 16, 128, 2048):
@@ -635,20 +689,25 @@ def run_sweep():
         nsets = max(2, min(64, -(-SET_BYTES // by)))
         sets = [(xr.clone(), torch.empty_like(xr)) for _ in range(nsets)]
         ts = steady_us([lambda a=a, o=o: bi.rmsnorm(a, g, 1e-5, out=o) for a, o in sets])
+        tg = graph_us([lambda a=a, o=o: bi.rmsnorm(a, g, 1e-5, out=o) for a, o in sets])
         del sets
         print(json.dumps({"sweep": "rmsnorm", "B": B, "H": 8192, "us": round(t, 2),
                           "GB/s": round(by / t / 1e3, 1),
                           "frac_hbm": round(by / t / 1e3 / peaks["hbm_gbs"], 3),
                           "steady_us": round(ts, 2), "steady_GB/s": round(by / ts / 1e3, 1),
                           "steady_frac_hbm": round(by / ts / 1e3 / peaks["hbm_gbs"], 3),
-                          "steady_sets": nsets, "steady_cold": nsets * by >= SET_BYTES}),
+                          "steady_sets": nsets, "steady_cold": nsets * by >= SET_BYTES,
+                          "graph_us": round(tg, 2),
+                          "graph_frac_hbm": round(by / tg / 1e3 / peaks["hbm_gbs"], 3)}),
               flush=True)
     for B, q, L in ((1, 1, 65540), (1, 8, 65540), (1, 8, 16388), (1, 8, 8196), (1, 8, 1028),
                     (8, 1, 65540), (64, 1, 16388), (64, 4, 8196)):
+        bi.set_batch_invariant_limit(INVARIANT)
         p = inputs.paged_inputs([L] * B, [q] * B, Hq=HQ, Hkv=HKV, D=HEAD_DIM, seed=4, device=dev)
         d = {k: getattr(p, k).to(dev) for k in ("q", "k_cache", "v_cache", "block_table",
                                                  "seq_lens", "cu_q")}
-        ws = torch.empty(bi.attn_workspace_size(B * q, HQ, HEAD_DIM, L), dtype=torch.uint8,
+        # 8x the invariant workspace: every chunk length is open to the fast path
+        ws = torch.empty(8 * bi.attn_workspace_size(B * q, HQ, HEAD_DIM, L), dtype=torch.uint8,
                          device=dev)
         out = torch.empty(B * q, HQ, HEAD_DIM, dtype=torch.bfloat16, device=dev)
         lse = torch.empty(B * q, HQ, dtype=torch.float32, device=dev)
@@ -662,12 +721,43 @@ def run_sweep():
                                                 max_q=q, max_seq_len=L,
                                                 scale=1 / math.sqrt(HEAD_DIM), out=out,
                                                 lse=lse, workspace=ws)], n=30)
+        # device time per call from a CUDA graph, rotating over copies of the caches
+        # until the set exceeds 2x L2
+        nsets = 1 if by >= SET_BYTES else min(64, -(-SET_BYTES // by))
+        caches = [(d["k_cache"], d["v_cache"])] + [
+            (d["k_cache"].clone(), d["v_cache"].clone()) for _ in range(nsets - 1)]
+        calls = [lambda kc=kc, vc=vc: bi.verify_block(
+            d["q"], kc, vc, d["block_table"], d["seq_lens"], d["cu_q"], max_q=q, max_seq_len=L,
+            scale=1 / math.sqrt(HEAD_DIM), out=out, lse=lse, workspace=ws) for kc, vc in caches]
+        n_graph = max(8, min(64, nsets * 2))
+        tg = graph_us(calls, n=n_graph)
+        bi.set_batch_invariant_limit(FAST)
+        tfg = graph_us(calls, n=n_graph)
+        del caches, calls
+        chunk = bi.attn_chunk(B, B * q, q, L, HQ, HKV, HEAD_DIM, ws.numel(), sms)
+        tf = t_us(lambda: bi.verify_block(d["q"], d["k_cache"], d["v_cache"], d["block_table"],
+                                          d["seq_lens"], d["cu_q"], max_q=q, max_seq_len=L,
+                                          scale=1 / math.sqrt(HEAD_DIM), out=out, lse=lse,
+                                          workspace=ws))
+        tfs = steady_us([lambda: bi.verify_block(d["q"], d["k_cache"], d["v_cache"],
+                                                 d["block_table"], d["seq_lens"], d["cu_q"],
+                                                 max_q=q, max_seq_len=L,
+                                                 scale=1 / math.sqrt(HEAD_DIM), out=out,
+                                                 lse=lse, workspace=ws)], n=30)
         print(json.dumps({"sweep": "attention", "B": B, "q": q, "Lk": L, "us": round(t, 2),
                           "GB/s": round(by / t / 1e3, 1),
                           "frac_hbm": round(by / t / 1e3 / peaks["hbm_gbs"], 3),
                           "steady_us": round(ts, 2), "steady_GB/s": round(by / ts / 1e3, 1),
                           "steady_frac_hbm": round(by / ts / 1e3 / peaks["hbm_gbs"], 3),
-                          "steady_cold": by >= SET_BYTES}), flush=True)
+                          "steady_cold": by >= SET_BYTES, "fast_chunk": chunk,
+                          "fast_us": round(tf, 2), "steady_fast_us": round(tfs, 2),
+                          "fast_frac_hbm": round(by / tf / 1e3 / peaks["hbm_gbs"], 3),
+                          "invariance_tax": round(t / tf - 1.0, 3),
+                          "graph_us": round(tg, 2), "graph_fast_us": round(tfg, 2),
+                          "graph_sets": nsets,
+                          "graph_frac_hbm": round(by / tg / 1e3 / peaks["hbm_gbs"], 3),
+                          "graph_fast_frac_hbm": round(by / tfg / 1e3 / peaks["hbm_gbs"], 3),
+                          "graph_invariance_tax": round(tg / tfg - 1.0, 3)}), flush=True)
         del p, d, ws
         torch.cuda.empty_cache()
 

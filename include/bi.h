@@ -30,12 +30,14 @@
  *     the device error word and the kernel returns; bi_device_status() then reports
  *     BI_ERR_TIMEOUT.  Nothing traps or aborts.  bi_last_error_message() gives a
  *     one-line, thread-local explanation of the last non-OK status.
- *   - Determinism contract: for a fixed library build, the bits of output row m of
- *     bi_matmul / bi_rmsnorm depend only on that row's inputs (and W / gamma), never on
- *     M, on the other rows, or on the row's position in the batch.  The bits of a
- *     query's attention output depend only on that query, its position and the keys
- *     and values at positions 0..pos of its own sequence -- not on the batch, on the
- *     verify-block width, or on the sequence's total length.
+ *   - Determinism contract: for a fixed library build, every call is deterministic
+ *     (same inputs and sizes, same bits).  Calls INSIDE the batch-invariant limit (see
+ *     below) are also batch invariant: the bits of output row m of bi_matmul /
+ *     bi_rmsnorm depend only on that row's inputs (and W / gamma), never on M, on the
+ *     other rows, or on the row's position in the batch; the bits of a query's
+ *     attention output depend only on that query, its position and the keys and values
+ *     at positions 0..pos of its own sequence -- not on the batch, on the verify-block
+ *     width, or on the sequence's total length.  bi_rmsnorm is batch invariant always.
  */
 #ifndef BI_H_
 #define BI_H_
@@ -92,14 +94,37 @@ const char* bi_last_error_message(void);
  * (read once, at the first call of any entry point).  When the leading dimension
  * (matmul M, RMSNorm rows) or the verify-block width (attention max_q) is <= limit,
  * the entry point MUST use its invariant configuration.  Above the limit, or with the
- * limit at 0, a library may pick a faster non-invariant path; this build has only the
- * invariant kernels, so every call is invariant whatever the limit says.
+ * limit at 0, the library picks a faster configuration from the call's sizes, whose
+ * bits then depend on those sizes:
+ *   - bi_matmul: split-K.  When one 128-row M-tile (M <= 128) leaves SMs idle, a cluster
+ *     of up to 8 CTAs shares each output tile, each CTA over a contiguous K range, and
+ *     the partials are added in ascending K order (the split count follows N, K, M and
+ *     the SM count; see bi_matmul_splits).
+ *   - bi_verify_block / bi_decode_attn: the split-KV chunk length (64 .. 2048 keys) is
+ *     chosen from the batch, heads, max_seq_len, block width and SM count by a cost
+ *     model, among the lengths whose partials fit in the caller's workspace (a
+ *     workspace of bi_attn_workspace_size() bytes admits lengths >= BI_ATTN_CHUNK; 8x
+ *     that admits all); see bi_attn_chunk.
+ *   - bi_rmsnorm has one configuration (already the fastest one).
+ * Applications that verify speculative blocks set the limit to cover their largest
+ * matmul M (batch x verify width) and their largest verify width.
  * A negative limit returns BI_ERR_INVALID_ARG and leaves the setting unchanged.
  * ------------------------------------------------------------------------------- */
 bi_status bi_set_batch_invariant_limit(int64_t limit);
 int64_t bi_get_batch_invariant_limit(void);
 /* 1 if a call with leading dimension / verify width `dim` falls inside the limit. */
 int bi_within_batch_invariant_limit(int64_t dim);
+
+/* Introspection (host only, no device access): the configuration a call with these
+ * sizes would run under the current limit, on a GPU with num_sms SMs.
+ * bi_matmul_splits: CTAs per output tile along K (1 = the invariant single K loop).
+ * bi_attn_chunk: split-KV chunk length in keys (BI_ATTN_CHUNK inside the limit);
+ *   workspace_bytes is the workspace the call would be given.
+ * Both return 0 for invalid sizes. */
+int bi_matmul_splits(int64_t M, int64_t N, int64_t K, int w_layout, int num_sms);
+int64_t bi_attn_chunk(int64_t batch, int64_t total_q, int64_t max_q, int64_t max_seq_len,
+                      int64_t num_q_heads, int64_t num_kv_heads, int64_t head_dim,
+                      size_t workspace_bytes, int num_sms);
 
 /* ---------------------------------------------------------------------------------
  * bi_matmul  [BOOK Case 3 and Case 6 "Matmul": one compiled config for all shapes, no
@@ -114,11 +139,14 @@ int bi_within_batch_invariant_limit(int64_t dim);
  *                 layout BI_W_KN: [K, N] with row stride ldw (ldw >= N).
  *   y       [M, N] row-major, row stride ldy (ldy >= N), dtype y_dtype.
  *   M, N, K >= 0; M = 0 or N = 0 is a no-op; K = 0 writes zeros.
- *   Invariant construction: one tcgen05 instruction shape (128 x 64 x 16, kind::f16, fp32
- *   accumulation in tensor memory) and one K order (64-wide K-blocks ascending, four
- *   16-wide steps ascending inside each) for every M.  Row m is always lane m%128 of
- *   M-tile m/128; rows beyond M are never stored.  Only scheduling follows M (how many X
- *   rows are staged, how many instruction tiles one CTA covers).
+ *   Invariant construction (M inside the batch-invariant limit): one tcgen05
+ *   instruction shape (128 x 64 x 16, kind::f16, fp32 accumulation in tensor memory)
+ *   and one K order (64-wide K-blocks ascending, four 16-wide steps ascending inside
+ *   each) for every M.  Row m is always lane m%128 of M-tile m/128; rows beyond M are
+ *   never stored.  Only scheduling follows M (how many X rows are staged, how many
+ *   instruction tiles one CTA covers).  Outside the limit the K loop may be split
+ *   (see the limit section): each part runs the same ascending K order over its range
+ *   and the fp32 partials are added in ascending K order before rounding.
  *   Alignment (TMA rule): x, w 16-byte aligned; ldx, ldw multiples of 8 elements;
  *   otherwise BI_ERR_UNSUPPORTED.  y needs only element alignment.
  *   Limits: M, N, K < 2^31.
@@ -182,11 +210,13 @@ size_t bi_attn_workspace_size(int64_t total_q, int64_t num_q_heads, int64_t head
  *   head h (KV head h / (num_q_heads/num_kv_heads)):
  *     out[t, h, :] = softmax_i(scale * q[t,h,:] . k_i) @ v_i over keys i = 0..pos
  *     lse[t, h]    = log sum_i exp(scale * q . k_i)            (natural log; nullable)
- *   Split-KV with a FIXED chunk length BI_ATTN_CHUNK counted from key 0: chunk c covers
- *   keys [c*CHUNK, (c+1)*CHUNK); a query uses chunks 0..pos/CHUNK, each reduced with the
- *   same instruction sequence whatever the batch or block width, and the partials are
- *   merged by log-sum-exp over a fixed tree (eight contiguous chunk ranges folded in
- *   ascending order, then combined in ascending order) that depends on pos alone.
+ *   Split-KV with a FIXED chunk length BI_ATTN_CHUNK counted from key 0 (max_q inside
+ *   the batch-invariant limit; outside it the length is chosen per call, see the limit
+ *   section): chunk c covers keys [c*CHUNK, (c+1)*CHUNK); a query uses chunks
+ *   0..pos/CHUNK, each reduced with the same instruction sequence whatever the batch or
+ *   block width, and the partials are merged by log-sum-exp over a fixed tree (eight
+ *   contiguous chunk ranges folded in ascending order, then combined in ascending
+ *   order) that depends on pos (and the chunk length) alone.
  *
  *   q        bf16 [total_q, num_q_heads, head_dim]; out bf16 same shape; lse fp32
  *            [total_q, num_q_heads] or NULL.  workspace: device memory of at least

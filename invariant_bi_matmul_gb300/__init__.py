@@ -35,6 +35,8 @@ SIGNATURES = {
     "bi_set_batch_invariant_limit": ([_i64], _int),
     "bi_get_batch_invariant_limit": ([], _i64),
     "bi_within_batch_invariant_limit": ([_i64], _int),
+    "bi_matmul_splits": ([_i64, _i64, _i64, _int, _int], _int),
+    "bi_attn_chunk": ([_i64, _i64, _i64, _i64, _i64, _i64, _i64, _sz, _int], _i64),
     "bi_matmul": ([_p, _i64, _p, _i64, _int, _p, _i64, _int, _i64, _i64, _i64, _p], _int),
     "bi_rmsnorm": ([_p, _i64, _p, _p, _i64, _int, _i64, _i64, _f32, _p], _int),
     "bi_kv_append": ([_p, _p, _p, _p, _i64, _p, _i64, _p, _p, _i64, _i64, _i64, _i64, _i64, _p],
@@ -141,6 +143,23 @@ def get_batch_invariant_limit() -> int:
 
 def within_batch_invariant_limit(dim: int) -> bool:
     return bool(lib().bi_within_batch_invariant_limit(int(dim)))
+
+
+def matmul_splits(M: int, N: int, K: int, w_layout: str = "nk", num_sms: int = 152) -> int:
+    """How many CTAs would share each output tile's K range for this shape under the
+    current limit (1: the invariant K loop).  0 for invalid sizes."""
+    lay = {"nk": BI_W_NK, "kn": BI_W_KN}[w_layout]
+    return int(lib().bi_matmul_splits(int(M), int(N), int(K), lay, int(num_sms)))
+
+
+def attn_chunk(batch: int, total_q: int, max_q: int, max_seq_len: int, num_q_heads: int,
+               num_kv_heads: int, head_dim: int, workspace_bytes: int,
+               num_sms: int = 152) -> int:
+    """The split-KV chunk length (keys) a verify/decode call with these sizes would use
+    under the current limit (ATTN_CHUNK inside it).  0 for invalid sizes."""
+    return int(lib().bi_attn_chunk(int(batch), int(total_q), int(max_q), int(max_seq_len),
+                                   int(num_q_heads), int(num_kv_heads), int(head_dim),
+                                   int(workspace_bytes), int(num_sms)))
 
 
 # ----------------------------------------------------------------------------- matmul

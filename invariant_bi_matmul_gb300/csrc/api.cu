@@ -136,6 +136,33 @@ BI_EXPORT int bi_within_batch_invariant_limit(int64_t dim) {
     return lim > 0 && dim <= lim ? 1 : 0;
 }
 
+BI_EXPORT int bi_matmul_splits(int64_t M, int64_t N, int64_t K, int w_layout, int num_sms) {
+    if (M < 1 || N < 1 || K < 1 || M > kI32Max || N > kI32Max || K > kI32Max || num_sms < 1 ||
+        (w_layout != BI_W_NK && w_layout != BI_W_KN))
+        return 0;
+    const bool split_ok = !bi_within_batch_invariant_limit(M);
+    return gemm_schedule(M, N, K, w_layout == BI_W_KN, num_sms, split_ok).splits;
+}
+
+BI_EXPORT int64_t bi_attn_chunk(int64_t batch, int64_t total_q, int64_t max_q,
+                                int64_t max_seq_len, int64_t num_q_heads, int64_t num_kv_heads,
+                                int64_t head_dim, size_t workspace_bytes, int num_sms) {
+    if (batch < 1 || total_q < batch || max_q < 1 || total_q > batch * max_q ||
+        max_seq_len < 1 || num_kv_heads < 1 || num_q_heads < 1 ||
+        num_q_heads % num_kv_heads != 0 || (head_dim != 64 && head_dim != 128) || num_sms < 1)
+        return 0;
+    PagedArgs a{};
+    a.batch = batch;
+    a.total_q = total_q;
+    a.max_q = max_q;
+    a.max_seq_len = max_seq_len;
+    a.hq = num_q_heads;
+    a.hkv = num_kv_heads;
+    a.head_dim = head_dim;
+    return int64_t(1) << attn_chunk_log2(a, workspace_bytes, num_sms,
+                                         bi_within_batch_invariant_limit(max_q) != 0);
+}
+
 // ========================================================================== matmul
 
 BI_EXPORT bi_status bi_matmul(const void* x, int64_t ldx, const void* w, int64_t ldw,
@@ -169,8 +196,11 @@ BI_EXPORT bi_status bi_matmul(const void* x, int64_t ldx, const void* w, int64_t
     cudaError_t why = cudaSuccess;
     const DeviceInfo* dev = current_device_info(&why);
     if (!dev) return cuda_fail(why, "bi_matmul: device query");
+    // inside the limit: the invariant schedule; outside it the split-K kernel may be used
+    const bool split_ok = !bi_within_batch_invariant_limit(M);
     cudaError_t e = launch_gemm(*dev, x, ldx, w, ldw, w_layout == BI_W_KN, y, ldy,
-                                y_dtype == BI_F32, M, N, K, reinterpret_cast<cudaStream_t>(stream));
+                                y_dtype == BI_F32, M, N, K, split_ok,
+                                reinterpret_cast<cudaStream_t>(stream));
     if (e != cudaSuccess) return cuda_fail(e, "bi_matmul: launch");
     return BI_OK;
 }
@@ -263,7 +293,11 @@ bi_status run_attention(const char* fn, const void* q, const PagedArgs& a, int64
     cudaError_t why = cudaSuccess;
     const DeviceInfo* dev = current_device_info(&why);
     if (!dev) return cuda_fail(why, fn);
-    cudaError_t e = launch_attention(*dev, q, a, scale, out, lse, workspace,
+    // inside the limit (verify width max_q): the fixed chunk length; outside it a chunk
+    // length chosen from the call's parallelism
+    const int chunk_log2 = attn_chunk_log2(a, ws_bytes, dev->num_sms,
+                                           bi_within_batch_invariant_limit(a.max_q) != 0);
+    cudaError_t e = launch_attention(*dev, q, a, scale, out, lse, workspace, chunk_log2,
                                      reinterpret_cast<cudaStream_t>(stream));
     if (e != cudaSuccess) return cuda_fail(e, fn);
     return BI_OK;

@@ -45,8 +45,9 @@ namespace bi {
 namespace {
 
 constexpr int PAGE = 64;
-constexpr int CHUNK = 512;
-constexpr int PAGES_PER_CHUNK = CHUNK / PAGE;
+constexpr int CHUNK_LOG2 = 9;  // the invariant chunk length: 512 keys
+constexpr int CHUNK = 1 << CHUNK_LOG2;
+constexpr int MIN_CHUNK_LOG2 = 6, MAX_CHUNK_LOG2 = 11;  // non-invariant calls: 64 .. 2048
 constexpr int MAXR = 32;       // query rows per (sequence, KV head): q_len * group size
 constexpr int NSM = 4;         // softmax warps 0..3, one per tensor-memory lane quarter
 constexpr int KSL = PAGE / NSM;  // keys of a page per softmax warp
@@ -134,8 +135,10 @@ attn_partial_kernel(const __grid_constant__ CUtensorMap tmap_k,
                     const int32_t* __restrict__ cu_q, int B, int total_q, int max_q,
                     int max_seq_len, int Hq, int Hkv, float scale_log2,
                     float* __restrict__ ws_o, float* __restrict__ ws_ml, int maxC,
-                    unsigned int* err) {
+                    int chunk_log2, unsigned int* err) {
     using C = Cfg<D>;
+    const int chunk = 1 << chunk_log2;         // keys per work item (CHUNK when invariant)
+    const int chunk_pages = chunk / PAGE;
     constexpr int NST = C::NST;
     extern __shared__ uint8_t smem_raw[];
     uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) &
@@ -198,7 +201,7 @@ attn_partial_kernel(const __grid_constant__ CUtensorMap tmap_k,
         const SeqInfo si = seq_info(seq_lens, cu_q, b);
         const bool ok = seq_ok(si, max_q, max_seq_len, total_q);
         if (!ok) latch_error(err, kErrDeviceArg);
-        prefix[b + 1] = ok ? ((si.L + CHUNK - 1) / CHUNK) * Hkv : 0;
+        prefix[b + 1] = ok ? ((si.L + chunk - 1) >> chunk_log2) * Hkv : 0;
         seq_len[b] = si.L;
         seq_t0[b] = si.t0;
         seq_qb[b] = uint8_t(ok ? si.qb : 0);  // <= BI_ATTN_MAX_Q
@@ -244,7 +247,7 @@ attn_partial_kernel(const __grid_constant__ CUtensorMap tmap_k,
         return si;
     };
     auto pages_of = [&](const SeqInfo& si, int c) {
-        return min(PAGES_PER_CHUNK, (si.L - c * CHUNK + PAGE - 1) / PAGE);
+        return min(chunk_pages, (si.L - c * chunk + PAGE - 1) / PAGE);
     };
     auto give_up = [&]() {
         if (!*abort_flag) {
@@ -275,7 +278,7 @@ attn_partial_kernel(const __grid_constant__ CUtensorMap tmap_k,
                 const int s = int(g % NST);
                 if (!wait(&empty[s], ((g / NST) & 1u) ^ 1u)) break;
                 if (elect_one()) {
-                    const int pidx = c * PAGES_PER_CHUNK + i;
+                    const int pidx = c * chunk_pages + i;
                     const int phys =
                         pidx < max_pages ? block_table[int64_t(b) * max_pages + pidx] : -1;
                     const bool valid = phys >= 0 && phys < num_pages;
@@ -408,7 +411,7 @@ attn_partial_kernel(const __grid_constant__ CUtensorMap tmap_k,
             const float* xs = x_sum + ob * ((NSM + 1) * MAXR);
             const float l_tot = ((xs[r] + xs[MAXR + r]) + xs[2 * MAXR + r]) + xs[3 * MAXR + r];
             const float m_ref = xs[NSM * MAXR + r];
-            const bool store = r < R && pos >= c * CHUNK;
+            const bool store = r < R && pos >= c * chunk;
             const int64_t idx = (int64_t(si.t0 + j) * Hq + int64_t(h) * G + gg) * maxC + c;
             // O row r of 32 columns at a time: staged through shared memory (rows padded
             // to 144 B, conflict-free) so that each store instruction writes four rows'
@@ -499,7 +502,7 @@ attn_partial_kernel(const __grid_constant__ CUtensorMap tmap_k,
                 const uint32_t gi = g + uint32_t(i);
                 const int s = int(gi % NST), sb = int(gi & 1u);
                 const uint32_t par = (gi >> 1) & 1u;
-                const int page0 = c * CHUNK + i * PAGE;  // first key of the page
+                const int page0 = c * chunk + i * PAGE;  // first key of the page
                 // all 64 scores of the page, then release the S buffer
                 if (!wait(&s_full[sb], par)) break;
                 tc_fence_after_sync();
@@ -629,7 +632,7 @@ attn_partial_kernel(const __grid_constant__ CUtensorMap tmap_k,
 
 constexpr int MERGE_WARPS = 8;
 
-// One CTA per (token, query head) merges the chunk partials 0 .. nC-1 (nC = pos/CHUNK+1).
+// One CTA per (token, query head) merges the chunk partials 0 .. nC-1 (nC = pos/chunk+1).
 // Warp w folds the contiguous range [w*nC/8, (w+1)*nC/8) in ascending order (max first,
 // then the exp2-weighted sums); the eight warp results are combined in ascending warp
 // order.  The tree is a function of nC alone, i.e. of the query's position.
@@ -638,7 +641,7 @@ __global__ void __launch_bounds__(MERGE_WARPS * 32)
 attn_merge_kernel(const int32_t* __restrict__ seq_lens, const int32_t* __restrict__ cu_q, int B,
                   int total_q, int max_q, int max_seq_len, int Hq,
                   const float* __restrict__ ws_o, const float* __restrict__ ws_ml, int maxC,
-                  __nv_bfloat16* __restrict__ out, float* __restrict__ lse) {
+                  int chunk_log2, __nv_bfloat16* __restrict__ out, float* __restrict__ lse) {
     constexpr int PER = D / 32;
     constexpr int UNROLL = 17;  // a warp's whole range up to 136 chunks (69,632 keys)
     __shared__ float sM[MERGE_WARPS], sL[MERGE_WARPS];
@@ -662,7 +665,7 @@ attn_merge_kernel(const int32_t* __restrict__ seq_lens, const int32_t* __restric
     const SeqInfo si = seq_info(seq_lens, cu_q, b);
     if (!seq_ok(si, max_q, max_seq_len, total_q) || t < si.t0 || t >= si.t0 + si.qb) return;
     const int pos = si.L - si.qb + (t - si.t0);
-    const int nC = pos / CHUNK + 1;
+    const int nC = (pos >> chunk_log2) + 1;
     const int64_t base = (int64_t(t) * Hq + hq) * maxC;
     const int c0 = warp * nC / MERGE_WARPS, c1 = (warp + 1) * nC / MERGE_WARPS;
 
@@ -793,7 +796,7 @@ kv_append_kernel(const uint4* __restrict__ k_new, const uint4* __restrict__ v_ne
 template <int D>
 cudaError_t launch_attention_t(const DeviceInfo& dev, const void* q, const PagedArgs& a,
                                float scale, void* out, float* lse, void* workspace,
-                               cudaStream_t stream) {
+                               int chunk_log2, cudaStream_t stream) {
     using Cf = Cfg<D>;
     const uint64_t rows = uint64_t(a.num_pages) * uint64_t(a.hkv) * PAGE;
     CUtensorMap tk, tv;
@@ -808,7 +811,8 @@ cudaError_t launch_attention_t(const DeviceInfo& dev, const void* q, const Paged
         if (e != cudaSuccess) return e;
         attr_done[dev.device] = true;
     }
-    const int maxC = int((a.max_seq_len + CHUNK - 1) / CHUNK);
+    const int chunk = 1 << chunk_log2;
+    const int maxC = int((a.max_seq_len + chunk - 1) / chunk);
     const int64_t items_bound = a.batch * int64_t(maxC) * a.hkv;
     if (items_bound > 0x7fffffffLL) return cudaErrorNotSupported;
     const int grid = int(items_bound < dev.num_sms ? items_bound : dev.num_sms);
@@ -819,20 +823,63 @@ cudaError_t launch_attention_t(const DeviceInfo& dev, const void* q, const Paged
         kern, dim3(grid), dim3(THREADS), Cf::SMEM, stream, tk, tv,
         static_cast<const __nv_bfloat16*>(q), a.block_table, int(a.max_pages), int(a.num_pages),
         a.seq_lens, a.cu_q, int(a.batch), int(a.total_q), int(a.max_q), int(a.max_seq_len),
-        int(a.hq), int(a.hkv), scale_log2, ws_o, ws_ml, maxC, dev.err_word);
+        int(a.hq), int(a.hkv), scale_log2, ws_o, ws_ml, maxC, chunk_log2, dev.err_word);
     if (e != cudaSuccess) return e;
     return launch_pdl(attn_merge_kernel<D>, dim3(unsigned(a.total_q * a.hq)),
                       dim3(MERGE_WARPS * 32), 0, stream, a.seq_lens, a.cu_q, int(a.batch),
                       int(a.total_q), int(a.max_q), int(a.max_seq_len), int(a.hq),
                       static_cast<const float*>(ws_o), static_cast<const float*>(ws_ml), maxC,
-                      static_cast<__nv_bfloat16*>(out), lse);
+                      chunk_log2, static_cast<__nv_bfloat16*>(out), lse);
 }
 
 }  // namespace
 
-size_t attn_workspace_bytes(int64_t total_q, int64_t hq, int64_t head_dim, int64_t max_seq_len) {
-    const int64_t chunks = (max_seq_len + CHUNK - 1) / CHUNK;
+namespace {
+size_t workspace_for(int64_t total_q, int64_t hq, int64_t head_dim, int64_t max_seq_len,
+                     int chunk_log2) {
+    const int64_t chunk = int64_t(1) << chunk_log2;
+    const int64_t chunks = (max_seq_len + chunk - 1) / chunk;
     return size_t(total_q) * size_t(hq) * size_t(chunks) * size_t(head_dim + 2) * sizeof(float);
+}
+}  // namespace
+
+size_t attn_workspace_bytes(int64_t total_q, int64_t hq, int64_t head_dim, int64_t max_seq_len) {
+    return workspace_for(total_q, hq, head_dim, max_seq_len, CHUNK_LOG2);
+}
+
+int attn_chunk_log2(const PagedArgs& a, size_t ws_bytes, int num_sms, bool invariant) {
+    if (invariant) return CHUNK_LOG2;
+    // Non-invariant call: the chunk length that minimises a simple cost in page-times.
+    // Sequences are taken to be max_seq_len long.  Work items are dealt round-robin to
+    // the persistent CTAs, so the busiest CTA runs ceil(items / SMs) of them; in the
+    // worst case only one in every (chunks per sequence) of those is a short last chunk.
+    // An item costs its pages plus a fixed overhead (pipeline turn-around, ~half a page)
+    // plus its partials (written by the partial kernel, read back by the merge) in
+    // page-equivalents of K+V bytes.  Ties go to the longer chunk (fewer partials).
+    // Only chunk lengths whose partials fit in the caller's workspace are considered.
+    const int64_t group = a.hq / a.hkv;
+    const double page_bytes = double(PAGE) * double(a.head_dim) * 2.0 * 2.0;
+    const double item_ovh =
+        0.5 + double(a.max_q * group) * double(a.head_dim + 2) * 4.0 * 2.0 / page_bytes;
+    int best = CHUNK_LOG2;
+    double best_cost = -1.0;
+    for (int lg = MAX_CHUNK_LOG2; lg >= MIN_CHUNK_LOG2; --lg) {
+        if (workspace_for(a.total_q, a.hq, a.head_dim, a.max_seq_len, lg) > ws_bytes) continue;
+        const int64_t chunk = int64_t(1) << lg;
+        const int64_t chunks = (a.max_seq_len + chunk - 1) / chunk;
+        const int64_t items = a.batch * a.hkv * chunks;
+        const int64_t per_cta = (items + num_sms - 1) / num_sms;
+        const int64_t tails = per_cta / chunks;
+        const double full_pages = double(chunk / PAGE);
+        const double tail_pages = double((a.max_seq_len - (chunks - 1) * chunk + PAGE - 1) / PAGE);
+        const double cost = double(per_cta) * item_ovh + double(per_cta - tails) * full_pages +
+                            double(tails) * tail_pages;
+        if (best_cost < 0.0 || cost < best_cost) {
+            best_cost = cost;
+            best = lg;
+        }
+    }
+    return best;
 }
 
 cudaError_t launch_kv_append(const DeviceInfo& dev, const void* k_new, const void* v_new,
@@ -848,9 +895,11 @@ cudaError_t launch_kv_append(const DeviceInfo& dev, const void* k_new, const voi
 
 cudaError_t launch_attention(const DeviceInfo& dev, const void* q, const PagedArgs& a,
                              float scale, void* out, float* lse, void* workspace,
-                             cudaStream_t stream) {
-    if (a.head_dim == 64) return launch_attention_t<64>(dev, q, a, scale, out, lse, workspace, stream);
-    return launch_attention_t<128>(dev, q, a, scale, out, lse, workspace, stream);
+                             int chunk_log2, cudaStream_t stream) {
+    if (chunk_log2 < MIN_CHUNK_LOG2 || chunk_log2 > MAX_CHUNK_LOG2) return cudaErrorNotSupported;
+    if (a.head_dim == 64)
+        return launch_attention_t<64>(dev, q, a, scale, out, lse, workspace, chunk_log2, stream);
+    return launch_attention_t<128>(dev, q, a, scale, out, lse, workspace, chunk_log2, stream);
 }
 
 }  // namespace bi

@@ -60,6 +60,7 @@ constexpr int MAX_NSUB = 256 / BN;          // two accumulators of nsub*BN colum
 constexpr int MAX_KBS = 8;                  // K-blocks per ring stage (K-major operands)
 constexpr int MAX_KBS_KN = 4;               // N-major W: one box spans 64*kbs <= 256 k-rows
 constexpr int MAX_STAGES = 48;
+constexpr int MAX_SPLITS = 8;               // split-K cluster size (portable maximum)
 constexpr int THREADS = 192;
 constexpr int EPI_THREADS = 128;
 constexpr int B_KB_BYTES = BN * BK * 2;     // one instruction tile's W block per K-block
@@ -74,7 +75,7 @@ constexpr int KN_SWIZZLE = KN_ATOM_N * 2;          // 64 or 128 bytes
 constexpr uint32_t KN_LAYOUT = KN_SWIZZLE == 128 ? 2u : 4u;
 
 static_assert(BN == 32 || BN == 64 || BN == 128, "instruction N must be 32, 64 or 128");
-static_assert((2 * MAX_STAGES + 5) * 8 + 16 <= CTRL_BYTES, "control block too small");
+static_assert((2 * MAX_STAGES + 7) * 8 + 16 <= CTRL_BYTES, "control block too small");
 
 struct GemmArgs {
     void* y;
@@ -86,9 +87,14 @@ struct GemmArgs {
     int blocked;         // K % 64 == 0: one rank-3 copy per operand per stage
     int stages;          // ring depth
     int w_stream_once;   // one M-tile: W is read exactly once (L2 evict-first hint)
+    // Split-K (the non-invariant kernel only): a cluster of `splits` CTAs shares each
+    // output tile, CTA rank r accumulating K-blocks [r*kb_per_split, (r+1)*kb_per_split).
+    // The invariant kernel has splits = 1 and kb_per_split = the number of K-blocks.
+    int splits;
+    int kb_per_split;
 };
 
-template <bool KN, bool F32OUT, int NSUB>
+template <bool KN, bool F32OUT, int NSUB, bool SPLIT>
 __global__ void __launch_bounds__(THREADS, 1)
 gemm_kernel(const __grid_constant__ CUtensorMap tmap_x, const __grid_constant__ CUtensorMap tmap_w,
             const GemmArgs args, unsigned int* err) {
@@ -107,7 +113,9 @@ gemm_kernel(const __grid_constant__ CUtensorMap tmap_x, const __grid_constant__ 
     uint64_t* tfull = empty + MAX_STAGES;
     uint64_t* tempty = tfull + 2;
     uint64_t* drain = tempty + 2;
-    uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(drain + 1);
+    uint64_t* red_full = drain + 1;  // split-K, rank 0: the other ranks' partials are in
+    uint64_t* red_free = drain + 2;  // split-K, rank > 0: rank 0 has read this rank's slot
+    uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(drain + 3);
     volatile int* abort_flag = reinterpret_cast<volatile int*>(tmem_slot + 1);
 
     const int warp = threadIdx.x >> 5;
@@ -118,6 +126,16 @@ gemm_kernel(const __grid_constant__ CUtensorMap tmap_x, const __grid_constant__ 
     const int n_tiles = (N + tile_n - 1) / tile_n;
     const int num_tiles = m_tiles * n_tiles;
     const int nkb = (K + BK - 1) / BK;
+    // Tiles are dealt out to CTAs (to clusters of `splits` CTAs when split), and this CTA
+    // accumulates K-blocks [kb0, kb1) of each of its tiles.
+    int rank = 0, first_tile = int(blockIdx.x), tile_step = int(gridDim.x);
+    if constexpr (SPLIT) {
+        rank = int(cluster_ctarank());
+        first_tile = int(cluster_id_x());
+        tile_step = int(cluster_count_x());
+    }
+    const int kb0 = rank * args.kb_per_split;
+    const int kb1 = kb0 + args.kb_per_split < nkb ? kb0 + args.kb_per_split : nkb;
     const uint32_t tmem_cols = uint32_t(2 * tile_n);  // two accumulators, power of two
 
     if (threadIdx.x == 0) {
@@ -130,6 +148,10 @@ gemm_kernel(const __grid_constant__ CUtensorMap tmap_x, const __grid_constant__ 
             mbar_init(&tempty[a], EPI_THREADS);
         }
         mbar_init(drain, 1);
+        if constexpr (SPLIT) {
+            mbar_init(red_full, uint32_t((args.splits - 1) * EPI_THREADS));
+            mbar_init(red_free, EPI_THREADS);
+        }
         *abort_flag = 0;
         fence_barrier_init();
     }
@@ -144,6 +166,8 @@ gemm_kernel(const __grid_constant__ CUtensorMap tmap_x, const __grid_constant__ 
     tc_fence_before_sync();
     __syncthreads();
     tc_fence_after_sync();
+    // the other CTAs of the cluster signal this CTA's barriers: all are initialised first
+    if constexpr (SPLIT) cluster_sync_all();
     const uint32_t tmem_base = *tmem_slot;
     // The set-up above touches no global memory.  The previous grid in the stream may
     // still be running: the producer starts fetching W (which no kernel of this library
@@ -217,10 +241,10 @@ gemm_kernel(const __grid_constant__ CUtensorMap tmap_x, const __grid_constant__ 
         // straight into the (empty) ring, so the weight stream overlaps the previous
         // kernel's tail.
         int early = 0;  // stages of the first tile whose W is already issued
-        if (int(blockIdx.x) < num_tiles) {
-            const int n0 = (int(blockIdx.x) % n_tiles) * tile_n;
-            for (int kb = 0; kb < nkb && early < S; kb += kbs, ++early) {
-                const int nk = nkb - kb < kbs ? nkb - kb : kbs;
+        if (first_tile < num_tiles) {
+            const int n0 = (first_tile % n_tiles) * tile_n;
+            for (int kb = kb0; kb < kb1 && early < S; kb += kbs, ++early) {
+                const int nk = kb1 - kb < kbs ? kb1 - kb : kbs;
                 if (elect_one()) {
                     mbar_arrive_expect_tx_s(full_s + uint32_t(early) * 8u, stage_tx(nk));
                     issue_w(uint32_t(early), n0, kb, nk);
@@ -230,16 +254,16 @@ gemm_kernel(const __grid_constant__ CUtensorMap tmap_x, const __grid_constant__ 
         }
         pdl_wait();
 
-        for (int t = blockIdx.x; ok && t < num_tiles; t += gridDim.x) {
+        for (int t = first_tile; ok && t < num_tiles; t += tile_step) {
             const int mt = t / n_tiles, nt = t % n_tiles;
             const int m0 = mt * BM, n0 = nt * tile_n;
-            for (int kb = 0; kb < nkb; kb += kbs) {
+            for (int kb = kb0; kb < kb1; kb += kbs) {
                 if (!mbar_wait_warp(&empty[stage], phase ^ 1u, abort_flag)) {
                     ok = false;
                     break;
                 }
                 if (elect_one()) {
-                    const int nk = nkb - kb < kbs ? nkb - kb : kbs;  // K-blocks in this stage
+                    const int nk = kb1 - kb < kbs ? kb1 - kb : kbs;  // K-blocks in this stage
                     if (int(issued) >= early) {
                         mbar_arrive_expect_tx_s(full_s + stage * 8u, stage_tx(nk));
                         issue_w(stage, n0, kb, nk);
@@ -288,7 +312,7 @@ gemm_kernel(const __grid_constant__ CUtensorMap tmap_x, const __grid_constant__ 
         uint32_t stage = 0, phase = 0;
         bool ok = true;
         int local = 0;
-        for (int t = blockIdx.x; ok && t < num_tiles; t += gridDim.x, ++local) {
+        for (int t = first_tile; ok && t < num_tiles; t += tile_step, ++local) {
             const int acc = local & 1;
             const uint32_t acc_phase = (local >> 1) & 1;
             if (!mbar_wait_warp(&tempty[acc], acc_phase ^ 1u, abort_flag)) {
@@ -297,20 +321,20 @@ gemm_kernel(const __grid_constant__ CUtensorMap tmap_x, const __grid_constant__ 
             }
             tc_fence_after_sync();
             const uint32_t d_tmem = tmem_base + uint32_t(acc * tile_n);
-            for (int kb = 0; kb < nkb; kb += kbs) {
+            for (int kb = kb0; kb < kb1; kb += kbs) {
                 if (!mbar_wait_warp(&full[stage], phase, abort_flag)) {
                     ok = false;
                     break;
                 }
                 tc_fence_after_sync();
-                const int nk = nkb - kb < kbs ? nkb - kb : kbs;
+                const int nk = kb1 - kb < kbs ? kb1 - kb : kbs;
                 if (elect_one()) {
                     // descriptors are advanced by adding (byte offset >> 4) to the start-
                     // address field; shared addresses stay below 2^18 so it never carries
                     uint64_t a_blk = a_desc0 + (uint64_t(stage * stage_a) >> 4);
                     uint64_t b_blk = b_desc0 + (uint64_t(stage * stage_b) >> 4);
                     for (int i = 0; i < nk; ++i, a_blk += a_step, b_blk += b_step) {
-                        const uint32_t first = (kb + i) == 0 ? 1u : 0u;
+                        const uint32_t first = (kb + i) == kb0 ? 1u : 0u;
 #pragma unroll
                         for (int k = 0; k < BK / UK; ++k) {
                             const uint64_t a_desc = a_blk + uint64_t(k * A_K16);
@@ -348,23 +372,78 @@ gemm_kernel(const __grid_constant__ CUtensorMap tmap_x, const __grid_constant__ 
         const int64_t ldy = args.ldy;
         const bool vec_ok = F32OUT ? ((ldy % 4) == 0 && (reinterpret_cast<uintptr_t>(y) % 16) == 0)
                                    : ((ldy % 8) == 0 && (reinterpret_cast<uintptr_t>(y) % 16) == 0);
-        for (int t = blockIdx.x; t < num_tiles; t += gridDim.x, ++local) {
+        // Split-K: rank r > 0 hands its fp32 partial to rank 0 through rank 0's shared
+        // memory (slot r-1 at the top of the ring area: a_rows rows of tile_n floats, the
+        // 16-byte pieces of row i rotated by i & 7 so that a warp's stores and loads hit
+        // distinct banks); rank 0 adds the slots to its own accumulator in ascending rank
+        // order, i.e. in ascending K.  Only warps whose lanes hold staged rows (live) touch
+        // tensor memory or the slots; every epilogue thread joins every barrier.
+        const int red_rows = args.a_rows;
+        const bool live = !SPLIT || quad * 32 < red_rows;
+        const bool red_row = row_in_tile < red_rows;
+        const uint32_t slot_bytes = uint32_t(red_rows * tile_n * 4);
+        const uint32_t red_base =
+            smem_addr(smem + RING_BYTES) - uint32_t(args.splits - 1) * slot_bytes;
+        const uint32_t row_off = uint32_t(row_in_tile * tile_n * 4);
+        const uint32_t rot = uint32_t(row_in_tile & 7);
+        uint32_t to_slot = 0, to_full = 0;
+        if (SPLIT && rank != 0) {
+            to_slot = cluster_map(red_base + uint32_t(rank - 1) * slot_bytes, 0);
+            to_full = cluster_map(smem_addr(red_full), 0);
+        }
+        for (int t = first_tile; t < num_tiles; t += tile_step, ++local) {
             const int acc = local & 1;
             const uint32_t acc_phase = (local >> 1) & 1;
             if (!mbar_wait_warp(&tfull[acc], acc_phase, abort_flag)) {
                 if (!*abort_flag) fail();
                 break;
             }
+            if (SPLIT) {
+                // rank 0: every partial of this tile has arrived; rank > 0: rank 0 has
+                // read this rank's previous partial out of the slot
+                const bool got = rank == 0
+                    ? mbar_wait_warp<true>(red_full, uint32_t(local & 1), abort_flag)
+                    : mbar_wait_warp<true>(red_free, uint32_t(local & 1) ^ 1u, abort_flag);
+                if (!got) {
+                    if (!*abort_flag) fail();
+                    break;
+                }
+            }
             tc_fence_after_sync();
             const int mt = t / n_tiles, nt = t % n_tiles;
             const int64_t gm = int64_t(mt) * BM + row_in_tile;
             for (int c = 0; c < tile_n; c += 32) {
                 uint32_t r[32];
-                tmem_load_32x32b_x32(
-                    tmem_base + (uint32_t(quad * 32) << 16) + uint32_t(acc * tile_n + c), r);
-                tmem_load_wait();
+                if (live) {
+                    tmem_load_32x32b_x32(
+                        tmem_base + (uint32_t(quad * 32) << 16) + uint32_t(acc * tile_n + c), r);
+                    tmem_load_wait();
+                }
+                if (SPLIT && rank != 0) {
+                    if (live && red_row) {
+#pragma unroll
+                        for (int q = 0; q < 8; ++q)
+                            st_cluster_v4(to_slot + row_off +
+                                              ((uint32_t(c / 4 + q) ^ rot) << 4),
+                                          r[4 * q], r[4 * q + 1], r[4 * q + 2], r[4 * q + 3]);
+                    }
+                    continue;  // rank > 0 writes nothing to Y
+                }
+                if (SPLIT && live && red_row) {
+                    for (int sp = 1; sp < args.splits; ++sp) {
+                        const uint32_t src = red_base + uint32_t(sp - 1) * slot_bytes + row_off;
+#pragma unroll
+                        for (int q = 0; q < 8; ++q) {
+                            const float4 v = ld_shared_v4f(src + ((uint32_t(c / 4 + q) ^ rot) << 4));
+                            r[4 * q] = __float_as_uint(__uint_as_float(r[4 * q]) + v.x);
+                            r[4 * q + 1] = __float_as_uint(__uint_as_float(r[4 * q + 1]) + v.y);
+                            r[4 * q + 2] = __float_as_uint(__uint_as_float(r[4 * q + 2]) + v.z);
+                            r[4 * q + 3] = __float_as_uint(__uint_as_float(r[4 * q + 3]) + v.w);
+                        }
+                    }
+                }
                 const int64_t gn0 = int64_t(nt) * tile_n + c;
-                if (gm < M && gn0 < N) {
+                if (live && gm < M && gn0 < N) {
                     if (F32OUT) {
                         float* yr = static_cast<float*>(y) + gm * ldy + gn0;
                         if (vec_ok && gn0 + 32 <= N) {
@@ -399,6 +478,16 @@ gemm_kernel(const __grid_constant__ CUtensorMap tmap_x, const __grid_constant__ 
             }
             tc_fence_before_sync();
             mbar_arrive(&tempty[acc]);
+            if (SPLIT) {
+                // release (cluster scope) orders this thread's slot stores / slot loads
+                // before the signal
+                if (rank != 0) {
+                    mbar_arrive_cluster(to_full);
+                } else {
+                    for (int sp = 1; sp < args.splits; ++sp)
+                        mbar_arrive_cluster(cluster_map(smem_addr(red_free), uint32_t(sp)));
+                }
+            }
         }
     }
 
@@ -408,12 +497,15 @@ gemm_kernel(const __grid_constant__ CUtensorMap tmap_x, const __grid_constant__ 
         tc_fence_after_sync();
         tmem_dealloc(tmem_base, tmem_cols);
     }
+    // no CTA leaves while another CTA of its cluster may still signal its barriers or
+    // write its shared memory (every loop above ends, by completion or by timeout)
+    if constexpr (SPLIT) cluster_sync_all();
 }
 
 template <bool KN, bool F32OUT, int NSUB>
 cudaError_t launch_t(const DeviceInfo& dev, const CUtensorMap& mx, const CUtensorMap& mw,
                      const GemmArgs& a, int grid, cudaStream_t s) {
-    auto kern = gemm_kernel<KN, F32OUT, NSUB>;
+    auto kern = gemm_kernel<KN, F32OUT, NSUB, false>;
     static bool attr_done[64] = {};
     if (dev.device >= 0 && dev.device < 64 && !attr_done[dev.device]) {
         cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize,
@@ -422,6 +514,47 @@ cudaError_t launch_t(const DeviceInfo& dev, const CUtensorMap& mx, const CUtenso
         attr_done[dev.device] = true;
     }
     return launch_pdl(kern, dim3(grid), dim3(THREADS), SMEM_BYTES, s, mx, mw, a, dev.err_word);
+}
+
+// The split-K kernel: clusters of a.splits CTAs, as many clusters as fit on the GPU at
+// once (cluster placement is limited by the GPCs, so this can be fewer than SMs/splits),
+// never more than there are tiles.
+template <bool KN, bool F32OUT>
+cudaError_t launch_split(const DeviceInfo& dev, const CUtensorMap& mx, const CUtensorMap& mw,
+                         const GemmArgs& a, int64_t tiles, cudaStream_t s) {
+    auto kern = gemm_kernel<KN, F32OUT, 1, true>;
+    static bool attr_done[64] = {};
+    static int fit[64][MAX_SPLITS + 1] = {};  // co-resident clusters per device and size
+    if (dev.device < 0 || dev.device >= 64 || a.splits < 2 || a.splits > MAX_SPLITS)
+        return cudaErrorNotSupported;
+    if (!attr_done[dev.device]) {
+        cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                             SMEM_BYTES);
+        if (e != cudaSuccess) return e;
+        attr_done[dev.device] = true;
+    }
+    int& n_fit = fit[dev.device][a.splits];
+    if (n_fit == 0) {
+        cudaLaunchConfig_t cfg = {};
+        cfg.gridDim = dim3(unsigned(a.splits));
+        cfg.blockDim = dim3(THREADS);
+        cfg.dynamicSmemBytes = SMEM_BYTES;
+        cudaLaunchAttribute attr[1];
+        attr[0].id = cudaLaunchAttributeClusterDimension;
+        attr[0].val.clusterDim.x = unsigned(a.splits);
+        attr[0].val.clusterDim.y = 1;
+        attr[0].val.clusterDim.z = 1;
+        cfg.attrs = attr;
+        cfg.numAttrs = 1;
+        int n = 0;
+        cudaError_t e = cudaOccupancyMaxActiveClusters(&n, kern, &cfg);
+        if (e != cudaSuccess) return e;
+        if (n < 1) return cudaErrorNotSupported;
+        n_fit = n;
+    }
+    const int clusters = int(tiles < n_fit ? tiles : n_fit);
+    return launch_pdl_cluster(kern, dim3(unsigned(clusters * a.splits)), dim3(THREADS),
+                              SMEM_BYTES, s, unsigned(a.splits), mx, mw, a, dev.err_word);
 }
 
 template <bool KN, bool F32OUT>
@@ -439,9 +572,11 @@ cudaError_t launch_nsub(const DeviceInfo& dev, const CUtensorMap& mx, const CUte
 
 int gemm_tile_n() { return BN; }
 
-GemmSchedule gemm_schedule(int64_t M, int64_t N, int64_t K, bool w_kn, int num_sms) {
+GemmSchedule gemm_schedule(int64_t M, int64_t N, int64_t K, bool w_kn, int num_sms,
+                           bool split_ok) {
     GemmSchedule g;
     const int64_t m_tiles = (M + BM - 1) / BM;
+    const int64_t nkb = (K + BK - 1) / BK;
     g.a_rows = m_tiles == 1 ? int((M + 7) / 8 * 8) : BM;
     // widest CTA tile that still gives every SM a tile (X is then re-read from L2 the
     // fewest times); a single instruction tile per CTA when even that is too few
@@ -452,18 +587,44 @@ GemmSchedule gemm_schedule(int64_t M, int64_t N, int64_t K, bool w_kn, int num_s
             break;
         }
     }
+    // Split-K (non-invariant kernel only): a single M-tile whose instruction tiles leave
+    // SMs idle gets a cluster of CTAs per tile, each over a contiguous K range, so more
+    // SMs stream W and each runs a shorter chain of dependent MMAs.  The reduction slots
+    // come out of the ring.
+    g.splits = 1;
+    g.ring_bytes = RING_BYTES;
+    if (split_ok && m_tiles == 1 && g.nsub == 1) {
+        int64_t sp = num_sms / ((N + BN - 1) / BN);
+        if (sp > MAX_SPLITS) sp = MAX_SPLITS;
+        if (sp > nkb) sp = nkb;
+        // the ring keeps room for at least four stages of one K-block
+        const int64_t slot = int64_t(g.a_rows) * BN * 4;
+        const int64_t blk1 = int64_t(g.a_rows) * BK * 2 + B_KB_BYTES;
+        while (sp >= 2 && RING_BYTES - (sp - 1) * slot < 4 * blk1) --sp;
+        if (sp >= 2) {
+            g.splits = int(sp);
+            g.ring_bytes = RING_BYTES - (g.splits - 1) * g.a_rows * BN * 4;
+        }
+    }
     // as many K-blocks per stage as keep at least four stages in the ring (fewer
-    // barrier round trips per MMA)
+    // barrier round trips per MMA) -- and, when split, at least four stages per CTA
     const int blk_bytes = g.a_rows * BK * 2 + g.nsub * B_KB_BYTES;
+    const int64_t per_cta = (nkb + g.splits - 1) / g.splits;
     g.kbs = 1;
     for (int kbs = w_kn ? MAX_KBS_KN : MAX_KBS; kbs >= 2; kbs >>= 1) {
-        if (RING_BYTES / (kbs * blk_bytes) >= 4) {
+        if (g.ring_bytes / (kbs * blk_bytes) >= 4 && (g.splits == 1 || per_cta >= 4 * kbs)) {
             g.kbs = kbs;
             break;
         }
     }
-    g.stages = RING_BYTES / (g.kbs * blk_bytes);
+    g.stages = g.ring_bytes / (g.kbs * blk_bytes);
     if (g.stages > MAX_STAGES) g.stages = MAX_STAGES;
+    g.kb_per_split = int(nkb);
+    if (g.splits > 1) {
+        const int64_t per = (per_cta + g.kbs - 1) / g.kbs * g.kbs;  // whole stages per CTA
+        g.splits = int((nkb + per - 1) / per);                     // no CTA without work
+        g.kb_per_split = int(per);
+    }
     g.tiles = m_tiles * ((N + int64_t(g.nsub) * BN - 1) / (int64_t(g.nsub) * BN));
     g.blocked = (K % BK) == 0 ? 1 : 0;
     return g;
@@ -471,20 +632,20 @@ GemmSchedule gemm_schedule(int64_t M, int64_t N, int64_t K, bool w_kn, int num_s
 
 cudaError_t launch_gemm(const DeviceInfo& dev, const void* x, int64_t ldx, const void* w,
                         int64_t ldw, bool w_kn, void* y, int64_t ldy, bool y_f32, int64_t M,
-                        int64_t N, int64_t K, cudaStream_t stream) {
+                        int64_t N, int64_t K, bool split_ok, cudaStream_t stream) {
     if (M == 0 || N == 0) return cudaSuccess;
     if (K == 0) {
         // an empty reduction: every output is +0 (all-zero bits in bf16 and fp32)
         const size_t es = y_f32 ? 4 : 2;
         return cudaMemset2DAsync(y, size_t(ldy) * es, 0, size_t(N) * es, size_t(M), stream);
     }
-    const GemmSchedule g = gemm_schedule(M, N, K, w_kn, dev.num_sms);
+    const GemmSchedule g = gemm_schedule(M, N, K, w_kn, dev.num_sms, split_ok);
     // an MMA reads A_MMA_BYTES from the start of its X block: the last X block's read must
     // stay inside the ring (it runs into the W blocks that follow the X blocks)
     const int64_t a_bytes = int64_t(g.a_rows) * BK * 2;
     const int64_t blocks = int64_t(g.stages) * g.kbs;
     if ((blocks - 1) * a_bytes + A_MMA_BYTES > blocks * (a_bytes + int64_t(g.nsub) * B_KB_BYTES) ||
-        blocks * (a_bytes + int64_t(g.nsub) * B_KB_BYTES) > RING_BYTES || g.stages < 2)
+        blocks * (a_bytes + int64_t(g.nsub) * B_KB_BYTES) > g.ring_bytes || g.stages < 2)
         return cudaErrorNotSupported;
     CUtensorMap mx, mw;
     bool ok;
@@ -516,6 +677,13 @@ cudaError_t launch_gemm(const DeviceInfo& dev, const void* x, int64_t ldx, const
     a.blocked = g.blocked;
     a.stages = g.stages;
     a.w_stream_once = (M + BM - 1) / BM == 1 ? 1 : 0;
+    a.splits = g.splits;
+    a.kb_per_split = g.kb_per_split;
+    if (g.splits > 1)
+        return w_kn ? (y_f32 ? launch_split<true, true>(dev, mx, mw, a, g.tiles, stream)
+                             : launch_split<true, false>(dev, mx, mw, a, g.tiles, stream))
+                    : (y_f32 ? launch_split<false, true>(dev, mx, mw, a, g.tiles, stream)
+                             : launch_split<false, false>(dev, mx, mw, a, g.tiles, stream));
     const int grid = int(g.tiles < dev.num_sms ? g.tiles : dev.num_sms);
     if (w_kn)
         return y_f32 ? launch_nsub<true, true>(dev, mx, mw, a, grid, stream)

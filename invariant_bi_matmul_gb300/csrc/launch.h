@@ -37,6 +37,27 @@ cudaError_t launch_pdl(void (*kernel)(KArgs...), dim3 grid, dim3 block, size_t s
     return cudaLaunchKernelEx(&cfg, kernel, std::forward<Args>(args)...);
 }
 
+// launch_pdl for a kernel launched in clusters of `cluster_x` CTAs along x.
+template <typename... KArgs, typename... Args>
+cudaError_t launch_pdl_cluster(void (*kernel)(KArgs...), dim3 grid, dim3 block, size_t smem,
+                               cudaStream_t stream, unsigned cluster_x, Args&&... args) {
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = grid;
+    cfg.blockDim = block;
+    cfg.dynamicSmemBytes = smem;
+    cfg.stream = stream;
+    cudaLaunchAttribute attr[2];
+    attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr[0].val.programmaticStreamSerializationAllowed = 1;
+    attr[1].id = cudaLaunchAttributeClusterDimension;
+    attr[1].val.clusterDim.x = cluster_x;
+    attr[1].val.clusterDim.y = 1;
+    attr[1].val.clusterDim.z = 1;
+    cfg.attrs = attr;
+    cfg.numAttrs = 2;
+    return cudaLaunchKernelEx(&cfg, kernel, std::forward<Args>(args)...);
+}
+
 struct DeviceInfo {
     int device = -1;
     int num_sms = 0;
@@ -55,20 +76,26 @@ cudaError_t launch_rmsnorm(const void* x, int64_t ldx, const void* gamma, void* 
 // Returns cudaErrorNotSupported when a TMA descriptor cannot be encoded.
 cudaError_t launch_gemm(const DeviceInfo& dev, const void* x, int64_t ldx, const void* w,
                         int64_t ldw, bool w_kn, void* y, int64_t ldy, bool y_f32, int64_t M,
-                        int64_t N, int64_t K, cudaStream_t stream);
+                        int64_t N, int64_t K, bool split_ok, cudaStream_t stream);
 int gemm_tile_n();
 
-// How a GEMM launch is scheduled (never what it computes): X rows staged per K-block,
-// 32-wide instruction tiles per CTA tile, shared-memory ring depth, CTA tiles.
+// How a GEMM launch is scheduled: X rows staged per K-block, instruction tiles per CTA
+// tile, shared-memory ring depth, CTA tiles -- none of which changes what an element
+// computes -- and, only when split_ok (a call outside the batch-invariant limit), the
+// split-K factor, which does.
 struct GemmSchedule {
     int a_rows = 128;
     int nsub = 1;
     int kbs = 1;
     int blocked = 0;
     int stages = 0;
+    int ring_bytes = 0;
+    int splits = 1;        // CTAs (one cluster) per output tile, each over a K range
+    int kb_per_split = 0;  // 64-wide K-blocks per split
     int64_t tiles = 0;
 };
-GemmSchedule gemm_schedule(int64_t M, int64_t N, int64_t K, bool w_kn, int num_sms);
+GemmSchedule gemm_schedule(int64_t M, int64_t N, int64_t K, bool w_kn, int num_sms,
+                           bool split_ok);
 
 // ------------------------------------------------------------ attention (attention.cu)
 struct PagedArgs {
@@ -94,9 +121,14 @@ cudaError_t launch_kv_append(const DeviceInfo& dev, const void* k_new, const voi
 
 size_t attn_workspace_bytes(int64_t total_q, int64_t hq, int64_t head_dim, int64_t max_seq_len);
 
+// The split-KV chunk length (log2 of keys per work item) of a call: the fixed invariant
+// length when `invariant`, else the length a cost model picks from the call's sizes,
+// the SM count and the workspace.
+int attn_chunk_log2(const PagedArgs& a, size_t ws_bytes, int num_sms, bool invariant);
+
 cudaError_t launch_attention(const DeviceInfo& dev, const void* q, const PagedArgs& a,
                              float scale, void* out, float* lse, void* workspace,
-                             cudaStream_t stream);
+                             int chunk_log2, cudaStream_t stream);
 
 cudaError_t launch_selftest_wait(const DeviceInfo& dev, unsigned long long timeout_ns,
                                  cudaStream_t stream);

@@ -22,6 +22,11 @@ to 8 tokens (the widest verify block); ``start`` instead loads synthetic cache r
 (seeded N(0,1) keys and values per sequence and layer, written with bi_kv_append), for
 small checks against the oracle.  Either way a sequence's context depends only on the
 sequence, never on the batch it runs in.
+
+The traces are batch invariant only while every call is inside the batch-invariant
+limit: matmuls of up to ``max_batch * max_width`` rows and verify blocks of up to
+``max_width`` tokens.  An ``invariant=True`` decoder (the default) refuses to run a block
+the current limit does not cover; ``invariant=False`` runs whatever the limit selects.
 """
 from __future__ import annotations
 
@@ -31,7 +36,7 @@ from typing import Callable, List, Optional, Sequence
 import torch
 
 from . import (add, argmax, attn_workspace_size, embedding, kv_append, matmul, rmsnorm, rope,
-               swiglu, verify_block)
+               swiglu, verify_block, within_batch_invariant_limit)
 from .inputs import PAGE_SIZE, DecoderConfig, decoder_context, decoder_first_token, page_permutation
 
 Drafter = Callable[[int, List[int], int], List[int]]
@@ -42,8 +47,10 @@ class GreedyDecoder:
     ``max_len`` tokens, evaluated in blocks of up to ``max_width`` tokens per sequence."""
 
     def __init__(self, cfg: DecoderConfig, weights: dict, max_batch: int, max_len: int,
-                 max_width: int = 4, device="cuda", page_seed: int = 0):
+                 max_width: int = 4, device="cuda", page_seed: int = 0,
+                 invariant: bool = True):
         self.cfg, self.w = cfg, weights
+        self.invariant = invariant
         self.dev = torch.device(device)
         self.max_batch, self.max_len, self.max_width = max_batch, max_len, max_width
         c = cfg
@@ -128,6 +135,12 @@ class GreedyDecoder:
         lens = [self.cached[b] + q_lens[b] for b in range(B)]
         if max(lens) > self.max_len:
             raise ValueError("sequence longer than max_len")
+        if self.invariant and not (within_batch_invariant_limit(T) and
+                                   within_batch_invariant_limit(max(q_lens))):
+            raise RuntimeError(f"the batch-invariant limit does not cover a block of {T} tokens "
+                               f"(widest {max(q_lens)}): raise it with "
+                               "set_batch_invariant_limit, or build the decoder with "
+                               "invariant=False")
         cu = [0]
         for q in q_lens:
             cu.append(cu[-1] + q)
