@@ -476,9 +476,16 @@ def main():
     ap.add_argument("--cpu-sample", action="store_true", default=True)
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--sweep", action="store_true")
+    ap.add_argument("--case", default=None,
+                    help="time one call shape instead of the step (for profiling): "
+                         "gemm:M:N:K[:kn][:fast] or attn:B:q:Lk[:fast]")
+    ap.add_argument("--case-reps", type=int, default=5)
     args = ap.parse_args()
     if args.warmup < 3:
         args.warmup = 3
+    if args.case:
+        run_case(args.case, args.case_reps)
+        return
 
     world = int(os.environ.get("WORLD_SIZE", "1"))
     rank = int(os.environ.get("RANK", "0"))
@@ -552,6 +559,64 @@ def main():
         "gemm_vs_cublas_m8": res["cublas"],
     }
     print(json.dumps(line), flush=True)
+
+
+def run_case(spec: str, reps: int):
+    """One call shape, `reps` times after three warm-up calls, each timed with CUDA events
+    (L2 evicted before each): the unit a profiler capture selects with -s 3 -c 1.
+    `fast` sets the batch-invariant limit to 0 (the non-invariant configuration), else
+    the limit covers the call."""
+    import torch
+    import invariant_bi_matmul_gb300 as bi
+    from invariant_bi_matmul_gb300 import inputs
+    parts = spec.split(":")
+    fast = "fast" in parts[1:]
+    bi.set_batch_invariant_limit(0 if fast else 1 << 40)
+    dev = torch.device("cuda:0")
+    flush = torch.ones(128 * 1024 * 1024, dtype=torch.float32, device=dev)
+    if parts[0] == "gemm":
+        M, N, K = (int(v) for v in parts[1:4])
+        lay = "kn" if "kn" in parts[4:] else "nk"
+        gi = inputs.gemm_inputs(M, N, K, seed=2)
+        x = gi.x.to(dev)
+        w = (gi.w_kn if lay == "kn" else gi.w_nk).to(dev)
+        y = torch.empty(M, N, dtype=torch.bfloat16, device=dev)
+        fn = lambda: bi.matmul(x, w, lay, out=y)  # noqa: E731
+        desc = {"case": "gemm", "M": M, "N": N, "K": K, "layout": lay,
+                "splits": bi.matmul_splits(M, N, K, lay,
+                                           torch.cuda.get_device_properties(dev).multi_processor_count)}
+    elif parts[0] == "attn":
+        B, q, L = (int(v) for v in parts[1:4])
+        p = inputs.paged_inputs([L] * B, [q] * B, Hq=HQ, Hkv=HKV, D=HEAD_DIM, seed=4, device=dev)
+        d = {k: getattr(p, k).to(dev) for k in ("q", "k_cache", "v_cache", "block_table",
+                                                 "seq_lens", "cu_q")}
+        ws = torch.empty(bi.attn_workspace_size(B * q, HQ, HEAD_DIM, L), dtype=torch.uint8,
+                         device=dev)
+        out = torch.empty(B * q, HQ, HEAD_DIM, dtype=torch.bfloat16, device=dev)
+        lse = torch.empty(B * q, HQ, dtype=torch.float32, device=dev)
+        fn = lambda: bi.verify_block(d["q"], d["k_cache"], d["v_cache"], d["block_table"],  # noqa: E731
+                                     d["seq_lens"], d["cu_q"], max_q=q, max_seq_len=L,
+                                     scale=1 / math.sqrt(HEAD_DIM), out=out, lse=lse,
+                                     workspace=ws)
+        desc = {"case": "attn", "B": B, "q": q, "Lk": L}
+    else:
+        raise SystemExit(f"unknown case {spec!r}")
+    for _ in range(3):
+        fn()
+    ts = []
+    for _ in range(reps):
+        flush.sum()
+        s0 = torch.cuda.Event(enable_timing=True)
+        s1 = torch.cuda.Event(enable_timing=True)
+        s0.record()
+        fn()
+        s1.record()
+        torch.cuda.synchronize()
+        ts.append(round(s0.elapsed_time(s1) * 1e3, 2))
+    if bi.device_status() != bi.BI_OK:
+        raise SystemExit("device error word set")
+    desc.update({"fast": fast, "us": ts})
+    print(json.dumps(desc), flush=True)
 
 
 def run_sweep():

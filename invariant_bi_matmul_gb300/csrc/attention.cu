@@ -81,9 +81,10 @@ struct Cfg {
     static constexpr int P_BYTES = MAXR * 128;
     static constexpr int RING_OFF = Q_BYTES + 2 * P_BYTES;
     static constexpr int BAR_OFF = RING_OFF + NST * STAGE_BYTES;
-    static constexpr int NBARS = 2 * NST + 14 + 2;      // ring, 7 pairs, q_full, drain
+    static constexpr int NBARS = 2 * NST + 16 + 2;      // ring, 8 pairs, q_full, drain
     static constexpr int XCH_OFF = BAR_OFF + NBARS * 8 + 16;
-    static constexpr int XCH_BYTES = 2 * (NSM + 1) * MAXR * 4;  // per item: sums, max
+    // per item: slice sums and the max; per page (two buffers): the slice maxima
+    static constexpr int XCH_BYTES = 2 * (NSM + 1) * MAXR * 4 + 2 * NSM * MAXR * 4;
     static constexpr int EPI_STRIDE = 32 * 4 + 16;      // staged O row: 32 floats + pad
     static constexpr size_t SMEM = 1024 + size_t(XCH_OFF) + XCH_BYTES + MAXR * EPI_STRIDE +
                                    NST * 4 + (MAX_BATCH + 1) * 4 + 2 * MAX_BATCH * 4 +
@@ -157,9 +158,11 @@ attn_partial_kernel(const __grid_constant__ CUtensorMap tmap_k,
     uint64_t* xs_bar = o_empty + 2;    // item k's row sums and max are in x_sum[k&1]
     uint64_t* q_full = xs_bar + 2;
     uint64_t* drain = q_full + 1;
-    uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(drain + 1);
+    uint64_t* xm_bar = drain + 1;      // page g's slice maxima are in x_max[g&1] (all warps)
+    uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(xm_bar + 2);
     float* x_sum = reinterpret_cast<float*>(smem + C::XCH_OFF);  // [2][NSM+1][MAXR]
-    uint8_t* epi_stage = reinterpret_cast<uint8_t*>(x_sum + 2 * (NSM + 1) * MAXR);
+    float* x_max = x_sum + 2 * (NSM + 1) * MAXR;                  // [2][NSM][MAXR]
+    uint8_t* epi_stage = reinterpret_cast<uint8_t*>(x_max + 2 * NSM * MAXR);
     int* stage_valid = reinterpret_cast<int*>(epi_stage + MAXR * C::EPI_STRIDE);
     int* prefix = stage_valid + NST;  // [B+1]
     int* seq_len = prefix + MAX_BATCH + 1;   // per sequence: length, first token, block width
@@ -192,6 +195,8 @@ attn_partial_kernel(const __grid_constant__ CUtensorMap tmap_k,
         }
         mbar_init(q_full, NSM);
         mbar_init(drain, 1);
+        mbar_init(&xm_bar[0], NSM);
+        mbar_init(&xm_bar[1], NSM);
         *abort_flag = 0;
         fence_barrier_init();
     }
@@ -503,11 +508,12 @@ attn_partial_kernel(const __grid_constant__ CUtensorMap tmap_k,
                 const int s = int(gi % NST), sb = int(gi & 1u);
                 const uint32_t par = (gi >> 1) & 1u;
                 const int page0 = c * chunk + i * PAGE;  // first key of the page
-                // all 64 scores of the page, then release the S buffer
+                // this warp's 16 scores of the page, then release the S buffer
                 if (!wait(&s_full[sb], par)) break;
                 tc_fence_after_sync();
-                uint32_t sv[PAGE];
-                tmem_load_32x32b_x64_sync(tmem_base + lane_base + uint32_t(C::S_COL + sb * PAGE), sv);
+                uint32_t sv[KSL];
+                tmem_load_32x32b_x16_sync(
+                    tmem_base + lane_base + uint32_t(C::S_COL + sb * PAGE + sw * KSL), sv);
                 tc_fence_before_sync();
                 __syncwarp();
                 if (lane == 0) mbar_arrive(&s_empty[sb]);
@@ -518,20 +524,33 @@ attn_partial_kernel(const __grid_constant__ CUtensorMap tmap_k,
                 const bool valid = stage_valid[s] != 0;
 
                 // causal mask (masked keys -> -inf) and the row max over the page, taken on
-                // the raw scores with a fixed tree (exact: max does not round); scaling by
-                // the positive scale_log2 afterwards gives the max of the scaled scores
-                float sm[PAGE];
+                // the raw scores (exact: max does not round, so neither the tree nor the
+                // order of the four slice maxima matters); scaling by the positive
+                // scale_log2 afterwards gives the max of the scaled scores
+                float sl[KSL];
 #pragma unroll
-                for (int k = 0; k < PAGE; ++k)
-                    sm[k] = (valid && page0 + k <= pos) ? __uint_as_float(sv[k]) : -INFINITY;
-                float mt[PAGE / 2];
+                for (int k = 0; k < KSL; ++k)
+                    sl[k] = (valid && page0 + sw * KSL + k <= pos) ? __uint_as_float(sv[k])
+                                                                  : -INFINITY;
+                float mt[KSL / 2];
 #pragma unroll
-                for (int k = 0; k < PAGE / 2; ++k) mt[k] = fmaxf(sm[k], sm[k + PAGE / 2]);
+                for (int k = 0; k < KSL / 2; ++k) mt[k] = fmaxf(sl[k], sl[k + KSL / 2]);
 #pragma unroll
-                for (int width = PAGE / 4; width >= 1; width /= 2)
+                for (int width = KSL / 4; width >= 1; width /= 2)
 #pragma unroll
                     for (int k = 0; k < width; ++k) mt[k] = fmaxf(mt[k], mt[k + width]);
-                const float m_page = mt[0] * scale_log2;
+                // the four warps' slice maxima of row r, through shared memory (buffer
+                // sb is rewritten only for page gi+2, after every warp has passed page
+                // gi+1's exchange and so has read this one)
+                float* xm = x_max + sb * (NSM * MAXR);
+                xm[sw * MAXR + r] = mt[0];
+                __syncwarp();
+                if (lane == 0) mbar_arrive(&xm_bar[sb]);
+                if (!wait(&xm_bar[sb], par)) break;
+                float m_raw = xm[r];
+#pragma unroll
+                for (int t = 1; t < NSM; ++t) m_raw = fmaxf(m_raw, xm[t * MAXR + r]);
+                const float m_page = m_raw * scale_log2;
 
                 // reference max: raised (and O, l rescaled) only when the page max exceeds
                 // it by more than 2^8, so p = exp2(s - m_ref) <= 2^8
@@ -560,16 +579,7 @@ attn_partial_kernel(const __grid_constant__ CUtensorMap tmap_k,
                     tc_fence_before_sync();
                 }
                 const float m_use = m_ref == -INFINITY ? 0.f : m_ref;
-                // this warp's 16 keys (selected with constant register indices); a masked
-                // key (-inf) gives p = +0
-                float sl[KSL];
-#pragma unroll
-                for (int k = 0; k < KSL; ++k) {
-                    float v = sm[k];
-#pragma unroll
-                    for (int t = 1; t < NSM; ++t) v = sw == t ? sm[t * KSL + k] : v;
-                    sl[k] = v;
-                }
+                // this warp's 16 keys; a masked key (-inf) gives p = +0
                 // p = exp2(s * scale_log2 - m), the row-slice sum by a fixed pairwise tree
                 float pv[KSL];
 #pragma unroll
