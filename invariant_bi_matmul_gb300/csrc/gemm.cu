@@ -94,7 +94,7 @@ struct GemmArgs {
     int kb_per_split;
 };
 
-template <bool KN, bool F32OUT, int NSUB, bool SPLIT>
+template <bool KN, bool F32OUT, int NSUB, bool SPLIT, int MSUB>
 __global__ void __launch_bounds__(THREADS, 1)
 gemm_kernel(const __grid_constant__ CUtensorMap tmap_x, const __grid_constant__ CUtensorMap tmap_w,
             const GemmArgs args, unsigned int* err) {
@@ -122,7 +122,8 @@ gemm_kernel(const __grid_constant__ CUtensorMap tmap_x, const __grid_constant__ 
     const int lane = threadIdx.x & 31;
     const int M = args.M, N = args.N, K = args.K;
     const int tile_n = nsub * BN;
-    const int m_tiles = (M + BM - 1) / BM;
+    constexpr int TILE_M = BM * MSUB;             // rows per CTA tile: MSUB instruction tiles
+    const int m_tiles = (M + TILE_M - 1) / TILE_M;
     const int n_tiles = (N + tile_n - 1) / tile_n;
     const int num_tiles = m_tiles * n_tiles;
     const int nkb = (K + BK - 1) / BK;
@@ -136,7 +137,11 @@ gemm_kernel(const __grid_constant__ CUtensorMap tmap_x, const __grid_constant__ 
     }
     const int kb0 = rank * args.kb_per_split;
     const int kb1 = kb0 + args.kb_per_split < nkb ? kb0 + args.kb_per_split : nkb;
-    const uint32_t tmem_cols = uint32_t(2 * tile_n);  // two accumulators, power of two
+    // two accumulators (the epilogue of one tile overlaps the next tile's main loop) when
+    // they fit in the 512 tensor-memory columns, else one
+    constexpr int NACC = 2 * MSUB * NSUB * BN <= 512 ? 2 : 1;
+    constexpr int ACC_COLS = MSUB * NSUB * BN;
+    const uint32_t tmem_cols = uint32_t(NACC * ACC_COLS);  // a power of two
 
     if (threadIdx.x == 0) {
         for (int s = 0; s < S; ++s) {
@@ -256,7 +261,7 @@ gemm_kernel(const __grid_constant__ CUtensorMap tmap_x, const __grid_constant__ 
 
         for (int t = first_tile; ok && t < num_tiles; t += tile_step) {
             const int mt = t / n_tiles, nt = t % n_tiles;
-            const int m0 = mt * BM, n0 = nt * tile_n;
+            const int m0 = mt * TILE_M, n0 = nt * tile_n;
             for (int kb = kb0; kb < kb1; kb += kbs) {
                 if (!mbar_wait_warp(&empty[stage], phase ^ 1u, abort_flag)) {
                     ok = false;
@@ -313,14 +318,14 @@ gemm_kernel(const __grid_constant__ CUtensorMap tmap_x, const __grid_constant__ 
         bool ok = true;
         int local = 0;
         for (int t = first_tile; ok && t < num_tiles; t += tile_step, ++local) {
-            const int acc = local & 1;
-            const uint32_t acc_phase = (local >> 1) & 1;
+            const int acc = local % NACC;
+            const uint32_t acc_phase = uint32_t(local / NACC) & 1u;
             if (!mbar_wait_warp(&tempty[acc], acc_phase ^ 1u, abort_flag)) {
                 ok = false;
                 break;
             }
             tc_fence_after_sync();
-            const uint32_t d_tmem = tmem_base + uint32_t(acc * tile_n);
+            const uint32_t d_tmem = tmem_base + uint32_t(acc * ACC_COLS);
             for (int kb = kb0; kb < kb1; kb += kbs) {
                 if (!mbar_wait_warp(&full[stage], phase, abort_flag)) {
                     ok = false;
@@ -337,12 +342,19 @@ gemm_kernel(const __grid_constant__ CUtensorMap tmap_x, const __grid_constant__ 
                         const uint32_t first = (kb + i) == kb0 ? 1u : 0u;
 #pragma unroll
                         for (int k = 0; k < BK / UK; ++k) {
-                            const uint64_t a_desc = a_blk + uint64_t(k * A_K16);
-                            uint64_t b_desc = b_blk + uint64_t(k * B_K16);
-                            uint32_t d = d_tmem;
 #pragma unroll
-                            for (int j = 0; j < NSUB; ++j, b_desc += b_sub, d += uint32_t(BN))
-                                tc_mma_bf16(d, a_desc, b_desc, idesc, (first && k == 0) ? 0u : 1u);
+                            for (int ms = 0; ms < MSUB; ++ms) {
+                                // instruction tile ms: X rows 128ms.., accumulator columns
+                                // ms*NSUB*BN..
+                                const uint64_t a_desc = a_blk + uint64_t(k * A_K16) +
+                                                        uint64_t(ms * (A_MMA_BYTES >> 4));
+                                uint64_t b_desc = b_blk + uint64_t(k * B_K16);
+                                uint32_t d = d_tmem + uint32_t(ms * NSUB * BN);
+#pragma unroll
+                                for (int j = 0; j < NSUB; ++j, b_desc += b_sub, d += uint32_t(BN))
+                                    tc_mma_bf16(d, a_desc, b_desc, idesc,
+                                                (first && k == 0) ? 0u : 1u);
+                            }
                         }
                     }
                     tc_commit_s(empty_s + stage * 8u);  // frees the stage once these MMAs finish
@@ -392,8 +404,8 @@ gemm_kernel(const __grid_constant__ CUtensorMap tmap_x, const __grid_constant__ 
             to_full = cluster_map(smem_addr(red_full), 0);
         }
         for (int t = first_tile; t < num_tiles; t += tile_step, ++local) {
-            const int acc = local & 1;
-            const uint32_t acc_phase = (local >> 1) & 1;
+            const int acc = local % NACC;
+            const uint32_t acc_phase = uint32_t(local / NACC) & 1u;
             if (!mbar_wait_warp(&tfull[acc], acc_phase, abort_flag)) {
                 if (!*abort_flag) fail();
                 break;
@@ -411,12 +423,15 @@ gemm_kernel(const __grid_constant__ CUtensorMap tmap_x, const __grid_constant__ 
             }
             tc_fence_after_sync();
             const int mt = t / n_tiles, nt = t % n_tiles;
-            const int64_t gm = int64_t(mt) * BM + row_in_tile;
+#pragma unroll 1
+            for (int ms = 0; ms < MSUB; ++ms)
             for (int c = 0; c < tile_n; c += 32) {
+                const int64_t gm = int64_t(mt) * TILE_M + ms * BM + row_in_tile;
                 uint32_t r[32];
                 if (live) {
-                    tmem_load_32x32b_x32(
-                        tmem_base + (uint32_t(quad * 32) << 16) + uint32_t(acc * tile_n + c), r);
+                    tmem_load_32x32b_x32(tmem_base + (uint32_t(quad * 32) << 16) +
+                                             uint32_t(acc * ACC_COLS + ms * NSUB * BN + c),
+                                         r);
                     tmem_load_wait();
                 }
                 if (SPLIT && rank != 0) {
@@ -502,10 +517,10 @@ gemm_kernel(const __grid_constant__ CUtensorMap tmap_x, const __grid_constant__ 
     if constexpr (SPLIT) cluster_sync_all();
 }
 
-template <bool KN, bool F32OUT, int NSUB>
+template <bool KN, bool F32OUT, int NSUB, int MSUB = 1>
 cudaError_t launch_t(const DeviceInfo& dev, const CUtensorMap& mx, const CUtensorMap& mw,
                      const GemmArgs& a, int grid, cudaStream_t s) {
-    auto kern = gemm_kernel<KN, F32OUT, NSUB, false>;
+    auto kern = gemm_kernel<KN, F32OUT, NSUB, false, MSUB>;
     static bool attr_done[64] = {};
     if (dev.device >= 0 && dev.device < 64 && !attr_done[dev.device]) {
         cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize,
@@ -522,7 +537,7 @@ cudaError_t launch_t(const DeviceInfo& dev, const CUtensorMap& mx, const CUtenso
 template <bool KN, bool F32OUT>
 cudaError_t launch_split(const DeviceInfo& dev, const CUtensorMap& mx, const CUtensorMap& mw,
                          const GemmArgs& a, int64_t tiles, cudaStream_t s) {
-    auto kern = gemm_kernel<KN, F32OUT, 1, true>;
+    auto kern = gemm_kernel<KN, F32OUT, 1, true, 1>;
     static bool attr_done[64] = {};
     static int fit[64][MAX_SPLITS + 1] = {};  // co-resident clusters per device and size
     if (dev.device < 0 || dev.device >= 64 || a.splits < 2 || a.splits > MAX_SPLITS)
@@ -563,7 +578,10 @@ cudaError_t launch_nsub(const DeviceInfo& dev, const CUtensorMap& mx, const CUte
     switch (a.nsub) {
         case 1: return launch_t<KN, F32OUT, 1>(dev, mx, mw, a, grid, s);
         case 2: return launch_t<KN, F32OUT, (MAX_NSUB >= 2 ? 2 : 1)>(dev, mx, mw, a, grid, s);
-        case 4: return launch_t<KN, F32OUT, (MAX_NSUB >= 4 ? 4 : 1)>(dev, mx, mw, a, grid, s);
+        case 4:
+            if (a.a_rows == 2 * BM)  // two instruction tiles along M per CTA tile
+                return launch_t<KN, F32OUT, (MAX_NSUB >= 4 ? 4 : 1), 2>(dev, mx, mw, a, grid, s);
+            return launch_t<KN, F32OUT, (MAX_NSUB >= 4 ? 4 : 1)>(dev, mx, mw, a, grid, s);
         default: return launch_t<KN, F32OUT, MAX_NSUB>(dev, mx, mw, a, grid, s);
     }
 }
@@ -587,6 +605,13 @@ GemmSchedule gemm_schedule(int64_t M, int64_t N, int64_t K, bool w_kn, int num_s
             break;
         }
     }
+    // Large M: 256 x 256 CTA tiles (two instruction tiles along M, four along N) carry
+    // 2 KB of operands per instruction instead of 3 KB, when they still give at least
+    // three quarters of the SMs a tile.  The instructions and their K order are those of
+    // every other tile shape.
+    const int64_t tiles_256 = ((M + 2 * BM - 1) / (2 * BM)) * ((N + 255) / 256);
+    const bool wide_m = MAX_NSUB >= 4 && g.nsub == 4 && 4 * tiles_256 >= 3 * num_sms;
+    if (wide_m) g.a_rows = 2 * BM;
     // Split-K (non-invariant kernel only): a single M-tile whose instruction tiles leave
     // SMs idle gets a cluster of CTAs per tile, each over a contiguous K range, so more
     // SMs stream W and each runs a shorter chain of dependent MMAs.  The reduction slots
@@ -625,7 +650,8 @@ GemmSchedule gemm_schedule(int64_t M, int64_t N, int64_t K, bool w_kn, int num_s
         g.splits = int((nkb + per - 1) / per);                     // no CTA without work
         g.kb_per_split = int(per);
     }
-    g.tiles = m_tiles * ((N + int64_t(g.nsub) * BN - 1) / (int64_t(g.nsub) * BN));
+    g.tiles = (wide_m ? (M + 2 * BM - 1) / (2 * BM) : m_tiles) *
+              ((N + int64_t(g.nsub) * BN - 1) / (int64_t(g.nsub) * BN));
     g.blocked = (K % BK) == 0 ? 1 : 0;
     return g;
 }
@@ -644,7 +670,8 @@ cudaError_t launch_gemm(const DeviceInfo& dev, const void* x, int64_t ldx, const
     // stay inside the ring (it runs into the W blocks that follow the X blocks)
     const int64_t a_bytes = int64_t(g.a_rows) * BK * 2;
     const int64_t blocks = int64_t(g.stages) * g.kbs;
-    if ((blocks - 1) * a_bytes + A_MMA_BYTES > blocks * (a_bytes + int64_t(g.nsub) * B_KB_BYTES) ||
+    const int64_t a_read = g.a_rows > BM ? a_bytes : A_MMA_BYTES;  // from an X block's start
+    if ((blocks - 1) * a_bytes + a_read > blocks * (a_bytes + int64_t(g.nsub) * B_KB_BYTES) ||
         blocks * (a_bytes + int64_t(g.nsub) * B_KB_BYTES) > g.ring_bytes || g.stages < 2)
         return cudaErrorNotSupported;
     CUtensorMap mx, mw;
