@@ -124,6 +124,22 @@ def test_matmul_parity_wide_cta_tiles_ragged_n(dev, layout):
         assert bits_equal(alone, y[i:i + 1])
 
 
+@pytest.mark.parametrize("layout", ["nk", "kn"])
+def test_matmul_parity_256_row_tiles_ragged(dev, layout):
+    """Large M and N: 256 x 256 CTA tiles (two instruction tiles along M), with M, N and
+    K all ragged (K not a multiple of the 64-wide K-block)."""
+    M, N, K = 1800, 4000, 328
+    gi = inputs.gemm_inputs(M, N, K, seed=83)
+    w = gi.w_nk if layout == "nk" else gi.w_kn
+    y = bi.matmul(gi.x.to(dev), w.to(dev), layout).cpu()
+    rows = [0, 127, 128, 255, 256, 1024, 1791, 1799]
+    ref = oracle.matmul(inputs.bf16_bits(gi.x[rows]), inputs.bf16_bits(gi.w_nk), oracle.W_NK)
+    check_bf16(y[rows], ref, f"256-row tiles {layout}")
+    for i in (128, 1799):
+        alone = bi.matmul(gi.x[i:i + 1].to(dev), w.to(dev), layout).cpu()
+        assert bits_equal(alone, y[i:i + 1])
+
+
 def test_matmul_permutation_and_repeat(dev):
     M, N, K = 300, 512, 1024
     gi = inputs.gemm_inputs(M, N, K, seed=41)
