@@ -72,6 +72,9 @@ def _declare(L: ctypes.CDLL) -> None:
     L.oracle_rope.argtypes = [_p, _i64, _p, _i64, _i64, _i64, _i64, _p, ctypes.c_double]
     L.oracle_swiglu.argtypes = [_p, _p, _p, _i64]
     L.oracle_add.argtypes = [_p, _p, _p, _i64]
+    L.oracle_log_softmax_f32.argtypes = [_p, _i64, _p, _i64, _i64, _i64]
+    L.oracle_mean_f32.argtypes = [_p, _i64, _i64, _i64, _p]
+    L.oracle_mean_bf16.argtypes = [_p, _i64, _i64, _i64, _p]
 
 
 def _ptr(a: np.ndarray):
@@ -279,6 +282,27 @@ def add(a: np.ndarray, b: np.ndarray) -> np.ndarray:
     y = np.empty(a.shape, dtype=np.float64)
     lib().oracle_add(_ptr(a), _ptr(b), _ptr(y), a.size)
     return y
+
+
+def log_softmax(x: np.ndarray) -> np.ndarray:
+    """Row-wise log-softmax of fp32 [rows, n] (or [n]) -> fp64, by the definition."""
+    x = _as(x, np.float32)
+    x2 = x.reshape(1, -1) if x.ndim == 1 else x
+    rows, n = x2.shape
+    y = np.empty((rows, n), dtype=np.float64)
+    lib().oracle_log_softmax_f32(_ptr(x2), n, _ptr(y), n, rows, n)
+    return y.reshape(x.shape)
+
+
+def mean(x: np.ndarray, bf16: bool = False) -> np.ndarray:
+    """Row means of [rows, n] (fp32 values, or bf16 bits with bf16=True) -> fp64 [rows]."""
+    x = _as(x, np.uint16 if bf16 else np.float32)
+    x2 = x.reshape(1, -1) if x.ndim == 1 else x
+    rows, n = x2.shape
+    out = np.empty(rows, dtype=np.float64)
+    fn = lib().oracle_mean_bf16 if bf16 else lib().oracle_mean_f32
+    fn(_ptr(x2), n, rows, n, _ptr(out))
+    return out
 
 
 def to_bf16(y: np.ndarray) -> np.ndarray:

@@ -374,3 +374,47 @@ ORACLE_API void oracle_add(const uint16_t* a, const uint16_t* b, double* y, int6
     for (int64_t i = 0; i < n; ++i)
         y[i] = (double)bf16_bits_to_f32(a[i]) + (double)bf16_bits_to_f32(b[i]);
 }
+
+/* ------------------------------------------------------------------------------ */
+/* Row-wise log-softmax and mean (book chapter "Batch-invariant kernels...",        */
+/* Sources: the companion library's mean and log-softmax overrides; the pages name  */
+/* the operations only, so these are the textbook definitions, in fp64):            */
+/*   log_softmax(x)_i = x_i - m - log(sum_j exp(x_j - m)),  m = max_j x_j          */
+/*   mean(x) = (sum_i x_i) / n                                                      */
+/* fp32 inputs are widened exactly; bf16 inputs by the bit shift above.             */
+/* ------------------------------------------------------------------------------ */
+ORACLE_API void oracle_log_softmax_f32(const float* x, int64_t ldx, double* y, int64_t ldy,
+                                       int64_t rows, int64_t n) {
+    for (int64_t r = 0; r < rows; ++r) {
+        const float* xr = x + r * ldx;
+        double m = -INFINITY;
+        int has_nan = 0;
+        for (int64_t i = 0; i < n; ++i) {
+            if (isnan(xr[i])) has_nan = 1;
+            else if ((double)xr[i] > m) m = (double)xr[i];
+        }
+        double s = 0.0;
+        for (int64_t i = 0; i < n; ++i) s += exp((double)xr[i] - m);
+        const double ls = log(s);
+        for (int64_t i = 0; i < n; ++i)
+            y[r * ldy + i] = has_nan ? NAN : ((double)xr[i] - m) - ls;
+    }
+}
+
+ORACLE_API void oracle_mean_f32(const float* x, int64_t ldx, int64_t rows, int64_t n,
+                                double* out) {
+    for (int64_t r = 0; r < rows; ++r) {
+        double s = 0.0;
+        for (int64_t i = 0; i < n; ++i) s += (double)x[r * ldx + i];
+        out[r] = s / (double)n;
+    }
+}
+
+ORACLE_API void oracle_mean_bf16(const uint16_t* x, int64_t ldx, int64_t rows, int64_t n,
+                                 double* out) {
+    for (int64_t r = 0; r < rows; ++r) {
+        double s = 0.0;
+        for (int64_t i = 0; i < n; ++i) s += (double)bf16_bits_to_f32(x[r * ldx + i]);
+        out[r] = s / (double)n;
+    }
+}
