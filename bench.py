@@ -765,6 +765,34 @@ def run_sweep():
                           "graph_us": round(tg, 2),
                           "graph_frac_hbm": round(by / tg / 1e3 / peaks["hbm_gbs"], 3)}),
               flush=True)
+    bi.set_batch_invariant_limit(INVARIANT)
+    # row-wise log-softmax (fp32 logits rows) and mean (bf16 activation rows)
+    for rows, n in ((32, 128256), (2048, 4096)):
+        xl = torch.randn(rows, n, device=dev)
+        by = 8 * rows * n
+        nsets = max(1, min(64, -(-SET_BYTES // by)))
+        sets = [(xl.clone(), torch.empty_like(xl)) for _ in range(nsets)]
+        t = t_us(lambda: bi.log_softmax(xl, out=sets[0][1]))
+        tg = graph_us([lambda a=a, o=o: bi.log_softmax(a, out=o) for a, o in sets])
+        del sets
+        print(json.dumps({"sweep": "log_softmax", "rows": rows, "n": n, "us": round(t, 2),
+                          "graph_us": round(tg, 2), "graph_GB/s": round(by / tg / 1e3, 1),
+                          "graph_frac_hbm": round(by / tg / 1e3 / peaks["hbm_gbs"], 3)}),
+              flush=True)
+    for rows, n in ((2048, 4096), (32, 128256)):
+        xm = torch.randn(rows, n, device=dev).to(torch.bfloat16)
+        om = torch.empty(rows, device=dev)
+        by = 2 * rows * n + 4 * rows
+        nsets = max(1, min(64, -(-SET_BYTES // by)))
+        sets = [xm.clone() for _ in range(nsets)]
+        t = t_us(lambda: bi.mean(xm, out=om))
+        tg = graph_us([lambda a=a: bi.mean(a, out=om) for a in sets])
+        del sets
+        print(json.dumps({"sweep": "mean", "rows": rows, "n": n, "dtype": "bf16",
+                          "us": round(t, 2), "graph_us": round(tg, 2),
+                          "graph_GB/s": round(by / tg / 1e3, 1),
+                          "graph_frac_hbm": round(by / tg / 1e3 / peaks["hbm_gbs"], 3)}),
+              flush=True)
     for B, q, L in ((1, 1, 65540), (1, 8, 65540), (1, 8, 16388), (1, 8, 8196), (1, 8, 1028),
                     (8, 1, 65540), (64, 1, 16388), (64, 4, 8196)):
         bi.set_batch_invariant_limit(INVARIANT)

@@ -26,7 +26,8 @@ ATTN_MAX_Q = 8
 ATTN_MAX_ROWS = 32
 STATIC_WS_BYTES = 32 * 1024 * 1024
 
-# every function include/bi.h and include/bi_glue.h declare, with its ctypes signature
+# every function include/bi.h, include/bi_glue.h and include/bi_rowwise.h declare, with
+# its ctypes signature
 _p, _i64, _f32, _sz, _int = ctypes.c_void_p, ctypes.c_int64, ctypes.c_float, ctypes.c_size_t, ctypes.c_int
 SIGNATURES = {
     "bi_abi_version": ([], _int),
@@ -56,6 +57,9 @@ SIGNATURES = {
     "bi_swiglu": ([_p, _i64, _p, _i64, _p, _i64, _i64, _i64, _p], _int),
     "bi_add": ([_p, _p, _p, _i64, _p], _int),
     "bi_argmax": ([_p, _i64, _i64, _i64, _p, _p], _int),
+    # row-wise reductions (include/bi_rowwise.h)
+    "bi_log_softmax": ([_p, _i64, _p, _i64, _i64, _i64, _p], _int),
+    "bi_mean": ([_p, _i64, _int, _i64, _i64, _p, _p], _int),
 }
 
 _lib: Optional[ctypes.CDLL] = None
@@ -419,4 +423,39 @@ def argmax(logits, out=None, stream=None):
         raise ValueError("out must be a contiguous int32 [rows] tensor")
     _check(lib().bi_argmax(_ptr(logits), _row_major_2d(logits, "logits"), rows, n, _ptr(out),
                            _stream(stream)))
+    return out
+
+
+# ------------------------------------------------------------------ row-wise reductions
+
+def log_softmax(x, out=None, stream=None):
+    """Row-wise log-softmax of fp32 [rows, n] (one CTA per row, fixed tree); out may be x."""
+    torch = _torch()
+    _need(x, torch.float32, "x", 2)
+    rows, n = x.shape
+    if out is None:
+        out = torch.empty_like(x)
+    _need(out, torch.float32, "out", 2)
+    if tuple(out.shape) != (rows, n):
+        raise ValueError("out must have the shape of x")
+    _check(lib().bi_log_softmax(_ptr(x), _row_major_2d(x, "x"), _ptr(out),
+                                _row_major_2d(out, "out"), rows, n, _stream(stream)))
+    return out
+
+
+def mean(x, out=None, stream=None):
+    """Row means (fp32 [rows]) of bf16 or fp32 [rows, n] (one CTA per row, fixed tree)."""
+    torch = _torch()
+    if x.dtype not in (torch.bfloat16, torch.float32):
+        raise ValueError("x must be bf16 or fp32")
+    _need(x, x.dtype, "x", 2)
+    rows, n = x.shape
+    if out is None:
+        out = torch.empty(rows, dtype=torch.float32, device=x.device)
+    _need(out, torch.float32, "out", 1)
+    if out.shape[0] != rows or not out.is_contiguous():
+        raise ValueError("out must be a contiguous fp32 [rows] tensor")
+    dt = BI_BF16 if x.dtype == torch.bfloat16 else BI_F32
+    _check(lib().bi_mean(_ptr(x), _row_major_2d(x, "x"), dt, rows, n, _ptr(out),
+                         _stream(stream)))
     return out

@@ -13,7 +13,7 @@ import pytest
 import invariant_bi_matmul_gb300 as bi
 
 ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
-HEADERS = [os.path.join(ROOT, "include", h) for h in ("bi.h", "bi_glue.h")]
+HEADERS = [os.path.join(ROOT, "include", h) for h in ("bi.h", "bi_glue.h", "bi_rowwise.h")]
 
 
 def declared_functions():
@@ -218,3 +218,17 @@ def test_glue_argument_errors_before_launch(L):
     assert L.bi_argmax(d + 2, 10, 1, 10, d, None) == bi.BI_ERR_INVALID_ARG
     assert "bi_argmax" in L.bi_last_error_message().decode()
     assert L.bi_argmax(d, 8, 0, 8, d, None) == bi.BI_OK  # rows = 0
+
+
+def test_rowwise_argument_errors_before_launch(L):
+    d = 1 << 20  # a fake, 16-byte aligned address: nothing may touch it
+    assert L.bi_log_softmax(d, 8, d, 8, 1, 0, None) == bi.BI_ERR_INVALID_ARG       # n < 1
+    assert L.bi_log_softmax(d, 4, d, 8, 1, 8, None) == bi.BI_ERR_INVALID_ARG       # ldx < n
+    assert L.bi_log_softmax(d + 2, 8, d, 8, 1, 8, None) == bi.BI_ERR_INVALID_ARG   # misaligned
+    assert L.bi_log_softmax(None, 8, d, 8, 1, 8, None) == bi.BI_ERR_INVALID_ARG
+    assert L.bi_log_softmax(None, 8, None, 8, 0, 8, None) == bi.BI_OK              # rows = 0
+    assert L.bi_mean(d, 8, 7, 1, 8, d, None) == bi.BI_ERR_INVALID_ARG              # dtype
+    assert L.bi_mean(d, 4, bi.BI_F32, 1, 8, d, None) == bi.BI_ERR_INVALID_ARG      # ldx < n
+    assert L.bi_mean(d + 1, 8, bi.BI_BF16, 1, 8, d, None) == bi.BI_ERR_INVALID_ARG
+    assert L.bi_mean(d, 8, bi.BI_F32, 1, 8, None, None) == bi.BI_ERR_INVALID_ARG
+    assert "bi_mean" in L.bi_last_error_message().decode()
