@@ -73,6 +73,11 @@ def _declare(L: ctypes.CDLL) -> None:
     L.oracle_swiglu.argtypes = [_p, _p, _p, _i64]
     L.oracle_add.argtypes = [_p, _p, _p, _i64]
     L.oracle_log_softmax_f32.argtypes = [_p, _i64, _p, _i64, _i64, _i64]
+    L.oracle_f16_widen.argtypes = [_p, _p, _i64]
+    L.oracle_matmul16.argtypes = [_p, _i64, _p, _i64, ctypes.c_int, _p, _i64, _i64, _i64, _i64,
+                                  ctypes.c_int]
+    L.oracle_rmsnorm16.argtypes = [_p, _i64, _p, _p, _i64, _i64, _i64, ctypes.c_float,
+                                   ctypes.c_int]
     L.oracle_mean_f32.argtypes = [_p, _i64, _i64, _i64, _p]
     L.oracle_mean_bf16.argtypes = [_p, _i64, _i64, _i64, _p]
 
@@ -281,6 +286,39 @@ def add(a: np.ndarray, b: np.ndarray) -> np.ndarray:
         raise ValueError("a and b shapes differ")
     y = np.empty(a.shape, dtype=np.float64)
     lib().oracle_add(_ptr(a), _ptr(b), _ptr(y), a.size)
+    return y
+
+
+BF16, F16 = 0, 2  # 16-bit input types of matmul16 / rmsnorm16
+
+
+def f16_widen(h: np.ndarray) -> np.ndarray:
+    """binary16 bit patterns -> fp32 values (exact), from the format definition."""
+    h = _as(h, np.uint16)
+    out = np.empty(h.shape, dtype=np.float32)
+    lib().oracle_f16_widen(_ptr(h), _ptr(out), h.size)
+    return out
+
+
+def matmul16(x: np.ndarray, w: np.ndarray, w_layout: int, dtype: int) -> np.ndarray:
+    """matmul for 16-bit bits of type dtype (BF16 or F16) -> unrounded fp32 [M, N]."""
+    x = _as(x, np.uint16)
+    w = _as(w, np.uint16)
+    M, K = x.shape
+    N = w.shape[0] if w_layout == W_NK else w.shape[1]
+    y = np.empty((M, N), dtype=np.float32)
+    lib().oracle_matmul16(_ptr(x), K, _ptr(w), w.shape[1], w_layout, _ptr(y), N, M, N, K,
+                          int(dtype))
+    return y
+
+
+def rmsnorm16(x: np.ndarray, gamma: np.ndarray, eps: float, dtype: int) -> np.ndarray:
+    """RMSNorm for 16-bit bits of type dtype (BF16 or F16) -> unrounded fp32 [rows, H]."""
+    x = _as(x, np.uint16)
+    gamma = _as(gamma, np.uint16)
+    rows, H = x.shape
+    y = np.empty((rows, H), dtype=np.float32)
+    lib().oracle_rmsnorm16(_ptr(x), H, _ptr(gamma), _ptr(y), H, rows, H, float(eps), int(dtype))
     return y
 
 

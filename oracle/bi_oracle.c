@@ -141,6 +141,29 @@ ORACLE_API int64_t oracle_argmax_f32(const float* v, int64_t n) {
 }
 
 /* ------------------------------------------------------------------------------ */
+/* IEEE binary16 -> fp32, from the format definition (1 sign, 5 exponent bits with  */
+/* bias 15, 10 mantissa bits; exponent 0 = subnormal m * 2^-24, 31 = inf/NaN).       */
+/* Every binary16 value is exactly representable in fp32.                           */
+/* ------------------------------------------------------------------------------ */
+static float f16_bits_to_f32(uint16_t h) {
+    const unsigned s = (h >> 15) & 1u, e = (h >> 10) & 0x1fu, m = h & 0x3ffu;
+    float v;
+    if (e == 0) v = ldexpf((float)m, -24);
+    else if (e == 31) v = m ? NAN : INFINITY;
+    else v = ldexpf((float)(m | 0x400u), (int)e - 25);
+    return s ? -v : v;
+}
+
+ORACLE_API void oracle_f16_widen(const uint16_t* h, float* out, int64_t n) {
+    for (int64_t i = 0; i < n; ++i) out[i] = f16_bits_to_f32(h[i]);
+}
+
+/* widen element i of a 16-bit operand: dtype 0 = bf16 bits, 2 = binary16 bits */
+static float widen16(const uint16_t* p, int64_t i, int dtype) {
+    return dtype == 2 ? f16_bits_to_f32(p[i]) : bf16_bits_to_f32(p[i]);
+}
+
+/* ------------------------------------------------------------------------------ */
 /* Matmul: Y[m,n] = sum_k X[m,k] * W(k,n), fp32 accumulation in ascending k.        */
 /* W layout 0 ("NK", transposed B, nn.Linear): W(k,n) = w[n*ldw + k].               */
 /* W layout 1 ("KN", natural B):              W(k,n) = w[k*ldw + n].                */
@@ -159,6 +182,25 @@ ORACLE_API void oracle_matmul(const uint16_t* x, int64_t ldx, const uint16_t* w,
                 float xv = bf16_bits_to_f32(x[m * ldx + k]);
                 float wv = bf16_bits_to_f32(w_layout == 0 ? w[n * ldw + k] : w[k * ldw + n]);
                 float prod = xv * wv;              /* exact: 8-bit x 8-bit significands */
+                acc = acc + prod;
+            }
+            y[m * ldy + n] = acc;
+        }
+    }
+}
+
+/* The same matmul for 16-bit inputs of either type (dtype 0 = bf16, 2 = binary16).  */
+/* A binary16 product is exact in fp32 as well (11-bit x 11-bit significands).      */
+ORACLE_API void oracle_matmul16(const uint16_t* x, int64_t ldx, const uint16_t* w, int64_t ldw,
+                                int w_layout, float* y, int64_t ldy, int64_t M, int64_t N,
+                                int64_t K, int dtype) {
+    for (int64_t m = 0; m < M; ++m) {
+        for (int64_t n = 0; n < N; ++n) {
+            float acc = 0.0f;
+            for (int64_t k = 0; k < K; ++k) {
+                float xv = widen16(x, m * ldx + k, dtype);
+                float wv = widen16(w, w_layout == 0 ? n * ldw + k : k * ldw + n, dtype);
+                float prod = xv * wv;
                 acc = acc + prod;
             }
             y[m * ldy + n] = acc;
@@ -189,6 +231,27 @@ ORACLE_API void oracle_rmsnorm(const uint16_t* x, int64_t ldx, const uint16_t* g
             float v = bf16_bits_to_f32(xr[i]);
             float t = v * inv;
             y[r * ldy + i] = t * bf16_bits_to_f32(gamma[i]);
+        }
+    }
+}
+
+/* The same RMSNorm for 16-bit x and gamma of either type (0 = bf16, 2 = binary16). */
+ORACLE_API void oracle_rmsnorm16(const uint16_t* x, int64_t ldx, const uint16_t* gamma,
+                                 float* y, int64_t ldy, int64_t rows, int64_t H, float eps,
+                                 int dtype) {
+    for (int64_t r = 0; r < rows; ++r) {
+        float ss = 0.0f;
+        for (int64_t i = 0; i < H; ++i) {
+            float v = widen16(x, r * ldx + i, dtype);
+            float sq = v * v;
+            ss = ss + sq;
+        }
+        float mean = ss / (float)H;
+        float inv = 1.0f / sqrtf(mean + eps);
+        for (int64_t i = 0; i < H; ++i) {
+            float v = widen16(x, r * ldx + i, dtype);
+            float t = v * inv;
+            y[r * ldy + i] = t * widen16(gamma, i, dtype);
         }
     }
 }
