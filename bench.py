@@ -745,6 +745,22 @@ def run_sweep():
                           "graph_nk_frac_tensor": round(fl / tng / 1e6 / tf_peak, 3)}),
               flush=True)
     del wsets
+    # IEEE binary16 inputs (bi_matmul_ex): the same kernel with f16 operands
+    xh, wh = x.to(torch.float16), wnk.to(torch.float16)
+    hsets = [wh] + [wh.clone() for _ in range(SET_BYTES // (2 * N * K) - 1)]
+    bi.set_batch_invariant_limit(INVARIANT)
+    for M in (8, 2048):
+        xm = xh[:M].contiguous()
+        y = torch.empty(M, N, dtype=torch.float16, device=dev)
+        tg = graph_us([lambda w=w: bi.matmul(xm, w, "nk", out=y) for w in hsets])
+        tcg = graph_us([lambda w=w: torch.matmul(xm, w.t(), out=y) for w in hsets])
+        fl, by = 2 * M * N * K, 2 * N * K + 4 * M * K
+        print(json.dumps({"sweep": "gemm_f16", "M": M, "K": K, "N": N, "graph_us": round(tg, 2),
+                          "graph_cublas_us": round(tcg, 2),
+                          "graph_frac_hbm": round(by / tg / 1e3 / peaks["hbm_gbs"], 3),
+                          "graph_frac_tensor": round(fl / tg / 1e6 / float(
+                              peaks.get("bf16_tflops", 1900.0)), 3)}), flush=True)
+    del hsets, xh, wh
     for B in (1, 3, 16, 128, 2048):
         xr, g = inputs.rmsnorm_inputs(B, 8192, seed=3)
         xr, g = xr.to(dev), g.to(dev)

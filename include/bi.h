@@ -66,7 +66,7 @@ typedef enum {
                                 skipped, never read or written out of bounds          */
 } bi_status;
 
-typedef enum { BI_BF16 = 0, BI_F32 = 1 } bi_dtype;
+typedef enum { BI_BF16 = 0, BI_F32 = 1, BI_F16 = 2 } bi_dtype;  /* BI_F16: IEEE binary16 */
 
 typedef enum {
     BI_W_NK = 0,  /* W stored [N, K] row-major ("b_transposed", nn.Linear weight)  */
@@ -155,6 +155,15 @@ bi_status bi_matmul(const void* x, int64_t ldx, const void* w, int64_t ldw, int 
                     void* y, int64_t ldy, int y_dtype, int64_t M, int64_t N, int64_t K,
                     bi_stream_t stream);
 
+/* bi_matmul with the input type given: in_dtype BI_BF16 or BI_F16 (IEEE binary16) for
+ * both x and w (one MMA type for both operands); y_dtype in_dtype (round to nearest even)
+ * or BI_F32.  [MLX-4279, the tester's comment: dense matmul divergence also shows for
+ * f16 inputs.]  Same construction, same invariance, same rules as bi_matmul (which is
+ * bi_matmul_ex with in_dtype = BI_BF16). */
+bi_status bi_matmul_ex(const void* x, int64_t ldx, const void* w, int64_t ldw, int w_layout,
+                       void* y, int64_t ldy, int in_dtype, int y_dtype, int64_t M, int64_t N,
+                       int64_t K, bi_stream_t stream);
+
 /* ---------------------------------------------------------------------------------
  * bi_rmsnorm  [BOOK Case 4 (definition and the load-dependent-tree defect) and Case 6
  * "RMSNorm": data-parallel, one row per core, never split]
@@ -172,6 +181,12 @@ bi_status bi_matmul(const void* x, int64_t ldx, const void* w, int64_t ldw, int 
 bi_status bi_rmsnorm(const void* x, int64_t ldx, const void* gamma, void* y, int64_t ldy,
                      int y_dtype, int64_t rows, int64_t hidden, float eps,
                      bi_stream_t stream);
+
+/* bi_rmsnorm with the input type given: x and gamma both in_dtype (BI_BF16 or BI_F16);
+ * y_dtype in_dtype or BI_F32.  Same tree and arithmetic after the exact widening. */
+bi_status bi_rmsnorm_ex(const void* x, int64_t ldx, const void* gamma, void* y, int64_t ldy,
+                        int in_dtype, int y_dtype, int64_t rows, int64_t hidden, float eps,
+                        bi_stream_t stream);
 
 /* ---------------------------------------------------------------------------------
  * Paged KV cache (shared by the three attention entry points)

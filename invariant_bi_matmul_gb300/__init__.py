@@ -18,7 +18,7 @@ HERE = os.path.dirname(os.path.abspath(__file__))
 LIB_PATH = os.environ.get("BI_LIBRARY_PATH") or os.path.join(HERE, "libbi.so")
 
 BI_OK, BI_ERR_INVALID_ARG, BI_ERR_UNSUPPORTED, BI_ERR_CUDA, BI_ERR_TIMEOUT, BI_ERR_DEVICE_ARG = range(6)
-BI_BF16, BI_F32 = 0, 1
+BI_BF16, BI_F32, BI_F16 = 0, 1, 2
 BI_W_NK, BI_W_KN = 0, 1
 PAGE_SIZE = 64
 ATTN_CHUNK = 512
@@ -39,7 +39,10 @@ SIGNATURES = {
     "bi_matmul_splits": ([_i64, _i64, _i64, _int, _int], _int),
     "bi_attn_chunk": ([_i64, _i64, _i64, _i64, _i64, _i64, _i64, _sz, _int], _i64),
     "bi_matmul": ([_p, _i64, _p, _i64, _int, _p, _i64, _int, _i64, _i64, _i64, _p], _int),
+    "bi_matmul_ex": ([_p, _i64, _p, _i64, _int, _p, _i64, _int, _int, _i64, _i64, _i64, _p],
+                     _int),
     "bi_rmsnorm": ([_p, _i64, _p, _p, _i64, _int, _i64, _i64, _f32, _p], _int),
+    "bi_rmsnorm_ex": ([_p, _i64, _p, _p, _i64, _int, _int, _i64, _i64, _f32, _p], _int),
     "bi_kv_append": ([_p, _p, _p, _p, _i64, _p, _i64, _p, _p, _i64, _i64, _i64, _i64, _i64, _p],
                      _int),
     "bi_attn_workspace_size": ([_i64, _i64, _i64, _i64], _sz),
@@ -168,43 +171,58 @@ def attn_chunk(batch: int, total_q: int, max_q: int, max_seq_len: int, num_q_hea
 
 # ----------------------------------------------------------------------------- matmul
 
-def matmul(x, w, w_layout: str = "nk", out=None, out_dtype=None, stream=None):
-    """Y = X @ W for X bf16 [M,K] and W bf16 [N,K] ("nk", nn.Linear) or [K,N] ("kn")."""
+def _in_dtype(t, name):
     torch = _torch()
-    _need(x, torch.bfloat16, "x", 2)
-    _need(w, torch.bfloat16, "w", 2)
+    if t.dtype == torch.bfloat16:
+        return BI_BF16
+    if t.dtype == torch.float16:
+        return BI_F16
+    raise ValueError(f"{name} must be bf16 or fp16")
+
+
+def matmul(x, w, w_layout: str = "nk", out=None, out_dtype=None, stream=None):
+    """Y = X @ W for X [M,K] and W [N,K] ("nk", nn.Linear) or [K,N] ("kn"), both bf16 or
+    both fp16; Y in the input type or fp32."""
+    torch = _torch()
+    dt = _in_dtype(x, "x")
+    _need(x, x.dtype, "x", 2)
+    _need(w, x.dtype, "w", 2)
     layout = {"nk": BI_W_NK, "kn": BI_W_KN}[w_layout]
     M, K = x.shape
     N = w.shape[0] if layout == BI_W_NK else w.shape[1]
     if (w.shape[1] if layout == BI_W_NK else w.shape[0]) != K:
         raise ValueError("inner dimensions of x and w differ")
     if out is None:
-        out = torch.empty(M, N, dtype=out_dtype or torch.bfloat16, device=x.device)
-    if out.dtype not in (torch.bfloat16, torch.float32) or tuple(out.shape) != (M, N):
-        raise ValueError("out must be [M,N] bf16 or fp32")
-    _check(lib().bi_matmul(_ptr(x), _row_major_2d(x, "x"), _ptr(w), _row_major_2d(w, "w"), layout,
-                           _ptr(out), _row_major_2d(out, "out"),
-                           BI_F32 if out.dtype == torch.float32 else BI_BF16, M, N, K,
-                           _stream(stream)))
+        out = torch.empty(M, N, dtype=out_dtype or x.dtype, device=x.device)
+    if out.dtype not in (x.dtype, torch.float32) or tuple(out.shape) != (M, N):
+        raise ValueError("out must be [M,N] of the input type or fp32")
+    _check(lib().bi_matmul_ex(_ptr(x), _row_major_2d(x, "x"), _ptr(w), _row_major_2d(w, "w"),
+                              layout, _ptr(out), _row_major_2d(out, "out"), dt,
+                              BI_F32 if out.dtype == torch.float32 else dt, M, N, K,
+                              _stream(stream)))
     return out
 
 
 # ---------------------------------------------------------------------------- rmsnorm
 
 def rmsnorm(x, gamma, eps: float, out=None, out_dtype=None, stream=None):
-    """y = x * rsqrt(mean(x^2) + eps) * gamma over the last dim of a bf16 [rows, H] x."""
+    """y = x * rsqrt(mean(x^2) + eps) * gamma over the last dim of [rows, H] x; x and
+    gamma both bf16 or both fp16; y in the input type or fp32."""
     torch = _torch()
-    _need(x, torch.bfloat16, "x", 2)
-    _need(gamma, torch.bfloat16, "gamma", 1)
+    dt = _in_dtype(x, "x")
+    _need(x, x.dtype, "x", 2)
+    _need(gamma, x.dtype, "gamma", 1)
     rows, H = x.shape
     if gamma.shape[0] != H or gamma.stride(0) != 1:
         raise ValueError("gamma must be a contiguous [H] tensor")
     if out is None:
-        out = torch.empty(rows, H, dtype=out_dtype or torch.bfloat16, device=x.device)
-    _check(lib().bi_rmsnorm(_ptr(x), _row_major_2d(x, "x"), _ptr(gamma), _ptr(out),
-                            _row_major_2d(out, "out"),
-                            BI_F32 if out.dtype == torch.float32 else BI_BF16, rows, H,
-                            float(eps), _stream(stream)))
+        out = torch.empty(rows, H, dtype=out_dtype or x.dtype, device=x.device)
+    if out.dtype not in (x.dtype, torch.float32):
+        raise ValueError("out must be of the input type or fp32")
+    _check(lib().bi_rmsnorm_ex(_ptr(x), _row_major_2d(x, "x"), _ptr(gamma), _ptr(out),
+                               _row_major_2d(out, "out"), dt,
+                               BI_F32 if out.dtype == torch.float32 else dt, rows, H,
+                               float(eps), _stream(stream)))
     return out
 
 

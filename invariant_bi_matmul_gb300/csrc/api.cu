@@ -165,44 +165,94 @@ BI_EXPORT int64_t bi_attn_chunk(int64_t batch, int64_t total_q, int64_t max_q,
 
 // ========================================================================== matmul
 
-BI_EXPORT bi_status bi_matmul(const void* x, int64_t ldx, const void* w, int64_t ldw,
-                              int w_layout, void* y, int64_t ldy, int y_dtype, int64_t M,
-                              int64_t N, int64_t K, bi_stream_t stream) {
+namespace {
+
+bi_status matmul_impl(const char* fn, const void* x, int64_t ldx, const void* w, int64_t ldw,
+                      int w_layout, void* y, int64_t ldy, int in_dtype, int y_dtype, int64_t M,
+                      int64_t N, int64_t K, bi_stream_t stream) {
     init_limit_from_env();
-    if (M < 0 || N < 0 || K < 0) return fail(BI_ERR_INVALID_ARG, "bi_matmul: negative M/N/K");
+    if (M < 0 || N < 0 || K < 0) return fail(BI_ERR_INVALID_ARG, "%s: negative M/N/K", fn);
     if (M > kI32Max || N > kI32Max || K > kI32Max)
-        return fail(BI_ERR_UNSUPPORTED, "bi_matmul: M, N, K must be < 2^31");
+        return fail(BI_ERR_UNSUPPORTED, "%s: M, N, K must be < 2^31", fn);
     if (w_layout != BI_W_NK && w_layout != BI_W_KN)
-        return fail(BI_ERR_INVALID_ARG, "bi_matmul: w_layout must be BI_W_NK or BI_W_KN");
-    if (y_dtype != BI_BF16 && y_dtype != BI_F32)
-        return fail(BI_ERR_INVALID_ARG, "bi_matmul: y_dtype must be BI_BF16 or BI_F32");
+        return fail(BI_ERR_INVALID_ARG, "%s: w_layout must be BI_W_NK or BI_W_KN", fn);
+    if (in_dtype != BI_BF16 && in_dtype != BI_F16)
+        return fail(BI_ERR_INVALID_ARG, "%s: in_dtype must be BI_BF16 or BI_F16", fn);
+    if (y_dtype != in_dtype && y_dtype != BI_F32)
+        return fail(BI_ERR_INVALID_ARG, "%s: y_dtype must be in_dtype or BI_F32", fn);
     if (M == 0 || N == 0) return BI_OK;
-    if (!y) return fail(BI_ERR_INVALID_ARG, "bi_matmul: null y");
-    if (ldy < N) return fail(BI_ERR_INVALID_ARG, "bi_matmul: ldy < N");
+    if (!y) return fail(BI_ERR_INVALID_ARG, "%s: null y", fn);
+    if (ldy < N) return fail(BI_ERR_INVALID_ARG, "%s: ldy < N", fn);
     const size_t ysz = y_dtype == BI_F32 ? 4 : 2;
-    if (!aligned(y, ysz)) return fail(BI_ERR_INVALID_ARG, "bi_matmul: y not element-aligned");
+    if (!aligned(y, ysz)) return fail(BI_ERR_INVALID_ARG, "%s: y not element-aligned", fn);
     if (K > 0) {
-        if (!x || !w) return fail(BI_ERR_INVALID_ARG, "bi_matmul: null x or w");
-        if (ldx < K) return fail(BI_ERR_INVALID_ARG, "bi_matmul: ldx < K");
+        if (!x || !w) return fail(BI_ERR_INVALID_ARG, "%s: null x or w", fn);
+        if (ldx < K) return fail(BI_ERR_INVALID_ARG, "%s: ldx < K", fn);
         if (w_layout == BI_W_NK && ldw < K)
-            return fail(BI_ERR_INVALID_ARG, "bi_matmul: ldw < K for layout NK");
+            return fail(BI_ERR_INVALID_ARG, "%s: ldw < K for layout NK", fn);
         if (w_layout == BI_W_KN && ldw < N)
-            return fail(BI_ERR_INVALID_ARG, "bi_matmul: ldw < N for layout KN");
+            return fail(BI_ERR_INVALID_ARG, "%s: ldw < N for layout KN", fn);
         if (!aligned(x, 16) || !aligned(w, 16) || ldx % 8 != 0 || ldw % 8 != 0)
             return fail(BI_ERR_UNSUPPORTED,
-                        "bi_matmul: x and w must be 16-byte aligned with ldx, ldw multiples of 8 "
-                        "(TMA rule)");
+                        "%s: x and w must be 16-byte aligned with ldx, ldw multiples of 8 "
+                        "(TMA rule)", fn);
     }
     cudaError_t why = cudaSuccess;
     const DeviceInfo* dev = current_device_info(&why);
-    if (!dev) return cuda_fail(why, "bi_matmul: device query");
+    if (!dev) return cuda_fail(why, fn);
     // inside the limit: the invariant schedule; outside it the split-K kernel may be used
     const bool split_ok = !bi_within_batch_invariant_limit(M);
     cudaError_t e = launch_gemm(*dev, x, ldx, w, ldw, w_layout == BI_W_KN, y, ldy,
-                                y_dtype == BI_F32, M, N, K, split_ok,
+                                y_dtype == BI_F32, M, N, K, split_ok, in_dtype == BI_F16,
                                 reinterpret_cast<cudaStream_t>(stream));
-    if (e != cudaSuccess) return cuda_fail(e, "bi_matmul: launch");
+    if (e != cudaSuccess) return cuda_fail(e, fn);
     return BI_OK;
+}
+
+bi_status rmsnorm_impl(const char* fn, const void* x, int64_t ldx, const void* gamma, void* y,
+                       int64_t ldy, int in_dtype, int y_dtype, int64_t rows, int64_t hidden,
+                       float eps, bi_stream_t stream) {
+    init_limit_from_env();
+    if (rows < 0) return fail(BI_ERR_INVALID_ARG, "%s: negative rows", fn);
+    if (hidden < 1 || hidden > (int64_t(1) << 20))
+        return fail(BI_ERR_INVALID_ARG, "%s: hidden must be in [1, 2^20]", fn);
+    if (in_dtype != BI_BF16 && in_dtype != BI_F16)
+        return fail(BI_ERR_INVALID_ARG, "%s: in_dtype must be BI_BF16 or BI_F16", fn);
+    if (y_dtype != in_dtype && y_dtype != BI_F32)
+        return fail(BI_ERR_INVALID_ARG, "%s: y_dtype must be in_dtype or BI_F32", fn);
+    if (!std::isfinite(eps) || eps < 0.0f)
+        return fail(BI_ERR_INVALID_ARG, "%s: eps must be finite and >= 0", fn);
+    if (rows == 0) return BI_OK;
+    if (!x || !gamma || !y) return fail(BI_ERR_INVALID_ARG, "%s: null pointer", fn);
+    if (ldx < hidden || ldy < hidden)
+        return fail(BI_ERR_INVALID_ARG, "%s: ldx and ldy must be >= hidden", fn);
+    const size_t ysz = y_dtype == BI_F32 ? 4 : 2;
+    if (!aligned(x, 2) || !aligned(gamma, 2) || !aligned(y, ysz))
+        return fail(BI_ERR_INVALID_ARG, "%s: pointers not element-aligned", fn);
+    cudaError_t why = cudaSuccess;
+    if (!current_device_info(&why)) return cuda_fail(why, fn);
+    cudaError_t e = launch_rmsnorm(x, ldx, gamma, y, ldy, y_dtype == BI_F32, rows, hidden, eps,
+                                   in_dtype == BI_F16, reinterpret_cast<cudaStream_t>(stream));
+    if (e != cudaSuccess) return cuda_fail(e, fn);
+    return BI_OK;
+}
+
+}  // namespace
+
+BI_EXPORT bi_status bi_matmul(const void* x, int64_t ldx, const void* w, int64_t ldw,
+                              int w_layout, void* y, int64_t ldy, int y_dtype, int64_t M,
+                              int64_t N, int64_t K, bi_stream_t stream) {
+    if (y_dtype != BI_BF16 && y_dtype != BI_F32)
+        return fail(BI_ERR_INVALID_ARG, "bi_matmul: y_dtype must be BI_BF16 or BI_F32");
+    return matmul_impl("bi_matmul", x, ldx, w, ldw, w_layout, y, ldy, BI_BF16, y_dtype, M, N, K,
+                       stream);
+}
+
+BI_EXPORT bi_status bi_matmul_ex(const void* x, int64_t ldx, const void* w, int64_t ldw,
+                                 int w_layout, void* y, int64_t ldy, int in_dtype, int y_dtype,
+                                 int64_t M, int64_t N, int64_t K, bi_stream_t stream) {
+    return matmul_impl("bi_matmul_ex", x, ldx, w, ldw, w_layout, y, ldy, in_dtype, y_dtype, M, N,
+                       K, stream);
 }
 
 // ========================================================================= rmsnorm
@@ -210,27 +260,17 @@ BI_EXPORT bi_status bi_matmul(const void* x, int64_t ldx, const void* w, int64_t
 BI_EXPORT bi_status bi_rmsnorm(const void* x, int64_t ldx, const void* gamma, void* y,
                                int64_t ldy, int y_dtype, int64_t rows, int64_t hidden, float eps,
                                bi_stream_t stream) {
-    init_limit_from_env();
-    if (rows < 0) return fail(BI_ERR_INVALID_ARG, "bi_rmsnorm: negative rows");
-    if (hidden < 1 || hidden > (int64_t(1) << 20))
-        return fail(BI_ERR_INVALID_ARG, "bi_rmsnorm: hidden must be in [1, 2^20]");
     if (y_dtype != BI_BF16 && y_dtype != BI_F32)
         return fail(BI_ERR_INVALID_ARG, "bi_rmsnorm: y_dtype must be BI_BF16 or BI_F32");
-    if (!std::isfinite(eps) || eps < 0.0f)
-        return fail(BI_ERR_INVALID_ARG, "bi_rmsnorm: eps must be finite and >= 0");
-    if (rows == 0) return BI_OK;
-    if (!x || !gamma || !y) return fail(BI_ERR_INVALID_ARG, "bi_rmsnorm: null pointer");
-    if (ldx < hidden || ldy < hidden)
-        return fail(BI_ERR_INVALID_ARG, "bi_rmsnorm: ldx and ldy must be >= hidden");
-    const size_t ysz = y_dtype == BI_F32 ? 4 : 2;
-    if (!aligned(x, 2) || !aligned(gamma, 2) || !aligned(y, ysz))
-        return fail(BI_ERR_INVALID_ARG, "bi_rmsnorm: pointers not element-aligned");
-    cudaError_t why = cudaSuccess;
-    if (!current_device_info(&why)) return cuda_fail(why, "bi_rmsnorm: device query");
-    cudaError_t e = launch_rmsnorm(x, ldx, gamma, y, ldy, y_dtype == BI_F32, rows, hidden, eps,
-                                   reinterpret_cast<cudaStream_t>(stream));
-    if (e != cudaSuccess) return cuda_fail(e, "bi_rmsnorm: launch");
-    return BI_OK;
+    return rmsnorm_impl("bi_rmsnorm", x, ldx, gamma, y, ldy, BI_BF16, y_dtype, rows, hidden, eps,
+                        stream);
+}
+
+BI_EXPORT bi_status bi_rmsnorm_ex(const void* x, int64_t ldx, const void* gamma, void* y,
+                                  int64_t ldy, int in_dtype, int y_dtype, int64_t rows,
+                                  int64_t hidden, float eps, bi_stream_t stream) {
+    return rmsnorm_impl("bi_rmsnorm_ex", x, ldx, gamma, y, ldy, in_dtype, y_dtype, rows, hidden,
+                        eps, stream);
 }
 
 // ======================================================================= attention

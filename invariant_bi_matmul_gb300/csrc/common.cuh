@@ -6,6 +6,7 @@
 
 #include <cuda.h>
 #include <cuda_bf16.h>
+#include <cuda_fp16.h>
 #include <cuda_runtime.h>
 #include <stdint.h>
 
@@ -458,13 +459,14 @@ __device__ __forceinline__ uint64_t umma_smem_desc(uint32_t saddr, uint32_t lbo,
            (static_cast<uint64_t>(layout & 7u) << 61);
 }
 
-// Instruction descriptor for kind::f16 with bf16 A/B and an fp32 accumulator.
+// Instruction descriptor for kind::f16 with bf16 A/B (or, with f16_ab, IEEE binary16
+// A/B -- both operands always of one type) and an fp32 accumulator.
 //   a_mn_major / b_mn_major: 0 = K-major operand in shared memory, 1 = M/N-major.
 __host__ __device__ constexpr uint32_t umma_idesc_bf16(int m, int n, int a_mn_major,
-                                                       int b_mn_major) {
+                                                       int b_mn_major, bool f16_ab = false) {
     return (1u << 4)                                        // D format: F32
-           | (1u << 7)                                      // A format: BF16
-           | (1u << 10)                                     // B format: BF16
+           | ((f16_ab ? 0u : 1u) << 7)                      // A format: F16 (0) / BF16 (1)
+           | ((f16_ab ? 0u : 1u) << 10)                     // B format: F16 (0) / BF16 (1)
            | (static_cast<uint32_t>(a_mn_major) << 15)      // A major
            | (static_cast<uint32_t>(b_mn_major) << 16)      // B major
            | (static_cast<uint32_t>(n >> 3) << 17)          // N / 8
@@ -500,6 +502,25 @@ __device__ __forceinline__ void mma_bf16_16816(float (&d)[4], const uint32_t (&a
 __device__ __forceinline__ uint32_t pack_bf16x2(float lo, float hi) {
     __nv_bfloat162 v = __floats2bfloat162_rn(lo, hi);  // .x = lo (low 16 bits)
     return *reinterpret_cast<uint32_t*>(&v);
+}
+
+__device__ __forceinline__ uint32_t pack_f16x2(float lo, float hi) {
+    __half2 v = __floats2half2_rn(lo, hi);  // .x = lo (low 16 bits)
+    return *reinterpret_cast<uint32_t*>(&v);
+}
+
+// Two 16-bit results rounded to nearest even: binary16 when f16, else bf16.
+__device__ __forceinline__ uint32_t pack16x2(float lo, float hi, bool f16) {
+    return f16 ? pack_f16x2(lo, hi) : pack_bf16x2(lo, hi);
+}
+
+__device__ __forceinline__ uint16_t round16(float v, bool f16) {
+    return f16 ? __half_as_ushort(__float2half_rn(v)) : __bfloat16_as_ushort(__float2bfloat16_rn(v));
+}
+
+// One 16-bit value widened to fp32 (exact): binary16 when f16, else bf16.
+__device__ __forceinline__ float widen16(uint16_t h, bool f16) {
+    return f16 ? __half2float(__ushort_as_half(h)) : __uint_as_float(uint32_t(h) << 16);
 }
 
 }  // namespace bi

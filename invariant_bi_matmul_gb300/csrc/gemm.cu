@@ -92,6 +92,7 @@ struct GemmArgs {
     // The invariant kernel has splits = 1 and kb_per_split = the number of K-blocks.
     int splits;
     int kb_per_split;
+    int f16;           // X, W (and a 16-bit Y) are IEEE binary16 instead of bf16
 };
 
 template <bool KN, bool F32OUT, int NSUB, bool SPLIT, int MSUB>
@@ -295,7 +296,7 @@ gemm_kernel(const __grid_constant__ CUtensorMap tmap_x, const __grid_constant__ 
     } else if (warp == 1) {
         // ---------------------------------------------------------------- MMA issuer
         // The whole warp runs the loop; one elected lane issues the MMAs and commits.
-        constexpr uint32_t idesc = umma_idesc_bf16(BM, BN, 0, KN ? 1 : 0);
+        const uint32_t idesc = umma_idesc_bf16(BM, BN, 0, KN ? 1 : 0, args.f16 != 0);
         // X: K-major, 128-byte swizzle, 8-row groups 1024 B apart; +32 B per k16 step
         const uint64_t a_desc0 = umma_smem_desc(smem_addr(sA), 16, 1024, 2);
         // W, layout NK: K-major like X.  Layout KN: N-major; k-rows of KN_SWIZZLE bytes,
@@ -384,6 +385,7 @@ gemm_kernel(const __grid_constant__ CUtensorMap tmap_x, const __grid_constant__ 
         const int64_t ldy = args.ldy;
         const bool vec_ok = F32OUT ? ((ldy % 4) == 0 && (reinterpret_cast<uintptr_t>(y) % 16) == 0)
                                    : ((ldy % 8) == 0 && (reinterpret_cast<uintptr_t>(y) % 16) == 0);
+        const bool h16 = args.f16 != 0;
         // Split-K: rank r > 0 hands its fp32 partial to rank 0 through rank 0's shared
         // memory (slot r-1 at the top of the ring area: a_rows rows of tile_n floats, the
         // 16-byte pieces of row i rotated by i & 7 so that a warp's stores and loads hit
@@ -473,20 +475,20 @@ gemm_kernel(const __grid_constant__ CUtensorMap tmap_x, const __grid_constant__ 
                                 if (gn0 + i < N) yr[i] = __uint_as_float(r[i]);
                         }
                     } else {
-                        __nv_bfloat16* yr = static_cast<__nv_bfloat16*>(y) + gm * ldy + gn0;
+                        uint16_t* yr = static_cast<uint16_t*>(y) + gm * ldy + gn0;
                         if (vec_ok && gn0 + 32 <= N) {
 #pragma unroll
                             for (int i = 0; i < 32; i += 8) {
                                 uint4 v;
-                                v.x = pack_bf16x2(__uint_as_float(r[i]), __uint_as_float(r[i + 1]));
-                                v.y = pack_bf16x2(__uint_as_float(r[i + 2]), __uint_as_float(r[i + 3]));
-                                v.z = pack_bf16x2(__uint_as_float(r[i + 4]), __uint_as_float(r[i + 5]));
-                                v.w = pack_bf16x2(__uint_as_float(r[i + 6]), __uint_as_float(r[i + 7]));
+                                v.x = pack16x2(__uint_as_float(r[i]), __uint_as_float(r[i + 1]), h16);
+                                v.y = pack16x2(__uint_as_float(r[i + 2]), __uint_as_float(r[i + 3]), h16);
+                                v.z = pack16x2(__uint_as_float(r[i + 4]), __uint_as_float(r[i + 5]), h16);
+                                v.w = pack16x2(__uint_as_float(r[i + 6]), __uint_as_float(r[i + 7]), h16);
                                 *reinterpret_cast<uint4*>(yr + i) = v;
                             }
                         } else {
                             for (int i = 0; i < 32; ++i)
-                                if (gn0 + i < N) yr[i] = __float2bfloat16_rn(__uint_as_float(r[i]));
+                                if (gn0 + i < N) yr[i] = round16(__uint_as_float(r[i]), h16);
                         }
                     }
                 }
@@ -658,10 +660,10 @@ GemmSchedule gemm_schedule(int64_t M, int64_t N, int64_t K, bool w_kn, int num_s
 
 cudaError_t launch_gemm(const DeviceInfo& dev, const void* x, int64_t ldx, const void* w,
                         int64_t ldw, bool w_kn, void* y, int64_t ldy, bool y_f32, int64_t M,
-                        int64_t N, int64_t K, bool split_ok, cudaStream_t stream) {
+                        int64_t N, int64_t K, bool split_ok, bool f16, cudaStream_t stream) {
     if (M == 0 || N == 0) return cudaSuccess;
     if (K == 0) {
-        // an empty reduction: every output is +0 (all-zero bits in bf16 and fp32)
+        // an empty reduction: every output is +0 (all-zero bits in bf16, binary16 and fp32)
         const size_t es = y_f32 ? 4 : 2;
         return cudaMemset2DAsync(y, size_t(ldy) * es, 0, size_t(N) * es, size_t(M), stream);
     }
@@ -678,19 +680,20 @@ cudaError_t launch_gemm(const DeviceInfo& dev, const void* x, int64_t ldx, const
     bool ok;
     if (g.blocked)
         ok = tmap_kblocked_bf16(&mx, x, uint64_t(K), uint64_t(M), uint64_t(ldx), BK,
-                                uint32_t(g.a_rows), uint32_t(g.kbs), 128);
+                                uint32_t(g.a_rows), uint32_t(g.kbs), 128, f16);
     else
-        ok = tmap_2d_bf16(&mx, x, uint64_t(K), uint64_t(M), uint64_t(ldx), BK, uint32_t(g.a_rows), 128);
+        ok = tmap_2d_bf16(&mx, x, uint64_t(K), uint64_t(M), uint64_t(ldx), BK, uint32_t(g.a_rows),
+                          128, f16);
     if (!ok) return cudaErrorNotSupported;
     if (w_kn)
         ok = tmap_2d_bf16(&mw, w, uint64_t(N), uint64_t(K), uint64_t(ldw), KN_ATOM_N,
-                          uint32_t(BK * g.kbs), KN_SWIZZLE);
+                          uint32_t(BK * g.kbs), KN_SWIZZLE, f16);
     else if (g.blocked)
         ok = tmap_kblocked_bf16(&mw, w, uint64_t(K), uint64_t(N), uint64_t(ldw), BK,
-                                uint32_t(g.nsub * BN), uint32_t(g.kbs), 128);
+                                uint32_t(g.nsub * BN), uint32_t(g.kbs), 128, f16);
     else
         ok = tmap_2d_bf16(&mw, w, uint64_t(K), uint64_t(N), uint64_t(ldw), BK,
-                          uint32_t(g.nsub * BN), 128);
+                          uint32_t(g.nsub * BN), 128, f16);
     if (!ok) return cudaErrorNotSupported;
     GemmArgs a;
     a.y = y;
@@ -706,6 +709,7 @@ cudaError_t launch_gemm(const DeviceInfo& dev, const void* x, int64_t ldx, const
     a.w_stream_once = (M + BM - 1) / BM == 1 ? 1 : 0;
     a.splits = g.splits;
     a.kb_per_split = g.kb_per_split;
+    a.f16 = f16 ? 1 : 0;
     if (g.splits > 1)
         return w_kn ? (y_f32 ? launch_split<true, true>(dev, mx, mw, a, g.tiles, stream)
                              : launch_split<true, false>(dev, mx, mw, a, g.tiles, stream))

@@ -69,14 +69,14 @@ const DeviceInfo* current_device_info(cudaError_t* why);
 
 // ---------------------------------------------------------------- RMSNorm (rmsnorm.cu)
 cudaError_t launch_rmsnorm(const void* x, int64_t ldx, const void* gamma, void* y, int64_t ldy,
-                           bool y_f32, int64_t rows, int64_t hidden, float eps,
+                           bool y_f32, int64_t rows, int64_t hidden, float eps, bool f16,
                            cudaStream_t stream);
 
 // ------------------------------------------------------------------- GEMM (gemm.cu)
 // Returns cudaErrorNotSupported when a TMA descriptor cannot be encoded.
 cudaError_t launch_gemm(const DeviceInfo& dev, const void* x, int64_t ldx, const void* w,
                         int64_t ldw, bool w_kn, void* y, int64_t ldy, bool y_f32, int64_t M,
-                        int64_t N, int64_t K, bool split_ok, cudaStream_t stream);
+                        int64_t N, int64_t K, bool split_ok, bool f16, cudaStream_t stream);
 int gemm_tile_n();
 
 // How a GEMM launch is scheduled: X rows staged per K-block, instruction tiles per CTA

@@ -36,23 +36,29 @@ __device__ __forceinline__ uint4 load_group_raw(const __nv_bfloat16* __restrict_
                       h[4] | (uint32_t(h[5]) << 16), h[6] | (uint32_t(h[7]) << 16));
 }
 
-__device__ __forceinline__ void unpack_group(const uint4& raw, float (&v)[8]) {
+// Eight 16-bit values widened to fp32 (exact): bf16, or IEEE binary16 when f16.
+__device__ __forceinline__ void unpack_group(const uint4& raw, float (&v)[8], bool f16) {
     const uint32_t w[4] = {raw.x, raw.y, raw.z, raw.w};
 #pragma unroll
     for (int i = 0; i < 4; ++i) {
-        v[2 * i] = __uint_as_float(w[i] << 16);
-        v[2 * i + 1] = __uint_as_float(w[i] & 0xffff0000u);
+        if (f16) {
+            v[2 * i] = widen16(uint16_t(w[i] & 0xffffu), true);
+            v[2 * i + 1] = widen16(uint16_t(w[i] >> 16), true);
+        } else {
+            v[2 * i] = __uint_as_float(w[i] << 16);
+            v[2 * i + 1] = __uint_as_float(w[i] & 0xffff0000u);
+        }
     }
 }
 
 __device__ __forceinline__ void load_group(const __nv_bfloat16* __restrict__ row, int64_t g,
-                                           int H, bool vec, float (&v)[8]) {
-    unpack_group(load_group_raw(row, g, H, vec), v);
+                                           int H, bool vec, float (&v)[8], bool f16) {
+    unpack_group(load_group_raw(row, g, H, vec), v, f16);
 }
 
 template <bool F32OUT>
 __device__ __forceinline__ void store_group(void* __restrict__ yrow, int64_t g, int H, bool vec,
-                                            const float (&o)[8]) {
+                                            const float (&o)[8], bool f16) {
     const int64_t e0 = g * 8;
     if (vec && e0 + 8 <= H) {
         if (F32OUT) {
@@ -61,10 +67,10 @@ __device__ __forceinline__ void store_group(void* __restrict__ yrow, int64_t g, 
             p[1] = make_float4(o[4], o[5], o[6], o[7]);
         } else {
             uint4 raw;
-            raw.x = pack_bf16x2(o[0], o[1]);
-            raw.y = pack_bf16x2(o[2], o[3]);
-            raw.z = pack_bf16x2(o[4], o[5]);
-            raw.w = pack_bf16x2(o[6], o[7]);
+            raw.x = pack16x2(o[0], o[1], f16);
+            raw.y = pack16x2(o[2], o[3], f16);
+            raw.z = pack16x2(o[4], o[5], f16);
+            raw.w = pack16x2(o[6], o[7], f16);
             *reinterpret_cast<uint4*>(static_cast<__nv_bfloat16*>(yrow) + e0) = raw;
         }
     } else {
@@ -74,7 +80,7 @@ __device__ __forceinline__ void store_group(void* __restrict__ yrow, int64_t g, 
                 if (F32OUT)
                     static_cast<float*>(yrow)[e0 + i] = o[i];
                 else
-                    static_cast<__nv_bfloat16*>(yrow)[e0 + i] = __float2bfloat16_rn(o[i]);
+                    static_cast<uint16_t*>(yrow)[e0 + i] = round16(o[i], f16);
             }
         }
     }
@@ -90,7 +96,7 @@ template <int MAXJ, bool F32OUT, int ROWS>
 __global__ void __launch_bounds__(kThreads)
 rmsnorm_kernel(const __nv_bfloat16* __restrict__ x, int64_t ldx,
                const __nv_bfloat16* __restrict__ gamma, void* __restrict__ y, int64_t ldy,
-               int64_t rows, int H, float eps, int vec) {
+               int64_t rows, int H, float eps, int vec, int f16) {
     __shared__ float warp_sums[ROWS][kWarps];
     pdl_wait();
     pdl_trigger();
@@ -98,6 +104,7 @@ rmsnorm_kernel(const __nv_bfloat16* __restrict__ x, int64_t ldx,
     const int64_t ngroups = (H + 7) / 8;
     const int t = threadIdx.x;
     const bool v16 = vec != 0;
+    const bool h16 = f16 != 0;  // x, gamma (and a 16-bit y) are binary16 instead of bf16
     constexpr int J = MAXJ > 0 ? MAXJ : 1;
 
     float acc[ROWS];
@@ -130,7 +137,7 @@ rmsnorm_kernel(const __nv_bfloat16* __restrict__ x, int64_t ldx,
                 const int64_t g = t + static_cast<int64_t>(j) * kThreads;
                 if (g < ngroups) {
                     float v[8];
-                    unpack_group(xs[rr][j], v);
+                    unpack_group(xs[rr][j], v, h16);
 #pragma unroll
                     for (int i = 0; i < 8; ++i) acc[rr] = fmaf(v[i], v[i], acc[rr]);
                 }
@@ -140,7 +147,7 @@ rmsnorm_kernel(const __nv_bfloat16* __restrict__ x, int64_t ldx,
         const __nv_bfloat16* __restrict__ xr = x + row0 * ldx;
         for (int64_t g = t; g < ngroups; g += kThreads) {
             float v[8];
-            load_group(xr, g, H, v16, v);
+            load_group(xr, g, H, v16, v, h16);
 #pragma unroll
             for (int i = 0; i < 8; ++i) acc[0] = fmaf(v[i], v[i], acc[0]);
         }
@@ -175,22 +182,22 @@ rmsnorm_kernel(const __nv_bfloat16* __restrict__ x, int64_t ldx,
                 const int64_t g = t + static_cast<int64_t>(j) * kThreads;
                 if (g < ngroups) {
                     float v[8], gm[8], o[8];
-                    unpack_group(xs[rr][j], v);
-                    unpack_group(gs[j], gm);
+                    unpack_group(xs[rr][j], v, h16);
+                    unpack_group(gs[j], gm, h16);
 #pragma unroll
                     for (int i = 0; i < 8; ++i) o[i] = (v[i] * inv) * gm[i];
-                    store_group<F32OUT>(yrow, g, H, v16, o);
+                    store_group<F32OUT>(yrow, g, H, v16, o, h16);
                 }
             }
         } else {
             const __nv_bfloat16* __restrict__ xr = x + row * ldx;
             for (int64_t g = t; g < ngroups; g += kThreads) {
                 float v[8], gm[8], o[8];
-                load_group(xr, g, H, v16, v);
-                load_group(gamma, g, H, v16, gm);
+                load_group(xr, g, H, v16, v, h16);
+                load_group(gamma, g, H, v16, gm, h16);
 #pragma unroll
                 for (int i = 0; i < 8; ++i) o[i] = (v[i] * inv) * gm[i];
-                store_group<F32OUT>(yrow, g, H, v16, o);
+                store_group<F32OUT>(yrow, g, H, v16, o, h16);
             }
         }
     }
@@ -198,24 +205,26 @@ rmsnorm_kernel(const __nv_bfloat16* __restrict__ x, int64_t ldx,
 
 template <int MAXJ, int ROWS>
 cudaError_t launch_impl(const void* x, int64_t ldx, const void* gamma, void* y, int64_t ldy,
-                        bool y_f32, int64_t rows, int H, float eps, int vec, cudaStream_t s) {
+                        bool y_f32, int64_t rows, int H, float eps, int vec, int f16,
+                        cudaStream_t s) {
     dim3 grid(static_cast<unsigned>((rows + ROWS - 1) / ROWS)), block(kThreads);
     auto xb = static_cast<const __nv_bfloat16*>(x);
     auto gb = static_cast<const __nv_bfloat16*>(gamma);
     if (y_f32)
         return launch_pdl(rmsnorm_kernel<MAXJ, true, ROWS>, grid, block, 0, s, xb, ldx, gb, y,
-                          ldy, rows, H, eps, vec);
+                          ldy, rows, H, eps, vec, f16);
     return launch_pdl(rmsnorm_kernel<MAXJ, false, ROWS>, grid, block, 0, s, xb, ldx, gb, y, ldy,
-                      rows, H, eps, vec);
+                      rows, H, eps, vec, f16);
 }
 
 }  // namespace
 
 cudaError_t launch_rmsnorm(const void* x, int64_t ldx, const void* gamma, void* y, int64_t ldy,
-                           bool y_f32, int64_t rows, int64_t hidden, float eps,
+                           bool y_f32, int64_t rows, int64_t hidden, float eps, bool f16,
                            cudaStream_t stream) {
     if (rows == 0) return cudaSuccess;
     const int H = static_cast<int>(hidden);
+    const int h16 = f16 ? 1 : 0;
     const size_t ysz = y_f32 ? 4 : 2;
     const bool vec = (reinterpret_cast<uintptr_t>(x) % 16 == 0) && (ldx % 8 == 0) &&
                      (reinterpret_cast<uintptr_t>(gamma) % 16 == 0) &&
@@ -232,20 +241,18 @@ cudaError_t launch_rmsnorm(const void* x, int64_t ldx, const void* gamma, void* 
         // two rows per CTA once there are enough rows to keep every SM busy: more bytes
         // in flight per thread (scheduling only; each row's arithmetic is unchanged)
         const bool two = n >= 1024;
+#define BI_RMS_ARGS xs, ldx, gamma, ys, ldy, y_f32, n, H, eps, vec, h16, stream
         if (groups_per_thread <= 1)
-            e = two ? launch_impl<1, 2>(xs, ldx, gamma, ys, ldy, y_f32, n, H, eps, vec, stream)
-                    : launch_impl<1, 1>(xs, ldx, gamma, ys, ldy, y_f32, n, H, eps, vec, stream);
+            e = two ? launch_impl<1, 2>(BI_RMS_ARGS) : launch_impl<1, 1>(BI_RMS_ARGS);
         else if (groups_per_thread <= 2)
-            e = two ? launch_impl<2, 2>(xs, ldx, gamma, ys, ldy, y_f32, n, H, eps, vec, stream)
-                    : launch_impl<2, 1>(xs, ldx, gamma, ys, ldy, y_f32, n, H, eps, vec, stream);
+            e = two ? launch_impl<2, 2>(BI_RMS_ARGS) : launch_impl<2, 1>(BI_RMS_ARGS);
         else if (groups_per_thread <= 4)
-            e = two ? launch_impl<4, 2>(xs, ldx, gamma, ys, ldy, y_f32, n, H, eps, vec, stream)
-                    : launch_impl<4, 1>(xs, ldx, gamma, ys, ldy, y_f32, n, H, eps, vec, stream);
+            e = two ? launch_impl<4, 2>(BI_RMS_ARGS) : launch_impl<4, 1>(BI_RMS_ARGS);
         else if (groups_per_thread <= kMaxGroupsInRegs)
-            e = launch_impl<kMaxGroupsInRegs, 1>(xs, ldx, gamma, ys, ldy, y_f32, n, H, eps, vec,
-                                                 stream);
+            e = launch_impl<kMaxGroupsInRegs, 1>(BI_RMS_ARGS);
         else
-            e = launch_impl<0, 1>(xs, ldx, gamma, ys, ldy, y_f32, n, H, eps, vec, stream);
+            e = launch_impl<0, 1>(BI_RMS_ARGS);
+#undef BI_RMS_ARGS
         if (e != cudaSuccess) return e;
     }
     return cudaSuccess;

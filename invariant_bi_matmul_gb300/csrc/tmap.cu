@@ -34,10 +34,11 @@ struct MapKey {
     uint64_t inner, outer, stride;
     uint32_t box_inner, box_outer, swizzle;
     uint32_t box_blocks;  // 0: rank-2 map; >0: rank-3 K-blocked map with this many blocks
+    bool f16;             // element type: IEEE binary16 instead of bf16
     bool operator==(const MapKey& o) const {
         return ptr == o.ptr && inner == o.inner && outer == o.outer && stride == o.stride &&
                box_inner == o.box_inner && box_outer == o.box_outer && swizzle == o.swizzle &&
-               box_blocks == o.box_blocks;
+               box_blocks == o.box_blocks && f16 == o.f16;
     }
 };
 struct MapKeyHash {
@@ -47,7 +48,7 @@ struct MapKeyHash {
         h ^= k.outer + 0x9E3779B97F4A7C15ull + (h << 6) + (h >> 2);
         h ^= k.stride + 0x9E3779B97F4A7C15ull + (h << 6) + (h >> 2);
         h ^= (uint64_t(k.box_inner) << 32 | k.box_outer) + (h << 6) + (h >> 2);
-        return size_t(h ^ k.swizzle ^ (uint64_t(k.box_blocks) << 40));
+        return size_t(h ^ k.swizzle ^ (uint64_t(k.box_blocks) << 40) ^ (uint64_t(k.f16) << 63));
     }
 };
 
@@ -55,9 +56,10 @@ std::mutex g_map_mu;
 std::unordered_map<MapKey, CUtensorMap, MapKeyHash> g_maps;
 
 bool tmap_bf16_impl(CUtensorMap* out, const void* ptr, uint64_t inner, uint64_t outer, uint64_t stride,
-                uint32_t box_inner, uint32_t box_outer, int swizzle_bytes, uint32_t box_blocks) {
+                uint32_t box_inner, uint32_t box_outer, int swizzle_bytes, uint32_t box_blocks,
+                bool f16) {
     const MapKey key{reinterpret_cast<uintptr_t>(ptr), inner, outer, stride, box_inner, box_outer,
-                     uint32_t(swizzle_bytes), box_blocks};
+                     uint32_t(swizzle_bytes), box_blocks, f16};
     {
         std::lock_guard<std::mutex> lk(g_map_mu);
         auto it = g_maps.find(key);
@@ -69,6 +71,8 @@ bool tmap_bf16_impl(CUtensorMap* out, const void* ptr, uint64_t inner, uint64_t 
     EncodeTiledFn fn = encode_fn();
     if (!fn) return false;
     CUtensorMap m;
+    const CUtensorMapDataType dt =
+        f16 ? CU_TENSOR_MAP_DATA_TYPE_FLOAT16 : CU_TENSOR_MAP_DATA_TYPE_BFLOAT16;
     const CUtensorMapSwizzle sw = swizzle_bytes == 128  ? CU_TENSOR_MAP_SWIZZLE_128B
                                   : swizzle_bytes == 64 ? CU_TENSOR_MAP_SWIZZLE_64B
                                                         : CU_TENSOR_MAP_SWIZZLE_32B;
@@ -78,7 +82,7 @@ bool tmap_bf16_impl(CUtensorMap* out, const void* ptr, uint64_t inner, uint64_t 
         const cuuint64_t strides[1] = {stride * 2};
         const cuuint32_t box[2] = {box_inner, box_outer};
         const cuuint32_t estr[2] = {1, 1};
-        r = fn(&m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, const_cast<void*>(ptr), dims, strides, box,
+        r = fn(&m, dt, 2, const_cast<void*>(ptr), dims, strides, box,
                estr, CU_TENSOR_MAP_INTERLEAVE_NONE, sw, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
                CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
     } else {
@@ -88,7 +92,7 @@ bool tmap_bf16_impl(CUtensorMap* out, const void* ptr, uint64_t inner, uint64_t 
         const cuuint64_t strides[2] = {stride * 2, uint64_t(box_inner) * 2};
         const cuuint32_t box[3] = {box_inner, box_outer, box_blocks};
         const cuuint32_t estr[3] = {1, 1, 1};
-        r = fn(&m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 3, const_cast<void*>(ptr), dims, strides, box,
+        r = fn(&m, dt, 3, const_cast<void*>(ptr), dims, strides, box,
                estr, CU_TENSOR_MAP_INTERLEAVE_NONE, sw, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
                CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
     }
@@ -103,16 +107,18 @@ bool tmap_bf16_impl(CUtensorMap* out, const void* ptr, uint64_t inner, uint64_t 
 }  // namespace
 
 bool tmap_2d_bf16(CUtensorMap* out, const void* ptr, uint64_t inner, uint64_t outer,
-                  uint64_t stride, uint32_t box_inner, uint32_t box_outer, int swizzle_bytes) {
-    return tmap_bf16_impl(out, ptr, inner, outer, stride, box_inner, box_outer, swizzle_bytes, 0);
+                  uint64_t stride, uint32_t box_inner, uint32_t box_outer, int swizzle_bytes,
+                  bool f16) {
+    return tmap_bf16_impl(out, ptr, inner, outer, stride, box_inner, box_outer, swizzle_bytes, 0,
+                          f16);
 }
 
 bool tmap_kblocked_bf16(CUtensorMap* out, const void* ptr, uint64_t inner, uint64_t outer,
                         uint64_t stride, uint32_t box_inner, uint32_t box_outer,
-                        uint32_t box_blocks, int swizzle_bytes) {
+                        uint32_t box_blocks, int swizzle_bytes, bool f16) {
     if (box_blocks == 0 || inner % box_inner != 0) return false;
     return tmap_bf16_impl(out, ptr, inner, outer, stride, box_inner, box_outer, swizzle_bytes,
-                          box_blocks);
+                          box_blocks, f16);
 }
 
 }  // namespace bi

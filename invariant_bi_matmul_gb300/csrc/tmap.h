@@ -8,9 +8,11 @@ namespace bi {
 
 // 2D bf16 tensor [outer][inner] with a row stride of `stride` elements, tiled in boxes
 // of box_inner x box_outer with the given shared-memory swizzle (32, 64 or 128 bytes).
+// f16: the elements are IEEE binary16 instead (same size, same layout).
 // Returns false if the descriptor cannot be encoded (alignment, stride, driver).
 bool tmap_2d_bf16(CUtensorMap* out, const void* ptr, uint64_t inner, uint64_t outer,
-                  uint64_t stride, uint32_t box_inner, uint32_t box_outer, int swizzle_bytes);
+                  uint64_t stride, uint32_t box_inner, uint32_t box_outer, int swizzle_bytes,
+                  bool f16 = false);
 
 // The same tensor viewed in rank 3 as (box_inner-wide column, row, column block), so one
 // copy of box (box_inner, box_outer, box_blocks) lands as box_blocks consecutive
@@ -18,6 +20,6 @@ bool tmap_2d_bf16(CUtensorMap* out, const void* ptr, uint64_t inner, uint64_t ou
 // Requires inner % box_inner == 0 (the view never reaches past a row).
 bool tmap_kblocked_bf16(CUtensorMap* out, const void* ptr, uint64_t inner, uint64_t outer,
                         uint64_t stride, uint32_t box_inner, uint32_t box_outer,
-                        uint32_t box_blocks, int swizzle_bytes);
+                        uint32_t box_blocks, int swizzle_bytes, bool f16 = false);
 
 }  // namespace bi

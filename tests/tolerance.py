@@ -49,10 +49,34 @@ def check_f32(gpu, oracle_f32, scale, what=""):
     return float(err.max()) if err.size else 0.0
 
 
+# binary16 outputs (the pages state no bar for them; derived): round to nearest even costs
+# at most 2^-11 relative (2^-25 absolute below the normal range), on top of the fp32
+# accumulation error the fp32 check allows (F32_REL of the natural scale S).
+F16_ULP_REL = 2.0 ** -11
+F16_SUB_ABS = 2.0 ** -25
+
+
+def check_f16(gpu, oracle_f32, scale, what=""):
+    g = to_f64(gpu)
+    o = np.asarray(oracle_f32, dtype=np.float64)
+    s = np.broadcast_to(np.asarray(scale, dtype=np.float64), o.shape)
+    assert g.shape == o.shape, (g.shape, o.shape)
+    assert np.all(np.isfinite(g)), f"{what}: non-finite GPU output"
+    err = np.abs(g - o)
+    bound = F16_ULP_REL * np.abs(o) + F16_SUB_ABS + F32_REL * s * (1 + F16_ULP_REL)
+    bad = err > bound
+    if bad.any():
+        i = np.unravel_index(np.argmax(err / bound), err.shape)
+        raise AssertionError(f"{what}: {int(bad.sum())} elements outside fp16 tolerance; worst at "
+                             f"{i}: gpu={g[i]!r} oracle={o[i]!r} scale={s[i]!r}")
+    return float(err.max()) if err.size else 0.0
+
+
 def bits_equal(a, b) -> bool:
     """Bitwise equality of two CUDA/CPU tensors of the same dtype."""
     import torch
     if a.dtype != b.dtype or a.shape != b.shape:
         return False
-    view = {torch.bfloat16: torch.int16, torch.float32: torch.int32}[a.dtype]
+    view = {torch.bfloat16: torch.int16, torch.float16: torch.int16,
+            torch.float32: torch.int32}[a.dtype]
     return bool(torch.equal(a.contiguous().view(view).cpu(), b.contiguous().view(view).cpu()))
