@@ -761,6 +761,18 @@ def run_sweep():
                           "graph_frac_tensor": round(fl / tg / 1e6 / float(
                               peaks.get("bf16_tflops", 1900.0)), 3)}), flush=True)
     del hsets, xh, wh
+    # fp32 inputs (CUDA cores): W 64 MB, one set (larger than L2)
+    xf, wf = x.float(), wnk.float()
+    for M in (8, 2048):
+        xm = xf[:M].contiguous()
+        y = torch.empty(M, N, dtype=torch.float32, device=dev)
+        tg = graph_us([lambda: bi.matmul(xm, wf, "nk", out=y)], n=8)
+        fl, by = 2 * M * N * K, 4 * N * K + 4 * M * K + 4 * M * N
+        print(json.dumps({"sweep": "gemm_f32", "M": M, "K": K, "N": N, "graph_us": round(tg, 2),
+                          "TFLOP/s": round(fl / tg / 1e6, 2),
+                          "graph_frac_hbm": round(by / tg / 1e3 / peaks["hbm_gbs"], 3)}),
+              flush=True)
+    del xf, wf
     for B in (1, 3, 16, 128, 2048):
         xr, g = inputs.rmsnorm_inputs(B, 8192, seed=3)
         xr, g = xr.to(dev), g.to(dev)

@@ -158,8 +158,11 @@ bi_status bi_matmul(const void* x, int64_t ldx, const void* w, int64_t ldw, int 
 /* bi_matmul with the input type given: in_dtype BI_BF16 or BI_F16 (IEEE binary16) for
  * both x and w (one MMA type for both operands); y_dtype in_dtype (round to nearest even)
  * or BI_F32.  [MLX-4279, the tester's comment: dense matmul divergence also shows for
- * f16 inputs.]  Same construction, same invariance, same rules as bi_matmul (which is
- * bi_matmul_ex with in_dtype = BI_BF16). */
+ * f16 and f32 inputs.]  Same construction, same invariance, same rules as bi_matmul (which
+ * is bi_matmul_ex with in_dtype = BI_BF16).
+ * in_dtype BI_F32 (y_dtype BI_F32): CUDA cores, each output the fmaf chain over k = 0 ..
+ * K-1 in ascending order from +0, for every M and tile; pointers need only element
+ * alignment; the batch-invariant limit has no effect (there is one configuration). */
 bi_status bi_matmul_ex(const void* x, int64_t ldx, const void* w, int64_t ldw, int w_layout,
                        void* y, int64_t ldy, int in_dtype, int y_dtype, int64_t M, int64_t N,
                        int64_t K, bi_stream_t stream);
@@ -182,8 +185,9 @@ bi_status bi_rmsnorm(const void* x, int64_t ldx, const void* gamma, void* y, int
                      int y_dtype, int64_t rows, int64_t hidden, float eps,
                      bi_stream_t stream);
 
-/* bi_rmsnorm with the input type given: x and gamma both in_dtype (BI_BF16 or BI_F16);
- * y_dtype in_dtype or BI_F32.  Same tree and arithmetic after the exact widening. */
+/* bi_rmsnorm with the input type given: x and gamma both in_dtype (BI_BF16, BI_F16 or
+ * BI_F32); y_dtype in_dtype or BI_F32.  Same tree and arithmetic after the exact
+ * widening (fp32: the same per-thread groups, butterfly and warp tree on fp32 values). */
 bi_status bi_rmsnorm_ex(const void* x, int64_t ldx, const void* gamma, void* y, int64_t ldy,
                         int in_dtype, int y_dtype, int64_t rows, int64_t hidden, float eps,
                         bi_stream_t stream);

@@ -177,12 +177,14 @@ def _in_dtype(t, name):
         return BI_BF16
     if t.dtype == torch.float16:
         return BI_F16
-    raise ValueError(f"{name} must be bf16 or fp16")
+    if t.dtype == torch.float32:
+        return BI_F32
+    raise ValueError(f"{name} must be bf16, fp16 or fp32")
 
 
 def matmul(x, w, w_layout: str = "nk", out=None, out_dtype=None, stream=None):
-    """Y = X @ W for X [M,K] and W [N,K] ("nk", nn.Linear) or [K,N] ("kn"), both bf16 or
-    both fp16; Y in the input type or fp32."""
+    """Y = X @ W for X [M,K] and W [N,K] ("nk", nn.Linear) or [K,N] ("kn"), both bf16, both
+    fp16 or both fp32; Y in the input type or fp32."""
     torch = _torch()
     dt = _in_dtype(x, "x")
     _need(x, x.dtype, "x", 2)
@@ -207,7 +209,7 @@ def matmul(x, w, w_layout: str = "nk", out=None, out_dtype=None, stream=None):
 
 def rmsnorm(x, gamma, eps: float, out=None, out_dtype=None, stream=None):
     """y = x * rsqrt(mean(x^2) + eps) * gamma over the last dim of [rows, H] x; x and
-    gamma both bf16 or both fp16; y in the input type or fp32."""
+    gamma both bf16, both fp16 or both fp32; y in the input type or fp32."""
     torch = _torch()
     dt = _in_dtype(x, "x")
     _need(x, x.dtype, "x", 2)

@@ -176,11 +176,27 @@ bi_status matmul_impl(const char* fn, const void* x, int64_t ldx, const void* w,
         return fail(BI_ERR_UNSUPPORTED, "%s: M, N, K must be < 2^31", fn);
     if (w_layout != BI_W_NK && w_layout != BI_W_KN)
         return fail(BI_ERR_INVALID_ARG, "%s: w_layout must be BI_W_NK or BI_W_KN", fn);
-    if (in_dtype != BI_BF16 && in_dtype != BI_F16)
-        return fail(BI_ERR_INVALID_ARG, "%s: in_dtype must be BI_BF16 or BI_F16", fn);
+    if (in_dtype != BI_BF16 && in_dtype != BI_F16 && in_dtype != BI_F32)
+        return fail(BI_ERR_INVALID_ARG, "%s: in_dtype must be BI_BF16, BI_F16 or BI_F32", fn);
     if (y_dtype != in_dtype && y_dtype != BI_F32)
         return fail(BI_ERR_INVALID_ARG, "%s: y_dtype must be in_dtype or BI_F32", fn);
     if (M == 0 || N == 0) return BI_OK;
+    if (in_dtype == BI_F32) {
+        if (!y || ldy < N) return fail(BI_ERR_INVALID_ARG, "%s: null y or ldy < N", fn);
+        if (K > 0) {
+            if (!x || !w) return fail(BI_ERR_INVALID_ARG, "%s: null x or w", fn);
+            if (ldx < K || ldw < (w_layout == BI_W_NK ? K : N))
+                return fail(BI_ERR_INVALID_ARG, "%s: ldx or ldw too small", fn);
+        }
+        if (!aligned(y, 4) || (K > 0 && (!aligned(x, 4) || !aligned(w, 4))))
+            return fail(BI_ERR_INVALID_ARG, "%s: pointers not element-aligned", fn);
+        cudaError_t why = cudaSuccess;
+        if (!current_device_info(&why)) return cuda_fail(why, fn);
+        cudaError_t e = launch_gemm_f32(x, ldx, w, ldw, w_layout == BI_W_KN, y, ldy, M, N, K,
+                                        reinterpret_cast<cudaStream_t>(stream));
+        if (e != cudaSuccess) return cuda_fail(e, fn);
+        return BI_OK;
+    }
     if (!y) return fail(BI_ERR_INVALID_ARG, "%s: null y", fn);
     if (ldy < N) return fail(BI_ERR_INVALID_ARG, "%s: ldy < N", fn);
     const size_t ysz = y_dtype == BI_F32 ? 4 : 2;
@@ -216,8 +232,8 @@ bi_status rmsnorm_impl(const char* fn, const void* x, int64_t ldx, const void* g
     if (rows < 0) return fail(BI_ERR_INVALID_ARG, "%s: negative rows", fn);
     if (hidden < 1 || hidden > (int64_t(1) << 20))
         return fail(BI_ERR_INVALID_ARG, "%s: hidden must be in [1, 2^20]", fn);
-    if (in_dtype != BI_BF16 && in_dtype != BI_F16)
-        return fail(BI_ERR_INVALID_ARG, "%s: in_dtype must be BI_BF16 or BI_F16", fn);
+    if (in_dtype != BI_BF16 && in_dtype != BI_F16 && in_dtype != BI_F32)
+        return fail(BI_ERR_INVALID_ARG, "%s: in_dtype must be BI_BF16, BI_F16 or BI_F32", fn);
     if (y_dtype != in_dtype && y_dtype != BI_F32)
         return fail(BI_ERR_INVALID_ARG, "%s: y_dtype must be in_dtype or BI_F32", fn);
     if (!std::isfinite(eps) || eps < 0.0f)
@@ -227,10 +243,17 @@ bi_status rmsnorm_impl(const char* fn, const void* x, int64_t ldx, const void* g
     if (ldx < hidden || ldy < hidden)
         return fail(BI_ERR_INVALID_ARG, "%s: ldx and ldy must be >= hidden", fn);
     const size_t ysz = y_dtype == BI_F32 ? 4 : 2;
-    if (!aligned(x, 2) || !aligned(gamma, 2) || !aligned(y, ysz))
+    const size_t xsz = in_dtype == BI_F32 ? 4 : 2;
+    if (!aligned(x, xsz) || !aligned(gamma, xsz) || !aligned(y, ysz))
         return fail(BI_ERR_INVALID_ARG, "%s: pointers not element-aligned", fn);
     cudaError_t why = cudaSuccess;
     if (!current_device_info(&why)) return cuda_fail(why, fn);
+    if (in_dtype == BI_F32) {
+        cudaError_t e = launch_rmsnorm_f32(x, ldx, gamma, y, ldy, rows, hidden, eps,
+                                           reinterpret_cast<cudaStream_t>(stream));
+        if (e != cudaSuccess) return cuda_fail(e, fn);
+        return BI_OK;
+    }
     cudaError_t e = launch_rmsnorm(x, ldx, gamma, y, ldy, y_dtype == BI_F32, rows, hidden, eps,
                                    in_dtype == BI_F16, reinterpret_cast<cudaStream_t>(stream));
     if (e != cudaSuccess) return cuda_fail(e, fn);

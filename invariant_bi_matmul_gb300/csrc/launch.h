@@ -79,6 +79,15 @@ cudaError_t launch_gemm(const DeviceInfo& dev, const void* x, int64_t ldx, const
                         int64_t N, int64_t K, bool split_ok, bool f16, cudaStream_t stream);
 int gemm_tile_n();
 
+// fp32 inputs (f32path.cu): CUDA-core matmul, one ascending fmaf chain per element, and
+// RMSNorm with the 16-bit kernel's tree.  y fp32.
+cudaError_t launch_gemm_f32(const void* x, int64_t ldx, const void* w, int64_t ldw, bool w_kn,
+                            void* y, int64_t ldy, int64_t M, int64_t N, int64_t K,
+                            cudaStream_t stream);
+cudaError_t launch_rmsnorm_f32(const void* x, int64_t ldx, const void* gamma, void* y,
+                               int64_t ldy, int64_t rows, int64_t hidden, float eps,
+                               cudaStream_t stream);
+
 // How a GEMM launch is scheduled: X rows staged per K-block, instruction tiles per CTA
 // tile, shared-memory ring depth, CTA tiles -- none of which changes what an element
 // computes -- and, only when split_ok (a call outside the batch-invariant limit), the

@@ -74,6 +74,9 @@ def _declare(L: ctypes.CDLL) -> None:
     L.oracle_add.argtypes = [_p, _p, _p, _i64]
     L.oracle_log_softmax_f32.argtypes = [_p, _i64, _p, _i64, _i64, _i64]
     L.oracle_f16_widen.argtypes = [_p, _p, _i64]
+    L.oracle_matmul_f32.argtypes = [_p, _i64, _p, _i64, ctypes.c_int, _p, _i64, _i64, _i64,
+                                    _i64]
+    L.oracle_rmsnorm_f32.argtypes = [_p, _i64, _p, _p, _i64, _i64, _i64, ctypes.c_float]
     L.oracle_matmul16.argtypes = [_p, _i64, _p, _i64, ctypes.c_int, _p, _i64, _i64, _i64, _i64,
                                   ctypes.c_int]
     L.oracle_rmsnorm16.argtypes = [_p, _i64, _p, _p, _i64, _i64, _i64, ctypes.c_float,
@@ -319,6 +322,28 @@ def rmsnorm16(x: np.ndarray, gamma: np.ndarray, eps: float, dtype: int) -> np.nd
     rows, H = x.shape
     y = np.empty((rows, H), dtype=np.float32)
     lib().oracle_rmsnorm16(_ptr(x), H, _ptr(gamma), _ptr(y), H, rows, H, float(eps), int(dtype))
+    return y
+
+
+def matmul_f32(x: np.ndarray, w: np.ndarray, w_layout: int) -> np.ndarray:
+    """matmul of fp32 x [M, K] and w (NK [N, K] or KN [K, N]) -> fp64 (exact products,
+    fp64 sum)."""
+    x = _as(x, np.float32)
+    w = _as(w, np.float32)
+    M, K = x.shape
+    N = w.shape[0] if w_layout == W_NK else w.shape[1]
+    y = np.empty((M, N), dtype=np.float64)
+    lib().oracle_matmul_f32(_ptr(x), K, _ptr(w), w.shape[1], w_layout, _ptr(y), N, M, N, K)
+    return y
+
+
+def rmsnorm_f32(x: np.ndarray, gamma: np.ndarray, eps: float) -> np.ndarray:
+    """RMSNorm of fp32 [rows, H] with fp32 gamma, the book's fp32 procedure."""
+    x = _as(x, np.float32)
+    gamma = _as(gamma, np.float32)
+    rows, H = x.shape
+    y = np.empty((rows, H), dtype=np.float32)
+    lib().oracle_rmsnorm_f32(_ptr(x), H, _ptr(gamma), _ptr(y), H, rows, H, float(eps))
     return y
 
 

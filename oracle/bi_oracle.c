@@ -481,3 +481,42 @@ ORACLE_API void oracle_mean_bf16(const uint16_t* x, int64_t ldx, int64_t rows, i
         out[r] = s / (double)n;
     }
 }
+
+/* ------------------------------------------------------------------------------ */
+/* fp32 inputs ("Fix/speculative shape invariance", ml-explore/mlx PR 4279, the     */
+/* tester's comment: f32 dense matmul).  Matmul: the exact sum of the exact          */
+/* products of the fp32 inputs, accumulated in fp64 (unrounded reference).           */
+/* RMSNorm: the fp32 procedure of oracle_rmsnorm (the book's order) on fp32 inputs. */
+/* ------------------------------------------------------------------------------ */
+ORACLE_API void oracle_matmul_f32(const float* x, int64_t ldx, const float* w, int64_t ldw,
+                                  int w_layout, double* y, int64_t ldy, int64_t M, int64_t N,
+                                  int64_t K) {
+    for (int64_t m = 0; m < M; ++m)
+        for (int64_t n = 0; n < N; ++n) {
+            double acc = 0.0;
+            for (int64_t k = 0; k < K; ++k) {
+                double xv = (double)x[m * ldx + k];
+                double wv = (double)(w_layout == 0 ? w[n * ldw + k] : w[k * ldw + n]);
+                acc += xv * wv;
+            }
+            y[m * ldy + n] = acc;
+        }
+}
+
+ORACLE_API void oracle_rmsnorm_f32(const float* x, int64_t ldx, const float* gamma, float* y,
+                                   int64_t ldy, int64_t rows, int64_t H, float eps) {
+    for (int64_t r = 0; r < rows; ++r) {
+        float ss = 0.0f;
+        for (int64_t i = 0; i < H; ++i) {
+            float v = x[r * ldx + i];
+            float sq = v * v;
+            ss = ss + sq;
+        }
+        float mean = ss / (float)H;
+        float inv = 1.0f / sqrtf(mean + eps);
+        for (int64_t i = 0; i < H; ++i) {
+            float t = x[r * ldx + i] * inv;
+            y[r * ldy + i] = t * gamma[i];
+        }
+    }
+}

@@ -74,3 +74,27 @@ def test_rmsnorm16_f16_closed_form_and_bf16_agreement():
     b = oracle.rmsnorm16(_bf16_exact(x), _bf16_exact(g), 1e-6, oracle.BF16)
     assert np.array_equal(a, b)
     assert np.array_equal(b, oracle.rmsnorm(_bf16_exact(x), _bf16_exact(g), 1e-6))
+
+
+def test_matmul_f32_exact_and_library_agreement():
+    """fp32 inputs: integers give exact results; a random case agrees with numpy's fp64
+    product of the same values (the oracle accumulates exact products in fp64)."""
+    rng = np.random.default_rng(6)
+    x = rng.integers(-1000, 1001, (4, 50)).astype(np.float32)
+    w = rng.integers(-1000, 1001, (6, 50)).astype(np.float32)
+    want = x.astype(np.float64) @ w.astype(np.float64).T
+    assert np.array_equal(oracle.matmul_f32(x, w, oracle.W_NK), want)
+    assert np.array_equal(oracle.matmul_f32(x, w.T.copy(), oracle.W_KN), want)
+    xr = rng.normal(size=(3, 700)).astype(np.float32)
+    wr = rng.normal(size=(5, 700)).astype(np.float32)
+    ref = xr.astype(np.float64) @ wr.astype(np.float64).T
+    assert np.allclose(oracle.matmul_f32(xr, wr, oracle.W_NK), ref, rtol=0, atol=1e-10)
+
+
+def test_rmsnorm_f32_matches_16bit_path_on_shared_values():
+    rng = np.random.default_rng(7)
+    x = rng.integers(-32, 33, (3, 48)) / 8.0
+    g = rng.integers(1, 9, 48) / 4.0
+    a = oracle.rmsnorm_f32(x.astype(np.float32), g.astype(np.float32), 1e-6)
+    b = oracle.rmsnorm16(_bf16_exact(x), _bf16_exact(g), 1e-6, oracle.BF16)
+    assert np.array_equal(a, b)
