@@ -246,3 +246,38 @@ def decoder_prompt(cfg: DecoderConfig, seq_id: int, seed: int, length: int) -> l
 def page_permutation(num_pages: int, seed: int) -> torch.Tensor:
     """A seeded permutation of physical page ids (int32)."""
     return torch.randperm(num_pages, generator=generator(seed)).to(torch.int32)
+
+
+# ------------------------------------------------------------------ quantized weights
+
+Q_MXFP4, Q_NVFP4, Q_MXFP8, Q_AFFINE4, Q_AFFINE8 = range(5)
+Q_NAMES = {"mxfp4": Q_MXFP4, "nvfp4": Q_NVFP4, "mxfp8": Q_MXFP8, "affine4": Q_AFFINE4,
+           "affine8": Q_AFFINE8}
+
+
+def quant_weights(fmt: int, N: int, K: int, gs: int, seed: int, row_pad_bytes: int = 16):
+    """Random codes and scales of a quantized W (no quantization arithmetic: the codes are
+    drawn directly).  Returns (wq uint8 [N, row bytes], scales, biases or None); rows of wq
+    are padded to a multiple of row_pad_bytes.  Block scales are E8M0 exponents near 2^-3
+    (mx formats) or E4M3 codes of moderate positive values (nvfp4); affine scales are
+    bf16 N(0, 0.005), biases bf16 N(0, 0.01).  FP8 codes avoid the NaN patterns."""
+    g = generator(seed)
+    four = fmt in (Q_MXFP4, Q_NVFP4, Q_AFFINE4)
+    nbytes = K // 2 if four else K
+    row = -(-nbytes // row_pad_bytes) * row_pad_bytes
+    wq = torch.zeros(N, row, dtype=torch.uint8)
+    codes = torch.randint(0, 256, (N, nbytes), generator=g, dtype=torch.int32)
+    if fmt == Q_MXFP8:
+        codes = torch.where((codes & 0x7F) == 0x7F, codes - 1, codes)  # no NaN codes
+    wq[:, :nbytes] = codes.to(torch.uint8)
+    groups = K // gs
+    if fmt in (Q_MXFP4, Q_MXFP8):
+        scales = torch.randint(120, 127, (N, groups), generator=g, dtype=torch.int32).to(torch.uint8)
+        biases = None
+    elif fmt == Q_NVFP4:
+        scales = torch.randint(0x28, 0x40, (N, groups), generator=g, dtype=torch.int32).to(torch.uint8)
+        biases = None
+    else:
+        scales = normal_bf16((N, groups), 0.0, 0.005, seed=seed * 7 + 1)
+        biases = normal_bf16((N, groups), 0.0, 0.01, seed=seed * 7 + 2)
+    return wq, scales, biases

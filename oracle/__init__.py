@@ -74,6 +74,10 @@ def _declare(L: ctypes.CDLL) -> None:
     L.oracle_add.argtypes = [_p, _p, _p, _i64]
     L.oracle_log_softmax_f32.argtypes = [_p, _i64, _p, _i64, _i64, _i64]
     L.oracle_f16_widen.argtypes = [_p, _p, _i64]
+    for name in ("oracle_decode_fp4", "oracle_decode_fp8", "oracle_decode_e8m0"):
+        getattr(L, name).argtypes = [_p, _p, _i64]
+    L.oracle_dequantize.argtypes = [_p, _i64, _p, _i64, _p, _i64, ctypes.c_int, _i64, _p, _i64,
+                                    _i64]
     L.oracle_matmul_f32.argtypes = [_p, _i64, _p, _i64, ctypes.c_int, _p, _i64, _i64, _i64,
                                     _i64]
     L.oracle_rmsnorm_f32.argtypes = [_p, _i64, _p, _p, _i64, _i64, _i64, ctypes.c_float]
@@ -345,6 +349,52 @@ def rmsnorm_f32(x: np.ndarray, gamma: np.ndarray, eps: float) -> np.ndarray:
     y = np.empty((rows, H), dtype=np.float32)
     lib().oracle_rmsnorm_f32(_ptr(x), H, _ptr(gamma), _ptr(y), H, rows, H, float(eps))
     return y
+
+
+# quantized weight formats (the encodings are documented in bi_oracle.c)
+Q_MXFP4, Q_NVFP4, Q_MXFP8, Q_AFFINE4, Q_AFFINE8 = range(5)
+
+
+def _decode(fn, codes):
+    codes = _as(codes, np.uint8)
+    out = np.empty(codes.shape, dtype=np.float32)
+    fn(_ptr(codes), _ptr(out), codes.size)
+    return out
+
+
+def decode_fp4(codes):
+    """FP4 E2M1 codes (low 4 bits of each byte) -> fp32 values."""
+    return _decode(lib().oracle_decode_fp4, codes)
+
+
+def decode_fp8(codes):
+    """FP8 E4M3 codes -> fp32 values (0x7F / 0xFF are NaN; no infinities)."""
+    return _decode(lib().oracle_decode_fp8, codes)
+
+
+def decode_e8m0(codes):
+    """E8M0 scale codes -> 2^(code-127) (255 is NaN)."""
+    return _decode(lib().oracle_decode_e8m0, codes)
+
+
+def dequantize(wq, scales, biases, fmt: int, gs: int, N: int, K: int) -> np.ndarray:
+    """Quantized W (NK: one row per output column) -> bf16 bits [N, K].  wq: uint8 codes
+    [N, K/2] (4-bit, low nibble first) or [N, K] (8-bit); scales: uint8 [N, K/gs] (block
+    formats) or bf16 bits [N, K/gs] (affine, with biases the same)."""
+    wq = _as(wq, np.uint8)
+    affine = fmt in (Q_AFFINE4, Q_AFFINE8)
+    scales = _as(scales, np.uint16 if affine else np.uint8)
+    b = _as(biases, np.uint16) if affine else np.zeros((1, 1), dtype=np.uint16)
+    out = np.empty((N, K), dtype=np.uint16)
+    lib().oracle_dequantize(_ptr(wq), wq.shape[1], _ptr(scales), scales.shape[1], _ptr(b),
+                            b.shape[1], int(fmt), int(gs), _ptr(out), N, K)
+    return out
+
+
+def qmatmul(x: np.ndarray, wq, scales, biases, fmt: int, gs: int, N: int) -> np.ndarray:
+    """bf16 x [M, K] times dequantized W^T -> unrounded fp32 [M, N] (the matmul above)."""
+    x = _as(x, np.uint16)
+    return matmul(x, dequantize(wq, scales, biases, fmt, gs, N, x.shape[1]), W_NK)
 
 
 def log_softmax(x: np.ndarray) -> np.ndarray:

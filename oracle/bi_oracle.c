@@ -520,3 +520,71 @@ ORACLE_API void oracle_rmsnorm_f32(const float* x, int64_t ldx, const float* gam
         }
     }
 }
+
+/* ------------------------------------------------------------------------------ */
+/* Quantized weights ("Fix/speculative shape invariance", ml-explore/mlx PR 4279,   */
+/* the tester's comment: affine group sizes 32/64/128, mxfp4, mxfp8, nvfp4; "Fix fp */
+/* quantized matmul corruption when the quantized dim is not a multiple of 32",     */
+/* Problem: nvfp4 groups of 16 allow K = 16 mod 32).  The pages name the formats;   */
+/* the element and scale encodings below follow their published definitions (OCP    */
+/* Microscaling formats: FP4 E2M1, FP8 E4M3, E8M0 scales; NVFP4: E2M1 elements with */
+/* an FP8 E4M3 scale per 16) and a plain affine code w = scale * q + bias.          */
+/* Layout (quantized along K, one row per output column n, "W layout NK"):          */
+/*   4-bit codes: byte k/2 of row n, element k in the low nibble when k is even.    */
+/*   8-bit codes: byte k of row n.                                                  */
+/*   block scales: one byte per block of gs elements, [N][K/gs].                    */
+/*   affine: bf16 scale and bias per group of gs, [N][K/gs] each; the dequantized   */
+/*   value is fmaf(scale, q, bias) in fp32 rounded to bf16 (nearest even).           */
+/* Every other format's dequantized value is exact in bf16.                         */
+/* ------------------------------------------------------------------------------ */
+enum { Q_MXFP4 = 0, Q_NVFP4 = 1, Q_MXFP8 = 2, Q_AFFINE4 = 3, Q_AFFINE8 = 4 };
+
+static float fp4_e2m1(unsigned c) {  /* sign bit 3, exponent bits 2-1 (bias 1), mantissa bit 0 */
+    const unsigned e = (c >> 1) & 3u, m = c & 1u;
+    const float mag = e == 0 ? 0.5f * (float)m : ldexpf(1.0f + 0.5f * (float)m, (int)e - 1);
+    return (c & 8u) ? -mag : mag;
+}
+
+static float fp8_e4m3(unsigned c) {  /* sign bit 7, exponent bits 6-3 (bias 7), mantissa 2-0 */
+    const unsigned e = (c >> 3) & 15u, m = c & 7u;
+    float mag;
+    if (e == 15 && m == 7) mag = NAN;  /* the only NaN pattern; no infinities */
+    else if (e == 0) mag = ldexpf((float)m, -9);
+    else mag = ldexpf((float)(8u + m), (int)e - 10);
+    return (c & 128u) ? -mag : mag;
+}
+
+static float scale_e8m0(unsigned c) { return c == 255 ? NAN : ldexpf(1.0f, (int)c - 127); }
+
+ORACLE_API void oracle_decode_fp4(const uint8_t* codes, float* out, int64_t n) {
+    for (int64_t i = 0; i < n; ++i) out[i] = fp4_e2m1(codes[i] & 15u);
+}
+ORACLE_API void oracle_decode_fp8(const uint8_t* codes, float* out, int64_t n) {
+    for (int64_t i = 0; i < n; ++i) out[i] = fp8_e4m3(codes[i]);
+}
+ORACLE_API void oracle_decode_e8m0(const uint8_t* codes, float* out, int64_t n) {
+    for (int64_t i = 0; i < n; ++i) out[i] = scale_e8m0(codes[i]);
+}
+
+/* Dequantized W as bf16 bits, [N][K] (row stride K). */
+ORACLE_API void oracle_dequantize(const uint8_t* wq, int64_t ldq, const void* scales,
+                                  int64_t lds, const uint16_t* biases, int64_t ldb, int format,
+                                  int64_t gs, uint16_t* out, int64_t N, int64_t K) {
+    for (int64_t n = 0; n < N; ++n)
+        for (int64_t k = 0; k < K; ++k) {
+            const int64_t g = k / gs;
+            unsigned code;
+            if (format == Q_MXFP8 || format == Q_AFFINE8) code = wq[n * ldq + k];
+            else code = (wq[n * ldq + k / 2] >> ((k & 1) ? 4 : 0)) & 15u;
+            float v;
+            if (format == Q_MXFP4) v = fp4_e2m1(code) * scale_e8m0(((const uint8_t*)scales)[n * lds + g]);
+            else if (format == Q_NVFP4) v = fp4_e2m1(code) * fp8_e4m3(((const uint8_t*)scales)[n * lds + g]);
+            else if (format == Q_MXFP8) v = fp8_e4m3(code) * scale_e8m0(((const uint8_t*)scales)[n * lds + g]);
+            else {
+                const float s = bf16_bits_to_f32(((const uint16_t*)scales)[n * lds + g]);
+                const float b = bf16_bits_to_f32(biases[n * ldb + g]);
+                v = fmaf(s, (float)code, b);
+            }
+            out[n * K + k] = f32_to_bf16_bits(v);
+        }
+}
