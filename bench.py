@@ -761,6 +761,28 @@ def run_sweep():
                           "graph_frac_tensor": round(fl / tg / 1e6 / float(
                               peaks.get("bf16_tflops", 1900.0)), 3)}), flush=True)
     del hsets, xh, wh
+    # quantized W (bi_qmatmul): rotating sets of packed codes larger than L2
+    for fmt, gs in (("mxfp4", 32), ("nvfp4", 16), ("mxfp8", 32), ("affine4", 64)):
+        q = inputs.Q_NAMES[fmt]
+        wq, sc, bq = inputs.quant_weights(q, N, K, gs, seed=5)
+        wq, sc = wq.to(dev), sc.to(dev)
+        bq = bq.to(dev) if bq is not None else None
+        wbytes = wq.numel() + sc.numel() * sc.element_size() + (
+            bq.numel() * bq.element_size() if bq is not None else 0)
+        qsets = [(wq, sc, bq)] + [(wq.clone(), sc.clone(), None if bq is None else bq.clone())
+                                  for _ in range(max(0, min(63, SET_BYTES // wbytes - 1)))]
+        for M in (8, 2048):
+            xm = x[:M].contiguous()
+            y = torch.empty(M, N, dtype=torch.bfloat16, device=dev)
+            tg = graph_us([lambda a=a, c=c, b=b: bi.qmatmul(xm, a, c, fmt, gs, K, biases=b, out=y)
+                           for a, c, b in qsets])
+            fl, by = 2 * M * N * K, wbytes + 2 * M * K + 2 * M * N
+            print(json.dumps({"sweep": "qmatmul", "format": fmt, "group": gs, "M": M, "K": K,
+                              "N": N, "graph_us": round(tg, 2),
+                              "graph_frac_hbm": round(by / tg / 1e3 / peaks["hbm_gbs"], 3),
+                              "graph_frac_tensor": round(fl / tg / 1e6 / float(
+                                  peaks.get("bf16_tflops", 1900.0)), 3)}), flush=True)
+        del qsets, wq, sc, bq
     # fp32 inputs (CUDA cores): W 64 MB, one set (larger than L2)
     xf, wf = x.float(), wnk.float()
     for M in (8, 2048):

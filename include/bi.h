@@ -168,6 +168,43 @@ bi_status bi_matmul_ex(const void* x, int64_t ldx, const void* w, int64_t ldw, i
                        int64_t K, bi_stream_t stream);
 
 /* ---------------------------------------------------------------------------------
+ * bi_qmatmul  [MLX-4279, the tester's comment: quantized matmul diverges most with the
+ * limit off (affine group sizes 32/64/128, mxfp4, mxfp8, nvfp4); QMM-3912, Problem and
+ * Fix: nvfp4's 16-element groups allow K = 16 mod 32, and every tail tile must be
+ * bounded (no read of the next row's codes, no store past N)]
+ *
+ *   Y[m, n] = sum_k X[m, k] * Wd(n, k),  Wd = W dequantized (below) and held as bf16,
+ *   fp32 accumulation with the instruction sequence and K order of bi_matmul (layout
+ *   NK), then bf16 RNE or fp32.  One configuration: the batch-invariant limit has no
+ *   effect, and row m's bits do not depend on M.
+ *
+ *   x        bf16 [M, K], row stride ldx (16-byte aligned, ldx % 8 == 0).
+ *   wq       packed codes, one row per output column n, row stride ldwq bytes (a multiple
+ *            of 16; 16-byte aligned):  4-bit formats: byte k/2 holds element k in its low
+ *            nibble when k is even, in its high nibble when odd;  8-bit formats: byte k.
+ *   scales   one per group of group_size consecutive k of a row, [N][K/group_size], row
+ *            stride lds:  BI_Q_MXFP4 / BI_Q_MXFP8: E8M0 bytes (2^(c-127), 255 = NaN);
+ *            BI_Q_NVFP4: FP8 E4M3 bytes;  affine: bf16.
+ *   biases   affine only: bf16 [N][K/group_size], row stride ldb (else ignored).
+ *   Elements: BI_Q_MXFP4, BI_Q_NVFP4: FP4 E2M1 (values 0, 0.5, 1, 1.5, 2, 3, 4, 6 and
+ *   negatives); BI_Q_MXFP8: FP8 E4M3 (0x7F/0xFF NaN, no infinities); affine 4/8-bit:
+ *   unsigned integers q.  Dequantized value: element * scale (exact in bf16) for the
+ *   block formats; for affine, fmaf(scale, q, bias) in fp32 rounded to bf16.
+ *   group_size: 32 (mxfp4, mxfp8), 16 (nvfp4), 32, 64 or 128 (affine); K a multiple of it.
+ * ------------------------------------------------------------------------------- */
+typedef enum {
+    BI_Q_MXFP4 = 0,
+    BI_Q_NVFP4 = 1,
+    BI_Q_MXFP8 = 2,
+    BI_Q_AFFINE4 = 3,
+    BI_Q_AFFINE8 = 4
+} bi_qformat;
+bi_status bi_qmatmul(const void* x, int64_t ldx, const void* wq, int64_t ldwq,
+                     const void* scales, int64_t lds, const void* biases, int64_t ldb,
+                     int qformat, int group_size, void* y, int64_t ldy, int y_dtype, int64_t M,
+                     int64_t N, int64_t K, bi_stream_t stream);
+
+/* ---------------------------------------------------------------------------------
  * bi_rmsnorm  [BOOK Case 4 (definition and the load-dependent-tree defect) and Case 6
  * "RMSNorm": data-parallel, one row per core, never split]
  *

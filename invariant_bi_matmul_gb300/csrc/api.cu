@@ -278,6 +278,58 @@ BI_EXPORT bi_status bi_matmul_ex(const void* x, int64_t ldx, const void* w, int6
                        K, stream);
 }
 
+// ================================================================ quantized matmul
+
+BI_EXPORT bi_status bi_qmatmul(const void* x, int64_t ldx, const void* wq, int64_t ldwq,
+                               const void* scales, int64_t lds, const void* biases, int64_t ldb,
+                               int qformat, int group_size, void* y, int64_t ldy, int y_dtype,
+                               int64_t M, int64_t N, int64_t K, bi_stream_t stream) {
+    const char* fn = "bi_qmatmul";
+    init_limit_from_env();
+    if (M < 0 || N < 0 || K < 0) return fail(BI_ERR_INVALID_ARG, "%s: negative M/N/K", fn);
+    if (M > kI32Max || N > kI32Max || K > kI32Max)
+        return fail(BI_ERR_UNSUPPORTED, "%s: M, N, K must be < 2^31", fn);
+    if (qformat < BI_Q_MXFP4 || qformat > BI_Q_AFFINE8)
+        return fail(BI_ERR_INVALID_ARG, "%s: unknown qformat", fn);
+    const bool affine = qformat == BI_Q_AFFINE4 || qformat == BI_Q_AFFINE8;
+    const int want_gs = qformat == BI_Q_NVFP4 ? 16 : 32;
+    if (affine ? (group_size != 32 && group_size != 64 && group_size != 128)
+               : group_size != want_gs)
+        return fail(BI_ERR_INVALID_ARG, "%s: group_size must be %s", fn,
+                    affine ? "32, 64 or 128" : (want_gs == 16 ? "16" : "32"));
+    if (K % group_size != 0)
+        return fail(BI_ERR_INVALID_ARG, "%s: K must be a multiple of group_size", fn);
+    if (y_dtype != BI_BF16 && y_dtype != BI_F32)
+        return fail(BI_ERR_INVALID_ARG, "%s: y_dtype must be BI_BF16 or BI_F32", fn);
+    if (M == 0 || N == 0) return BI_OK;
+    if (!y || ldy < N) return fail(BI_ERR_INVALID_ARG, "%s: null y or ldy < N", fn);
+    const size_t ysz = y_dtype == BI_F32 ? 4 : 2;
+    if (!aligned(y, ysz)) return fail(BI_ERR_INVALID_ARG, "%s: y not element-aligned", fn);
+    if (K > 0) {
+        const bool eight = qformat == BI_Q_MXFP8 || qformat == BI_Q_AFFINE8;
+        const int64_t row_bytes = eight ? K : K / 2;
+        if (!x || !wq || !scales || (affine && !biases))
+            return fail(BI_ERR_INVALID_ARG, "%s: null x, wq, scales or biases", fn);
+        if (ldx < K || ldwq < row_bytes || lds < K / group_size ||
+            (affine && ldb < K / group_size))
+            return fail(BI_ERR_INVALID_ARG, "%s: a row stride is too small", fn);
+        if (!aligned(x, 16) || ldx % 8 != 0 || !aligned(wq, 16) || ldwq % 16 != 0)
+            return fail(BI_ERR_UNSUPPORTED,
+                        "%s: x and wq must be 16-byte aligned, ldx a multiple of 8 and ldwq a "
+                        "multiple of 16 bytes (TMA rule)", fn);
+        if (affine && (!aligned(scales, 2) || !aligned(biases, 2)))
+            return fail(BI_ERR_INVALID_ARG, "%s: scales and biases not element-aligned", fn);
+    }
+    cudaError_t why = cudaSuccess;
+    const DeviceInfo* dev = current_device_info(&why);
+    if (!dev) return cuda_fail(why, fn);
+    cudaError_t e = launch_qgemm(*dev, x, ldx, wq, ldwq, scales, lds, biases, ldb, qformat,
+                                 group_size, y, ldy, y_dtype == BI_F32, M, N, K,
+                                 reinterpret_cast<cudaStream_t>(stream));
+    if (e != cudaSuccess) return cuda_fail(e, fn);
+    return BI_OK;
+}
+
 // ========================================================================= rmsnorm
 
 BI_EXPORT bi_status bi_rmsnorm(const void* x, int64_t ldx, const void* gamma, void* y,

@@ -63,6 +63,12 @@ constexpr int MAX_STAGES = 48;
 constexpr int MAX_SPLITS = 8;               // split-K cluster size (portable maximum)
 constexpr int THREADS = 192;
 constexpr int EPI_THREADS = 128;
+// Quantized W: four more warps (6..9) turn the packed codes of each stage into the bf16
+// operand tile; at most MAX_QSTAGES ring stages, one K-block each.
+constexpr int QTHREADS = THREADS + 128;
+constexpr int CONV_WARPS = 4;
+constexpr int MAX_QSTAGES = 16;
+constexpr int Q_RAW_KB_BYTES = 64 * BK;     // packed codes of 64 rows x one K-block (8-bit)
 constexpr int B_KB_BYTES = BN * BK * 2;     // one instruction tile's W block per K-block
 constexpr int A_MMA_BYTES = BM * BK * 2;    // 16 KiB: what one MMA reads from an X block
 constexpr int SMEM_BYTES = 220 * 1024;      // dynamic shared memory per CTA
@@ -75,7 +81,8 @@ constexpr int KN_SWIZZLE = KN_ATOM_N * 2;          // 64 or 128 bytes
 constexpr uint32_t KN_LAYOUT = KN_SWIZZLE == 128 ? 2u : 4u;
 
 static_assert(BN == 32 || BN == 64 || BN == 128, "instruction N must be 32, 64 or 128");
-static_assert((2 * MAX_STAGES + 7) * 8 + 16 <= CTRL_BYTES, "control block too small");
+static_assert((2 * MAX_STAGES + 7 + MAX_QSTAGES) * 8 + 16 <= CTRL_BYTES,
+              "control block too small");
 
 struct GemmArgs {
     void* y;
@@ -93,10 +100,43 @@ struct GemmArgs {
     int splits;
     int kb_per_split;
     int f16;           // X, W (and a 16-bit Y) are IEEE binary16 instead of bf16
+    // Quantized W (QUANT kernels only): format (0 mxfp4, 1 nvfp4, 2 mxfp8, 3 affine 4-bit,
+    // 4 affine 8-bit), group size, per-group scales (bytes, or bf16 for affine, row
+    // stride lds) and affine biases (bf16, row stride ldb); packed bytes per row per K-block.
+    int qfmt;
+    int gs;
+    const void* qscales;
+    int64_t lds;
+    const uint16_t* qbiases;
+    int64_t ldb;
+    int q_kb_bytes;
 };
 
-template <bool KN, bool F32OUT, int NSUB, bool SPLIT, int MSUB>
-__global__ void __launch_bounds__(THREADS, 1)
+// ----------------------------------------------------------- quantized-code decoding
+// From the format definitions (OCP Microscaling FP4 E2M1, FP8 E4M3 and E8M0 scales);
+// every decoded value is exact in fp32.
+__device__ __forceinline__ float dec_e2m1(uint32_t c) {
+    const uint32_t e = (c >> 1) & 3u, m = c & 1u;
+    const uint32_t mag = e == 0 ? (m ? 0x3F000000u : 0u) : (((e + 126u) << 23) | (m << 22));
+    return __uint_as_float(mag | ((c & 8u) << 28));
+}
+
+__device__ __forceinline__ float dec_e4m3(uint32_t c) {
+    const uint32_t e = (c >> 3) & 15u, m = c & 7u;
+    float mag;
+    if (e == 15u && m == 7u) mag = __uint_as_float(0x7fc00000u);
+    else if (e == 0u) mag = float(m) * 0.001953125f;  // m * 2^-9
+    else mag = __uint_as_float(((e + 120u) << 23) | (m << 20));
+    return (c & 0x80u) ? -mag : mag;
+}
+
+__device__ __forceinline__ float dec_e8m0(uint32_t c) {
+    return c == 255u ? __uint_as_float(0x7fc00000u)
+                     : (c == 0u ? __uint_as_float(0x00400000u) : __uint_as_float(c << 23));
+}
+
+template <bool KN, bool F32OUT, int NSUB, bool SPLIT, int MSUB, bool QUANT>
+__global__ void __launch_bounds__(QUANT ? QTHREADS : THREADS, 1)
 gemm_kernel(const __grid_constant__ CUtensorMap tmap_x, const __grid_constant__ CUtensorMap tmap_w,
             const GemmArgs args, unsigned int* err) {
     extern __shared__ uint8_t smem_raw[];
@@ -109,6 +149,8 @@ gemm_kernel(const __grid_constant__ CUtensorMap tmap_x, const __grid_constant__ 
     const int b_bytes = nsub * B_KB_BYTES;        // one W block (one K-block, every sub-tile)
     uint8_t* sA = smem;                           // S*kbs X blocks
     uint8_t* sB = smem + S * kbs * a_bytes;       // S*kbs W blocks
+    uint8_t* sR = sB + S * kbs * b_bytes;         // QUANT: S packed-code blocks
+    const int r_bytes = nsub * Q_RAW_KB_BYTES;
     uint64_t* full = reinterpret_cast<uint64_t*>(smem + RING_BYTES);
     uint64_t* empty = full + MAX_STAGES;
     uint64_t* tfull = empty + MAX_STAGES;
@@ -116,7 +158,8 @@ gemm_kernel(const __grid_constant__ CUtensorMap tmap_x, const __grid_constant__ 
     uint64_t* drain = tempty + 2;
     uint64_t* red_full = drain + 1;  // split-K, rank 0: the other ranks' partials are in
     uint64_t* red_free = drain + 2;  // split-K, rank > 0: rank 0 has read this rank's slot
-    uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(drain + 3);
+    uint64_t* conv = drain + 3;      // QUANT: stage s's bf16 W tile is written
+    uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(conv + MAX_QSTAGES);
     volatile int* abort_flag = reinterpret_cast<volatile int*>(tmem_slot + 1);
 
     const int warp = threadIdx.x >> 5;
@@ -148,6 +191,7 @@ gemm_kernel(const __grid_constant__ CUtensorMap tmap_x, const __grid_constant__ 
         for (int s = 0; s < S; ++s) {
             mbar_init(&full[s], 1);
             mbar_init(&empty[s], 1);
+            if (QUANT) mbar_init(&conv[s], CONV_WARPS);
         }
         for (int a = 0; a < 2; ++a) {
             mbar_init(&tfull[a], 1);
@@ -200,7 +244,14 @@ gemm_kernel(const __grid_constant__ CUtensorMap tmap_x, const __grid_constant__ 
         auto issue_w = [&](uint32_t st, int n0, int kb, int nk) {
             const uint32_t bar = full_s + st * 8u;
             const uint32_t b_dst = sB_s + st * stage_b;
-            if (KN) {
+            if (QUANT) {
+                // the packed codes of the K-block (one stage = one K-block), rows n0..
+                const uint32_t r_dst = smem_addr(sR) + st * uint32_t(r_bytes);
+                if (w_once)
+                    tma_load_2d_s_hint(r_dst, &tmap_w, bar, kb * args.q_kb_bytes, n0, w_policy);
+                else
+                    tma_load_2d_s(r_dst, &tmap_w, bar, kb * args.q_kb_bytes, n0);
+            } else if (KN) {
                 // per swizzle atom (KN_ATOM_N columns) one box of 64*kbs k-rows
                 for (int c = 0; c < tile_n; c += KN_ATOM_N) {
                     const uint32_t dst = b_dst + uint32_t(c / KN_ATOM_N) * uint32_t(kbs * KN_ATOM_BYTES);
@@ -240,6 +291,7 @@ gemm_kernel(const __grid_constant__ CUtensorMap tmap_x, const __grid_constant__ 
         auto stage_tx = [&](int nk) {
             const int x_blocks = blocked ? kbs : nk;
             const int w_blocks = (blocked || KN) ? kbs : nk;
+            if (QUANT) return uint32_t(x_blocks * a_bytes + nsub * 64 * args.q_kb_bytes);
             return uint32_t(x_blocks * a_bytes + w_blocks * b_bytes);
         };
 
@@ -328,7 +380,8 @@ gemm_kernel(const __grid_constant__ CUtensorMap tmap_x, const __grid_constant__ 
             tc_fence_after_sync();
             const uint32_t d_tmem = tmem_base + uint32_t(acc * ACC_COLS);
             for (int kb = kb0; kb < kb1; kb += kbs) {
-                if (!mbar_wait_warp(&full[stage], phase, abort_flag)) {
+                if (!mbar_wait_warp(&full[stage], phase, abort_flag) ||
+                    (QUANT && !mbar_wait_warp(&conv[stage], phase, abort_flag))) {
                     ok = false;
                     break;
                 }
@@ -375,7 +428,7 @@ gemm_kernel(const __grid_constant__ CUtensorMap tmap_x, const __grid_constant__ 
         if (elect_one()) tc_commit(drain);
         __syncwarp();
         mbar_wait(drain, 0, nullptr, 100000000ull);
-    } else {
+    } else if (warp < 6) {
         // ------------------------------------------------------------------ epilogue
         pdl_wait();  // Y may still be read by the previous grid
         const int quad = warp & 3;  // TMEM lanes 32*quad .. 32*quad+31
@@ -506,6 +559,119 @@ gemm_kernel(const __grid_constant__ CUtensorMap tmap_x, const __grid_constant__ 
                 }
             }
         }
+    } else if (QUANT) {
+        // --------------------------------------------------------------- converters
+        // The four converter warps turn each stage's packed codes into the bf16 W tile
+        // the MMA reads (K-major, 128-byte swizzle: the layout a TMA copy of bf16 W would
+        // give), once the stage's copies have landed; all four take every stage, in order
+        // (so each waits on a stage's barrier one phase at a time), thread ct of 128 on
+        // the 8-element chunks ct, ct+128, ...  The group scales of the next stage are
+        // read from global memory while the current stage converts.  Every dequantized
+        // value except the affine ones is exact in bf16; affine is fmaf(scale, q, bias)
+        // rounded to bf16.  Rows past N and K-blocks past K become zeros.
+        constexpr int NCH = NSUB * 64 * 8 / 128;  // chunks per converter thread
+        const int ct = (warp - 6) * 32 + lane;
+        const int fmt = args.qfmt;
+        const bool eight = fmt == 2 || fmt == 4;
+        const bool affine = fmt >= 3;
+        const uint8_t* qs8 = static_cast<const uint8_t*>(args.qscales);
+        const uint16_t* qs16 = static_cast<const uint16_t*>(args.qscales);
+        const int nkb_t = kb1 - kb0;
+        const int tiles_mine = first_tile < num_tiles
+                                   ? (num_tiles - 1 - first_tile) / tile_step + 1 : 0;
+        const int iters = tiles_mine * nkb_t;
+        // scale (and bias) of every chunk of iteration j, decoded to fp32
+        auto fetch = [&](int j, float (&sc)[NCH], float (&bs)[NCH]) {
+            const int t = first_tile + (j / nkb_t) * tile_step;
+            const int kb = kb0 + j % nkb_t;
+            const int n0 = (t % n_tiles) * tile_n;
+#pragma unroll
+            for (int q = 0; q < NCH; ++q) {
+                const int c = ct + q * 128;
+                const int n = n0 + (c >> 3), k0 = kb * BK + 8 * (c & 7);
+                sc[q] = 0.f;
+                bs[q] = 0.f;
+                if (n < N && k0 < K) {
+                    const int64_t grp = int64_t(n) * args.lds + k0 / args.gs;
+                    if (!affine) {
+                        sc[q] = fmt == 1 ? dec_e4m3(qs8[grp]) : dec_e8m0(qs8[grp]);
+                    } else {
+                        sc[q] = widen16(qs16[grp], false);
+                        bs[q] = widen16(args.qbiases[int64_t(n) * args.ldb + k0 / args.gs], false);
+                    }
+                }
+            }
+        };
+        float sc[NCH], bs[NCH], sc_n[NCH], bs_n[NCH];
+        if (iters > 0) fetch(0, sc, bs);
+        uint32_t stage = 0, phase = 0;
+        bool ok = true;
+        for (int j = 0; j < iters; ++j) {
+            if (j + 1 < iters) fetch(j + 1, sc_n, bs_n);
+            const int t = first_tile + (j / nkb_t) * tile_step;
+            const int kb = kb0 + j % nkb_t;
+            const int n0 = (t % n_tiles) * tile_n;
+            if (!mbar_wait_warp(&full[stage], phase, abort_flag)) {
+                ok = false;
+                break;
+            }
+            const uint8_t* raw = sR + stage * r_bytes;
+            uint8_t* wt = sB + stage * b_bytes;
+#pragma unroll
+            for (int q = 0; q < NCH; ++q) {
+                const int c = ct + q * 128;
+                const int r = c >> 3, jj = c & 7;
+                const int n = n0 + r, k0 = kb * BK + 8 * jj;
+                float v[8];
+                if (n < N && k0 < K) {  // K % 16 == 0: all 8 elements are in range
+                    uint32_t code[8];
+                    const uint8_t* rp = raw + r * args.q_kb_bytes;
+                    if (eight) {
+                        const uint2 w = *reinterpret_cast<const uint2*>(rp + 8 * jj);
+#pragma unroll
+                        for (int e = 0; e < 4; ++e) {
+                            code[e] = (w.x >> (8 * e)) & 255u;
+                            code[e + 4] = (w.y >> (8 * e)) & 255u;
+                        }
+                    } else {
+                        const uint32_t w = *reinterpret_cast<const uint32_t*>(rp + 4 * jj);
+#pragma unroll
+                        for (int e = 0; e < 8; ++e) code[e] = (w >> (4 * e)) & 15u;
+                    }
+                    if (!affine) {
+#pragma unroll
+                        for (int e = 0; e < 8; ++e)
+                            v[e] = (fmt == 2 ? dec_e4m3(code[e]) : dec_e2m1(code[e])) * sc[q];
+                    } else {
+#pragma unroll
+                        for (int e = 0; e < 8; ++e) v[e] = fmaf(sc[q], float(code[e]), bs[q]);
+                    }
+                } else {
+#pragma unroll
+                    for (int e = 0; e < 8; ++e) v[e] = 0.f;
+                }
+                uint4 pk;
+                pk.x = pack_bf16x2(v[0], v[1]);
+                pk.y = pack_bf16x2(v[2], v[3]);
+                pk.z = pack_bf16x2(v[4], v[5]);
+                pk.w = pack_bf16x2(v[6], v[7]);
+                *reinterpret_cast<uint4*>(wt + (r >> 6) * B_KB_BYTES + ((r & 63) >> 3) * 1024 +
+                                          (r & 7) * 128 + ((jj ^ (r & 7)) << 4)) = pk;
+            }
+            fence_proxy_async_smem();  // generic writes, read by the MMA (async proxy)
+            __syncwarp();
+            if (lane == 0) mbar_arrive(&conv[stage]);
+#pragma unroll
+            for (int q = 0; q < NCH; ++q) {
+                sc[q] = sc_n[q];
+                bs[q] = bs_n[q];
+            }
+            if (++stage == uint32_t(S)) {
+                stage = 0;
+                phase ^= 1u;
+            }
+        }
+        if (!ok && lane == 0 && !*abort_flag) fail();
     }
 
     tc_fence_before_sync();
@@ -522,7 +688,7 @@ gemm_kernel(const __grid_constant__ CUtensorMap tmap_x, const __grid_constant__ 
 template <bool KN, bool F32OUT, int NSUB, int MSUB = 1>
 cudaError_t launch_t(const DeviceInfo& dev, const CUtensorMap& mx, const CUtensorMap& mw,
                      const GemmArgs& a, int grid, cudaStream_t s) {
-    auto kern = gemm_kernel<KN, F32OUT, NSUB, false, MSUB>;
+    auto kern = gemm_kernel<KN, F32OUT, NSUB, false, MSUB, false>;
     static bool attr_done[64] = {};
     if (dev.device >= 0 && dev.device < 64 && !attr_done[dev.device]) {
         cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize,
@@ -539,7 +705,7 @@ cudaError_t launch_t(const DeviceInfo& dev, const CUtensorMap& mx, const CUtenso
 template <bool KN, bool F32OUT>
 cudaError_t launch_split(const DeviceInfo& dev, const CUtensorMap& mx, const CUtensorMap& mw,
                          const GemmArgs& a, int64_t tiles, cudaStream_t s) {
-    auto kern = gemm_kernel<KN, F32OUT, 1, true, 1>;
+    auto kern = gemm_kernel<KN, F32OUT, 1, true, 1, false>;
     static bool attr_done[64] = {};
     static int fit[64][MAX_SPLITS + 1] = {};  // co-resident clusters per device and size
     if (dev.device < 0 || dev.device >= 64 || a.splits < 2 || a.splits > MAX_SPLITS)
@@ -572,6 +738,20 @@ cudaError_t launch_split(const DeviceInfo& dev, const CUtensorMap& mx, const CUt
     const int clusters = int(tiles < n_fit ? tiles : n_fit);
     return launch_pdl_cluster(kern, dim3(unsigned(clusters * a.splits)), dim3(THREADS),
                               SMEM_BYTES, s, unsigned(a.splits), mx, mw, a, dev.err_word);
+}
+
+template <bool F32OUT, int NSUB>
+cudaError_t launch_q(const DeviceInfo& dev, const CUtensorMap& mx, const CUtensorMap& mw,
+                     const GemmArgs& a, int grid, cudaStream_t s) {
+    auto kern = gemm_kernel<false, F32OUT, NSUB, false, 1, true>;
+    static bool attr_done[64] = {};
+    if (dev.device >= 0 && dev.device < 64 && !attr_done[dev.device]) {
+        cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                             SMEM_BYTES);
+        if (e != cudaSuccess) return e;
+        attr_done[dev.device] = true;
+    }
+    return launch_pdl(kern, dim3(grid), dim3(QTHREADS), SMEM_BYTES, s, mx, mw, a, dev.err_word);
 }
 
 template <bool KN, bool F32OUT>
@@ -721,6 +901,71 @@ cudaError_t launch_gemm(const DeviceInfo& dev, const void* x, int64_t ldx, const
                      : launch_nsub<true, false>(dev, mx, mw, a, grid, stream);
     return y_f32 ? launch_nsub<false, true>(dev, mx, mw, a, grid, stream)
                  : launch_nsub<false, false>(dev, mx, mw, a, grid, stream);
+}
+
+cudaError_t launch_qgemm(const DeviceInfo& dev, const void* x, int64_t ldx, const void* wq,
+                         int64_t ldq, const void* scales, int64_t lds, const void* biases,
+                         int64_t ldb, int fmt, int gs, void* y, int64_t ldy, bool y_f32,
+                         int64_t M, int64_t N, int64_t K, cudaStream_t stream) {
+    if (M == 0 || N == 0) return cudaSuccess;
+    if (K == 0) {
+        const size_t es = y_f32 ? 4 : 2;
+        return cudaMemset2DAsync(y, size_t(ldy) * es, 0, size_t(N) * es, size_t(M), stream);
+    }
+    // the invariant schedule with one K-block per stage and 128-row CTA tiles
+    const int64_t m_tiles = (M + BM - 1) / BM;
+    const int a_rows = m_tiles == 1 ? int((M + 7) / 8 * 8) : BM;
+    int nsub = 1;
+    for (int ns = MAX_NSUB; ns >= 2; ns >>= 1) {
+        if (m_tiles * ((N + int64_t(ns) * BN - 1) / (int64_t(ns) * BN)) >= dev.num_sms) {
+            nsub = ns;
+            break;
+        }
+    }
+    const int64_t blk = int64_t(a_rows) * BK * 2 + int64_t(nsub) * (B_KB_BYTES + Q_RAW_KB_BYTES);
+    int stages = int(RING_BYTES / blk);
+    if (stages > MAX_QSTAGES) stages = MAX_QSTAGES;
+    if (stages < 2 || int64_t(stages - 1) * a_rows * BK * 2 + A_MMA_BYTES > int64_t(stages) * blk)
+        return cudaErrorNotSupported;
+    const bool eight = fmt == 2 || fmt == 4;
+    const int q_kb_bytes = eight ? BK : BK / 2;
+    CUtensorMap mx, mw;
+    if (!tmap_2d_bf16(&mx, x, uint64_t(K), uint64_t(M), uint64_t(ldx), BK, uint32_t(a_rows), 128) ||
+        !tmap_2d_u8(&mw, wq, uint64_t(eight ? K : K / 2), uint64_t(N), uint64_t(ldq),
+                    uint32_t(q_kb_bytes), uint32_t(nsub * BN)))
+        return cudaErrorNotSupported;
+    GemmArgs a{};
+    a.y = y;
+    a.ldy = ldy;
+    a.M = int(M);
+    a.N = int(N);
+    a.K = int(K);
+    a.a_rows = a_rows;
+    a.nsub = nsub;
+    a.kbs = 1;
+    a.blocked = 0;
+    a.stages = stages;
+    a.w_stream_once = m_tiles == 1 ? 1 : 0;
+    a.splits = 1;
+    a.kb_per_split = int((K + BK - 1) / BK);
+    a.f16 = 0;
+    a.qfmt = fmt;
+    a.gs = gs;
+    a.qscales = scales;
+    a.lds = lds;
+    a.qbiases = static_cast<const uint16_t*>(biases);
+    a.ldb = ldb;
+    a.q_kb_bytes = q_kb_bytes;
+    const int64_t tiles = m_tiles * ((N + int64_t(nsub) * BN - 1) / (int64_t(nsub) * BN));
+    const int grid = int(tiles < dev.num_sms ? tiles : dev.num_sms);
+    switch (nsub) {
+        case 1: return y_f32 ? launch_q<true, 1>(dev, mx, mw, a, grid, stream)
+                             : launch_q<false, 1>(dev, mx, mw, a, grid, stream);
+        case 2: return y_f32 ? launch_q<true, (MAX_NSUB >= 2 ? 2 : 1)>(dev, mx, mw, a, grid, stream)
+                             : launch_q<false, (MAX_NSUB >= 2 ? 2 : 1)>(dev, mx, mw, a, grid, stream);
+        default: return y_f32 ? launch_q<true, MAX_NSUB>(dev, mx, mw, a, grid, stream)
+                              : launch_q<false, MAX_NSUB>(dev, mx, mw, a, grid, stream);
+    }
 }
 
 }  // namespace bi

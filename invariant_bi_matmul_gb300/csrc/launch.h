@@ -79,6 +79,14 @@ cudaError_t launch_gemm(const DeviceInfo& dev, const void* x, int64_t ldx, const
                         int64_t N, int64_t K, bool split_ok, bool f16, cudaStream_t stream);
 int gemm_tile_n();
 
+// Quantized W (gemm.cu): bf16 X times W decoded from packed codes (format 0 mxfp4,
+// 1 nvfp4, 2 mxfp8, 3 affine 4-bit, 4 affine 8-bit) with the invariant GEMM's
+// instruction sequence.  Returns cudaErrorNotSupported when a descriptor cannot be made.
+cudaError_t launch_qgemm(const DeviceInfo& dev, const void* x, int64_t ldx, const void* wq,
+                         int64_t ldq, const void* scales, int64_t lds, const void* biases,
+                         int64_t ldb, int fmt, int gs, void* y, int64_t ldy, bool y_f32,
+                         int64_t M, int64_t N, int64_t K, cudaStream_t stream);
+
 // fp32 inputs (f32path.cu): CUDA-core matmul, one ascending fmaf chain per element, and
 // RMSNorm with the 16-bit kernel's tree.  y fp32.
 cudaError_t launch_gemm_f32(const void* x, int64_t ldx, const void* w, int64_t ldw, bool w_kn,

@@ -22,4 +22,9 @@ bool tmap_kblocked_bf16(CUtensorMap* out, const void* ptr, uint64_t inner, uint6
                         uint64_t stride, uint32_t box_inner, uint32_t box_outer,
                         uint32_t box_blocks, int swizzle_bytes, bool f16 = false);
 
+// 2D byte tensor [outer][inner_bytes] (row stride stride_bytes, a multiple of 16), boxes of
+// box_inner bytes x box_outer rows, no swizzle; bytes outside the tensor read as 0.
+bool tmap_2d_u8(CUtensorMap* out, const void* ptr, uint64_t inner_bytes, uint64_t outer,
+                uint64_t stride_bytes, uint32_t box_inner, uint32_t box_outer);
+
 }  // namespace bi

@@ -1,0 +1,116 @@
+"""bi_qmatmul on the GPU: quantized W (mxfp4, nvfp4, mxfp8, affine 4/8-bit at group
+sizes 32/64/128) against the oracle, including nvfp4 with K = 16 mod 32 ("Fix fp
+quantized matmul corruption when the quantized dim is not a multiple of 32", Problem and
+Fix) and ragged N; bit-identical to bi_matmul on the dequantized weights; rows bitwise
+across M ("Fix/speculative shape invariance", the tester's comment: quantized matmul is
+where the paths diverged most)."""
+import numpy as np
+import pytest
+import torch
+
+import oracle
+from invariant_bi_matmul_gb300 import inputs
+from tolerance import bits_equal, check_bf16, check_f32
+
+pytestmark = pytest.mark.gpu
+
+bi = pytest.importorskip("invariant_bi_matmul_gb300")
+
+FORMATS = [("mxfp4", 32), ("nvfp4", 16), ("mxfp8", 32), ("affine4", 32), ("affine4", 64),
+           ("affine4", 128), ("affine8", 32), ("affine8", 128)]
+
+
+@pytest.fixture(scope="module")
+def dev():
+    if not torch.cuda.is_available():
+        pytest.skip("no CUDA device")
+    return torch.device("cuda:0")
+
+
+def _weights(fmt, N, K, gs, seed):
+    q = inputs.Q_NAMES[fmt]
+    wq, sc, b = inputs.quant_weights(q, N, K, gs, seed)
+    affine = b is not None
+    sc_np = inputs.bf16_bits(sc) if affine else sc.numpy()
+    b_np = inputs.bf16_bits(b) if affine else None
+    wd = oracle.dequantize(wq.numpy(), sc_np, b_np, q, gs, N, K)  # bf16 bits [N, K]
+    return wq, sc, b, wd
+
+
+def _run(dev, x, wq, sc, b, fmt, gs, K, out_dtype=None):
+    return bi.qmatmul(x.to(dev), wq.to(dev), sc.to(dev), fmt, gs, K,
+                      biases=None if b is None else b.to(dev), out_dtype=out_dtype)
+
+
+@pytest.mark.parametrize("fmt,gs", FORMATS)
+@pytest.mark.parametrize("M,N,K", [(8, 1024, 4096), (3, 200, 1040), (130, 96, 256)])
+def test_qmatmul_matches_oracle(dev, fmt, gs, M, N, K):
+    if K % gs:
+        pytest.skip("K must be a multiple of the group size")
+    x = inputs.normal_bf16((M, K), seed=M + K)
+    wq, sc, b, wd = _weights(fmt, N, K, gs, seed=N + gs)
+    ref = oracle.matmul(inputs.bf16_bits(x), wd, oracle.W_NK)
+    wv = (wd.astype(np.uint32) << 16).view(np.float32).astype(np.float64)
+    scale = np.abs(x.float().numpy().astype(np.float64)) @ np.abs(wv).T
+    y = _run(dev, x, wq, sc, b, fmt, gs, K)
+    check_bf16(y, ref, f"qmatmul {fmt} gs{gs} {M}x{N}x{K}")
+    y32 = _run(dev, x, wq, sc, b, fmt, gs, K, out_dtype=torch.float32)
+    check_f32(y32, ref, scale, f"qmatmul fp32 {fmt} gs{gs} {M}x{N}x{K}")
+    # the same instruction sequence as the dense GEMM on the dequantized weights
+    wdt = torch.from_numpy(wd.view(np.int16)).view(torch.bfloat16).to(dev)
+    assert bits_equal(y32, bi.matmul(x.to(dev), wdt, "nk", out_dtype=torch.float32))
+
+
+@pytest.mark.parametrize("fmt,gs", [("mxfp4", 32), ("nvfp4", 16), ("affine4", 64)])
+def test_qmatmul_rows_invariant_across_M(dev, fmt, gs):
+    N, K = 4096, 4096
+    x = inputs.normal_bf16((300, K), seed=77)
+    wq, sc, b, _ = _weights(fmt, N, K, gs, seed=78)
+    xd = x.to(dev)
+    args = (wq.to(dev), sc.to(dev), fmt, gs, K)
+    kw = {} if b is None else {"biases": b.to(dev)}
+    full = bi.qmatmul(xd, *args, **kw)
+    for M in (1, 2, 4, 8, 9, 64, 128, 129, 299):
+        assert bits_equal(bi.qmatmul(xd[:M].contiguous(), *args, **kw), full[:M]), M
+    old = bi.get_batch_invariant_limit()
+    bi.set_batch_invariant_limit(0)  # one configuration: the limit changes nothing
+    try:
+        assert bits_equal(bi.qmatmul(xd[:8].contiguous(), *args, **kw), full[:8])
+    finally:
+        bi.set_batch_invariant_limit(old)
+
+
+@pytest.mark.parametrize("fmt,gs", [("mxfp4", 32), ("affine8", 64)])
+@pytest.mark.parametrize("M,N", [(1024, 4864), (1280, 4096)])
+def test_qmatmul_wide_tiles_sampled(dev, fmt, gs, M, N):
+    """Four 64-wide instruction tiles per CTA (three ring stages), one and two tiles per
+    CTA: sampled rows against the oracle, and bit-identical to the dense GEMM."""
+    K = 256
+    x = inputs.normal_bf16((M, K), seed=M)
+    wq, sc, b, wd = _weights(fmt, N, K, gs, seed=N)
+    y = _run(dev, x, wq, sc, b, fmt, gs, K, out_dtype=torch.float32)
+    assert bi.device_status() == bi.BI_OK
+    rows = [0, 127, 128, M // 2, M - 1]
+    ref = oracle.matmul(inputs.bf16_bits(x[rows]), wd, oracle.W_NK)
+    wv = (wd.astype(np.uint32) << 16).view(np.float32).astype(np.float64)
+    scale = np.abs(x[rows].float().numpy().astype(np.float64)) @ np.abs(wv).T
+    check_f32(y.cpu()[rows], ref, scale, f"wide qmatmul {fmt} {M}x{N}")
+    wdt = torch.from_numpy(wd.view(np.int16)).view(torch.bfloat16).to(dev)
+    assert bits_equal(y, bi.matmul(x.to(dev), wdt, "nk", out_dtype=torch.float32))
+
+
+def test_qmatmul_repeat_and_guard_bands(dev):
+    """Run-to-run identical, and nothing written outside y (the out-of-bounds store race of
+    the tail tile is run-to-run nondeterminism)."""
+    M, N, K = 5, 200, 1040
+    x = inputs.normal_bf16((M, K), seed=90)
+    wq, sc, _, _ = _weights("nvfp4", N, K, 16, seed=91)
+    buf = torch.full((M + 2, N + 8), 7.0, dtype=torch.bfloat16, device=dev)
+    out = buf[1:M + 1, :N]
+    seen = set()
+    for _ in range(30):
+        bi.qmatmul(x.to(dev), wq.to(dev), sc.to(dev), "nvfp4", 16, K, out=out)
+        seen.add(bytes(out.contiguous().view(torch.int16).cpu().numpy()))
+    assert len(seen) == 1
+    assert torch.all(buf[0] == 7.0) and torch.all(buf[M + 1] == 7.0)
+    assert torch.all(buf[1:M + 1, N:] == 7.0)
