@@ -41,6 +41,8 @@
 // Every mbarrier wait is bounded: a wait that runs out latches the device error word,
 // raises a CTA-wide abort flag, drains outstanding copies and MMAs (bounded), frees
 // tensor memory and returns.
+#include <type_traits>
+
 #include "common.cuh"
 #include "launch.h"
 #include "tmap.h"
@@ -113,14 +115,9 @@ struct GemmArgs {
 };
 
 // ----------------------------------------------------------- quantized-code decoding
-// From the format definitions (OCP Microscaling FP4 E2M1, FP8 E4M3 and E8M0 scales);
-// every decoded value is exact in fp32.
-__device__ __forceinline__ float dec_e2m1(uint32_t c) {
-    const uint32_t e = (c >> 1) & 3u, m = c & 1u;
-    const uint32_t mag = e == 0 ? (m ? 0x3F000000u : 0u) : (((e + 126u) << 23) | (m << 22));
-    return __uint_as_float(mag | ((c & 8u) << 28));
-}
-
+// From the format definitions (OCP Microscaling FP8 E4M3 and E8M0 scale codes; the FP4
+// E2M1 and FP8 E4M3 elements go through the hardware's exact two-at-a-time conversions
+// below); every decoded value is exact in fp32.
 __device__ __forceinline__ float dec_e4m3(uint32_t c) {
     const uint32_t e = (c >> 3) & 15u, m = c & 7u;
     float mag;
@@ -128,6 +125,26 @@ __device__ __forceinline__ float dec_e4m3(uint32_t c) {
     else if (e == 0u) mag = float(m) * 0.001953125f;  // m * 2^-9
     else mag = __uint_as_float(((e + 120u) << 23) | (m << 20));
     return (c & 0x80u) ? -mag : mag;
+}
+
+// Two codes to two halves, exactly (every FP4 E2M1 and FP8 E4M3 value is a binary16
+// value): the low code (low nibble / low byte) to the low half.
+__device__ __forceinline__ uint32_t cvt_e2m1x2(uint32_t byte) {
+    uint32_t d;
+    asm("{\n\t.reg .b8 t;\n\tcvt.u8.u32 t, %1;\n\tcvt.rn.f16x2.e2m1x2 %0, t;\n\t}"
+        : "=r"(d) : "r"(byte));
+    return d;
+}
+
+__device__ __forceinline__ uint32_t cvt_e4m3x2(uint32_t two) {
+    uint32_t d;
+    asm("{\n\t.reg .b16 t;\n\tcvt.u16.u32 t, %1;\n\tcvt.rn.f16x2.e4m3x2 %0, t;\n\t}"
+        : "=r"(d) : "r"(two));
+    return d;
+}
+
+__device__ __forceinline__ float2 h2_to_f2(uint32_t h2) {
+    return __half22float2(*reinterpret_cast<const __half2*>(&h2));
 }
 
 __device__ __forceinline__ float dec_e8m0(uint32_t c) {
@@ -572,7 +589,6 @@ gemm_kernel(const __grid_constant__ CUtensorMap tmap_x, const __grid_constant__ 
         constexpr int NCH = NSUB * 64 * 8 / 128;  // chunks per converter thread
         const int ct = (warp - 6) * 32 + lane;
         const int fmt = args.qfmt;
-        const bool eight = fmt == 2 || fmt == 4;
         const bool affine = fmt >= 3;
         const uint8_t* qs8 = static_cast<const uint8_t*>(args.qscales);
         const uint16_t* qs16 = static_cast<const uint16_t*>(args.qscales);
@@ -617,46 +633,70 @@ gemm_kernel(const __grid_constant__ CUtensorMap tmap_x, const __grid_constant__ 
             }
             const uint8_t* raw = sR + stage * r_bytes;
             uint8_t* wt = sB + stage * b_bytes;
+            // one specialised loop per format (the format is uniform over the launch)
+            auto convert = [&](auto tag) {
+                constexpr int F = decltype(tag)::value;
 #pragma unroll
-            for (int q = 0; q < NCH; ++q) {
-                const int c = ct + q * 128;
-                const int r = c >> 3, jj = c & 7;
-                const int n = n0 + r, k0 = kb * BK + 8 * jj;
-                float v[8];
-                if (n < N && k0 < K) {  // K % 16 == 0: all 8 elements are in range
-                    uint32_t code[8];
-                    const uint8_t* rp = raw + r * args.q_kb_bytes;
-                    if (eight) {
-                        const uint2 w = *reinterpret_cast<const uint2*>(rp + 8 * jj);
+                for (int q = 0; q < NCH; ++q) {
+                    const int c = ct + q * 128;
+                    const int r = c >> 3, jj = c & 7;
+                    const int n = n0 + r, k0 = kb * BK + 8 * jj;
+                    float v[8];
+                    if (n < N && k0 < K) {  // K % 16 == 0: all 8 elements are in range
+                        const uint8_t* rp = raw + r * args.q_kb_bytes;
+                        if (F == 0 || F == 1) {  // FP4 E2M1 codes times the block scale
+                            const uint32_t w = *reinterpret_cast<const uint32_t*>(rp + 4 * jj);
 #pragma unroll
-                        for (int e = 0; e < 4; ++e) {
-                            code[e] = (w.x >> (8 * e)) & 255u;
-                            code[e + 4] = (w.y >> (8 * e)) & 255u;
+                            for (int e = 0; e < 4; ++e) {
+                                const float2 f = h2_to_f2(cvt_e2m1x2((w >> (8 * e)) & 255u));
+                                v[2 * e] = f.x * sc[q];
+                                v[2 * e + 1] = f.y * sc[q];
+                            }
+                        } else if (F == 2) {  // FP8 E4M3 codes times the block scale
+                            const uint2 w = *reinterpret_cast<const uint2*>(rp + 8 * jj);
+#pragma unroll
+                            for (int e = 0; e < 4; ++e) {
+                                const uint32_t pair = ((e < 2 ? w.x : w.y) >> (16 * (e & 1))) & 0xffffu;
+                                const float2 f = h2_to_f2(cvt_e4m3x2(pair));
+                                v[2 * e] = f.x * sc[q];
+                                v[2 * e + 1] = f.y * sc[q];
+                            }
+                        } else {  // affine: fmaf(scale, q, bias)
+                            uint32_t code[8];
+                            if (F == 4) {
+                                const uint2 w = *reinterpret_cast<const uint2*>(rp + 8 * jj);
+#pragma unroll
+                                for (int e = 0; e < 4; ++e) {
+                                    code[e] = (w.x >> (8 * e)) & 255u;
+                                    code[e + 4] = (w.y >> (8 * e)) & 255u;
+                                }
+                            } else {
+                                const uint32_t w = *reinterpret_cast<const uint32_t*>(rp + 4 * jj);
+#pragma unroll
+                                for (int e = 0; e < 8; ++e) code[e] = (w >> (4 * e)) & 15u;
+                            }
+#pragma unroll
+                            for (int e = 0; e < 8; ++e) v[e] = fmaf(sc[q], float(code[e]), bs[q]);
                         }
                     } else {
-                        const uint32_t w = *reinterpret_cast<const uint32_t*>(rp + 4 * jj);
 #pragma unroll
-                        for (int e = 0; e < 8; ++e) code[e] = (w >> (4 * e)) & 15u;
+                        for (int e = 0; e < 8; ++e) v[e] = 0.f;
                     }
-                    if (!affine) {
-#pragma unroll
-                        for (int e = 0; e < 8; ++e)
-                            v[e] = (fmt == 2 ? dec_e4m3(code[e]) : dec_e2m1(code[e])) * sc[q];
-                    } else {
-#pragma unroll
-                        for (int e = 0; e < 8; ++e) v[e] = fmaf(sc[q], float(code[e]), bs[q]);
-                    }
-                } else {
-#pragma unroll
-                    for (int e = 0; e < 8; ++e) v[e] = 0.f;
+                    uint4 pk;
+                    pk.x = pack_bf16x2(v[0], v[1]);
+                    pk.y = pack_bf16x2(v[2], v[3]);
+                    pk.z = pack_bf16x2(v[4], v[5]);
+                    pk.w = pack_bf16x2(v[6], v[7]);
+                    *reinterpret_cast<uint4*>(wt + (r >> 6) * B_KB_BYTES + ((r & 63) >> 3) * 1024 +
+                                              (r & 7) * 128 + ((jj ^ (r & 7)) << 4)) = pk;
                 }
-                uint4 pk;
-                pk.x = pack_bf16x2(v[0], v[1]);
-                pk.y = pack_bf16x2(v[2], v[3]);
-                pk.z = pack_bf16x2(v[4], v[5]);
-                pk.w = pack_bf16x2(v[6], v[7]);
-                *reinterpret_cast<uint4*>(wt + (r >> 6) * B_KB_BYTES + ((r & 63) >> 3) * 1024 +
-                                          (r & 7) * 128 + ((jj ^ (r & 7)) << 4)) = pk;
+            };
+            switch (fmt) {
+                case 0: convert(std::integral_constant<int, 0>{}); break;
+                case 1: convert(std::integral_constant<int, 1>{}); break;
+                case 2: convert(std::integral_constant<int, 2>{}); break;
+                case 3: convert(std::integral_constant<int, 3>{}); break;
+                default: convert(std::integral_constant<int, 4>{}); break;
             }
             fence_proxy_async_smem();  // generic writes, read by the MMA (async proxy)
             __syncwarp();
