@@ -208,7 +208,7 @@ gemm_kernel(const __grid_constant__ CUtensorMap tmap_x, const __grid_constant__ 
         for (int s = 0; s < S; ++s) {
             mbar_init(&full[s], 1);
             mbar_init(&empty[s], 1);
-            if (QUANT) mbar_init(&conv[s], CONV_WARPS);
+            if (QUANT) mbar_init(&conv[s], CONV_WARPS / 2);  // the two warps of a group
         }
         for (int a = 0; a < 2; ++a) {
             mbar_init(&tfull[a], 1);
@@ -578,52 +578,28 @@ gemm_kernel(const __grid_constant__ CUtensorMap tmap_x, const __grid_constant__ 
         }
     } else if (QUANT) {
         // --------------------------------------------------------------- converters
-        // The four converter warps turn each stage's packed codes into the bf16 W tile
-        // the MMA reads (K-major, 128-byte swizzle: the layout a TMA copy of bf16 W would
-        // give), once the stage's copies have landed; all four take every stage, in order
-        // (so each waits on a stage's barrier one phase at a time), thread ct of 128 on
-        // the 8-element chunks ct, ct+128, ...  The group scales of the next stage are
-        // read from global memory while the current stage converts.  Every dequantized
-        // value except the affine ones is exact in bf16; affine is fmaf(scale, q, bias)
-        // rounded to bf16.  Rows past N and K-blocks past K become zeros.
-        constexpr int NCH = NSUB * 64 * 8 / 128;  // chunks per converter thread
-        const int ct = (warp - 6) * 32 + lane;
+        // Two groups of two converter warps turn the stages' packed codes into the bf16 W
+        // tiles the MMA reads (K-major, 128-byte swizzle: the layout a TMA copy of bf16 W
+        // would give), once a stage's copies have landed.  Group g takes the iterations
+        // (stages) i = g mod 2; the ring has an even number of stages, so a group takes
+        // every use of its stages in order and waits on each barrier one phase at a
+        // time.  Thread ct of a group's 64 converts the 8-element chunks ct, ct+64, ...
+        // Every dequantized value except the affine ones is exact in bf16; affine is
+        // fmaf(scale, q, bias) rounded to bf16.  Rows past N and K-blocks past K become
+        // zeros.
+        constexpr int NCH = NSUB * 64 * 8 / 64;  // chunks per converter thread
+        const int cgrp = (warp - 6) >> 1;
+        const int ct = ((warp - 6) & 1) * 32 + lane;
         const int fmt = args.qfmt;
-        const bool affine = fmt >= 3;
         const uint8_t* qs8 = static_cast<const uint8_t*>(args.qscales);
         const uint16_t* qs16 = static_cast<const uint16_t*>(args.qscales);
         const int nkb_t = kb1 - kb0;
         const int tiles_mine = first_tile < num_tiles
                                    ? (num_tiles - 1 - first_tile) / tile_step + 1 : 0;
         const int iters = tiles_mine * nkb_t;
-        // scale (and bias) of every chunk of iteration j, decoded to fp32
-        auto fetch = [&](int j, float (&sc)[NCH], float (&bs)[NCH]) {
-            const int t = first_tile + (j / nkb_t) * tile_step;
-            const int kb = kb0 + j % nkb_t;
-            const int n0 = (t % n_tiles) * tile_n;
-#pragma unroll
-            for (int q = 0; q < NCH; ++q) {
-                const int c = ct + q * 128;
-                const int n = n0 + (c >> 3), k0 = kb * BK + 8 * (c & 7);
-                sc[q] = 0.f;
-                bs[q] = 0.f;
-                if (n < N && k0 < K) {
-                    const int64_t grp = int64_t(n) * args.lds + k0 / args.gs;
-                    if (!affine) {
-                        sc[q] = fmt == 1 ? dec_e4m3(qs8[grp]) : dec_e8m0(qs8[grp]);
-                    } else {
-                        sc[q] = widen16(qs16[grp], false);
-                        bs[q] = widen16(args.qbiases[int64_t(n) * args.ldb + k0 / args.gs], false);
-                    }
-                }
-            }
-        };
-        float sc[NCH], bs[NCH], sc_n[NCH], bs_n[NCH];
-        if (iters > 0) fetch(0, sc, bs);
-        uint32_t stage = 0, phase = 0;
+        uint32_t stage = uint32_t(cgrp), phase = 0;
         bool ok = true;
-        for (int j = 0; j < iters; ++j) {
-            if (j + 1 < iters) fetch(j + 1, sc_n, bs_n);
+        for (int j = cgrp; j < iters; j += 2) {
             const int t = first_tile + (j / nkb_t) * tile_step;
             const int kb = kb0 + j % nkb_t;
             const int n0 = (t % n_tiles) * tile_n;
@@ -636,21 +612,32 @@ gemm_kernel(const __grid_constant__ CUtensorMap tmap_x, const __grid_constant__ 
             // one specialised loop per format (the format is uniform over the launch)
             auto convert = [&](auto tag) {
                 constexpr int F = decltype(tag)::value;
-#pragma unroll
+#pragma unroll 4
                 for (int q = 0; q < NCH; ++q) {
-                    const int c = ct + q * 128;
+                    const int c = ct + q * 64;
                     const int r = c >> 3, jj = c & 7;
                     const int n = n0 + r, k0 = kb * BK + 8 * jj;
                     float v[8];
                     if (n < N && k0 < K) {  // K % 16 == 0: all 8 elements are in range
                         const uint8_t* rp = raw + r * args.q_kb_bytes;
+                        // the group's scale (and bias): a row's scales are read in order
+                        // across the stages, so after a row's first line they come from L1
+                        const int64_t grp = int64_t(n) * args.lds + k0 / args.gs;
+                        float scq, bsq = 0.f;
+                        if (F == 0 || F == 2) scq = dec_e8m0(__ldg(qs8 + grp));
+                        else if (F == 1) scq = dec_e4m3(__ldg(qs8 + grp));
+                        else {
+                            scq = widen16(__ldg(qs16 + grp), false);
+                            bsq = widen16(__ldg(args.qbiases + int64_t(n) * args.ldb + k0 / args.gs),
+                                          false);
+                        }
                         if (F == 0 || F == 1) {  // FP4 E2M1 codes times the block scale
                             const uint32_t w = *reinterpret_cast<const uint32_t*>(rp + 4 * jj);
 #pragma unroll
                             for (int e = 0; e < 4; ++e) {
                                 const float2 f = h2_to_f2(cvt_e2m1x2((w >> (8 * e)) & 255u));
-                                v[2 * e] = f.x * sc[q];
-                                v[2 * e + 1] = f.y * sc[q];
+                                v[2 * e] = f.x * scq;
+                                v[2 * e + 1] = f.y * scq;
                             }
                         } else if (F == 2) {  // FP8 E4M3 codes times the block scale
                             const uint2 w = *reinterpret_cast<const uint2*>(rp + 8 * jj);
@@ -658,8 +645,8 @@ gemm_kernel(const __grid_constant__ CUtensorMap tmap_x, const __grid_constant__ 
                             for (int e = 0; e < 4; ++e) {
                                 const uint32_t pair = ((e < 2 ? w.x : w.y) >> (16 * (e & 1))) & 0xffffu;
                                 const float2 f = h2_to_f2(cvt_e4m3x2(pair));
-                                v[2 * e] = f.x * sc[q];
-                                v[2 * e + 1] = f.y * sc[q];
+                                v[2 * e] = f.x * scq;
+                                v[2 * e + 1] = f.y * scq;
                             }
                         } else {  // affine: fmaf(scale, q, bias)
                             uint32_t code[8];
@@ -676,7 +663,7 @@ gemm_kernel(const __grid_constant__ CUtensorMap tmap_x, const __grid_constant__ 
                                 for (int e = 0; e < 8; ++e) code[e] = (w >> (4 * e)) & 15u;
                             }
 #pragma unroll
-                            for (int e = 0; e < 8; ++e) v[e] = fmaf(sc[q], float(code[e]), bs[q]);
+                            for (int e = 0; e < 8; ++e) v[e] = fmaf(scq, float(code[e]), bsq);
                         }
                     } else {
 #pragma unroll
@@ -701,13 +688,9 @@ gemm_kernel(const __grid_constant__ CUtensorMap tmap_x, const __grid_constant__ 
             fence_proxy_async_smem();  // generic writes, read by the MMA (async proxy)
             __syncwarp();
             if (lane == 0) mbar_arrive(&conv[stage]);
-#pragma unroll
-            for (int q = 0; q < NCH; ++q) {
-                sc[q] = sc_n[q];
-                bs[q] = bs_n[q];
-            }
-            if (++stage == uint32_t(S)) {
-                stage = 0;
+            stage += 2;  // S is even: the group stays on its own stages
+            if (stage >= uint32_t(S)) {
+                stage -= uint32_t(S);
                 phase ^= 1u;
             }
         }
@@ -965,6 +948,7 @@ cudaError_t launch_qgemm(const DeviceInfo& dev, const void* x, int64_t ldx, cons
     const int64_t blk = int64_t(a_rows) * BK * 2 + int64_t(nsub) * (B_KB_BYTES + Q_RAW_KB_BYTES);
     int stages = int(RING_BYTES / blk);
     if (stages > MAX_QSTAGES) stages = MAX_QSTAGES;
+    stages &= ~1;  // even: each of the two converter groups owns every other stage
     if (stages < 2 || int64_t(stages - 1) * a_rows * BK * 2 + A_MMA_BYTES > int64_t(stages) * blk)
         return cudaErrorNotSupported;
     const bool eight = fmt == 2 || fmt == 4;
