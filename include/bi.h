@@ -115,6 +115,20 @@ int64_t bi_get_batch_invariant_limit(void);
 /* 1 if a call with leading dimension / verify width `dim` falls inside the limit. */
 int bi_within_batch_invariant_limit(int64_t dim);
 
+/* ---------------------------------------------------------------------------------
+ * Weight prefetch (process-wide, default 0).  Each kernel is launched so that it may
+ * start while the previous kernel in its stream is still running; by default it reads
+ * no global memory until that kernel has finished.  With the setting at 1, bi_matmul*
+ * and bi_qmatmul start streaming W (the codes, scales and biases for bi_qmatmul) before
+ * that point, which hides part of the weight stream behind the previous kernel's tail.
+ * Set it only if no kernel writes a weight operand right before a call that reads it on
+ * the same stream (weights that are fixed for the life of the program qualify; a matmul
+ * whose W is the previous matmul's Y does not).  The setting does not change any result.
+ * bi_set_weight_prefetch returns BI_ERR_INVALID_ARG for values other than 0 and 1.
+ * ------------------------------------------------------------------------------- */
+bi_status bi_set_weight_prefetch(int on);
+int bi_get_weight_prefetch(void);
+
 /* Introspection (host only, no device access): the configuration a call with these
  * sizes would run under the current limit, on a GPU with num_sms SMs.
  * bi_matmul_splits: CTAs per output tile along K (1 = the invariant single K loop).

@@ -36,6 +36,8 @@ SIGNATURES = {
     "bi_set_batch_invariant_limit": ([_i64], _int),
     "bi_get_batch_invariant_limit": ([], _i64),
     "bi_within_batch_invariant_limit": ([_i64], _int),
+    "bi_set_weight_prefetch": ([_int], _int),
+    "bi_get_weight_prefetch": ([], _int),
     "bi_matmul_splits": ([_i64, _i64, _i64, _int, _int], _int),
     "bi_attn_chunk": ([_i64, _i64, _i64, _i64, _i64, _i64, _i64, _sz, _int], _i64),
     "bi_matmul": ([_p, _i64, _p, _i64, _int, _p, _i64, _int, _i64, _i64, _i64, _p], _int),
@@ -152,6 +154,16 @@ def get_batch_invariant_limit() -> int:
 
 def within_batch_invariant_limit(dim: int) -> bool:
     return bool(lib().bi_within_batch_invariant_limit(int(dim)))
+
+
+def set_weight_prefetch(on: bool) -> None:
+    """Let matmuls start reading their weights before the previous kernel in the stream
+    has finished.  Only for weights no kernel writes right before the call reads them."""
+    _check(lib().bi_set_weight_prefetch(1 if on else 0))
+
+
+def get_weight_prefetch() -> bool:
+    return bool(lib().bi_get_weight_prefetch())
 
 
 def matmul_splits(M: int, N: int, K: int, w_layout: str = "nk", num_sms: int = 152) -> int:

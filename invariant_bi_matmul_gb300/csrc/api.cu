@@ -44,6 +44,9 @@ bi_status cuda_fail(cudaError_t e, const char* what) {
 
 // ------------------------------------------------------------------ limit (atomic)
 std::atomic<int64_t> g_limit{0};
+// early weight reads (bi_set_weight_prefetch); off: every kernel waits for the previous
+// grid in its stream before it reads global memory
+std::atomic<int> g_weight_prefetch{0};
 std::once_flag g_limit_once;
 
 void init_limit_from_env() {
@@ -129,6 +132,14 @@ BI_EXPORT int64_t bi_get_batch_invariant_limit(void) {
     init_limit_from_env();
     return g_limit.load();
 }
+
+BI_EXPORT bi_status bi_set_weight_prefetch(int on) {
+    if (on != 0 && on != 1) return fail(BI_ERR_INVALID_ARG, "weight prefetch must be 0 or 1");
+    g_weight_prefetch.store(on);
+    return BI_OK;
+}
+
+BI_EXPORT int bi_get_weight_prefetch(void) { return g_weight_prefetch.load(); }
 
 BI_EXPORT int bi_within_batch_invariant_limit(int64_t dim) {
     init_limit_from_env();
@@ -220,6 +231,7 @@ bi_status matmul_impl(const char* fn, const void* x, int64_t ldx, const void* w,
     const bool split_ok = !bi_within_batch_invariant_limit(M);
     cudaError_t e = launch_gemm(*dev, x, ldx, w, ldw, w_layout == BI_W_KN, y, ldy,
                                 y_dtype == BI_F32, M, N, K, split_ok, in_dtype == BI_F16,
+                                g_weight_prefetch.load() != 0,
                                 reinterpret_cast<cudaStream_t>(stream));
     if (e != cudaSuccess) return cuda_fail(e, fn);
     return BI_OK;
@@ -325,6 +337,7 @@ BI_EXPORT bi_status bi_qmatmul(const void* x, int64_t ldx, const void* wq, int64
     if (!dev) return cuda_fail(why, fn);
     cudaError_t e = launch_qgemm(*dev, x, ldx, wq, ldwq, scales, lds, biases, ldb, qformat,
                                  group_size, y, ldy, y_dtype == BI_F32, M, N, K,
+                                 g_weight_prefetch.load() != 0,
                                  reinterpret_cast<cudaStream_t>(stream));
     if (e != cudaSuccess) return cuda_fail(e, fn);
     return BI_OK;

@@ -65,12 +65,14 @@ constexpr int MAX_STAGES = 48;
 constexpr int MAX_SPLITS = 8;               // split-K cluster size (portable maximum)
 constexpr int THREADS = 192;
 constexpr int EPI_THREADS = 128;
-// Quantized W: four more warps (6..9) turn the packed codes of each stage into the bf16
-// operand tile; at most MAX_QSTAGES ring stages, one K-block each.
+// Quantized W: four more warps (6..9) turn the packed codes of each stage into bf16
+// operand tiles.  The ring (at most MAX_QSTAGES stages, one K-block each) holds X blocks
+// and packed codes only; the bf16 tiles live in a separate ring of MAX_QWBUF buffers.
 constexpr int QTHREADS = THREADS + 128;
 constexpr int CONV_WARPS = 4;
 constexpr int MAX_QSTAGES = 16;
-constexpr int Q_RAW_KB_BYTES = 64 * BK;     // packed codes of 64 rows x one K-block (8-bit)
+constexpr int MAX_QWBUF = 4;
+constexpr int Q_SROW = 16;  // bytes of staged scales (or biases) per tile row and stage
 constexpr int B_KB_BYTES = BN * BK * 2;     // one instruction tile's W block per K-block
 constexpr int A_MMA_BYTES = BM * BK * 2;    // 16 KiB: what one MMA reads from an X block
 constexpr int SMEM_BYTES = 220 * 1024;      // dynamic shared memory per CTA
@@ -83,7 +85,7 @@ constexpr int KN_SWIZZLE = KN_ATOM_N * 2;          // 64 or 128 bytes
 constexpr uint32_t KN_LAYOUT = KN_SWIZZLE == 128 ? 2u : 4u;
 
 static_assert(BN == 32 || BN == 64 || BN == 128, "instruction N must be 32, 64 or 128");
-static_assert((2 * MAX_STAGES + 7 + MAX_QSTAGES) * 8 + 16 <= CTRL_BYTES,
+static_assert((2 * MAX_STAGES + 7 + 2 * MAX_QWBUF) * 8 + 16 <= CTRL_BYTES,
               "control block too small");
 
 struct GemmArgs {
@@ -96,6 +98,9 @@ struct GemmArgs {
     int blocked;         // K % 64 == 0: one rank-3 copy per operand per stage
     int stages;          // ring depth
     int w_stream_once;   // one M-tile: W is read exactly once (L2 evict-first hint)
+    int w_early;         // W (codes, scales, biases) may be read before the previous grid
+                         // in the stream has finished: the caller has promised that grid
+                         // does not write them
     // Split-K (the non-invariant kernel only): a cluster of `splits` CTAs shares each
     // output tile, CTA rank r accumulating K-blocks [r*kb_per_split, (r+1)*kb_per_split).
     // The invariant kernel has splits = 1 and kb_per_split = the number of K-blocks.
@@ -112,12 +117,16 @@ struct GemmArgs {
     const uint16_t* qbiases;
     int64_t ldb;
     int q_kb_bytes;
+    int wbufs;         // bf16 W tile buffers (even, <= MAX_QWBUF)
+    int q_staged;      // the scales (and biases) come with the codes, by TMA, Q_SROW bytes
+                       // per row and stage starting at a 16-byte boundary; else the
+                       // converters load them from global memory
 };
 
 // ----------------------------------------------------------- quantized-code decoding
-// From the format definitions (OCP Microscaling FP8 E4M3 and E8M0 scale codes; the FP4
-// E2M1 and FP8 E4M3 elements go through the hardware's exact two-at-a-time conversions
-// below); every decoded value is exact in fp32.
+// From the format definitions (OCP Microscaling FP8 E4M3 and E8M0 scale codes; FP8 E4M3
+// elements go through the hardware's exact two-at-a-time conversion below, FP4 E2M1
+// elements through a byte lookup); every decoded value is exact in fp32 and in bf16.
 __device__ __forceinline__ float dec_e4m3(uint32_t c) {
     const uint32_t e = (c >> 3) & 15u, m = c & 7u;
     float mag;
@@ -127,15 +136,8 @@ __device__ __forceinline__ float dec_e4m3(uint32_t c) {
     return (c & 0x80u) ? -mag : mag;
 }
 
-// Two codes to two halves, exactly (every FP4 E2M1 and FP8 E4M3 value is a binary16
-// value): the low code (low nibble / low byte) to the low half.
-__device__ __forceinline__ uint32_t cvt_e2m1x2(uint32_t byte) {
-    uint32_t d;
-    asm("{\n\t.reg .b8 t;\n\tcvt.u8.u32 t, %1;\n\tcvt.rn.f16x2.e2m1x2 %0, t;\n\t}"
-        : "=r"(d) : "r"(byte));
-    return d;
-}
-
+// Two codes to two halves, exactly (every FP8 E4M3 value is a binary16 value): the low
+// byte to the low half.
 __device__ __forceinline__ uint32_t cvt_e4m3x2(uint32_t two) {
     uint32_t d;
     asm("{\n\t.reg .b16 t;\n\tcvt.u16.u32 t, %1;\n\tcvt.rn.f16x2.e4m3x2 %0, t;\n\t}"
@@ -152,9 +154,49 @@ __device__ __forceinline__ float dec_e8m0(uint32_t c) {
                      : (c == 0u ? __uint_as_float(0x00400000u) : __uint_as_float(c << 23));
 }
 
+// Byte permute (PTX prmt, default mode): byte n of the result is byte (sel nibble n & 7)
+// of the pair {b, a} (a = bytes 0-3); a nibble with bit 3 set instead fills the byte
+// with copies of the selected byte's top bit.
+__device__ __forceinline__ uint32_t prmt(uint32_t a, uint32_t b, uint32_t sel) {
+    uint32_t d;
+    asm("prmt.b32 %0, %1, %2, %3;" : "=r"(d) : "r"(a), "r"(b), "r"(sel));
+    return d;
+}
+
+__device__ __forceinline__ uint32_t mul_bf16x2(uint32_t a, uint32_t b) {
+    uint32_t d;
+    asm("mul.rn.bf16x2 %0, %1, %2;" : "=r"(d) : "r"(a), "r"(b));
+    return d;
+}
+
+// Eight FP4 E2M1 codes (one word, low nibble first) to four bf16x2 words, exactly and
+// without conversion instructions: the bf16 of each magnitude (0, 0.5, 1, 1.5, 2, 3, 4,
+// 6) is looked up one byte at a time, and each code's sign bit becomes its half's.
+__device__ __forceinline__ void e2m1x8_to_bf16(uint32_t w, uint32_t (&o)[4]) {
+    // low bytes of the eight magnitudes: 00 00 80 c0 00 40 80 c0; high: 00 3f 3f 3f 40 40 40 40
+    constexpr uint32_t LO_A = 0xc0800000u, LO_B = 0xc0804000u;
+    constexpr uint32_t HI_A = 0x3f3f3f00u, HI_B = 0x40404040u;
+    const uint32_t m = w & 0x77777777u;  // one magnitude index per nibble
+    const uint32_t lo03 = prmt(LO_A, LO_B, m), hi03 = prmt(HI_A, HI_B, m);
+    const uint32_t lo47 = prmt(LO_A, LO_B, m >> 16), hi47 = prmt(HI_A, HI_B, m >> 16);
+    // code 2j+1's sign is the top bit of byte j of w, code 2j's that of byte j of w << 4
+    const uint32_t w4 = w << 4;
+    o[0] = prmt(lo03, hi03, 0x5140u) | (prmt(w, w4, 0x80c0u) & 0x80008000u);
+    o[1] = prmt(lo03, hi03, 0x7362u) | (prmt(w, w4, 0x90d0u) & 0x80008000u);
+    o[2] = prmt(lo47, hi47, 0x5140u) | (prmt(w, w4, 0xa0e0u) & 0x80008000u);
+    o[3] = prmt(lo47, hi47, 0x7362u) | (prmt(w, w4, 0xb0f0u) & 0x80008000u);
+}
+
+// An integer code c < 2^23 as fp32 without a conversion instruction: the bits of 2^23 + c
+// (byte `byte_sel` of `word` placed in the mantissa's low byte) minus 2^23, exact.
+__device__ __forceinline__ float byte_to_f32(uint32_t word, uint32_t byte_sel) {
+    return __uint_as_float(prmt(word, 0x4b000000u, 0x7440u | byte_sel)) - 8388608.0f;
+}
+
 template <bool KN, bool F32OUT, int NSUB, bool SPLIT, int MSUB, bool QUANT>
 __global__ void __launch_bounds__(QUANT ? QTHREADS : THREADS, 1)
 gemm_kernel(const __grid_constant__ CUtensorMap tmap_x, const __grid_constant__ CUtensorMap tmap_w,
+            const __grid_constant__ CUtensorMap tmap_s, const __grid_constant__ CUtensorMap tmap_b,
             const GemmArgs args, unsigned int* err) {
     extern __shared__ uint8_t smem_raw[];
     uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) &
@@ -165,9 +207,15 @@ gemm_kernel(const __grid_constant__ CUtensorMap tmap_x, const __grid_constant__ 
     const int a_bytes = args.a_rows * (BK * 2);   // one X block (one K-block)
     const int b_bytes = nsub * B_KB_BYTES;        // one W block (one K-block, every sub-tile)
     uint8_t* sA = smem;                           // S*kbs X blocks
-    uint8_t* sB = smem + S * kbs * a_bytes;       // S*kbs W blocks
-    uint8_t* sR = sB + S * kbs * b_bytes;         // QUANT: S packed-code blocks
-    const int r_bytes = nsub * Q_RAW_KB_BYTES;
+    uint8_t* sB = smem + S * kbs * a_bytes;       // S*kbs W blocks (QUANT: wbufs W tiles)
+    uint8_t* sR = sB + (QUANT ? args.wbufs : S * kbs) * b_bytes;  // QUANT: S code blocks
+    // QUANT stage: the packed codes, then (staged) a block of scales and, affine, biases
+    const bool q_aff = args.qfmt >= 3;
+    const int codes_bytes = nsub * 64 * args.q_kb_bytes;
+    const int s_blk = nsub * 64 * Q_SROW;
+    const int r_bytes = codes_bytes + (args.q_staged ? (q_aff ? 2 : 1) * s_blk : 0);
+    const int gsh = QUANT ? 31 - __clz(args.gs) : 0;  // the group size is a power of two
+    const int s_epb = q_aff ? Q_SROW / 2 : Q_SROW;     // staged elements per row
     uint64_t* full = reinterpret_cast<uint64_t*>(smem + RING_BYTES);
     uint64_t* empty = full + MAX_STAGES;
     uint64_t* tfull = empty + MAX_STAGES;
@@ -175,8 +223,9 @@ gemm_kernel(const __grid_constant__ CUtensorMap tmap_x, const __grid_constant__ 
     uint64_t* drain = tempty + 2;
     uint64_t* red_full = drain + 1;  // split-K, rank 0: the other ranks' partials are in
     uint64_t* red_free = drain + 2;  // split-K, rank > 0: rank 0 has read this rank's slot
-    uint64_t* conv = drain + 3;      // QUANT: stage s's bf16 W tile is written
-    uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(conv + MAX_QSTAGES);
+    uint64_t* conv = drain + 3;             // QUANT: W tile buffer b is written
+    uint64_t* wfree = conv + MAX_QWBUF;     // QUANT: the MMAs reading buffer b are done
+    uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(wfree + MAX_QWBUF);
     volatile int* abort_flag = reinterpret_cast<volatile int*>(tmem_slot + 1);
 
     const int warp = threadIdx.x >> 5;
@@ -208,7 +257,12 @@ gemm_kernel(const __grid_constant__ CUtensorMap tmap_x, const __grid_constant__ 
         for (int s = 0; s < S; ++s) {
             mbar_init(&full[s], 1);
             mbar_init(&empty[s], 1);
-            if (QUANT) mbar_init(&conv[s], CONV_WARPS / 2);  // the two warps of a group
+        }
+        if (QUANT) {
+            for (int b = 0; b < args.wbufs; ++b) {
+                mbar_init(&conv[b], CONV_WARPS / 2);  // the two warps of a group
+                mbar_init(&wfree[b], 1);
+            }
         }
         for (int a = 0; a < 2; ++a) {
             mbar_init(&tfull[a], 1);
@@ -237,9 +291,9 @@ gemm_kernel(const __grid_constant__ CUtensorMap tmap_x, const __grid_constant__ 
     if constexpr (SPLIT) cluster_sync_all();
     const uint32_t tmem_base = *tmem_slot;
     // The set-up above touches no global memory.  The previous grid in the stream may
-    // still be running: the producer starts fetching W (which no kernel of this library
-    // writes) before it waits for that grid, and X only after; the epilogue waits before
-    // its first store; the MMA warp touches only shared and tensor memory.
+    // still be running: the producer (and the converters) read W before waiting for that
+    // grid only when the caller has allowed it (w_early), X always after; the epilogue
+    // waits before its first store; the MMA warp touches only shared and tensor memory.
     pdl_trigger();
 
     auto fail = [&]() {
@@ -268,6 +322,14 @@ gemm_kernel(const __grid_constant__ CUtensorMap tmap_x, const __grid_constant__ 
                     tma_load_2d_s_hint(r_dst, &tmap_w, bar, kb * args.q_kb_bytes, n0, w_policy);
                 else
                     tma_load_2d_s(r_dst, &tmap_w, bar, kb * args.q_kb_bytes, n0);
+                if (args.q_staged) {
+                    // the groups of the K-block, from the 16-byte boundary at or below
+                    // its first group (the block's groups all fall in the 16 bytes)
+                    const int xs = ((kb * BK) >> gsh) & ~(s_epb - 1);
+                    tma_load_2d_s(r_dst + uint32_t(codes_bytes), &tmap_s, bar, xs, n0);
+                    if (q_aff)
+                        tma_load_2d_s(r_dst + uint32_t(codes_bytes + s_blk), &tmap_b, bar, xs, n0);
+                }
             } else if (KN) {
                 // per swizzle atom (KN_ATOM_N columns) one box of 64*kbs k-rows
                 for (int c = 0; c < tile_n; c += KN_ATOM_N) {
@@ -308,13 +370,15 @@ gemm_kernel(const __grid_constant__ CUtensorMap tmap_x, const __grid_constant__ 
         auto stage_tx = [&](int nk) {
             const int x_blocks = blocked ? kbs : nk;
             const int w_blocks = (blocked || KN) ? kbs : nk;
-            if (QUANT) return uint32_t(x_blocks * a_bytes + nsub * 64 * args.q_kb_bytes);
+            if (QUANT) return uint32_t(x_blocks * a_bytes + r_bytes);
             return uint32_t(x_blocks * a_bytes + w_blocks * b_bytes);
         };
 
-        // Before the previous grid is done: W of the first tile's first stages goes
-        // straight into the (empty) ring, so the weight stream overlaps the previous
-        // kernel's tail.
+        // With w_early, before the previous grid is done: W of the first tile's first
+        // stages goes straight into the (empty) ring, so the weight stream overlaps the
+        // previous kernel's tail.  Without it the wait comes first (the previous grid may
+        // have written W) and the same copies are simply the ring's first.
+        if (!args.w_early) pdl_wait();
         int early = 0;  // stages of the first tile whose W is already issued
         if (first_tile < num_tiles) {
             const int n0 = (first_tile % n_tiles) * tile_n;
@@ -385,6 +449,7 @@ gemm_kernel(const __grid_constant__ CUtensorMap tmap_x, const __grid_constant__ 
         const uint32_t stage_a = uint32_t(kbs * a_bytes), stage_b = uint32_t(kbs * b_bytes);
         const uint32_t empty_s = smem_addr(empty);
         uint32_t stage = 0, phase = 0;
+        uint32_t wb = 0, wphase = 0;  // QUANT: the W tile buffer and its phase
         bool ok = true;
         int local = 0;
         for (int t = first_tile; ok && t < num_tiles; t += tile_step, ++local) {
@@ -398,7 +463,7 @@ gemm_kernel(const __grid_constant__ CUtensorMap tmap_x, const __grid_constant__ 
             const uint32_t d_tmem = tmem_base + uint32_t(acc * ACC_COLS);
             for (int kb = kb0; kb < kb1; kb += kbs) {
                 if (!mbar_wait_warp(&full[stage], phase, abort_flag) ||
-                    (QUANT && !mbar_wait_warp(&conv[stage], phase, abort_flag))) {
+                    (QUANT && !mbar_wait_warp(&conv[wb], wphase, abort_flag))) {
                     ok = false;
                     break;
                 }
@@ -408,7 +473,7 @@ gemm_kernel(const __grid_constant__ CUtensorMap tmap_x, const __grid_constant__ 
                     // descriptors are advanced by adding (byte offset >> 4) to the start-
                     // address field; shared addresses stay below 2^18 so it never carries
                     uint64_t a_blk = a_desc0 + (uint64_t(stage * stage_a) >> 4);
-                    uint64_t b_blk = b_desc0 + (uint64_t(stage * stage_b) >> 4);
+                    uint64_t b_blk = b_desc0 + (uint64_t((QUANT ? wb : stage) * stage_b) >> 4);
                     for (int i = 0; i < nk; ++i, a_blk += a_step, b_blk += b_step) {
                         const uint32_t first = (kb + i) == kb0 ? 1u : 0u;
 #pragma unroll
@@ -429,11 +494,16 @@ gemm_kernel(const __grid_constant__ CUtensorMap tmap_x, const __grid_constant__ 
                         }
                     }
                     tc_commit_s(empty_s + stage * 8u);  // frees the stage once these MMAs finish
+                    if (QUANT) tc_commit(&wfree[wb]);     // and the W tile buffer
                 }
                 __syncwarp();
                 if (++stage == uint32_t(S)) {
                     stage = 0;
                     phase ^= 1u;
+                }
+                if (QUANT && ++wb == uint32_t(args.wbufs)) {
+                    wb = 0;
+                    wphase ^= 1u;
                 }
             }
             if (!ok) break;
@@ -580,119 +650,193 @@ gemm_kernel(const __grid_constant__ CUtensorMap tmap_x, const __grid_constant__ 
         // --------------------------------------------------------------- converters
         // Two groups of two converter warps turn the stages' packed codes into the bf16 W
         // tiles the MMA reads (K-major, 128-byte swizzle: the layout a TMA copy of bf16 W
-        // would give), once a stage's copies have landed.  Group g takes the iterations
-        // (stages) i = g mod 2; the ring has an even number of stages, so a group takes
-        // every use of its stages in order and waits on each barrier one phase at a
-        // time.  Thread ct of a group's 64 converts the 8-element chunks ct, ct+64, ...
-        // Every dequantized value except the affine ones is exact in bf16; affine is
-        // fmaf(scale, q, bias) rounded to bf16.  Rows past N and K-blocks past K become
-        // zeros.
-        constexpr int NCH = NSUB * 64 * 8 / 64;  // chunks per converter thread
+        // would give), once a stage's copies have landed and the tile buffer is free.
+        // Group g takes the iterations i = g mod 2; the ring and the buffer ring both have
+        // an even length, so a group takes every use of its stages and buffers in order and
+        // waits on each barrier one phase at a time.  Thread ct of a group's 64 converts whole rows of the K-block: tile rows
+        // ct, ct+64, ...  Its rows' scales (and biases) for its next stage are loaded
+        // from global memory before it waits for the current one, so their latency hides
+        // behind the conversion.  Every dequantized value except the affine ones is exact
+        // in bf16; affine is fmaf(scale, q, bias) rounded to bf16.  Rows past N and
+        // columns past K become zeros.
         const int cgrp = (warp - 6) >> 1;
         const int ct = ((warp - 6) & 1) * 32 + lane;
-        const int fmt = args.qfmt;
         const uint8_t* qs8 = static_cast<const uint8_t*>(args.qscales);
         const uint16_t* qs16 = static_cast<const uint16_t*>(args.qscales);
         const int nkb_t = kb1 - kb0;
         const int tiles_mine = first_tile < num_tiles
                                    ? (num_tiles - 1 - first_tile) / tile_step + 1 : 0;
         const int iters = tiles_mine * nkb_t;
-        uint32_t stage = uint32_t(cgrp), phase = 0;
+        const bool staged = args.q_staged != 0;
+        if (!args.w_early) pdl_wait();  // scales may come from the previous grid
         bool ok = true;
-        for (int j = cgrp; j < iters; j += 2) {
-            const int t = first_tile + (j / nkb_t) * tile_step;
-            const int kb = kb0 + j % nkb_t;
-            const int n0 = (t % n_tiles) * tile_n;
-            if (!mbar_wait_warp(&full[stage], phase, abort_flag)) {
-                ok = false;
-                break;
-            }
-            const uint8_t* raw = sR + stage * r_bytes;
-            uint8_t* wt = sB + stage * b_bytes;
-            // one specialised loop per format (the format is uniform over the launch)
-            auto convert = [&](auto tag) {
-                constexpr int F = decltype(tag)::value;
-#pragma unroll 4
-                for (int q = 0; q < NCH; ++q) {
-                    const int c = ct + q * 64;
-                    const int r = c >> 3, jj = c & 7;
-                    const int n = n0 + r, k0 = kb * BK + 8 * jj;
-                    float v[8];
-                    if (n < N && k0 < K) {  // K % 16 == 0: all 8 elements are in range
-                        const uint8_t* rp = raw + r * args.q_kb_bytes;
-                        // the group's scale (and bias): a row's scales are read in order
-                        // across the stages, so after a row's first line they come from L1
-                        const int64_t grp = int64_t(n) * args.lds + k0 / args.gs;
-                        float scq, bsq = 0.f;
-                        if (F == 0 || F == 2) scq = dec_e8m0(__ldg(qs8 + grp));
-                        else if (F == 1) scq = dec_e4m3(__ldg(qs8 + grp));
-                        else {
-                            scq = widen16(__ldg(qs16 + grp), false);
-                            bsq = widen16(__ldg(args.qbiases + int64_t(n) * args.ldb + k0 / args.gs),
-                                          false);
-                        }
-                        if (F == 0 || F == 1) {  // FP4 E2M1 codes times the block scale
-                            const uint32_t w = *reinterpret_cast<const uint32_t*>(rp + 4 * jj);
+        // one specialised loop per format (the format is uniform over the launch)
+        auto run = [&](auto tag) {
+            constexpr int F = decltype(tag)::value;
+            constexpr bool AFF = F >= 3;
+            constexpr int G = F == 1 ? 4 : 2;  // scale segments per K-block row
+            constexpr int SEG = BK / G;        // columns per segment (<= the group size)
+            constexpr int RW = (F == 2 || F == 4) ? BK / 4 : BK / 8;  // code words per row
+            // raw scale (and bias) codes of iteration j's rows, one per segment
+            auto fetch = [&](int j, uint32_t (&sc)[NSUB][G], uint32_t (&bs)[NSUB][G]) {
+                const int t = first_tile + (j / nkb_t) * tile_step;
+                const int kb = kb0 + j % nkb_t;
+                const int n0 = (t % n_tiles) * tile_n;
 #pragma unroll
-                            for (int e = 0; e < 4; ++e) {
-                                const float2 f = h2_to_f2(cvt_e2m1x2((w >> (8 * e)) & 255u));
-                                v[2 * e] = f.x * scq;
-                                v[2 * e + 1] = f.y * scq;
-                            }
-                        } else if (F == 2) {  // FP8 E4M3 codes times the block scale
-                            const uint2 w = *reinterpret_cast<const uint2*>(rp + 8 * jj);
+                for (int q = 0; q < NSUB; ++q) {
+                    const int n = n0 + ct + 64 * q;
 #pragma unroll
-                            for (int e = 0; e < 4; ++e) {
-                                const uint32_t pair = ((e < 2 ? w.x : w.y) >> (16 * (e & 1))) & 0xffffu;
-                                const float2 f = h2_to_f2(cvt_e4m3x2(pair));
-                                v[2 * e] = f.x * scq;
-                                v[2 * e + 1] = f.y * scq;
-                            }
-                        } else {  // affine: fmaf(scale, q, bias)
-                            uint32_t code[8];
-                            if (F == 4) {
-                                const uint2 w = *reinterpret_cast<const uint2*>(rp + 8 * jj);
-#pragma unroll
-                                for (int e = 0; e < 4; ++e) {
-                                    code[e] = (w.x >> (8 * e)) & 255u;
-                                    code[e + 4] = (w.y >> (8 * e)) & 255u;
-                                }
+                    for (int g = 0; g < G; ++g) {
+                        const int k = kb * BK + g * SEG;
+                        sc[q][g] = 0u;
+                        bs[q][g] = 0u;
+                        if (n < N && k < K) {
+                            const int64_t gi = int64_t(k >> gsh);
+                            if (AFF) {
+                                sc[q][g] = __ldg(qs16 + int64_t(n) * args.lds + gi);
+                                bs[q][g] = __ldg(args.qbiases + int64_t(n) * args.ldb + gi);
                             } else {
-                                const uint32_t w = *reinterpret_cast<const uint32_t*>(rp + 4 * jj);
-#pragma unroll
-                                for (int e = 0; e < 8; ++e) code[e] = (w >> (4 * e)) & 15u;
+                                sc[q][g] = __ldg(qs8 + int64_t(n) * args.lds + gi);
                             }
-#pragma unroll
-                            for (int e = 0; e < 8; ++e) v[e] = fmaf(scq, float(code[e]), bsq);
                         }
-                    } else {
-#pragma unroll
-                        for (int e = 0; e < 8; ++e) v[e] = 0.f;
                     }
-                    uint4 pk;
-                    pk.x = pack_bf16x2(v[0], v[1]);
-                    pk.y = pack_bf16x2(v[2], v[3]);
-                    pk.z = pack_bf16x2(v[4], v[5]);
-                    pk.w = pack_bf16x2(v[6], v[7]);
-                    *reinterpret_cast<uint4*>(wt + (r >> 6) * B_KB_BYTES + ((r & 63) >> 3) * 1024 +
-                                              (r & 7) * 128 + ((jj ^ (r & 7)) << 4)) = pk;
                 }
             };
-            switch (fmt) {
-                case 0: convert(std::integral_constant<int, 0>{}); break;
-                case 1: convert(std::integral_constant<int, 1>{}); break;
-                case 2: convert(std::integral_constant<int, 2>{}); break;
-                case 3: convert(std::integral_constant<int, 3>{}); break;
-                default: convert(std::integral_constant<int, 4>{}); break;
+            uint32_t sc[NSUB][G] = {}, bs[NSUB][G] = {};
+            if (!staged && cgrp < iters) fetch(cgrp, sc, bs);
+            uint32_t stage = uint32_t(cgrp), phase = 0;
+            uint32_t wb = uint32_t(cgrp), wphase = 0;
+            for (int j = cgrp; j < iters; j += 2) {
+                uint32_t nsc[NSUB][G] = {}, nbs[NSUB][G] = {};
+                if (!staged && j + 2 < iters) fetch(j + 2, nsc, nbs);
+                const int t = first_tile + (j / nkb_t) * tile_step;
+                const int kb = kb0 + j % nkb_t;
+                const int n0 = (t % n_tiles) * tile_n;
+                if (!mbar_wait_warp(&full[stage], phase, abort_flag) ||
+                    !mbar_wait_warp(&wfree[wb], wphase ^ 1u, abort_flag)) {
+                    ok = false;
+                    break;
+                }
+                const uint8_t* raw = sR + stage * r_bytes;
+                uint8_t* wt = sB + wb * b_bytes;
+                if (staged) {  // this stage's scales (and biases) from shared memory
+                    const int xs = ((kb * BK) >> gsh) & ~(s_epb - 1);
+                    const uint8_t* ss = raw + codes_bytes;
+#pragma unroll
+                    for (int q = 0; q < NSUB; ++q) {
+                        const int r = ct + 64 * q;
+#pragma unroll
+                        for (int g = 0; g < G; ++g) {
+                            const int gi = ((kb * BK + g * SEG) >> gsh) - xs;
+                            if (AFF) {
+                                sc[q][g] = reinterpret_cast<const uint16_t*>(ss)[r * (Q_SROW / 2) + gi];
+                                bs[q][g] = reinterpret_cast<const uint16_t*>(ss + s_blk)[r * (Q_SROW / 2) + gi];
+                            } else {
+                                sc[q][g] = ss[r * Q_SROW + gi];
+                            }
+                        }
+                    }
+                }
+#pragma unroll
+                for (int q = 0; q < NSUB; ++q) {
+                    const int r = ct + 64 * q;
+                    const bool row_live = n0 + r < N;
+                    uint32_t cw[RW];
+#pragma unroll
+                    for (int i = 0; i < RW / 4; ++i) {
+                        const uint4 u = *reinterpret_cast<const uint4*>(raw + r * (RW * 4) + 16 * i);
+                        cw[4 * i] = u.x;
+                        cw[4 * i + 1] = u.y;
+                        cw[4 * i + 2] = u.z;
+                        cw[4 * i + 3] = u.w;
+                    }
+                    float scf[G], bsf[G];
+#pragma unroll
+                    for (int g = 0; g < G; ++g) {
+                        if (F == 0 || F == 2) scf[g] = dec_e8m0(sc[q][g]);
+                        else if (F == 1) scf[g] = dec_e4m3(sc[q][g]);
+                        else scf[g] = widen16(uint16_t(sc[q][g]), false);
+                        bsf[g] = AFF ? widen16(uint16_t(bs[q][g]), false) : 0.f;
+                    }
+                    uint8_t* wrow = wt + q * B_KB_BYTES + (ct >> 3) * 1024 + (ct & 7) * 128;
+#pragma unroll
+                    for (int p = 0; p < 8; ++p) {  // 8-column pieces (16 bytes of bf16)
+                        const bool live = row_live && kb * BK + 8 * p < K;  // K % 16 == 0
+                        uint4 pk;
+                        if (F == 0 || F == 1) {
+                            // FP4 E2M1 codes times the block scale, in bf16: every product
+                            // is exact in bf16 (or overflows), so bf16 arithmetic rounds
+                            // nothing
+                            uint32_t o[4];
+                            e2m1x8_to_bf16(cw[p], o);
+                            const uint32_t s2 = (__float_as_uint(scf[(8 * p) / SEG]) >> 16) * 0x10001u;
+                            pk.x = live ? mul_bf16x2(o[0], s2) : 0u;
+                            pk.y = live ? mul_bf16x2(o[1], s2) : 0u;
+                            pk.z = live ? mul_bf16x2(o[2], s2) : 0u;
+                            pk.w = live ? mul_bf16x2(o[3], s2) : 0u;
+                            *reinterpret_cast<uint4*>(wrow + ((p ^ (ct & 7)) << 4)) = pk;
+                            continue;
+                        }
+                        const float s = scf[(8 * p) / SEG], b = bsf[(8 * p) / SEG];
+                        float v[8];
+                        if (live) {
+                            if (F == 2) {  // FP8 E4M3 codes times the block scale
+#pragma unroll
+                                for (int e = 0; e < 4; ++e) {
+                                    const uint32_t pair = (cw[2 * p + (e >> 1)] >> (16 * (e & 1))) & 0xffffu;
+                                    const float2 f = h2_to_f2(cvt_e4m3x2(pair));
+                                    v[2 * e] = f.x * s;
+                                    v[2 * e + 1] = f.y * s;
+                                }
+                            } else if (F == 4) {  // affine 8-bit: fmaf(scale, q, bias)
+#pragma unroll
+                                for (int e = 0; e < 8; ++e)
+                                    v[e] = fmaf(s, byte_to_f32(cw[2 * p + (e >> 2)], e & 3), b);
+                            } else {  // affine 4-bit: nibbles spread to bytes first
+                                const uint32_t ev = cw[p] & 0x0f0f0f0fu, od = (cw[p] >> 4) & 0x0f0f0f0fu;
+#pragma unroll
+                                for (int e = 0; e < 8; ++e)
+                                    v[e] = fmaf(s, byte_to_f32(e & 1 ? od : ev, e >> 1), b);
+                            }
+                        } else {
+#pragma unroll
+                            for (int e = 0; e < 8; ++e) v[e] = 0.f;
+                        }
+                        pk.x = pack_bf16x2(v[0], v[1]);
+                        pk.y = pack_bf16x2(v[2], v[3]);
+                        pk.z = pack_bf16x2(v[4], v[5]);
+                        pk.w = pack_bf16x2(v[6], v[7]);
+                        *reinterpret_cast<uint4*>(wrow + ((p ^ (ct & 7)) << 4)) = pk;
+                    }
+                }
+                fence_proxy_async_smem();  // generic writes, read by the MMA (async proxy)
+                __syncwarp();
+                if (lane == 0) mbar_arrive(&conv[wb]);
+                stage += 2;  // S and wbufs are even: the group stays on its own stages
+                if (stage >= uint32_t(S)) {  // and buffers
+                    stage -= uint32_t(S);
+                    phase ^= 1u;
+                }
+                wb += 2;
+                if (wb >= uint32_t(args.wbufs)) {
+                    wb -= uint32_t(args.wbufs);
+                    wphase ^= 1u;
+                }
+#pragma unroll
+                for (int q = 0; q < NSUB; ++q)
+#pragma unroll
+                    for (int g = 0; g < G; ++g) {
+                        sc[q][g] = nsc[q][g];
+                        bs[q][g] = nbs[q][g];
+                    }
             }
-            fence_proxy_async_smem();  // generic writes, read by the MMA (async proxy)
-            __syncwarp();
-            if (lane == 0) mbar_arrive(&conv[stage]);
-            stage += 2;  // S is even: the group stays on its own stages
-            if (stage >= uint32_t(S)) {
-                stage -= uint32_t(S);
-                phase ^= 1u;
-            }
+        };
+        switch (args.qfmt) {
+            case 0: run(std::integral_constant<int, 0>{}); break;
+            case 1: run(std::integral_constant<int, 1>{}); break;
+            case 2: run(std::integral_constant<int, 2>{}); break;
+            case 3: run(std::integral_constant<int, 3>{}); break;
+            default: run(std::integral_constant<int, 4>{}); break;
         }
         if (!ok && lane == 0 && !*abort_flag) fail();
     }
@@ -719,7 +863,8 @@ cudaError_t launch_t(const DeviceInfo& dev, const CUtensorMap& mx, const CUtenso
         if (e != cudaSuccess) return e;
         attr_done[dev.device] = true;
     }
-    return launch_pdl(kern, dim3(grid), dim3(THREADS), SMEM_BYTES, s, mx, mw, a, dev.err_word);
+    return launch_pdl(kern, dim3(grid), dim3(THREADS), SMEM_BYTES, s, mx, mw, mw, mw, a,
+                      dev.err_word);
 }
 
 // The split-K kernel: clusters of a.splits CTAs, as many clusters as fit on the GPU at
@@ -760,12 +905,13 @@ cudaError_t launch_split(const DeviceInfo& dev, const CUtensorMap& mx, const CUt
     }
     const int clusters = int(tiles < n_fit ? tiles : n_fit);
     return launch_pdl_cluster(kern, dim3(unsigned(clusters * a.splits)), dim3(THREADS),
-                              SMEM_BYTES, s, unsigned(a.splits), mx, mw, a, dev.err_word);
+                              SMEM_BYTES, s, unsigned(a.splits), mx, mw, mw, mw, a, dev.err_word);
 }
 
 template <bool F32OUT, int NSUB>
 cudaError_t launch_q(const DeviceInfo& dev, const CUtensorMap& mx, const CUtensorMap& mw,
-                     const GemmArgs& a, int grid, cudaStream_t s) {
+                     const CUtensorMap& ms, const CUtensorMap& mb, const GemmArgs& a, int grid,
+                     cudaStream_t s) {
     auto kern = gemm_kernel<false, F32OUT, NSUB, false, 1, true>;
     static bool attr_done[64] = {};
     if (dev.device >= 0 && dev.device < 64 && !attr_done[dev.device]) {
@@ -774,7 +920,8 @@ cudaError_t launch_q(const DeviceInfo& dev, const CUtensorMap& mx, const CUtenso
         if (e != cudaSuccess) return e;
         attr_done[dev.device] = true;
     }
-    return launch_pdl(kern, dim3(grid), dim3(QTHREADS), SMEM_BYTES, s, mx, mw, a, dev.err_word);
+    return launch_pdl(kern, dim3(grid), dim3(QTHREADS), SMEM_BYTES, s, mx, mw, ms, mb, a,
+                      dev.err_word);
 }
 
 template <bool KN, bool F32OUT>
@@ -863,7 +1010,8 @@ GemmSchedule gemm_schedule(int64_t M, int64_t N, int64_t K, bool w_kn, int num_s
 
 cudaError_t launch_gemm(const DeviceInfo& dev, const void* x, int64_t ldx, const void* w,
                         int64_t ldw, bool w_kn, void* y, int64_t ldy, bool y_f32, int64_t M,
-                        int64_t N, int64_t K, bool split_ok, bool f16, cudaStream_t stream) {
+                        int64_t N, int64_t K, bool split_ok, bool f16, bool w_early,
+                        cudaStream_t stream) {
     if (M == 0 || N == 0) return cudaSuccess;
     if (K == 0) {
         // an empty reduction: every output is +0 (all-zero bits in bf16, binary16 and fp32)
@@ -898,7 +1046,7 @@ cudaError_t launch_gemm(const DeviceInfo& dev, const void* x, int64_t ldx, const
         ok = tmap_2d_bf16(&mw, w, uint64_t(K), uint64_t(N), uint64_t(ldw), BK,
                           uint32_t(g.nsub * BN), 128, f16);
     if (!ok) return cudaErrorNotSupported;
-    GemmArgs a;
+    GemmArgs a{};
     a.y = y;
     a.ldy = ldy;
     a.M = int(M);
@@ -910,6 +1058,7 @@ cudaError_t launch_gemm(const DeviceInfo& dev, const void* x, int64_t ldx, const
     a.blocked = g.blocked;
     a.stages = g.stages;
     a.w_stream_once = (M + BM - 1) / BM == 1 ? 1 : 0;
+    a.w_early = w_early ? 1 : 0;
     a.splits = g.splits;
     a.kb_per_split = g.kb_per_split;
     a.f16 = f16 ? 1 : 0;
@@ -929,7 +1078,7 @@ cudaError_t launch_gemm(const DeviceInfo& dev, const void* x, int64_t ldx, const
 cudaError_t launch_qgemm(const DeviceInfo& dev, const void* x, int64_t ldx, const void* wq,
                          int64_t ldq, const void* scales, int64_t lds, const void* biases,
                          int64_t ldb, int fmt, int gs, void* y, int64_t ldy, bool y_f32,
-                         int64_t M, int64_t N, int64_t K, cudaStream_t stream) {
+                         int64_t M, int64_t N, int64_t K, bool w_early, cudaStream_t stream) {
     if (M == 0 || N == 0) return cudaSuccess;
     if (K == 0) {
         const size_t es = y_f32 ? 4 : 2;
@@ -945,14 +1094,45 @@ cudaError_t launch_qgemm(const DeviceInfo& dev, const void* x, int64_t ldx, cons
             break;
         }
     }
-    const int64_t blk = int64_t(a_rows) * BK * 2 + int64_t(nsub) * (B_KB_BYTES + Q_RAW_KB_BYTES);
-    int stages = int(RING_BYTES / blk);
-    if (stages > MAX_QSTAGES) stages = MAX_QSTAGES;
-    stages &= ~1;  // even: each of the two converter groups owns every other stage
-    if (stages < 2 || int64_t(stages - 1) * a_rows * BK * 2 + A_MMA_BYTES > int64_t(stages) * blk)
-        return cudaErrorNotSupported;
     const bool eight = fmt == 2 || fmt == 4;
+    const bool aff = fmt >= 3;
     const int q_kb_bytes = eight ? BK : BK / 2;
+    // Scales (and biases) travel with the codes, by TMA, when their rows start on 16-byte
+    // boundaries (a tensor map's rule); else the converters load them themselves.
+    CUtensorMap ms, mb;
+    const int64_t groups = K / gs;
+    bool staged = false;
+    if (reinterpret_cast<uintptr_t>(scales) % 16 == 0 && (lds * (aff ? 2 : 1)) % 16 == 0 &&
+        (!aff || (reinterpret_cast<uintptr_t>(biases) % 16 == 0 && (ldb * 2) % 16 == 0))) {
+        staged = aff ? tmap_2d_u16(&ms, scales, uint64_t(groups), uint64_t(N), uint64_t(lds * 2),
+                                   Q_SROW / 2, uint32_t(nsub * BN)) &&
+                           tmap_2d_u16(&mb, biases, uint64_t(groups), uint64_t(N),
+                                       uint64_t(ldb * 2), Q_SROW / 2, uint32_t(nsub * BN))
+                     : tmap_2d_u8(&ms, scales, uint64_t(groups), uint64_t(N), uint64_t(lds),
+                                  Q_SROW, uint32_t(nsub * BN));
+    }
+    // the ring's stages hold an X block and a packed-code block (and the staged scales);
+    // the bf16 tiles the converters write get their own buffers: four when the ring can
+    // still be four stages deep, else two
+    const int64_t a_bytes = int64_t(a_rows) * BK * 2;
+    const int64_t blk = a_bytes + int64_t(nsub) * 64 * q_kb_bytes +
+                        (staged ? (aff ? 2 : 1) * int64_t(nsub) * 64 * Q_SROW : 0);
+    const int64_t b_bytes = int64_t(nsub) * B_KB_BYTES;
+    int wbufs = 0, stages = 0;
+    for (int wb = MAX_QWBUF; wb >= 2; wb -= 2) {
+        int st = int((RING_BYTES - wb * b_bytes) / blk);
+        if (st > MAX_QSTAGES) st = MAX_QSTAGES;
+        st &= ~1;  // even: each of the two converter groups owns every other stage
+        if (st >= 4 || (wb == 2 && st >= 2)) {
+            wbufs = wb;
+            stages = st;
+            break;
+        }
+    }
+    // an MMA reads A_MMA_BYTES from the start of its X block: the last block's read runs
+    // into the tile buffers that follow the X blocks and must stay inside the ring
+    if (wbufs == 0 || (stages - 1) * a_bytes + A_MMA_BYTES > stages * a_bytes + wbufs * b_bytes)
+        return cudaErrorNotSupported;
     CUtensorMap mx, mw;
     if (!tmap_2d_bf16(&mx, x, uint64_t(K), uint64_t(M), uint64_t(ldx), BK, uint32_t(a_rows), 128) ||
         !tmap_2d_u8(&mw, wq, uint64_t(eight ? K : K / 2), uint64_t(N), uint64_t(ldq),
@@ -970,6 +1150,7 @@ cudaError_t launch_qgemm(const DeviceInfo& dev, const void* x, int64_t ldx, cons
     a.blocked = 0;
     a.stages = stages;
     a.w_stream_once = m_tiles == 1 ? 1 : 0;
+    a.w_early = w_early ? 1 : 0;
     a.splits = 1;
     a.kb_per_split = int((K + BK - 1) / BK);
     a.f16 = 0;
@@ -980,15 +1161,19 @@ cudaError_t launch_qgemm(const DeviceInfo& dev, const void* x, int64_t ldx, cons
     a.qbiases = static_cast<const uint16_t*>(biases);
     a.ldb = ldb;
     a.q_kb_bytes = q_kb_bytes;
+    a.wbufs = wbufs;
+    a.q_staged = staged ? 1 : 0;
+    if (!staged) ms = mb = mw;  // unused
+    else if (!aff) mb = ms;
     const int64_t tiles = m_tiles * ((N + int64_t(nsub) * BN - 1) / (int64_t(nsub) * BN));
     const int grid = int(tiles < dev.num_sms ? tiles : dev.num_sms);
     switch (nsub) {
-        case 1: return y_f32 ? launch_q<true, 1>(dev, mx, mw, a, grid, stream)
-                             : launch_q<false, 1>(dev, mx, mw, a, grid, stream);
-        case 2: return y_f32 ? launch_q<true, (MAX_NSUB >= 2 ? 2 : 1)>(dev, mx, mw, a, grid, stream)
-                             : launch_q<false, (MAX_NSUB >= 2 ? 2 : 1)>(dev, mx, mw, a, grid, stream);
-        default: return y_f32 ? launch_q<true, MAX_NSUB>(dev, mx, mw, a, grid, stream)
-                              : launch_q<false, MAX_NSUB>(dev, mx, mw, a, grid, stream);
+        case 1: return y_f32 ? launch_q<true, 1>(dev, mx, mw, ms, mb, a, grid, stream)
+                             : launch_q<false, 1>(dev, mx, mw, ms, mb, a, grid, stream);
+        case 2: return y_f32 ? launch_q<true, (MAX_NSUB >= 2 ? 2 : 1)>(dev, mx, mw, ms, mb, a, grid, stream)
+                             : launch_q<false, (MAX_NSUB >= 2 ? 2 : 1)>(dev, mx, mw, ms, mb, a, grid, stream);
+        default: return y_f32 ? launch_q<true, MAX_NSUB>(dev, mx, mw, ms, mb, a, grid, stream)
+                              : launch_q<false, MAX_NSUB>(dev, mx, mw, ms, mb, a, grid, stream);
     }
 }
 

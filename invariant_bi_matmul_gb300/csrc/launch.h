@@ -73,10 +73,12 @@ cudaError_t launch_rmsnorm(const void* x, int64_t ldx, const void* gamma, void* 
                            cudaStream_t stream);
 
 // ------------------------------------------------------------------- GEMM (gemm.cu)
-// Returns cudaErrorNotSupported when a TMA descriptor cannot be encoded.
+// Returns cudaErrorNotSupported when a TMA descriptor cannot be encoded.  w_early: W
+// may be read before the previous grid in the stream has finished (it does not write W).
 cudaError_t launch_gemm(const DeviceInfo& dev, const void* x, int64_t ldx, const void* w,
                         int64_t ldw, bool w_kn, void* y, int64_t ldy, bool y_f32, int64_t M,
-                        int64_t N, int64_t K, bool split_ok, bool f16, cudaStream_t stream);
+                        int64_t N, int64_t K, bool split_ok, bool f16, bool w_early,
+                        cudaStream_t stream);
 int gemm_tile_n();
 
 // Quantized W (gemm.cu): bf16 X times W decoded from packed codes (format 0 mxfp4,
@@ -85,7 +87,7 @@ int gemm_tile_n();
 cudaError_t launch_qgemm(const DeviceInfo& dev, const void* x, int64_t ldx, const void* wq,
                          int64_t ldq, const void* scales, int64_t lds, const void* biases,
                          int64_t ldb, int fmt, int gs, void* y, int64_t ldy, bool y_f32,
-                         int64_t M, int64_t N, int64_t K, cudaStream_t stream);
+                         int64_t M, int64_t N, int64_t K, bool w_early, cudaStream_t stream);
 
 // fp32 inputs (f32path.cu): CUDA-core matmul, one ascending fmaf chain per element, and
 // RMSNorm with the 16-bit kernel's tree.  y fp32.

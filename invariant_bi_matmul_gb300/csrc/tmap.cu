@@ -106,19 +106,35 @@ bool tmap_bf16_impl(CUtensorMap* out, const void* ptr, uint64_t inner, uint64_t 
 
 }  // namespace
 
-bool tmap_2d_u8(CUtensorMap* out, const void* ptr, uint64_t inner_bytes, uint64_t outer,
-                uint64_t stride_bytes, uint32_t box_inner, uint32_t box_outer) {
-    // (encoded on every call: one driver call, no cache)
+namespace {
+
+// (encoded on every call: one driver call, no cache)
+bool tmap_2d_plain(CUtensorMap* out, CUtensorMapDataType type, const void* ptr, uint64_t inner,
+                   uint64_t outer, uint64_t stride_bytes, uint32_t box_inner, uint32_t box_outer) {
     EncodeTiledFn fn = encode_fn();
     if (!fn) return false;
-    const cuuint64_t dims[2] = {inner_bytes, outer};
+    const cuuint64_t dims[2] = {inner, outer};
     const cuuint64_t strides[1] = {stride_bytes};
     const cuuint32_t box[2] = {box_inner, box_outer};
     const cuuint32_t estr[2] = {1, 1};
-    return fn(out, CU_TENSOR_MAP_DATA_TYPE_UINT8, 2, const_cast<void*>(ptr), dims, strides, box,
-              estr, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_NONE,
+    return fn(out, type, 2, const_cast<void*>(ptr), dims, strides, box, estr,
+              CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_NONE,
               CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) ==
            CUDA_SUCCESS;
+}
+
+}  // namespace
+
+bool tmap_2d_u8(CUtensorMap* out, const void* ptr, uint64_t inner_bytes, uint64_t outer,
+                uint64_t stride_bytes, uint32_t box_inner, uint32_t box_outer) {
+    return tmap_2d_plain(out, CU_TENSOR_MAP_DATA_TYPE_UINT8, ptr, inner_bytes, outer,
+                         stride_bytes, box_inner, box_outer);
+}
+
+bool tmap_2d_u16(CUtensorMap* out, const void* ptr, uint64_t inner, uint64_t outer,
+                 uint64_t stride_bytes, uint32_t box_inner, uint32_t box_outer) {
+    return tmap_2d_plain(out, CU_TENSOR_MAP_DATA_TYPE_UINT16, ptr, inner, outer, stride_bytes,
+                         box_inner, box_outer);
 }
 
 bool tmap_2d_bf16(CUtensorMap* out, const void* ptr, uint64_t inner, uint64_t outer,

@@ -26,5 +26,8 @@ bool tmap_kblocked_bf16(CUtensorMap* out, const void* ptr, uint64_t inner, uint6
 // box_inner bytes x box_outer rows, no swizzle; bytes outside the tensor read as 0.
 bool tmap_2d_u8(CUtensorMap* out, const void* ptr, uint64_t inner_bytes, uint64_t outer,
                 uint64_t stride_bytes, uint32_t box_inner, uint32_t box_outer);
+// The same for 16-bit elements (inner and box_inner in elements).
+bool tmap_2d_u16(CUtensorMap* out, const void* ptr, uint64_t inner, uint64_t outer,
+                 uint64_t stride_bytes, uint32_t box_inner, uint32_t box_outer);
 
 }  // namespace bi

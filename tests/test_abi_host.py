@@ -71,6 +71,20 @@ def test_limit_set_get_and_reject_negative(L):
         L.bi_set_batch_invariant_limit(old)
 
 
+def test_weight_prefetch_set_get_and_reject_other_values(L):
+    old = L.bi_get_weight_prefetch()
+    try:
+        assert old == 0                                        # off unless asked for
+        assert L.bi_set_weight_prefetch(1) == bi.BI_OK
+        assert L.bi_get_weight_prefetch() == 1
+        assert L.bi_set_weight_prefetch(2) == bi.BI_ERR_INVALID_ARG
+        assert L.bi_get_weight_prefetch() == 1                 # unchanged
+        assert L.bi_set_weight_prefetch(0) == bi.BI_OK
+        assert L.bi_get_weight_prefetch() == 0
+    finally:
+        L.bi_set_weight_prefetch(old)
+
+
 @pytest.mark.parametrize("env,want", [("12", 12), ("0", 0), ("-3", 0), ("abc", 0), (None, 0)])
 def test_limit_initial_value_from_environment(env, want):
     code = ("import invariant_bi_matmul_gb300 as bi; "

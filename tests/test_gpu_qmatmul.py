@@ -114,3 +114,92 @@ def test_qmatmul_repeat_and_guard_bands(dev):
     assert len(seen) == 1
     assert torch.all(buf[0] == 7.0) and torch.all(buf[M + 1] == 7.0)
     assert torch.all(buf[1:M + 1, N:] == 7.0)
+
+
+def _same_or_both_nan(a, b):
+    """Bitwise equality of two fp32 tensors, any NaN matching any NaN."""
+    a, b = a.contiguous().cpu(), b.contiguous().cpu()
+    same = a.view(torch.int32) == b.view(torch.int32)
+    return bool(torch.all(same | (torch.isnan(a) & torch.isnan(b))))
+
+
+def _block_enumeration(fmt, gs, K):
+    """Every (scale code, element code) pair of a block format, one pair per W row: the
+    row's only nonzero code sits at column (37 n) mod K, its group takes the scale code
+    under test and the other groups the code of 1.0."""
+    eight = fmt == "mxfp8"
+    ncode = 256 if eight else 16
+    N = 256 * ncode
+    n = np.arange(N)
+    kpos = (n * 37) % K
+    codes = np.zeros((N, K), np.uint8)
+    codes[n, kpos] = (n % ncode).astype(np.uint8)
+    scales = np.full((N, K // gs), 0x38 if fmt == "nvfp4" else 127, np.uint8)
+    scales[n, kpos // gs] = (n // ncode).astype(np.uint8)
+    wq = codes if eight else (codes[:, 0::2] | (codes[:, 1::2] << 4)).astype(np.uint8)
+    return wq, scales, None, N
+
+
+def _affine_enumeration(fmt, gs, K, seed):
+    """Affine codes drawn uniformly with bf16 scales and biases of random sign, mantissa
+    and exponent field 0 .. 0xE0 (subnormals included; no overflow)."""
+    rng = np.random.default_rng(seed)
+    N = 2048
+    nb = K if fmt == "affine8" else K // 2
+    wq = rng.integers(0, 256, (N, nb), dtype=np.uint8)
+
+    def bf16_bits(shape):
+        return ((rng.integers(0, 2, shape) << 15) | (rng.integers(0, 0xE1, shape) << 7)
+                | rng.integers(0, 128, shape)).astype(np.uint16)
+    return wq, bf16_bits((N, K // gs)), bf16_bits((N, K // gs)), N
+
+
+def _padded(a, row_bytes=16):
+    """The same values in rows of row_bytes bytes (scales whose rows start on 16-byte
+    boundaries travel with the codes by TMA; others are loaded by the converters)."""
+    out = np.zeros((a.shape[0], max(row_bytes // a.itemsize, a.shape[1])), a.dtype)
+    out[:, :a.shape[1]] = a
+    return out
+
+
+@pytest.mark.parametrize("pad", [False, True])
+@pytest.mark.parametrize("fmt,gs,K", [("mxfp4", 32, 64), ("nvfp4", 16, 64), ("mxfp8", 32, 64),
+                                      ("affine4", 32, 64), ("affine4", 128, 128),
+                                      ("affine8", 64, 64)])
+def test_qmatmul_dequantizes_every_code_exactly(dev, fmt, gs, K, pad):
+    """Identity X reads the dequantized W back out of Y (each Y element is one product
+    W x 1 plus products with 0): every E2M1 / E4M3 code under every E8M0 / E4M3 scale
+    code (NaN scales, overflow to infinity and subnormal results included) and affine
+    codes under scales and biases of every exponent.  Y equals bi_matmul on the oracle's
+    dequantized W bit for bit everywhere, and equals the oracle's values wherever the
+    row holds no infinity or NaN and the value is zero or normal (whether the tensor
+    cores keep subnormal inputs is theirs to decide, the same on both paths)."""
+    q = inputs.Q_NAMES[fmt]
+    if fmt.startswith("affine"):
+        wq, sc, b, N = _affine_enumeration(fmt, gs, K, seed=K + gs)
+    else:
+        wq, sc, b, N = _block_enumeration(fmt, gs, K)
+    wd = oracle.dequantize(wq, sc, b, q, gs, N, K)  # bf16 bits [N, K]
+    x = torch.eye(K, dtype=torch.bfloat16, device=dev)
+    to_dev = lambda a: torch.from_numpy(a.view(np.int16) if a.dtype == np.uint16 else a).to(dev)
+    ng = K // gs
+    sct = to_dev(_padded(sc) if pad else sc)[:, :ng]
+    if b is not None:
+        sct = sct.view(torch.bfloat16)
+    bt = None if b is None else to_dev(_padded(b) if pad else b)[:, :ng].view(torch.bfloat16)
+    yq = bi.qmatmul(x, to_dev(wq), sct, fmt, gs, K, biases=bt, out_dtype=torch.float32)
+    wdt = torch.from_numpy(wd.view(np.int16)).view(torch.bfloat16).to(dev)
+    yd = bi.matmul(x, wdt, "nk", out_dtype=torch.float32)
+    assert _same_or_both_nan(yq, yd), f"{fmt}: quantized and dense paths differ"
+    wv = (wd.astype(np.uint32) << 16).view(np.float32)         # [N, K]
+    y = yd.cpu().numpy()                                       # [K, N]
+    row_finite = np.all(np.isfinite(wv), axis=1)
+    plain = (np.abs(wv) >= np.float32(2.0 ** -126)) | (wv == 0)
+    mask = row_finite[None, :] & plain.T
+    assert np.array_equal(y[mask], wv.T[mask]), f"{fmt}: values differ from the oracle"
+    assert np.all(np.isnan(y[np.isnan(wv).T])), f"{fmt}: NaN weights lost"
+    lone_inf = np.isinf(wv).T & (np.sum(~np.isfinite(wv), axis=1) == 1)[None, :]
+    assert np.array_equal(y[lone_inf], wv.T[lone_inf]), f"{fmt}: infinite weights differ"
+    if not fmt.startswith("affine"):  # the enumeration reached every kind of value
+        assert mask.sum() > 0 and np.isnan(wv).sum() > 0
+        assert (lone_inf.sum() > 0) == (fmt != "nvfp4")  # 6 x 448 stays finite
