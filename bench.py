@@ -254,6 +254,9 @@ def run_gpu(args, rank, world, local_rank):
     dev = torch.device(f"cuda:{local_rank}")
     torch.cuda.set_device(dev)
     bi.set_batch_invariant_limit(M_TOK)
+    # the weights are fixed for the whole run and no kernel writes them: matmuls may start
+    # streaming them while the previous kernel finishes
+    bi.set_weight_prefetch(True)
     st = Step(dev)
     calls = st.calls()
     names = [n for n, _ in calls]
@@ -572,6 +575,7 @@ def run_case(spec: str, reps: int):
     parts = spec.split(":")
     fast = "fast" in parts[1:]
     bi.set_batch_invariant_limit(0 if fast else 1 << 40)
+    bi.set_weight_prefetch(True)  # fixed weights
     dev = torch.device("cuda:0")
     flush = torch.ones(128 * 1024 * 1024, dtype=torch.float32, device=dev)
     if parts[0] == "gemm":
@@ -633,6 +637,7 @@ def run_sweep():
     from invariant_bi_matmul_gb300 import inputs
     peaks, peak_kind = load_peaks()
     dev = torch.device("cuda:0")
+    bi.set_weight_prefetch(True)  # every timed weight is fixed
     # evict L2 by READING a buffer 4x its size (a write-based flush would leave dirty lines
     # whose write-back then competes with the timed kernel's reads)
     flush = torch.ones(128 * 1024 * 1024, dtype=torch.float32, device=dev)
