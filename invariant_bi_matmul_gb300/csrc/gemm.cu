@@ -429,11 +429,11 @@ gemm_kernel(const __grid_constant__ CUtensorMap tmap_x, const __grid_constant__ 
     } else if (warp == 1) {
         // ---------------------------------------------------------------- MMA issuer
         // The whole warp runs the loop; one elected lane issues the MMAs and commits.
-        // K-major W: the tile's NSUB*BN rows are contiguous (8-row groups 1024 B apart), so
-        // one instruction of N = NSUB*BN covers every sub-tile and reads each X block once
-        // per k16 step.  N-major W: one instruction per swizzle atom column.
-        const uint32_t idesc = umma_idesc_bf16(BM, KN ? BN : NSUB * BN, 0, KN ? 1 : 0,
-                                               args.f16 != 0);
+        // One instruction of N = NSUB*BN covers every sub-tile and reads each X block once
+        // per k16 step.  K-major W: the tile's rows are contiguous (8-row groups 1024 B
+        // apart); N-major W: its swizzle-atom columns sit the descriptor's leading-byte
+        // offset apart.
+        const uint32_t idesc = umma_idesc_bf16(BM, NSUB * BN, 0, KN ? 1 : 0, args.f16 != 0);
         // X: K-major, 128-byte swizzle, 8-row groups 1024 B apart; +32 B per k16 step
         const uint64_t a_desc0 = umma_smem_desc(smem_addr(sA), 16, 1024, 2);
         // W, layout NK: K-major like X.  Layout KN: N-major; k-rows of KN_SWIZZLE bytes,
@@ -448,8 +448,6 @@ gemm_kernel(const __grid_constant__ CUtensorMap tmap_x, const __grid_constant__ 
         constexpr int B_K16 = KN ? (UK * KN_SWIZZLE) >> 4 : (UK * 2) >> 4;
         const uint64_t a_step = uint64_t(a_bytes >> 4);
         const uint64_t b_step = uint64_t((KN ? KN_ATOM_BYTES : b_bytes) >> 4);
-        const uint64_t b_sub = uint64_t(KN ? ((BN / KN_ATOM_N) * kbs * KN_ATOM_BYTES) >> 4
-                                           : B_KB_BYTES >> 4);
         const uint32_t stage_a = uint32_t(kbs * a_bytes), stage_b = uint32_t(kbs * b_bytes);
         const uint32_t empty_s = smem_addr(empty);
         uint32_t stage = 0, phase = 0;
@@ -490,15 +488,7 @@ gemm_kernel(const __grid_constant__ CUtensorMap tmap_x, const __grid_constant__ 
                                                         uint64_t(ms * (A_MMA_BYTES >> 4));
                                 uint64_t b_desc = b_blk + uint64_t(k * B_K16);
                                 uint32_t d = d_tmem + uint32_t(ms * NSUB * BN);
-                                if constexpr (!KN) {
-                                    tc_mma_bf16(d, a_desc, b_desc, idesc,
-                                                (first && k == 0) ? 0u : 1u);
-                                } else {
-#pragma unroll
-                                    for (int j = 0; j < NSUB; ++j, b_desc += b_sub, d += uint32_t(BN))
-                                        tc_mma_bf16(d, a_desc, b_desc, idesc,
-                                                    (first && k == 0) ? 0u : 1u);
-                                }
+                                tc_mma_bf16(d, a_desc, b_desc, idesc, (first && k == 0) ? 0u : 1u);
                             }
                         }
                     }
