@@ -947,21 +947,32 @@ GemmSchedule gemm_schedule(int64_t M, int64_t N, int64_t K, bool w_kn, int num_s
     const int64_t m_tiles = (M + BM - 1) / BM;
     const int64_t nkb = (K + BK - 1) / BK;
     g.a_rows = m_tiles == 1 ? int((M + 7) / 8 * 8) : BM;
-    // widest CTA tile that still gives every SM a tile (X is then re-read from L2 the
-    // fewest times); a single instruction tile per CTA when even that is too few
-    g.nsub = 1;
-    for (int ns = MAX_NSUB; ns >= 2; ns >>= 1) {
-        if (m_tiles * ((N + int64_t(ns) * BN - 1) / (int64_t(ns) * BN)) >= num_sms) {
-            g.nsub = ns;
-            break;
+    // CTA tile shape from a cost model: per K-block a CTA spends the longer of its MMAs
+    // (about 8192 flop per cycle per SM) and its operand copies (about 64 bytes per cycle
+    // per SM from L2), and the tiles run in ceil(tiles / SMs) waves.  Candidates: 128 x
+    // 64*nsub (nsub 1, 2, 4) and 256 x 256 (two instruction tiles along M); the widest
+    // wins ties (X and W are re-read from L2 the fewest times).  The instructions and
+    // their K order are the same for every shape.
+    const int single_rows = g.a_rows;
+    double best = 0.0;
+    bool wide_m = false;
+    for (int msub = 2; msub >= 1; --msub) {
+        for (int ns = MAX_NSUB; ns >= 1; ns >>= 1) {
+            if (msub == 2 && (ns != 4 || m_tiles < 2)) continue;
+            const int64_t tm = int64_t(BM) * msub;
+            const int64_t tiles = ((M + tm - 1) / tm) * ((N + int64_t(ns) * BN - 1) / (int64_t(ns) * BN));
+            const int64_t waves = (tiles + num_sms - 1) / num_sms;
+            const int64_t rows = msub == 2 ? tm : (m_tiles == 1 ? single_rows : BM);
+            const double mma = double(msub) * ns * BM * BN * BK * 2 / 8192.0;
+            const double copy = (double(rows) * BK * 2 + double(ns) * B_KB_BYTES) / 64.0;
+            const double cost = double(waves) * double(nkb) * (mma > copy ? mma : copy);
+            if (best == 0.0 || cost < best) {
+                best = cost;
+                g.nsub = ns;
+                wide_m = msub == 2;
+            }
         }
     }
-    // Large M: 256 x 256 CTA tiles (two instruction tiles along M, four along N) carry
-    // 2 KB of operands per instruction instead of 3 KB, when they still give at least
-    // three quarters of the SMs a tile.  The instructions and their K order are those of
-    // every other tile shape.
-    const int64_t tiles_256 = ((M + 2 * BM - 1) / (2 * BM)) * ((N + 255) / 256);
-    const bool wide_m = MAX_NSUB >= 4 && g.nsub == 4 && 4 * tiles_256 >= 3 * num_sms;
     if (wide_m) g.a_rows = 2 * BM;
     // Split-K (non-invariant kernel only): a single M-tile whose instruction tiles leave
     // SMs idle gets a cluster of CTAs per tile, each over a contiguous K range, so more
