@@ -140,6 +140,28 @@ def test_matmul_parity_256_row_tiles_ragged(dev, layout):
         assert bits_equal(alone, y[i:i + 1])
 
 
+@pytest.mark.parametrize("layout", ["nk", "kn"])
+@pytest.mark.parametrize("M,N,K", [(300, 904, 1000), (512, 4096, 4096), (96, 2000, 520)])
+def test_matmul_mid_m_ragged_guard_bands(dev, layout, M, N, K):
+    """Mid-size M (the tile-shape cost model's narrow and 128-wide CTA tiles), N not a
+    multiple of the CTA tile and ragged K: sampled rows against the oracle, rows bitwise
+    equal to the row computed alone, nothing written outside Y."""
+    gi = inputs.gemm_inputs(M, N, K, seed=M + N)
+    w = (gi.w_nk if layout == "nk" else gi.w_kn).to(dev)
+    buf = torch.full((M + 2, N + 8), 7.0, dtype=torch.bfloat16, device=dev)
+    out = buf[1:M + 1, :N]
+    bi.matmul(gi.x.to(dev), w, layout, out=out)
+    y = out.cpu()
+    rows = sorted({0, 63, 64, M // 2, M - 1})
+    ref = oracle.matmul(inputs.bf16_bits(gi.x[rows]), inputs.bf16_bits(gi.w_nk), oracle.W_NK)
+    check_bf16(y[rows], ref, f"mid-M {M}x{N}x{K} {layout}")
+    for i in (0, M - 1):
+        alone = bi.matmul(gi.x[i:i + 1].to(dev), w, layout).cpu()
+        assert bits_equal(alone, y[i:i + 1]), f"row {i} differs alone"
+    assert torch.all(buf[0] == 7.0) and torch.all(buf[M + 1] == 7.0)
+    assert torch.all(buf[1:M + 1, N:] == 7.0)
+
+
 def test_matmul_permutation_and_repeat(dev):
     M, N, K = 300, 512, 1024
     gi = inputs.gemm_inputs(M, N, K, seed=41)
