@@ -51,7 +51,7 @@ namespace bi {
 namespace {
 
 #ifndef BI_GEMM_BN
-#define BI_GEMM_BN 64
+#define BI_GEMM_BN 32
 #endif
 
 constexpr int BM = 128;                     // instruction M: token rows
@@ -84,7 +84,7 @@ constexpr int KN_ATOM_BYTES = KN_ATOM_N * 2 * BK;  // one atom column of a K-blo
 constexpr int KN_SWIZZLE = KN_ATOM_N * 2;          // 64 or 128 bytes
 constexpr uint32_t KN_LAYOUT = KN_SWIZZLE == 128 ? 2u : 4u;
 
-static_assert(BN == 32 || BN == 64 || BN == 128, "instruction N must be 32, 64 or 128");
+static_assert(BN == 32 || BN == 64, "instruction sub-tile N must be 32 or 64");
 static_assert((2 * MAX_STAGES + 7 + 2 * MAX_QWBUF) * 8 + 16 <= CTRL_BYTES,
               "control block too small");
 
@@ -211,8 +211,8 @@ gemm_kernel(const __grid_constant__ CUtensorMap tmap_x, const __grid_constant__ 
     uint8_t* sR = sB + (QUANT ? args.wbufs : S * kbs) * b_bytes;  // QUANT: S code blocks
     // QUANT stage: the packed codes, then (staged) a block of scales and, affine, biases
     const bool q_aff = args.qfmt >= 3;
-    const int codes_bytes = nsub * 64 * args.q_kb_bytes;
-    const int s_blk = nsub * 64 * Q_SROW;
+    const int codes_bytes = nsub * BN * args.q_kb_bytes;
+    const int s_blk = nsub * BN * Q_SROW;
     const int r_bytes = codes_bytes + (args.q_staged ? (q_aff ? 2 : 1) * s_blk : 0);
     const int gsh = QUANT ? 31 - __clz(args.gs) : 0;  // the group size is a power of two
     const int s_epb = q_aff ? Q_SROW / 2 : Q_SROW;     // staged elements per row
@@ -660,6 +660,8 @@ gemm_kernel(const __grid_constant__ CUtensorMap tmap_x, const __grid_constant__ 
         // columns past K become zeros.
         const int cgrp = (warp - 6) >> 1;
         const int ct = ((warp - 6) & 1) * 32 + lane;
+        // the tile's rows in units of 64 (a quantized tile is 64, 128 or 256 rows)
+        constexpr int QR = NSUB * BN >= 64 ? NSUB * BN / 64 : 1;
         const uint8_t* qs8 = static_cast<const uint8_t*>(args.qscales);
         const uint16_t* qs16 = static_cast<const uint16_t*>(args.qscales);
         const int nkb_t = kb1 - kb0;
@@ -677,12 +679,12 @@ gemm_kernel(const __grid_constant__ CUtensorMap tmap_x, const __grid_constant__ 
             constexpr int SEG = BK / G;        // columns per segment (<= the group size)
             constexpr int RW = (F == 2 || F == 4) ? BK / 4 : BK / 8;  // code words per row
             // raw scale (and bias) codes of iteration j's rows, one per segment
-            auto fetch = [&](int j, uint32_t (&sc)[NSUB][G], uint32_t (&bs)[NSUB][G]) {
+            auto fetch = [&](int j, uint32_t (&sc)[QR][G], uint32_t (&bs)[QR][G]) {
                 const int t = first_tile + (j / nkb_t) * tile_step;
                 const int kb = kb0 + j % nkb_t;
                 const int n0 = (t % n_tiles) * tile_n;
 #pragma unroll
-                for (int q = 0; q < NSUB; ++q) {
+                for (int q = 0; q < QR; ++q) {
                     const int n = n0 + ct + 64 * q;
 #pragma unroll
                     for (int g = 0; g < G; ++g) {
@@ -701,12 +703,12 @@ gemm_kernel(const __grid_constant__ CUtensorMap tmap_x, const __grid_constant__ 
                     }
                 }
             };
-            uint32_t sc[NSUB][G] = {}, bs[NSUB][G] = {};
+            uint32_t sc[QR][G] = {}, bs[QR][G] = {};
             if (!staged && cgrp < iters) fetch(cgrp, sc, bs);
             uint32_t stage = uint32_t(cgrp), phase = 0;
             uint32_t wb = uint32_t(cgrp), wphase = 0;
             for (int j = cgrp; j < iters; j += 2) {
-                uint32_t nsc[NSUB][G] = {}, nbs[NSUB][G] = {};
+                uint32_t nsc[QR][G] = {}, nbs[QR][G] = {};
                 if (!staged && j + 2 < iters) fetch(j + 2, nsc, nbs);
                 const int t = first_tile + (j / nkb_t) * tile_step;
                 const int kb = kb0 + j % nkb_t;
@@ -722,7 +724,7 @@ gemm_kernel(const __grid_constant__ CUtensorMap tmap_x, const __grid_constant__ 
                     const int xs = ((kb * BK) >> gsh) & ~(s_epb - 1);
                     const uint8_t* ss = raw + codes_bytes;
 #pragma unroll
-                    for (int q = 0; q < NSUB; ++q) {
+                    for (int q = 0; q < QR; ++q) {
                         const int r = ct + 64 * q;
 #pragma unroll
                         for (int g = 0; g < G; ++g) {
@@ -737,7 +739,7 @@ gemm_kernel(const __grid_constant__ CUtensorMap tmap_x, const __grid_constant__ 
                     }
                 }
 #pragma unroll
-                for (int q = 0; q < NSUB; ++q) {
+                for (int q = 0; q < QR; ++q) {
                     const int r = ct + 64 * q;
                     const bool row_live = n0 + r < N;
                     uint32_t cw[RW];
@@ -757,7 +759,7 @@ gemm_kernel(const __grid_constant__ CUtensorMap tmap_x, const __grid_constant__ 
                         else scf[g] = widen16(uint16_t(sc[q][g]), false);
                         bsf[g] = AFF ? widen16(uint16_t(bs[q][g]), false) : 0.f;
                     }
-                    uint8_t* wrow = wt + q * B_KB_BYTES + (ct >> 3) * 1024 + (ct & 7) * 128;
+                    uint8_t* wrow = wt + q * (64 * BK * 2) + (ct >> 3) * 1024 + (ct & 7) * 128;
 #pragma unroll
                     for (int p = 0; p < 8; ++p) {  // 8-column pieces (16 bytes of bf16)
                         const bool live = row_live && kb * BK + 8 * p < K;  // K % 16 == 0
@@ -822,7 +824,7 @@ gemm_kernel(const __grid_constant__ CUtensorMap tmap_x, const __grid_constant__ 
                     wphase ^= 1u;
                 }
 #pragma unroll
-                for (int q = 0; q < NSUB; ++q)
+                for (int q = 0; q < QR; ++q)
 #pragma unroll
                     for (int g = 0; g < G; ++g) {
                         sc[q][g] = nsc[q][g];
@@ -928,12 +930,12 @@ cudaError_t launch_nsub(const DeviceInfo& dev, const CUtensorMap& mx, const CUte
                         const GemmArgs& a, int grid, cudaStream_t s) {
     switch (a.nsub) {
         case 1: return launch_t<KN, F32OUT, 1>(dev, mx, mw, a, grid, s);
-        case 2: return launch_t<KN, F32OUT, (MAX_NSUB >= 2 ? 2 : 1)>(dev, mx, mw, a, grid, s);
-        case 4:
+        case 2: return launch_t<KN, F32OUT, 2>(dev, mx, mw, a, grid, s);
+        case 4: return launch_t<KN, F32OUT, 4>(dev, mx, mw, a, grid, s);
+        default:
             if (a.a_rows == 2 * BM)  // two instruction tiles along M per CTA tile
-                return launch_t<KN, F32OUT, (MAX_NSUB >= 4 ? 4 : 1), 2>(dev, mx, mw, a, grid, s);
-            return launch_t<KN, F32OUT, (MAX_NSUB >= 4 ? 4 : 1)>(dev, mx, mw, a, grid, s);
-        default: return launch_t<KN, F32OUT, MAX_NSUB>(dev, mx, mw, a, grid, s);
+                return launch_t<KN, F32OUT, MAX_NSUB, 2>(dev, mx, mw, a, grid, s);
+            return launch_t<KN, F32OUT, MAX_NSUB>(dev, mx, mw, a, grid, s);
     }
 }
 
@@ -950,15 +952,15 @@ GemmSchedule gemm_schedule(int64_t M, int64_t N, int64_t K, bool w_kn, int num_s
     // CTA tile shape from a cost model: per K-block a CTA spends the longer of its MMAs
     // (about 8192 flop per cycle per SM) and its operand copies (about 64 bytes per cycle
     // per SM from L2), and the tiles run in ceil(tiles / SMs) waves.  Candidates: 128 x
-    // 64*nsub (nsub 1, 2, 4) and 256 x 256 (two instruction tiles along M); the widest
-    // wins ties (X and W are re-read from L2 the fewest times).  The instructions and
-    // their K order are the same for every shape.
+    // BN*nsub (32 to 256 columns) and 256 x 256 (two instruction tiles along M); the
+    // widest wins ties (X and W are re-read from L2 the fewest times).  The instructions
+    // and their K order are the same for every shape.
     const int single_rows = g.a_rows;
     double best = 0.0;
     bool wide_m = false;
     for (int msub = 2; msub >= 1; --msub) {
         for (int ns = MAX_NSUB; ns >= 1; ns >>= 1) {
-            if (msub == 2 && (ns != 4 || m_tiles < 2)) continue;
+            if (msub == 2 && (ns != MAX_NSUB || m_tiles < 2)) continue;
             const int64_t tm = int64_t(BM) * msub;
             const int64_t tiles = ((M + tm - 1) / tm) * ((N + int64_t(ns) * BN - 1) / (int64_t(ns) * BN));
             const int64_t waves = (tiles + num_sms - 1) / num_sms;
@@ -1097,8 +1099,11 @@ cudaError_t launch_qgemm(const DeviceInfo& dev, const void* x, int64_t ldx, cons
     // the invariant schedule with one K-block per stage and 128-row CTA tiles
     const int64_t m_tiles = (M + BM - 1) / BM;
     const int a_rows = m_tiles == 1 ? int((M + 7) / 8 * 8) : BM;
-    int nsub = 1;
-    for (int ns = MAX_NSUB; ns >= 2; ns >>= 1) {
+    // tiles of 64, 128 or 256 rows of W (the converters work in 64-row units): the widest
+    // that still gives every SM a tile
+    constexpr int QMIN = 64 / BN;
+    int nsub = QMIN;
+    for (int ns = MAX_NSUB; ns > QMIN; ns >>= 1) {
         if (m_tiles * ((N + int64_t(ns) * BN - 1) / (int64_t(ns) * BN)) >= dev.num_sms) {
             nsub = ns;
             break;
@@ -1125,8 +1130,8 @@ cudaError_t launch_qgemm(const DeviceInfo& dev, const void* x, int64_t ldx, cons
     // the bf16 tiles the converters write get their own buffers: four when the ring can
     // still be four stages deep, else two
     const int64_t a_bytes = int64_t(a_rows) * BK * 2;
-    const int64_t blk = a_bytes + int64_t(nsub) * 64 * q_kb_bytes +
-                        (staged ? (aff ? 2 : 1) * int64_t(nsub) * 64 * Q_SROW : 0);
+    const int64_t blk = a_bytes + int64_t(nsub) * BN * q_kb_bytes +
+                        (staged ? (aff ? 2 : 1) * int64_t(nsub) * BN * Q_SROW : 0);
     const int64_t b_bytes = int64_t(nsub) * B_KB_BYTES;
     int wbufs = 0, stages = 0;
     for (int wb = MAX_QWBUF; wb >= 2; wb -= 2) {
@@ -1178,10 +1183,10 @@ cudaError_t launch_qgemm(const DeviceInfo& dev, const void* x, int64_t ldx, cons
     const int64_t tiles = m_tiles * ((N + int64_t(nsub) * BN - 1) / (int64_t(nsub) * BN));
     const int grid = int(tiles < dev.num_sms ? tiles : dev.num_sms);
     switch (nsub) {
-        case 1: return y_f32 ? launch_q<true, 1>(dev, mx, mw, ms, mb, a, grid, stream)
-                             : launch_q<false, 1>(dev, mx, mw, ms, mb, a, grid, stream);
-        case 2: return y_f32 ? launch_q<true, (MAX_NSUB >= 2 ? 2 : 1)>(dev, mx, mw, ms, mb, a, grid, stream)
-                             : launch_q<false, (MAX_NSUB >= 2 ? 2 : 1)>(dev, mx, mw, ms, mb, a, grid, stream);
+        case QMIN: return y_f32 ? launch_q<true, QMIN>(dev, mx, mw, ms, mb, a, grid, stream)
+                                : launch_q<false, QMIN>(dev, mx, mw, ms, mb, a, grid, stream);
+        case 2 * QMIN: return y_f32 ? launch_q<true, 2 * QMIN>(dev, mx, mw, ms, mb, a, grid, stream)
+                                    : launch_q<false, 2 * QMIN>(dev, mx, mw, ms, mb, a, grid, stream);
         default: return y_f32 ? launch_q<true, MAX_NSUB>(dev, mx, mw, ms, mb, a, grid, stream)
                               : launch_q<false, MAX_NSUB>(dev, mx, mw, ms, mb, a, grid, stream);
     }

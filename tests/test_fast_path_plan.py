@@ -35,8 +35,8 @@ def test_inside_the_limit_everything_is_the_invariant_configuration(limit):
 
 def test_limit_boundary_is_inclusive(limit):
     limit(8)
-    assert bi.matmul_splits(8, 4096, 4096) == 1
-    assert bi.matmul_splits(9, 4096, 4096) > 1
+    assert bi.matmul_splits(8, 2048, 4096) == 1
+    assert bi.matmul_splits(9, 2048, 4096) > 1
     assert chunk(1, 8, 1028, ws(8, 1028, 8)) == bi.ATTN_CHUNK
     limit(7)
     assert chunk(1, 8, 1028, ws(8, 1028, 8)) != bi.ATTN_CHUNK
@@ -44,16 +44,18 @@ def test_limit_boundary_is_inclusive(limit):
 
 def test_split_k_outside_the_limit(limit):
     limit(0)  # disabled: every call may take the fast path
-    # one M-tile whose 64 column tiles leave most of the 152 SMs idle: split
-    assert bi.matmul_splits(1, 4096, 4096) == 2
-    assert bi.matmul_splits(128, 4096, 4096, "kn") == 2
-    assert bi.matmul_splits(8, 1024, 4096) == 8          # 16 tiles, capped at 8 per tile
+    # one M-tile whose 32-column tiles leave most of the 152 SMs idle: split
+    assert bi.matmul_splits(1, 2048, 4096) == 2          # 64 tiles
+    assert bi.matmul_splits(128, 2048, 4096, "kn") == 2
+    assert bi.matmul_splits(8, 1024, 4096) == 4          # 32 tiles
+    assert bi.matmul_splits(8, 512, 4096) == 8           # 16 tiles, capped at 8 per tile
     # two M-tiles, or enough column tiles, or a single K-block: no split
+    assert bi.matmul_splits(1, 4096, 4096) == 1          # 128 tiles
     assert bi.matmul_splits(129, 4096, 4096) == 1
     assert bi.matmul_splits(8, 14336, 4096) == 1
     assert bi.matmul_splits(8, 128256, 4096) == 1
     assert bi.matmul_splits(4, 64, 64) == 1
-    # the reduction slots (rows x 64 fp32 per extra CTA) must leave the ring room
+    # the reduction slots (rows x 32 fp32 per extra CTA) must leave the ring room
     assert 2 <= bi.matmul_splits(100, 1024, 4096) < 8
     # no CTA without K-blocks, whatever the split
     for K in (64 * 3, 64 * 9 + 5, 4160, 14336):

@@ -35,8 +35,8 @@ def sms(dev):
 
 FAST_SHAPES = [
     # (M, N, K, layout); every one splits K at limit 0 on a 152-SM GPU
-    (1, 4096, 4096, "nk"),      # 2 CTAs per tile
-    (8, 1024, 4096, "kn"),      # 8 CTAs per tile
+    (1, 2048, 4096, "nk"),      # 2 CTAs per tile
+    (8, 1024, 4096, "kn"),      # 4 CTAs per tile
     (5, 1000, 4160, "nk"),      # ragged N, K tail (one copy per K-block)
     (100, 1024, 4096, "nk"),    # 104 staged rows: the slots limit the split
     (128, 512, 1000, "kn"),     # a full M-tile, ragged K
@@ -89,7 +89,7 @@ def test_matmul_limit_experiment(dev, sms):
     (14 comparisons):
     at limit 0 the M = 256 call runs one K loop per tile while M = 1 splits K, so rows
     differ; with the limit covering 256 every call is the invariant kernel."""
-    N = K = 4096
+    N, K = 2048, 4096
     gi = inputs.gemm_inputs(256, N, K, seed=11)
     x, w = gi.x.to(dev), gi.w_nk.to(dev)
 
