@@ -320,7 +320,9 @@ attn_partial_kernel(const __grid_constant__ CUtensorMap tmap_k,
         // S(page) = Q K^T into S buffer (page & 1); O(item) += P V, issued two pages behind
         // S so the softmax of page i overlaps the scores of page i+1.
         constexpr uint32_t idesc_s = umma_idesc_bf16(MMA_M, PAGE, 0, 0);  // K K-major
-        constexpr uint32_t idesc_pv = umma_idesc_bf16(MMA_M, 64, 0, 1);   // V N-major
+        // V N-major; one instruction spans every 64-column box of V (the boxes sit the
+        // descriptor's leading-byte offset apart), so each P slice is read once per step
+        constexpr uint32_t idesc_pv = umma_idesc_bf16(MMA_M, D, 0, 1);
         const uint64_t q_desc0 = umma_smem_desc(smem_addr(sQ), 16, 1024, 2);
         const uint64_t p_desc0 = umma_smem_desc(smem_addr(sP), 16, 1024, 2);
         const uint64_t k_desc0 = umma_smem_desc(smem_addr(sStage), 16, 1024, 2);
@@ -338,11 +340,8 @@ attn_partial_kernel(const __grid_constant__ CUtensorMap tmap_k,
                 const uint32_t o_tmem = tmem_base + uint32_t(C::O_COL + ob * D);
 #pragma unroll
                 for (int k = 0; k < PAGE / 16; ++k)      // keys 16k .. 16k+15: +32 B in P,
-#pragma unroll                                           // +16 rows (2 KB) in V
-                    for (int nh = 0; nh < C::BOXES; ++nh)
-                        tc_mma_bf16(o_tmem + uint32_t(nh * 64), p_desc + uint64_t(k * 2),
-                                    v_desc + uint64_t(nh * (C::BOX_BYTES >> 4) + k * 128),
-                                    idesc_pv, (first && k == 0) ? 0u : 1u);
+                    tc_mma_bf16(o_tmem, p_desc + uint64_t(k * 2),   // +16 rows (2 KB) in V
+                                v_desc + uint64_t(k * 128), idesc_pv, (first && k == 0) ? 0u : 1u);
                 tc_commit(&p_empty[pb]);
                 tc_commit(&empty[s]);   // K and V of the page are no longer read
                 if (last) tc_commit(&o_full[ob]);
