@@ -101,7 +101,7 @@ def recorded_traffic():
     s = re.search(r"source_digest:\s*([0-9a-f]+)", text)
     if not m or not s:
         return None
-    if s.group(1) != source_digest("attention.cu", "common.cuh"):
+    if s.group(1) != source_digest("attention.cu", "attn_common.cuh", "common.cuh"):
         return None
     return float(m.group(1))
 

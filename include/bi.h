@@ -316,6 +316,32 @@ bi_status bi_decode_attn(const void* q, const void* k_cache, const void* v_cache
                          int64_t page_size, float scale, void* out, float* lse,
                          void* workspace, size_t workspace_bytes, bi_stream_t stream);
 
+/* bi_prefill_attn  [BOOK Case 6 "Attention" and the paragraph after its table: serving
+ * engines slice sequences (chunked prefill, prefix caching), and token 1000 must reduce
+ * identically whether 0 or 999 tokens are already cached -- one loop over cache and new
+ * tokens]
+ *
+ *   bi_verify_block for blocks of any width: a prompt cut into chunks of any sizes, each
+ *   chunk's K/V appended (bi_kv_append) before its call, or a prompt continuing a cached
+ *   prefix.  Every query is reduced exactly as bi_verify_block / bi_decode_attn reduce
+ *   it inside the batch-invariant limit (chunk length BI_ATTN_CHUNK, the same
+ *   per-page steps, the same merge tree), so its out and lse bits do not depend on how
+ *   the sequence was split into calls or on the other queries of the call.  The limit
+ *   has no effect (one configuration).
+ *
+ *   Arguments as bi_verify_block, except: max_q >= 1 without upper bound, and
+ *   num_q_heads / num_kv_heads must divide 128 (a tile is 128 query rows: 128 / G tokens
+ *   times the G query heads of one KV head).  Workspace: bi_attn_workspace_size(total_q,
+ *   num_q_heads, head_dim, max_seq_len) bytes.  Device-resident arguments are checked as
+ *   in bi_verify_block. */
+bi_status bi_prefill_attn(const void* q, const void* k_cache, const void* v_cache,
+                          int64_t num_pages, const int32_t* block_table, int64_t max_pages,
+                          const int32_t* seq_lens, const int32_t* cu_q, int64_t batch,
+                          int64_t total_q, int64_t max_q, int64_t max_seq_len,
+                          int64_t num_q_heads, int64_t num_kv_heads, int64_t head_dim,
+                          int64_t page_size, float scale, void* out, float* lse,
+                          void* workspace, size_t workspace_bytes, bi_stream_t stream);
+
 /* ---------------------------------------------------------------------------------
  * bi_verify_block_static_ws -- bi_verify_block without a caller-provided workspace.
  * (No counterpart on the pages; it exists for callers that cannot allocate.)

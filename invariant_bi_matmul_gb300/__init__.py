@@ -52,6 +52,8 @@ SIGNATURES = {
     "bi_attn_workspace_size": ([_i64, _i64, _i64, _i64], _sz),
     "bi_verify_block": ([_p, _p, _p, _i64, _p, _i64, _p, _p, _i64, _i64, _i64, _i64, _i64, _i64,
                          _i64, _i64, _f32, _p, _p, _p, _sz, _p], _int),
+    "bi_prefill_attn": ([_p, _p, _p, _i64, _p, _i64, _p, _p, _i64, _i64, _i64, _i64, _i64, _i64,
+                         _i64, _i64, _f32, _p, _p, _p, _sz, _p], _int),
     "bi_decode_attn": ([_p, _p, _p, _i64, _p, _i64, _p, _i64, _i64, _i64, _i64, _i64, _i64, _f32,
                         _p, _p, _p, _sz, _p], _int),
     "bi_verify_block_static_ws": ([_p, _p, _p, _i64, _p, _i64, _p, _p, _i64, _i64, _i64, _i64, _i64,
@@ -348,6 +350,27 @@ def verify_block(q, k_cache, v_cache, block_table, seq_lens, cu_q, max_q: int, m
     out, lse = _attn_out(q, out, lse, want_lse)
     ws, ws_bytes = _workspace(workspace, attn_workspace_size(T, hq, d, max_seq_len), q.device)
     _check(lib().bi_verify_block(_ptr(q), _ptr(k_cache), _ptr(v_cache), num_pages,
+                                 _ptr(block_table), block_table.shape[1], _ptr(seq_lens),
+                                 _ptr(cu_q), seq_lens.shape[0], T, int(max_q), int(max_seq_len),
+                                 hq, hkv, d, page, float(scale), _ptr(out), _ptr(lse), _ptr(ws),
+                                 ws_bytes, _stream(stream)))
+    return out, lse
+
+
+def prefill_attn(q, k_cache, v_cache, block_table, seq_lens, cu_q, max_q: int, max_seq_len: int,
+                 scale: float, out=None, lse=None, want_lse=True, workspace=None, stream=None):
+    """verify_block for blocks of any width (chunked prefill, prefix caching): every query
+    reduced exactly as verify_block / decode_attn reduce it."""
+    torch = _torch()
+    num_pages, hkv, page, d = _paged_common(k_cache, v_cache, block_table, seq_lens)
+    _need(q, torch.bfloat16, "q", 3)
+    _need(cu_q, torch.int32, "cu_q", 1)
+    if not q.is_contiguous() or not cu_q.is_contiguous():
+        raise ValueError("q and cu_q must be contiguous")
+    T, hq, _ = q.shape
+    out, lse = _attn_out(q, out, lse, want_lse)
+    ws, ws_bytes = _workspace(workspace, attn_workspace_size(T, hq, d, max_seq_len), q.device)
+    _check(lib().bi_prefill_attn(_ptr(q), _ptr(k_cache), _ptr(v_cache), num_pages,
                                  _ptr(block_table), block_table.shape[1], _ptr(seq_lens),
                                  _ptr(cu_q), seq_lens.shape[0], T, int(max_q), int(max_seq_len),
                                  hq, hkv, d, page, float(scale), _ptr(out), _ptr(lse), _ptr(ws),

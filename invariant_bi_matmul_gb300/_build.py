@@ -18,7 +18,7 @@ BUILD_DIR = os.path.join(HERE, "_build")
 LIB_PATH = os.path.join(HERE, "libbi.so")
 
 SOURCES = ["api.cu", "rmsnorm.cu", "gemm.cu", "attention.cu", "selftest.cu", "tmap.cu",
-           "static_ws.cu", "glue.cu", "rowwise.cu", "f32path.cu"]
+           "static_ws.cu", "glue.cu", "rowwise.cu", "f32path.cu", "prefill.cu"]
 ARCH = ["-gencode", "arch=compute_103a,code=sm_103a"]
 NVCC_FLAGS = ARCH + ["-O3", "-std=c++17", "-lineinfo", "-Xcompiler", "-fPIC,-fvisibility=hidden",
                      f"-I{INCLUDE}", f"-I{CSRC}"]

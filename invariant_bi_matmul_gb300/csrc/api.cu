@@ -365,7 +365,8 @@ BI_EXPORT bi_status bi_rmsnorm_ex(const void* x, int64_t ldx, const void* gamma,
 
 namespace {
 
-bi_status check_paged(const char* fn, const PagedArgs& a, int64_t page_size, bool need_cu_q) {
+bi_status check_paged(const char* fn, const PagedArgs& a, int64_t page_size, bool need_cu_q,
+                      bool prefill = false) {
     if (a.batch < 0 || a.total_q < 0)
         return fail(BI_ERR_INVALID_ARG, "%s: negative batch or total_q", fn);
     if (a.head_dim != 64 && a.head_dim != 128)
@@ -379,11 +380,21 @@ bi_status check_paged(const char* fn, const PagedArgs& a, int64_t page_size, boo
         return fail(BI_ERR_INVALID_ARG, "%s: num_pages and max_pages must be >= 1", fn);
     if (a.num_pages * a.hkv * BI_PAGE_SIZE > kI32Max)
         return fail(BI_ERR_UNSUPPORTED, "%s: cache too large for 32-bit TMA row coordinates", fn);
-    if (a.max_q < 1 || a.max_q > BI_ATTN_MAX_Q)
-        return fail(BI_ERR_UNSUPPORTED, "%s: max_q must be in [1, %d]", fn, BI_ATTN_MAX_Q);
-    if (a.max_q * (a.hq / a.hkv) > BI_ATTN_MAX_ROWS)
-        return fail(BI_ERR_UNSUPPORTED, "%s: max_q * (num_q_heads/num_kv_heads) must be <= %d",
-                    fn, BI_ATTN_MAX_ROWS);
+    if (prefill) {
+        if (a.max_q < 1) return fail(BI_ERR_INVALID_ARG, "%s: max_q must be >= 1", fn);
+        const int64_t G = a.hq / a.hkv;
+        if (G > 128 || 128 % G != 0)
+            return fail(BI_ERR_UNSUPPORTED,
+                        "%s: num_q_heads/num_kv_heads must divide 128 (128/G tokens per tile)",
+                        fn);
+    } else {
+        if (a.max_q < 1 || a.max_q > BI_ATTN_MAX_Q)
+            return fail(BI_ERR_UNSUPPORTED, "%s: max_q must be in [1, %d]", fn, BI_ATTN_MAX_Q);
+        if (a.max_q * (a.hq / a.hkv) > BI_ATTN_MAX_ROWS)
+            return fail(BI_ERR_UNSUPPORTED,
+                        "%s: max_q * (num_q_heads/num_kv_heads) must be <= %d", fn,
+                        BI_ATTN_MAX_ROWS);
+    }
     if (a.batch > BI_ATTN_MAX_BATCH)
         return fail(BI_ERR_UNSUPPORTED, "%s: batch must be <= %d", fn, BI_ATTN_MAX_BATCH);
     if (a.max_seq_len < 1 || a.max_seq_len > a.max_pages * BI_PAGE_SIZE)
@@ -488,6 +499,38 @@ BI_EXPORT bi_status bi_verify_block(const void* q, const void* k_cache, const vo
                 total_q, max_q, max_seq_len, num_q_heads, num_kv_heads, head_dim};
     return run_attention("bi_verify_block", q, a, page_size, scale, out, lse, workspace,
                          workspace_bytes, stream);
+}
+
+BI_EXPORT bi_status bi_prefill_attn(const void* q, const void* k_cache, const void* v_cache,
+                                    int64_t num_pages, const int32_t* block_table,
+                                    int64_t max_pages, const int32_t* seq_lens,
+                                    const int32_t* cu_q, int64_t batch, int64_t total_q,
+                                    int64_t max_q, int64_t max_seq_len, int64_t num_q_heads,
+                                    int64_t num_kv_heads, int64_t head_dim, int64_t page_size,
+                                    float scale, void* out, float* lse, void* workspace,
+                                    size_t workspace_bytes, bi_stream_t stream) {
+    const char* fn = "bi_prefill_attn";
+    PagedArgs a{k_cache, v_cache, num_pages, block_table, max_pages, seq_lens, cu_q, batch,
+                total_q, max_q, max_seq_len, num_q_heads, num_kv_heads, head_dim};
+    bi_status s = check_paged(fn, a, page_size, true, true);
+    if (s != BI_OK) return s;
+    if (!std::isfinite(scale)) return fail(BI_ERR_INVALID_ARG, "%s: scale must be finite", fn);
+    if (a.batch == 0) return BI_OK;
+    if (!cu_q) return fail(BI_ERR_INVALID_ARG, "%s: null cu_q", fn);
+    if (!q || !out || !workspace) return fail(BI_ERR_INVALID_ARG, "%s: null q/out/workspace", fn);
+    if (!aligned(q, 16) || !aligned(out, 16) || !aligned(workspace, 16) || (lse && !aligned(lse, 4)))
+        return fail(BI_ERR_UNSUPPORTED, "%s: q, out and workspace must be 16-byte aligned", fn);
+    const size_t need = attn_workspace_bytes(a.total_q, a.hq, a.head_dim, a.max_seq_len);
+    if (workspace_bytes < need)
+        return fail(BI_ERR_INVALID_ARG, "%s: workspace too small (%zu < %zu bytes)", fn,
+                    workspace_bytes, need);
+    cudaError_t why = cudaSuccess;
+    const DeviceInfo* dev = current_device_info(&why);
+    if (!dev) return cuda_fail(why, fn);
+    cudaError_t e = launch_prefill(*dev, q, a, scale, out, lse, workspace,
+                                   reinterpret_cast<cudaStream_t>(stream));
+    if (e != cudaSuccess) return cuda_fail(e, fn);
+    return BI_OK;
 }
 
 BI_EXPORT bi_status bi_decode_attn(const void* q, const void* k_cache, const void* v_cache,

@@ -36,17 +36,11 @@
 // are repeated in each of the four tensor-memory lane quarters); warp 4 reads each
 // finished O out and writes the chunk partial while the next item runs.  Work items (sequence, KV head, chunk) are
 // enumerated on the device from seq_lens, so mixed-length batches launch no idle CTAs.
-#include "common.cuh"
-#include "launch.h"
-#include "tmap.h"
-#include "bi.h"
+#include "attn_common.cuh"
 
 namespace bi {
 namespace {
 
-constexpr int PAGE = 64;
-constexpr int CHUNK_LOG2 = 9;  // the invariant chunk length: 512 keys
-constexpr int CHUNK = 1 << CHUNK_LOG2;
 constexpr int MIN_CHUNK_LOG2 = 6, MAX_CHUNK_LOG2 = 11;  // non-invariant calls: 64 .. 2048
 constexpr int PV_LAG = 2;      // P V of page g is issued after S of page g+2
 constexpr int MAXR = 32;       // query rows per (sequence, KV head): q_len * group size
@@ -57,10 +51,7 @@ constexpr int PRODUCER = NSM + 1, MMA_WARP = NSM + 2;
 constexpr int THREADS = (NSM + 3) * 32;
 constexpr int MMA_M = 128;     // instruction rows: Q rows repeated once per lane quarter
 constexpr int TMEM_COLS = 512;
-constexpr float kRescaleLog2 = 8.0f;  // rescale O only when the row max grows by > 2^8
 constexpr int MAX_BATCH = BI_ATTN_MAX_BATCH;
-constexpr float kLog2e = 1.4426950408889634f;
-constexpr float kLn2 = 0.6931471805599453f;
 
 static_assert(CHUNK % PAGE == 0, "chunk must hold whole pages");
 static_assert(PAGE == 64 && KSL == 16, "a page is one 64-column S tile, 16 keys per warp");
@@ -97,34 +88,6 @@ struct Cfg {
     static_assert(RING_OFF % 1024 == 0 && BAR_OFF % 1024 == 0, "1024-byte aligned buffers");
     static_assert(SMEM <= 232448, "shared memory per CTA");
 };
-
-// byte offset of (row, 16-byte chunk) in a 128-byte-swizzled box (the TMA SWIZZLE_128B
-// pattern: chunk index XOR row mod 8)
-__device__ __forceinline__ uint32_t swz(int row, int chunk) {
-    return uint32_t(row) * 128u + (uint32_t((chunk ^ (row & 7)) & 7) << 4);
-}
-
-struct SeqInfo {
-    int L, qb, t0;
-};
-
-__device__ __forceinline__ SeqInfo seq_info(const int32_t* seq_lens, const int32_t* cu_q, int b) {
-    SeqInfo s;
-    s.L = seq_lens[b];
-    if (cu_q) {
-        s.t0 = cu_q[b];
-        s.qb = cu_q[b + 1] - s.t0;
-    } else {
-        s.t0 = b;
-        s.qb = 1;
-    }
-    return s;
-}
-
-__device__ __forceinline__ bool seq_ok(const SeqInfo& s, int max_q, int max_seq_len, int total_q) {
-    return s.L >= 1 && s.L <= max_seq_len && s.qb >= 1 && s.qb <= max_q && s.qb <= s.L &&
-           s.t0 >= 0 && s.t0 + s.qb <= total_q;
-}
 
 // ------------------------------------------------------------------- partial kernel
 
@@ -844,14 +807,23 @@ cudaError_t launch_attention_t(const DeviceInfo& dev, const void* q, const Paged
         a.seq_lens, a.cu_q, int(a.batch), int(a.total_q), int(a.max_q), int(a.max_seq_len),
         int(a.hq), int(a.hkv), scale_log2, ws_o, ws_ml, maxC, chunk_log2, dev.err_word);
     if (e != cudaSuccess) return e;
-    return launch_pdl(attn_merge_kernel<D>, dim3(unsigned(a.total_q * a.hq)),
-                      dim3(MERGE_WARPS * 32), 0, stream, a.seq_lens, a.cu_q, int(a.batch),
-                      int(a.total_q), int(a.max_q), int(a.max_seq_len), int(a.hq),
-                      static_cast<const float*>(ws_o), static_cast<const float*>(ws_ml), maxC,
-                      chunk_log2, static_cast<__nv_bfloat16*>(out), lse);
+    return launch_attn_merge(a, workspace, chunk_log2, out, lse, stream);
 }
 
 }  // namespace
+
+cudaError_t launch_attn_merge(const PagedArgs& a, void* workspace, int chunk_log2, void* out,
+                              float* lse, cudaStream_t stream) {
+    const int chunk = 1 << chunk_log2;
+    const int maxC = int((a.max_seq_len + chunk - 1) / chunk);
+    const float* ws_o = static_cast<const float*>(workspace);
+    const float* ws_ml = ws_o + a.total_q * a.hq * int64_t(maxC) * a.head_dim;
+    auto kern = a.head_dim == 64 ? attn_merge_kernel<64> : attn_merge_kernel<128>;
+    return launch_pdl(kern, dim3(unsigned(a.total_q * a.hq)), dim3(MERGE_WARPS * 32), 0, stream,
+                      a.seq_lens, a.cu_q, int(a.batch), int(a.total_q), int(a.max_q),
+                      int(a.max_seq_len), int(a.hq), ws_o, ws_ml, maxC, chunk_log2,
+                      static_cast<__nv_bfloat16*>(out), lse);
+}
 
 namespace {
 size_t workspace_for(int64_t total_q, int64_t hq, int64_t head_dim, int64_t max_seq_len,

@@ -149,6 +149,17 @@ cudaError_t launch_attention(const DeviceInfo& dev, const void* q, const PagedAr
                              float scale, void* out, float* lse, void* workspace,
                              int chunk_log2, cudaStream_t stream);
 
+// The log-sum-exp merge of the chunk partials in `workspace` (as the split-KV kernels
+// leave them for chunk length 2^chunk_log2) into out (and lse).
+cudaError_t launch_attn_merge(const PagedArgs& a, void* workspace, int chunk_log2, void* out,
+                              float* lse, cudaStream_t stream);
+
+// Chunked prefill (prefill.cu): blocks of any width, each query reduced exactly as the
+// decode / verify kernels reduce it (invariant chunk length), then the same merge.
+cudaError_t launch_prefill(const DeviceInfo& dev, const void* q, const PagedArgs& a,
+                           float scale, void* out, float* lse, void* workspace,
+                           cudaStream_t stream);
+
 cudaError_t launch_selftest_wait(const DeviceInfo& dev, unsigned long long timeout_ns,
                                  cudaStream_t stream);
 

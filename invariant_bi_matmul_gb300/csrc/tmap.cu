@@ -131,6 +131,21 @@ bool tmap_2d_u8(CUtensorMap* out, const void* ptr, uint64_t inner_bytes, uint64_
                          stride_bytes, box_inner, box_outer);
 }
 
+bool tmap_3d_bf16(CUtensorMap* out, const void* ptr, uint64_t d0, uint64_t d1, uint64_t d2,
+                  uint64_t stride1, uint64_t stride2, uint32_t box0, uint32_t box1,
+                  uint32_t box2) {
+    EncodeTiledFn fn = encode_fn();
+    if (!fn) return false;
+    const cuuint64_t dims[3] = {d0, d1, d2};
+    const cuuint64_t strides[2] = {stride1 * 2, stride2 * 2};
+    const cuuint32_t box[3] = {box0, box1, box2};
+    const cuuint32_t estr[3] = {1, 1, 1};
+    return fn(out, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 3, const_cast<void*>(ptr), dims, strides,
+              box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+              CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) ==
+           CUDA_SUCCESS;
+}
+
 bool tmap_2d_u16(CUtensorMap* out, const void* ptr, uint64_t inner, uint64_t outer,
                  uint64_t stride_bytes, uint32_t box_inner, uint32_t box_outer) {
     return tmap_2d_plain(out, CU_TENSOR_MAP_DATA_TYPE_UINT16, ptr, inner, outer, stride_bytes,

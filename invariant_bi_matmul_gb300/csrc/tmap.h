@@ -26,6 +26,12 @@ bool tmap_kblocked_bf16(CUtensorMap* out, const void* ptr, uint64_t inner, uint6
 // box_inner bytes x box_outer rows, no swizzle; bytes outside the tensor read as 0.
 bool tmap_2d_u8(CUtensorMap* out, const void* ptr, uint64_t inner_bytes, uint64_t outer,
                 uint64_t stride_bytes, uint32_t box_inner, uint32_t box_outer);
+// 3D bf16 tensor [d2][d1][d0] with element strides stride1 (between d1 rows) and
+// stride2 (between d2 slabs), boxes box0 x box1 x box2 landing densely in shared memory,
+// 128-byte swizzle; elements outside the tensor read as 0.  No cache.
+bool tmap_3d_bf16(CUtensorMap* out, const void* ptr, uint64_t d0, uint64_t d1, uint64_t d2,
+                  uint64_t stride1, uint64_t stride2, uint32_t box0, uint32_t box1,
+                  uint32_t box2);
 // The same for 16-bit elements (inner and box_inner in elements).
 bool tmap_2d_u16(CUtensorMap* out, const void* ptr, uint64_t inner, uint64_t outer,
                  uint64_t stride_bytes, uint32_t box_inner, uint32_t box_outer);

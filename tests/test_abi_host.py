@@ -181,6 +181,33 @@ def test_attention_argument_errors_before_launch(L):
     assert _verify(L, batch=0, total_q=0) == bi.BI_OK
 
 
+def _prefill(L, **kw):
+    d = ctypes.c_void_p(256)
+    a = dict(q=d, k=d, v=d, num_pages=4, bt=d, max_pages=4, sl=d, cu=d, batch=1, total_q=200,
+             max_q=200, max_seq_len=200, hq=32, hkv=8, D=128, page=64, scale=0.1, out=d,
+             lse=None, ws=d, ws_bytes=1 << 30)
+    a.update(kw)
+    return L.bi_prefill_attn(a["q"], a["k"], a["v"], a["num_pages"], a["bt"], a["max_pages"],
+                             a["sl"], a["cu"], a["batch"], a["total_q"], a["max_q"],
+                             a["max_seq_len"], a["hq"], a["hkv"], a["D"], a["page"],
+                             ctypes.c_float(a["scale"]), a["out"], a["lse"], a["ws"],
+                             a["ws_bytes"], None)
+
+
+def test_prefill_argument_errors_before_launch(L):
+    """Blocks wider than a verify block are its purpose; a group size that does not divide
+    the 128-row tile, max_q < 1 and the verify block's other rules are refused."""
+    assert _prefill(L, hq=24, hkv=8) == bi.BI_ERR_UNSUPPORTED     # G = 3
+    assert "divide 128" in _err(L)
+    assert _prefill(L, max_q=0) == bi.BI_ERR_INVALID_ARG
+    assert _prefill(L, D=96) == bi.BI_ERR_UNSUPPORTED
+    assert _prefill(L, total_q=201) == bi.BI_ERR_INVALID_ARG       # > batch * max_q
+    assert _prefill(L, cu=None) == bi.BI_ERR_INVALID_ARG
+    assert _prefill(L, ws_bytes=16) == bi.BI_ERR_INVALID_ARG
+    assert _prefill(L, q=ctypes.c_void_p(258)) == bi.BI_ERR_UNSUPPORTED
+    assert _prefill(L, batch=0, total_q=0) == bi.BI_OK
+
+
 def test_workspace_size_formula(L):
     # one (m, l, o[D]) fp32 partial per (token, head, 512-key chunk)
     assert L.bi_attn_workspace_size(8, 32, 128, 65540) == 8 * 32 * 129 * (128 + 2) * 4
