@@ -612,27 +612,111 @@ attn_partial_kernel(const __grid_constant__ CUtensorMap tmap_k,
 
 // --------------------------------------------------------------------- merge kernel
 
-constexpr int MERGE_WARPS = 8;
+constexpr int MERGE_WARPS = 8;    // chunk ranges of the merge tree
+constexpr int64_t kMergeRowsMin = 4096;  // rows from which a warp per row merges
+constexpr int MERGE_UNROLL = 17;  // partials requested per round trip (136 chunks in 8)
 
-// One CTA per (token, query head) merges the chunk partials 0 .. nC-1 (nC = pos/chunk+1).
-// Warp w folds the contiguous range [w*nC/8, (w+1)*nC/8) in ascending order (max first,
-// then the exp2-weighted sums); the eight warp results are combined in ascending warp
-// order.  The tree is a function of nC alone, i.e. of the query's position.
+// The merge tree of one (token, query head) row with nC = pos/chunk + 1 chunk partials:
+// range w = [w*nC/8, (w+1)*nC/8) is folded in ascending chunk order (its max first, then
+// the exp2-weighted sums), and the eight range results are combined in ascending range
+// order -- a tree fixed by nC, i.e. by the query's position.  Both merge kernels below run
+// exactly these two functions, so they give the same bits.
+
+// Fold chunks [c0, c1) of the row at `base` (lane holds dims lane*PER ..): range max Mw,
+// weighted sum Lw and weighted o sums acc.
 template <int D>
-__global__ void __launch_bounds__(MERGE_WARPS * 32)
-attn_merge_kernel(const int32_t* __restrict__ seq_lens, const int32_t* __restrict__ cu_q, int B,
-                  int total_q, int max_q, int max_seq_len, int Hq,
-                  const float* __restrict__ ws_o, const float* __restrict__ ws_ml, int maxC,
-                  int chunk_log2, __nv_bfloat16* __restrict__ out, float* __restrict__ lse) {
+__device__ __forceinline__ void merge_fold(const float* __restrict__ ws_o,
+                                           const float* __restrict__ ws_ml, int64_t base, int c0,
+                                           int c1, int lane, float& Mw, float& Lw,
+                                           float (&acc)[D / 32]) {
     constexpr int PER = D / 32;
-    constexpr int UNROLL = 17;  // a warp's whole range up to 136 chunks (69,632 keys)
-    __shared__ float sM[MERGE_WARPS], sL[MERGE_WARPS];
-    __shared__ float sO[MERGE_WARPS][D];
-    pdl_wait();
-    pdl_trigger();
-    const int t = int(blockIdx.x / unsigned(Hq));
-    const int hq = int(blockIdx.x - unsigned(t) * unsigned(Hq));
-    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+    // The first MERGE_UNROLL partials of the range are requested before anything else
+    // (for ranges up to MERGE_UNROLL chunks: all of them, in one global round trip).
+    auto load = [&](int c, float (&v)[PER], float2& ml) {
+        ml = *reinterpret_cast<const float2*>(ws_ml + (base + c) * 2);
+        const float* src = ws_o + (base + c) * D + lane * PER;
+        if (PER == 4) {
+            const float4 f = *reinterpret_cast<const float4*>(src);
+            v[0] = f.x; v[1 % PER] = f.y; v[2 % PER] = f.z; v[3 % PER] = f.w;
+        } else {
+            const float2 f = *reinterpret_cast<const float2*>(src);
+            v[0] = f.x; v[1 % PER] = f.y;
+        }
+    };
+    float v[MERGE_UNROLL][PER];
+    float2 ml[MERGE_UNROLL];
+#pragma unroll
+    for (int u = 0; u < MERGE_UNROLL; ++u)
+        if (c0 + u < c1) load(c0 + u, v[u], ml[u]);
+
+    // range max (exact in any order): from the registers when the whole range was loaded
+    // above, else lanes stride over the chunks and a butterfly combines them
+    Mw = -INFINITY;
+    if (c1 - c0 <= MERGE_UNROLL) {
+#pragma unroll
+        for (int u = 0; u < MERGE_UNROLL; ++u)
+            if (c0 + u < c1) Mw = fmaxf(Mw, ml[u].x);
+    } else {
+        for (int c = c0 + lane; c < c1; c += 32) Mw = fmaxf(Mw, ws_ml[(base + c) * 2]);
+#pragma unroll
+        for (int off = 16; off >= 1; off >>= 1)
+            Mw = fmaxf(Mw, __shfl_xor_sync(0xffffffffu, Mw, off));
+    }
+
+    Lw = 0.f;
+#pragma unroll
+    for (int i = 0; i < PER; ++i) acc[i] = 0.f;
+    for (int c = c0; c < c1; c += MERGE_UNROLL) {
+        if (c > c0) {
+#pragma unroll
+            for (int u = 0; u < MERGE_UNROLL; ++u)  // issue the loads of the next chunks first
+                if (c + u < c1) load(c + u, v[u], ml[u]);
+        }
+#pragma unroll
+        for (int u = 0; u < MERGE_UNROLL; ++u) {  // then fold them in ascending chunk order
+            if (c + u < c1) {
+                const float wgt = exp2f(ml[u].x - Mw);
+                Lw = Lw + wgt * ml[u].y;
+#pragma unroll
+                for (int i = 0; i < PER; ++i) acc[i] = acc[i] + wgt * v[u][i];
+            }
+        }
+    }
+}
+
+// Combine the eight range results (Mw[w], Lw[w], acc of range w through get_acc(w, i)) in
+// ascending range order and store the row (and its natural-log LSE).
+template <int D, class AccFn>
+__device__ __forceinline__ void merge_combine(const float (&Mw)[MERGE_WARPS],
+                                              const float (&Lw)[MERGE_WARPS], AccFn get_acc,
+                                              int lane, __nv_bfloat16* __restrict__ dst_row,
+                                              float* lse_slot) {
+    constexpr int PER = D / 32;
+    float M = -INFINITY;
+#pragma unroll
+    for (int w = 0; w < MERGE_WARPS; ++w) M = fmaxf(M, Mw[w]);
+    float L = 0.f;
+    float o[PER];
+#pragma unroll
+    for (int i = 0; i < PER; ++i) o[i] = 0.f;
+#pragma unroll
+    for (int w = 0; w < MERGE_WARPS; ++w) {
+        const float wgt = exp2f(Mw[w] - M);  // an empty range has Mw = -inf: weight 0
+        L = L + wgt * Lw[w];
+#pragma unroll
+        for (int i = 0; i < PER; ++i) o[i] = o[i] + wgt * get_acc(w, i);
+    }
+    __nv_bfloat16* dst = dst_row + lane * PER;
+#pragma unroll
+    for (int i = 0; i < PER; ++i) dst[i] = __float2bfloat16_rn(o[i] / L);
+    if (lse_slot && lane == 0) *lse_slot = (M + log2f(L)) * kLn2;
+}
+
+// Row (token t, query head hq) of the call: its sequence and position, or false when the
+// sequence is malformed or the token belongs to none.
+__device__ __forceinline__ bool merge_row(const int32_t* __restrict__ seq_lens,
+                                          const int32_t* __restrict__ cu_q, int B, int total_q,
+                                          int max_q, int max_seq_len, int t, int& pos) {
     int b;
     if (cu_q) {
         int lo = 0, hi = B;  // largest b with cu_q[b] <= t
@@ -645,65 +729,33 @@ attn_merge_kernel(const int32_t* __restrict__ seq_lens, const int32_t* __restric
         b = t;
     }
     const SeqInfo si = seq_info(seq_lens, cu_q, b);
-    if (!seq_ok(si, max_q, max_seq_len, total_q) || t < si.t0 || t >= si.t0 + si.qb) return;
-    const int pos = si.L - si.qb + (t - si.t0);
+    if (!seq_ok(si, max_q, max_seq_len, total_q) || t < si.t0 || t >= si.t0 + si.qb) return false;
+    pos = si.L - si.qb + (t - si.t0);
+    return true;
+}
+
+// One CTA per row: warp w folds range w (latency: a few rows, long contexts).
+template <int D>
+__global__ void __launch_bounds__(MERGE_WARPS * 32)
+attn_merge_kernel(const int32_t* __restrict__ seq_lens, const int32_t* __restrict__ cu_q, int B,
+                  int total_q, int max_q, int max_seq_len, int Hq,
+                  const float* __restrict__ ws_o, const float* __restrict__ ws_ml, int maxC,
+                  int chunk_log2, __nv_bfloat16* __restrict__ out, float* __restrict__ lse) {
+    constexpr int PER = D / 32;
+    __shared__ float sM[MERGE_WARPS], sL[MERGE_WARPS];
+    __shared__ float sO[MERGE_WARPS][D];
+    pdl_wait();
+    pdl_trigger();
+    const int t = int(blockIdx.x / unsigned(Hq));
+    const int hq = int(blockIdx.x - unsigned(t) * unsigned(Hq));
+    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+    int pos;
+    if (!merge_row(seq_lens, cu_q, B, total_q, max_q, max_seq_len, t, pos)) return;
     const int nC = (pos >> chunk_log2) + 1;
     const int64_t base = (int64_t(t) * Hq + hq) * maxC;
-    const int c0 = warp * nC / MERGE_WARPS, c1 = (warp + 1) * nC / MERGE_WARPS;
-
-    // The first UNROLL partials of the range are requested before anything else (for
-    // ranges up to UNROLL chunks: all of them, in one global round trip).
-    auto load = [&](int c, float (&v)[PER], float2& ml) {
-        ml = *reinterpret_cast<const float2*>(ws_ml + (base + c) * 2);
-        const float* src = ws_o + (base + c) * D + lane * PER;
-        if (PER == 4) {
-            const float4 f = *reinterpret_cast<const float4*>(src);
-            v[0] = f.x; v[1 % PER] = f.y; v[2 % PER] = f.z; v[3 % PER] = f.w;
-        } else {
-            const float2 f = *reinterpret_cast<const float2*>(src);
-            v[0] = f.x; v[1 % PER] = f.y;
-        }
-    };
-    float v[UNROLL][PER];
-    float2 ml[UNROLL];
-#pragma unroll
-    for (int u = 0; u < UNROLL; ++u)
-        if (c0 + u < c1) load(c0 + u, v[u], ml[u]);
-
-    // range max (exact in any order): from the registers when the whole range was loaded
-    // above, else lanes stride over the chunks and a butterfly combines them
-    float Mw = -INFINITY;
-    if (c1 - c0 <= UNROLL) {
-#pragma unroll
-        for (int u = 0; u < UNROLL; ++u)
-            if (c0 + u < c1) Mw = fmaxf(Mw, ml[u].x);
-    } else {
-        for (int c = c0 + lane; c < c1; c += 32) Mw = fmaxf(Mw, ws_ml[(base + c) * 2]);
-#pragma unroll
-        for (int off = 16; off >= 1; off >>= 1)
-            Mw = fmaxf(Mw, __shfl_xor_sync(0xffffffffu, Mw, off));
-    }
-
-    float Lw = 0.f;
-    float acc[PER];
-#pragma unroll
-    for (int i = 0; i < PER; ++i) acc[i] = 0.f;
-    for (int c = c0; c < c1; c += UNROLL) {
-        if (c > c0) {
-#pragma unroll
-            for (int u = 0; u < UNROLL; ++u)  // issue the loads of UNROLL chunks first
-                if (c + u < c1) load(c + u, v[u], ml[u]);
-        }
-#pragma unroll
-        for (int u = 0; u < UNROLL; ++u) {  // then fold them in ascending chunk order
-            if (c + u < c1) {
-                const float wgt = exp2f(ml[u].x - Mw);
-                Lw = Lw + wgt * ml[u].y;
-#pragma unroll
-                for (int i = 0; i < PER; ++i) acc[i] = acc[i] + wgt * v[u][i];
-            }
-        }
-    }
+    float Mw, Lw, acc[PER];
+    merge_fold<D>(ws_o, ws_ml, base, warp * nC / MERGE_WARPS, (warp + 1) * nC / MERGE_WARPS,
+                  lane, Mw, Lw, acc);
     if (lane == 0) {
         sM[warp] = Mw;
         sL[warp] = Lw;
@@ -712,24 +764,88 @@ attn_merge_kernel(const int32_t* __restrict__ seq_lens, const int32_t* __restric
     for (int i = 0; i < PER; ++i) sO[warp][lane * PER + i] = acc[i];
     __syncthreads();
     if (warp != 0) return;
-    float M = -INFINITY;
-#pragma unroll
-    for (int w = 0; w < MERGE_WARPS; ++w) M = fmaxf(M, sM[w]);
-    float L = 0.f;
-    float o[PER];
-#pragma unroll
-    for (int i = 0; i < PER; ++i) o[i] = 0.f;
+    float M8[MERGE_WARPS], L8[MERGE_WARPS];
 #pragma unroll
     for (int w = 0; w < MERGE_WARPS; ++w) {
-        const float wgt = exp2f(sM[w] - M);  // an empty range has sM = -inf: weight 0
-        L = L + wgt * sL[w];
-#pragma unroll
-        for (int i = 0; i < PER; ++i) o[i] = o[i] + wgt * sO[w][lane * PER + i];
+        M8[w] = sM[w];
+        L8[w] = sL[w];
     }
-    __nv_bfloat16* dst = out + (int64_t(t) * Hq + hq) * D + lane * PER;
+    merge_combine<D>(M8, L8, [&](int w, int i) { return sO[w][lane * PER + i]; }, lane,
+                     out + (int64_t(t) * Hq + hq) * D, lse ? lse + int64_t(t) * Hq + hq : nullptr);
+}
+
+// One warp per row, eight rows per CTA: the same tree, its eight ranges folded one after
+// another (throughput: many rows, e.g. a prefill block).
+template <int D>
+__global__ void __launch_bounds__(MERGE_WARPS * 32)
+attn_merge_rows_kernel(const int32_t* __restrict__ seq_lens, const int32_t* __restrict__ cu_q,
+                       int B, int total_q, int max_q, int max_seq_len, int Hq,
+                       const float* __restrict__ ws_o, const float* __restrict__ ws_ml, int maxC,
+                       int chunk_log2, __nv_bfloat16* __restrict__ out,
+                       float* __restrict__ lse) {
+    constexpr int PER = D / 32;
+    pdl_wait();
+    pdl_trigger();
+    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+    const int64_t row = int64_t(blockIdx.x) * MERGE_WARPS + warp;
+    if (row >= int64_t(total_q) * Hq) return;
+    const int t = int(row / Hq);
+    const int hq = int(row - int64_t(t) * Hq);
+    int pos;
+    if (!merge_row(seq_lens, cu_q, B, total_q, max_q, max_seq_len, t, pos)) return;
+    const int nC = (pos >> chunk_log2) + 1;
+    const int64_t base = (int64_t(t) * Hq + hq) * maxC;
+    float M8[MERGE_WARPS], L8[MERGE_WARPS], acc8[MERGE_WARPS][PER];
+    if (nC <= MERGE_UNROLL) {
+        // every partial of the row in one round trip, then each range folded from the
+        // registers with merge_fold's arithmetic (max first, then the weighted sums in
+        // ascending chunk order)
+        float v[MERGE_UNROLL][PER];
+        float2 ml[MERGE_UNROLL];
 #pragma unroll
-    for (int i = 0; i < PER; ++i) dst[i] = __float2bfloat16_rn(o[i] / L);
-    if (lse && lane == 0) lse[int64_t(t) * Hq + hq] = (M + log2f(L)) * kLn2;
+        for (int c = 0; c < MERGE_UNROLL; ++c) {
+            if (c < nC) {
+                ml[c] = *reinterpret_cast<const float2*>(ws_ml + (base + c) * 2);
+                const float* src = ws_o + (base + c) * D + lane * PER;
+                if (PER == 4) {
+                    const float4 f = *reinterpret_cast<const float4*>(src);
+                    v[c][0] = f.x; v[c][1 % PER] = f.y; v[c][2 % PER] = f.z; v[c][3 % PER] = f.w;
+                } else {
+                    const float2 f = *reinterpret_cast<const float2*>(src);
+                    v[c][0] = f.x; v[c][1 % PER] = f.y;
+                }
+            }
+        }
+#pragma unroll
+        for (int w = 0; w < MERGE_WARPS; ++w) {
+            const int c0 = w * nC / MERGE_WARPS, c1 = (w + 1) * nC / MERGE_WARPS;
+            float Mw = -INFINITY;
+#pragma unroll
+            for (int c = 0; c < MERGE_UNROLL; ++c)
+                if (c >= c0 && c < c1) Mw = fmaxf(Mw, ml[c].x);
+            float Lw = 0.f;
+#pragma unroll
+            for (int i = 0; i < PER; ++i) acc8[w][i] = 0.f;
+#pragma unroll
+            for (int c = 0; c < MERGE_UNROLL; ++c) {
+                if (c >= c0 && c < c1) {
+                    const float wgt = exp2f(ml[c].x - Mw);
+                    Lw = Lw + wgt * ml[c].y;
+#pragma unroll
+                    for (int i = 0; i < PER; ++i) acc8[w][i] = acc8[w][i] + wgt * v[c][i];
+                }
+            }
+            M8[w] = Mw;
+            L8[w] = Lw;
+        }
+    } else {
+#pragma unroll
+        for (int w = 0; w < MERGE_WARPS; ++w)
+            merge_fold<D>(ws_o, ws_ml, base, w * nC / MERGE_WARPS, (w + 1) * nC / MERGE_WARPS,
+                          lane, M8[w], L8[w], acc8[w]);
+    }
+    merge_combine<D>(M8, L8, [&](int w, int i) { return acc8[w][i]; }, lane,
+                     out + (int64_t(t) * Hq + hq) * D, lse ? lse + int64_t(t) * Hq + hq : nullptr);
 }
 
 // ------------------------------------------------------------------ KV-append kernel
@@ -818,11 +934,22 @@ cudaError_t launch_attn_merge(const PagedArgs& a, void* workspace, int chunk_log
     const int maxC = int((a.max_seq_len + chunk - 1) / chunk);
     const float* ws_o = static_cast<const float*>(workspace);
     const float* ws_ml = ws_o + a.total_q * a.hq * int64_t(maxC) * a.head_dim;
-    auto kern = a.head_dim == 64 ? attn_merge_kernel<64> : attn_merge_kernel<128>;
-    return launch_pdl(kern, dim3(unsigned(a.total_q * a.hq)), dim3(MERGE_WARPS * 32), 0, stream,
-                      a.seq_lens, a.cu_q, int(a.batch), int(a.total_q), int(a.max_q),
-                      int(a.max_seq_len), int(a.hq), ws_o, ws_ml, maxC, chunk_log2,
-                      static_cast<__nv_bfloat16*>(out), lse);
+    const int64_t rows = a.total_q * a.hq;
+    // few rows or long rows: a CTA per row, its eight ranges in parallel; many rows of at
+    // most MERGE_UNROLL chunks: a warp per row, all its partials loaded at once (both run
+    // the same tree, so the choice does not change any bit)
+    if (rows < kMergeRowsMin || maxC > MERGE_UNROLL) {
+        auto kern = a.head_dim == 64 ? attn_merge_kernel<64> : attn_merge_kernel<128>;
+        return launch_pdl(kern, dim3(unsigned(rows)), dim3(MERGE_WARPS * 32), 0, stream,
+                          a.seq_lens, a.cu_q, int(a.batch), int(a.total_q), int(a.max_q),
+                          int(a.max_seq_len), int(a.hq), ws_o, ws_ml, maxC, chunk_log2,
+                          static_cast<__nv_bfloat16*>(out), lse);
+    }
+    auto kern = a.head_dim == 64 ? attn_merge_rows_kernel<64> : attn_merge_rows_kernel<128>;
+    return launch_pdl(kern, dim3(unsigned((rows + MERGE_WARPS - 1) / MERGE_WARPS)),
+                      dim3(MERGE_WARPS * 32), 0, stream, a.seq_lens, a.cu_q, int(a.batch),
+                      int(a.total_q), int(a.max_q), int(a.max_seq_len), int(a.hq), ws_o, ws_ml,
+                      maxC, chunk_log2, static_cast<__nv_bfloat16*>(out), lse);
 }
 
 namespace {
