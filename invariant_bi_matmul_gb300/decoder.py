@@ -17,8 +17,10 @@ token the verify block computed at its position; the first mismatch is replaced 
 greedy token, which ends the step.
 
 Contexts: each sequence starts with ``cfg.context`` tokens already in its KV caches.
-``prefill`` computes them from a prompt through the same kernels, in causal blocks of up
-to 8 tokens (the widest verify block); ``start`` instead loads synthetic cache rows
+``prefill`` computes them from a prompt through the same kernels, in causal blocks of
+``prefill_width`` tokens (blocks wider than a verify block go through the chunked-prefill
+attention, which reduces every query exactly as the verify kernel does, so the cache
+bits do not depend on the block width); ``start`` instead loads synthetic cache rows
 (seeded N(0,1) keys and values per sequence and layer, written with bi_kv_append), for
 small checks against the oracle.  Either way a sequence's context depends only on the
 sequence, never on the batch it runs in.
@@ -35,8 +37,8 @@ from typing import Callable, List, Optional, Sequence
 
 import torch
 
-from . import (add, argmax, attn_workspace_size, embedding, kv_append, matmul, rmsnorm, rope,
-               swiglu, verify_block, within_batch_invariant_limit)
+from . import (ATTN_MAX_Q, add, argmax, attn_workspace_size, embedding, kv_append, matmul,
+               prefill_attn, rmsnorm, rope, swiglu, verify_block, within_batch_invariant_limit)
 from .inputs import PAGE_SIZE, DecoderConfig, decoder_context, decoder_first_token, page_permutation
 
 Drafter = Callable[[int, List[int], int], List[int]]
@@ -44,15 +46,17 @@ Drafter = Callable[[int, List[int], int], List[int]]
 
 class GreedyDecoder:
     """A decoder stack with paged KV caches for up to ``max_batch`` sequences of up to
-    ``max_len`` tokens, evaluated in blocks of up to ``max_width`` tokens per sequence."""
+    ``max_len`` tokens, evaluated in blocks of up to ``max_width`` tokens per sequence
+    (``prefill_width`` for prompts, default ``max_width``)."""
 
     def __init__(self, cfg: DecoderConfig, weights: dict, max_batch: int, max_len: int,
                  max_width: int = 4, device="cuda", page_seed: int = 0,
-                 invariant: bool = True):
+                 invariant: bool = True, prefill_width: int = 0):
         self.cfg, self.w = cfg, weights
         self.invariant = invariant
         self.dev = torch.device(device)
         self.max_batch, self.max_len, self.max_width = max_batch, max_len, max_width
+        self.prefill_width = max(prefill_width, max_width)
         c = cfg
         pps = math.ceil(max_len / PAGE_SIZE)
         self.num_pages = max_batch * pps
@@ -64,7 +68,8 @@ class GreedyDecoder:
                         for _ in range(c.layers)]
         self.v_cache = [torch.zeros(shape, dtype=torch.bfloat16, device=self.dev)
                         for _ in range(c.layers)]
-        T = max_batch * max_width
+        T = max_batch * self.prefill_width     # activations: the widest block
+        Td = max_batch * max_width               # logits: decoding blocks only
         bf = dict(dtype=torch.bfloat16, device=self.dev)
         self.h = torch.empty(T, c.hidden, **bf)
         self.x = torch.empty(T, c.hidden, **bf)
@@ -76,8 +81,8 @@ class GreedyDecoder:
         self.g = torch.empty(T, c.inter, **bf)
         self.u = torch.empty(T, c.inter, **bf)
         self.a = torch.empty(T, c.inter, **bf)
-        self.logits = torch.empty(T, c.vocab, dtype=torch.float32, device=self.dev)
-        self.tokens = torch.empty(T, dtype=torch.int32, device=self.dev)
+        self.logits = torch.empty(Td, c.vocab, dtype=torch.float32, device=self.dev)
+        self.tokens = torch.empty(Td, dtype=torch.int32, device=self.dev)
         self.ids = torch.empty(T, dtype=torch.int32, device=self.dev)
         self.seq_lens = torch.empty(max_batch, dtype=torch.int32, device=self.dev)
         self.cu_q = torch.empty(max_batch + 1, dtype=torch.int32, device=self.dev)
@@ -130,8 +135,10 @@ class GreedyDecoder:
         c, w = self.cfg, self.w
         B = self.batch
         T = len(ids)
-        if len(q_lens) != B or sum(q_lens) != T or max(q_lens) > self.max_width:
-            raise ValueError("one block of 1..max_width tokens per sequence")
+        widest = self.max_width if logits else self.prefill_width
+        if len(q_lens) != B or sum(q_lens) != T or max(q_lens) > widest:
+            raise ValueError("one block of 1..max_width (prefill: prefill_width) tokens per "
+                             "sequence")
         lens = [self.cached[b] + q_lens[b] for b in range(B)]
         if max(lens) > self.max_len:
             raise ValueError("sequence longer than max_len")
@@ -163,9 +170,11 @@ class GreedyDecoder:
             rope(q, sl, cq, c.theta)
             rope(k, sl, cq, c.theta)
             kv_append(k, v, self.k_cache[i], self.v_cache[i], bt, sl, cq)
-            verify_block(q, self.k_cache[i], self.v_cache[i], bt, sl, cq, max_q=max(q_lens),
-                         max_seq_len=max(lens), scale=self.scale, out=attn, want_lse=False,
-                         workspace=self.ws)
+            # blocks wider than a verify block: the chunked-prefill kernel (same bits)
+            attend = verify_block if max(q_lens) <= ATTN_MAX_Q else prefill_attn
+            attend(q, self.k_cache[i], self.v_cache[i], bt, sl, cq, max_q=max(q_lens),
+                   max_seq_len=max(lens), scale=self.scale, out=attn, want_lse=False,
+                   workspace=self.ws)
             matmul(attn.view(T, c.heads * c.head_dim), w[p + "wo"], out=o)
             add(h, o, out=h)
             rmsnorm(h, w[p + "mlp_norm"], c.eps, out=x)
@@ -183,14 +192,14 @@ class GreedyDecoder:
     # ------------------------------------------------------------------ prefill
     def prefill(self, prompts: Sequence[Sequence[int]], width: Optional[int] = None) -> None:
         """Puts prompts (one per cache slot 0..len-1, all of one length P) through the
-        stack: tokens 0..P-2 in causal blocks of `width` (default max_width), their K/V
-        into the caches; token P-1 becomes the first input of decoding."""
+        stack: tokens 0..P-2 in causal blocks of `width` (default prefill_width), their
+        K/V into the caches; token P-1 becomes the first input of decoding."""
         B = len(prompts)
         P = len(prompts[0])
-        width = width or self.max_width
+        width = width or self.prefill_width
         if not 1 <= B <= self.max_batch or any(len(p) != P for p in prompts) or P < 1:
             raise ValueError("1..max_batch prompts of one length >= 1")
-        if not 1 <= width <= self.max_width or P - 1 + self.max_width > self.max_len:
+        if not 1 <= width <= self.prefill_width or P - 1 + self.max_width > self.max_len:
             raise ValueError("width or prompt length out of range")
         self.batch = B
         self.cached = [0] * B

@@ -4,7 +4,8 @@
     blocks of 4 with drafted tokens) against the oracle's forward pass fed the same
     tokens;
   * prefill: a prompt put through the stack in blocks of 8 leaves the same cache bits
-    as in blocks of 4 or alone in the batch, and matches the oracle's logits after it;
+    as in blocks of 4, 1 or 7, as in blocks of 40 or 44 (the chunked-prefill attention)
+    and alone in the batch, and matches the oracle's logits after it;
   * invariance at full size: 8 Llama-3-8B-shaped layers, 8192-token prompts prefilled
     through the kernels, 256 greedy steps -- the token traces are identical whether
     decoded token by token or with verify blocks of 4 (drafts replayed, random, or 25%
@@ -184,11 +185,13 @@ def _slot_rows(dec, layer, slot, n):
 def test_tiny_prefill_is_invariant_to_block_width_and_batch(dev):
     cfg, seed, P = inputs.TINY_DECODER, 505, 45
     w = inputs.decoder_weights(cfg, seed, device=dev, std=0.05, norm_std=0.1)
-    dec = GreedyDecoder(cfg, w, max_batch=3, max_len=P + 16, max_width=8, device=dev)
+    dec = GreedyDecoder(cfg, w, max_batch=3, max_len=P + 16, max_width=8, device=dev,
+                        prefill_width=44)
     prompts = [inputs.decoder_prompt(cfg, s, seed, P) for s in range(3)]
     dec.prefill(prompts, width=8)
     batch3 = [[t.clone() for t in _slot_rows(dec, l, 0, P - 1)] for l in range(cfg.layers)]
-    for width in (4, 1, 7):
+    # blocks of 4, 1, 7 (verify kernel) and 40 + 4, 44 (chunked-prefill kernel)
+    for width in (4, 1, 7, 40, 44):
         dec.prefill(prompts[:1], width=width)
         for l in range(cfg.layers):
             k, v = _slot_rows(dec, l, 0, P - 1)
@@ -252,9 +255,10 @@ def test_llama3_8b_8_layer_greedy_traces_identical(dev):
     cfg, seed, steps, width = inputs.LLAMA3_8B_8L, 503, 256, 4
     w = inputs.decoder_weights(cfg, seed, device=dev)
     dec = GreedyDecoder(cfg, w, max_batch=32, max_len=cfg.context + 2 * steps + 16,
-                        max_width=8, device=dev, page_seed=11)
-    # 8193-token prompts: 8192 context tokens prefilled in blocks of 8 through the
-    # kernels, the last one the first input of decoding; one snapshot for every run
+                        max_width=8, device=dev, page_seed=11, prefill_width=256)
+    # 8193-token prompts: 8192 context tokens prefilled in blocks of 256 through the
+    # kernels (the chunked-prefill attention), the last one the first input of decoding;
+    # one snapshot for every run
     t0 = time.perf_counter()
     dec.prefill([inputs.decoder_prompt(cfg, s, seed, cfg.context + 1) for s in range(32)])
     torch.cuda.synchronize()
