@@ -18,7 +18,8 @@
 //     accumulate in tensor memory; head-dim steps of 16 in ascending order);
 //   * the chunk's pages are folded in ascending order with an online softmax against a
 //     reference max m that is raised only when a page's row max exceeds it by more than
-//     2^8 (then O and the row sums are rescaled by exp2(m_old - m_new)); P = exp2(S - m)
+//     2^8 (then O and the row sums are rescaled by 2^(m_old - m_new)); P = 2^(S - m)
+//     (both powers by the hardware's ex2 approximation, see attn_common.cuh)
 //     is rounded to bf16 and O += P V accumulates in tensor memory (tcgen05, the page's
 //     keys in 16-key steps, ascending); each of four warps sums its 16-key slice of the
 //     row key by key, and the four slice sums are added in ascending slice order;
@@ -528,7 +529,7 @@ attn_partial_kernel(const __grid_constant__ CUtensorMap tmap_k,
                 // it by more than 2^8, so p = exp2(s - m_ref) <= 2^8
                 const bool raise = m_page > m_ref + kRescaleLog2 ||
                                    (m_ref == -INFINITY && m_page != -INFINITY);
-                const float factor = raise ? exp2f(m_ref - m_page) : 1.f;  // 0 on the first
+                const float factor = raise ? ex2(m_ref - m_page) : 1.f;  // 0 on the first
                 if (raise) m_ref = m_page;
                 l_run *= factor;
                 // P buffer sb is free once P V of page gi-2 has completed
@@ -555,7 +556,7 @@ attn_partial_kernel(const __grid_constant__ CUtensorMap tmap_k,
                 // p = exp2(s * scale_log2 - m), the row-slice sum by a fixed pairwise tree
                 float pv[KSL];
 #pragma unroll
-                for (int k = 0; k < KSL; ++k) pv[k] = exp2f(fmaf(sl[k], scale_log2, -m_use));
+                for (int k = 0; k < KSL; ++k) pv[k] = ex2(fmaf(sl[k], scale_log2, -m_use));
                 uint32_t pk[KSL / 2];
 #pragma unroll
                 for (int k = 0; k < KSL; k += 2) pk[k / 2] = pack_bf16x2(pv[k], pv[k + 1]);

@@ -19,6 +19,15 @@ constexpr float kRescaleLog2 = 8.0f;  // rescale O only when the row max grows b
 constexpr float kLog2e = 1.4426950408889634f;
 constexpr float kLn2 = 0.6931471805599453f;
 
+// 2^x by the hardware's approximation (PTX ex2.approx.ftz.f32: at most 2 ulp from 2^x;
+// results below 2^-126 flush to +0; 2^-inf = +0).  The softmax of every split-KV kernel
+// takes P and the rescale factors from this one function, so they agree bit for bit.
+__device__ __forceinline__ float ex2(float x) {
+    float y;
+    asm("ex2.approx.ftz.f32 %0, %1;" : "=f"(y) : "f"(x));
+    return y;
+}
+
 // byte offset of (row, 16-byte chunk) in a 128-byte-swizzled box (the TMA SWIZZLE_128B
 // pattern: chunk index XOR row mod 8)
 __device__ __forceinline__ uint32_t swz(int row, int chunk) {

@@ -14,7 +14,8 @@
 //   * per 64-key page: S = Q K^T by tcgen05 (M = 128, N = 64, the head dimension in 16-wide
 //     steps, ascending), keys > pos masked to -inf, the exact page row max, the reference
 //     max m raised only when the page max exceeds it by more than 2^8 (O and the sums then
-//     scaled by exp2(m_old - m_new)), P = exp2(S*scale_log2 - m) rounded to bf16,
+//     scaled by 2^(m_old - m_new)), P = 2^(S*scale_log2 - m) rounded to bf16 (both
+//     powers by the same ex2 as the decode kernel),
 //     O += P V by tcgen05 (N = head_dim, keys in 16-wide steps, ascending), and the row
 //     sum kept as four running sums of the page's 16-key slices (each slice summed by the
 //     same pairwise tree), added in ascending slice order at the end of the chunk;
@@ -473,9 +474,15 @@ attn_prefill_kernel(const __grid_constant__ CUtensorMap tmap_k,
                 if (!wait(&full[s], (gi / NST) & 1u)) break;
                 const bool valid = stage_valid[s] != 0;
                 float sl[PAGE];
+                if (__all_sync(0xffffffffu, valid && page0 + PAGE - 1 <= pos)) {
+                    // every key of the page is visible to every row of the warp
 #pragma unroll
-                for (int kk = 0; kk < PAGE; ++kk)
-                    sl[kk] = (valid && page0 + kk <= pos) ? __uint_as_float(sv[kk]) : -INFINITY;
+                    for (int kk = 0; kk < PAGE; ++kk) sl[kk] = __uint_as_float(sv[kk]);
+                } else {
+#pragma unroll
+                    for (int kk = 0; kk < PAGE; ++kk)
+                        sl[kk] = (valid && page0 + kk <= pos) ? __uint_as_float(sv[kk]) : -INFINITY;
+                }
                 // the exact row max of the page (max does not round: any order)
                 float mt[PAGE / 2];
 #pragma unroll
@@ -487,7 +494,7 @@ attn_prefill_kernel(const __grid_constant__ CUtensorMap tmap_k,
                 const float m_page = mt[0] * scale_log2;
                 const bool raise = m_page > m_ref + kRescaleLog2 ||
                                    (m_ref == -INFINITY && m_page != -INFINITY);
-                const float factor = raise ? exp2f(m_ref - m_page) : 1.f;
+                const float factor = raise ? ex2(m_ref - m_page) : 1.f;
                 if (raise) m_ref = m_page;
 #pragma unroll
                 for (int q4 = 0; q4 < 4; ++q4) l_run[q4] *= factor;
@@ -517,7 +524,7 @@ attn_prefill_kernel(const __grid_constant__ CUtensorMap tmap_k,
                     float pv[16];
 #pragma unroll
                     for (int kk = 0; kk < 16; ++kk)
-                        pv[kk] = exp2f(fmaf(sl[16 * q4 + kk], scale_log2, -m_use));
+                        pv[kk] = ex2(fmaf(sl[16 * q4 + kk], scale_log2, -m_use));
                     uint32_t pk[8];
 #pragma unroll
                     for (int kk = 0; kk < 16; kk += 2) pk[kk / 2] = pack_bf16x2(pv[kk], pv[kk + 1]);
