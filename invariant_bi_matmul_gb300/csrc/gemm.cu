@@ -65,11 +65,11 @@ constexpr int MAX_STAGES = 48;
 constexpr int MAX_SPLITS = 8;               // split-K cluster size (portable maximum)
 constexpr int THREADS = 192;
 constexpr int EPI_THREADS = 128;
-// Quantized W: four more warps (6..9) turn the packed codes of each stage into bf16
+// Quantized W: eight more warps (6..13) turn the packed codes of each stage into bf16
 // operand tiles.  The ring (at most MAX_QSTAGES stages, one K-block each) holds X blocks
 // and packed codes only; the bf16 tiles live in a separate ring of MAX_QWBUF buffers.
-constexpr int QTHREADS = THREADS + 128;
-constexpr int CONV_WARPS = 4;
+constexpr int QTHREADS = THREADS + 256;
+constexpr int CONV_WARPS = 8;
 constexpr int MAX_QSTAGES = 16;
 constexpr int MAX_QWBUF = 4;
 constexpr int Q_SROW = 16;  // bytes of staged scales (or biases) per tile row and stage
@@ -260,7 +260,7 @@ gemm_kernel(const __grid_constant__ CUtensorMap tmap_x, const __grid_constant__ 
         }
         if (QUANT) {
             for (int b = 0; b < args.wbufs; ++b) {
-                mbar_init(&conv[b], CONV_WARPS / 2);  // the two warps of a group
+                mbar_init(&conv[b], CONV_WARPS / 2);  // the four warps of a group
                 mbar_init(&wfree[b], 1);
             }
         }
@@ -647,18 +647,20 @@ gemm_kernel(const __grid_constant__ CUtensorMap tmap_x, const __grid_constant__ 
         }
     } else if (QUANT) {
         // --------------------------------------------------------------- converters
-        // Two groups of two converter warps turn the stages' packed codes into the bf16 W
+        // Two groups of four converter warps turn the stages' packed codes into the bf16 W
         // tiles the MMA reads (K-major, 128-byte swizzle: the layout a TMA copy of bf16 W
         // would give), once a stage's copies have landed and the tile buffer is free.
         // Group g takes the iterations i = g mod 2; the ring and the buffer ring both have
         // an even length, so a group takes every use of its stages and buffers in order and
-        // waits on each barrier one phase at a time.  Thread ct of a group's 64 converts whole rows of the K-block: tile rows
-        // ct, ct+64, ...  Its rows' scales (and biases) for its next stage are loaded
-        // from global memory before it waits for the current one, so their latency hides
-        // behind the conversion.  Every dequantized value except the affine ones is exact
-        // in bf16; affine is fmaf(scale, q, bias) rounded to bf16.  Rows past N and
+        // waits on each barrier one phase at a time.  A group's 128 threads work in two
+        // halves of 64 (a warp pair each): thread ct of half h converts columns 32h..32h+31
+        // of the K-block in tile rows ct, ct+64, ...  Without staged scales, a thread's
+        // scales (and biases) for its next stage are loaded from global memory before it
+        // waits for the current one.  Every dequantized value except the affine ones is
+        // exact in bf16; affine is fmaf(scale, q, bias) rounded to bf16.  Rows past N and
         // columns past K become zeros.
-        const int cgrp = (warp - 6) >> 1;
+        const int cgrp = (warp - 6) >> 2;
+        const int half = ((warp - 6) >> 1) & 1;
         const int ct = ((warp - 6) & 1) * 32 + lane;
         // the tile's rows in units of 64 (a quantized tile is 64, 128 or 256 rows)
         constexpr int QR = NSUB * BN >= 64 ? NSUB * BN / 64 : 1;
@@ -676,10 +678,12 @@ gemm_kernel(const __grid_constant__ CUtensorMap tmap_x, const __grid_constant__ 
             constexpr int F = decltype(tag)::value;
             constexpr bool AFF = F >= 3;
             constexpr int G = F == 1 ? 4 : 2;  // scale segments per K-block row
+            constexpr int GH = G / 2;          // ... per half row
             constexpr int SEG = BK / G;        // columns per segment (<= the group size)
             constexpr int RW = (F == 2 || F == 4) ? BK / 4 : BK / 8;  // code words per row
-            // raw scale (and bias) codes of iteration j's rows, one per segment
-            auto fetch = [&](int j, uint32_t (&sc)[QR][G], uint32_t (&bs)[QR][G]) {
+            constexpr int HW = RW / 2;         // ... per half row
+            // raw scale (and bias) codes of iteration j's rows, one per segment of the half
+            auto fetch = [&](int j, uint32_t (&sc)[QR][GH], uint32_t (&bs)[QR][GH]) {
                 const int t = first_tile + (j / nkb_t) * tile_step;
                 const int kb = kb0 + j % nkb_t;
                 const int n0 = (t % n_tiles) * tile_n;
@@ -687,28 +691,28 @@ gemm_kernel(const __grid_constant__ CUtensorMap tmap_x, const __grid_constant__ 
                 for (int q = 0; q < QR; ++q) {
                     const int n = n0 + ct + 64 * q;
 #pragma unroll
-                    for (int g = 0; g < G; ++g) {
-                        const int k = kb * BK + g * SEG;
-                        sc[q][g] = 0u;
-                        bs[q][g] = 0u;
+                    for (int gg = 0; gg < GH; ++gg) {
+                        const int k = kb * BK + (half * GH + gg) * SEG;
+                        sc[q][gg] = 0u;
+                        bs[q][gg] = 0u;
                         if (n < N && k < K) {
                             const int64_t gi = int64_t(k >> gsh);
                             if (AFF) {
-                                sc[q][g] = __ldg(qs16 + int64_t(n) * args.lds + gi);
-                                bs[q][g] = __ldg(args.qbiases + int64_t(n) * args.ldb + gi);
+                                sc[q][gg] = __ldg(qs16 + int64_t(n) * args.lds + gi);
+                                bs[q][gg] = __ldg(args.qbiases + int64_t(n) * args.ldb + gi);
                             } else {
-                                sc[q][g] = __ldg(qs8 + int64_t(n) * args.lds + gi);
+                                sc[q][gg] = __ldg(qs8 + int64_t(n) * args.lds + gi);
                             }
                         }
                     }
                 }
             };
-            uint32_t sc[QR][G] = {}, bs[QR][G] = {};
+            uint32_t sc[QR][GH] = {}, bs[QR][GH] = {};
             if (!staged && cgrp < iters) fetch(cgrp, sc, bs);
             uint32_t stage = uint32_t(cgrp), phase = 0;
             uint32_t wb = uint32_t(cgrp), wphase = 0;
             for (int j = cgrp; j < iters; j += 2) {
-                uint32_t nsc[QR][G] = {}, nbs[QR][G] = {};
+                uint32_t nsc[QR][GH] = {}, nbs[QR][GH] = {};
                 if (!staged && j + 2 < iters) fetch(j + 2, nsc, nbs);
                 const int t = first_tile + (j / nkb_t) * tile_step;
                 const int kb = kb0 + j % nkb_t;
@@ -727,13 +731,13 @@ gemm_kernel(const __grid_constant__ CUtensorMap tmap_x, const __grid_constant__ 
                     for (int q = 0; q < QR; ++q) {
                         const int r = ct + 64 * q;
 #pragma unroll
-                        for (int g = 0; g < G; ++g) {
-                            const int gi = ((kb * BK + g * SEG) >> gsh) - xs;
+                        for (int gg = 0; gg < GH; ++gg) {
+                            const int gi = ((kb * BK + (half * GH + gg) * SEG) >> gsh) - xs;
                             if (AFF) {
-                                sc[q][g] = reinterpret_cast<const uint16_t*>(ss)[r * (Q_SROW / 2) + gi];
-                                bs[q][g] = reinterpret_cast<const uint16_t*>(ss + s_blk)[r * (Q_SROW / 2) + gi];
+                                sc[q][gg] = reinterpret_cast<const uint16_t*>(ss)[r * (Q_SROW / 2) + gi];
+                                bs[q][gg] = reinterpret_cast<const uint16_t*>(ss + s_blk)[r * (Q_SROW / 2) + gi];
                             } else {
-                                sc[q][g] = ss[r * Q_SROW + gi];
+                                sc[q][gg] = ss[r * Q_SROW + gi];
                             }
                         }
                     }
@@ -742,26 +746,28 @@ gemm_kernel(const __grid_constant__ CUtensorMap tmap_x, const __grid_constant__ 
                 for (int q = 0; q < QR; ++q) {
                     const int r = ct + 64 * q;
                     const bool row_live = n0 + r < N;
-                    uint32_t cw[RW];
+                    uint32_t cw[HW];  // the code words of this half row
 #pragma unroll
-                    for (int i = 0; i < RW / 4; ++i) {
-                        const uint4 u = *reinterpret_cast<const uint4*>(raw + r * (RW * 4) + 16 * i);
+                    for (int i = 0; i < HW / 4; ++i) {
+                        const uint4 u = *reinterpret_cast<const uint4*>(raw + r * (RW * 4) +
+                                                                        half * (HW * 4) + 16 * i);
                         cw[4 * i] = u.x;
                         cw[4 * i + 1] = u.y;
                         cw[4 * i + 2] = u.z;
                         cw[4 * i + 3] = u.w;
                     }
-                    float scf[G], bsf[G];
+                    float scf[GH], bsf[GH];
 #pragma unroll
-                    for (int g = 0; g < G; ++g) {
-                        if (F == 0 || F == 2) scf[g] = dec_e8m0(sc[q][g]);
-                        else if (F == 1) scf[g] = dec_e4m3(sc[q][g]);
-                        else scf[g] = widen16(uint16_t(sc[q][g]), false);
-                        bsf[g] = AFF ? widen16(uint16_t(bs[q][g]), false) : 0.f;
+                    for (int gg = 0; gg < GH; ++gg) {
+                        if (F == 0 || F == 2) scf[gg] = dec_e8m0(sc[q][gg]);
+                        else if (F == 1) scf[gg] = dec_e4m3(sc[q][gg]);
+                        else scf[gg] = widen16(uint16_t(sc[q][gg]), false);
+                        bsf[gg] = AFF ? widen16(uint16_t(bs[q][gg]), false) : 0.f;
                     }
                     uint8_t* wrow = wt + q * (64 * BK * 2) + (ct >> 3) * 1024 + (ct & 7) * 128;
 #pragma unroll
-                    for (int p = 0; p < 8; ++p) {  // 8-column pieces (16 bytes of bf16)
+                    for (int pp = 0; pp < 4; ++pp) {  // 8-column pieces (16 bytes of bf16)
+                        const int p = 4 * half + pp;
                         const bool live = row_live && kb * BK + 8 * p < K;  // K % 16 == 0
                         uint4 pk;
                         if (F == 0 || F == 1) {
@@ -769,8 +775,8 @@ gemm_kernel(const __grid_constant__ CUtensorMap tmap_x, const __grid_constant__ 
                             // is exact in bf16 (or overflows), so bf16 arithmetic rounds
                             // nothing
                             uint32_t o[4];
-                            e2m1x8_to_bf16(cw[p], o);
-                            const uint32_t s2 = (__float_as_uint(scf[(8 * p) / SEG]) >> 16) * 0x10001u;
+                            e2m1x8_to_bf16(cw[pp], o);
+                            const uint32_t s2 = (__float_as_uint(scf[(8 * pp) / SEG]) >> 16) * 0x10001u;
                             pk.x = live ? mul_bf16x2(o[0], s2) : 0u;
                             pk.y = live ? mul_bf16x2(o[1], s2) : 0u;
                             pk.z = live ? mul_bf16x2(o[2], s2) : 0u;
@@ -778,13 +784,13 @@ gemm_kernel(const __grid_constant__ CUtensorMap tmap_x, const __grid_constant__ 
                             *reinterpret_cast<uint4*>(wrow + ((p ^ (ct & 7)) << 4)) = pk;
                             continue;
                         }
-                        const float s = scf[(8 * p) / SEG], b = bsf[(8 * p) / SEG];
+                        const float s = scf[(8 * pp) / SEG], b = bsf[(8 * pp) / SEG];
                         float v[8];
                         if (live) {
                             if (F == 2) {  // FP8 E4M3 codes times the block scale
 #pragma unroll
                                 for (int e = 0; e < 4; ++e) {
-                                    const uint32_t pair = (cw[2 * p + (e >> 1)] >> (16 * (e & 1))) & 0xffffu;
+                                    const uint32_t pair = (cw[2 * pp + (e >> 1)] >> (16 * (e & 1))) & 0xffffu;
                                     const float2 f = h2_to_f2(cvt_e4m3x2(pair));
                                     v[2 * e] = f.x * s;
                                     v[2 * e + 1] = f.y * s;
@@ -792,9 +798,9 @@ gemm_kernel(const __grid_constant__ CUtensorMap tmap_x, const __grid_constant__ 
                             } else if (F == 4) {  // affine 8-bit: fmaf(scale, q, bias)
 #pragma unroll
                                 for (int e = 0; e < 8; ++e)
-                                    v[e] = fmaf(s, byte_to_f32(cw[2 * p + (e >> 2)], e & 3), b);
+                                    v[e] = fmaf(s, byte_to_f32(cw[2 * pp + (e >> 2)], e & 3), b);
                             } else {  // affine 4-bit: nibbles spread to bytes first
-                                const uint32_t ev = cw[p] & 0x0f0f0f0fu, od = (cw[p] >> 4) & 0x0f0f0f0fu;
+                                const uint32_t ev = cw[pp] & 0x0f0f0f0fu, od = (cw[pp] >> 4) & 0x0f0f0f0fu;
 #pragma unroll
                                 for (int e = 0; e < 8; ++e)
                                     v[e] = fmaf(s, byte_to_f32(e & 1 ? od : ev, e >> 1), b);
@@ -826,9 +832,9 @@ gemm_kernel(const __grid_constant__ CUtensorMap tmap_x, const __grid_constant__ 
 #pragma unroll
                 for (int q = 0; q < QR; ++q)
 #pragma unroll
-                    for (int g = 0; g < G; ++g) {
-                        sc[q][g] = nsc[q][g];
-                        bs[q][g] = nbs[q][g];
+                    for (int gg = 0; gg < GH; ++gg) {
+                        sc[q][gg] = nsc[q][gg];
+                        bs[q][gg] = nbs[q][gg];
                     }
             }
         };
