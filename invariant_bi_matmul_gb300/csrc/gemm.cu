@@ -652,18 +652,20 @@ gemm_kernel(const __grid_constant__ CUtensorMap tmap_x, const __grid_constant__ 
         // would give), once a stage's copies have landed and the tile buffer is free.
         // Group g takes the iterations i = g mod 2; the ring and the buffer ring both have
         // an even length, so a group takes every use of its stages and buffers in order and
-        // waits on each barrier one phase at a time.  A group's 128 threads work in two
-        // halves of 64 (a warp pair each): thread ct of half h converts columns 32h..32h+31
-        // of the K-block in tile rows ct, ct+64, ...  Without staged scales, a thread's
+        // waits on each barrier one phase at a time.  A group's 128 threads split each
+        // K-block row into PARTS parts: tiles of 64 rows or more in two halves of 64
+        // threads (a warp pair each; thread ct of half h converts columns 32h..32h+31 of
+        // tile rows ct, ct+64, ...), 32-row tiles in four quarters of 32 (a warp each;
+        // lane ct converts columns 16h..16h+15 of row ct).  Without staged scales, a thread's
         // scales (and biases) for its next stage are loaded from global memory before it
         // waits for the current one.  Every dequantized value except the affine ones is
         // exact in bf16; affine is fmaf(scale, q, bias) rounded to bf16.  Rows past N and
         // columns past K become zeros.
+        constexpr int PARTS = NSUB * BN >= 64 ? 2 : 4;        // threads per tile row
+        constexpr int QR = NSUB * BN >= 64 ? NSUB * BN / 64 : 1;  // rows per thread
         const int cgrp = (warp - 6) >> 2;
-        const int half = ((warp - 6) >> 1) & 1;
-        const int ct = ((warp - 6) & 1) * 32 + lane;
-        // the tile's rows in units of 64 (a quantized tile is 64, 128 or 256 rows)
-        constexpr int QR = NSUB * BN >= 64 ? NSUB * BN / 64 : 1;
+        const int half = PARTS == 2 ? ((warp - 6) >> 1) & 1 : (warp - 6) & 3;  // the part
+        const int ct = PARTS == 2 ? ((warp - 6) & 1) * 32 + lane : lane;
         const uint8_t* qs8 = static_cast<const uint8_t*>(args.qscales);
         const uint16_t* qs16 = static_cast<const uint16_t*>(args.qscales);
         const int nkb_t = kb1 - kb0;
@@ -678,10 +680,12 @@ gemm_kernel(const __grid_constant__ CUtensorMap tmap_x, const __grid_constant__ 
             constexpr int F = decltype(tag)::value;
             constexpr bool AFF = F >= 3;
             constexpr int G = F == 1 ? 4 : 2;  // scale segments per K-block row
-            constexpr int GH = G / 2;          // ... per half row
             constexpr int SEG = BK / G;        // columns per segment (<= the group size)
+            constexpr int PP = 8 / PARTS;      // 8-column pieces per part
+            constexpr int GH = (PP * 8 + SEG - 1) / SEG;  // segments a part spans
             constexpr int RW = (F == 2 || F == 4) ? BK / 4 : BK / 8;  // code words per row
-            constexpr int HW = RW / 2;         // ... per half row
+            constexpr int HW = RW / PARTS;     // ... per part
+            const int seg0 = (half * PP * 8) / SEG;  // the part's first segment
             // raw scale (and bias) codes of iteration j's rows, one per segment of the half
             auto fetch = [&](int j, uint32_t (&sc)[QR][GH], uint32_t (&bs)[QR][GH]) {
                 const int t = first_tile + (j / nkb_t) * tile_step;
@@ -692,7 +696,7 @@ gemm_kernel(const __grid_constant__ CUtensorMap tmap_x, const __grid_constant__ 
                     const int n = n0 + ct + 64 * q;
 #pragma unroll
                     for (int gg = 0; gg < GH; ++gg) {
-                        const int k = kb * BK + (half * GH + gg) * SEG;
+                        const int k = kb * BK + (seg0 + gg) * SEG;
                         sc[q][gg] = 0u;
                         bs[q][gg] = 0u;
                         if (n < N && k < K) {
@@ -732,7 +736,7 @@ gemm_kernel(const __grid_constant__ CUtensorMap tmap_x, const __grid_constant__ 
                         const int r = ct + 64 * q;
 #pragma unroll
                         for (int gg = 0; gg < GH; ++gg) {
-                            const int gi = ((kb * BK + (half * GH + gg) * SEG) >> gsh) - xs;
+                            const int gi = ((kb * BK + (seg0 + gg) * SEG) >> gsh) - xs;
                             if (AFF) {
                                 sc[q][gg] = reinterpret_cast<const uint16_t*>(ss)[r * (Q_SROW / 2) + gi];
                                 bs[q][gg] = reinterpret_cast<const uint16_t*>(ss + s_blk)[r * (Q_SROW / 2) + gi];
@@ -746,15 +750,21 @@ gemm_kernel(const __grid_constant__ CUtensorMap tmap_x, const __grid_constant__ 
                 for (int q = 0; q < QR; ++q) {
                     const int r = ct + 64 * q;
                     const bool row_live = n0 + r < N;
-                    uint32_t cw[HW];  // the code words of this half row
+                    uint32_t cw[HW];  // the code words of this part of the row
+                    const uint8_t* crow = raw + r * (RW * 4) + half * (HW * 4);
+                    if constexpr (HW >= 4) {
 #pragma unroll
-                    for (int i = 0; i < HW / 4; ++i) {
-                        const uint4 u = *reinterpret_cast<const uint4*>(raw + r * (RW * 4) +
-                                                                        half * (HW * 4) + 16 * i);
-                        cw[4 * i] = u.x;
-                        cw[4 * i + 1] = u.y;
-                        cw[4 * i + 2] = u.z;
-                        cw[4 * i + 3] = u.w;
+                        for (int i = 0; i < HW / 4; ++i) {
+                            const uint4 u = *reinterpret_cast<const uint4*>(crow + 16 * i);
+                            cw[4 * i] = u.x;
+                            cw[4 * i + 1] = u.y;
+                            cw[4 * i + 2] = u.z;
+                            cw[4 * i + 3] = u.w;
+                        }
+                    } else {
+                        const uint2 u = *reinterpret_cast<const uint2*>(crow);
+                        cw[0] = u.x;
+                        cw[1 % HW] = u.y;
                     }
                     float scf[GH], bsf[GH];
 #pragma unroll
@@ -766,8 +776,12 @@ gemm_kernel(const __grid_constant__ CUtensorMap tmap_x, const __grid_constant__ 
                     }
                     uint8_t* wrow = wt + q * (64 * BK * 2) + (ct >> 3) * 1024 + (ct & 7) * 128;
 #pragma unroll
-                    for (int pp = 0; pp < 4; ++pp) {  // 8-column pieces (16 bytes of bf16)
-                        const int p = 4 * half + pp;
+                    for (int pp = 0; pp < PP; ++pp) {  // 8-column pieces (16 bytes of bf16)
+                        const int p = PP * half + pp;
+                        // the piece's segment within the part (the part starts on a
+                        // segment boundary, or -- quarters of 32-column segments -- inside
+                        // one): known at compile time
+                        const int gg = PARTS == 2 ? (8 * pp) / SEG : 0;
                         const bool live = row_live && kb * BK + 8 * p < K;  // K % 16 == 0
                         uint4 pk;
                         if (F == 0 || F == 1) {
@@ -776,7 +790,7 @@ gemm_kernel(const __grid_constant__ CUtensorMap tmap_x, const __grid_constant__ 
                             // nothing
                             uint32_t o[4];
                             e2m1x8_to_bf16(cw[pp], o);
-                            const uint32_t s2 = (__float_as_uint(scf[(8 * pp) / SEG]) >> 16) * 0x10001u;
+                            const uint32_t s2 = (__float_as_uint(scf[gg]) >> 16) * 0x10001u;
                             pk.x = live ? mul_bf16x2(o[0], s2) : 0u;
                             pk.y = live ? mul_bf16x2(o[1], s2) : 0u;
                             pk.z = live ? mul_bf16x2(o[2], s2) : 0u;
@@ -784,7 +798,7 @@ gemm_kernel(const __grid_constant__ CUtensorMap tmap_x, const __grid_constant__ 
                             *reinterpret_cast<uint4*>(wrow + ((p ^ (ct & 7)) << 4)) = pk;
                             continue;
                         }
-                        const float s = scf[(8 * pp) / SEG], b = bsf[(8 * pp) / SEG];
+                        const float s = scf[gg], b = bsf[gg];
                         float v[8];
                         if (live) {
                             if (F == 2) {  // FP8 E4M3 codes times the block scale
@@ -1105,9 +1119,8 @@ cudaError_t launch_qgemm(const DeviceInfo& dev, const void* x, int64_t ldx, cons
     // the invariant schedule with one K-block per stage and 128-row CTA tiles
     const int64_t m_tiles = (M + BM - 1) / BM;
     const int a_rows = m_tiles == 1 ? int((M + 7) / 8 * 8) : BM;
-    // tiles of 64, 128 or 256 rows of W (the converters work in 64-row units): the widest
-    // that still gives every SM a tile
-    constexpr int QMIN = 64 / BN;
+    // tiles of 32 to 256 rows of W: the widest that still gives every SM a tile
+    constexpr int QMIN = 1;
     int nsub = QMIN;
     for (int ns = MAX_NSUB; ns > QMIN; ns >>= 1) {
         if (m_tiles * ((N + int64_t(ns) * BN - 1) / (int64_t(ns) * BN)) >= dev.num_sms) {
@@ -1189,10 +1202,12 @@ cudaError_t launch_qgemm(const DeviceInfo& dev, const void* x, int64_t ldx, cons
     const int64_t tiles = m_tiles * ((N + int64_t(nsub) * BN - 1) / (int64_t(nsub) * BN));
     const int grid = int(tiles < dev.num_sms ? tiles : dev.num_sms);
     switch (nsub) {
-        case QMIN: return y_f32 ? launch_q<true, QMIN>(dev, mx, mw, ms, mb, a, grid, stream)
-                                : launch_q<false, QMIN>(dev, mx, mw, ms, mb, a, grid, stream);
-        case 2 * QMIN: return y_f32 ? launch_q<true, 2 * QMIN>(dev, mx, mw, ms, mb, a, grid, stream)
-                                    : launch_q<false, 2 * QMIN>(dev, mx, mw, ms, mb, a, grid, stream);
+        case 1: return y_f32 ? launch_q<true, 1>(dev, mx, mw, ms, mb, a, grid, stream)
+                             : launch_q<false, 1>(dev, mx, mw, ms, mb, a, grid, stream);
+        case 2: return y_f32 ? launch_q<true, 2>(dev, mx, mw, ms, mb, a, grid, stream)
+                             : launch_q<false, 2>(dev, mx, mw, ms, mb, a, grid, stream);
+        case 4: return y_f32 ? launch_q<true, 4>(dev, mx, mw, ms, mb, a, grid, stream)
+                             : launch_q<false, 4>(dev, mx, mw, ms, mb, a, grid, stream);
         default: return y_f32 ? launch_q<true, MAX_NSUB>(dev, mx, mw, ms, mb, a, grid, stream)
                               : launch_q<false, MAX_NSUB>(dev, mx, mw, ms, mb, a, grid, stream);
     }
