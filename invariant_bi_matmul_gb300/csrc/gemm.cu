@@ -72,7 +72,8 @@ constexpr int QTHREADS = THREADS + 256;
 constexpr int CONV_WARPS = 8;
 constexpr int MAX_QSTAGES = 16;
 constexpr int MAX_QWBUF = 4;
-constexpr int Q_SROW = 16;  // bytes of staged scales (or biases) per tile row and stage
+constexpr int Q_SROW = 16;     // bytes of staged scales (or biases) per tile row, one K-block
+constexpr int Q_SROW_KBS = 64; // ... for stages of several K-blocks (up to 8)
 constexpr int B_KB_BYTES = BN * BK * 2;     // one instruction tile's W block per K-block
 constexpr int A_MMA_BYTES = BM * BK * 2;    // 16 KiB: what one MMA reads from an X block
 constexpr int SMEM_BYTES = 220 * 1024;      // dynamic shared memory per CTA
@@ -118,9 +119,10 @@ struct GemmArgs {
     int64_t ldb;
     int q_kb_bytes;
     int wbufs;         // bf16 W tile buffers (even, <= MAX_QWBUF)
-    int q_staged;      // the scales (and biases) come with the codes, by TMA, Q_SROW bytes
+    int q_staged;      // the scales (and biases) come with the codes, by TMA, q_srow bytes
                        // per row and stage starting at a 16-byte boundary; else the
-                       // converters load them from global memory
+                       // converters load them from global memory (then kbs = 1)
+    int q_srow;        // Q_SROW (one K-block per stage) or Q_SROW_KBS
 };
 
 // ----------------------------------------------------------- quantized-code decoding
@@ -208,14 +210,15 @@ gemm_kernel(const __grid_constant__ CUtensorMap tmap_x, const __grid_constant__ 
     const int b_bytes = nsub * B_KB_BYTES;        // one W block (one K-block, every sub-tile)
     uint8_t* sA = smem;                           // S*kbs X blocks
     uint8_t* sB = smem + S * kbs * a_bytes;       // S*kbs W blocks (QUANT: wbufs W tiles)
-    uint8_t* sR = sB + (QUANT ? args.wbufs : S * kbs) * b_bytes;  // QUANT: S code blocks
+    uint8_t* sR = sB + (QUANT ? args.wbufs : S) * kbs * b_bytes;  // QUANT: S code blocks
     // QUANT stage: the packed codes, then (staged) a block of scales and, affine, biases
     const bool q_aff = args.qfmt >= 3;
-    const int codes_bytes = nsub * BN * args.q_kb_bytes;
-    const int s_blk = nsub * BN * Q_SROW;
+    const int codes_bytes = nsub * BN * args.q_kb_bytes * kbs;  // rows of kbs K-blocks
+    const int s_row = args.q_srow;
+    const int s_blk = nsub * BN * s_row;
     const int r_bytes = codes_bytes + (args.q_staged ? (q_aff ? 2 : 1) * s_blk : 0);
     const int gsh = QUANT ? 31 - __clz(args.gs) : 0;  // the group size is a power of two
-    const int s_epb = q_aff ? Q_SROW / 2 : Q_SROW;     // staged elements per row
+    const int s_epb = q_aff ? Q_SROW / 2 : Q_SROW;     // window alignment (16 bytes), elements
     uint64_t* full = reinterpret_cast<uint64_t*>(smem + RING_BYTES);
     uint64_t* empty = full + MAX_STAGES;
     uint64_t* tfull = empty + MAX_STAGES;
@@ -669,9 +672,10 @@ gemm_kernel(const __grid_constant__ CUtensorMap tmap_x, const __grid_constant__ 
         const uint8_t* qs8 = static_cast<const uint8_t*>(args.qscales);
         const uint16_t* qs16 = static_cast<const uint16_t*>(args.qscales);
         const int nkb_t = kb1 - kb0;
+        const int spt = (nkb_t + kbs - 1) / kbs;  // stages per tile
         const int tiles_mine = first_tile < num_tiles
                                    ? (num_tiles - 1 - first_tile) / tile_step + 1 : 0;
-        const int iters = tiles_mine * nkb_t;
+        const int iters = tiles_mine * spt;
         const bool staged = args.q_staged != 0;
         if (!args.w_early) pdl_wait();  // scales may come from the previous grid
         bool ok = true;
@@ -688,7 +692,7 @@ gemm_kernel(const __grid_constant__ CUtensorMap tmap_x, const __grid_constant__ 
             const int seg0 = (half * PP * 8) / SEG;  // the part's first segment
             // raw scale (and bias) codes of iteration j's rows, one per segment of the half
             auto fetch = [&](int j, uint32_t (&sc)[QR][GH], uint32_t (&bs)[QR][GH]) {
-                const int t = first_tile + (j / nkb_t) * tile_step;
+                const int t = first_tile + (j / nkb_t) * tile_step;  // (kbs = 1 here)
                 const int kb = kb0 + j % nkb_t;
                 const int n0 = (t % n_tiles) * tile_n;
 #pragma unroll
@@ -718,8 +722,9 @@ gemm_kernel(const __grid_constant__ CUtensorMap tmap_x, const __grid_constant__ 
             for (int j = cgrp; j < iters; j += 2) {
                 uint32_t nsc[QR][GH] = {}, nbs[QR][GH] = {};
                 if (!staged && j + 2 < iters) fetch(j + 2, nsc, nbs);
-                const int t = first_tile + (j / nkb_t) * tile_step;
-                const int kb = kb0 + j % nkb_t;
+                const int t = first_tile + (j / spt) * tile_step;
+                const int kbf = kb0 + (j % spt) * kbs;      // the stage's first K-block
+                const int nk = kb1 - kbf < kbs ? kb1 - kbf : kbs;
                 const int n0 = (t % n_tiles) * tile_n;
                 if (!mbar_wait_warp(&full[stage], phase, abort_flag) ||
                     !mbar_wait_warp(&wfree[wb], wphase ^ 1u, abort_flag)) {
@@ -727,9 +732,14 @@ gemm_kernel(const __grid_constant__ CUtensorMap tmap_x, const __grid_constant__ 
                     break;
                 }
                 const uint8_t* raw = sR + stage * r_bytes;
-                uint8_t* wt = sB + wb * b_bytes;
-                if (staged) {  // this stage's scales (and biases) from shared memory
-                    const int xs = ((kb * BK) >> gsh) & ~(s_epb - 1);
+                // the staged scale window starts at the 16-byte boundary at or below the
+                // stage's first group
+                const int xs = ((kbf * BK) >> gsh) & ~(s_epb - 1);
+#pragma unroll 1
+                for (int ki = 0; ki < nk; ++ki) {  // the stage's K-blocks
+                const int kb = kbf + ki;
+                uint8_t* wt = sB + (wb * kbs + ki) * b_bytes;
+                if (staged) {  // this K-block's scales (and biases) from shared memory
                     const uint8_t* ss = raw + codes_bytes;
 #pragma unroll
                     for (int q = 0; q < QR; ++q) {
@@ -738,10 +748,10 @@ gemm_kernel(const __grid_constant__ CUtensorMap tmap_x, const __grid_constant__ 
                         for (int gg = 0; gg < GH; ++gg) {
                             const int gi = ((kb * BK + (seg0 + gg) * SEG) >> gsh) - xs;
                             if (AFF) {
-                                sc[q][gg] = reinterpret_cast<const uint16_t*>(ss)[r * (Q_SROW / 2) + gi];
-                                bs[q][gg] = reinterpret_cast<const uint16_t*>(ss + s_blk)[r * (Q_SROW / 2) + gi];
+                                sc[q][gg] = reinterpret_cast<const uint16_t*>(ss)[r * (s_row / 2) + gi];
+                                bs[q][gg] = reinterpret_cast<const uint16_t*>(ss + s_blk)[r * (s_row / 2) + gi];
                             } else {
-                                sc[q][gg] = ss[r * Q_SROW + gi];
+                                sc[q][gg] = ss[r * s_row + gi];
                             }
                         }
                     }
@@ -751,7 +761,7 @@ gemm_kernel(const __grid_constant__ CUtensorMap tmap_x, const __grid_constant__ 
                     const int r = ct + 64 * q;
                     const bool row_live = n0 + r < N;
                     uint32_t cw[HW];  // the code words of this part of the row
-                    const uint8_t* crow = raw + r * (RW * 4) + half * (HW * 4);
+                    const uint8_t* crow = raw + r * (kbs * RW * 4) + ki * (RW * 4) + half * (HW * 4);
                     if constexpr (HW >= 4) {
 #pragma unroll
                         for (int i = 0; i < HW / 4; ++i) {
@@ -830,6 +840,7 @@ gemm_kernel(const __grid_constant__ CUtensorMap tmap_x, const __grid_constant__ 
                         *reinterpret_cast<uint4*>(wrow + ((p ^ (ct & 7)) << 4)) = pk;
                     }
                 }
+                }  // K-blocks of the stage
                 fence_proxy_async_smem();  // generic writes, read by the MMA (async proxy)
                 __syncwarp();
                 if (lane == 0) mbar_arrive(&conv[wb]);
@@ -1133,44 +1144,70 @@ cudaError_t launch_qgemm(const DeviceInfo& dev, const void* x, int64_t ldx, cons
     const int q_kb_bytes = eight ? BK : BK / 2;
     // Scales (and biases) travel with the codes, by TMA, when their rows start on 16-byte
     // boundaries (a tensor map's rule); else the converters load them themselves.
-    CUtensorMap ms, mb;
-    const int64_t groups = K / gs;
-    bool staged = false;
-    if (reinterpret_cast<uintptr_t>(scales) % 16 == 0 && (lds * (aff ? 2 : 1)) % 16 == 0 &&
-        (!aff || (reinterpret_cast<uintptr_t>(biases) % 16 == 0 && (ldb * 2) % 16 == 0))) {
-        staged = aff ? tmap_2d_u16(&ms, scales, uint64_t(groups), uint64_t(N), uint64_t(lds * 2),
-                                   Q_SROW / 2, uint32_t(nsub * BN)) &&
-                           tmap_2d_u16(&mb, biases, uint64_t(groups), uint64_t(N),
-                                       uint64_t(ldb * 2), Q_SROW / 2, uint32_t(nsub * BN))
-                     : tmap_2d_u8(&ms, scales, uint64_t(groups), uint64_t(N), uint64_t(lds),
-                                  Q_SROW, uint32_t(nsub * BN));
-    }
-    // the ring's stages hold an X block and a packed-code block (and the staged scales);
-    // the bf16 tiles the converters write get their own buffers: four when the ring can
-    // still be four stages deep, else two
+    const bool stageable =
+        reinterpret_cast<uintptr_t>(scales) % 16 == 0 && (lds * (aff ? 2 : 1)) % 16 == 0 &&
+        (!aff || (reinterpret_cast<uintptr_t>(biases) % 16 == 0 && (ldb * 2) % 16 == 0));
+    // One M-tile (small M): stages of several K-blocks (a code box of at most 256 bytes a
+    // row, a 64-byte scale window covering them), so the per-stage copies, barriers and
+    // commits are paid once per several K-blocks; they need staged scales.
     const int64_t a_bytes = int64_t(a_rows) * BK * 2;
-    const int64_t blk = a_bytes + int64_t(nsub) * BN * q_kb_bytes +
-                        (staged ? (aff ? 2 : 1) * int64_t(nsub) * BN * Q_SROW : 0);
-    const int64_t b_bytes = int64_t(nsub) * B_KB_BYTES;
-    int wbufs = 0, stages = 0;
-    for (int wb = MAX_QWBUF; wb >= 2; wb -= 2) {
-        int st = int((RING_BYTES - wb * b_bytes) / blk);
-        if (st > MAX_QSTAGES) st = MAX_QSTAGES;
-        st &= ~1;  // even: each of the two converter groups owns every other stage
-        if (st >= 4 || (wb == 2 && st >= 2)) {
-            wbufs = wb;
-            stages = st;
-            break;
+    // The ring's stages hold kbs X blocks and their packed codes (and the staged scales);
+    // the bf16 tiles the converters write get their own buffers (kbs tiles each): four
+    // when the ring can still be four stages deep, else two.
+    auto plan = [&](int k, bool with_scales, int srow, int& wbufs_out, int& stages_out) {
+        const int64_t blk = k * (a_bytes + int64_t(nsub) * BN * q_kb_bytes) +
+                            (with_scales ? (aff ? 2 : 1) * int64_t(nsub) * BN * srow : 0);
+        const int64_t bb = int64_t(k) * nsub * B_KB_BYTES;
+        wbufs_out = stages_out = 0;
+        for (int wb = MAX_QWBUF; wb >= 2; wb -= 2) {
+            int st = int((RING_BYTES - wb * bb) / blk);
+            if (st > MAX_QSTAGES) st = MAX_QSTAGES;
+            st &= ~1;  // even: each of the two converter groups owns every other stage
+            if (st >= 4 || (wb == 2 && st >= 2)) {
+                wbufs_out = wb;
+                stages_out = st;
+                return;
+            }
+        }
+    };
+    int kbs = 1, wbufs = 0, stages = 0;
+    if (stageable && m_tiles == 1) {
+        const int64_t nkb = (K + BK - 1) / BK;
+        kbs = 256 / q_kb_bytes < 8 ? 256 / q_kb_bytes : 8;
+        while (kbs > 1 && nkb < 4 * kbs) kbs >>= 1;  // keep >= 4 stages per tile
+        for (; kbs > 1; kbs >>= 1) {                   // and a ring of >= 4 stages
+            plan(kbs, true, Q_SROW_KBS, wbufs, stages);
+            if (stages >= 4) break;
         }
     }
+    CUtensorMap ms, mb;
+    const int64_t groups = K / gs;
+    auto stage_scales = [&](int srow) {
+        return aff ? tmap_2d_u16(&ms, scales, uint64_t(groups), uint64_t(N), uint64_t(lds * 2),
+                                 uint32_t(srow / 2), uint32_t(nsub * BN)) &&
+                         tmap_2d_u16(&mb, biases, uint64_t(groups), uint64_t(N),
+                                     uint64_t(ldb * 2), uint32_t(srow / 2), uint32_t(nsub * BN))
+                   : tmap_2d_u8(&ms, scales, uint64_t(groups), uint64_t(N), uint64_t(lds),
+                                uint32_t(srow), uint32_t(nsub * BN));
+    };
+    bool staged = stageable && stage_scales(kbs > 1 ? Q_SROW_KBS : Q_SROW);
+    if (!staged && kbs > 1) {  // no window of several K-blocks: one K-block per stage
+        kbs = 1;
+        staged = stageable && stage_scales(Q_SROW);
+    }
+    const int s_row = kbs > 1 ? Q_SROW_KBS : Q_SROW;
+    plan(kbs, staged, s_row, wbufs, stages);
+    const int64_t b_bytes = int64_t(kbs) * nsub * B_KB_BYTES;
     // an MMA reads A_MMA_BYTES from the start of its X block: the last block's read runs
     // into the tile buffers that follow the X blocks and must stay inside the ring
-    if (wbufs == 0 || (stages - 1) * a_bytes + A_MMA_BYTES > stages * a_bytes + wbufs * b_bytes)
+    if (wbufs == 0 ||
+        (int64_t(stages) * kbs - 1) * a_bytes + A_MMA_BYTES > int64_t(stages) * kbs * a_bytes +
+                                                                 wbufs * b_bytes)
         return cudaErrorNotSupported;
     CUtensorMap mx, mw;
     if (!tmap_2d_bf16(&mx, x, uint64_t(K), uint64_t(M), uint64_t(ldx), BK, uint32_t(a_rows), 128) ||
         !tmap_2d_u8(&mw, wq, uint64_t(eight ? K : K / 2), uint64_t(N), uint64_t(ldq),
-                    uint32_t(q_kb_bytes), uint32_t(nsub * BN)))
+                    uint32_t(kbs * q_kb_bytes), uint32_t(nsub * BN)))
         return cudaErrorNotSupported;
     GemmArgs a{};
     a.y = y;
@@ -1180,7 +1217,7 @@ cudaError_t launch_qgemm(const DeviceInfo& dev, const void* x, int64_t ldx, cons
     a.K = int(K);
     a.a_rows = a_rows;
     a.nsub = nsub;
-    a.kbs = 1;
+    a.kbs = kbs;
     a.blocked = 0;
     a.stages = stages;
     a.w_stream_once = m_tiles == 1 ? 1 : 0;
@@ -1197,6 +1234,7 @@ cudaError_t launch_qgemm(const DeviceInfo& dev, const void* x, int64_t ldx, cons
     a.q_kb_bytes = q_kb_bytes;
     a.wbufs = wbufs;
     a.q_staged = staged ? 1 : 0;
+    a.q_srow = s_row;
     if (!staged) ms = mb = mw;  // unused
     else if (!aff) mb = ms;
     const int64_t tiles = m_tiles * ((N + int64_t(nsub) * BN - 1) / (int64_t(nsub) * BN));

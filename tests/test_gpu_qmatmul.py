@@ -155,9 +155,11 @@ def _affine_enumeration(fmt, gs, K, seed):
 
 
 def _padded(a, row_bytes=16):
-    """The same values in rows of row_bytes bytes (scales whose rows start on 16-byte
-    boundaries travel with the codes by TMA; others are loaded by the converters)."""
-    out = np.zeros((a.shape[0], max(row_bytes // a.itemsize, a.shape[1])), a.dtype)
+    """The same values in rows padded to a multiple of row_bytes bytes (scales whose rows
+    start on 16-byte boundaries travel with the codes by TMA; others are loaded by the
+    converters)."""
+    per = row_bytes // a.itemsize
+    out = np.zeros((a.shape[0], -(-a.shape[1] // per) * per), a.dtype)
     out[:, :a.shape[1]] = a
     return out
 
@@ -203,3 +205,33 @@ def test_qmatmul_dequantizes_every_code_exactly(dev, fmt, gs, K, pad):
     if not fmt.startswith("affine"):  # the enumeration reached every kind of value
         assert mask.sum() > 0 and np.isnan(wv).sum() > 0
         assert (lone_inf.sum() > 0) == (fmt != "nvfp4")  # 6 x 448 stays finite
+
+
+@pytest.mark.parametrize("fmt,gs", FORMATS)
+@pytest.mark.parametrize("M,N,K", [(1, 300, 1600), (5, 200, 4160), (8, 96, 512)])
+def test_qmatmul_small_m_multi_kblock_stages(dev, fmt, gs, M, N, K):
+    """Small M with TMA-staged scales (rows padded to a 16-byte pitch): the kernel takes
+    several K-blocks per stage, the last stage short (K = 1600: 25 K-blocks in stages of
+    4; K = 4160: 65 in stages of 8).  Oracle parity, and the bits of the dense GEMM on the
+    dequantized weights."""
+    if K % gs:
+        pytest.skip("K must be a multiple of the group size")
+    wq, sc, b, wd = _weights(fmt, N, K, gs, seed=M + N + K)
+    affine = b is not None
+    sc_np = inputs.bf16_bits(sc) if affine else sc.numpy()
+    sct = torch.from_numpy(_padded(sc_np).view(np.int16) if affine else _padded(sc_np))
+    sct = sct.to(dev)[:, :K // gs]
+    if affine:
+        sct = sct.view(torch.bfloat16)
+    bt = None
+    if affine:
+        bt = torch.from_numpy(_padded(inputs.bf16_bits(b)).view(np.int16)).to(dev)[:, :K // gs]
+        bt = bt.view(torch.bfloat16)
+    x = inputs.normal_bf16((M, K), seed=K + M)
+    y32 = bi.qmatmul(x.to(dev), wq.to(dev), sct, fmt, gs, K, biases=bt, out_dtype=torch.float32)
+    ref = oracle.matmul(inputs.bf16_bits(x), wd, oracle.W_NK)
+    wv = (wd.astype(np.uint32) << 16).view(np.float32).astype(np.float64)
+    scale = np.abs(x.float().numpy().astype(np.float64)) @ np.abs(wv).T
+    check_f32(y32, ref, scale, f"qmatmul staged {fmt} gs{gs} {M}x{N}x{K}")
+    wdt = torch.from_numpy(wd.view(np.int16)).view(torch.bfloat16).to(dev)
+    assert bits_equal(y32, bi.matmul(x.to(dev), wdt, "nk", out_dtype=torch.float32))
