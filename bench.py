@@ -625,7 +625,7 @@ def run_case(spec: str, reps: int):
 
 def run_sweep():
     """Extra JSON lines: GEMM over M (both layouts, vs cuBLAS), RMSNorm at hidden 8192,
-    attention over the pages' Lk and q.  Two timings per shape: one call with L2 evicted
+    attention over the pages' Lk and q, chunked prefill.  Two timings per shape: one call with L2 evicted
     before it (`*_us`, includes the launch), and `steady_*_us`, the per-call time of a
     back-to-back stream over rotating input sets larger than 2x L2 (for attention, one
     set when its K/V already exceed that; otherwise marked warm).  Each GEMM and attention
@@ -907,6 +907,32 @@ def run_sweep():
                           "graph_fast_frac_hbm": round(by / tfg / 1e3 / peaks["hbm_gbs"], 3),
                           "graph_invariance_tax": round(tg / tfg - 1.0, 3)}), flush=True)
         del p, d, ws
+        torch.cuda.empty_cache()
+
+    # chunked prefill (causal): the whole prompt, and 512 new tokens after a cached prefix.
+    # Tensor-bound: flops = 4 * D * Hq * sum over queries of (keys seen)
+    for L, qb in ((8192, 8192), (8192, 512), (65540, 512)):
+        bi.set_batch_invariant_limit(INVARIANT)
+        p = inputs.paged_inputs([L], [qb], Hq=HQ, Hkv=HKV, D=HEAD_DIM, seed=5, device=dev)
+        d = {k: getattr(p, k).to(dev) for k in ("q", "k_cache", "v_cache", "block_table",
+                                                 "seq_lens", "cu_q")}
+        ws = torch.empty(bi.attn_workspace_size(qb, HQ, HEAD_DIM, L), dtype=torch.uint8,
+                         device=dev)
+        out = torch.empty(qb, HQ, HEAD_DIM, dtype=torch.bfloat16, device=dev)
+        call = lambda: bi.prefill_attn(d["q"], d["k_cache"], d["v_cache"], d["block_table"],
+                                       d["seq_lens"], d["cu_q"], max_q=qb, max_seq_len=L,
+                                       scale=1 / math.sqrt(HEAD_DIM), out=out, want_lse=False,
+                                       workspace=ws)
+        t = t_us(call)
+        tg = graph_us([call], n=4, reps=5)
+        seen = float(sum(range(L - qb + 1, L + 1)))
+        flops = 4.0 * HEAD_DIM * HQ * seen
+        print(json.dumps({"sweep": "prefill", "Lk": L, "new_tokens": qb, "us": round(t, 2),
+                          "graph_us": round(tg, 2),
+                          "TFLOP/s": round(flops / tg / 1e6, 1),
+                          "graph_frac_tensor": round(flops / tg / 1e6 / peaks["bf16_tflops"], 3),
+                          "tokens/s": round(qb / tg * 1e6)}), flush=True)
+        del p, d, ws, out
         torch.cuda.empty_cache()
 
 
