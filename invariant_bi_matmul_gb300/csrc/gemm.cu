@@ -436,7 +436,11 @@ gemm_kernel(const __grid_constant__ CUtensorMap tmap_x, const __grid_constant__ 
         // per k16 step.  K-major W: the tile's rows are contiguous (8-row groups 1024 B
         // apart); N-major W: its swizzle-atom columns sit the descriptor's leading-byte
         // offset apart.
-        const uint32_t idesc = umma_idesc_bf16(BM, NSUB * BN, 0, KN ? 1 : 0, args.f16 != 0);
+        // A tile of at most 64 rows (M <= 64) runs M = 64 instructions: half the X bytes
+        // read per instruction, the same per-element products and K order
+        const bool m64 = MSUB == 1 && args.a_rows <= 64;
+        const uint32_t idesc =
+            umma_idesc_bf16(m64 ? 64 : BM, NSUB * BN, 0, KN ? 1 : 0, args.f16 != 0);
         // X: K-major, 128-byte swizzle, 8-row groups 1024 B apart; +32 B per k16 step
         const uint64_t a_desc0 = umma_smem_desc(smem_addr(sA), 16, 1024, 2);
         // W, layout NK: K-major like X.  Layout KN: N-major; k-rows of KN_SWIZZLE bytes,
@@ -521,7 +525,12 @@ gemm_kernel(const __grid_constant__ CUtensorMap tmap_x, const __grid_constant__ 
         // ------------------------------------------------------------------ epilogue
         pdl_wait();  // Y may still be read by the previous grid
         const int quad = warp & 3;  // TMEM lanes 32*quad .. 32*quad+31
-        const int row_in_tile = quad * 32 + lane;
+        // M = 128 instructions: tile row i in lane i.  M = 64 instructions (tiles of at most
+        // 64 rows): rows 16q .. 16q+15 in lanes 32q .. 32q+15; the other lanes hold no row
+        // (given a row index past the tile, so nothing reads or writes for them)
+        const bool m64 = MSUB == 1 && args.a_rows <= 64;
+        const int row_in_tile =
+            !m64 ? quad * 32 + lane : (lane < 16 ? quad * 16 + lane : BM + lane);
         int local = 0;
         void* const y = args.y;
         const int64_t ldy = args.ldy;
@@ -535,7 +544,7 @@ gemm_kernel(const __grid_constant__ CUtensorMap tmap_x, const __grid_constant__ 
         // order, i.e. in ascending K.  Only warps whose lanes hold staged rows (live) touch
         // tensor memory or the slots; every epilogue thread joins every barrier.
         const int red_rows = args.a_rows;
-        const bool live = !SPLIT || quad * 32 < red_rows;
+        const bool live = !SPLIT || quad * (m64 ? 16 : 32) < red_rows;
         const bool red_row = row_in_tile < red_rows;
         const uint32_t slot_bytes = uint32_t(red_rows * tile_n * 4);
         const uint32_t red_base =
