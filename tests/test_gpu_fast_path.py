@@ -38,6 +38,7 @@ FAST_SHAPES = [
     (1, 2048, 4096, "nk"),      # 2 CTAs per tile
     (8, 1024, 4096, "kn"),      # 4 CTAs per tile
     (5, 1000, 4160, "nk"),      # ragged N, K tail (one copy per K-block)
+    (50, 1024, 4096, "kn"),     # 56 staged rows: M = 64 instructions, four lane quarters
     (100, 1024, 4096, "nk"),    # 104 staged rows: the slots limit the split
     (128, 512, 1000, "kn"),     # a full M-tile, ragged K
     (3, 64, 4096, "nk"),        # a single column tile

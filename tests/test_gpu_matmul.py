@@ -36,6 +36,7 @@ SHAPES = [
     (3, 200, 200),                                     # ragged N and K tails
     (130, 96, 320),                                    # two M tiles, ragged M
     (257, 64, 64), (5, 33, 8), (2, 1000, 1032),
+    (61, 304, 520),                                    # M = 64 instructions, every lane quarter
 ]
 
 
@@ -84,8 +85,11 @@ def test_matmul_rows_invariant_across_M(dev, layout):
     x = gi.x.to(dev)
     full = bi.matmul(x, w, layout)
     # every M crosses a different staging / CTA-tiling choice of the scheduler:
-    # staged X rows 8..128, one to eight 32-wide instruction tiles per CTA
-    for M in (1, 2, 3, 4, 8, 9, 16, 17, 64, 100, 127, 128, 129, 256, 600, 1000, 1500):
+    # staged X rows 8..128, one to eight 32-wide instruction tiles per CTA, M = 64
+    # instructions up to 64 rows (rows in all four lane quarters from M = 49) and M = 128
+    # ones from 65
+    for M in (1, 2, 3, 4, 8, 9, 16, 17, 33, 49, 64, 65, 100, 127, 128, 129, 256, 600, 1000,
+              1500):
         part = bi.matmul(x[:M].contiguous(), w, layout)
         assert bits_equal(part, full[:M]), f"rows differ at M={M}"
     # a row evaluated alone from the middle of the batch (not only the first rows)
