@@ -321,7 +321,10 @@ def run_gpu(args, rank, world, local_rank):
 def run_e2e(st: Step, args, dist):
     """Same step through the public Python API with host buffers: pinned H2D of the
     step's inputs (hidden states, new K/V), the five calls, D2H of the result, every
-    step; timed on the host clock around the synchronised loop."""
+    step; timed on the host clock around the synchronised loop.  Two ways of issuing it:
+    `graph` captures the copies and the five calls once in a CUDA graph and replays it
+    every step (how a serving loop issues a fixed-shape decode step); `eager` issues every
+    copy and call from Python each step."""
     import torch
     import invariant_bi_matmul_gb300 as bi
     dev = st.dev
@@ -333,7 +336,7 @@ def run_e2e(st: Step, args, dist):
     kn = torch.empty_like(st.k_new)
     vn = torch.empty_like(st.v_new)
 
-    def step():
+    def body():
         x.copy_(hx, non_blocking=True)
         kn.copy_(hk, non_blocking=True)
         vn.copy_(hv, non_blocking=True)
@@ -345,20 +348,47 @@ def run_e2e(st: Step, args, dist):
                         workspace=st.ws)
         bi.matmul(st.o.view(M_TOK, HIDDEN), st.w_o, "kn", out=st.y)
         hy.copy_(st.y, non_blocking=True)
+
+    def eager_step():
+        body()
+        torch.cuda.current_stream(dev).synchronize()
+
+    side = torch.cuda.Stream(dev)
+    side.wait_stream(torch.cuda.current_stream(dev))
+    with torch.cuda.stream(side):
+        for _ in range(3):
+            body()
+    torch.cuda.current_stream(dev).wait_stream(side)
+    torch.cuda.synchronize(dev)
+    graph = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(graph):
+        body()
+
+    def graph_step():
+        graph.replay()
         torch.cuda.current_stream(dev).synchronize()
 
     n = max(10, min(args.steps, 2000))
-    for _ in range(3):
-        step()
-    if dist:
-        torch.distributed.barrier()
-    t0 = time.perf_counter()
-    for _ in range(n):
-        step()
-    dt = max_over_ranks((time.perf_counter() - t0) / n, dev)
+    out = {}
+    for name, step in (("graph", graph_step), ("eager", eager_step)):
+        for _ in range(3):
+            step()
+        if dist:
+            torch.distributed.barrier()
+        t0 = time.perf_counter()
+        for _ in range(n):
+            step()
+        out[name] = max_over_ranks((time.perf_counter() - t0) / n, dev)
+    # the graph's result equals the eager step's (same inputs, same kernels)
+    y_eager = hy.clone()
+    graph_step()
+    if not torch.equal(hy.view(torch.int16), y_eager.view(torch.int16)):
+        raise SystemExit("graph replay and eager step disagree")
+    del graph
     h2d = hx.numel() * 2 + hk.numel() * 2 + hv.numel() * 2
     d2h = hy.numel() * 2
-    return {"sec_per_step": dt, "h2d": h2d, "d2h": d2h, "steps": n}
+    return {"sec_per_step": out["graph"], "sec_per_step_eager": out["eager"], "h2d": h2d,
+            "d2h": d2h, "steps": n}
 
 
 def gemm_vs_cublas(st: Step):
@@ -555,7 +585,13 @@ def main():
         "cpu_baseline": cpu,
         "e2e": {"value": round(job_throughput(total, world, e2e["sec_per_step"]), 1), "unit": "GB/s",
                 "h2d_bytes_per_step": e2e["h2d"], "d2h_bytes_per_step": e2e["d2h"],
-                "ms_per_step": round(e2e["sec_per_step"] * 1e3, 4)},
+                "ms_per_step": round(e2e["sec_per_step"] * 1e3, 4),
+                "issue": "the step's copies and calls captured once in a CUDA graph, "
+                         "replayed and synchronised every step",
+                "eager": {"value": round(job_throughput(total, world,
+                                                        e2e["sec_per_step_eager"]), 1),
+                          "ms_per_step": round(e2e["sec_per_step_eager"] * 1e3, 4),
+                          "issue": "every copy and call issued from Python each step"}},
         "gpu_launches": Step.LAUNCHES_PER_STEP * args.steps,
         "clocks": res["clocks"],
         "parts": parts,
