@@ -511,7 +511,7 @@ def main():
     ap.add_argument("--sweep", action="store_true")
     ap.add_argument("--case", default=None,
                     help="time one call shape instead of the step (for profiling): "
-                         "gemm:M:N:K[:kn][:fast] or attn:B:q:Lk[:fast]")
+                         "gemm:M:N:K[:kn][:fast], attn:B:q:Lk[:fast] or prefill:Lk:new")
     ap.add_argument("--case-reps", type=int, default=5)
     args = ap.parse_args()
     if args.warmup < 3:
@@ -639,6 +639,19 @@ def run_case(spec: str, reps: int):
                                      scale=1 / math.sqrt(HEAD_DIM), out=out, lse=lse,
                                      workspace=ws)
         desc = {"case": "attn", "B": B, "q": q, "Lk": L}
+    elif parts[0] == "prefill":
+        L, qb = (int(v) for v in parts[1:3])  # prompt length, new tokens (the last qb)
+        p = inputs.paged_inputs([L], [qb], Hq=HQ, Hkv=HKV, D=HEAD_DIM, seed=5, device=dev)
+        d = {k: getattr(p, k).to(dev) for k in ("q", "k_cache", "v_cache", "block_table",
+                                                 "seq_lens", "cu_q")}
+        ws = torch.empty(bi.attn_workspace_size(qb, HQ, HEAD_DIM, L), dtype=torch.uint8,
+                         device=dev)
+        out = torch.empty(qb, HQ, HEAD_DIM, dtype=torch.bfloat16, device=dev)
+        fn = lambda: bi.prefill_attn(d["q"], d["k_cache"], d["v_cache"], d["block_table"],  # noqa: E731
+                                     d["seq_lens"], d["cu_q"], max_q=qb, max_seq_len=L,
+                                     scale=1 / math.sqrt(HEAD_DIM), out=out, want_lse=False,
+                                     workspace=ws)
+        desc = {"case": "prefill", "Lk": L, "new_tokens": qb}
     else:
         raise SystemExit(f"unknown case {spec!r}")
     for _ in range(3):

@@ -776,8 +776,10 @@ attn_merge_kernel(const int32_t* __restrict__ seq_lens, const int32_t* __restric
 }
 
 // One warp per row, eight rows per CTA: the same tree, its eight ranges folded one after
-// another (throughput: many rows, e.g. a prefill block).
-template <int D>
+// another (throughput: many rows, e.g. a prefill block).  UNR (>= the rows' chunk count)
+// sizes the register window that holds a row's partials: the smaller it is, the more CTAs
+// share an SM and the more rows' loads are in flight (it changes no arithmetic).
+template <int D, int UNR>
 __global__ void __launch_bounds__(MERGE_WARPS * 32)
 attn_merge_rows_kernel(const int32_t* __restrict__ seq_lens, const int32_t* __restrict__ cu_q,
                        int B, int total_q, int max_q, int max_seq_len, int Hq,
@@ -796,54 +798,49 @@ attn_merge_rows_kernel(const int32_t* __restrict__ seq_lens, const int32_t* __re
     if (!merge_row(seq_lens, cu_q, B, total_q, max_q, max_seq_len, t, pos)) return;
     const int nC = (pos >> chunk_log2) + 1;
     const int64_t base = (int64_t(t) * Hq + hq) * maxC;
+    // the host picks UNR >= maxC >= nC for every valid row
+    if (nC > UNR) return;
     float M8[MERGE_WARPS], L8[MERGE_WARPS], acc8[MERGE_WARPS][PER];
-    if (nC <= MERGE_UNROLL) {
-        // every partial of the row in one round trip, then each range folded from the
-        // registers with merge_fold's arithmetic (max first, then the weighted sums in
-        // ascending chunk order)
-        float v[MERGE_UNROLL][PER];
-        float2 ml[MERGE_UNROLL];
+    // every partial of the row in one round trip, then each range folded from the
+    // registers with merge_fold's arithmetic (max first, then the weighted sums in
+    // ascending chunk order)
+    float v[UNR][PER];
+    float2 ml[UNR];
 #pragma unroll
-        for (int c = 0; c < MERGE_UNROLL; ++c) {
-            if (c < nC) {
-                ml[c] = *reinterpret_cast<const float2*>(ws_ml + (base + c) * 2);
-                const float* src = ws_o + (base + c) * D + lane * PER;
-                if (PER == 4) {
-                    const float4 f = *reinterpret_cast<const float4*>(src);
-                    v[c][0] = f.x; v[c][1 % PER] = f.y; v[c][2 % PER] = f.z; v[c][3 % PER] = f.w;
-                } else {
-                    const float2 f = *reinterpret_cast<const float2*>(src);
-                    v[c][0] = f.x; v[c][1 % PER] = f.y;
-                }
+    for (int c = 0; c < UNR; ++c) {
+        if (c < nC) {
+            ml[c] = *reinterpret_cast<const float2*>(ws_ml + (base + c) * 2);
+            const float* src = ws_o + (base + c) * D + lane * PER;
+            if (PER == 4) {
+                const float4 f = *reinterpret_cast<const float4*>(src);
+                v[c][0] = f.x; v[c][1 % PER] = f.y; v[c][2 % PER] = f.z; v[c][3 % PER] = f.w;
+            } else {
+                const float2 f = *reinterpret_cast<const float2*>(src);
+                v[c][0] = f.x; v[c][1 % PER] = f.y;
             }
         }
+    }
 #pragma unroll
-        for (int w = 0; w < MERGE_WARPS; ++w) {
-            const int c0 = w * nC / MERGE_WARPS, c1 = (w + 1) * nC / MERGE_WARPS;
-            float Mw = -INFINITY;
+    for (int w = 0; w < MERGE_WARPS; ++w) {
+        const int c0 = w * nC / MERGE_WARPS, c1 = (w + 1) * nC / MERGE_WARPS;
+        float Mw = -INFINITY;
 #pragma unroll
-            for (int c = 0; c < MERGE_UNROLL; ++c)
-                if (c >= c0 && c < c1) Mw = fmaxf(Mw, ml[c].x);
-            float Lw = 0.f;
+        for (int c = 0; c < UNR; ++c)
+            if (c >= c0 && c < c1) Mw = fmaxf(Mw, ml[c].x);
+        float Lw = 0.f;
 #pragma unroll
-            for (int i = 0; i < PER; ++i) acc8[w][i] = 0.f;
+        for (int i = 0; i < PER; ++i) acc8[w][i] = 0.f;
 #pragma unroll
-            for (int c = 0; c < MERGE_UNROLL; ++c) {
-                if (c >= c0 && c < c1) {
-                    const float wgt = exp2f(ml[c].x - Mw);
-                    Lw = Lw + wgt * ml[c].y;
+        for (int c = 0; c < UNR; ++c) {
+            if (c >= c0 && c < c1) {
+                const float wgt = exp2f(ml[c].x - Mw);
+                Lw = Lw + wgt * ml[c].y;
 #pragma unroll
-                    for (int i = 0; i < PER; ++i) acc8[w][i] = acc8[w][i] + wgt * v[c][i];
-                }
+                for (int i = 0; i < PER; ++i) acc8[w][i] = acc8[w][i] + wgt * v[c][i];
             }
-            M8[w] = Mw;
-            L8[w] = Lw;
         }
-    } else {
-#pragma unroll
-        for (int w = 0; w < MERGE_WARPS; ++w)
-            merge_fold<D>(ws_o, ws_ml, base, w * nC / MERGE_WARPS, (w + 1) * nC / MERGE_WARPS,
-                          lane, M8[w], L8[w], acc8[w]);
+        M8[w] = Mw;
+        L8[w] = Lw;
     }
     merge_combine<D>(M8, L8, [&](int w, int i) { return acc8[w][i]; }, lane,
                      out + (int64_t(t) * Hq + hq) * D, lse ? lse + int64_t(t) * Hq + hq : nullptr);
@@ -946,7 +943,13 @@ cudaError_t launch_attn_merge(const PagedArgs& a, void* workspace, int chunk_log
                           int(a.max_seq_len), int(a.hq), ws_o, ws_ml, maxC, chunk_log2,
                           static_cast<__nv_bfloat16*>(out), lse);
     }
-    auto kern = a.head_dim == 64 ? attn_merge_rows_kernel<64> : attn_merge_rows_kernel<128>;
+    auto kern = a.head_dim == 64
+                    ? (maxC <= 4 ? attn_merge_rows_kernel<64, 4>
+                                 : maxC <= 8 ? attn_merge_rows_kernel<64, 8>
+                                             : attn_merge_rows_kernel<64, MERGE_UNROLL>)
+                    : (maxC <= 4 ? attn_merge_rows_kernel<128, 4>
+                                 : maxC <= 8 ? attn_merge_rows_kernel<128, 8>
+                                             : attn_merge_rows_kernel<128, MERGE_UNROLL>);
     return launch_pdl(kern, dim3(unsigned((rows + MERGE_WARPS - 1) / MERGE_WARPS)),
                       dim3(MERGE_WARPS * 32), 0, stream, a.seq_lens, a.cu_q, int(a.batch),
                       int(a.total_q), int(a.max_q), int(a.max_seq_len), int(a.hq), ws_o, ws_ml,
