@@ -127,7 +127,7 @@ __device__ __forceinline__ bool mbar_wait(uint64_t* bar, uint32_t parity,
     }
 }
 
-// The same wait by every lane of a warp, with one warp-wide verdict (so a timeout never
+// The same wait by every lane of a warp, with one warp-wide result (so a timeout never
 // splits a warp that then meets elect.sync or a collective).
 template <bool CLUSTER = false>
 __device__ __forceinline__ bool mbar_wait_warp(uint64_t* bar, uint32_t parity,
