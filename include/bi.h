@@ -153,12 +153,13 @@ int64_t bi_attn_chunk(int64_t batch, int64_t total_q, int64_t max_q, int64_t max
  *                 layout BI_W_KN: [K, N] with row stride ldw (ldw >= N).
  *   y       [M, N] row-major, row stride ldy (ldy >= N), dtype y_dtype.
  *   M, N, K >= 0; M = 0 or N = 0 is a no-op; K = 0 writes zeros.
- *   Invariant construction (M inside the batch-invariant limit): one tcgen05
- *   instruction shape (128 x 64 x 16, kind::f16, fp32 accumulation in tensor memory)
- *   and one K order (64-wide K-blocks ascending, four 16-wide steps ascending inside
- *   each) for every M.  Row m is always lane m%128 of M-tile m/128; rows beyond M are
- *   never stored.  Only scheduling follows M (how many X rows are staged, how many
- *   instruction tiles one CTA covers).  Outside the limit the K loop may be split
+ *   Invariant construction (M inside the batch-invariant limit): one K order for every
+ *   M (64-wide K-blocks ascending, four 16-wide kind::f16 steps ascending inside each,
+ *   fp32 accumulation in tensor memory, no split of K).  The instruction's height (64
+ *   rows for tiles of at most 64 rows, else 128), its width (32 to 256 columns) and the
+ *   CTA tile follow M; an element's 16-product step does not depend on them, which the
+ *   library's tests check on fp32 output bits at every shape it picks.  Rows beyond M
+ *   are never stored.  Outside the limit the K loop may be split
  *   (see the limit section): each part runs the same ascending K order over its range
  *   and the fp32 partials are added in ascending K order before rounding.
  *   Alignment (TMA rule): x, w 16-byte aligned; ldx, ldw multiples of 8 elements;
@@ -349,14 +350,23 @@ bi_status bi_prefill_attn(const void* q, const void* k_cache, const void* v_cach
  * For callers that cannot call cudaMalloc where they run attention (code recorded into
  * or replayed from someone else's CUDA graph, allocator-free runtimes that only hand
  * over the tensors they own, real-time paths where an allocation and its implicit
- * synchronisation are not allowed).  Same arguments and results as bi_verify_block
- * minus workspace / workspace_bytes: the workspace is a fixed device array of
- * BI_STATIC_WS_BYTES inside the library, present on every GPU that loads it until the
+ * synchronisation are not allowed).  Same arguments as bi_verify_block minus
+ * workspace / workspace_bytes, and the same results as bi_verify_block given a workspace
+ * of exactly bi_attn_workspace_size(total_q, num_q_heads, head_dim, max_seq_len) bytes
+ * (outside the batch-invariant limit the chunk length depends on the workspace size, so
+ * that size is what this entry point passes on).  The workspace is a fixed device array
+ * of BI_STATIC_WS_BYTES inside the library, present on every GPU that loads it until the
  * process exits.  Nothing is allocated.
  *   - A block whose bi_attn_workspace_size(...) exceeds BI_STATIC_WS_BYTES is refused
- *     with BI_ERR_UNSUPPORTED (message names both sizes); use bi_verify_block then.
+ *     with BI_ERR_UNSUPPORTED (message names both sizes); use bi_verify_block then.  This
+ *     size check comes first, so a call whose sizes are both invalid and too large is
+ *     reported as BI_ERR_UNSUPPORTED; the other arguments are checked as in
+ *     bi_verify_block.
  *   - The first call on a device looks the array's device address up
- *     (cudaGetSymbolAddress); make that first call before any stream capture.
+ *     (cudaGetSymbolAddress) and keeps it for the life of the process; make that first
+ *     call before any stream capture.  After cudaDeviceReset (or anything else that
+ *     destroys the device's primary context) the kept address is stale: a process that
+ *     resets a device must not call this entry point again.
  *   - Every call shares the one array and it keeps the last call's contents (nothing in
  *     it needs to start at zero).  Calls whose kernels overlap on the GPU -- different
  *     streams, different host threads -- race on it: serialise them.

@@ -1,7 +1,7 @@
 // common.cuh -- device-side building blocks shared by the libbi kernels (sm_103a only):
 // inline-PTX wrappers for mbarriers, TMA bulk-tensor copies, tcgen05 (tensor memory,
-// UMMA descriptors, MMA issue, TMEM loads) and the legacy mma.sync / ldmatrix path,
-// plus the bounded-wait discipline every kernel follows.
+// UMMA descriptors, MMA issue, TMEM loads), 16-bit packing helpers, and the
+// bounded-wait discipline every kernel follows.
 #pragma once
 
 #include <cuda.h>
@@ -473,31 +473,7 @@ __host__ __device__ constexpr uint32_t umma_idesc_bf16(int m, int n, int a_mn_ma
            | (static_cast<uint32_t>(m >> 4) << 24);         // M / 16
 }
 
-// -------------------------------------------------- legacy warp MMA (attention path)
-
-__device__ __forceinline__ void ldmatrix_x4(uint32_t saddr, uint32_t& r0, uint32_t& r1,
-                                            uint32_t& r2, uint32_t& r3) {
-    asm volatile("ldmatrix.sync.aligned.m8n8.x4.shared.b16 {%0, %1, %2, %3}, [%4];"
-                 : "=r"(r0), "=r"(r1), "=r"(r2), "=r"(r3)
-                 : "r"(saddr));
-}
-
-__device__ __forceinline__ void ldmatrix_x4_trans(uint32_t saddr, uint32_t& r0, uint32_t& r1,
-                                                  uint32_t& r2, uint32_t& r3) {
-    asm volatile("ldmatrix.sync.aligned.m8n8.x4.trans.shared.b16 {%0, %1, %2, %3}, [%4];"
-                 : "=r"(r0), "=r"(r1), "=r"(r2), "=r"(r3)
-                 : "r"(saddr));
-}
-
-// D(16x8 fp32) += A(16x16 bf16, row) * B(16x8 bf16, col)
-__device__ __forceinline__ void mma_bf16_16816(float (&d)[4], const uint32_t (&a)[4],
-                                               uint32_t b0, uint32_t b1) {
-    asm volatile(
-        "mma.sync.aligned.m16n8k16.row.col.f32.bf16.bf16.f32 "
-        "{%0, %1, %2, %3}, {%4, %5, %6, %7}, {%8, %9}, {%0, %1, %2, %3};"
-        : "+f"(d[0]), "+f"(d[1]), "+f"(d[2]), "+f"(d[3])
-        : "r"(a[0]), "r"(a[1]), "r"(a[2]), "r"(a[3]), "r"(b0), "r"(b1));
-}
+// ------------------------------------------------------------- 16-bit packing
 
 __device__ __forceinline__ uint32_t pack_bf16x2(float lo, float hi) {
     __nv_bfloat162 v = __floats2bfloat162_rn(lo, hi);  // .x = lo (low 16 bits)

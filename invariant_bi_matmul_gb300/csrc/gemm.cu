@@ -9,24 +9,30 @@
 // reduction) and the review thread (both B orientations must be covered).
 //
 // What decides the bits of Y[m, n] -- identical for every M:
-//   * the instruction tcgen05.mma.cta_group::1.kind::f16 of shape 128 x 64 x 16 (bf16 in,
-//     fp32 accumulator in tensor memory), always with token row m at lane m % 128 of
-//     M-tile m / 128 and column n in the 64-wide instruction tile n / 64;
+//   * the kind::f16 instruction (tcgen05.mma.cta_group::1, bf16 or binary16 in, fp32
+//     accumulator in tensor memory) and its 16-wide K step: each element adds the 16
+//     products of one K slice to its own fp32 accumulator;
 //   * the K order: 64-wide K-blocks in ascending order, and inside a block the four
 //     16-wide steps in ascending order, the first one overwriting the accumulator;
-//   * the epilogue: fp32 -> bf16 round-to-nearest-even (or fp32 as is).
-// What follows M (scheduling only; never an element's instruction sequence):
-//   * a_rows: how many X rows are staged per K-block (M rounded up to 8, at most 128).
-//     The MMA always reads 128 rows; rows past a_rows read whatever lies in shared
-//     memory after the staged rows and land in tensor-memory lanes that are never
-//     stored, so no real row depends on them;
-//   * nsub: how many adjacent instruction tiles one CTA covers with the X block it staged
-//     (1 for small M to spread W over every SM, up to 4 for large M to stop re-reading X
-//     from L2);
+//   * the epilogue: fp32 -> bf16 (or binary16) round-to-nearest-even, or fp32 as is.
+// What follows M (scheduling, and the instruction's shape):
+//   * the instruction's height: 64 rows when a tile stages at most 64 rows (row 16q+r in
+//     tensor-memory lane 32q+r), else 128 (row m in lane m % 128);
+//   * the instruction's width, 32 to 256 columns: one instruction covers the CTA tile's
+//     nsub 32-column sub-tiles;
+//   * the CTA tile, from a cost model (gemm_schedule): 128 x 32*nsub, or 256 x 256 (two
+//     instructions along M) for large M, so different M run different template instances;
+//   * a_rows: how many X rows are staged per K-block (M rounded up to 8, at most 128, or
+//     256); rows past a_rows land in lanes that are never stored;
 //   * kbs and stages: how many K-blocks one ring stage carries and how deep the ring is.
-// (A 128 x N x 16 instruction costs about the same ~60 cycles for N up to 128, so N
-// trades small-M parallelism (N/64 CTAs at M <= 128) against large-M tensor throughput;
-// 64 is the fixed compromise.)
+// The book chapter's Case 6 names a smaller instruction at small M as one way to break
+// invariance, because an instruction may group or round its products differently.  Here
+// the shape changes, so the invariance rests on each element's 16-product step not
+// depending on the instruction's height or width.  That is a property of the hardware,
+// not of this code; the tests pin it on fp32 accumulator bits with operands built to
+// expose any regrouping (cancelling pairs of large products, subnormal inputs and
+// products) at every height and width the schedule picks, both layouts, bf16, binary16
+// and quantized W.
 //
 // Warp roles (192 threads, persistent, one CTA per SM): warp 0 = TMA producer, warp 1 =
 // TMEM allocator + MMA issuer, warps 2..5 = epilogue (tcgen05.ld -> convert -> global).
@@ -54,8 +60,8 @@ namespace {
 #define BI_GEMM_BN 32
 #endif
 
-constexpr int BM = 128;                     // instruction M: token rows
-constexpr int BN = BI_GEMM_BN;              // instruction N: output columns
+constexpr int BM = 128;                     // rows of an M-tile (64-row instructions below 65)
+constexpr int BN = BI_GEMM_BN;              // columns of a sub-tile (an instruction spans nsub)
 constexpr int BK = 64;                      // K-block: one 128-byte swizzle row of bf16
 constexpr int UK = 16;                      // K of one kind::f16 instruction
 constexpr int MAX_NSUB = 256 / BN;          // two accumulators of nsub*BN columns in 512

@@ -83,8 +83,11 @@ extern "C" __attribute__((visibility("default"))) bi_status bi_verify_block_stat
         bi::set_last_error_message(msg);
         return BI_ERR_CUDA;
     }
+    // The workspace size passed on is the block's own need, not the scratch's size: outside
+    // the batch-invariant limit the chunk length is chosen among those whose partials fit
+    // the workspace, so this gives the choice (and the bits) of bi_verify_block called with
+    // exactly bi_attn_workspace_size() bytes.
     return bi_verify_block(q, k_cache, v_cache, num_pages, block_table, max_pages, seq_lens, cu_q,
                            batch, total_q, max_q, max_seq_len, num_q_heads, num_kv_heads,
-                           head_dim, page_size, scale, out, lse, ws, size_t(BI_STATIC_WS_BYTES),
-                           stream);
+                           head_dim, page_size, scale, out, lse, ws, need, stream);
 }

@@ -45,6 +45,53 @@ def bf16_bits(t: torch.Tensor):
     return t.detach().cpu().contiguous().view(torch.int16).numpy().view("uint16")
 
 
+# ------------------------------------------------- order-sensitive GEMM operands
+
+# Per dtype: mantissa bits, exponent range of the ordinary values, exponent of the large
+# cancelling values, and the subnormal step of the format.
+_ADV = {torch.bfloat16: (7, -10, 10, 10, -133), torch.float16: (10, -8, 7, 7, -24)}
+
+
+def adversarial_operand(rows: int, K: int, seed: int, role: str,
+                        dtype=torch.bfloat16) -> torch.Tensor:
+    """A [rows, K] operand whose dot products expose how a multiply-accumulate unit groups
+    and rounds the terms of a 16-wide K slice.  In every slice of 16:
+      * positions 0,1 and 8,9 hold a cancelling pair: X repeats one large value at k and
+        k+1 (role "x"), W holds a large value and its negation (role "w"), so the two
+        products (about 2^20 for bf16, 2^14 for f16) cancel exactly for every row and
+        column, and whatever small terms were added next to them survive or not by the
+        order and width of the additions;
+      * position 5 (role "x") or 6 (role "w") holds a subnormal value of the format (one
+        step of 2^-133 for bf16, 2^-24 for f16, times 1..127), which meets an ordinary
+        value of the other operand;
+      * position 12 holds, for bf16, a value near 2^-64 (X) or 2^-70 (W), so that product
+        falls in fp32's subnormal range;
+      * the rest are +-(1 + m/2^p) * 2^e with e uniform in a wide range (bf16 -10..10,
+        f16 -8..7), so products span about 2^-20 .. 2^20.
+    Values are drawn as integers and assembled exactly; nothing is rounded."""
+    if role not in ("x", "w"):
+        raise ValueError("role is 'x' or 'w'")
+    pbits, emin, emax, big, sub = _ADV[dtype]
+    g = generator(seed)
+    sign = torch.randint(0, 2, (rows, K), generator=g).to(torch.float64) * 2 - 1
+    mant = 1 + torch.randint(0, 1 << pbits, (rows, K), generator=g).to(torch.float64) / (1 << pbits)
+    expo = torch.randint(emin, emax + 1, (rows, K), generator=g).to(torch.float64)
+    v = sign * mant * torch.pow(2.0, expo)
+    k = torch.arange(K) % 16
+    for a in (0, 8):
+        first, second = (k == a), (k == a + 1)
+        big_vals = sign[:, first] * mant[:, first] * 2.0 ** big
+        v[:, first] = big_vals
+        v[:, second[:K]] = big_vals[:, :int(second.sum())] * (1.0 if role == "x" else -1.0)
+    steps = torch.randint(1, 128, (rows, K), generator=g).to(torch.float64)
+    ks = 5 if role == "x" else 6
+    v[:, k == ks] = (sign * steps * 2.0 ** sub)[:, k == ks]
+    if dtype == torch.bfloat16:
+        tiny = -64 if role == "x" else -70
+        v[:, k == 12] = (sign * mant * 2.0 ** tiny)[:, k == 12]
+    return v.to(dtype)
+
+
 # ----------------------------------------------------------------------------- GEMM
 
 @dataclass

@@ -12,7 +12,7 @@ import torch
 
 import oracle
 from invariant_bi_matmul_gb300 import inputs
-from tolerance import bits_equal, check_bf16, check_f32
+from tolerance import bits_equal, check_bf16, check_f32, check_rows_rel_l2
 
 pytestmark = pytest.mark.gpu
 
@@ -148,6 +148,7 @@ def test_chosen_chunk_parity(dev, sms, case):
     ref, ref_lse = oracle.attention(b(p.q), kc, vc, p.block_table.numpy(), p.seq_lens.numpy(),
                                     p.cu_q.numpy(), 32, 1.0 / np.sqrt(128))
     check_bf16(out, ref, f"chunk {c} case {case}")
+    check_rows_rel_l2(out, ref, what=f"chunk {c} case {case}")
     assert np.allclose(lse.cpu().numpy(), ref_lse, rtol=1e-5, atol=1e-4)
     # same bits on a repeat
     out2, lse2 = bi.verify_block(d.q, d.k_cache, d.v_cache, d.block_table, d.seq_lens, d.cu_q,
@@ -175,6 +176,7 @@ def test_long_chunks_sampled_parity_and_decode(dev, sms):
                                             p.seq_lens.cpu().numpy(), p.cu_q.cpu().numpy(),
                                             bb, 0, h, 32, 1.0 / np.sqrt(128))
         check_bf16(out[bb, h], ref, f"2048-key chunks b={bb} h={h}")
+        check_rows_rel_l2(out[bb, h], ref, what=f"2048-key chunks b={bb} h={h}")
         assert abs(float(lse[bb, h]) - ref_lse) < 1e-4
 
 

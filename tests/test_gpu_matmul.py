@@ -211,17 +211,25 @@ def test_matmul_edges_and_guard_bands(dev):
     assert bi.device_status() == bi.BI_OK
 
 
-def test_limit_gate_does_not_change_bits(dev):
-    """Limit 0 (disabled) and limit >= M must give the same bits: this build has only
-    the invariant configuration."""
+def test_limit_gate_selects_the_configuration(dev):
+    """Inside the limit (M <= limit) the invariant single K loop runs, and a row's bits
+    equal the row alone; with the limit at 0 this shape (one M-tile, eight 32-column
+    tiles) takes a split-K cluster instead ("Fix/speculative shape invariance", Changes:
+    dimensions above the limit keep the optimized paths).  Both meet the oracle bar."""
     gi = inputs.gemm_inputs(8, 256, 256, seed=71)
     x, w = gi.x.to(dev), gi.w_nk.to(dev)
+    ref = oracle.matmul(inputs.bf16_bits(gi.x), inputs.bf16_bits(gi.w_nk), oracle.W_NK)
     old = bi.get_batch_invariant_limit()
     try:
         bi.set_batch_invariant_limit(0)
-        a = bi.matmul(x, w, "nk")
+        assert bi.matmul_splits(8, 256, 256) > 1
+        a = bi.matmul(x, w, "nk", out_dtype=torch.float32)
         bi.set_batch_invariant_limit(8)
-        b = bi.matmul(x, w, "nk")
+        assert bi.matmul_splits(8, 256, 256) == 1
+        b = bi.matmul(x, w, "nk", out_dtype=torch.float32)
+        alone = bi.matmul(x[3:4].contiguous(), w, "nk", out_dtype=torch.float32)
     finally:
         bi.set_batch_invariant_limit(old)
-    assert bits_equal(a, b)
+    check_f32(a, ref, _abs_scale(gi.x, gi.w_nk), "limit 0 (split K)")
+    check_f32(b, ref, _abs_scale(gi.x, gi.w_nk), "inside the limit")
+    assert bits_equal(alone, b[3:4])

@@ -34,7 +34,7 @@ def _worker(rank, world, port, out):
 
 def test_max_over_ranks_and_weak_scaling_throughput():
     world = 2
-    out = mp.Manager().dict()
+    out = mp.get_context("spawn").Manager().dict()
     mp.spawn(_worker, args=(world, _free_port(), out), nprocs=world, join=True)
     assert dict(out) == {0: 20.0, 1: 20.0}
     import bench

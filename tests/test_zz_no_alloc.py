@@ -70,18 +70,49 @@ def test_static_workspace_matches_caller_workspace_twice(dev):
 
 
 def test_static_workspace_refuses_blocks_beyond_its_size(dev):
-    # 64 sequences x 8 tokens x 32 heads x 129 chunks x 520 B is far above 32 MiB
-    need = bi.attn_workspace_size(512, 32, 128, 65540)
+    """A valid block too large for the scratch: 64 sequences of 65,540 keys with verify
+    blocks of 8 (512 tokens x 32 heads x 129 chunks of partials, far above 32 MiB).  The
+    block tables all point at four shared pages, so the block costs no memory."""
+    B, L, q = 64, 65540, 8
+    need = bi.attn_workspace_size(B * q, 32, 128, L)
     assert need > bi.STATIC_WS_BYTES
-    t, _, _ = _block([1028], [4], seed=303, dev=dev)
-    out = torch.empty(4, 32, 128, dtype=torch.bfloat16, device=dev)
-    lse = torch.empty(4, 32, dtype=torch.float32, device=dev)
-    L = bi.lib()
-    num_pages, hkv, page, _ = t["k_cache"].shape
-    rc = L.bi_verify_block_static_ws(
-        t["q"].data_ptr(), t["k_cache"].data_ptr(), t["v_cache"].data_ptr(), num_pages,
-        t["block_table"].data_ptr(), t["block_table"].shape[1], t["seq_lens"].data_ptr(),
-        t["cu_q"].data_ptr(), 1, 4, 4, 10 ** 7, 32, 8, 128, page, ctypes.c_float(0.1),
-        out.data_ptr(), lse.data_ptr(), torch.cuda.current_stream().cuda_stream)
+    max_pages = -(-L // 64)
+    kc = torch.zeros(4, 8, 64, 128, dtype=torch.bfloat16, device=dev)
+    vc = torch.zeros_like(kc)
+    bt = (torch.arange(B * max_pages, dtype=torch.int32, device=dev) % 4).view(B, max_pages)
+    sl = torch.full((B,), L, dtype=torch.int32, device=dev)
+    cu = torch.arange(0, B * q + 1, q, dtype=torch.int32, device=dev)
+    qt = torch.zeros(B * q, 32, 128, dtype=torch.bfloat16, device=dev)
+    out = torch.empty_like(qt)
+    lse = torch.empty(B * q, 32, dtype=torch.float32, device=dev)
+    L_ = bi.lib()
+    rc = L_.bi_verify_block_static_ws(
+        qt.data_ptr(), kc.data_ptr(), vc.data_ptr(), 4, bt.data_ptr(), max_pages, sl.data_ptr(),
+        cu.data_ptr(), B, B * q, q, L, 32, 8, 128, 64, ctypes.c_float(0.1), out.data_ptr(),
+        lse.data_ptr(), torch.cuda.current_stream().cuda_stream)
     assert rc == bi.BI_ERR_UNSUPPORTED
-    assert "static scratch" in L.bi_last_error_message().decode()
+    assert "static scratch" in L_.bi_last_error_message().decode()
+    assert bi.device_status() == bi.BI_OK
+
+
+def test_static_workspace_outside_the_limit_matches_exact_workspace(dev):
+    """With the limit at 0 the chunk length follows the workspace size: the entry point
+    gives the bits of bi_verify_block handed exactly bi_attn_workspace_size() bytes."""
+    t, max_q, max_len = _block([8196, 16388], [8, 8], seed=304, dev=dev)
+    old = bi.get_batch_invariant_limit()
+    bi.set_batch_invariant_limit(0)
+    try:
+        T = t["q"].shape[0]
+        need = bi.attn_workspace_size(T, 32, 128, max_len)
+        ws = torch.empty(need, dtype=torch.uint8, device=dev)
+        ref, ref_lse = bi.verify_block(t["q"], t["k_cache"], t["v_cache"], t["block_table"],
+                                       t["seq_lens"], t["cu_q"], max_q=max_q,
+                                       max_seq_len=max_len, scale=1.0 / np.sqrt(128),
+                                       workspace=ws)
+        out = torch.empty_like(ref)
+        lse = torch.empty_like(ref_lse)
+        assert _static_call(t, max_q, max_len, out, lse) == bi.BI_OK
+        torch.cuda.synchronize()
+    finally:
+        bi.set_batch_invariant_limit(old)
+    assert bits_equal(out, ref) and bits_equal(lse, ref_lse)
