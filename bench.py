@@ -47,6 +47,8 @@ EPS = 1e-5
 PAGE = 64
 
 SAMPLE_EVERY = 16  # steps between the ones whose calls are individually timed
+REPEAT_MIN_S = 1.5  # wall time of repeated K-step measurements (clock samples need it)
+REPEAT_MAX = 100000
 
 FALLBACK_PEAKS = {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustained": 1700.0}
 
@@ -278,44 +280,72 @@ def run_gpu(args, rank, world, local_rank):
     if bi.device_status() != bi.BI_OK:
         raise RuntimeError("device error word set during warm-up")
 
-    # Per-call CUDA events (same stream as the launches) on every SAMPLE_EVERY-th step of
-    # the timed region: an event recorded between two kernels breaks the programmatic
+    # The timed measurement is K steps bracketed by a barrier and a synchronize, timed
+    # with CUDA events on the launching stream.  It is repeated (REPEAT_MIN_S of repeats,
+    # at least three) so that the clock sampler sees the GPU under this load; the value
+    # is the median repeat.  Per-call CUDA events are recorded on every SAMPLE_EVERY-th
+    # step of every repeat: an event recorded between two kernels breaks the programmatic
     # dependent-launch overlap between them, so recording one around every call of every
-    # step would slow the step it measures.  The sampled steps give the per-call
-    # durations (parts, roofline); start/end events around all K steps give the value.
-    n_sampled = (args.steps + SAMPLE_EVERY - 1) // SAMPLE_EVERY
-    ev = [[torch.cuda.Event(enable_timing=True) for _ in range(len(calls) + 1)]
-          for _ in range(n_sampled)]
+    # step would slow the step it measures.  Those sampled steps give the per-call
+    # durations (parts, roofline).
+    # Sampled steps sit in the second half of each repeat: a repeat starts after a
+    # synchronize, so its first steps run as fast as the host issues them, and the extra
+    # event records of a sampled step would then time the host's issue gaps; by half-way
+    # the host is far enough ahead that the events time the kernels.
+    half = args.steps // 2
+    sampled = [k for k in range(half, args.steps) if (k - half) % SAMPLE_EVERY == 0]
+    is_sampled = set(sampled)
     dist = world > 1
-    if dist:
-        torch.distributed.barrier()
-    torch.cuda.synchronize()
-    start = torch.cuda.Event(enable_timing=True)
-    end = torch.cuda.Event(enable_timing=True)
-    with ClockSampler(local_rank) as clocks:
+
+    def timed_block(rec):
+        ev = [[torch.cuda.Event(enable_timing=True) for _ in range(len(calls) + 1)]
+              for _ in sampled] if rec else None
+        if dist:
+            torch.distributed.barrier()
+        torch.cuda.synchronize()
+        start = torch.cuda.Event(enable_timing=True)
+        end = torch.cuda.Event(enable_timing=True)
         start.record()
         for k in range(args.steps):
-            one_step(ev[k // SAMPLE_EVERY] if k % SAMPLE_EVERY == 0 else None)
+            one_step(ev[(k - half) // SAMPLE_EVERY] if rec and k in is_sampled else None)
         end.record()
         torch.cuda.synchronize()
-    if dist:
-        torch.distributed.barrier()
-    elapsed_ms = start.elapsed_time(end)
+        if dist:
+            torch.distributed.barrier()
+        return start.elapsed_time(end), ev
+
+    reps_ms, events = [], []
+
+    def rep():
+        ms_rep, ev = timed_block(True)
+        reps_ms.append(max_over_ranks(ms_rep, dev))
+        events.extend(ev)
+
+    with ClockSampler(local_rank) as clocks:
+        t_wall = time.perf_counter()
+        for _ in range(3):
+            rep()
+        per = (time.perf_counter() - t_wall) / 3
+        # every rank runs the same number of repeats (the largest any rank asks for)
+        more = max_over_ranks(float(max(0, math.ceil((REPEAT_MIN_S - 3 * per) / per))), dev)
+        for _ in range(min(int(more), REPEAT_MAX)):
+            rep()
     per_call_ms = {n: 0.0 for n in names}
-    for k in range(n_sampled):
+    for evs in events:
         for i, n in enumerate(names):
-            per_call_ms[n] += ev[k][i].elapsed_time(ev[k][i + 1])
-    per_call_ms = {n: v / n_sampled for n, v in per_call_ms.items()}
+            per_call_ms[n] += evs[i].elapsed_time(evs[i + 1])
+    per_call_ms = {n: v / len(events) for n, v in per_call_ms.items()}
     status = bi.device_status()
     if status != bi.BI_OK:
         raise RuntimeError(f"device error word after the timed region: {status}")
-
-    t_max = max_over_ranks(elapsed_ms, dev)
+    elapsed_ms = statistics.median(reps_ms)
 
     e2e = run_e2e(st, args, dist)
     extra = gemm_vs_cublas(st) if rank == 0 else {}
-    return {"elapsed_ms": t_max, "per_call_ms": per_call_ms, "clocks": clocks.summary(),
-            "e2e": e2e, "cublas": extra}
+    kern = kernel_table(dev) if rank == 0 else {}
+    return {"elapsed_ms": elapsed_ms, "reps_ms": reps_ms, "sampled_steps": len(events),
+            "per_call_ms": per_call_ms, "clocks": clocks.summary(), "e2e": e2e,
+            "cublas": extra, "kernels": kern}
 
 
 def run_e2e(st: Step, args, dist):
@@ -416,73 +446,237 @@ def gemm_vs_cublas(st: Step):
     return {"bi_matmul_us": round(a, 2), "cublas_us": round(b, 2), "ratio": round(a / b, 3)}
 
 
+def graph_time_us(fns, n=64, reps=7):
+    """Per-call device time of n calls (cycling through fns) captured in one CUDA graph
+    and replayed, timed with CUDA events around each replay (median of reps): no host
+    launch cost between the calls, so kernels shorter than the Python binding's per-call
+    cost are timed as the GPU runs them back to back."""
+    import torch
+    side = torch.cuda.Stream()
+    side.wait_stream(torch.cuda.current_stream())
+    with torch.cuda.stream(side):
+        for f in fns:  # first calls (function attributes, occupancy queries) uncaptured
+            f()
+    torch.cuda.current_stream().wait_stream(side)
+    torch.cuda.synchronize()
+    g = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(g):
+        for i in range(n):
+            fns[i % len(fns)]()
+    g.replay()
+    torch.cuda.synchronize()
+    ts = []
+    for _ in range(reps):
+        s = torch.cuda.Event(enable_timing=True)
+        e = torch.cuda.Event(enable_timing=True)
+        s.record()
+        g.replay()
+        e.record()
+        torch.cuda.synchronize()
+        ts.append(s.elapsed_time(e) * 1e3 / n)
+    del g
+    return statistics.median(ts)
+
+
+def kernel_table(dev):
+    """The metric's per-kernel half, measured in the same run: the invariant GEMM at
+    K = N = 4096 for M = 1, 2, 4, 8 (both W layouts; HBM-bound: GB/s and the fraction of
+    the measured HBM copy rate) with cuBLAS (torch.matmul, free to split K) at the same
+    shapes and layouts, M = 256 and 2048 (TFLOP/s against the measured bf16 burst peak),
+    and RMSNorm [2048, 8192].  Each figure is the per-call device time of 64 back-to-back
+    calls in one CUDA graph over rotating weight (or input) sets of 256 MB, more than twice
+    the L2, so every call reads its operands from HBM; median of 7 replays."""
+    import torch
+    import invariant_bi_matmul_gb300 as bi
+    from invariant_bi_matmul_gb300 import inputs
+    peaks, kind = load_peaks()
+    hbm, tf = float(peaks["hbm_gbs"]), float(peaks.get("bf16_tflops", 1900.0))
+    N = K = 4096
+    sets = 256 * 1024 * 1024 // (2 * N * K)
+    gi = inputs.gemm_inputs(2048, N, K, seed=2)
+    x = gi.x.to(dev)
+    wnk = [gi.w_nk.to(dev)]
+    wnk += [wnk[0].clone() for _ in range(sets - 1)]
+    wkn = [gi.w_kn.to(dev)]
+    wkn += [wkn[0].clone() for _ in range(sets - 1)]
+    out = {"_how": (f"per-call device time, 64 calls in one CUDA graph over {sets} rotating "
+                    "copies of W (256 MB, > 2x L2), median of 7 replays; peaks "
+                    f"{kind}: HBM {hbm} GB/s, bf16 {tf} TFLOP/s (burst)")}
+    old = bi.get_batch_invariant_limit()
+    bi.set_batch_invariant_limit(1 << 40)
+    try:
+        for M in (1, 2, 4, 8, 256, 2048):
+            xm = x[:M].contiguous()
+            y = torch.empty(M, N, dtype=torch.bfloat16, device=dev)
+            fl = 2.0 * M * N * K
+            by = 2.0 * N * K + 2.0 * M * K + 2.0 * M * N
+            row = {}
+            for lay, ws, cub in (("nk", wnk, lambda w: torch.matmul(xm, w.t(), out=y)),
+                                 ("kn", wkn, lambda w: torch.matmul(xm, w, out=y))):
+                if M > 8 and lay == "kn":
+                    continue
+                t = graph_time_us([lambda w=w: bi.matmul(xm, w, lay, out=y) for w in ws])
+                tc = graph_time_us([lambda w=w: cub(w) for w in ws])
+                row[lay] = {"us": round(t, 2), "TFLOP/s": round(fl / t / 1e6, 1),
+                            "GB/s": round(by / t / 1e3, 1),
+                            "frac_hbm": round(by / t / 1e3 / hbm, 4),
+                            "frac_tensor": round(fl / t / 1e6 / tf, 4),
+                            "cublas_us": round(tc, 2), "vs_cublas": round(t / tc, 3)}
+            row["bound"] = "hbm" if M <= 64 else "tensor"
+            out[f"gemm_M{M}"] = row
+        xr, g = inputs.rmsnorm_inputs(2048, 8192, seed=3)
+        xr, g = xr.to(dev), g.to(dev)
+        by = 4.0 * 2048 * 8192 + 2 * 8192
+        rs = [(xr.clone(), torch.empty_like(xr)) for _ in range(8)]
+        t = graph_time_us([lambda a=a, o=o: bi.rmsnorm(a, g, 1e-5, out=o) for a, o in rs])
+        out["rmsnorm_B2048_H8192"] = {"us": round(t, 2), "GB/s": round(by / t / 1e3, 1),
+                                      "frac_hbm": round(by / t / 1e3 / hbm, 4), "bound": "hbm"}
+    finally:
+        bi.set_batch_invariant_limit(old)
+    del wnk, wkn
+    torch.cuda.empty_cache()
+    return out
+
+
 # --------------------------------------------------------------------- oracle arm
 
-def oracle_step_sample(frac_cols: int = 8, frac_rows: int = 8):
-    """One bounded sample of the step on the CPU oracle: every RMSNorm row and KV-append
-    token, 1/frac_cols of each matmul's output columns, 1/frac_rows of the attention
-    (token, head) rows.  Returns (estimated full-step seconds, description)."""
-    import numpy as np
-    import torch
-    import oracle
-    from invariant_bi_matmul_gb300 import inputs
-    if not hasattr(oracle_step_sample, "data"):
+def cpu_info():
+    """(cores this process may run on, CPU model name)."""
+    import platform
+    cores = len(os.sched_getaffinity(0)) if hasattr(os, "sched_getaffinity") else os.cpu_count()
+    model = None
+    try:
+        out = subprocess.run(["lscpu"], capture_output=True, text=True, timeout=10).stdout
+        for line in out.splitlines():
+            if line.startswith("Model name:"):
+                model = line.split(":", 1)[1].strip()
+                break
+    except (OSError, subprocess.SubprocessError):
+        pass
+    return int(cores or 1), model or platform.processor() or platform.machine()
+
+
+class OracleStep:
+    """The bench step on the CPU oracle, chained as on the GPU: RMSNorm -> NK matmul (q)
+    -> KV append -> verify attention on that q -> KN matmul of its output.  Inputs are the
+    same seeded recipe as the GPU step (drawn on the CPU).  `run(pool)` computes every
+    output of the step; `pool` (a thread pool, or None for one thread) runs independent
+    output columns and attention rows concurrently: the oracle's C code releases the GIL,
+    and nothing in a column or row depends on another."""
+
+    def __init__(self, threads: int):
+        import numpy as np
+        from invariant_bi_matmul_gb300 import inputs
         g = inputs.gemm_inputs(M_TOK, HIDDEN, HIDDEN, seed=5)
         p = inputs.paged_inputs([LK], [M_TOK], Hq=HQ, Hkv=HKV, D=HEAD_DIM, seed=8)
         b = inputs.bf16_bits
-        oracle_step_sample.data = dict(
-            x=b(g.x), gamma=b(inputs.normal_bf16((HIDDEN,), 1.0, 0.1, seed=6)),
-            w_q=b(g.w_nk), w_o=b(inputs.gemm_inputs(1, HIDDEN, HIDDEN, seed=7).w_kn),
-            q=b(p.q), kn=b(p.k_new), vn=b(p.v_new), kc=b(p.k_cache), vc=b(p.v_cache),
-            bt=p.block_table.numpy(), sl=p.seq_lens.numpy(), cu=p.cu_q.numpy())
-    d = oracle_step_sample.data
-    ncols = HIDDEN // frac_cols
-    t = {}
-    t0 = time.perf_counter()
-    h = oracle.rmsnorm(d["x"], d["gamma"], EPS)
-    t["rmsnorm"] = time.perf_counter() - t0
-    hb = oracle.bf16_round(h)
-    t0 = time.perf_counter()
-    oracle.matmul(hb, np.ascontiguousarray(d["w_q"][:ncols]), oracle.W_NK)
-    t["matmul_nk"] = (time.perf_counter() - t0) * frac_cols
-    t0 = time.perf_counter()
-    kc, vc = oracle.kv_append(d["kn"], d["vn"], d["kc"], d["vc"], d["bt"], d["sl"], d["cu"], PAGE)
-    t["kv_append"] = time.perf_counter() - t0
-    t0 = time.perf_counter()
-    rows = [(j, hh) for j in range(M_TOK) for hh in range(HQ)][::frac_rows]
-    for j, hh in rows:
-        oracle.attention_row(d["q"], kc, vc, d["bt"], d["sl"], d["cu"], 0, j, hh, HQ,
-                             1.0 / math.sqrt(HEAD_DIM))
-    t["verify_block"] = (time.perf_counter() - t0) * frac_rows
-    t0 = time.perf_counter()
-    oracle.matmul(hb, np.ascontiguousarray(d["w_o"][:, :ncols]), oracle.W_KN)
-    t["matmul_kn"] = (time.perf_counter() - t0) * frac_cols
-    desc = (f"all {M_TOK} RMSNorm rows and KV-append tokens, 1/{frac_cols} of each matmul's "
-            f"output columns, 1/{frac_rows} of the {M_TOK * HQ} attention (token, head) rows; "
-            f"times scaled to the full step")
-    return sum(t.values()), desc, t
+        self.x = b(g.x)
+        self.gamma = b(inputs.normal_bf16((HIDDEN,), 1.0, 0.1, seed=6))
+        w_q, w_o = b(g.w_nk), b(inputs.gemm_inputs(1, HIDDEN, HIDDEN, seed=7).w_kn)
+        self.kn, self.vn, self.kc, self.vc = b(p.k_new), b(p.v_new), b(p.k_cache), b(p.v_cache)
+        self.bt, self.sl, self.cu = p.block_table.numpy(), p.seq_lens.numpy(), p.cu_q.numpy()
+        # output-column blocks of both weights, cut once (layout preserved)
+        nb = max(1, min(threads * 2, 64))
+        edges = [HIDDEN * i // nb for i in range(nb + 1)]
+        self.cols = list(zip(edges[:-1], edges[1:]))
+        self.wq_blocks = [np.ascontiguousarray(w_q[c0:c1]) for c0, c1 in self.cols]
+        self.wo_blocks = [np.ascontiguousarray(w_o[:, c0:c1]) for c0, c1 in self.cols]
+
+    def _matmul(self, xb, blocks, layout, pool):
+        import numpy as np
+        import oracle
+        run = (lambda w: oracle.matmul(xb, w, layout))
+        parts = list(pool.map(run, blocks)) if pool else [run(w) for w in blocks]
+        return np.concatenate(parts, axis=1)
+
+    def run(self, pool=None):
+        import numpy as np
+        import oracle
+        h = oracle.bf16_round(oracle.rmsnorm(self.x, self.gamma, EPS))
+        q = oracle.bf16_round(self._matmul(h, self.wq_blocks, oracle.W_NK, pool))
+        q = q.reshape(M_TOK, HQ, HEAD_DIM)
+        kc, vc = oracle.kv_append(self.kn, self.vn, self.kc, self.vc, self.bt, self.sl, self.cu,
+                                  PAGE)
+        rows = [(j, hh) for j in range(M_TOK) for hh in range(HQ)]
+        one = (lambda r: oracle.attention_row(q, kc, vc, self.bt, self.sl, self.cu, 0, r[0],
+                                              r[1], HQ, 1.0 / math.sqrt(HEAD_DIM))[0])
+        o = list(pool.map(one, rows)) if pool else [one(r) for r in rows]
+        ob = oracle.bf16_round(np.stack(o).astype(np.float32)).reshape(M_TOK, HIDDEN)
+        return self._matmul(ob, self.wo_blocks, oracle.W_KN, pool)
+
+    def sample_single_thread(self, frac: int = 8):
+        """A bounded single-thread sample (about 1/frac of the step's arithmetic): all
+        RMSNorm rows and KV-append tokens, 1/frac of each matmul's output columns, 1/frac of
+        the attention rows; returns (seconds scaled to the full step, description)."""
+        import numpy as np
+        import oracle
+        t0 = time.perf_counter()
+        h = oracle.bf16_round(oracle.rmsnorm(self.x, self.gamma, EPS))
+        kc, vc = oracle.kv_append(self.kn, self.vn, self.kc, self.vc, self.bt, self.sl, self.cu,
+                                  PAGE)
+        fixed = time.perf_counter() - t0
+        nb = max(1, len(self.cols) // frac)
+        t0 = time.perf_counter()
+        for w in self.wq_blocks[:nb]:
+            oracle.matmul(h, w, oracle.W_NK)
+        for w in self.wo_blocks[:nb]:
+            oracle.matmul(h, w, oracle.W_KN)
+        mm = (time.perf_counter() - t0) * len(self.cols) / nb
+        q = np.zeros((M_TOK, HQ, HEAD_DIM), np.uint16)
+        rows = [(j, hh) for j in range(M_TOK) for hh in range(HQ)][::frac]
+        t0 = time.perf_counter()
+        for j, hh in rows:
+            oracle.attention_row(q, kc, vc, self.bt, self.sl, self.cu, 0, j, hh, HQ,
+                                 1.0 / math.sqrt(HEAD_DIM))
+        at = (time.perf_counter() - t0) * (M_TOK * HQ) / len(rows)
+        desc = (f"one thread: all {M_TOK} RMSNorm rows and KV-append tokens, {nb} of "
+                f"{len(self.cols)} column blocks of each matmul, 1/{frac} of the "
+                f"{M_TOK * HQ} attention rows; times scaled to the full step")
+        return fixed + mm + at, desc
+
+
+def oracle_baseline(steps: int, warmup: int):
+    """The oracle on every host core for `steps` full steps (after `warmup`), plus a
+    bounded single-thread sample: a cpu_baseline object and the per-step seconds."""
+    from concurrent.futures import ThreadPoolExecutor
+    cores, model = cpu_info()
+    st = OracleStep(cores)
+    one_s, one_desc = st.sample_single_thread()
+    total = sum(step_bytes().values())
+    with ThreadPoolExecutor(max_workers=cores) as pool:
+        for _ in range(warmup):
+            st.run(pool)
+        secs = []
+        for _ in range(steps):
+            t0 = time.perf_counter()
+            st.run(pool)
+            secs.append(time.perf_counter() - t0)
+    sec = statistics.median(secs)
+    base = {"value": round(total / sec / 1e9, 4), "unit": "GB/s", "cores": cores,
+            "kind": "oracle", "cpu_model": model,
+            "sample": (f"{steps} full steps (every output of the step, chained as on the GPU) on "
+                       f"{cores} threads over independent output columns and attention rows; "
+                       f"median step {sec:.3f} s"),
+            "single_thread": {"value": round(total / one_s / 1e9, 4), "cores": 1,
+                              "sample": one_desc}}
+    return base, secs
 
 
 def run_reference(args, rank, world):
     if rank != 0:
         return
-    total_bytes = sum(step_bytes().values())
-    for _ in range(args.warmup):
-        oracle_step_sample()
-    secs = []
-    for _ in range(args.steps):
-        s, desc, _ = oracle_step_sample()
-        secs.append(s)
-    sec = statistics.mean(secs)
-    value = total_bytes / sec / 1e9
+    base, secs = oracle_baseline(args.steps, args.warmup)
+    sec = statistics.median(secs)
+    value = sum(step_bytes().values()) / sec / 1e9
     line = {
-        "impl": "reference", "metric": METRIC, "value": value, "unit": "GB/s", "n_gpus": 1,
-        "steps": args.steps, "warmup": args.warmup, "ms_per_step": sec * 1e3,
+        "impl": "reference", "metric": METRIC, "value": round(value, 4), "unit": "GB/s",
+        "n_gpus": 1, "steps": args.steps, "warmup": args.warmup,
+        "ms_per_step": round(sec * 1e3, 2), "ms_per_step_total": round(sum(secs) * 1e3, 1),
         "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f32",
         "data": "synthetic", "config": workload_config(),
-        "cpu_baseline": {"value": value, "unit": "GB/s", "cores": 1, "kind": "oracle",
-                         "sample": desc},
-        "e2e": {"value": value, "unit": "GB/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
+        "cpu_baseline": base,
+        "e2e": {"value": round(value, 4), "unit": "GB/s", "h2d_bytes_per_step": 0,
+                "d2h_bytes_per_step": 0},
     }
     print(json.dumps(line), flush=True)
 
@@ -503,7 +697,7 @@ def workload_config():
 def main():
     ap = argparse.ArgumentParser()
     ap.add_argument("--gpus", type=int, default=1)
-    ap.add_argument("--steps", type=int, default=20000)
+    ap.add_argument("--steps", type=int, default=2000)
     ap.add_argument("--warmup", type=int, default=50)
     ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
     ap.add_argument("--cpu-sample", action="store_true", default=True)
@@ -525,7 +719,7 @@ def main():
     local_rank = int(os.environ.get("LOCAL_RANK", "0"))
 
     if args.impl == "reference":
-        if args.steps == 20000:
+        if args.steps == 2000:
             args.steps = 10
         if args.warmup == 50:
             args.warmup = 3
@@ -535,9 +729,7 @@ def main():
     # The oracle baseline runs before any CUDA work (no fork after CUDA init).
     cpu = None
     if rank == 0 and world == 1 and not args.no_cpu_baseline:
-        s, desc, _ = oracle_step_sample()
-        cpu = {"value": sum(step_bytes().values()) / s / 1e9, "unit": "GB/s", "cores": 1,
-               "kind": "oracle", "sample": desc}
+        cpu, _ = oracle_baseline(steps=3, warmup=1)
 
     import torch
     if world > 1:
@@ -558,9 +750,10 @@ def main():
     value = job_throughput(total, world, ms * 1e-3)
     calls_ms = res["per_call_ms"]
     share = {n: round(v / sum(calls_ms.values()), 4) for n, v in calls_ms.items()}
-    parts = {"_note": f"per-call CUDA events on every {SAMPLE_EVERY}th timed step "
-                      f"({(args.steps + SAMPLE_EVERY - 1) // SAMPLE_EVERY} steps); those steps run "
-                      "without launch overlap, so the parts add up to more than ms_per_step"}
+    parts = {"_note": f"per-call CUDA events on every {SAMPLE_EVERY}th step of the second "
+                      f"half of each repeat ({res['sampled_steps']} steps over all repeats); "
+                      "those steps run without launch overlap between calls, so the parts add "
+                      "up to more than ms_per_step"}
     for n, v in calls_ms.items():
         parts[n] = {"us": round(v * 1e3, 2), "GB/s": round(nbytes[n] / (v * 1e-3) / 1e9, 1),
                     "share": share[n]}
@@ -593,9 +786,17 @@ def main():
                           "ms_per_step": round(e2e["sec_per_step_eager"] * 1e3, 4),
                           "issue": "every copy and call issued from Python each step"}},
         "gpu_launches": Step.LAUNCHES_PER_STEP * args.steps,
+        "gpu_launches_note": "per timed measurement of K steps (every repeat launches as many)",
         "clocks": res["clocks"],
+        "timing": {"repeats": len(res["reps_ms"]),
+                   "ms_per_step_min": round(min(res["reps_ms"]) / args.steps, 5),
+                   "ms_per_step_max": round(max(res["reps_ms"]) / args.steps, 5),
+                   "how": f"each repeat times exactly {args.steps} steps (barrier and "
+                          "synchronize on both sides, CUDA events on the launching stream); "
+                          "value and ms_per_step are the median repeat"},
         "parts": parts,
         "gemm_vs_cublas_m8": res["cublas"],
+        "kernels": res["kernels"],
     }
     print(json.dumps(line), flush=True)
 
@@ -719,34 +920,7 @@ def run_sweep():
         torch.cuda.synchronize()
         return s.elapsed_time(e) * 1e3 / n
 
-    def graph_us(fns, n=64, reps=7):
-        """Per-call device time of n calls (cycling through fns) captured in one CUDA
-        graph: no host launch cost between the calls, so kernels shorter than the Python
-        binding's per-call cost are timed as the GPU runs them back to back."""
-        side = torch.cuda.Stream()
-        side.wait_stream(torch.cuda.current_stream())
-        with torch.cuda.stream(side):
-            for f in fns:  # first calls (function attributes, occupancy queries) uncaptured
-                f()
-        torch.cuda.current_stream().wait_stream(side)
-        torch.cuda.synchronize()
-        g = torch.cuda.CUDAGraph()
-        with torch.cuda.graph(g):
-            for i in range(n):
-                fns[i % len(fns)]()
-        g.replay()
-        torch.cuda.synchronize()
-        ts = []
-        for _ in range(reps):
-            s = torch.cuda.Event(enable_timing=True)
-            e = torch.cuda.Event(enable_timing=True)
-            s.record()
-            g.replay()
-            e.record()
-            torch.cuda.synchronize()
-            ts.append(s.elapsed_time(e) * 1e3 / n)
-        del g
-        return statistics.median(ts)
+    graph_us = graph_time_us
 
     SET_BYTES = 256 * 1024 * 1024  # rotating inputs: more than 2x the 126 MB L2
     INVARIANT, FAST = 1 << 40, 0   # limits: every call inside it / the limit disabled

@@ -269,7 +269,11 @@ bi_status bi_kv_append(const void* k_new, const void* v_new, void* k_cache, void
 
 /* Bytes of caller-provided workspace bi_verify_block / bi_decode_attn need: one fp32
  * partial (m, l, o[head_dim]) per (token, query head, chunk), for chunks of
- * BI_ATTN_CHUNK keys up to max_seq_len.  Returns 0 for invalid arguments. */
+ * BI_ATTN_CHUNK keys up to max_seq_len, rounded up to 16 bytes, then one 4-byte item
+ * counter per (token, query head), rounded up to 16 bytes (the counters of one call's
+ * (sequence, KV head) pairs: the merge of a pair starts as soon as its chunks are done).
+ * The call zeroes the counters itself; no part of the workspace needs initialising.
+ * Returns 0 for invalid arguments. */
 size_t bi_attn_workspace_size(int64_t total_q, int64_t num_q_heads, int64_t head_dim,
                               int64_t max_seq_len);
 

@@ -92,8 +92,11 @@ struct Cfg {
 
 // ------------------------------------------------------------------- partial kernel
 
+// At most 144 registers a thread (7 warps: 32,256 of the SM's 65,536), so that a CTA
+// of the merge kernel (256 threads, at most 128 registers) fits beside it on the SM and
+// can merge a (sequence, KV head) as soon as its items are counted.
 template <int D>
-__global__ void __launch_bounds__(THREADS, 1)
+__global__ void __maxnreg__(144)
 attn_partial_kernel(const __grid_constant__ CUtensorMap tmap_k,
                     const __grid_constant__ CUtensorMap tmap_v,
                     const __nv_bfloat16* __restrict__ q, const int32_t* __restrict__ block_table,
@@ -101,7 +104,7 @@ attn_partial_kernel(const __grid_constant__ CUtensorMap tmap_k,
                     const int32_t* __restrict__ cu_q, int B, int total_q, int max_q,
                     int max_seq_len, int Hq, int Hkv, float scale_log2,
                     float* __restrict__ ws_o, float* __restrict__ ws_ml, int maxC,
-                    int chunk_log2, unsigned int* err) {
+                    int chunk_log2, unsigned int* __restrict__ cnt, unsigned int* err) {
     using C = Cfg<D>;
     const int chunk = 1 << chunk_log2;         // keys per work item (CHUNK when invariant)
     const int chunk_pages = chunk / PAGE;
@@ -239,6 +242,9 @@ attn_partial_kernel(const __grid_constant__ CUtensorMap tmap_k,
             tma_prefetch_desc(&tmap_k);
             tma_prefetch_desc(&tmap_v);
         }
+        // K and V are read once per call: first in line for L2 eviction, so the chunk
+        // partials (written here, read back by the merge) stay in L2
+        const uint64_t kv_policy = l2_policy_evict_first();
         uint32_t g = 0;
         for (int w = blockIdx.x; ok && w < total; w += gridDim.x) {
             int b, c, h;
@@ -259,9 +265,10 @@ attn_partial_kernel(const __grid_constant__ CUtensorMap tmap_k,
                         const int row = (phys * Hkv + h) * PAGE;
 #pragma unroll
                         for (int bx = 0; bx < C::BOXES; ++bx) {
-                            tma_load_2d(st + bx * C::BOX_BYTES, &tmap_k, &full[s], bx * 64, row);
-                            tma_load_2d(st + C::PAGE_BYTES + bx * C::BOX_BYTES, &tmap_v, &full[s],
-                                        bx * 64, row);
+                            tma_load_2d_hint(st + bx * C::BOX_BYTES, &tmap_k, &full[s], bx * 64,
+                                             row, kv_policy);
+                            tma_load_2d_hint(st + C::PAGE_BYTES + bx * C::BOX_BYTES, &tmap_v,
+                                             &full[s], bx * 64, row, kv_policy);
                         }
                     } else {
                         latch_error(err, kErrDeviceArg);
@@ -420,6 +427,11 @@ attn_partial_kernel(const __grid_constant__ CUtensorMap tmap_k,
             __syncwarp();
             if (lane == 0) mbar_arrive(&o_empty[ob]);
             if (store) *reinterpret_cast<float2*>(ws_ml + idx * 2) = make_float2(m_ref, l_tot);
+            // the item's partials are written: count it for its (sequence, KV head), which
+            // the merge waits on (every lane's stores are ordered before the count)
+            __threadfence();
+            __syncwarp();
+            if (lane == 0) atomicAdd(cnt + b * Hkv + h, 1u);
         }
         if (!ok && lane == 0) give_up();
     } else if (warp < NSM) {
@@ -519,6 +531,16 @@ attn_partial_kernel(const __grid_constant__ CUtensorMap tmap_k,
                 xm[sw * MAXR + r] = mt[0];
                 __syncwarp();
                 if (lane == 0) mbar_arrive(&xm_bar[sb]);
+                // While the other warps' slice maxima arrive, P is computed against the
+                // current reference max, which the page keeps unless a row raises it (the
+                // common case).  If any row raises, P is computed again below with the new
+                // reference, so the values are exactly those computed after the exchange.
+                float pv[KSL];
+                {
+                    const float m_spec = m_ref == -INFINITY ? 0.f : m_ref;
+#pragma unroll
+                    for (int k = 0; k < KSL; ++k) pv[k] = ex2(fmaf(sl[k], scale_log2, -m_spec));
+                }
                 if (!wait(&xm_bar[sb], par)) break;
                 float m_raw = xm[r];
 #pragma unroll
@@ -532,6 +554,22 @@ attn_partial_kernel(const __grid_constant__ CUtensorMap tmap_k,
                 const float factor = raise ? ex2(m_ref - m_page) : 1.f;  // 0 on the first
                 if (raise) m_ref = m_page;
                 l_run *= factor;
+                // this warp's 16 keys; a masked key (-inf) gives p = +0
+                // p = exp2(s * scale_log2 - m), the row-slice sum by a fixed pairwise tree
+                if (__any_sync(0xffffffffu, raise)) {
+                    const float m_use = m_ref == -INFINITY ? 0.f : m_ref;
+#pragma unroll
+                    for (int k = 0; k < KSL; ++k) pv[k] = ex2(fmaf(sl[k], scale_log2, -m_use));
+                }
+                uint32_t pk[KSL / 2];
+#pragma unroll
+                for (int k = 0; k < KSL; k += 2) pk[k / 2] = pack_bf16x2(pv[k], pv[k + 1]);
+#pragma unroll
+                for (int width = KSL / 2; width >= 1; width /= 2)
+#pragma unroll
+                    for (int k = 0; k < width; ++k) pv[k] = pv[k] + pv[k + width];
+                const float ps = pv[0];
+                l_run = l_run + ps;
                 // P buffer sb is free once P V of page gi-2 has completed
                 if (!wait(&p_empty[sb], par ^ 1u)) break;
                 if (sw == 0 && i > 0 && __any_sync(0xffffffffu, raise)) {
@@ -551,21 +589,6 @@ attn_partial_kernel(const __grid_constant__ CUtensorMap tmap_k,
                     }
                     tc_fence_before_sync();
                 }
-                const float m_use = m_ref == -INFINITY ? 0.f : m_ref;
-                // this warp's 16 keys; a masked key (-inf) gives p = +0
-                // p = exp2(s * scale_log2 - m), the row-slice sum by a fixed pairwise tree
-                float pv[KSL];
-#pragma unroll
-                for (int k = 0; k < KSL; ++k) pv[k] = ex2(fmaf(sl[k], scale_log2, -m_use));
-                uint32_t pk[KSL / 2];
-#pragma unroll
-                for (int k = 0; k < KSL; k += 2) pk[k / 2] = pack_bf16x2(pv[k], pv[k + 1]);
-#pragma unroll
-                for (int width = KSL / 2; width >= 1; width /= 2)
-#pragma unroll
-                    for (int k = 0; k < width; ++k) pv[k] = pv[k] + pv[k + width];
-                const float ps = pv[0];
-                l_run = l_run + ps;
                 // this warp's 16 keys of P row r (two 16-byte pieces of the 128-byte row)
                 uint8_t* pbuf = sP + sb * C::P_BYTES;
                 *reinterpret_cast<uint4*>(pbuf + swz(r, 2 * sw)) =
@@ -633,14 +656,16 @@ __device__ __forceinline__ void merge_fold(const float* __restrict__ ws_o,
     constexpr int PER = D / 32;
     // The first MERGE_UNROLL partials of the range are requested before anything else
     // (for ranges up to MERGE_UNROLL chunks: all of them, in one global round trip).
+    // loads at L2 (ld.global.cg): the partial kernel may still be running, and this SM's
+    // L1 may hold a neighbouring row's line from before that row was complete
     auto load = [&](int c, float (&v)[PER], float2& ml) {
-        ml = *reinterpret_cast<const float2*>(ws_ml + (base + c) * 2);
+        ml = __ldcg(reinterpret_cast<const float2*>(ws_ml + (base + c) * 2));
         const float* src = ws_o + (base + c) * D + lane * PER;
         if (PER == 4) {
-            const float4 f = *reinterpret_cast<const float4*>(src);
+            const float4 f = __ldcg(reinterpret_cast<const float4*>(src));
             v[0] = f.x; v[1 % PER] = f.y; v[2 % PER] = f.z; v[3 % PER] = f.w;
         } else {
-            const float2 f = *reinterpret_cast<const float2*>(src);
+            const float2 f = __ldcg(reinterpret_cast<const float2*>(src));
             v[0] = f.x; v[1 % PER] = f.y;
         }
     };
@@ -658,7 +683,7 @@ __device__ __forceinline__ void merge_fold(const float* __restrict__ ws_o,
         for (int u = 0; u < MERGE_UNROLL; ++u)
             if (c0 + u < c1) Mw = fmaxf(Mw, ml[u].x);
     } else {
-        for (int c = c0 + lane; c < c1; c += 32) Mw = fmaxf(Mw, ws_ml[(base + c) * 2]);
+        for (int c = c0 + lane; c < c1; c += 32) Mw = fmaxf(Mw, __ldcg(ws_ml + (base + c) * 2));
 #pragma unroll
         for (int off = 16; off >= 1; off >>= 1)
             Mw = fmaxf(Mw, __shfl_xor_sync(0xffffffffu, Mw, off));
@@ -717,7 +742,8 @@ __device__ __forceinline__ void merge_combine(const float (&Mw)[MERGE_WARPS],
 // sequence is malformed or the token belongs to none.
 __device__ __forceinline__ bool merge_row(const int32_t* __restrict__ seq_lens,
                                           const int32_t* __restrict__ cu_q, int B, int total_q,
-                                          int max_q, int max_seq_len, int t, int& pos) {
+                                          int max_q, int max_seq_len, int t, int& pos, int& bq,
+                                          int& len) {
     int b;
     if (cu_q) {
         int lo = 0, hi = B;  // largest b with cu_q[b] <= t
@@ -732,26 +758,71 @@ __device__ __forceinline__ bool merge_row(const int32_t* __restrict__ seq_lens,
     const SeqInfo si = seq_info(seq_lens, cu_q, b);
     if (!seq_ok(si, max_q, max_seq_len, total_q) || t < si.t0 || t >= si.t0 + si.qb) return false;
     pos = si.L - si.qb + (t - si.t0);
+    bq = b;
+    len = si.L;
     return true;
+}
+
+__device__ __forceinline__ unsigned int ld_acquire_u32(const unsigned int* p) {
+    unsigned int v;
+    asm volatile("ld.acquire.gpu.global.u32 %0, [%1];" : "=r"(v) : "l"(p) : "memory");
+    return v;
+}
+
+// Waits (bounded, about kWaitTimeoutNs) until the partial kernel has counted `target`
+// finished items of one (sequence, KV head); acquire, so the items' partials are visible
+// to this thread and, after a barrier, to its CTA or warp.  False on timeout.
+__device__ __noinline__ bool wait_items(const unsigned int* cnt, unsigned int target) {
+    if (ld_acquire_u32(cnt) >= target) return true;
+    const long long budget = static_cast<long long>(kWaitTimeoutNs) * 5 / 2;  // cycles
+    const long long t0 = clock64();
+    for (;;) {
+        __nanosleep(256);
+        if (ld_acquire_u32(cnt) >= target) return true;
+        if (clock64() - t0 > budget) return false;
+    }
+}
+
+// Zeroes the item counters of one call (after the previous grid in the stream, which may
+// be the previous call's merge still reading them); the partial kernel waits for this grid.
+__global__ void __launch_bounds__(256) attn_count_reset_kernel(unsigned int* cnt, int n) {
+    pdl_wait();
+    pdl_trigger();
+    for (int i = blockIdx.x * 256 + threadIdx.x; i < n; i += gridDim.x * 256) cnt[i] = 0u;
 }
 
 // One CTA per row: warp w folds range w (latency: a few rows, long contexts).
 template <int D>
 __global__ void __launch_bounds__(MERGE_WARPS * 32)
 attn_merge_kernel(const int32_t* __restrict__ seq_lens, const int32_t* __restrict__ cu_q, int B,
-                  int total_q, int max_q, int max_seq_len, int Hq,
-                  const float* __restrict__ ws_o, const float* __restrict__ ws_ml, int maxC,
-                  int chunk_log2, __nv_bfloat16* __restrict__ out, float* __restrict__ lse) {
+                  int total_q, int max_q, int max_seq_len, int Hq, int Hkv,
+                  const float* ws_o, const float* ws_ml, int maxC, int chunk_log2,
+                  const unsigned int* cnt, __nv_bfloat16* __restrict__ out,
+                  float* __restrict__ lse, unsigned int* err) {
     constexpr int PER = D / 32;
     __shared__ float sM[MERGE_WARPS], sL[MERGE_WARPS];
     __shared__ float sO[MERGE_WARPS][D];
-    pdl_wait();
+    __shared__ int s_ready;
+    // With item counters this grid may start while the partial kernel runs: every grid
+    // before that kernel has completed (it waited for them before letting this one
+    // launch), and each row waits for its own (sequence, KV head)'s items below.
+    // Without counters, the whole previous grid.
+    if (!cnt) pdl_wait();
     pdl_trigger();
     const int t = int(blockIdx.x / unsigned(Hq));
     const int hq = int(blockIdx.x - unsigned(t) * unsigned(Hq));
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-    int pos;
-    if (!merge_row(seq_lens, cu_q, B, total_q, max_q, max_seq_len, t, pos)) return;
+    int pos, b, L;
+    if (!merge_row(seq_lens, cu_q, B, total_q, max_q, max_seq_len, t, pos, b, L)) return;
+    if (cnt) {
+        if (threadIdx.x == 0) {
+            const unsigned int items = unsigned((L + (1 << chunk_log2) - 1) >> chunk_log2);
+            s_ready = wait_items(cnt + b * Hkv + hq / (Hq / Hkv), items) ? 1 : 0;
+            if (!s_ready) latch_error(err, kErrTimeout);
+        }
+        __syncthreads();
+        if (!s_ready) return;
+    }
     const int nC = (pos >> chunk_log2) + 1;
     const int64_t base = (int64_t(t) * Hq + hq) * maxC;
     float Mw, Lw, acc[PER];
@@ -782,20 +853,30 @@ attn_merge_kernel(const int32_t* __restrict__ seq_lens, const int32_t* __restric
 template <int D, int UNR>
 __global__ void __launch_bounds__(MERGE_WARPS * 32)
 attn_merge_rows_kernel(const int32_t* __restrict__ seq_lens, const int32_t* __restrict__ cu_q,
-                       int B, int total_q, int max_q, int max_seq_len, int Hq,
-                       const float* __restrict__ ws_o, const float* __restrict__ ws_ml, int maxC,
-                       int chunk_log2, __nv_bfloat16* __restrict__ out,
-                       float* __restrict__ lse) {
+                       int B, int total_q, int max_q, int max_seq_len, int Hq, int Hkv,
+                       const float* ws_o, const float* ws_ml, int maxC, int chunk_log2,
+                       const unsigned int* cnt, __nv_bfloat16* __restrict__ out,
+                       float* __restrict__ lse, unsigned int* err) {
     constexpr int PER = D / 32;
-    pdl_wait();
+    if (!cnt) pdl_wait();  // see attn_merge_kernel
     pdl_trigger();
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
     const int64_t row = int64_t(blockIdx.x) * MERGE_WARPS + warp;
     if (row >= int64_t(total_q) * Hq) return;
     const int t = int(row / Hq);
     const int hq = int(row - int64_t(t) * Hq);
-    int pos;
-    if (!merge_row(seq_lens, cu_q, B, total_q, max_q, max_seq_len, t, pos)) return;
+    int pos, b, L;
+    if (!merge_row(seq_lens, cu_q, B, total_q, max_q, max_seq_len, t, pos, b, L)) return;
+    if (cnt) {
+        int ready = 1;
+        if (lane == 0) {
+            const unsigned int items = unsigned((L + (1 << chunk_log2) - 1) >> chunk_log2);
+            ready = wait_items(cnt + b * Hkv + hq / (Hq / Hkv), items) ? 1 : 0;
+            if (!ready) latch_error(err, kErrTimeout);
+        }
+        __syncwarp();  // orders lane 0's acquire before the other lanes' loads
+        if (!__shfl_sync(0xffffffffu, ready, 0)) return;
+    }
     const int nC = (pos >> chunk_log2) + 1;
     const int64_t base = (int64_t(t) * Hq + hq) * maxC;
     // the host picks UNR >= maxC >= nC for every valid row
@@ -808,14 +889,14 @@ attn_merge_rows_kernel(const int32_t* __restrict__ seq_lens, const int32_t* __re
     float2 ml[UNR];
 #pragma unroll
     for (int c = 0; c < UNR; ++c) {
-        if (c < nC) {
-            ml[c] = *reinterpret_cast<const float2*>(ws_ml + (base + c) * 2);
+        if (c < nC) {  // at L2, as merge_fold loads
+            ml[c] = __ldcg(reinterpret_cast<const float2*>(ws_ml + (base + c) * 2));
             const float* src = ws_o + (base + c) * D + lane * PER;
             if (PER == 4) {
-                const float4 f = *reinterpret_cast<const float4*>(src);
+                const float4 f = __ldcg(reinterpret_cast<const float4*>(src));
                 v[c][0] = f.x; v[c][1 % PER] = f.y; v[c][2 % PER] = f.z; v[c][3 % PER] = f.w;
             } else {
-                const float2 f = *reinterpret_cast<const float2*>(src);
+                const float2 f = __ldcg(reinterpret_cast<const float2*>(src));
                 v[c][0] = f.x; v[c][1 % PER] = f.y;
             }
         }
@@ -889,6 +970,22 @@ kv_append_kernel(const uint4* __restrict__ k_new, const uint4* __restrict__ v_ne
     v_cache[dst] = v_new[src];
 }
 
+// Workspace of one call: the chunk partials (o [T][Hq][chunks][D], then (m, l)
+// [T][Hq][chunks][2], fp32), then at the next 16-byte boundary one item counter per
+// (sequence, KV head), bounded by T x Hq words.
+size_t partials_bytes(int64_t total_q, int64_t hq, int64_t head_dim, int64_t chunks) {
+    const size_t b = size_t(total_q) * size_t(hq) * size_t(chunks) * size_t(head_dim + 2) *
+                     sizeof(float);
+    return (b + 15) / 16 * 16;
+}
+
+size_t workspace_for(int64_t total_q, int64_t hq, int64_t head_dim, int64_t max_seq_len,
+                     int chunk_log2) {
+    const int64_t chunk = int64_t(1) << chunk_log2;
+    const int64_t chunks = (max_seq_len + chunk - 1) / chunk;
+    return partials_bytes(total_q, hq, head_dim, chunks) +
+           (size_t(total_q) * size_t(hq) * sizeof(unsigned int) + 15) / 16 * 16;
+}
 template <int D>
 cudaError_t launch_attention_t(const DeviceInfo& dev, const void* q, const PagedArgs& a,
                                float scale, void* out, float* lse, void* workspace,
@@ -914,20 +1011,27 @@ cudaError_t launch_attention_t(const DeviceInfo& dev, const void* q, const Paged
     const int grid = int(items_bound < dev.num_sms ? items_bound : dev.num_sms);
     float* ws_o = static_cast<float*>(workspace);
     float* ws_ml = ws_o + a.total_q * a.hq * int64_t(maxC) * D;
+    unsigned int* cnt = reinterpret_cast<unsigned int*>(
+        static_cast<uint8_t*>(workspace) + partials_bytes(a.total_q, a.hq, D, maxC));
+    const int ncnt = int(a.batch * a.hkv);
     const float scale_log2 = scale * kLog2e;
-    cudaError_t e = launch_pdl(
+    cudaError_t e = launch_pdl(attn_count_reset_kernel, dim3((ncnt + 1023) / 1024), dim3(256), 0,
+                               stream, cnt, ncnt);
+    if (e != cudaSuccess) return e;
+    e = launch_pdl(
         kern, dim3(grid), dim3(THREADS), Cf::SMEM, stream, tk, tv,
         static_cast<const __nv_bfloat16*>(q), a.block_table, int(a.max_pages), int(a.num_pages),
         a.seq_lens, a.cu_q, int(a.batch), int(a.total_q), int(a.max_q), int(a.max_seq_len),
-        int(a.hq), int(a.hkv), scale_log2, ws_o, ws_ml, maxC, chunk_log2, dev.err_word);
+        int(a.hq), int(a.hkv), scale_log2, ws_o, ws_ml, maxC, chunk_log2, cnt, dev.err_word);
     if (e != cudaSuccess) return e;
-    return launch_attn_merge(a, workspace, chunk_log2, out, lse, stream);
+    return launch_attn_merge(a, workspace, chunk_log2, out, lse, cnt, dev.err_word, stream);
 }
 
 }  // namespace
 
 cudaError_t launch_attn_merge(const PagedArgs& a, void* workspace, int chunk_log2, void* out,
-                              float* lse, cudaStream_t stream) {
+                              float* lse, const unsigned int* cnt, unsigned int* err,
+                              cudaStream_t stream) {
     const int chunk = 1 << chunk_log2;
     const int maxC = int((a.max_seq_len + chunk - 1) / chunk);
     const float* ws_o = static_cast<const float*>(workspace);
@@ -940,8 +1044,8 @@ cudaError_t launch_attn_merge(const PagedArgs& a, void* workspace, int chunk_log
         auto kern = a.head_dim == 64 ? attn_merge_kernel<64> : attn_merge_kernel<128>;
         return launch_pdl(kern, dim3(unsigned(rows)), dim3(MERGE_WARPS * 32), 0, stream,
                           a.seq_lens, a.cu_q, int(a.batch), int(a.total_q), int(a.max_q),
-                          int(a.max_seq_len), int(a.hq), ws_o, ws_ml, maxC, chunk_log2,
-                          static_cast<__nv_bfloat16*>(out), lse);
+                          int(a.max_seq_len), int(a.hq), int(a.hkv), ws_o, ws_ml, maxC,
+                          chunk_log2, cnt, static_cast<__nv_bfloat16*>(out), lse, err);
     }
     auto kern = a.head_dim == 64
                     ? (maxC <= 4 ? attn_merge_rows_kernel<64, 4>
@@ -952,18 +1056,10 @@ cudaError_t launch_attn_merge(const PagedArgs& a, void* workspace, int chunk_log
                                              : attn_merge_rows_kernel<128, MERGE_UNROLL>);
     return launch_pdl(kern, dim3(unsigned((rows + MERGE_WARPS - 1) / MERGE_WARPS)),
                       dim3(MERGE_WARPS * 32), 0, stream, a.seq_lens, a.cu_q, int(a.batch),
-                      int(a.total_q), int(a.max_q), int(a.max_seq_len), int(a.hq), ws_o, ws_ml,
-                      maxC, chunk_log2, static_cast<__nv_bfloat16*>(out), lse);
+                      int(a.total_q), int(a.max_q), int(a.max_seq_len), int(a.hq), int(a.hkv),
+                      ws_o, ws_ml, maxC, chunk_log2, cnt, static_cast<__nv_bfloat16*>(out), lse,
+                      err);
 }
-
-namespace {
-size_t workspace_for(int64_t total_q, int64_t hq, int64_t head_dim, int64_t max_seq_len,
-                     int chunk_log2) {
-    const int64_t chunk = int64_t(1) << chunk_log2;
-    const int64_t chunks = (max_seq_len + chunk - 1) / chunk;
-    return size_t(total_q) * size_t(hq) * size_t(chunks) * size_t(head_dim + 2) * sizeof(float);
-}
-}  // namespace
 
 size_t attn_workspace_bytes(int64_t total_q, int64_t hq, int64_t head_dim, int64_t max_seq_len) {
     return workspace_for(total_q, hq, head_dim, max_seq_len, CHUNK_LOG2);

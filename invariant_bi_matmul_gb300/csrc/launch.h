@@ -150,9 +150,13 @@ cudaError_t launch_attention(const DeviceInfo& dev, const void* q, const PagedAr
                              int chunk_log2, cudaStream_t stream);
 
 // The log-sum-exp merge of the chunk partials in `workspace` (as the split-KV kernels
-// leave them for chunk length 2^chunk_log2) into out (and lse).
+// leave them for chunk length 2^chunk_log2) into out (and lse).  With `cnt` (the item
+// counters the decode / verify partial kernel increments) each row waits for its own
+// (sequence, KV head)'s items and the merge may overlap the partial kernel; with nullptr
+// it waits for the whole previous grid.  Timeouts are latched in `err`.
 cudaError_t launch_attn_merge(const PagedArgs& a, void* workspace, int chunk_log2, void* out,
-                              float* lse, cudaStream_t stream);
+                              float* lse, const unsigned int* cnt, unsigned int* err,
+                              cudaStream_t stream);
 
 // Chunked prefill (prefill.cu): blocks of any width, each query reduced exactly as the
 // decode / verify kernels reduce it (invariant chunk length), then the same merge.

@@ -610,7 +610,7 @@ cudaError_t launch_prefill_t(const DeviceInfo& dev, const void* q, const PagedAr
                                int(a.max_seq_len), int(a.hq), int(a.hkv), scale * kLog2e, ws_o,
                                ws_ml, maxC, dev.err_word);
     if (e != cudaSuccess) return e;
-    return launch_attn_merge(a, workspace, CHUNK_LOG2, out, lse, stream);
+    return launch_attn_merge(a, workspace, CHUNK_LOG2, out, lse, nullptr, dev.err_word, stream);
 }
 
 }  // namespace

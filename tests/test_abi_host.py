@@ -209,9 +209,12 @@ def test_prefill_argument_errors_before_launch(L):
 
 
 def test_workspace_size_formula(L):
-    # one (m, l, o[D]) fp32 partial per (token, head, 512-key chunk)
-    assert L.bi_attn_workspace_size(8, 32, 128, 65540) == 8 * 32 * 129 * (128 + 2) * 4
-    assert L.bi_attn_workspace_size(1, 4, 64, 128) == 1 * 4 * 1 * 66 * 4
+    # one (m, l, o[D]) fp32 partial per (token, head, 512-key chunk), then one 4-byte item
+    # counter per (token, head), each part rounded up to 16 bytes
+    r16 = lambda n: -(-n // 16) * 16  # noqa: E731
+    assert L.bi_attn_workspace_size(8, 32, 128, 65540) == r16(8 * 32 * 129 * 130 * 4) + r16(8 * 32 * 4)
+    assert L.bi_attn_workspace_size(1, 4, 64, 128) == r16(1 * 4 * 1 * 66 * 4) + r16(4 * 4)
+    assert L.bi_attn_workspace_size(3, 1, 64, 64) == r16(3 * 66 * 4) + r16(3 * 4)
     assert L.bi_attn_workspace_size(1, 4, 96, 128) == 0
     assert L.bi_attn_workspace_size(1, 4, 64, 0) == 0
 

@@ -55,6 +55,10 @@ def test_reference_arm_prints_one_oracle_line():
     assert len(lines) == 1
     d = json.loads(lines[0])
     assert d["impl"] == "reference" and d["unit"] == "GB/s" and d["value"] > 0
-    assert d["cpu_baseline"]["kind"] == "oracle" and d["cpu_baseline"]["cores"] == 1
+    assert d["cpu_baseline"]["kind"] == "oracle" and d["cpu_baseline"]["cores"] >= 1
+    assert d["cpu_baseline"]["value"] == d["value"] and d["cpu_baseline"]["cpu_model"]
+    assert d["cpu_baseline"]["single_thread"]["cores"] == 1
+    # what ran: steps x ms_per_step is the measured total, not an extrapolation
+    assert d["steps"] * d["ms_per_step"] <= 1.5 * d["ms_per_step_total"]
     assert d["e2e"]["h2d_bytes_per_step"] == 0 and d["e2e"]["value"] == d["value"]
     assert d["metric"].startswith("invariant GEMM")
