@@ -398,6 +398,18 @@ bi_status bi_device_status(bi_stream_t stream);
  * usable.  Used by the tests to exercise the timeout path without faulting a GPU. */
 bi_status bi_selftest_wait_timeout(uint64_t timeout_ns, bi_stream_t stream);
 
+/* Failure-detection self-test of the real kernels: sets the budget of every bounded wait
+ * in the GEMM, attention and prefill kernels (and the merge) of the current device to
+ * timeout_ns nanoseconds (1e3 .. 1e10), or back to the library default (about 4 s) with
+ * 0.  Stream-ordered (kernels issued on `stream` after the call see it; the call
+ * synchronises `stream`).  With a budget shorter than a call's runtime the call's waits
+ * run out: the kernels latch BI_ERR_TIMEOUT in the error word, raise their CTA's abort
+ * flag, let the copies and MMAs already issued complete (each such drain bounded by
+ * 100 ms, not by this budget), free tensor memory and return, leaving the context
+ * usable.  The outputs of a call that timed out are undefined.  Process-wide per device;
+ * for tests only.  BI_ERR_INVALID_ARG for other values. */
+bi_status bi_selftest_set_wait_budget(uint64_t timeout_ns, bi_stream_t stream);
+
 #ifdef __cplusplus
 }
 #endif

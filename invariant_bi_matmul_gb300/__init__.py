@@ -60,6 +60,7 @@ SIGNATURES = {
                                    _i64, _i64, _i64, _f32, _p, _p, _p], _int),
     "bi_device_status": ([_p], _int),
     "bi_selftest_wait_timeout": ([ctypes.c_uint64, _p], _int),
+    "bi_selftest_set_wait_budget": ([ctypes.c_uint64, _p], _int),
     # decoder glue (include/bi_glue.h)
     "bi_embedding": ([_p, _i64, _i64, _p, _i64, _p, _i64, _p], _int),
     "bi_rope": ([_p, _i64, _i64, _i64, _i64, _p, _p, _i64, _f32, _p], _int),
@@ -428,6 +429,12 @@ def device_status(stream=None) -> int:
 
 def selftest_wait_timeout(timeout_ns: int, stream=None) -> None:
     _check(lib().bi_selftest_wait_timeout(int(timeout_ns), _stream(stream)))
+
+
+def selftest_set_wait_budget(timeout_ns: int, stream=None) -> None:
+    """Budget of every bounded wait in the kernels (ns; 0 = the library default).  Tests
+    only: see include/bi.h."""
+    _check(lib().bi_selftest_set_wait_budget(int(timeout_ns), _stream(stream)))
 
 
 # ----------------------------------------------------------------------- decoder glue

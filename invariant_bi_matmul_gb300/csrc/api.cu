@@ -20,7 +20,9 @@ namespace bi {
 
 // One 32-bit error word per device (bits: kErrTimeout, kErrDeviceArg).  Host code only
 // ever uses the address obtained from cudaGetSymbolAddress for the current device.
-__device__ unsigned int g_error_word;
+// Per device: the error word (element 0) and, as the 64-bit word at elements 2..3, the
+// budget of the kernels' bounded waits in ns (0 = the default; only a self-test sets it).
+__device__ __align__(16) unsigned int g_error_block[4];
 
 namespace {
 
@@ -86,8 +88,8 @@ const DeviceInfo* current_device_info(cudaError_t* why) {
         int sms = 0;
         e = cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, d);
         void* word = nullptr;
-        if (e == cudaSuccess) e = cudaGetSymbolAddress(&word, g_error_word);
-        if (e == cudaSuccess) e = cudaMemset(word, 0, sizeof(unsigned int));
+        if (e == cudaSuccess) e = cudaGetSymbolAddress(&word, g_error_block);
+        if (e == cudaSuccess) e = cudaMemset(word, 0, sizeof(g_error_block));
         if (e != cudaSuccess) {
             if (why) *why = e;
             return nullptr;
@@ -564,6 +566,22 @@ BI_EXPORT bi_status bi_device_status(bi_stream_t stream) {
         return fail(BI_ERR_DEVICE_ARG,
                     "a kernel skipped work on an out-of-range device-resident argument "
                     "(error word 0x%x)", word);
+    return BI_OK;
+}
+
+BI_EXPORT bi_status bi_selftest_set_wait_budget(uint64_t timeout_ns, bi_stream_t stream) {
+    if (timeout_ns != 0ull && (timeout_ns < 1000ull || timeout_ns > 10000000000ull))
+        return fail(BI_ERR_INVALID_ARG,
+                    "bi_selftest_set_wait_budget: timeout_ns must be 0 or in [1e3, 1e10]");
+    cudaError_t why = cudaSuccess;
+    const DeviceInfo* dev = current_device_info(&why);
+    if (!dev) return cuda_fail(why, "bi_selftest_set_wait_budget: device query");
+    cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
+    // stream-ordered: kernels issued on `stream` after this call read the new budget
+    const unsigned long long v = timeout_ns;
+    cudaError_t e = cudaMemcpyAsync(dev->err_word + 2, &v, sizeof v, cudaMemcpyHostToDevice, s);
+    if (e == cudaSuccess) e = cudaStreamSynchronize(s);
+    if (e != cudaSuccess) return cuda_fail(e, "bi_selftest_set_wait_budget");
     return BI_OK;
 }
 

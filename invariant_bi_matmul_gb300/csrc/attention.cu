@@ -137,6 +137,7 @@ attn_partial_kernel(const __grid_constant__ CUtensorMap tmap_k,
     int* seq_t0 = seq_len + MAX_BATCH;
     uint8_t* seq_qb = reinterpret_cast<uint8_t*>(seq_t0 + MAX_BATCH);
     volatile int* abort_flag = reinterpret_cast<volatile int*>(seq_qb + MAX_BATCH);
+    const unsigned long long wait_ns = wait_budget_ns(err);
 
     const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
     const int G = Hq / Hkv;
@@ -230,7 +231,7 @@ attn_partial_kernel(const __grid_constant__ CUtensorMap tmap_k,
     };
     bool ok = true;
     auto wait = [&](uint64_t* bar, uint32_t parity) {
-        if (ok && !mbar_wait_warp(bar, parity, abort_flag)) ok = false;
+        if (ok && !mbar_wait_warp(bar, parity, abort_flag, wait_ns)) ok = false;
         return ok;
     };
 
@@ -769,12 +770,13 @@ __device__ __forceinline__ unsigned int ld_acquire_u32(const unsigned int* p) {
     return v;
 }
 
-// Waits (bounded, about kWaitTimeoutNs) until the partial kernel has counted `target`
-// finished items of one (sequence, KV head); acquire, so the items' partials are visible
-// to this thread and, after a barrier, to its CTA or warp.  False on timeout.
-__device__ __noinline__ bool wait_items(const unsigned int* cnt, unsigned int target) {
+// Waits (bounded by timeout_ns) until the partial kernel has counted `target` finished
+// items of one (sequence, KV head); acquire, so the items' partials are visible to this
+// thread and, after a barrier, to its CTA or warp.  False on timeout.
+__device__ __noinline__ bool wait_items(const unsigned int* cnt, unsigned int target,
+                                        unsigned long long timeout_ns) {
     if (ld_acquire_u32(cnt) >= target) return true;
-    const long long budget = static_cast<long long>(kWaitTimeoutNs) * 5 / 2;  // cycles
+    const long long budget = static_cast<long long>(timeout_ns) * 5 / 2;  // cycles
     const long long t0 = clock64();
     for (;;) {
         __nanosleep(256);
@@ -817,7 +819,7 @@ attn_merge_kernel(const int32_t* __restrict__ seq_lens, const int32_t* __restric
     if (cnt) {
         if (threadIdx.x == 0) {
             const unsigned int items = unsigned((L + (1 << chunk_log2) - 1) >> chunk_log2);
-            s_ready = wait_items(cnt + b * Hkv + hq / (Hq / Hkv), items) ? 1 : 0;
+            s_ready = wait_items(cnt + b * Hkv + hq / (Hq / Hkv), items, wait_budget_ns(err)) ? 1 : 0;
             if (!s_ready) latch_error(err, kErrTimeout);
         }
         __syncthreads();
@@ -871,7 +873,7 @@ attn_merge_rows_kernel(const int32_t* __restrict__ seq_lens, const int32_t* __re
         int ready = 1;
         if (lane == 0) {
             const unsigned int items = unsigned((L + (1 << chunk_log2) - 1) >> chunk_log2);
-            ready = wait_items(cnt + b * Hkv + hq / (Hq / Hkv), items) ? 1 : 0;
+            ready = wait_items(cnt + b * Hkv + hq / (Hq / Hkv), items, wait_budget_ns(err)) ? 1 : 0;
             if (!ready) latch_error(err, kErrTimeout);
         }
         __syncwarp();  // orders lane 0's acquire before the other lanes' loads

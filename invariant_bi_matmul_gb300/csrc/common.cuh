@@ -42,6 +42,15 @@ __device__ __forceinline__ void latch_error(unsigned int* err, unsigned int bits
     if (err) atomicOr(err, bits);
 }
 
+// The budget of a kernel's bounded waits, read once per kernel: kWaitTimeoutNs unless a
+// test has shortened it (bi_selftest_set_wait_budget stores it as the 64-bit word that
+// follows the device error word; 0 means the default).
+__device__ __forceinline__ unsigned long long wait_budget_ns(const unsigned int* err) {
+    if (!err) return kWaitTimeoutNs;
+    const unsigned long long b = *reinterpret_cast<const volatile unsigned long long*>(err + 2);
+    return b != 0ull ? b : kWaitTimeoutNs;
+}
+
 // Programmatic dependent launch: wait until the previous grid in the stream has completed
 // and its memory is visible (call before the first global access), and let the next
 // grid be scheduled early (its own wait still orders it after this grid).
@@ -103,27 +112,21 @@ __device__ __forceinline__ bool mbar_try_wait(uint64_t* bar, uint32_t parity) {
 
 // Waits for the phase with the given parity to complete.  Returns false (and never
 // hangs) when `*abort_flag` becomes non-zero or when about `timeout_ns` have passed.
-// The fast path is a bare try_wait; the abort flag and the SM cycle counter (a cheap
-// register read, unlike %globaltimer) are consulted only every 64 polls, and the
-// budget is counted in cycles at <= 2.5 GHz, so a slower clock only lengthens it.
+// The fast path is a bare try_wait; after it, every poll also reads the abort flag and
+// the SM cycle counter (a cheap register read, unlike %globaltimer).  A try_wait may
+// suspend the thread for a while, so checking on every poll keeps short budgets honest.
+// The budget is counted in cycles at <= 2.5 GHz, so a slower clock only lengthens it.
 template <bool CLUSTER = false>
 __device__ __forceinline__ bool mbar_wait(uint64_t* bar, uint32_t parity,
                                           const volatile int* abort_flag,
                                           unsigned long long timeout_ns = kWaitTimeoutNs) {
     if (mbar_try_wait<CLUSTER>(bar, parity)) return true;
     const long long budget = static_cast<long long>(timeout_ns) * 5 / 2;  // cycles
-    long long t0 = 0;
-    for (uint32_t it = 1;; ++it) {
+    const long long t0 = clock64();
+    for (;;) {
         if (mbar_try_wait<CLUSTER>(bar, parity)) return true;
-        if ((it & 63u) == 0u) {
-            if (abort_flag && *abort_flag) return false;
-            const long long now = clock64();
-            if (t0 == 0) {
-                t0 = now;
-            } else if (now - t0 > budget) {
-                return false;
-            }
-        }
+        if (abort_flag && *abort_flag) return false;
+        if (clock64() - t0 > budget) return false;
     }
 }
 

@@ -236,6 +236,7 @@ gemm_kernel(const __grid_constant__ CUtensorMap tmap_x, const __grid_constant__ 
     uint64_t* wfree = conv + MAX_QWBUF;     // QUANT: the MMAs reading buffer b are done
     uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(wfree + MAX_QWBUF);
     volatile int* abort_flag = reinterpret_cast<volatile int*>(tmem_slot + 1);
+    const unsigned long long wait_ns = wait_budget_ns(err);
 
     const int warp = threadIdx.x >> 5;
     const int lane = threadIdx.x & 31;
@@ -406,7 +407,7 @@ gemm_kernel(const __grid_constant__ CUtensorMap tmap_x, const __grid_constant__ 
             const int mt = t / n_tiles, nt = t % n_tiles;
             const int m0 = mt * TILE_M, n0 = nt * tile_n;
             for (int kb = kb0; kb < kb1; kb += kbs) {
-                if (!mbar_wait_warp(&empty[stage], phase ^ 1u, abort_flag)) {
+                if (!mbar_wait_warp(&empty[stage], phase ^ 1u, abort_flag, wait_ns)) {
                     ok = false;
                     break;
                 }
@@ -470,15 +471,15 @@ gemm_kernel(const __grid_constant__ CUtensorMap tmap_x, const __grid_constant__ 
         for (int t = first_tile; ok && t < num_tiles; t += tile_step, ++local) {
             const int acc = local % NACC;
             const uint32_t acc_phase = uint32_t(local / NACC) & 1u;
-            if (!mbar_wait_warp(&tempty[acc], acc_phase ^ 1u, abort_flag)) {
+            if (!mbar_wait_warp(&tempty[acc], acc_phase ^ 1u, abort_flag, wait_ns)) {
                 ok = false;
                 break;
             }
             tc_fence_after_sync();
             const uint32_t d_tmem = tmem_base + uint32_t(acc * ACC_COLS);
             for (int kb = kb0; kb < kb1; kb += kbs) {
-                if (!mbar_wait_warp(&full[stage], phase, abort_flag) ||
-                    (QUANT && !mbar_wait_warp(&conv[wb], wphase, abort_flag))) {
+                if (!mbar_wait_warp(&full[stage], phase, abort_flag, wait_ns) ||
+                    (QUANT && !mbar_wait_warp(&conv[wb], wphase, abort_flag, wait_ns))) {
                     ok = false;
                     break;
                 }
@@ -565,7 +566,7 @@ gemm_kernel(const __grid_constant__ CUtensorMap tmap_x, const __grid_constant__ 
         for (int t = first_tile; t < num_tiles; t += tile_step, ++local) {
             const int acc = local % NACC;
             const uint32_t acc_phase = uint32_t(local / NACC) & 1u;
-            if (!mbar_wait_warp(&tfull[acc], acc_phase, abort_flag)) {
+            if (!mbar_wait_warp(&tfull[acc], acc_phase, abort_flag, wait_ns)) {
                 if (!*abort_flag) fail();
                 break;
             }
@@ -573,8 +574,8 @@ gemm_kernel(const __grid_constant__ CUtensorMap tmap_x, const __grid_constant__ 
                 // rank 0: every partial of this tile has arrived; rank > 0: rank 0 has
                 // read this rank's previous partial out of the slot
                 const bool got = rank == 0
-                    ? mbar_wait_warp<true>(red_full, uint32_t(local & 1), abort_flag)
-                    : mbar_wait_warp<true>(red_free, uint32_t(local & 1) ^ 1u, abort_flag);
+                    ? mbar_wait_warp<true>(red_full, uint32_t(local & 1), abort_flag, wait_ns)
+                    : mbar_wait_warp<true>(red_free, uint32_t(local & 1) ^ 1u, abort_flag, wait_ns);
                 if (!got) {
                     if (!*abort_flag) fail();
                     break;
@@ -741,8 +742,8 @@ gemm_kernel(const __grid_constant__ CUtensorMap tmap_x, const __grid_constant__ 
                 const int kbf = kb0 + (j % spt) * kbs;      // the stage's first K-block
                 const int nk = kb1 - kbf < kbs ? kb1 - kbf : kbs;
                 const int n0 = (t % n_tiles) * tile_n;
-                if (!mbar_wait_warp(&full[stage], phase, abort_flag) ||
-                    !mbar_wait_warp(&wfree[wb], wphase ^ 1u, abort_flag)) {
+                if (!mbar_wait_warp(&full[stage], phase, abort_flag, wait_ns) ||
+                    !mbar_wait_warp(&wfree[wb], wphase ^ 1u, abort_flag, wait_ns)) {
                     ok = false;
                     break;
                 }

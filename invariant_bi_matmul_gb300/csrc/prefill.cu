@@ -113,6 +113,7 @@ attn_prefill_kernel(const __grid_constant__ CUtensorMap tmap_k,
     int* seq_t0 = seq_len + P_MAX_BATCH;
     int* seq_qb = seq_t0 + P_MAX_BATCH;
     volatile int* abort_flag = seq_qb + P_MAX_BATCH;
+    const unsigned long long wait_ns = wait_budget_ns(err);
 
     const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
     const int G = Hq / Hkv;        // query heads per KV head (divides P_ROWS)
@@ -245,7 +246,7 @@ attn_prefill_kernel(const __grid_constant__ CUtensorMap tmap_k,
     };
     bool ok = true;
     auto wait = [&](uint64_t* bar, uint32_t parity) {
-        if (ok && !mbar_wait_warp(bar, parity, abort_flag)) ok = false;
+        if (ok && !mbar_wait_warp(bar, parity, abort_flag, wait_ns)) ok = false;
         return ok;
     };
 
