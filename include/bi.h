@@ -219,6 +219,24 @@ bi_status bi_qmatmul(const void* x, int64_t ldx, const void* wq, int64_t ldwq,
                      int qformat, int group_size, void* y, int64_t ldy, int y_dtype, int64_t M,
                      int64_t N, int64_t K, bi_stream_t stream);
 
+/* bi_qmatmul with the layout of W given  [QMM-3912, Problem and The three defects: the
+ * natural-layout kernel (qmm_n) is where the nvfp4 16-column tail was stored out of
+ * bounds; MLX-4279 review thread: both B orientations]
+ *   w_layout BI_W_NK: as bi_qmatmul.
+ *   w_layout BI_W_KN (natural layout, Y = X * Wd with Wd [K, N]): wq holds one row per k,
+ *     row stride ldwq bytes, the row's N codes packed as above (4-bit: byte n/2, low
+ *     nibble for even n); scales [K][N/group_size] (row stride lds), one per group of
+ *     group_size consecutive n of a row; biases likewise.  N must be a multiple of
+ *     group_size; K any (rows past K read as zeros).  The dequantized tile is laid out as
+ *     bi_matmul's layout-KN W and runs its instruction sequence and K order, so
+ *     Y = bi_matmul(x, Wd, BI_W_KN) bit for bit, for every M (one configuration).
+ *   Both layouts: every tail tile is bounded (codes past N or K are never read into a
+ *   live element, no store past N). */
+bi_status bi_qmatmul_ex(const void* x, int64_t ldx, const void* wq, int64_t ldwq,
+                        const void* scales, int64_t lds, const void* biases, int64_t ldb,
+                        int qformat, int group_size, int w_layout, void* y, int64_t ldy,
+                        int y_dtype, int64_t M, int64_t N, int64_t K, bi_stream_t stream);
+
 /* ---------------------------------------------------------------------------------
  * bi_rmsnorm  [BOOK Case 4 (definition and the load-dependent-tree defect) and Case 6
  * "RMSNorm": data-parallel, one row per core, never split]

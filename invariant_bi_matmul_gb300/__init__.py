@@ -45,6 +45,8 @@ SIGNATURES = {
                      _int),
     "bi_qmatmul": ([_p, _i64, _p, _i64, _p, _i64, _p, _i64, _int, _int, _p, _i64, _int, _i64,
                     _i64, _i64, _p], _int),
+    "bi_qmatmul_ex": ([_p, _i64, _p, _i64, _p, _i64, _p, _i64, _int, _int, _int, _p, _i64, _int,
+                       _i64, _i64, _i64, _p], _int),
     "bi_rmsnorm": ([_p, _i64, _p, _p, _i64, _int, _i64, _i64, _f32, _p], _int),
     "bi_rmsnorm_ex": ([_p, _i64, _p, _p, _i64, _int, _int, _i64, _i64, _f32, _p], _int),
     "bi_kv_append": ([_p, _p, _p, _p, _i64, _p, _i64, _p, _p, _i64, _i64, _i64, _i64, _i64, _p],
@@ -228,9 +230,10 @@ Q_FORMATS = {"mxfp4": 0, "nvfp4": 1, "mxfp8": 2, "affine4": 3, "affine8": 4}
 
 
 def qmatmul(x, wq, scales, fmt: str, group_size: int, K: int, biases=None, out=None,
-            out_dtype=None, stream=None):
-    """Y = X @ dequant(W)^T for bf16 X [M, K] and quantized W (uint8 codes [N, row bytes],
-    see include/bi.h for the encodings); Y bf16 or fp32."""
+            out_dtype=None, stream=None, layout: str = "nk", N: Optional[int] = None):
+    """Y = X @ dequant(W)^T for bf16 X [M, K] and quantized W: layout "nk" (uint8 codes
+    [N, row bytes], quantized along K) or "kn" (codes [K, row bytes] quantized along N;
+    N must be given); see include/bi.h for the encodings.  Y bf16 or fp32."""
     torch = _torch()
     q = Q_FORMATS[fmt]
     _need(x, torch.bfloat16, "x", 2)
@@ -238,7 +241,11 @@ def qmatmul(x, wq, scales, fmt: str, group_size: int, K: int, biases=None, out=N
     M, kx = x.shape
     if kx != K:
         raise ValueError("x must have K columns")
-    N = wq.shape[0]
+    lay = {"nk": BI_W_NK, "kn": BI_W_KN}[layout]
+    if lay == BI_W_NK:
+        N = wq.shape[0]
+    elif N is None or wq.shape[0] != K:
+        raise ValueError("layout 'kn' needs N and codes [K, row bytes]")
     affine = fmt.startswith("affine")
     _need(scales, torch.bfloat16 if affine else torch.uint8, "scales", 2)
     if affine:
@@ -247,11 +254,11 @@ def qmatmul(x, wq, scales, fmt: str, group_size: int, K: int, biases=None, out=N
         out = torch.empty(M, N, dtype=out_dtype or torch.bfloat16, device=x.device)
     if out.dtype not in (torch.bfloat16, torch.float32) or tuple(out.shape) != (M, N):
         raise ValueError("out must be [M,N] bf16 or fp32")
-    _check(lib().bi_qmatmul(
+    _check(lib().bi_qmatmul_ex(
         _ptr(x), _row_major_2d(x, "x"), _ptr(wq), wq.stride(0), _ptr(scales), scales.stride(0),
         _ptr(biases) if affine else None, biases.stride(0) if affine else 0, q, int(group_size),
-        _ptr(out), _row_major_2d(out, "out"), BI_F32 if out.dtype == torch.float32 else BI_BF16,
-        M, N, K, _stream(stream)))
+        lay, _ptr(out), _row_major_2d(out, "out"),
+        BI_F32 if out.dtype == torch.float32 else BI_BF16, M, int(N), K, _stream(stream)))
     return out
 
 

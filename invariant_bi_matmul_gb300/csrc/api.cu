@@ -294,12 +294,15 @@ BI_EXPORT bi_status bi_matmul_ex(const void* x, int64_t ldx, const void* w, int6
 
 // ================================================================ quantized matmul
 
-BI_EXPORT bi_status bi_qmatmul(const void* x, int64_t ldx, const void* wq, int64_t ldwq,
-                               const void* scales, int64_t lds, const void* biases, int64_t ldb,
-                               int qformat, int group_size, void* y, int64_t ldy, int y_dtype,
-                               int64_t M, int64_t N, int64_t K, bi_stream_t stream) {
-    const char* fn = "bi_qmatmul";
+namespace {
+bi_status qmatmul_impl(const char* fn, const void* x, int64_t ldx, const void* wq, int64_t ldwq,
+                       const void* scales, int64_t lds, const void* biases, int64_t ldb,
+                       int qformat, int group_size, int w_layout, void* y, int64_t ldy,
+                       int y_dtype, int64_t M, int64_t N, int64_t K, bi_stream_t stream) {
     init_limit_from_env();
+    if (w_layout != BI_W_NK && w_layout != BI_W_KN)
+        return fail(BI_ERR_INVALID_ARG, "%s: w_layout must be BI_W_NK or BI_W_KN", fn);
+    const bool kn = w_layout == BI_W_KN;
     if (M < 0 || N < 0 || K < 0) return fail(BI_ERR_INVALID_ARG, "%s: negative M/N/K", fn);
     if (M > kI32Max || N > kI32Max || K > kI32Max)
         return fail(BI_ERR_UNSUPPORTED, "%s: M, N, K must be < 2^31", fn);
@@ -311,8 +314,11 @@ BI_EXPORT bi_status bi_qmatmul(const void* x, int64_t ldx, const void* wq, int64
                : group_size != want_gs)
         return fail(BI_ERR_INVALID_ARG, "%s: group_size must be %s", fn,
                     affine ? "32, 64 or 128" : (want_gs == 16 ? "16" : "32"));
-    if (K % group_size != 0)
+    if (!kn && K % group_size != 0)
         return fail(BI_ERR_INVALID_ARG, "%s: K must be a multiple of group_size", fn);
+    if (kn && N % group_size != 0)
+        return fail(BI_ERR_INVALID_ARG,
+                    "%s: N must be a multiple of group_size (layout KN: groups along N)", fn);
     if (y_dtype != BI_BF16 && y_dtype != BI_F32)
         return fail(BI_ERR_INVALID_ARG, "%s: y_dtype must be BI_BF16 or BI_F32", fn);
     if (M == 0 || N == 0) return BI_OK;
@@ -321,11 +327,14 @@ BI_EXPORT bi_status bi_qmatmul(const void* x, int64_t ldx, const void* wq, int64
     if (!aligned(y, ysz)) return fail(BI_ERR_INVALID_ARG, "%s: y not element-aligned", fn);
     if (K > 0) {
         const bool eight = qformat == BI_Q_MXFP8 || qformat == BI_Q_AFFINE8;
-        const int64_t row_bytes = eight ? K : K / 2;
+        // packed codes and groups run along the quantized dimension: K (layout NK, a row
+        // per output column) or N (layout KN, a row per k)
+        const int64_t qdim = kn ? N : K;
+        const int64_t row_bytes = eight ? qdim : qdim / 2;
         if (!x || !wq || !scales || (affine && !biases))
             return fail(BI_ERR_INVALID_ARG, "%s: null x, wq, scales or biases", fn);
-        if (ldx < K || ldwq < row_bytes || lds < K / group_size ||
-            (affine && ldb < K / group_size))
+        if (ldx < K || ldwq < row_bytes || lds < qdim / group_size ||
+            (affine && ldb < qdim / group_size))
             return fail(BI_ERR_INVALID_ARG, "%s: a row stride is too small", fn);
         if (!aligned(x, 16) || ldx % 8 != 0 || !aligned(wq, 16) || ldwq % 16 != 0)
             return fail(BI_ERR_UNSUPPORTED,
@@ -337,12 +346,33 @@ BI_EXPORT bi_status bi_qmatmul(const void* x, int64_t ldx, const void* wq, int64
     cudaError_t why = cudaSuccess;
     const DeviceInfo* dev = current_device_info(&why);
     if (!dev) return cuda_fail(why, fn);
-    cudaError_t e = launch_qgemm(*dev, x, ldx, wq, ldwq, scales, lds, biases, ldb, qformat,
-                                 group_size, y, ldy, y_dtype == BI_F32, M, N, K,
-                                 g_weight_prefetch.load() != 0,
-                                 reinterpret_cast<cudaStream_t>(stream));
+    cudaError_t e =
+        kn ? launch_qgemm_kn(*dev, x, ldx, wq, ldwq, scales, lds, biases, ldb, qformat,
+                             group_size, y, ldy, y_dtype == BI_F32, M, N, K,
+                             g_weight_prefetch.load() != 0, reinterpret_cast<cudaStream_t>(stream))
+           : launch_qgemm(*dev, x, ldx, wq, ldwq, scales, lds, biases, ldb, qformat,
+                          group_size, y, ldy, y_dtype == BI_F32, M, N, K,
+                          g_weight_prefetch.load() != 0, reinterpret_cast<cudaStream_t>(stream));
     if (e != cudaSuccess) return cuda_fail(e, fn);
     return BI_OK;
+}
+}  // namespace
+
+BI_EXPORT bi_status bi_qmatmul(const void* x, int64_t ldx, const void* wq, int64_t ldwq,
+                               const void* scales, int64_t lds, const void* biases, int64_t ldb,
+                               int qformat, int group_size, void* y, int64_t ldy, int y_dtype,
+                               int64_t M, int64_t N, int64_t K, bi_stream_t stream) {
+    return qmatmul_impl("bi_qmatmul", x, ldx, wq, ldwq, scales, lds, biases, ldb, qformat,
+                        group_size, BI_W_NK, y, ldy, y_dtype, M, N, K, stream);
+}
+
+BI_EXPORT bi_status bi_qmatmul_ex(const void* x, int64_t ldx, const void* wq, int64_t ldwq,
+                                  const void* scales, int64_t lds, const void* biases,
+                                  int64_t ldb, int qformat, int group_size, int w_layout, void* y,
+                                  int64_t ldy, int y_dtype, int64_t M, int64_t N, int64_t K,
+                                  bi_stream_t stream) {
+    return qmatmul_impl("bi_qmatmul_ex", x, ldx, wq, ldwq, scales, lds, biases, ldb, qformat,
+                        group_size, w_layout, y, ldy, y_dtype, M, N, K, stream);
 }
 
 // ========================================================================= rmsnorm

@@ -325,7 +325,16 @@ gemm_kernel(const __grid_constant__ CUtensorMap tmap_x, const __grid_constant__ 
         auto issue_w = [&](uint32_t st, int n0, int kb, int nk) {
             const uint32_t bar = full_s + st * 8u;
             const uint32_t b_dst = sB_s + st * stage_b;
-            if (QUANT) {
+            if (QUANT && KN) {
+                // natural layout: the K-block's 64 rows of packed codes, columns n0.. of
+                // the tile (x in bytes: n0 * bits / 8)
+                const uint32_t r_dst = smem_addr(sR) + st * uint32_t(r_bytes);
+                const int xb = (n0 * args.q_kb_bytes) / BK;
+                if (w_once)
+                    tma_load_2d_s_hint(r_dst, &tmap_w, bar, xb, kb * BK, w_policy);
+                else
+                    tma_load_2d_s(r_dst, &tmap_w, bar, xb, kb * BK);
+            } else if (QUANT) {
                 // the packed codes of the K-block (one stage = one K-block), rows n0..
                 const uint32_t r_dst = smem_addr(sR) + st * uint32_t(r_bytes);
                 if (w_once)
@@ -664,6 +673,171 @@ gemm_kernel(const __grid_constant__ CUtensorMap tmap_x, const __grid_constant__ 
                 }
             }
         }
+    } else if (QUANT && KN) {
+        // ---------------------------------------------- converters, natural layout
+        // W is stored [K, N] and quantized along N (one scale per group of gs columns of a
+        // row k; "Fix fp quantized matmul corruption...", the natural-layout qmm_n).  A
+        // stage holds one K-block's 64 rows of packed codes for the tile's columns.  The
+        // two groups of four converter warps take alternate stages (as for the transposed
+        // layout) and write the bf16 tile in the layout a TMA copy of bf16 W [K, N] gives
+        // (N-major, atoms of KN_ATOM_N columns, KN_SWIZZLE-byte swizzle), so the MMA and
+        // its K order are those of the dense KN GEMM.  A thread converts 8-column pieces
+        // (k-row kr, columns 8c8 ..): the same per-element arithmetic as the transposed
+        // layout.  Rows past K and columns past N become zeros; scales are read only for
+        // elements inside W, one iteration ahead.
+        constexpr int PPR = NSUB * BN / 8;       // 8-column pieces per k-row
+        constexpr int NP = BK * PPR / 128;       // pieces per thread per K-block
+        static_assert(NP >= 1 && (BK * PPR) % 128 == 0, "pieces per converter thread");
+        const int cgrp = (warp - 6) >> 2;
+        const int ct = ((warp - 6) & 3) * 32 + lane;  // 0..127 within the group
+        const uint8_t* qs8 = static_cast<const uint8_t*>(args.qscales);
+        const uint16_t* qs16 = static_cast<const uint16_t*>(args.qscales);
+        const int spt = kb1 - kb0;  // stages per tile: one K-block each
+        const int tiles_mine = first_tile < num_tiles
+                                   ? (num_tiles - 1 - first_tile) / tile_step + 1 : 0;
+        const int iters = tiles_mine * spt;
+        if (!args.w_early) pdl_wait();  // scales may come from the previous grid
+        bool ok = true;
+        auto run = [&](auto tag) {
+            constexpr int F = decltype(tag)::value;
+            constexpr bool AFF = F >= 3;
+            constexpr bool EIGHT = F == 2 || F == 4;
+            constexpr int RB = EIGHT ? NSUB * BN : NSUB * BN / 2;  // code bytes per k-row
+            // raw scale (and bias) codes of iteration j's pieces
+            auto fetch = [&](int j, uint32_t (&sc)[NP], uint32_t (&bs)[NP]) {
+                const int t = first_tile + (j / spt) * tile_step;
+                const int kb = kb0 + j % spt;
+                const int n0 = (t % n_tiles) * tile_n;
+#pragma unroll
+                for (int i = 0; i < NP; ++i) {
+                    const int pc = ct + 128 * i;
+                    const int k = kb * BK + pc / PPR;
+                    const int n = n0 + (pc % PPR) * 8;
+                    sc[i] = 0u;
+                    bs[i] = 0u;
+                    if (k < K && n < N) {
+                        const int64_t gi = int64_t(n >> gsh);
+                        if (AFF) {
+                            sc[i] = __ldg(qs16 + int64_t(k) * args.lds + gi);
+                            bs[i] = __ldg(args.qbiases + int64_t(k) * args.ldb + gi);
+                        } else {
+                            sc[i] = __ldg(qs8 + int64_t(k) * args.lds + gi);
+                        }
+                    }
+                }
+            };
+            uint32_t sc[NP] = {}, bs[NP] = {};
+            if (cgrp < iters) fetch(cgrp, sc, bs);
+            uint32_t stage = uint32_t(cgrp), phase = 0;
+            uint32_t wb = uint32_t(cgrp), wphase = 0;
+            for (int j = cgrp; j < iters; j += 2) {
+                uint32_t nsc[NP] = {}, nbs[NP] = {};
+                if (j + 2 < iters) fetch(j + 2, nsc, nbs);
+                const int t = first_tile + (j / spt) * tile_step;
+                const int kb = kb0 + j % spt;
+                const int n0 = (t % n_tiles) * tile_n;
+                if (!mbar_wait_warp(&full[stage], phase, abort_flag, wait_ns) ||
+                    !mbar_wait_warp(&wfree[wb], wphase ^ 1u, abort_flag, wait_ns)) {
+                    ok = false;
+                    break;
+                }
+                const uint8_t* raw = sR + stage * r_bytes;
+                uint8_t* wt = sB + wb * b_bytes;
+#pragma unroll
+                for (int i = 0; i < NP; ++i) {
+                    const int pc = ct + 128 * i;
+                    const int kr = pc / PPR, c8 = pc % PPR;
+                    const bool live = kb * BK + kr < K && n0 + 8 * c8 < N;
+                    uint32_t cw[2];
+                    if (EIGHT) {
+                        const uint2 u = *reinterpret_cast<const uint2*>(raw + kr * RB + 8 * c8);
+                        cw[0] = u.x;
+                        cw[1] = u.y;
+                    } else {
+                        cw[0] = *reinterpret_cast<const uint32_t*>(raw + kr * RB + 4 * c8);
+                        cw[1] = 0u;
+                    }
+                    float scf;
+                    if (F == 0 || F == 2) scf = dec_e8m0(sc[i]);
+                    else if (F == 1) scf = dec_e4m3(sc[i]);
+                    else scf = widen16(uint16_t(sc[i]), false);
+                    const float bsf = AFF ? widen16(uint16_t(bs[i]), false) : 0.f;
+                    uint4 pk;
+                    if (F == 0 || F == 1) {
+                        uint32_t o[4];
+                        e2m1x8_to_bf16(cw[0], o);
+                        const uint32_t s2 = (__float_as_uint(scf) >> 16) * 0x10001u;
+                        pk.x = live ? mul_bf16x2(o[0], s2) : 0u;
+                        pk.y = live ? mul_bf16x2(o[1], s2) : 0u;
+                        pk.z = live ? mul_bf16x2(o[2], s2) : 0u;
+                        pk.w = live ? mul_bf16x2(o[3], s2) : 0u;
+                    } else {
+                        float v[8];
+                        if (live) {
+                            if (F == 2) {
+#pragma unroll
+                                for (int e = 0; e < 4; ++e) {
+                                    const uint32_t pair = (cw[e >> 1] >> (16 * (e & 1))) & 0xffffu;
+                                    const float2 f = h2_to_f2(cvt_e4m3x2(pair));
+                                    v[2 * e] = f.x * scf;
+                                    v[2 * e + 1] = f.y * scf;
+                                }
+                            } else if (F == 4) {
+#pragma unroll
+                                for (int e = 0; e < 8; ++e)
+                                    v[e] = fmaf(scf, byte_to_f32(cw[e >> 2], e & 3), bsf);
+                            } else {
+                                const uint32_t ev = cw[0] & 0x0f0f0f0fu;
+                                const uint32_t od = (cw[0] >> 4) & 0x0f0f0f0fu;
+#pragma unroll
+                                for (int e = 0; e < 8; ++e)
+                                    v[e] = fmaf(scf, byte_to_f32(e & 1 ? od : ev, e >> 1), bsf);
+                            }
+                        } else {
+#pragma unroll
+                            for (int e = 0; e < 8; ++e) v[e] = 0.f;
+                        }
+                        pk.x = pack_bf16x2(v[0], v[1]);
+                        pk.y = pack_bf16x2(v[2], v[3]);
+                        pk.z = pack_bf16x2(v[4], v[5]);
+                        pk.w = pack_bf16x2(v[6], v[7]);
+                    }
+                    // atom c8 / (KN_ATOM_N / 8), k-row kr (KN_SWIZZLE bytes), 16-byte piece
+                    // c8 % (KN_ATOM_N / 8) under the swizzle a TMA copy applies
+                    constexpr int PA = KN_ATOM_N / 8;  // pieces per atom row
+                    const int pa = c8 % PA;
+                    const int sw = KN_SWIZZLE == 128 ? (kr & 7) : ((kr >> 1) & 3);
+                    *reinterpret_cast<uint4*>(wt + (c8 / PA) * KN_ATOM_BYTES + kr * KN_SWIZZLE +
+                                              ((pa ^ sw) << 4)) = pk;
+                }
+                fence_proxy_async_smem();  // generic writes, read by the MMA (async proxy)
+                __syncwarp();
+                if (lane == 0) mbar_arrive(&conv[wb]);
+                stage += 2;
+                if (stage >= uint32_t(S)) {
+                    stage -= uint32_t(S);
+                    phase ^= 1u;
+                }
+                wb += 2;
+                if (wb >= uint32_t(args.wbufs)) {
+                    wb -= uint32_t(args.wbufs);
+                    wphase ^= 1u;
+                }
+#pragma unroll
+                for (int i = 0; i < NP; ++i) {
+                    sc[i] = nsc[i];
+                    bs[i] = nbs[i];
+                }
+            }
+        };
+        switch (args.qfmt) {
+            case 0: run(std::integral_constant<int, 0>{}); break;
+            case 1: run(std::integral_constant<int, 1>{}); break;
+            case 2: run(std::integral_constant<int, 2>{}); break;
+            case 3: run(std::integral_constant<int, 3>{}); break;
+            default: run(std::integral_constant<int, 4>{}); break;
+        }
+        if (!ok && lane == 0 && !*abort_flag) fail();
     } else if (QUANT) {
         // --------------------------------------------------------------- converters
         // Two groups of four converter warps turn the stages' packed codes into the bf16 W
@@ -956,11 +1130,11 @@ cudaError_t launch_split(const DeviceInfo& dev, const CUtensorMap& mx, const CUt
                               SMEM_BYTES, s, unsigned(a.splits), mx, mw, mw, mw, a, dev.err_word);
 }
 
-template <bool F32OUT, int NSUB>
+template <bool F32OUT, int NSUB, bool KN = false>
 cudaError_t launch_q(const DeviceInfo& dev, const CUtensorMap& mx, const CUtensorMap& mw,
                      const CUtensorMap& ms, const CUtensorMap& mb, const GemmArgs& a, int grid,
                      cudaStream_t s) {
-    auto kern = gemm_kernel<false, F32OUT, NSUB, false, 1, true>;
+    auto kern = gemm_kernel<KN, F32OUT, NSUB, false, 1, true>;
     static bool attr_done[64] = {};
     if (dev.device >= 0 && dev.device < 64 && !attr_done[dev.device]) {
         cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize,
@@ -1132,6 +1306,91 @@ cudaError_t launch_gemm(const DeviceInfo& dev, const void* x, int64_t ldx, const
                      : launch_nsub<true, false>(dev, mx, mw, a, grid, stream);
     return y_f32 ? launch_nsub<false, true>(dev, mx, mw, a, grid, stream)
                  : launch_nsub<false, false>(dev, mx, mw, a, grid, stream);
+}
+
+// Quantized W in the natural layout: codes [K, N] (row k: N codes, packed bytes, row
+// stride ldq), quantized along N (scales [K, N/gs], row stride lds; biases likewise).
+// One K-block per stage; the scales are read by the converters, one stage ahead.
+cudaError_t launch_qgemm_kn(const DeviceInfo& dev, const void* x, int64_t ldx, const void* wq,
+                            int64_t ldq, const void* scales, int64_t lds, const void* biases,
+                            int64_t ldb, int fmt, int gs, void* y, int64_t ldy, bool y_f32,
+                            int64_t M, int64_t N, int64_t K, bool w_early, cudaStream_t stream) {
+    if (M == 0 || N == 0) return cudaSuccess;
+    if (K == 0) {
+        const size_t es = y_f32 ? 4 : 2;
+        return cudaMemset2DAsync(y, size_t(ldy) * es, 0, size_t(N) * es, size_t(M), stream);
+    }
+    const int64_t m_tiles = (M + BM - 1) / BM;
+    const int a_rows = m_tiles == 1 ? int((M + 7) / 8 * 8) : BM;
+    int nsub = 1;  // the widest tile that still gives every SM a tile
+    for (int ns = MAX_NSUB; ns > 1; ns >>= 1) {
+        if (m_tiles * ((N + int64_t(ns) * BN - 1) / (int64_t(ns) * BN)) >= dev.num_sms) {
+            nsub = ns;
+            break;
+        }
+    }
+    const bool eight = fmt == 2 || fmt == 4;
+    const int q_kb_bytes = eight ? BK : BK / 2;  // code bytes per 64 elements
+    const int64_t a_bytes = int64_t(a_rows) * BK * 2;
+    const int64_t blk = a_bytes + int64_t(nsub) * BN * q_kb_bytes;  // X block + codes
+    const int64_t bb = int64_t(nsub) * B_KB_BYTES;                   // one bf16 W tile
+    int wbufs = 0, stages = 0;
+    for (int wb = MAX_QWBUF; wb >= 2; wb -= 2) {
+        int st = int((RING_BYTES - wb * bb) / blk);
+        if (st > MAX_QSTAGES) st = MAX_QSTAGES;
+        st &= ~1;  // even: each converter group owns every other stage
+        if (st >= 4 || (wb == 2 && st >= 2)) {
+            wbufs = wb;
+            stages = st;
+            break;
+        }
+    }
+    if (wbufs == 0 || (int64_t(stages) - 1) * a_bytes + A_MMA_BYTES >
+                          int64_t(stages) * a_bytes + wbufs * bb)
+        return cudaErrorNotSupported;
+    CUtensorMap mx, mw;
+    if (!tmap_2d_bf16(&mx, x, uint64_t(K), uint64_t(M), uint64_t(ldx), BK, uint32_t(a_rows), 128) ||
+        !tmap_2d_u8(&mw, wq, uint64_t(eight ? N : N / 2), uint64_t(K), uint64_t(ldq),
+                    uint32_t(eight ? nsub * BN : nsub * BN / 2), uint32_t(BK)))
+        return cudaErrorNotSupported;
+    GemmArgs a{};
+    a.y = y;
+    a.ldy = ldy;
+    a.M = int(M);
+    a.N = int(N);
+    a.K = int(K);
+    a.a_rows = a_rows;
+    a.nsub = nsub;
+    a.kbs = 1;
+    a.blocked = 0;
+    a.stages = stages;
+    a.w_stream_once = m_tiles == 1 ? 1 : 0;
+    a.w_early = w_early ? 1 : 0;
+    a.splits = 1;
+    a.kb_per_split = int((K + BK - 1) / BK);
+    a.f16 = 0;
+    a.qfmt = fmt;
+    a.gs = gs;
+    a.qscales = scales;
+    a.lds = lds;
+    a.qbiases = static_cast<const uint16_t*>(biases);
+    a.ldb = ldb;
+    a.q_kb_bytes = q_kb_bytes;
+    a.wbufs = wbufs;
+    a.q_staged = 0;
+    a.q_srow = Q_SROW;
+    const int64_t tiles = m_tiles * ((N + int64_t(nsub) * BN - 1) / (int64_t(nsub) * BN));
+    const int grid = int(tiles < dev.num_sms ? tiles : dev.num_sms);
+    switch (nsub) {
+        case 1: return y_f32 ? launch_q<true, 1, true>(dev, mx, mw, mw, mw, a, grid, stream)
+                             : launch_q<false, 1, true>(dev, mx, mw, mw, mw, a, grid, stream);
+        case 2: return y_f32 ? launch_q<true, 2, true>(dev, mx, mw, mw, mw, a, grid, stream)
+                             : launch_q<false, 2, true>(dev, mx, mw, mw, mw, a, grid, stream);
+        case 4: return y_f32 ? launch_q<true, 4, true>(dev, mx, mw, mw, mw, a, grid, stream)
+                             : launch_q<false, 4, true>(dev, mx, mw, mw, mw, a, grid, stream);
+        default: return y_f32 ? launch_q<true, MAX_NSUB, true>(dev, mx, mw, mw, mw, a, grid, stream)
+                              : launch_q<false, MAX_NSUB, true>(dev, mx, mw, mw, mw, a, grid, stream);
+    }
 }
 
 cudaError_t launch_qgemm(const DeviceInfo& dev, const void* x, int64_t ldx, const void* wq,

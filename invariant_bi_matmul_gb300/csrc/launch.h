@@ -89,6 +89,13 @@ cudaError_t launch_qgemm(const DeviceInfo& dev, const void* x, int64_t ldx, cons
                          int64_t ldb, int fmt, int gs, void* y, int64_t ldy, bool y_f32,
                          int64_t M, int64_t N, int64_t K, bool w_early, cudaStream_t stream);
 
+// The same for W in the natural layout: codes [K, N] quantized along N (one scale per
+// group of gs consecutive columns of a row).
+cudaError_t launch_qgemm_kn(const DeviceInfo& dev, const void* x, int64_t ldx, const void* wq,
+                            int64_t ldq, const void* scales, int64_t lds, const void* biases,
+                            int64_t ldb, int fmt, int gs, void* y, int64_t ldy, bool y_f32,
+                            int64_t M, int64_t N, int64_t K, bool w_early, cudaStream_t stream);
+
 // fp32 inputs (f32path.cu): CUDA-core matmul, one ascending fmaf chain per element, and
 // RMSNorm with the 16-bit kernel's tree.  y fp32.
 cudaError_t launch_gemm_f32(const void* x, int64_t ldx, const void* w, int64_t ldw, bool w_kn,
