@@ -246,7 +246,8 @@ class Step:
                                               HIDDEN, 0, M_TOK, HIDDEN, HIDDEN, s)),
         ]
 
-    LAUNCHES_PER_STEP = 6  # rmsnorm, gemm, kv_append, attention partial + merge, gemm
+    # rmsnorm, gemm, kv_append, attention (counter reset, partial, merge), gemm
+    LAUNCHES_PER_STEP = 7
 
 
 def run_gpu(args, rank, world, local_rank):
