@@ -92,11 +92,8 @@ struct Cfg {
 
 // ------------------------------------------------------------------- partial kernel
 
-// At most 144 registers a thread (7 warps: 32,256 of the SM's 65,536), so that a CTA
-// of the merge kernel (256 threads, at most 128 registers) fits beside it on the SM and
-// can merge a (sequence, KV head) as soon as its items are counted.
 template <int D>
-__global__ void __maxnreg__(144)
+__global__ void __launch_bounds__(THREADS, 1)
 attn_partial_kernel(const __grid_constant__ CUtensorMap tmap_k,
                     const __grid_constant__ CUtensorMap tmap_v,
                     const __nv_bfloat16* __restrict__ q, const int32_t* __restrict__ block_table,
