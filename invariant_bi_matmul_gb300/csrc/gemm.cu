@@ -857,7 +857,11 @@ gemm_kernel(const __grid_constant__ CUtensorMap tmap_x, const __grid_constant__ 
         constexpr int PARTS = NSUB * BN >= 64 ? 2 : 4;        // threads per tile row
         constexpr int QR = NSUB * BN >= 64 ? NSUB * BN / 64 : 1;  // rows per thread
         const int cgrp = (warp - 6) >> 2;
-        const int half = PARTS == 2 ? ((warp - 6) >> 1) & 1 : (warp - 6) & 3;  // the part
+        // the part: for quarters, lane ct of the group's warp w takes quarter (w + ct) mod 4,
+        // so a warp's lanes read four different 8-byte columns of their rows (the rows of a
+        // code stage are a multiple of 128 bytes apart: one column would put every lane on
+        // the same banks) and the four warps still cover every (row, quarter) once
+        const int half = PARTS == 2 ? ((warp - 6) >> 1) & 1 : ((warp - 6) + lane) & 3;
         const int ct = PARTS == 2 ? ((warp - 6) & 1) * 32 + lane : lane;
         const uint8_t* qs8 = static_cast<const uint8_t*>(args.qscales);
         const uint16_t* qs16 = static_cast<const uint16_t*>(args.qscales);
