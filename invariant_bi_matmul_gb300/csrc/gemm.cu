@@ -90,6 +90,13 @@ constexpr int KN_ATOM_N = BN < 64 ? BN : 64;
 constexpr int KN_ATOM_BYTES = KN_ATOM_N * 2 * BK;  // one atom column of a K-block
 constexpr int KN_SWIZZLE = KN_ATOM_N * 2;          // 64 or 128 bytes
 constexpr uint32_t KN_LAYOUT = KN_SWIZZLE == 128 ? 2u : 4u;
+// Quantized W in the natural layout: K-blocks per stage for a tile of nsub instruction
+// tiles, so that a converter thread holds at most 8 prefetched scale codes (its pieces
+// per K-block: nsub*BN/16) and a code box spans at most 256 k-rows
+__host__ __device__ constexpr int qkn_max_kbs(int nsub) {
+    return nsub * BN / 16 >= 8 ? 1 : (8 / (nsub * BN / 16) < MAX_KBS_KN ? 8 / (nsub * BN / 16)
+                                                                        : MAX_KBS_KN);
+}
 
 static_assert(BN == 32 || BN == 64, "instruction sub-tile N must be 32 or 64");
 static_assert((2 * MAX_STAGES + 7 + 2 * MAX_QWBUF) * 8 + 16 <= CTRL_BYTES,
@@ -328,6 +335,7 @@ gemm_kernel(const __grid_constant__ CUtensorMap tmap_x, const __grid_constant__ 
             if (QUANT && KN) {
                 // natural layout: the K-block's 64 rows of packed codes, columns n0.. of
                 // the tile (x in bytes: n0 * bits / 8)
+                // (rows of the stage's kbs K-blocks: one box of 64*kbs rows, zeros past K)
                 const uint32_t r_dst = smem_addr(sR) + st * uint32_t(r_bytes);
                 const int xb = (n0 * args.q_kb_bytes) / BK;
                 if (w_once)
@@ -677,7 +685,7 @@ gemm_kernel(const __grid_constant__ CUtensorMap tmap_x, const __grid_constant__ 
         // ---------------------------------------------- converters, natural layout
         // W is stored [K, N] and quantized along N (one scale per group of gs columns of a
         // row k; "Fix fp quantized matmul corruption...", the natural-layout qmm_n).  A
-        // stage holds one K-block's 64 rows of packed codes for the tile's columns.  The
+        // stage holds kbs K-blocks' 64*kbs rows of packed codes for the tile's columns.  The
         // two groups of four converter warps take alternate stages (as for the transposed
         // layout) and write the bf16 tile in the layout a TMA copy of bf16 W [K, N] gives
         // (N-major, atoms of KN_ATOM_N columns, KN_SWIZZLE-byte swizzle), so the MMA and
@@ -687,12 +695,14 @@ gemm_kernel(const __grid_constant__ CUtensorMap tmap_x, const __grid_constant__ 
         // elements inside W, one iteration ahead.
         constexpr int PPR = NSUB * BN / 8;       // 8-column pieces per k-row
         constexpr int NP = BK * PPR / 128;       // pieces per thread per K-block
+        constexpr int MAXK = qkn_max_kbs(NSUB);  // K-blocks per stage, at most
         static_assert(NP >= 1 && (BK * PPR) % 128 == 0, "pieces per converter thread");
         const int cgrp = (warp - 6) >> 2;
         const int ct = ((warp - 6) & 3) * 32 + lane;  // 0..127 within the group
         const uint8_t* qs8 = static_cast<const uint8_t*>(args.qscales);
         const uint16_t* qs16 = static_cast<const uint16_t*>(args.qscales);
-        const int spt = kb1 - kb0;  // stages per tile: one K-block each
+        const int nkb_t = kb1 - kb0;
+        const int spt = (nkb_t + kbs - 1) / kbs;  // stages per tile
         const int tiles_mine = first_tile < num_tiles
                                    ? (num_tiles - 1 - first_tile) / tile_step + 1 : 0;
         const int iters = tiles_mine * spt;
@@ -703,38 +713,42 @@ gemm_kernel(const __grid_constant__ CUtensorMap tmap_x, const __grid_constant__ 
             constexpr bool AFF = F >= 3;
             constexpr bool EIGHT = F == 2 || F == 4;
             constexpr int RB = EIGHT ? NSUB * BN : NSUB * BN / 2;  // code bytes per k-row
-            // raw scale (and bias) codes of iteration j's pieces
-            auto fetch = [&](int j, uint32_t (&sc)[NP], uint32_t (&bs)[NP]) {
+            // raw scale (and bias) codes of stage j's pieces, K-block by K-block
+            auto fetch = [&](int j, uint32_t (&sc)[MAXK][NP], uint32_t (&bs)[MAXK][NP]) {
                 const int t = first_tile + (j / spt) * tile_step;
-                const int kb = kb0 + j % spt;
+                const int kbf = kb0 + (j % spt) * kbs;
                 const int n0 = (t % n_tiles) * tile_n;
 #pragma unroll
-                for (int i = 0; i < NP; ++i) {
-                    const int pc = ct + 128 * i;
-                    const int k = kb * BK + pc / PPR;
-                    const int n = n0 + (pc % PPR) * 8;
-                    sc[i] = 0u;
-                    bs[i] = 0u;
-                    if (k < K && n < N) {
-                        const int64_t gi = int64_t(n >> gsh);
-                        if (AFF) {
-                            sc[i] = __ldg(qs16 + int64_t(k) * args.lds + gi);
-                            bs[i] = __ldg(args.qbiases + int64_t(k) * args.ldb + gi);
-                        } else {
-                            sc[i] = __ldg(qs8 + int64_t(k) * args.lds + gi);
+                for (int kk = 0; kk < MAXK; ++kk) {
+#pragma unroll
+                    for (int i = 0; i < NP; ++i) {
+                        const int pc = ct + 128 * i;
+                        const int k = (kbf + kk) * BK + pc / PPR;
+                        const int n = n0 + (pc % PPR) * 8;
+                        sc[kk][i] = 0u;
+                        bs[kk][i] = 0u;
+                        if (kk < kbs && kbf + kk < kb1 && k < K && n < N) {
+                            const int64_t gi = int64_t(n >> gsh);
+                            if (AFF) {
+                                sc[kk][i] = __ldg(qs16 + int64_t(k) * args.lds + gi);
+                                bs[kk][i] = __ldg(args.qbiases + int64_t(k) * args.ldb + gi);
+                            } else {
+                                sc[kk][i] = __ldg(qs8 + int64_t(k) * args.lds + gi);
+                            }
                         }
                     }
                 }
             };
-            uint32_t sc[NP] = {}, bs[NP] = {};
+            uint32_t sc[MAXK][NP] = {}, bs[MAXK][NP] = {};
             if (cgrp < iters) fetch(cgrp, sc, bs);
             uint32_t stage = uint32_t(cgrp), phase = 0;
             uint32_t wb = uint32_t(cgrp), wphase = 0;
             for (int j = cgrp; j < iters; j += 2) {
-                uint32_t nsc[NP] = {}, nbs[NP] = {};
+                uint32_t nsc[MAXK][NP] = {}, nbs[MAXK][NP] = {};
                 if (j + 2 < iters) fetch(j + 2, nsc, nbs);
                 const int t = first_tile + (j / spt) * tile_step;
-                const int kb = kb0 + j % spt;
+                const int kbf = kb0 + (j % spt) * kbs;      // the stage's first K-block
+                const int nk = kb1 - kbf < kbs ? kb1 - kbf : kbs;
                 const int n0 = (t % n_tiles) * tile_n;
                 if (!mbar_wait_warp(&full[stage], phase, abort_flag, wait_ns) ||
                     !mbar_wait_warp(&wfree[wb], wphase ^ 1u, abort_flag, wait_ns)) {
@@ -742,73 +756,80 @@ gemm_kernel(const __grid_constant__ CUtensorMap tmap_x, const __grid_constant__ 
                     break;
                 }
                 const uint8_t* raw = sR + stage * r_bytes;
-                uint8_t* wt = sB + wb * b_bytes;
+                uint8_t* wt = sB + wb * kbs * b_bytes;
 #pragma unroll
-                for (int i = 0; i < NP; ++i) {
-                    const int pc = ct + 128 * i;
-                    const int kr = pc / PPR, c8 = pc % PPR;
-                    const bool live = kb * BK + kr < K && n0 + 8 * c8 < N;
-                    uint32_t cw[2];
-                    if (EIGHT) {
-                        const uint2 u = *reinterpret_cast<const uint2*>(raw + kr * RB + 8 * c8);
-                        cw[0] = u.x;
-                        cw[1] = u.y;
-                    } else {
-                        cw[0] = *reinterpret_cast<const uint32_t*>(raw + kr * RB + 4 * c8);
-                        cw[1] = 0u;
-                    }
-                    float scf;
-                    if (F == 0 || F == 2) scf = dec_e8m0(sc[i]);
-                    else if (F == 1) scf = dec_e4m3(sc[i]);
-                    else scf = widen16(uint16_t(sc[i]), false);
-                    const float bsf = AFF ? widen16(uint16_t(bs[i]), false) : 0.f;
-                    uint4 pk;
-                    if (F == 0 || F == 1) {
-                        uint32_t o[4];
-                        e2m1x8_to_bf16(cw[0], o);
-                        const uint32_t s2 = (__float_as_uint(scf) >> 16) * 0x10001u;
-                        pk.x = live ? mul_bf16x2(o[0], s2) : 0u;
-                        pk.y = live ? mul_bf16x2(o[1], s2) : 0u;
-                        pk.z = live ? mul_bf16x2(o[2], s2) : 0u;
-                        pk.w = live ? mul_bf16x2(o[3], s2) : 0u;
-                    } else {
-                        float v[8];
-                        if (live) {
-                            if (F == 2) {
+                for (int kk = 0; kk < MAXK; ++kk) {
+                    if (kk >= nk) break;
+                    const int kb = kbf + kk;
 #pragma unroll
-                                for (int e = 0; e < 4; ++e) {
-                                    const uint32_t pair = (cw[e >> 1] >> (16 * (e & 1))) & 0xffffu;
-                                    const float2 f = h2_to_f2(cvt_e4m3x2(pair));
-                                    v[2 * e] = f.x * scf;
-                                    v[2 * e + 1] = f.y * scf;
-                                }
-                            } else if (F == 4) {
-#pragma unroll
-                                for (int e = 0; e < 8; ++e)
-                                    v[e] = fmaf(scf, byte_to_f32(cw[e >> 2], e & 3), bsf);
-                            } else {
-                                const uint32_t ev = cw[0] & 0x0f0f0f0fu;
-                                const uint32_t od = (cw[0] >> 4) & 0x0f0f0f0fu;
-#pragma unroll
-                                for (int e = 0; e < 8; ++e)
-                                    v[e] = fmaf(scf, byte_to_f32(e & 1 ? od : ev, e >> 1), bsf);
-                            }
+                    for (int i = 0; i < NP; ++i) {
+                        const int pc = ct + 128 * i;
+                        const int kr = pc / PPR, c8 = pc % PPR;
+                        const bool live = kb * BK + kr < K && n0 + 8 * c8 < N;
+                        const uint8_t* crow = raw + (kk * BK + kr) * RB;
+                        uint32_t cw[2];
+                        if (EIGHT) {
+                            const uint2 u = *reinterpret_cast<const uint2*>(crow + 8 * c8);
+                            cw[0] = u.x;
+                            cw[1] = u.y;
                         } else {
-#pragma unroll
-                            for (int e = 0; e < 8; ++e) v[e] = 0.f;
+                            cw[0] = *reinterpret_cast<const uint32_t*>(crow + 4 * c8);
+                            cw[1] = 0u;
                         }
-                        pk.x = pack_bf16x2(v[0], v[1]);
-                        pk.y = pack_bf16x2(v[2], v[3]);
-                        pk.z = pack_bf16x2(v[4], v[5]);
-                        pk.w = pack_bf16x2(v[6], v[7]);
+                        float scf;
+                        if (F == 0 || F == 2) scf = dec_e8m0(sc[kk][i]);
+                        else if (F == 1) scf = dec_e4m3(sc[kk][i]);
+                        else scf = widen16(uint16_t(sc[kk][i]), false);
+                        const float bsf = AFF ? widen16(uint16_t(bs[kk][i]), false) : 0.f;
+                        uint4 pk;
+                        if (F == 0 || F == 1) {
+                            uint32_t o[4];
+                            e2m1x8_to_bf16(cw[0], o);
+                            const uint32_t s2 = (__float_as_uint(scf) >> 16) * 0x10001u;
+                            pk.x = live ? mul_bf16x2(o[0], s2) : 0u;
+                            pk.y = live ? mul_bf16x2(o[1], s2) : 0u;
+                            pk.z = live ? mul_bf16x2(o[2], s2) : 0u;
+                            pk.w = live ? mul_bf16x2(o[3], s2) : 0u;
+                        } else {
+                            float v[8];
+                            if (live) {
+                                if (F == 2) {
+#pragma unroll
+                                    for (int e = 0; e < 4; ++e) {
+                                        const uint32_t pair = (cw[e >> 1] >> (16 * (e & 1))) & 0xffffu;
+                                        const float2 f = h2_to_f2(cvt_e4m3x2(pair));
+                                        v[2 * e] = f.x * scf;
+                                        v[2 * e + 1] = f.y * scf;
+                                    }
+                                } else if (F == 4) {
+#pragma unroll
+                                    for (int e = 0; e < 8; ++e)
+                                        v[e] = fmaf(scf, byte_to_f32(cw[e >> 2], e & 3), bsf);
+                                } else {
+                                    const uint32_t ev = cw[0] & 0x0f0f0f0fu;
+                                    const uint32_t od = (cw[0] >> 4) & 0x0f0f0f0fu;
+#pragma unroll
+                                    for (int e = 0; e < 8; ++e)
+                                        v[e] = fmaf(scf, byte_to_f32(e & 1 ? od : ev, e >> 1), bsf);
+                                }
+                            } else {
+#pragma unroll
+                                for (int e = 0; e < 8; ++e) v[e] = 0.f;
+                            }
+                            pk.x = pack_bf16x2(v[0], v[1]);
+                            pk.y = pack_bf16x2(v[2], v[3]);
+                            pk.z = pack_bf16x2(v[4], v[5]);
+                            pk.w = pack_bf16x2(v[6], v[7]);
+                        }
+                        // atom c8 / (KN_ATOM_N / 8) (atoms kbs K-blocks apart), K-block kk,
+                        // k-row kr (KN_SWIZZLE bytes), 16-byte piece c8 % (KN_ATOM_N / 8)
+                        // under the swizzle a TMA copy applies
+                        constexpr int PA = KN_ATOM_N / 8;  // pieces per atom row
+                        const int pa = c8 % PA;
+                        const int sw = KN_SWIZZLE == 128 ? (kr & 7) : ((kr >> 1) & 3);
+                        *reinterpret_cast<uint4*>(wt + ((c8 / PA) * kbs + kk) * KN_ATOM_BYTES +
+                                                  kr * KN_SWIZZLE + ((pa ^ sw) << 4)) = pk;
                     }
-                    // atom c8 / (KN_ATOM_N / 8), k-row kr (KN_SWIZZLE bytes), 16-byte piece
-                    // c8 % (KN_ATOM_N / 8) under the swizzle a TMA copy applies
-                    constexpr int PA = KN_ATOM_N / 8;  // pieces per atom row
-                    const int pa = c8 % PA;
-                    const int sw = KN_SWIZZLE == 128 ? (kr & 7) : ((kr >> 1) & 3);
-                    *reinterpret_cast<uint4*>(wt + (c8 / PA) * KN_ATOM_BYTES + kr * KN_SWIZZLE +
-                                              ((pa ^ sw) << 4)) = pk;
                 }
                 fence_proxy_async_smem();  // generic writes, read by the MMA (async proxy)
                 __syncwarp();
@@ -824,10 +845,12 @@ gemm_kernel(const __grid_constant__ CUtensorMap tmap_x, const __grid_constant__ 
                     wphase ^= 1u;
                 }
 #pragma unroll
-                for (int i = 0; i < NP; ++i) {
-                    sc[i] = nsc[i];
-                    bs[i] = nbs[i];
-                }
+                for (int kk = 0; kk < MAXK; ++kk)
+#pragma unroll
+                    for (int i = 0; i < NP; ++i) {
+                        sc[kk][i] = nsc[kk][i];
+                        bs[kk][i] = nbs[kk][i];
+                    }
             }
         };
         switch (args.qfmt) {
@@ -1314,7 +1337,9 @@ cudaError_t launch_gemm(const DeviceInfo& dev, const void* x, int64_t ldx, const
 
 // Quantized W in the natural layout: codes [K, N] (row k: N codes, packed bytes, row
 // stride ldq), quantized along N (scales [K, N/gs], row stride lds; biases likewise).
-// One K-block per stage; the scales are read by the converters, one stage ahead.
+// The scales are read by the converters, one stage ahead.  One M-tile (small M): stages
+// of several K-blocks (one code box of 64*kbs rows), so the per-stage copies, barriers
+// and commits are paid once per several K-blocks.
 cudaError_t launch_qgemm_kn(const DeviceInfo& dev, const void* x, int64_t ldx, const void* wq,
                             int64_t ldq, const void* scales, int64_t lds, const void* biases,
                             int64_t ldb, int fmt, int gs, void* y, int64_t ldy, bool y_f32,
@@ -1336,26 +1361,40 @@ cudaError_t launch_qgemm_kn(const DeviceInfo& dev, const void* x, int64_t ldx, c
     const bool eight = fmt == 2 || fmt == 4;
     const int q_kb_bytes = eight ? BK : BK / 2;  // code bytes per 64 elements
     const int64_t a_bytes = int64_t(a_rows) * BK * 2;
-    const int64_t blk = a_bytes + int64_t(nsub) * BN * q_kb_bytes;  // X block + codes
-    const int64_t bb = int64_t(nsub) * B_KB_BYTES;                   // one bf16 W tile
-    int wbufs = 0, stages = 0;
-    for (int wb = MAX_QWBUF; wb >= 2; wb -= 2) {
-        int st = int((RING_BYTES - wb * bb) / blk);
-        if (st > MAX_QSTAGES) st = MAX_QSTAGES;
-        st &= ~1;  // even: each converter group owns every other stage
-        if (st >= 4 || (wb == 2 && st >= 2)) {
-            wbufs = wb;
-            stages = st;
-            break;
+    auto plan = [&](int k, int& wbufs_out, int& stages_out) {
+        const int64_t blk = k * (a_bytes + int64_t(nsub) * BN * q_kb_bytes);  // X + codes
+        const int64_t bb = int64_t(k) * nsub * B_KB_BYTES;                    // bf16 W tiles
+        wbufs_out = stages_out = 0;
+        for (int wb = MAX_QWBUF; wb >= 2; wb -= 2) {
+            int st = int((RING_BYTES - wb * bb) / blk);
+            if (st > MAX_QSTAGES) st = MAX_QSTAGES;
+            st &= ~1;  // even: each converter group owns every other stage
+            if (st >= 4 || (wb == 2 && st >= 2)) {
+                wbufs_out = wb;
+                stages_out = st;
+                return;
+            }
+        }
+    };
+    int kbs = 1, wbufs = 0, stages = 0;
+    if (m_tiles == 1) {
+        const int64_t nkb = (K + BK - 1) / BK;
+        for (kbs = qkn_max_kbs(int(nsub)); kbs > 1 && nkb < 4 * kbs; kbs >>= 1) {
+        }  // keep >= 4 stages per tile
+        for (; kbs > 1; kbs >>= 1) {  // and a ring of >= 4 stages
+            plan(kbs, wbufs, stages);
+            if (stages >= 4) break;
         }
     }
-    if (wbufs == 0 || (int64_t(stages) - 1) * a_bytes + A_MMA_BYTES >
-                          int64_t(stages) * a_bytes + wbufs * bb)
+    plan(kbs, wbufs, stages);
+    const int64_t bb = int64_t(kbs) * nsub * B_KB_BYTES;
+    if (wbufs == 0 || (int64_t(stages) * kbs - 1) * a_bytes + A_MMA_BYTES >
+                          int64_t(stages) * kbs * a_bytes + wbufs * bb)
         return cudaErrorNotSupported;
     CUtensorMap mx, mw;
     if (!tmap_2d_bf16(&mx, x, uint64_t(K), uint64_t(M), uint64_t(ldx), BK, uint32_t(a_rows), 128) ||
         !tmap_2d_u8(&mw, wq, uint64_t(eight ? N : N / 2), uint64_t(K), uint64_t(ldq),
-                    uint32_t(eight ? nsub * BN : nsub * BN / 2), uint32_t(BK)))
+                    uint32_t(eight ? nsub * BN : nsub * BN / 2), uint32_t(kbs * BK)))
         return cudaErrorNotSupported;
     GemmArgs a{};
     a.y = y;
@@ -1365,7 +1404,7 @@ cudaError_t launch_qgemm_kn(const DeviceInfo& dev, const void* x, int64_t ldx, c
     a.K = int(K);
     a.a_rows = a_rows;
     a.nsub = nsub;
-    a.kbs = 1;
+    a.kbs = kbs;
     a.blocked = 0;
     a.stages = stages;
     a.w_stream_once = m_tiles == 1 ? 1 : 0;
