@@ -74,10 +74,10 @@ struct Cfg {
     static constexpr int P_BYTES = MAXR * 128;
     static constexpr int RING_OFF = Q_BYTES + 2 * P_BYTES;
     static constexpr int BAR_OFF = RING_OFF + NST * STAGE_BYTES;
-    static constexpr int NBARS = 2 * NST + 16 + 2;      // ring, 8 pairs, q_full, drain
+    static constexpr int NBARS = 2 * NST + 14 + 2;      // ring, 7 pairs, q_full, drain
     static constexpr int XCH_OFF = BAR_OFF + NBARS * 8 + 16;
-    // per item: slice sums and the max; per page (two buffers): the slice maxima
-    static constexpr int XCH_BYTES = 2 * (NSM + 1) * MAXR * 4 + 2 * NSM * MAXR * 4;
+    // per item (two buffers): the slice sums and the max
+    static constexpr int XCH_BYTES = 2 * (NSM + 1) * MAXR * 4;
     static constexpr int EPI_STRIDE = 32 * 4 + 16;      // staged O row: 32 floats + pad
     static constexpr size_t SMEM = 1024 + size_t(XCH_OFF) + XCH_BYTES + MAXR * EPI_STRIDE +
                                    NST * 4 + (MAX_BATCH + 1) * 4 + 2 * MAX_BATCH * 4 +
@@ -123,11 +123,9 @@ attn_partial_kernel(const __grid_constant__ CUtensorMap tmap_k,
     uint64_t* xs_bar = o_empty + 2;    // item k's row sums and max are in x_sum[k&1]
     uint64_t* q_full = xs_bar + 2;
     uint64_t* drain = q_full + 1;
-    uint64_t* xm_bar = drain + 1;      // page g's slice maxima are in x_max[g&1] (all warps)
-    uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(xm_bar + 2);
+    uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(drain + 1);
     float* x_sum = reinterpret_cast<float*>(smem + C::XCH_OFF);  // [2][NSM+1][MAXR]
-    float* x_max = x_sum + 2 * (NSM + 1) * MAXR;                  // [2][NSM][MAXR]
-    uint8_t* epi_stage = reinterpret_cast<uint8_t*>(x_max + 2 * NSM * MAXR);
+    uint8_t* epi_stage = reinterpret_cast<uint8_t*>(x_sum + 2 * (NSM + 1) * MAXR);
     int* stage_valid = reinterpret_cast<int*>(epi_stage + MAXR * C::EPI_STRIDE);
     int* prefix = stage_valid + NST;  // [B+1]
     int* seq_len = prefix + MAX_BATCH + 1;   // per sequence: length, first token, block width
@@ -161,8 +159,6 @@ attn_partial_kernel(const __grid_constant__ CUtensorMap tmap_k,
         }
         mbar_init(q_full, NSM);
         mbar_init(drain, 1);
-        mbar_init(&xm_bar[0], NSM);
-        mbar_init(&xm_bar[1], NSM);
         *abort_flag = 0;
         fence_barrier_init();
     }
@@ -491,12 +487,14 @@ attn_partial_kernel(const __grid_constant__ CUtensorMap tmap_k,
                 const int s = int(gi % NST), sb = int(gi & 1u);
                 const uint32_t par = (gi >> 1) & 1u;
                 const int page0 = c * chunk + i * PAGE;  // first key of the page
-                // this warp's 16 scores of the page, then release the S buffer
+                // the whole page of scores of row r (every lane quarter holds all 64 keys
+                // of the query rows) and this warp's 16-key slice of it, then release the
+                // S buffer
                 if (!wait(&s_full[sb], par)) break;
                 tc_fence_after_sync();
-                uint32_t sv[KSL];
-                tmem_load_32x32b_x16_sync(
-                    tmem_base + lane_base + uint32_t(C::S_COL + sb * PAGE + sw * KSL), sv);
+                uint32_t sa[PAGE], sv[KSL];
+                const uint32_t s_tm = tmem_base + lane_base + uint32_t(C::S_COL + sb * PAGE);
+                tmem_load_x64_x16_sync(s_tm, s_tm + uint32_t(sw * KSL), sa, sv);
                 tc_fence_before_sync();
                 __syncwarp();
                 if (lane == 0) mbar_arrive(&s_empty[sb]);
@@ -507,42 +505,39 @@ attn_partial_kernel(const __grid_constant__ CUtensorMap tmap_k,
                 const bool valid = stage_valid[s] != 0;
 
                 // causal mask (masked keys -> -inf) and the row max over the page, taken on
-                // the raw scores (exact: max does not round, so neither the tree nor the
-                // order of the four slice maxima matters); scaling by the positive
-                // scale_log2 afterwards gives the max of the scaled scores
-                float sl[KSL];
-#pragma unroll
-                for (int k = 0; k < KSL; ++k)
-                    sl[k] = (valid && page0 + sw * KSL + k <= pos) ? __uint_as_float(sv[k])
-                                                                  : -INFINITY;
-                float mt[KSL / 2];
-#pragma unroll
-                for (int k = 0; k < KSL / 2; ++k) mt[k] = fmaxf(sl[k], sl[k + KSL / 2]);
-#pragma unroll
-                for (int width = KSL / 4; width >= 1; width /= 2)
-#pragma unroll
-                    for (int k = 0; k < width; ++k) mt[k] = fmaxf(mt[k], mt[k + width]);
-                // the four warps' slice maxima of row r, through shared memory (buffer
-                // sb is rewritten only for page gi+2, after every warp has passed page
-                // gi+1's exchange and so has read this one)
-                float* xm = x_max + sb * (NSM * MAXR);
-                xm[sw * MAXR + r] = mt[0];
-                __syncwarp();
-                if (lane == 0) mbar_arrive(&xm_bar[sb]);
-                // While the other warps' slice maxima arrive, P is computed against the
-                // current reference max, which the page keeps unless a row raises it (the
-                // common case).  If any row raises, P is computed again below with the new
-                // reference, so the values are exactly those computed after the exchange.
-                float pv[KSL];
+                // the raw scores (exact: max does not round, so neither the tree nor its
+                // grouping matters, and each warp finds the same page max with no exchange);
+                // scaling by the positive scale_log2 afterwards gives the max of the scaled
+                // scores.  A page that every query of the block sees in full needs no mask
+                // for the block's rows; the padding rows past R (zero Q, never stored) then
+                // see it too, which changes nothing in the other rows.
+                float sl[KSL], m_raw;
                 {
-                    const float m_spec = m_ref == -INFINITY ? 0.f : m_ref;
+                    float a[PAGE];
+                    if (valid && page0 + PAGE - 1 <= L - qb) {
 #pragma unroll
-                    for (int k = 0; k < KSL; ++k) pv[k] = ex2(fmaf(sl[k], scale_log2, -m_spec));
+                        for (int k = 0; k < PAGE; ++k) a[k] = __uint_as_float(sa[k]);
+#pragma unroll
+                        for (int k = 0; k < KSL; ++k) sl[k] = __uint_as_float(sv[k]);
+                    } else {
+                        const int lim = valid ? pos - page0 : -1;  // last visible key, or < 0
+#pragma unroll
+                        for (int k = 0; k < PAGE; ++k)
+                            a[k] = k <= lim ? __uint_as_float(sa[k]) : -INFINITY;
+#pragma unroll
+                        for (int k = 0; k < KSL; ++k)
+                            sl[k] = sw * KSL + k <= lim ? __uint_as_float(sv[k]) : -INFINITY;
+                    }
+                    float t1[22], t2[8];
+#pragma unroll
+                    for (int k = 0; k < 21; ++k) t1[k] = fmax3(a[3 * k], a[3 * k + 1], a[3 * k + 2]);
+                    t1[21] = a[63];
+#pragma unroll
+                    for (int k = 0; k < 7; ++k) t2[k] = fmax3(t1[3 * k], t1[3 * k + 1], t1[3 * k + 2]);
+                    t2[7] = t1[21];
+                    m_raw = fmax3(fmax3(t2[0], t2[1], t2[2]), fmax3(t2[3], t2[4], t2[5]),
+                                  fmaxf(t2[6], t2[7]));
                 }
-                if (!wait(&xm_bar[sb], par)) break;
-                float m_raw = xm[r];
-#pragma unroll
-                for (int t = 1; t < NSM; ++t) m_raw = fmaxf(m_raw, xm[t * MAXR + r]);
                 const float m_page = m_raw * scale_log2;
 
                 // reference max: raised (and O, l rescaled) only when the page max exceeds
@@ -554,7 +549,8 @@ attn_partial_kernel(const __grid_constant__ CUtensorMap tmap_k,
                 l_run *= factor;
                 // this warp's 16 keys; a masked key (-inf) gives p = +0
                 // p = exp2(s * scale_log2 - m), the row-slice sum by a fixed pairwise tree
-                if (__any_sync(0xffffffffu, raise)) {
+                float pv[KSL];
+                {
                     const float m_use = m_ref == -INFINITY ? 0.f : m_ref;
 #pragma unroll
                     for (int k = 0; k < KSL; ++k) pv[k] = ex2(fmaf(sl[k], scale_log2, -m_use));
