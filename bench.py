@@ -343,7 +343,7 @@ def run_gpu(args, rank, world, local_rank):
 
     e2e = run_e2e(st, args, dist)
     extra = gemm_vs_cublas(st) if rank == 0 else {}
-    kern = kernel_table(dev) if rank == 0 else {}
+    kern = kernel_table(dev, st) if rank == 0 else {}
     return {"elapsed_ms": elapsed_ms, "reps_ms": reps_ms, "sampled_steps": len(events),
             "per_call_ms": per_call_ms, "clocks": clocks.summary(), "e2e": e2e,
             "cublas": extra, "kernels": kern}
@@ -479,14 +479,17 @@ def graph_time_us(fns, n=64, reps=7):
     return statistics.median(ts)
 
 
-def kernel_table(dev):
+def kernel_table(dev, st=None):
     """The metric's per-kernel half, measured in the same run: the invariant GEMM at
     K = N = 4096 for M = 1, 2, 4, 8 (both W layouts; HBM-bound: GB/s and the fraction of
     the measured HBM copy rate) with cuBLAS (torch.matmul, free to split K) at the same
     shapes and layouts, M = 256 and 2048 (TFLOP/s against the measured bf16 burst peak),
     and RMSNorm [2048, 8192].  Each figure is the per-call device time of 64 back-to-back
     calls in one CUDA graph over rotating weight (or input) sets of 256 MB, more than twice
-    the L2, so every call reads its operands from HBM; median of 7 replays."""
+    the L2, so every call reads its operands from HBM; median of 7 replays.  With the
+    step's buffers `st`: the step's verify call timed the same way (32 calls; its K/V,
+    268 MB, already exceed twice the L2), and the floor of any call timed with a pair of
+    CUDA events: an empty-sized kernel between two events, with the host ahead."""
     import torch
     import invariant_bi_matmul_gb300 as bi
     from invariant_bi_matmul_gb300 import inputs
@@ -532,6 +535,26 @@ def kernel_table(dev):
         t = graph_time_us([lambda a=a, o=o: bi.rmsnorm(a, g, 1e-5, out=o) for a, o in rs])
         out["rmsnorm_B2048_H8192"] = {"us": round(t, 2), "GB/s": round(by / t / 1e3, 1),
                                       "frac_hbm": round(by / t / 1e3 / hbm, 4), "bound": "hbm"}
+        if st is not None:
+            t = graph_time_us([lambda: bi.verify_block(
+                st.q, st.k_cache, st.v_cache, st.block_table, st.seq_lens, st.cu_q,
+                max_q=M_TOK, max_seq_len=LK, scale=st.scale, out=st.o, lse=st.lse,
+                workspace=st.ws)], n=32)
+            by = step_bytes()["verify_block"]
+            out["verify_block"] = {"us": round(t, 2), "GB/s": round(by / t / 1e3, 1),
+                                   "frac_hbm": round(by / t / 1e3 / hbm, 4), "bound": "hbm"}
+            tiny = torch.zeros(1, device=dev)
+            ts = []
+            for _ in range(21):
+                torch.cuda._sleep(200000)  # the GPU busy while the host records ahead
+                s0 = torch.cuda.Event(enable_timing=True)
+                s1 = torch.cuda.Event(enable_timing=True)
+                s0.record()
+                tiny.add_(1.0)
+                s1.record()
+                torch.cuda.synchronize()
+                ts.append(s0.elapsed_time(s1) * 1e3)
+            out["event_pair_floor_us"] = round(statistics.median(ts), 2)
     finally:
         bi.set_batch_invariant_limit(old)
     del wnk, wkn
@@ -768,6 +791,12 @@ def main():
             "frac": round(achieved / hbm, 4), "peak_source": f"{peak_kind} hbm_gbs",
             "traffic": recorded_traffic() if dom == "verify_block" else None,
             "algorithmic_bytes": nbytes[dom]}
+    kv = res["kernels"].get("verify_block") if dom == "verify_block" else None
+    if kv:
+        # the same call back to back in a CUDA graph, and the floor that a pair of events
+        # adds to any single call: context for the event-timed figure above
+        roof["graph_timed"] = {"us": kv["us"], "achieved": kv["GB/s"], "frac": kv["frac_hbm"],
+                               "event_pair_floor_us": res["kernels"].get("event_pair_floor_us")}
     e2e = res["e2e"]
     line = {
         "metric": METRIC, "value": round(value, 1), "unit": "GB/s", "n_gpus": world,
