@@ -89,7 +89,17 @@ constexpr int RING_BYTES = SMEM_BYTES - 1024 /* alignment slack */ - CTRL_BYTES;
 constexpr int KN_ATOM_N = BN < 64 ? BN : 64;
 constexpr int KN_ATOM_BYTES = KN_ATOM_N * 2 * BK;  // one atom column of a K-block
 constexpr int KN_SWIZZLE = KN_ATOM_N * 2;          // 64 or 128 bytes
-constexpr uint32_t KN_LAYOUT = KN_SWIZZLE == 128 ? 2u : 4u;
+// Dense W in layout KN can be staged in atoms of 64 columns (128-byte rows, 128-byte
+// swizzle), so that every TMA row segment is a whole 128-byte line: always for tiles of 64
+// columns or more, and for 32-column tiles when few X rows are staged (the W stream sets
+// the pace there; a 32-column tile then stages the 64-column atom that holds it, twice its
+// own bytes from L2, and its MMA starts 64 bytes into each row).  Otherwise, and for
+// quantized natural-layout W (whose converters write KN_ATOM_N atoms), KN_ATOM_N atoms.
+constexpr int DKN_ATOM_N = 64;
+constexpr int DKN_MAX_ROWS = 32;  // X rows staged at most for the wide atoms of 32-column tiles
+__host__ __device__ constexpr int dkn_cols(int nsub) {  // W columns staged per K-block
+    return nsub * BN > DKN_ATOM_N ? nsub * BN : DKN_ATOM_N;
+}
 // Quantized W in the natural layout: K-blocks per stage for a tile of nsub instruction
 // tiles, so that a converter thread holds at most 8 prefetched scale codes (its pieces
 // per K-block: nsub*BN/16) and a code box spans at most 256 k-rows
@@ -136,6 +146,7 @@ struct GemmArgs {
                        // per row and stage starting at a 16-byte boundary; else the
                        // converters load them from global memory (then kbs = 1)
     int q_srow;        // Q_SROW (one K-block per stage) or Q_SROW_KBS
+    int kn_wide;       // dense layout-KN W staged in 64-column atoms (see DKN_ATOM_N)
 };
 
 // ----------------------------------------------------------- quantized-code decoding
@@ -220,7 +231,13 @@ gemm_kernel(const __grid_constant__ CUtensorMap tmap_x, const __grid_constant__ 
     constexpr int nsub = NSUB;
     const int kbs = args.kbs;
     const int a_bytes = args.a_rows * (BK * 2);   // one X block (one K-block)
-    const int b_bytes = nsub * B_KB_BYTES;        // one W block (one K-block, every sub-tile)
+    // one W block (one K-block, every sub-tile; wide KN atoms: whole 64-column atoms)
+    const bool DKN = KN && !QUANT && args.kn_wide != 0;
+    const int WA_N = DKN ? DKN_ATOM_N : KN_ATOM_N;            // N-major atom columns
+    const int WA_BYTES = WA_N * 2 * BK;                       // one atom of a K-block
+    const int WA_SW = WA_N * 2;                               // its swizzle (bytes)
+    const uint32_t WA_LAYOUT = WA_SW == 128 ? 2u : 4u;
+    const int b_bytes = DKN ? dkn_cols(NSUB) * BK * 2 : nsub * B_KB_BYTES;
     uint8_t* sA = smem;                           // S*kbs X blocks
     uint8_t* sB = smem + S * kbs * a_bytes;       // S*kbs W blocks (QUANT: wbufs W tiles)
     uint8_t* sR = sB + (QUANT ? args.wbufs : S) * kbs * b_bytes;  // QUANT: S code blocks
@@ -358,13 +375,17 @@ gemm_kernel(const __grid_constant__ CUtensorMap tmap_x, const __grid_constant__ 
                         tma_load_2d_s(r_dst + uint32_t(codes_bytes + s_blk), &tmap_b, bar, xs, n0);
                 }
             } else if (KN) {
-                // per swizzle atom (KN_ATOM_N columns) one box of 64*kbs k-rows
-                for (int c = 0; c < tile_n; c += KN_ATOM_N) {
-                    const uint32_t dst = b_dst + uint32_t(c / KN_ATOM_N) * uint32_t(kbs * KN_ATOM_BYTES);
-                    if (w_once)
-                        tma_load_2d_s_hint(dst, &tmap_w, bar, n0 + c, kb * BK, w_policy);
+                // per swizzle atom (WA_N columns) one box of 64*kbs k-rows, from the atom
+                // that holds column n0 (a 32-column tile shares its atom with the next
+                // tile's CTA: no evict-first hint then, so the line waits in L2 for it)
+                const int na = n0 / WA_N * WA_N;
+                const int cols = DKN ? dkn_cols(NSUB) : tile_n;
+                for (int c = 0; c < cols; c += WA_N) {
+                    const uint32_t dst = b_dst + uint32_t(c / WA_N) * uint32_t(kbs * WA_BYTES);
+                    if (w_once && cols == tile_n)
+                        tma_load_2d_s_hint(dst, &tmap_w, bar, na + c, kb * BK, w_policy);
                     else
-                        tma_load_2d_s(dst, &tmap_w, bar, n0 + c, kb * BK);
+                        tma_load_2d_s(dst, &tmap_w, bar, na + c, kb * BK);
                 }
             } else if (blocked) {
                 if (w_once)
@@ -467,18 +488,18 @@ gemm_kernel(const __grid_constant__ CUtensorMap tmap_x, const __grid_constant__ 
             umma_idesc_bf16(m64 ? 64 : BM, NSUB * BN, 0, KN ? 1 : 0, args.f16 != 0);
         // X: K-major, 128-byte swizzle, 8-row groups 1024 B apart; +32 B per k16 step
         const uint64_t a_desc0 = umma_smem_desc(smem_addr(sA), 16, 1024, 2);
-        // W, layout NK: K-major like X.  Layout KN: N-major; k-rows of KN_SWIZZLE bytes,
-        // 8 k-rows per swizzle-atom group, atoms of KN_ATOM_N columns KN_ATOM_BYTES apart;
-        // a k16 step skips 16 k-rows
-        // (KN: a stage holds, per atom of KN_ATOM_N columns, kbs K-blocks of 64 k-rows, so
-        // atoms sit kbs*KN_ATOM_BYTES apart and K-blocks KN_ATOM_BYTES apart)
-        const uint64_t b_desc0 = KN ? umma_smem_desc(smem_addr(sB), uint32_t(kbs * KN_ATOM_BYTES),
-                                                     8 * KN_SWIZZLE, KN_LAYOUT)
+        // W, layout NK: K-major like X.  Layout KN: N-major; k-rows of WA_SW bytes, 8
+        // k-rows per swizzle-atom group, atoms of WA_N columns WA_BYTES apart; a k16 step
+        // skips 16 k-rows
+        // (KN: a stage holds, per atom of WA_N columns, kbs K-blocks of 64 k-rows, so
+        // atoms sit kbs*WA_BYTES apart and K-blocks WA_BYTES apart)
+        const uint64_t b_desc0 = KN ? umma_smem_desc(smem_addr(sB), uint32_t(kbs * WA_BYTES),
+                                                     8 * WA_SW, WA_LAYOUT)
                                     : umma_smem_desc(smem_addr(sB), 16, 1024, 2);
         constexpr int A_K16 = (UK * 2) >> 4;
-        constexpr int B_K16 = KN ? (UK * KN_SWIZZLE) >> 4 : (UK * 2) >> 4;
+        const int B_K16 = KN ? (UK * WA_SW) >> 4 : (UK * 2) >> 4;
         const uint64_t a_step = uint64_t(a_bytes >> 4);
-        const uint64_t b_step = uint64_t((KN ? KN_ATOM_BYTES : b_bytes) >> 4);
+        const uint64_t b_step = uint64_t((KN ? WA_BYTES : b_bytes) >> 4);
         const uint32_t stage_a = uint32_t(kbs * a_bytes), stage_b = uint32_t(kbs * b_bytes);
         const uint32_t empty_s = smem_addr(empty);
         uint32_t stage = 0, phase = 0;
@@ -494,6 +515,8 @@ gemm_kernel(const __grid_constant__ CUtensorMap tmap_x, const __grid_constant__ 
             }
             tc_fence_after_sync();
             const uint32_t d_tmem = tmem_base + uint32_t(acc * ACC_COLS);
+            // dense KN, 32-column tile: its columns start 64 bytes into the atom's rows
+            const uint64_t b_col = DKN ? uint64_t((((t % n_tiles) * tile_n) % WA_N) * 2 >> 4) : 0;
             for (int kb = kb0; kb < kb1; kb += kbs) {
                 if (!mbar_wait_warp(&full[stage], phase, abort_flag, wait_ns) ||
                     (QUANT && !mbar_wait_warp(&conv[wb], wphase, abort_flag, wait_ns))) {
@@ -506,7 +529,8 @@ gemm_kernel(const __grid_constant__ CUtensorMap tmap_x, const __grid_constant__ 
                     // descriptors are advanced by adding (byte offset >> 4) to the start-
                     // address field; shared addresses stay below 2^18 so it never carries
                     uint64_t a_blk = a_desc0 + (uint64_t(stage * stage_a) >> 4);
-                    uint64_t b_blk = b_desc0 + (uint64_t((QUANT ? wb : stage) * stage_b) >> 4);
+                    uint64_t b_blk = b_desc0 + (uint64_t((QUANT ? wb : stage) * stage_b) >> 4) +
+                                     b_col;
                     for (int i = 0; i < nk; ++i, a_blk += a_step, b_blk += b_step) {
                         const uint32_t first = (kb + i) == kb0 ? 1u : 0u;
 #pragma unroll
@@ -1224,6 +1248,8 @@ GemmSchedule gemm_schedule(int64_t M, int64_t N, int64_t K, bool w_kn, int num_s
         }
     }
     if (wide_m) g.a_rows = 2 * BM;
+    g.kn_wide = w_kn && (g.nsub * BN >= DKN_ATOM_N || g.a_rows <= DKN_MAX_ROWS) ? 1 : 0;
+    const int w_kb = g.kn_wide ? dkn_cols(g.nsub) * BK * 2 : g.nsub * B_KB_BYTES;
     // Split-K (non-invariant kernel only): a single M-tile whose instruction tiles leave
     // SMs idle gets a cluster of CTAs per tile, each over a contiguous K range, so more
     // SMs stream W and each runs a shorter chain of dependent MMAs.  The reduction slots
@@ -1236,7 +1262,7 @@ GemmSchedule gemm_schedule(int64_t M, int64_t N, int64_t K, bool w_kn, int num_s
         if (sp > nkb) sp = nkb;
         // the ring keeps room for at least four stages of one K-block
         const int64_t slot = int64_t(g.a_rows) * BN * 4;
-        const int64_t blk1 = int64_t(g.a_rows) * BK * 2 + B_KB_BYTES;
+        const int64_t blk1 = int64_t(g.a_rows) * BK * 2 + w_kb;
         while (sp >= 2 && RING_BYTES - (sp - 1) * slot < 4 * blk1) --sp;
         if (sp >= 2) {
             g.splits = int(sp);
@@ -1245,7 +1271,7 @@ GemmSchedule gemm_schedule(int64_t M, int64_t N, int64_t K, bool w_kn, int num_s
     }
     // as many K-blocks per stage as keep at least four stages in the ring (fewer
     // barrier round trips per MMA) -- and, when split, at least four stages per CTA
-    const int blk_bytes = g.a_rows * BK * 2 + g.nsub * B_KB_BYTES;
+    const int blk_bytes = g.a_rows * BK * 2 + w_kb;
     const int64_t per_cta = (nkb + g.splits - 1) / g.splits;
     g.kbs = 1;
     for (int kbs = w_kn ? MAX_KBS_KN : MAX_KBS; kbs >= 2; kbs >>= 1) {
@@ -1284,8 +1310,9 @@ cudaError_t launch_gemm(const DeviceInfo& dev, const void* x, int64_t ldx, const
     const int64_t a_bytes = int64_t(g.a_rows) * BK * 2;
     const int64_t blocks = int64_t(g.stages) * g.kbs;
     const int64_t a_read = g.a_rows > BM ? a_bytes : A_MMA_BYTES;  // from an X block's start
-    if ((blocks - 1) * a_bytes + a_read > blocks * (a_bytes + int64_t(g.nsub) * B_KB_BYTES) ||
-        blocks * (a_bytes + int64_t(g.nsub) * B_KB_BYTES) > g.ring_bytes || g.stages < 2)
+    const int64_t w_blk = g.kn_wide ? int64_t(dkn_cols(g.nsub)) * BK * 2 : int64_t(g.nsub) * B_KB_BYTES;
+    if ((blocks - 1) * a_bytes + a_read > blocks * (a_bytes + w_blk) ||
+        blocks * (a_bytes + w_blk) > g.ring_bytes || g.stages < 2)
         return cudaErrorNotSupported;
     CUtensorMap mx, mw;
     bool ok;
@@ -1297,8 +1324,9 @@ cudaError_t launch_gemm(const DeviceInfo& dev, const void* x, int64_t ldx, const
                           128, f16);
     if (!ok) return cudaErrorNotSupported;
     if (w_kn)
-        ok = tmap_2d_bf16(&mw, w, uint64_t(N), uint64_t(K), uint64_t(ldw), KN_ATOM_N,
-                          uint32_t(BK * g.kbs), KN_SWIZZLE, f16);
+        ok = tmap_2d_bf16(&mw, w, uint64_t(N), uint64_t(K), uint64_t(ldw),
+                          g.kn_wide ? DKN_ATOM_N : KN_ATOM_N, uint32_t(BK * g.kbs),
+                          g.kn_wide ? DKN_ATOM_N * 2 : KN_SWIZZLE, f16);
     else if (g.blocked)
         ok = tmap_kblocked_bf16(&mw, w, uint64_t(K), uint64_t(N), uint64_t(ldw), BK,
                                 uint32_t(g.nsub * BN), uint32_t(g.kbs), 128, f16);
@@ -1322,6 +1350,7 @@ cudaError_t launch_gemm(const DeviceInfo& dev, const void* x, int64_t ldx, const
     a.splits = g.splits;
     a.kb_per_split = g.kb_per_split;
     a.f16 = f16 ? 1 : 0;
+    a.kn_wide = g.kn_wide;
     if (g.splits > 1)
         return w_kn ? (y_f32 ? launch_split<true, true>(dev, mx, mw, a, g.tiles, stream)
                              : launch_split<true, false>(dev, mx, mw, a, g.tiles, stream))

@@ -118,6 +118,7 @@ struct GemmSchedule {
     int ring_bytes = 0;
     int splits = 1;        // CTAs (one cluster) per output tile, each over a K range
     int kb_per_split = 0;  // 64-wide K-blocks per split
+    int kn_wide = 0;       // layout KN: W staged in 64-column atoms
     int64_t tiles = 0;
 };
 GemmSchedule gemm_schedule(int64_t M, int64_t N, int64_t K, bool w_kn, int num_sms,
