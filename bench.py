@@ -729,7 +729,8 @@ def main():
     ap.add_argument("--sweep", action="store_true")
     ap.add_argument("--case", default=None,
                     help="time one call shape instead of the step (for profiling): "
-                         "gemm:M:N:K[:kn][:fast], attn:B:q:Lk[:fast] or prefill:Lk:new")
+                         "gemm:M:N:K[:kn][:fast], qgemm:M:N:K:format[:kn], "
+                         "attn:B:q:Lk[:fast] or prefill:Lk:new")
     ap.add_argument("--case-reps", type=int, default=5)
     args = ap.parse_args()
     if args.warmup < 3:
@@ -856,6 +857,19 @@ def run_case(spec: str, reps: int):
         desc = {"case": "gemm", "M": M, "N": N, "K": K, "layout": lay,
                 "splits": bi.matmul_splits(M, N, K, lay,
                                            torch.cuda.get_device_properties(dev).multi_processor_count)}
+    elif parts[0] == "qgemm":
+        M, N, K = (int(v) for v in parts[1:4])
+        fmt = parts[4]
+        lay = "kn" if "kn" in parts[5:] else "nk"
+        gs = {"mxfp4": 32, "nvfp4": 16, "mxfp8": 32, "affine4": 64, "affine8": 32}[fmt]
+        wq, sc, bq = (inputs.quant_weights(inputs.Q_NAMES[fmt], N, K, gs, seed=5) if lay == "nk"
+                      else inputs.quant_weights(inputs.Q_NAMES[fmt], K, N, gs, seed=5))
+        wq, sc = wq.to(dev), sc.to(dev)
+        bq = bq.to(dev) if bq is not None else None
+        x = inputs.normal_bf16((M, K), seed=2).to(dev)
+        y = torch.empty(M, N, dtype=torch.bfloat16, device=dev)
+        fn = lambda: bi.qmatmul(x, wq, sc, fmt, gs, K, biases=bq, out=y, layout=lay, N=N)  # noqa: E731
+        desc = {"case": "qgemm", "M": M, "N": N, "K": K, "format": fmt, "layout": lay}
     elif parts[0] == "attn":
         B, q, L = (int(v) for v in parts[1:4])
         p = inputs.paged_inputs([L] * B, [q] * B, Hq=HQ, Hkv=HKV, D=HEAD_DIM, seed=4, device=dev)

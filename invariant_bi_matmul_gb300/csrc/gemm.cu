@@ -71,11 +71,20 @@ constexpr int MAX_STAGES = 48;
 constexpr int MAX_SPLITS = 8;               // split-K cluster size (portable maximum)
 constexpr int THREADS = 192;
 constexpr int EPI_THREADS = 128;
-// Quantized W: eight more warps (6..13) turn the packed codes of each stage into bf16
-// operand tiles.  The ring (at most MAX_QSTAGES stages, one K-block each) holds X blocks
-// and packed codes only; the bf16 tiles live in a separate ring of MAX_QWBUF buffers.
-constexpr int QTHREADS = THREADS + 256;
+// Quantized W: eight (or sixteen, see conv_warps) more warps from warp 6 on turn the
+// packed codes of each stage into bf16 operand tiles.  The ring (at most MAX_QSTAGES
+// stages) holds X blocks and packed codes only; the bf16 tiles live in a separate ring of
+// MAX_QWBUF buffers.
 constexpr int CONV_WARPS = 8;
+// Converter warps of a QUANT kernel: sixteen (two groups of eight, each group's two halves
+// taking alternate K-blocks of a stage) for transposed-layout W in 32-column tiles (small
+// M: the conversion sets the pace and the registers allow 704 threads), else eight.
+__host__ __device__ constexpr int conv_warps(bool kn, int nsub) {
+    return !kn && nsub == 1 ? 2 * CONV_WARPS : CONV_WARPS;
+}
+__host__ __device__ constexpr int gemm_threads(bool quant, bool kn, int nsub) {
+    return quant ? THREADS + 32 * conv_warps(kn, nsub) : THREADS;
+}
 constexpr int MAX_QSTAGES = 16;
 constexpr int MAX_QWBUF = 4;
 constexpr int Q_SROW = 16;     // bytes of staged scales (or biases) per tile row, one K-block
@@ -220,7 +229,7 @@ __device__ __forceinline__ float byte_to_f32(uint32_t word, uint32_t byte_sel) {
 }
 
 template <bool KN, bool F32OUT, int NSUB, bool SPLIT, int MSUB, bool QUANT>
-__global__ void __launch_bounds__(QUANT ? QTHREADS : THREADS, 1)
+__global__ void __launch_bounds__(gemm_threads(QUANT, KN, NSUB), 1)
 gemm_kernel(const __grid_constant__ CUtensorMap tmap_x, const __grid_constant__ CUtensorMap tmap_w,
             const __grid_constant__ CUtensorMap tmap_s, const __grid_constant__ CUtensorMap tmap_b,
             const GemmArgs args, unsigned int* err) {
@@ -294,7 +303,7 @@ gemm_kernel(const __grid_constant__ CUtensorMap tmap_x, const __grid_constant__ 
         }
         if (QUANT) {
             for (int b = 0; b < args.wbufs; ++b) {
-                mbar_init(&conv[b], CONV_WARPS / 2);  // the four warps of a group
+                mbar_init(&conv[b], conv_warps(KN, NSUB) / 2);  // the warps of a group
                 mbar_init(&wfree[b], 1);
             }
         }
@@ -903,13 +912,18 @@ gemm_kernel(const __grid_constant__ CUtensorMap tmap_x, const __grid_constant__ 
         // columns past K become zeros.
         constexpr int PARTS = NSUB * BN >= 64 ? 2 : 4;        // threads per tile row
         constexpr int QR = NSUB * BN >= 64 ? NSUB * BN / 64 : 1;  // rows per thread
-        const int cgrp = (warp - 6) >> 2;
+        // a group of GW warps: GW / 4 sets of four, set `sub` taking the stage's K-blocks
+        // ki with ki mod SUBS == sub (each set covers every row and part of a K-block)
+        constexpr int GW = conv_warps(KN, NSUB) / 2, SUBS = GW / 4;
+        const int cgrp = (warp - 6) / GW;
+        const int sub = ((warp - 6) % GW) >> 2;
+        const int w4 = (warp - 6) & 3;
         // the part: for quarters, lane ct of the group's warp w takes quarter (w + ct) mod 4,
         // so a warp's lanes read four different 8-byte columns of their rows (the rows of a
         // code stage are a multiple of 128 bytes apart: one column would put every lane on
         // the same banks) and the four warps still cover every (row, quarter) once
-        const int half = PARTS == 2 ? ((warp - 6) >> 1) & 1 : ((warp - 6) + lane) & 3;
-        const int ct = PARTS == 2 ? ((warp - 6) & 1) * 32 + lane : lane;
+        const int half = PARTS == 2 ? (w4 >> 1) & 1 : (w4 + lane) & 3;
+        const int ct = PARTS == 2 ? (w4 & 1) * 32 + lane : lane;
         const uint8_t* qs8 = static_cast<const uint8_t*>(args.qscales);
         const uint16_t* qs16 = static_cast<const uint16_t*>(args.qscales);
         const int nkb_t = kb1 - kb0;
@@ -977,7 +991,7 @@ gemm_kernel(const __grid_constant__ CUtensorMap tmap_x, const __grid_constant__ 
                 // stage's first group
                 const int xs = ((kbf * BK) >> gsh) & ~(s_epb - 1);
 #pragma unroll 1
-                for (int ki = 0; ki < nk; ++ki) {  // the stage's K-blocks
+                for (int ki = sub; ki < nk; ki += SUBS) {  // the stage's K-blocks (this set's)
                 const int kb = kbf + ki;
                 uint8_t* wt = sB + (wb * kbs + ki) * b_bytes;
                 if (staged) {  // this K-block's scales (and biases) from shared memory
@@ -1193,8 +1207,8 @@ cudaError_t launch_q(const DeviceInfo& dev, const CUtensorMap& mx, const CUtenso
         if (e != cudaSuccess) return e;
         attr_done[dev.device] = true;
     }
-    return launch_pdl(kern, dim3(grid), dim3(QTHREADS), SMEM_BYTES, s, mx, mw, ms, mb, a,
-                      dev.err_word);
+    return launch_pdl(kern, dim3(grid), dim3(gemm_threads(true, KN, NSUB)), SMEM_BYTES, s, mx,
+                      mw, ms, mb, a, dev.err_word);
 }
 
 template <bool KN, bool F32OUT>
