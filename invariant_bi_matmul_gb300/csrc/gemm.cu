@@ -436,10 +436,13 @@ gemm_kernel(const __grid_constant__ CUtensorMap tmap_x, const __grid_constant__ 
         // previous kernel's tail.  Without it the wait comes first (the previous grid may
         // have written W) and the same copies are simply the ring's first.
         if (!args.w_early) pdl_wait();
+        // At most two stages of W go out before X: the SM's TMA unit serves copies in
+        // order, so the first X block would otherwise queue behind the whole ring of W
+        const int EARLY_W = S < 2 ? S : 2;
         int early = 0;  // stages of the first tile whose W is already issued
         if (first_tile < num_tiles) {
             const int n0 = (first_tile % n_tiles) * tile_n;
-            for (int kb = kb0; kb < kb1 && early < S; kb += kbs, ++early) {
+            for (int kb = kb0; kb < kb1 && early < EARLY_W; kb += kbs, ++early) {
                 const int nk = kb1 - kb < kbs ? kb1 - kb : kbs;
                 if (elect_one()) {
                     mbar_arrive_expect_tx_s(full_s + uint32_t(early) * 8u, stage_tx(nk));
