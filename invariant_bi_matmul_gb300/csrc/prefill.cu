@@ -68,7 +68,9 @@ struct PCfg {
         1024 + size_t(MISC_OFF) + size_t(NST + (P_MAX_BATCH + 1) + 3 * P_MAX_BATCH + 4) * 4;
     static constexpr int S_COL = 0;                       // S buffers: columns [0,64), [64,128)
     static constexpr int O_COL = 2 * PAGE;                // O buffers (by item): D columns each
-    static_assert(O_COL + 2 * D <= P_TMEM_COLS, "tensor memory columns");
+    // P buffers (by page): 128 rows x 64 keys of bf16, two keys per 32-bit column
+    static constexpr int P_TCOL = O_COL + 2 * D;
+    static_assert(P_TCOL + 2 * (PAGE / 2) <= P_TMEM_COLS, "tensor memory columns");
     static_assert(RING_OFF % 1024 == 0 && BAR_OFF % 1024 == 0, "1024-byte aligned buffers");
     static_assert(SMEM <= 232448, "shared memory per CTA");
 };
@@ -90,7 +92,6 @@ attn_prefill_kernel(const __grid_constant__ CUtensorMap tmap_k,
     uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) &
                                                ~uintptr_t(1023));
     uint8_t* sQ = smem;
-    uint8_t* sP = smem + C::Q_BYTES;                     // two P buffers
     uint8_t* sStage = smem + C::RING_OFF;
     uint64_t* full = reinterpret_cast<uint64_t*>(smem + C::BAR_OFF);
     uint64_t* empty = full + NST;
@@ -302,7 +303,6 @@ attn_prefill_kernel(const __grid_constant__ CUtensorMap tmap_k,
         constexpr uint32_t idesc_s = umma_idesc_bf16(128, PAGE, 0, 0);  // K K-major
         constexpr uint32_t idesc_pv = umma_idesc_bf16(128, D, 0, 1);    // V N-major
         const uint64_t q_desc0 = umma_smem_desc(smem_addr(sQ), 16, 1024, 2);
-        const uint64_t p_desc0 = umma_smem_desc(smem_addr(sP), 16, 1024, 2);
         const uint64_t k_desc0 = umma_smem_desc(smem_addr(sStage), 16, 1024, 2);
         const uint64_t v_desc0 =
             umma_smem_desc(smem_addr(sStage + C::PAGE_BYTES), C::BOX_BYTES, 1024, 2);
@@ -313,13 +313,13 @@ attn_prefill_kernel(const __grid_constant__ CUtensorMap tmap_k,
             if (first && !wait(&o_empty[ob], (uint32_t(item >> 1) & 1u) ^ 1u)) return;
             tc_fence_after_sync();
             if (elect_one()) {
-                const uint64_t p_desc = p_desc0 + uint64_t((pb * C::P_BYTES) >> 4);
+                const uint32_t p_tmem = tmem_base + uint32_t(C::P_TCOL + pb * (PAGE / 2));
                 const uint64_t v_desc = v_desc0 + uint64_t((s * C::STAGE_BYTES) >> 4);
                 const uint32_t o_tmem = tmem_base + uint32_t(C::O_COL + ob * D);
 #pragma unroll
-                for (int kk = 0; kk < PAGE / 16; ++kk)  // keys 16kk..: +32 B in P, +2 KB in V
-                    tc_mma_bf16(o_tmem, p_desc + uint64_t(kk * 2), v_desc + uint64_t(kk * 128),
-                                idesc_pv, (first && kk == 0) ? 0u : 1u);
+                for (int kk = 0; kk < PAGE / 16; ++kk)  // keys 16kk..: +8 columns of P, +2 KB in V
+                    tc_mma_bf16_ts(o_tmem, p_tmem + uint32_t(kk * 8), v_desc + uint64_t(kk * 128),
+                                   idesc_pv, (first && kk == 0) ? 0u : 1u);
                 tc_commit(&p_empty[pb]);
                 tc_commit(&empty[s]);   // K and V of the page are no longer read
                 if (last) tc_commit(&o_full[ob]);
@@ -500,6 +500,7 @@ attn_prefill_kernel(const __grid_constant__ CUtensorMap tmap_k,
 #pragma unroll
                 for (int q4 = 0; q4 < 4; ++q4) l_run[q4] *= factor;
                 if (!wait(&p_empty[sb], par ^ 1u)) break;
+                tc_fence_after_sync();  // P V of page gi-2 read this P buffer: now rewritten
                 if (i > 0 && __any_sync(0xffffffffu, raise)) {
                     // this quarter's O rows *= factor once P V of page gi-1 has completed
                     const uint32_t gp = gi - 1u;
@@ -519,26 +520,26 @@ attn_prefill_kernel(const __grid_constant__ CUtensorMap tmap_k,
                     tc_fence_before_sync();
                 }
                 const float m_use = m_ref == -INFINITY ? 0.f : m_ref;
-                uint8_t* prow = sP + sb * C::P_BYTES;
+                uint32_t pk[PAGE / 2];  // row r of P, two keys per word
 #pragma unroll
                 for (int q4 = 0; q4 < 4; ++q4) {  // 16-key slice q4
                     float pv[16];
 #pragma unroll
                     for (int kk = 0; kk < 16; ++kk)
                         pv[kk] = ex2(fmaf(sl[16 * q4 + kk], scale_log2, -m_use));
-                    uint32_t pk[8];
 #pragma unroll
-                    for (int kk = 0; kk < 16; kk += 2) pk[kk / 2] = pack_bf16x2(pv[kk], pv[kk + 1]);
+                    for (int kk = 0; kk < 16; kk += 2)
+                        pk[8 * q4 + kk / 2] = pack_bf16x2(pv[kk], pv[kk + 1]);
 #pragma unroll
                     for (int width = 8; width >= 1; width /= 2)
 #pragma unroll
                         for (int kk = 0; kk < width; ++kk) pv[kk] = pv[kk] + pv[kk + width];
                     l_run[q4] = l_run[q4] + pv[0];
-                    *reinterpret_cast<uint4*>(prow + swz(r, 2 * q4)) =
-                        make_uint4(pk[0], pk[1], pk[2], pk[3]);
-                    *reinterpret_cast<uint4*>(prow + swz(r, 2 * q4 + 1)) =
-                        make_uint4(pk[4], pk[5], pk[6], pk[7]);
                 }
+                // P into this quarter's lanes of the page's P buffer in tensor memory (the
+                // P V MMA reads it from there)
+                tmem_store_32x32b_x32_sync(
+                    tmem_base + lane_base + uint32_t(C::P_TCOL + sb * (PAGE / 2)), pk);
                 // V rows of this warp's 16 keys past the sequence end (or of an invalid
                 // page) are zeroed so unwritten cache slots cannot inject NaN/Inf via 0 * v
                 const int vend = valid ? L - page0 : 0;
@@ -552,7 +553,8 @@ attn_prefill_kernel(const __grid_constant__ CUtensorMap tmap_k,
                             make_uint4(0, 0, 0, 0);
                     }
                 }
-                fence_proxy_async_smem();
+                fence_proxy_async_smem();  // the zeroed V rows, read by the MMA
+                tc_fence_before_sync();    // the P stores, before the arrival
                 __syncwarp();
                 if (lane == 0) mbar_arrive(&p_full[sb]);
             }
