@@ -141,8 +141,12 @@ attn_partial_kernel(const __grid_constant__ CUtensorMap tmap_k,
         tmem_alloc(tmem_slot, TMEM_COLS);
         tmem_relinquish();
     }
-    pdl_wait();
-    pdl_trigger();
+    // No griddepcontrol.wait here.  The grid right before this one is always the call's
+    // own counter reset, which waits for its predecessors before it lets this grid launch:
+    // every kernel that wrote an input (Q, the cache, the block table, the lengths) or
+    // last read the workspace has completed by now.  Only the item counters the reset
+    // zeroes are not yet safe; the epilogue warp waits for the reset grid before its first
+    // count, and triggers the merge's launch after that wait.
     if (tid == 0) {
         for (int i = 0; i < NST; ++i) {
             mbar_init(&full[i], 1);
@@ -244,13 +248,21 @@ attn_partial_kernel(const __grid_constant__ CUtensorMap tmap_k,
             int b, c, h;
             decode(w, b, c, h);
             const int npages = pages_of(seq_of(b), c);
+            int phys_l = -1;  // lane k: the physical page of page (i & ~31) + k of the item
             for (int i = 0; i < npages; ++i, ++g) {
+                // the item's block-table entries are read 32 at a time, one per lane, before
+                // the wait for a free stage: one load latency per item at the ring's start
+                // instead of one per page
+                if ((i & 31) == 0) {
+                    const int pidx = c * chunk_pages + i + lane;
+                    phys_l = (i + lane < npages && pidx < max_pages)
+                                 ? block_table[int64_t(b) * max_pages + pidx]
+                                 : -1;
+                }
                 const int s = int(g % NST);
                 if (!wait(&empty[s], ((g / NST) & 1u) ^ 1u)) break;
+                const int phys = __shfl_sync(0xffffffffu, phys_l, i & 31);
                 if (elect_one()) {
-                    const int pidx = c * chunk_pages + i;
-                    const int phys =
-                        pidx < max_pages ? block_table[int64_t(b) * max_pages + pidx] : -1;
                     const bool valid = phys >= 0 && phys < num_pages;
                     stage_valid[s] = valid ? 1 : 0;
                     if (valid) {
@@ -376,6 +388,7 @@ attn_partial_kernel(const __grid_constant__ CUtensorMap tmap_k,
         // softmax warps move on to the next item meanwhile.
         const int r = lane;
         int item = 0;
+        bool reset_done = false;  // griddepcontrol.wait passed (the counters are zeroed)
         for (int w = blockIdx.x; ok && w < total; w += gridDim.x, ++item) {
             int b, c, h;
             decode(w, b, c, h);
@@ -425,9 +438,20 @@ attn_partial_kernel(const __grid_constant__ CUtensorMap tmap_k,
             // the merge waits on (every lane's stores are ordered before the count)
             __threadfence();
             __syncwarp();
+            if (!reset_done) {
+                pdl_wait();
+                pdl_trigger();
+                reset_done = true;
+            }
             if (lane == 0) atomicAdd(cnt + b * Hkv + h, 1u);
         }
         if (!ok && lane == 0) give_up();
+        // a CTA with no item (or one that gave up) still waits before it completes, so the
+        // merge grid never launches ahead of the reset
+        if (!reset_done) {
+            pdl_wait();
+            pdl_trigger();
+        }
     } else if (warp < NSM) {
         // ------------------------------------------------------------------- softmax
         // Warp sw (0..3) reads tensor-memory lanes 32sw .. 32sw+31, which hold a copy of
