@@ -30,7 +30,10 @@
 // warps, one per quarter, write the partials.
 //
 // Warps: 0..3 softmax, 4..7 epilogue (quarter = warp mod 4), 8 TMA producer of K/V pages,
-// 9 MMA issuer (and TMEM owner; it also copies each item's Q tile by TMA).  Work items
+// 9 S issuer (and TMEM owner; it also copies each item's Q tile by TMA), 10 P V issuer.
+// The two issuers run apart, so the scores of later pages are never queued behind a P V
+// that waits for its P, and P has four tensor-memory buffers, so the softmax of page g
+// waits only for the P V of page g-4.  Work items
 // (sequence, query tile, KV head, chunk), chunk fastest, are dealt to CTAs in contiguous
 // runs so that consecutive items share the Q tile.
 #include "attn_common.cuh"
@@ -40,26 +43,28 @@ namespace {
 
 constexpr int P_NSM = 4;                 // softmax warps
 constexpr int P_EPI = 4;                 // first epilogue warp (quarters 0..3)
-constexpr int P_PRODUCER = 8, P_MMA = 9;
-constexpr int P_THREADS = 10 * 32;
+constexpr int P_PRODUCER = 8, P_MMA = 9, P_PV = 10;
+constexpr int P_THREADS = 11 * 32;
+constexpr int P_NPB = 4;                 // P buffers in tensor memory (by page)
+static_assert(PAGE == 64, "the page max below is a three-input max tree over 64 keys");
 constexpr int P_ROWS = 128;              // query rows per tile, one per TMEM lane
 constexpr int P_TMEM_COLS = 512;
 constexpr int P_MAX_BATCH = BI_ATTN_MAX_BATCH;
 
 template <int D>
 struct PCfg {
-    static constexpr int NST = D == 64 ? 8 : 4;          // page stages in the ring
+    static constexpr int NST = D == 64 ? 8 : 5;          // page stages in the ring
     static constexpr int BOXES = D / 64;                 // 64-element (128 B) column boxes
     static constexpr int BOX_BYTES = PAGE * 128;         // one box of a page: 64 rows x 128 B
     static constexpr int PAGE_BYTES = BOXES * BOX_BYTES;
     static constexpr int STAGE_BYTES = 2 * PAGE_BYTES;   // K page + V page
     static constexpr int QBOX_BYTES = P_ROWS * 128;
     static constexpr int Q_BYTES = BOXES * QBOX_BYTES;
-    static constexpr int P_BYTES = P_ROWS * 128;         // 128 rows x 64 keys, bf16
-    static constexpr int RING_OFF = Q_BYTES + 2 * P_BYTES;
+    static constexpr int RING_OFF = Q_BYTES;             // (P lives in tensor memory)
     static constexpr int BAR_OFF = RING_OFF + NST * STAGE_BYTES;
-    // ring (2 NST), seven pairs (s, p, o full / empty and xs), q_full, q_free, drain
-    static constexpr int NBARS = 2 * NST + 17;
+    // ring (2 NST), s / o full and empty pairs, p full / empty per P buffer, the xs pair,
+    // q_full, q_free, and one drain per issuer
+    static constexpr int NBARS = 2 * NST + 4 + 2 * P_NPB + 4 + 2 + 4;
     // the barriers, then the tensor-memory address slot (8 bytes), then the (m, l) rows
     static constexpr int XS_OFF = (BAR_OFF + NBARS * 8 + 8 + 15) / 16 * 16;
     static constexpr int XS_BYTES = 2 * P_ROWS * 8;       // per O buffer: (m, l) per row
@@ -70,7 +75,7 @@ struct PCfg {
     static constexpr int O_COL = 2 * PAGE;                // O buffers (by item): D columns each
     // P buffers (by page): 128 rows x 64 keys of bf16, two keys per 32-bit column
     static constexpr int P_TCOL = O_COL + 2 * D;
-    static_assert(P_TCOL + 2 * (PAGE / 2) <= P_TMEM_COLS, "tensor memory columns");
+    static_assert(P_TCOL + P_NPB * (PAGE / 2) <= P_TMEM_COLS, "tensor memory columns");
     static_assert(RING_OFF % 1024 == 0 && BAR_OFF % 1024 == 0, "1024-byte aligned buffers");
     static_assert(SMEM <= 232448, "shared memory per CTA");
 };
@@ -97,16 +102,17 @@ attn_prefill_kernel(const __grid_constant__ CUtensorMap tmap_k,
     uint64_t* empty = full + NST;
     uint64_t* s_full = empty + NST;    // scores of page g in S buffer g&1
     uint64_t* s_empty = s_full + 2;    // ... read by the four softmax warps
-    uint64_t* p_full = s_empty + 2;    // P of page g in P buffer g&1 (four softmax warps)
-    uint64_t* p_empty = p_full + 2;    // P V of page g has completed (MMA commit)
-    uint64_t* o_full = p_empty + 2;    // item k's O (buffer k&1) is complete (MMA commit)
+    uint64_t* p_full = s_empty + 2;    // P of page g in P buffer g%4 (four softmax warps)
+    uint64_t* p_empty = p_full + P_NPB;  // P V of page g has completed (MMA commit)
+    uint64_t* o_full = p_empty + P_NPB;  // item k's O (buffer k&1) is complete (MMA commit)
     uint64_t* o_empty = o_full + 2;    // ... and read out by the four epilogue warps
     uint64_t* xs_bar = o_empty + 2;    // item k's (m, l) per row are in xs[k&1]
     uint64_t* q_full = xs_bar + 2;     // the Q tile has landed (TMA)
     uint64_t* q_free = q_full + 1;     // every MMA reading the previous Q tile is done
-    uint64_t* drain = q_free + 1;
-    uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(drain + 1);
-    static_assert(C::XS_OFF >= C::BAR_OFF + (2 * NST + 17) * 8 + 8, "barriers overlap xs");
+    uint64_t* drain = q_free + 1;      // [2]: S issuer, P V issuer
+    uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(drain + 2);
+    static_assert(C::XS_OFF >= C::BAR_OFF + (2 * NST + 4 + 2 * P_NPB + 4 + 2 + 4) * 8 + 8,
+                  "barriers overlap xs");
     float2* xs = reinterpret_cast<float2*>(smem + C::XS_OFF);  // [2][P_ROWS]
     int* stage_valid = reinterpret_cast<int*>(smem + C::MISC_OFF);
     int* prefix = stage_valid + NST;            // [B+1] items before sequence b
@@ -131,18 +137,21 @@ attn_prefill_kernel(const __grid_constant__ CUtensorMap tmap_k,
             mbar_init(&full[i], 1);
             mbar_init(&empty[i], 1);   // released by the MMA warp's commit after P V
         }
+        for (int i = 0; i < P_NPB; ++i) {
+            mbar_init(&p_full[i], P_NSM);
+            mbar_init(&p_empty[i], 1);
+        }
         for (int i = 0; i < 2; ++i) {
             mbar_init(&s_full[i], 1);
             mbar_init(&s_empty[i], P_NSM);
-            mbar_init(&p_full[i], P_NSM);
-            mbar_init(&p_empty[i], 1);
             mbar_init(&o_full[i], 1);
             mbar_init(&o_empty[i], 4);
             mbar_init(&xs_bar[i], P_NSM);
         }
         mbar_init(q_full, 1);
         mbar_init(q_free, 1);
-        mbar_init(drain, 1);
+        mbar_init(&drain[0], 1);
+        mbar_init(&drain[1], 1);
         *abort_flag = 0;
         fence_barrier_init();
     }
@@ -296,47 +305,19 @@ attn_prefill_kernel(const __grid_constant__ CUtensorMap tmap_k,
             }
         }
     } else if (warp == P_MMA) {
-        // ---------------------------------------------------------------- MMA issuer
-        // S(page) = Q K^T into S buffer (page & 1); O(item) += P V two pages behind S, as in
-        // the decode kernel.  At each new Q tile: the MMAs that read the old tile complete,
-        // then this warp copies the new one.
+        // ----------------------------------------------------------------- S issuer
+        // S(page) = Q K^T into S buffer (page & 1), as soon as the page has landed and the
+        // softmax has read the buffer's previous scores.  At each new Q tile: the S MMAs
+        // that read the old tile (the only readers of Q) complete, then this warp copies
+        // the new one.
         constexpr uint32_t idesc_s = umma_idesc_bf16(128, PAGE, 0, 0);  // K K-major
-        constexpr uint32_t idesc_pv = umma_idesc_bf16(128, D, 0, 1);    // V N-major
         const uint64_t q_desc0 = umma_smem_desc(smem_addr(sQ), 16, 1024, 2);
         const uint64_t k_desc0 = umma_smem_desc(smem_addr(sStage), 16, 1024, 2);
-        const uint64_t v_desc0 =
-            umma_smem_desc(smem_addr(sStage + C::PAGE_BYTES), C::BOX_BYTES, 1024, 2);
         if (lane == 0) tma_prefetch_desc(&tmap_q);
-        auto issue_pv = [&](uint32_t gj, int item, bool first, bool last) {
-            const int s = int(gj % NST), pb = int(gj & 1u), ob = item & 1;
-            if (!wait(&p_full[pb], (gj >> 1) & 1u)) return;
-            if (first && !wait(&o_empty[ob], (uint32_t(item >> 1) & 1u) ^ 1u)) return;
-            tc_fence_after_sync();
-            if (elect_one()) {
-                const uint32_t p_tmem = tmem_base + uint32_t(C::P_TCOL + pb * (PAGE / 2));
-                const uint64_t v_desc = v_desc0 + uint64_t((s * C::STAGE_BYTES) >> 4);
-                const uint32_t o_tmem = tmem_base + uint32_t(C::O_COL + ob * D);
-#pragma unroll
-                for (int kk = 0; kk < PAGE / 16; ++kk)  // keys 16kk..: +8 columns of P, +2 KB in V
-                    tc_mma_bf16_ts(o_tmem, p_tmem + uint32_t(kk * 8), v_desc + uint64_t(kk * 128),
-                                   idesc_pv, (first && kk == 0) ? 0u : 1u);
-                tc_commit(&p_empty[pb]);
-                tc_commit(&empty[s]);   // K and V of the page are no longer read
-                if (last) tc_commit(&o_full[ob]);
-            }
-            __syncwarp();
-        };
         uint32_t g = 0, qgen = 0;
         bool q_in_flight = false;
-        int item = 0;
-        struct Pend {
-            int item;
-            bool first, last;
-        };
-        Pend pa{0, false, false}, pb{0, false, false};
-        int npend = 0;
         Cursor k = seek(w_begin);
-        for (int w = w_begin; ok && w < w_end; ++w, advance(k), ++item) {
+        for (int w = w_begin; ok && w < w_end; ++w, advance(k)) {
             const int npages = item_pages(k);
             if (w == w_begin || k.c == 0) {
                 // a new Q tile: rows r = token (r / G) of the tile x head r mod G
@@ -378,29 +359,59 @@ attn_prefill_kernel(const __grid_constant__ CUtensorMap tmap_k,
                     tc_commit(&s_full[sb]);
                 }
                 __syncwarp();
-                if (npend == 2) {
-                    issue_pv(gi - 2u, pa.item, pa.first, pa.last);
-                    pa = pb;
-                    --npend;
-                }
-                if (!ok) break;
-                const Pend cur{item, i == 0, i == npages - 1};
-                if (npend == 0) pa = cur; else pb = cur;
-                ++npend;
             }
             g += uint32_t(npages);
         }
-        if (ok && npend >= 1) issue_pv(g - uint32_t(npend), pa.item, pa.first, pa.last);
-        if (ok && npend == 2) issue_pv(g - 1u, pb.item, pb.first, pb.last);
         if (!ok) {
             if (lane == 0) give_up();
             // a Q copy still in flight lands before the CTA exits (bounded)
             if (q_in_flight) mbar_wait(q_full, qgen & 1u, nullptr, 100000000ull);
         }
         // every MMA this warp issued completes before tensor memory is released
-        if (elect_one()) tc_commit(drain);
+        if (elect_one()) tc_commit(&drain[0]);
         __syncwarp();
-        mbar_wait(drain, 0, nullptr, 100000000ull);
+        mbar_wait(&drain[0], 0, nullptr, 100000000ull);
+    } else if (warp == P_PV) {
+        // --------------------------------------------------------------- P V issuer
+        // O(item) += P V of each page once the softmax has written its P (buffer page % 4).
+        // The page's S completed before the softmax read it, so this warp's commit after
+        // P V marks the whole stage free.
+        constexpr uint32_t idesc_pv = umma_idesc_bf16(128, D, 0, 1);    // V N-major
+        const uint64_t v_desc0 =
+            umma_smem_desc(smem_addr(sStage + C::PAGE_BYTES), C::BOX_BYTES, 1024, 2);
+        uint32_t g = 0;
+        int item = 0;
+        Cursor k = seek(w_begin);
+        for (int w = w_begin; ok && w < w_end; ++w, advance(k), ++item) {
+            const int npages = item_pages(k);
+            const int ob = item & 1;
+            for (int i = 0; i < npages; ++i) {
+                const uint32_t gi = g + uint32_t(i);
+                const int s = int(gi % NST), pb = int(gi % P_NPB);
+                if (!wait(&p_full[pb], (gi / P_NPB) & 1u)) break;
+                // the O buffer of this item was read out for item-2
+                if (i == 0 && !wait(&o_empty[ob], (uint32_t(item >> 1) & 1u) ^ 1u)) break;
+                tc_fence_after_sync();
+                if (elect_one()) {
+                    const uint32_t p_tmem = tmem_base + uint32_t(C::P_TCOL + pb * (PAGE / 2));
+                    const uint64_t v_desc = v_desc0 + uint64_t((s * C::STAGE_BYTES) >> 4);
+                    const uint32_t o_tmem = tmem_base + uint32_t(C::O_COL + ob * D);
+#pragma unroll
+                    for (int kk = 0; kk < PAGE / 16; ++kk)  // keys 16kk..: +8 columns of P, +2 KB in V
+                        tc_mma_bf16_ts(o_tmem, p_tmem + uint32_t(kk * 8), v_desc + uint64_t(kk * 128),
+                                       idesc_pv, (i == 0 && kk == 0) ? 0u : 1u);
+                    tc_commit(&p_empty[pb]);
+                    tc_commit(&empty[s]);   // K and V of the page are no longer read
+                    if (i == npages - 1) tc_commit(&o_full[ob]);
+                }
+                __syncwarp();
+            }
+            g += uint32_t(npages);
+        }
+        if (!ok && lane == 0) give_up();
+        if (elect_one()) tc_commit(&drain[1]);
+        __syncwarp();
+        mbar_wait(&drain[1], 0, nullptr, 100000000ull);
     } else if (warp >= P_EPI) {
         // ------------------------------------------------------------------ epilogue
         // Quarter e = warp mod 4: rows 32e..32e+31 of item k's O (buffer k&1), written
@@ -484,14 +495,22 @@ attn_prefill_kernel(const __grid_constant__ CUtensorMap tmap_k,
                     for (int kk = 0; kk < PAGE; ++kk)
                         sl[kk] = (valid && page0 + kk <= pos) ? __uint_as_float(sv[kk]) : -INFINITY;
                 }
-                // the exact row max of the page (max does not round: any order)
-                float mt[PAGE / 2];
+                // the exact row max of the page (max does not round: any order), by
+                // three-input maxima: 31 instructions instead of 63
+                float mt[1];
+                {
+                    float t1[22], t2[8];
 #pragma unroll
-                for (int kk = 0; kk < PAGE / 2; ++kk) mt[kk] = fmaxf(sl[kk], sl[kk + PAGE / 2]);
+                    for (int kk = 0; kk < 21; ++kk)
+                        t1[kk] = fmax3(sl[3 * kk], sl[3 * kk + 1], sl[3 * kk + 2]);
+                    t1[21] = sl[63];
 #pragma unroll
-                for (int width = PAGE / 4; width >= 1; width /= 2)
-#pragma unroll
-                    for (int kk = 0; kk < width; ++kk) mt[kk] = fmaxf(mt[kk], mt[kk + width]);
+                    for (int kk = 0; kk < 7; ++kk)
+                        t2[kk] = fmax3(t1[3 * kk], t1[3 * kk + 1], t1[3 * kk + 2]);
+                    t2[7] = t1[21];
+                    mt[0] = fmax3(fmax3(t2[0], t2[1], t2[2]), fmax3(t2[3], t2[4], t2[5]),
+                                  fmaxf(t2[6], t2[7]));
+                }
                 const float m_page = mt[0] * scale_log2;
                 const bool raise = m_page > m_ref + kRescaleLog2 ||
                                    (m_ref == -INFINITY && m_page != -INFINITY);
@@ -499,12 +518,13 @@ attn_prefill_kernel(const __grid_constant__ CUtensorMap tmap_k,
                 if (raise) m_ref = m_page;
 #pragma unroll
                 for (int q4 = 0; q4 < 4; ++q4) l_run[q4] *= factor;
-                if (!wait(&p_empty[sb], par ^ 1u)) break;
-                tc_fence_after_sync();  // P V of page gi-2 read this P buffer: now rewritten
+                const int pb = int(gi % P_NPB);
+                if (!wait(&p_empty[pb], ((gi / P_NPB) & 1u) ^ 1u)) break;
+                tc_fence_after_sync();  // P V of page gi-4 read this P buffer: now rewritten
                 if (i > 0 && __any_sync(0xffffffffu, raise)) {
                     // this quarter's O rows *= factor once P V of page gi-1 has completed
                     const uint32_t gp = gi - 1u;
-                    if (!wait(&p_empty[gp & 1u], (gp >> 1) & 1u)) break;
+                    if (!wait(&p_empty[gp % P_NPB], (gp / P_NPB) & 1u)) break;
                     tc_fence_after_sync();
 #pragma unroll 1
                     for (int cc = 0; cc < D / 32; ++cc) {
@@ -539,7 +559,7 @@ attn_prefill_kernel(const __grid_constant__ CUtensorMap tmap_k,
                 // P into this quarter's lanes of the page's P buffer in tensor memory (the
                 // P V MMA reads it from there)
                 tmem_store_32x32b_x32_sync(
-                    tmem_base + lane_base + uint32_t(C::P_TCOL + sb * (PAGE / 2)), pk);
+                    tmem_base + lane_base + uint32_t(C::P_TCOL + pb * (PAGE / 2)), pk);
                 // V rows of this warp's 16 keys past the sequence end (or of an invalid
                 // page) are zeroed so unwritten cache slots cannot inject NaN/Inf via 0 * v
                 const int vend = valid ? L - page0 : 0;
@@ -552,11 +572,11 @@ attn_prefill_kernel(const __grid_constant__ CUtensorMap tmap_k,
                         *reinterpret_cast<uint4*>(vst + bx * C::BOX_BYTES + r0 * 128 + rem * 16) =
                             make_uint4(0, 0, 0, 0);
                     }
+                    fence_proxy_async_smem();  // the zeroed V rows, read by the MMA
                 }
-                fence_proxy_async_smem();  // the zeroed V rows, read by the MMA
                 tc_fence_before_sync();    // the P stores, before the arrival
                 __syncwarp();
-                if (lane == 0) mbar_arrive(&p_full[sb]);
+                if (lane == 0) mbar_arrive(&p_full[pb]);
             }
             if (!ok) break;
             g += uint32_t(npages);
