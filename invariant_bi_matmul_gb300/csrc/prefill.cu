@@ -53,7 +53,7 @@ constexpr int P_MAX_BATCH = BI_ATTN_MAX_BATCH;
 
 template <int D>
 struct PCfg {
-    static constexpr int NST = D == 64 ? 8 : 5;          // page stages in the ring
+    static constexpr int NST = D == 64 ? 8 : 4;          // page stages in the ring
     static constexpr int BOXES = D / 64;                 // 64-element (128 B) column boxes
     static constexpr int BOX_BYTES = PAGE * 128;         // one box of a page: 64 rows x 128 B
     static constexpr int PAGE_BYTES = BOXES * BOX_BYTES;
@@ -69,8 +69,12 @@ struct PCfg {
     static constexpr int XS_OFF = (BAR_OFF + NBARS * 8 + 8 + 15) / 16 * 16;
     static constexpr int XS_BYTES = 2 * P_ROWS * 8;       // per O buffer: (m, l) per row
     static constexpr int MISC_OFF = XS_OFF + XS_BYTES;
-    static constexpr size_t SMEM =
-        1024 + size_t(MISC_OFF) + size_t(NST + (P_MAX_BATCH + 1) + 3 * P_MAX_BATCH + 4) * 4;
+    static constexpr int MISC_BYTES = (NST + (P_MAX_BATCH + 1) + 3 * P_MAX_BATCH + 4) * 4;
+    // per epilogue warp: 32 O rows of 32 floats, staged for coalesced stores (rows padded
+    // to 144 bytes: conflict-free both ways)
+    static constexpr int EPI_STRIDE = 32 * 4 + 16;
+    static constexpr int EPI_OFF = (MISC_OFF + MISC_BYTES + 15) / 16 * 16;
+    static constexpr size_t SMEM = 1024 + size_t(EPI_OFF) + size_t(4 * 32 * EPI_STRIDE);
     static constexpr int S_COL = 0;                       // S buffers: columns [0,64), [64,128)
     static constexpr int O_COL = 2 * PAGE;                // O buffers (by item): D columns each
     // P buffers (by page): 128 rows x 64 keys of bf16, two keys per 32-bit column
@@ -418,6 +422,7 @@ attn_prefill_kernel(const __grid_constant__ CUtensorMap tmap_k,
         // with their (m, l) as the chunk partial of every row that reduces the chunk.
         const int e = warp & 3;
         const int r = 32 * e + lane;
+        uint8_t* epi_stage = smem + C::EPI_OFF + e * (32 * C::EPI_STRIDE);
         int item = 0;
         Cursor k = seek(w_begin);
         for (int w = w_begin; ok && w < w_end; ++w, advance(k), ++item) {
@@ -433,18 +438,31 @@ attn_prefill_kernel(const __grid_constant__ CUtensorMap tmap_k,
             const int64_t idx =
                 (int64_t(seq_t0[k.b] + j) * Hq + int64_t(k.h) * G + gg) * maxC + k.c;
             const uint32_t lane_base = uint32_t(32 * e) << 16;
+            // O rows 32 columns at a time, staged through shared memory so that each store
+            // instruction writes four rows' 128-byte segments instead of 32 scattered
+            // 16-byte pieces
+            const int rr = lane >> 3, part = lane & 7;  // reader: row within 4, 16-B piece
 #pragma unroll 1
             for (int cc = 0; cc < D / 32; ++cc) {
                 uint32_t v[32];
                 tmem_load_32x32b_x32_sync(
                     tmem_base + lane_base + uint32_t(C::O_COL + ob * D + cc * 32), v);
-                if (store) {
-                    float* dst = ws_o + idx * D + cc * 32;
 #pragma unroll
-                    for (int q4 = 0; q4 < 8; ++q4)
-                        *reinterpret_cast<uint4*>(dst + 4 * q4) =
-                            make_uint4(v[4 * q4], v[4 * q4 + 1], v[4 * q4 + 2], v[4 * q4 + 3]);
+                for (int q4 = 0; q4 < 8; ++q4)
+                    *reinterpret_cast<uint4*>(epi_stage + lane * C::EPI_STRIDE + q4 * 16) =
+                        make_uint4(v[4 * q4], v[4 * q4 + 1], v[4 * q4 + 2], v[4 * q4 + 3]);
+                __syncwarp();
+#pragma unroll
+                for (int q8 = 0; q8 < 8; ++q8) {
+                    const int row = 4 * q8 + rr;
+                    const bool st = __shfl_sync(0xffffffffu, store ? 1 : 0, row) != 0;
+                    const int64_t ridx = __shfl_sync(0xffffffffu, idx, row);
+                    if (st)
+                        *reinterpret_cast<uint4*>(ws_o + ridx * D + cc * 32 + part * 4) =
+                            *reinterpret_cast<const uint4*>(epi_stage + row * C::EPI_STRIDE +
+                                                           part * 16);
                 }
+                __syncwarp();
             }
             tc_fence_before_sync();
             __syncwarp();
