@@ -494,8 +494,9 @@ def kernel_table(dev, st=None):
     calls in one CUDA graph over rotating weight (or input) sets of 256 MB, more than twice
     the L2, so every call reads its operands from HBM; median of 7 replays.  With the
     step's buffers `st`: the step's verify call timed the same way (32 calls; its K/V,
-    268 MB, already exceed twice the L2), and the floor of any call timed with a pair of
-    CUDA events: an empty-sized kernel between two events, with the host ahead."""
+    268 MB, already exceed twice the L2), the same call with 1, 2 and 4 queries, and the
+    floor of any call timed with a pair of CUDA events: an empty-sized kernel between two
+    events, with the host ahead."""
     import torch
     import invariant_bi_matmul_gb300 as bi
     from invariant_bi_matmul_gb300 import inputs
@@ -549,6 +550,18 @@ def kernel_table(dev, st=None):
             by = step_bytes()["verify_block"]
             out["verify_block"] = {"us": round(t, 2), "GB/s": round(by / t / 1e3, 1),
                                    "frac_hbm": round(by / t / 1e3 / hbm, 4), "bound": "hbm"}
+            # the same cache and sequence with blocks of 1, 2 and 4 queries (the last
+            # tokens of the sequence), so the line covers decode and every verify width
+            for qn in (1, 2, 4):
+                cu = torch.tensor([0, qn], dtype=torch.int32, device=dev)
+                t = graph_time_us([lambda qn=qn, cu=cu: bi.verify_block(
+                    st.q[:qn], st.k_cache, st.v_cache, st.block_table, st.seq_lens, cu,
+                    max_q=qn, max_seq_len=LK, scale=st.scale, out=st.o[:qn],
+                    lse=st.lse[:qn], workspace=st.ws)], n=32)
+                by = LK * HKV * HEAD_DIM * 2 * 2 + qn * HQ * (HEAD_DIM * 2 * 2 + 4)
+                out[f"verify_q{qn}"] = {"us": round(t, 2), "GB/s": round(by / t / 1e3, 1),
+                                        "frac_hbm": round(by / t / 1e3 / hbm, 4),
+                                        "bound": "hbm"}
             tiny = torch.zeros(1, device=dev)
             ts = []
             for _ in range(21):
