@@ -139,7 +139,7 @@ attn_prefill_kernel(const __grid_constant__ CUtensorMap tmap_k,
     if (tid == 0) {
         for (int i = 0; i < NST; ++i) {
             mbar_init(&full[i], 1);
-            mbar_init(&empty[i], 1);   // released by the MMA warp's commit after P V
+            mbar_init(&empty[i], 1);   // released by the P V warp's commit after P V
         }
         for (int i = 0; i < P_NPB; ++i) {
             mbar_init(&p_full[i], P_NSM);
