@@ -97,6 +97,7 @@ attn_prefill_kernel(const __grid_constant__ CUtensorMap tmap_k,
     using C = PCfg<D>;
     constexpr int NST = C::NST;
     constexpr int chunk_pages = CHUNK / PAGE;
+    static_assert(chunk_pages <= 32, "an item's block-table entries are read one per lane");
     extern __shared__ uint8_t smem_raw[];
     uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) &
                                                ~uintptr_t(1023));
@@ -273,14 +274,18 @@ attn_prefill_kernel(const __grid_constant__ CUtensorMap tmap_k,
         uint32_t g = 0;
         Cursor k = seek(w_begin);
         for (int w = w_begin; ok && w < w_end; ++w, advance(k)) {
-            const int npages = item_pages(k);
+            const int npages = item_pages(k);  // <= chunk_pages = 8
+            // the item's block-table entries, one per lane, read before the first wait for
+            // a free stage: no dependent global load between a stage freeing and its copy
+            const int pidx_l = k.c * chunk_pages + lane;
+            const int phys_l = (lane < npages && pidx_l < max_pages)
+                                   ? block_table[int64_t(k.b) * max_pages + pidx_l]
+                                   : -1;
             for (int i = 0; i < npages; ++i, ++g) {
                 const int s = int(g % NST);
                 if (!wait(&empty[s], ((g / NST) & 1u) ^ 1u)) break;
+                const int phys = __shfl_sync(0xffffffffu, phys_l, i);
                 if (elect_one()) {
-                    const int pidx = k.c * chunk_pages + i;
-                    const int phys =
-                        pidx < max_pages ? block_table[int64_t(k.b) * max_pages + pidx] : -1;
                     const bool valid = phys >= 0 && phys < num_pages;
                     stage_valid[s] = valid ? 1 : 0;
                     if (valid) {
