@@ -491,6 +491,14 @@ attn_prefill_kernel(const __grid_constant__ CUtensorMap tmap_k,
             const int j = k.qt * TQ + r / G;
             const int pos = j < qb ? L - qb + j : -1;
             const int ob = item & 1;
+            // whether each page of the item is in the cache, from the block table (the
+            // producer's test on the same entries), one page per lane: the softmax needs
+            // no stage's landing for it, only for the pages whose V rows it zeroes
+            const int pidx_l = k.c * chunk_pages + lane;
+            const int phys_l = (lane < npages && pidx_l < max_pages)
+                                   ? block_table[int64_t(k.b) * max_pages + pidx_l]
+                                   : -1;
+            const bool valid_l = phys_l >= 0 && phys_l < num_pages;
             float m_ref = -INFINITY;
             float l_run[4] = {0.f, 0.f, 0.f, 0.f};  // running sums of the four 16-key slices
             for (int i = 0; i < npages && ok; ++i) {
@@ -506,8 +514,7 @@ attn_prefill_kernel(const __grid_constant__ CUtensorMap tmap_k,
                 tc_fence_before_sync();
                 __syncwarp();
                 if (lane == 0) mbar_arrive(&s_empty[sb]);
-                if (!wait(&full[s], (gi / NST) & 1u)) break;
-                const bool valid = stage_valid[s] != 0;
+                const bool valid = __shfl_sync(0xffffffffu, valid_l ? 1 : 0, i) != 0;
                 float sl[PAGE];
                 if (__all_sync(0xffffffffu, valid && page0 + PAGE - 1 <= pos)) {
                     // every key of the page is visible to every row of the warp
@@ -587,6 +594,8 @@ attn_prefill_kernel(const __grid_constant__ CUtensorMap tmap_k,
                 // page) are zeroed so unwritten cache slots cannot inject NaN/Inf via 0 * v
                 const int vend = valid ? L - page0 : 0;
                 if (vend < (sw + 1) * 16) {
+                    // after the stage's copies have landed (an invalid page's stage had none)
+                    if (!wait(&full[s], (gi / NST) & 1u)) break;
                     const int r0 = max(vend, sw * 16);
                     uint8_t* vst = sStage + s * C::STAGE_BYTES + C::PAGE_BYTES;
                     const int n16 = ((sw + 1) * 16 - r0) * 8;  // 16-byte pieces per box
