@@ -69,7 +69,7 @@ struct PCfg {
     static constexpr int XS_OFF = (BAR_OFF + NBARS * 8 + 8 + 15) / 16 * 16;
     static constexpr int XS_BYTES = 2 * P_ROWS * 8;       // per O buffer: (m, l) per row
     static constexpr int MISC_OFF = XS_OFF + XS_BYTES;
-    static constexpr int MISC_BYTES = (NST + (P_MAX_BATCH + 1) + 3 * P_MAX_BATCH + 4) * 4;
+    static constexpr int MISC_BYTES = ((P_MAX_BATCH + 1) + 3 * P_MAX_BATCH + 4) * 4;
     // per epilogue warp: 32 O rows of 32 floats, staged for coalesced stores (rows padded
     // to 144 bytes: conflict-free both ways)
     static constexpr int EPI_STRIDE = 32 * 4 + 16;
@@ -119,8 +119,7 @@ attn_prefill_kernel(const __grid_constant__ CUtensorMap tmap_k,
     static_assert(C::XS_OFF >= C::BAR_OFF + (2 * NST + 4 + 2 * P_NPB + 4 + 2 + 4) * 8 + 8,
                   "barriers overlap xs");
     float2* xs = reinterpret_cast<float2*>(smem + C::XS_OFF);  // [2][P_ROWS]
-    int* stage_valid = reinterpret_cast<int*>(smem + C::MISC_OFF);
-    int* prefix = stage_valid + NST;            // [B+1] items before sequence b
+    int* prefix = reinterpret_cast<int*>(smem + C::MISC_OFF);  // [B+1] items before sequence b
     int* seq_len = prefix + P_MAX_BATCH + 1;    // per sequence: length, first token, width
     int* seq_t0 = seq_len + P_MAX_BATCH;
     int* seq_qb = seq_t0 + P_MAX_BATCH;
@@ -287,7 +286,6 @@ attn_prefill_kernel(const __grid_constant__ CUtensorMap tmap_k,
                 const int phys = __shfl_sync(0xffffffffu, phys_l, i);
                 if (elect_one()) {
                     const bool valid = phys >= 0 && phys < num_pages;
-                    stage_valid[s] = valid ? 1 : 0;
                     if (valid) {
                         uint8_t* st = sStage + s * C::STAGE_BYTES;
                         mbar_arrive_expect_tx(&full[s], C::STAGE_BYTES);
